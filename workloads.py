@@ -1,0 +1,184 @@
+"""Seeded synthetic inputs for the dg GEMM workloads.
+
+This module only draws random numbers (a CPU torch.Generator, seed 0 by
+default) and lays them out in the operand conventions of the library:
+  A  M x K row-major (fp16 or int8),
+  B  N rows of K (fp16 or int8), or N rows of K/2 bytes of packed 4-bit codes,
+  C  M x N row-major (fp16),  bias  [N] (fp16).
+It holds none of the GEMM arithmetic: the oracle and the CUDA path both take
+their inputs from here and from nowhere else.
+
+Random bytes are drawn uniformly over 0..255 for packed 4-bit weights, which
+makes each of the two codes in a byte uniform over the 16 codes and
+independent of the other, so no packing step is needed.
+"""
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+import torch
+
+
+@dataclass
+class Case:
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype_a: str            # "f16" | "i8"
+    dtype_b: str            # "f16" | "i8" | "e2m1"
+    A: np.ndarray           # [M, lda]   (logical columns 0..K-1)
+    B: np.ndarray           # [N, ldb] elements, or [N, ldb/2] bytes for e2m1
+    C: Optional[np.ndarray] = None
+    bias: Optional[np.ndarray] = None
+    alpha: float = 1.0
+    beta: float = 0.0
+    epilogue: str = "none"
+    lda: int = 0
+    ldb: int = 0
+    meta: dict = field(default_factory=dict)
+
+    def flops(self):
+        return 2.0 * self.M * self.N * self.K
+
+
+def _gen(seed):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def _normal(g, shape, std):
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(torch.float16).numpy()
+
+
+def _uniform_pm1(g, shape):
+    x = torch.rand(*shape, generator=g, dtype=torch.float32)
+    x.mul_(2.0).sub_(1.0)
+    return x.to(torch.float16).numpy()
+
+
+def _int8(g, shape):
+    return torch.randint(-128, 128, shape, generator=g, dtype=torch.int16).to(torch.int8).numpy()
+
+
+def _bytes(g, shape):
+    return torch.randint(0, 256, shape, generator=g, dtype=torch.int16).to(torch.uint8).numpy()
+
+
+def _pad_cols(x, ld):
+    """Place x [rows, cols] in a zero-initialised [rows, ld] buffer."""
+    if ld == x.shape[1]:
+        return np.ascontiguousarray(x)
+    out = np.zeros((x.shape[0], ld), dtype=x.dtype)
+    out[:, : x.shape[1]] = x
+    return out
+
+
+def random_case(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", alpha=1.0,
+                beta=0.0, seed=0, dist="normal", lda=None, ldb=None, name=None):
+    """A general random case for parity tests.
+
+    dist: "normal" -> N(0,1)/sqrt(K) operands (the square-GEMM recipe),
+          "uniform" -> U[-1,1) operands.
+    C ~ N(0,1) fp16 whenever beta != 0; bias ~ N(0, 0.1) fp16 when the
+    epilogue has a bias.  lda/ldb default to the smallest legal padded
+    leading dimension (K rounded up to 8 fp16 / 16 int8 elements, 32 codes
+    for packed 4-bit), so every leading dimension is a 16-byte multiple.
+    """
+    g = _gen(seed)
+    if dtype_a == "f16":
+        lda = lda or _round_up(K, 8)
+        if dist == "normal":
+            A = _normal(g, (M, K), 1.0 / math.sqrt(K)) if dtype_b == "f16" else _normal(g, (M, K), 1.0)
+        else:
+            A = _uniform_pm1(g, (M, K))
+    elif dtype_a == "i8":
+        lda = lda or _round_up(K, 16)
+        A = _int8(g, (M, K))
+    else:
+        raise ValueError(dtype_a)
+    if dtype_b == "f16":
+        ldb = ldb or _round_up(K, 8)
+        B = _normal(g, (N, K), 1.0 / math.sqrt(K)) if dist == "normal" else _uniform_pm1(g, (N, K))
+        B = _pad_cols(B, ldb)
+    elif dtype_b == "i8":
+        ldb = ldb or _round_up(K, 16)
+        B = _pad_cols(_int8(g, (N, K)), ldb)
+    elif dtype_b == "e2m1":
+        ldb = ldb or _round_up(K, 32)
+        nbytes = (K + 1) // 2
+        Bp = _bytes(g, (N, nbytes))
+        if K % 2:
+            Bp[:, -1] &= 0x0F  # the unused high nibble of an odd row is left zero
+        B = _pad_cols(Bp, ldb // 2)
+    else:
+        raise ValueError(dtype_b)
+    A = _pad_cols(A, lda)
+    C = None
+    if beta != 0.0:
+        C = _int32(g, (M, N)) if dtype_a == "i8" else _normal(g, (M, N), 1.0)
+    bias = None
+    if epilogue in ("bias", "bias_gelu"):
+        bias = _normal(g, (N,), 0.1)
+    return Case(name or "random_%s_%s_%dx%dx%d" % (dtype_a, dtype_b, M, N, K), M, N, K,
+                dtype_a, dtype_b, A, B, C, bias, float(alpha), float(beta), epilogue, lda, ldb)
+
+
+def _int32(g, shape):
+    return torch.randint(-(1 << 20), 1 << 20, shape, generator=g, dtype=torch.int32).numpy()
+
+
+def _round_up(x, m):
+    return (x + m - 1) // m * m
+
+
+# ---------------------------------------------------------------------------
+# The named workloads.  Each recipe states its sizes and distributions.
+# ---------------------------------------------------------------------------
+
+def f16_256(seed=0):
+    """FP16 256^3, A and B ~ U[-1,1), alpha=1, beta=0, no epilogue."""
+    c = random_case(256, 256, 256, "f16", "f16", dist="uniform", seed=seed, name="f16_256")
+    return c
+
+
+def f16_square(n, seed=0):
+    """FP16 n^3, A,B ~ N(0,1)/sqrt(K), C ~ N(0,1), D = 1.0*A.B + 0.5*C."""
+    return random_case(n, n, n, "f16", "f16", alpha=1.0, beta=0.5, seed=seed,
+                       name="f16_%d" % n)
+
+
+def i8_square(n=4096, seed=0):
+    """INT8 n^3, A,B uniform integers in [-128, 127], alpha=1, beta=0, int32 out."""
+    return random_case(n, n, n, "i8", "i8", seed=seed, name="i8_%d" % n)
+
+
+def thin(N, K, seed=0):
+    """M=1 FP16 GEMV-shaped GEMM, a and B ~ N(0,1)/sqrt(K), alpha=1, beta=0."""
+    return random_case(1, N, K, "f16", "f16", seed=seed, name="thin_1x%dx%d" % (N, K))
+
+
+def w4a16(M, N=8960, K=1536, seed=0):
+    """W4A16: packed E2M1 weights (uniform codes), A ~ N(0,1) fp16,
+    bias ~ N(0, 0.1) fp16 (0.1 read as the standard deviation), bias + erf-GELU."""
+    return random_case(M, N, K, "f16", "e2m1", epilogue="bias_gelu", seed=seed,
+                       name="w4a16_m%d" % M)
+
+
+WORKLOADS = {
+    "f16_256": lambda: f16_256(),
+    "f16_2048": lambda: f16_square(2048),
+    "f16_4096": lambda: f16_square(4096),
+    "f16_8192": lambda: f16_square(8192),
+    "i8_4096": lambda: i8_square(4096),
+    "thin_1x4096x131072": lambda: thin(4096, 131072),
+    "thin_1x256x12800": lambda: thin(256, 12800),
+    "w4a16_m16": lambda: w4a16(16),
+    "w4a16_m2048": lambda: w4a16(2048),
+}
