@@ -1,0 +1,459 @@
+"""Throughput of the dg GEMM path on GB300 (one JSON line on rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dg|reference]
+                  [--workload NAME] [--all]
+
+A step is one dg_gemm call: planning (cached), the tcgen05 main loop and the
+fused alpha/beta/bias/GELU epilogue over one batch of synthetic inputs.  The
+default workload is the FP16 GEMM M = N = K = 4096 with D = 1.0*A.B + 0.5*C,
+A, B ~ N(0,1)/sqrt(K), C ~ N(0,1) (seed 0).  Steps rotate over several input
+sets whose total size is several times the 129 MB L2, so no step reads
+operands another step left in L2.
+
+--impl reference times the CPU oracle (fp64 definition of the same GEMM) on
+the host cores, one bounded row sample of the same workload per step.
+
+Multi-GPU (torchrun, one process per GPU): the GEMM does not shard, so each
+rank runs an independent replica (weak scaling); value = all ranks' FLOPs /
+the slowest rank's time.
+"""
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+L2_BYTES = 129 * 1000 * 1000
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons of one GPU through NVML
+    (read-only queries) in a background thread."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, index, period_s=0.005):
+        self.index, self.period = index, period_s
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))  # 1 = SM
+            self.max_mhz = int(mx.value)
+            self.ok = True
+        except OSError:
+            pass
+
+    def _read(self):
+        mhz, reasons = ctypes.c_uint(), ctypes.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz))
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(self.handle, ctypes.byref(reasons))
+        return int(mhz.value), int(reasons.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.samples.append(self._read())
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "unavailable"}
+        busy = [m for m, r in self.samples if not (r & 0x1)] or [m for m, _ in self.samples]
+        seen = 0
+        for _, r in self.samples:
+            seen |= r
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if seen & b and b != 0x1],
+                "samples": len(self.samples), "source": "nvml"}
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "ptx.cuh", "epilogue.cuh", "gemv.cu"):
+        p = os.path.join(ROOT, "precision_matmul_dg_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def workload_info(name):
+    info = {
+        "f16_4096": ("FP16 GEMM M=N=K=4096, D=1.0*A.B+0.5*C, A,B~N(0,1)/sqrt(K), C~N(0,1)",
+                     "tensor"),
+        "f16_2048": ("FP16 GEMM M=N=K=2048, D=1.0*A.B+0.5*C", "tensor"),
+        "f16_8192": ("FP16 GEMM M=N=K=8192, D=1.0*A.B+0.5*C", "tensor"),
+        "f16_256": ("FP16 GEMM M=N=K=256, A,B~U[-1,1)", "tensor"),
+        "thin_1x4096x131072": ("FP16 GEMV M=1,N=4096,K=131072 split-K", "hbm"),
+        "thin_1x256x12800": ("FP16 GEMV M=1,N=256,K=12800 split-K", "hbm"),
+    }
+    return info[name]
+
+
+def algorithmic_bytes(case):
+    eb = 2
+    b = case.M * case.K * eb + case.N * case.K * eb + case.M * case.N * 2
+    if case.beta != 0:
+        b += case.M * case.N * 2
+    if case.bias is not None:
+        b += case.N * 2
+    return b
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_dg(args, world, rank, local):
+    import precision_matmul_dg_gb300 as dg
+    from precision_matmul_dg_gb300 import build as dg_build
+    if rank == 0 or world > 1:
+        dg_build.build()
+    dev = torch.device("cuda", local)
+    name = args.workload
+    desc, bound = workload_info(name)
+    base = workloads.WORKLOADS[name]()
+    set_bytes = base.A.nbytes + base.B.nbytes + base.M * base.N * 2
+    nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes)) if set_bytes < 3 * L2_BYTES else 1
+    nsets = min(nsets, 16)
+    sets = []
+    g = torch.Generator(device=dev)
+    for s in range(nsets):
+        A = torch.from_numpy(base.A).to(dev)
+        B = torch.from_numpy(base.B).to(dev)
+        C = (torch.from_numpy(base.C).to(dev) if base.C is not None else
+             torch.zeros(base.M, base.N, dtype=torch.float16, device=dev))
+        if s > 0:  # further sets: same recipe, seeded on the device
+            g.manual_seed(1000 + s)
+            A.normal_(0, 1.0 / math.sqrt(base.K), generator=g)
+            B.normal_(0, 1.0 / math.sqrt(base.K), generator=g)
+            if base.C is not None:
+                C.normal_(0, 1.0, generator=g)
+        bias = torch.from_numpy(base.bias).to(dev) if base.bias is not None else None
+        sets.append((A, B, C, bias))
+    stream = torch.cuda.current_stream(dev)
+    plan = dg.plan_tiles(base.M, base.N, base.K, base.dtype_a, base.dtype_b, base.epilogue)[0]
+
+    def step(i, ev=None):
+        A, B, C, bias = sets[i % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        dg.gemm(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
+                epilogue=base.epilogue, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    dg.check_status(stream)
+    torch.cuda.synchronize(dev)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    launches0 = dg.launch_count()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with sampler:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    launches = dg.launch_count() - launches0
+    dg.check_status(stream)
+    total_ms = t0.elapsed_time(t1)
+    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+
+    total_ms_max = max_over_ranks(total_ms, world)
+    flops = base.flops()
+    total_flops = sum_over_ranks(flops * args.steps, world)
+    value = total_flops / (total_ms_max * 1e-3) / 1e12
+
+    # e2e: the same GEMM through the public API with pinned host buffers,
+    # host->device copies of A, B, C and the device->host read of D timed.
+    hA = torch.from_numpy(base.A).pin_memory()
+    hB = torch.from_numpy(base.B).pin_memory()
+    hC = (torch.from_numpy(base.C) if base.C is not None else
+          torch.zeros(base.M, base.N, dtype=torch.float16)).pin_memory()
+    hD = torch.empty(base.M, base.N, dtype=torch.float16).pin_memory()
+    dA, dB, dC, dbias = sets[0]
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        dC.copy_(hC, non_blocking=True)
+        dg.gemm(dA, dB, dC, K=base.K, bias=dbias, alpha=base.alpha, beta=base.beta,
+                epilogue=base.epilogue, stream=stream)
+        hD.copy_(dC, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = sum_over_ranks(flops * e2e_steps, world) / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    achieved = flops / (kern_avg_ms * 1e-3) / 1e12
+    if bound == "tensor":
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": "%s bf16 dense burst (fp16 runs at the bf16 rate)" % peak_src}
+    else:
+        gbs = algorithmic_bytes(base) / (kern_avg_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(gbs / peak, 4), "peak_source": "%s copy bandwidth" % peak_src}
+    kname = "gemm_f16_tc_kernel" if plan["kernel_name"] == "tc" else "gemv_splitk_kernel"
+    roof["kernel"] = kname
+    roof["kernel_avg_us"] = round(kern_avg_ms * 1e3, 2)
+    roof["traffic"] = recorded_traffic(kname)
+
+    line = {
+        "metric": "GEMM TFLOP/s (INT8 TOPS) and % of GB300 dense peak; GB/s vs HBM for M=1",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms_max / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded, recipe in workloads.py)",
+        "config": {"workload": desc, "name": name, "M": base.M, "N": base.N, "K": base.K,
+                   "alpha": base.alpha, "beta": base.beta, "epilogue": base.epilogue,
+                   "l2": "%d rotating input sets, %.0f MB > L2" % (nsets, nsets * set_bytes / 1e6)
+                   if nsets > 1 else "inputs larger than L2",
+                   "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "plan": {k: plan[k] for k in ("kernel_name", "m_tile", "n_tile", "k_tile",
+                                                 "split_k", "stages", "grid")}},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(hA.nbytes + hB.nbytes + hC.nbytes),
+                "d2h_bytes_per_step": int(hD.nbytes)},
+        "gpu_launches": int(launches),
+        "clocks": sampler.summary(),
+    }
+    return line
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_sample_rate(case, budget_s, rows_per_call):
+    """Times the oracle (fp64 definition) on row samples of `case` for about
+    budget_s seconds; returns (TFLOP/s, seconds, rows done)."""
+    import oracle
+    rng = np.random.default_rng(0)
+    done_rows, t_total = 0, 0.0
+    while t_total < budget_s and done_rows < 64 * case.M:
+        rows = rng.choice(case.M, size=min(rows_per_call, case.M), replace=False)
+        t = time.perf_counter()
+        oracle.gemm_reference(case.A, case.B, case.K, case.dtype_a, case.dtype_b, C=case.C,
+                              bias=case.bias, alpha=case.alpha, beta=case.beta,
+                              epilogue=case.epilogue, rows=rows)
+        t_total += time.perf_counter() - t
+        done_rows += len(rows)
+    flops = 2.0 * done_rows * case.N * case.K
+    return flops / t_total / 1e12, t_total, done_rows
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    name = args.workload
+    desc, _ = workload_info(name)
+    case = workloads.WORKLOADS[name]()
+    rows = max(1, min(case.M, 64))
+    import oracle
+    rng = np.random.default_rng(1)
+
+    def step():
+        r = rng.choice(case.M, size=rows, replace=False)
+        oracle.gemm_reference(case.A, case.B, case.K, case.dtype_a, case.dtype_b, C=case.C,
+                              bias=case.bias, alpha=case.alpha, beta=case.beta,
+                              epilogue=case.epilogue, rows=r)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    flops = 2.0 * rows * case.N * case.K * args.steps
+    value = flops / dt / 1e12
+    sample = "%d random rows of the %dx%dx%d product per step (%s)" % (rows, case.M, case.N,
+                                                                      case.K, name)
+    return {
+        "impl": "reference",
+        "metric": "GEMM TFLOP/s (INT8 TOPS) and % of GB300 dense peak; GB/s vs HBM for M=1",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, recipe in workloads.py)",
+        "config": {"workload": desc, "name": name, "M": case.M, "N": case.N, "K": case.K},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
+    ap.add_argument("--workload", default="f16_4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        import subprocess
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               "--nproc-per-node", str(args.gpus), "--master-addr", "127.0.0.1",
+               "--master-port", "29511", os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    line = run_dg(args, world, rank, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            case = workloads.WORKLOADS[args.workload]()
+            v, secs, rows = oracle_sample_rate(case, budget_s=10.0, rows_per_call=256)
+            line["cpu_baseline"] = {
+                "value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                "sample": "%d rows of the %dx%dx%d product in %.1f s (fp64 numpy BLAS, "
+                          "default threads)" % (rows, case.M, case.N, case.K, secs)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * dg.h -- C ABI of libdg, a GEMM library for one NVIDIA GB300 GPU (sm_103a).
+ *
+ *   D = epilogue(alpha * A.B + beta * C)
+ *
+ * The operation is the one stated in the "DeepGEMM" articles this library
+ * follows (kwkr.cn/news/562171, section 3.2 step 3: the fused epilogue
+ * "alpha * C + beta * D" and the launch argument order A, B, C, alpha, beta,
+ * m, n, k; section 2.2 third layer: bias and GELU fused into the GEMM;
+ * discosf.com/news/5532976, section 2.2 layer 2: the precision triple
+ * {weight, activation, output}, e.g. int4_e2m1 x fp16 -> fp16; section 3.5:
+ * FP32 accumulation with an FP16 output cast).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All sizes are element counts of type int64_t.
+ *  - A is M x K, row-major, leading dimension lda (elements, lda >= K).
+ *  - B is K x N stored "column-major": N rows of K contiguous elements,
+ *    leading dimension ldb (elements, ldb >= K).  For DG_E2M1, B holds two
+ *    4-bit codes per byte: byte p of a row carries k = 2p in its low nibble
+ *    and k = 2p+1 in its high nibble; ldb counts codes, is even, and a row is
+ *    ldb/2 bytes long.
+ *  - C (input, read only when beta != 0) and D (output) share one buffer,
+ *    row-major M x N with leading dimension N (BLAS in/out convention).  Its
+ *    type is FP16 for the floating-point pairs and INT32 for INT8 x INT8.
+ *  - bias is FP16 [N], read only by the bias epilogues.
+ *  - Every pointer is caller-owned device memory; libdg never frees it.
+ *  - A and B must be 16-byte aligned and lda/ldb must span a multiple of 16
+ *    bytes (the tensor-memory-access engine reads them in tiles); C must be
+ *    16-byte aligned; bias 2-byte aligned.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *    Invalid arguments are rejected synchronously, before any launch, with a
+ *    status and a message in dg_last_error().  Faults in a launched kernel
+ *    surface at the caller's next synchronisation (CUDA semantics); a kernel
+ *    whose internal pipeline wait runs past its time limit records
+ *    DG_ERR_TIMEOUT in a per-device status word that dg_check_status() reads.
+ */
+#ifndef DG_H_
+#define DG_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime type is a pointer to this opaque struct). */
+typedef struct CUstream_st *dg_stream_t;
+
+typedef enum {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, bad size or leading dimension */
+  DG_ERR_UNSUPPORTED = 2,        /* dtype pair, epilogue or scalar this path does not take */
+  DG_ERR_NO_VALID_CANDIDATE = 3, /* the planner found no tile that meets every constraint */
+  DG_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
+  DG_ERR_TIMEOUT = 5,            /* a device-side pipeline wait ran past its limit */
+  DG_ERR_INVALID_STATE = 6       /* no usable device, or a plan that does not fit the call */
+} dg_status;
+
+/* Input element types (the output type follows from the pair). */
+typedef enum {
+  DG_F16 = 0,   /* IEEE binary16 */
+  DG_I8 = 1,    /* two's-complement int8 */
+  DG_E2M1 = 2   /* 4-bit float: sign | 2-bit exponent (bias 1) | 1-bit mantissa */
+} dg_dtype;
+
+/* Fused epilogue applied to t = alpha*acc + beta*C:  bias adds bias[j] to t,
+ * GELU takes 0.5*t*(1 + erf(t/sqrt(2))) (after the bias when both are set). */
+typedef enum {
+  DG_EPI_NONE = 0,
+  DG_EPI_BIAS = 1,
+  DG_EPI_GELU = 2,
+  DG_EPI_BIAS_GELU = 3
+} dg_epilogue;
+
+/* Kernel families a plan can select. */
+typedef enum {
+  DG_KERNEL_TC = 0,    /* tensor-core pipeline: TMA -> SMEM ring -> tcgen05.mma -> TMEM -> fused epilogue */
+  DG_KERNEL_GEMV = 1   /* thin-M split-K streaming kernel on the CUDA cores */
+} dg_kernel;
+
+/* Hardware description the planner solves against
+ * (kwkr.cn/news/562171, section 3.2 step 1: compute capability, shared memory
+ * per SM, L2 size, threads per SM, tensor-core types; extended here with the
+ * resources a Blackwell SM exposes). */
+typedef struct {
+  int sm_count;
+  int cc_major, cc_minor;
+  int smem_per_block_optin;   /* bytes one CTA may use */
+  int smem_per_sm;            /* bytes per SM */
+  int regs_per_sm;            /* 32-bit registers per SM */
+  int regs_per_thread_max;
+  int max_threads_per_sm;
+  int tmem_cols;              /* tensor-memory columns per SM (128 lanes x 32 bit each); 0 = none */
+  int64_t l2_bytes;
+  double hbm_gbps;            /* bytes/ns; 0 = unknown */
+  double tc_f16_tflops;       /* dense FP16 tensor rate; 0 = unknown */
+  double clock_ghz;
+} dg_hw_desc;
+
+/* One tile plan (kwkr.cn/news/562171, section 2.2 first layer: a solution
+ * (M_tile, N_tile, K_tile) of the shared-memory / register / occupancy
+ * constraint system; here with split-K, pipeline depth and CTA pairing). */
+typedef struct {
+  int kernel;       /* dg_kernel */
+  int m_tile;       /* rows of D per CTA (or per CTA pair when cta_group == 2) */
+  int n_tile;       /* columns of D per CTA */
+  int k_tile;       /* K elements per pipeline stage */
+  int split_k;      /* number of K slices reduced deterministically (1 = none) */
+  int stages;       /* shared-memory ring depth */
+  int cta_group;    /* 1, or 2 for a tcgen05 CTA pair */
+  int swap_ab;      /* 1: the kernel computes D^T = B^T.A^T (thin-M tensor path) */
+  int smem_bytes;   /* dynamic shared memory of the launch */
+  int threads;      /* threads per CTA */
+  int grid;         /* CTAs launched */
+  double occupancy; /* wave efficiency: work units / (waves * SMs) */
+  double est_us;    /* cost-model time */
+  double est_tflops;
+} dg_tile_plan;
+
+/* Fill *out for CUDA device `device` from cudaDeviceGetAttribute.
+ * Returns DG_ERR_INVALID_STATE when no such device exists. */
+dg_status dg_query_hw(int device, dg_hw_desc *out);
+
+/* The tile planner (kwkr.cn/news/562171, section 2.2 first layer and
+ * section 3.2 step 2; discosf.com/news/5532976, section 4.1 stage 2).
+ * Enumerates the tile space of the kernels this library ships, keeps the
+ * candidates whose shared memory, tensor memory, registers and threads fit
+ * `hw` and whose wave efficiency is at least target_occupancy, and writes up
+ * to max_out of them to out[], best estimated time first.  *n_out receives
+ * the number written.  hw == NULL means the current device.  Host only: no
+ * GPU work.  DG_ERR_NO_VALID_CANDIDATE when nothing survives the pruning. */
+dg_status dg_plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                        dg_epilogue epilogue, const dg_hw_desc *hw, double target_occupancy,
+                        dg_tile_plan *out, int max_out, int *n_out);
+
+/* D = epilogue(alpha * A.B + beta * C) with the planner's best plan.
+ * Supported pairs: F16 x F16 and F16 x E2M1 (FP32 accumulation, FP16 out,
+ * any epilogue) and I8 x I8 (exact INT32 accumulation, INT32 out, no
+ * epilogue, integral alpha and beta, wrap-around modulo 2^32).
+ * M == 0 or N == 0 is a no-op; K == 0 gives epilogue(beta * C).
+ * May grow a per-(device, stream) split-K workspace the first time a shape
+ * needs it (cudaMalloc; libdg owns it until dg_shutdown). */
+dg_status dg_gemm(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                  const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                  const void *bias, float alpha, float beta, dg_epilogue epilogue,
+                  dg_stream_t stream);
+
+/* As dg_gemm, but runs `plan` (one returned by dg_plan_tiles for the same
+ * M, N, K and dtypes).  DG_ERR_INVALID_STATE when the plan does not fit. */
+dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                          const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
+                          const void *bias, float alpha, float beta, dg_epilogue epilogue,
+                          const dg_tile_plan *plan, dg_stream_t stream);
+
+/* Message for the last failing call on this thread ("" if none).  Valid
+ * until the next libdg call on the same thread. */
+const char *dg_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: DG_ERR_TIMEOUT if a kernel gave up on a pipeline wait since the last
+ * check, DG_ERR_CUDA if the stream reports an error, else DG_OK. */
+dg_status dg_check_status(dg_stream_t stream);
+
+/* Time limit of every device-side pipeline wait, in nanoseconds
+ * (default 1e9).  0 restores the default.  Applies to later launches. */
+dg_status dg_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook: one CTA waits on a barrier that nothing completes, with the
+ * current time limit, then records DG_ERR_TIMEOUT in the status word and
+ * returns.  Lets a test exercise the timeout path without a fault. */
+dg_status dg_selftest_wait_timeout(dg_stream_t stream);
+
+/* Kernels launched by this process through libdg so far. */
+uint64_t dg_launch_count(void);
+
+/* Frees the split-K workspaces and cached state of every device. */
+dg_status dg_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H_ */

@@ -1,0 +1,246 @@
+"""Python binding of libdg (ctypes): argument marshalling only.
+
+Every step of the GEMM runs in libdg's CUDA kernels.  This module loads the
+in-tree ``libdg.so`` (built by ``precision_matmul_dg_gb300.build``), declares
+the C signatures of ``include/dg.h`` and turns tensors into pointers and
+leading dimensions.  PyTorch is used for device memory and streams only.
+There is no fallback: if the library is missing, every call raises.
+"""
+
+import ctypes
+import os
+
+__all__ = [
+    "DgError", "F16", "I8", "E2M1", "EPILOGUES", "lib", "lib_path", "gemm", "gemm_raw",
+    "plan_tiles", "query_hw", "last_error", "check_status", "set_wait_timeout_ns",
+    "selftest_wait_timeout", "launch_count", "shutdown", "HwDesc", "TilePlan", "EXPORTS",
+]
+
+F16, I8, E2M1 = 0, 1, 2
+DTYPES = {"f16": F16, "i8": I8, "e2m1": E2M1}
+EPILOGUES = {"none": 0, "bias": 1, "gelu": 2, "bias_gelu": 3}
+STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
+          3: "DG_ERR_NO_VALID_CANDIDATE", 4: "DG_ERR_CUDA", 5: "DG_ERR_TIMEOUT",
+          6: "DG_ERR_INVALID_STATE"}
+KERNELS = {0: "tc", 1: "gemv", -1: "none"}
+
+# Every symbol include/dg.h declares.
+EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_last_error",
+           "dg_check_status", "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout",
+           "dg_launch_count", "dg_shutdown"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def lib_path():
+    return os.path.join(_HERE, "libdg.so")
+
+
+class DgError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__("%s: %s" % (self.name, message))
+
+
+class HwDesc(ctypes.Structure):
+    _fields_ = [("sm_count", ctypes.c_int), ("cc_major", ctypes.c_int), ("cc_minor", ctypes.c_int),
+                ("smem_per_block_optin", ctypes.c_int), ("smem_per_sm", ctypes.c_int),
+                ("regs_per_sm", ctypes.c_int), ("regs_per_thread_max", ctypes.c_int),
+                ("max_threads_per_sm", ctypes.c_int), ("tmem_cols", ctypes.c_int),
+                ("l2_bytes", ctypes.c_int64), ("hbm_gbps", ctypes.c_double),
+                ("tc_f16_tflops", ctypes.c_double), ("clock_ghz", ctypes.c_double)]
+
+    def as_dict(self):
+        return {f[0]: getattr(self, f[0]) for f in self._fields_}
+
+
+class TilePlan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("m_tile", ctypes.c_int), ("n_tile", ctypes.c_int),
+                ("k_tile", ctypes.c_int), ("split_k", ctypes.c_int), ("stages", ctypes.c_int),
+                ("cta_group", ctypes.c_int), ("swap_ab", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int), ("grid", ctypes.c_int),
+                ("occupancy", ctypes.c_double), ("est_us", ctypes.c_double),
+                ("est_tflops", ctypes.c_double)]
+
+    def as_dict(self):
+        d = {f[0]: getattr(self, f[0]) for f in self._fields_}
+        d["kernel_name"] = KERNELS.get(self.kernel, str(self.kernel))
+        return d
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libdg.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError("libdg.so is not built (%s); run __graft_entry__.build()" % path)
+    L = ctypes.CDLL(path)
+    i64, vp, i32, f32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.dg_query_hw.argtypes = [i32, ctypes.POINTER(HwDesc)]
+    L.dg_plan_tiles.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(HwDesc),
+                                ctypes.c_double, ctypes.POINTER(TilePlan), i32,
+                                ctypes.POINTER(ctypes.c_int)]
+    gemm_args = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, vp, f32, f32, i32]
+    L.dg_gemm.argtypes = gemm_args + [vp]
+    L.dg_gemm_planned.argtypes = gemm_args + [ctypes.POINTER(TilePlan), vp]
+    L.dg_last_error.restype = ctypes.c_char_p
+    L.dg_last_error.argtypes = []
+    L.dg_check_status.argtypes = [vp]
+    L.dg_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.dg_selftest_wait_timeout.argtypes = [vp]
+    L.dg_launch_count.restype = ctypes.c_uint64
+    L.dg_launch_count.argtypes = []
+    L.dg_shutdown.argtypes = []
+    for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_check_status",
+                 "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout", "dg_shutdown"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def last_error():
+    return lib().dg_last_error().decode()
+
+
+def _check(status):
+    if status != 0:
+        raise DgError(status, last_error())
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(d):
+    return DTYPES[d] if isinstance(d, str) else int(d)
+
+
+def _epi_code(e):
+    return EPILOGUES[e] if isinstance(e, str) else int(e)
+
+
+def gemm_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue,
+             stream=None, plan=None):
+    """dg_gemm / dg_gemm_planned with the C argument order.  A, B, C, bias are
+    tensors or raw device addresses; dtypes and epilogue are names or codes."""
+    L = lib()
+    args = (int(M), int(N), int(K), _dtype_code(dtype_a), _dtype_code(dtype_b), _ptr(A), int(lda),
+            _ptr(B), int(ldb), _ptr(C), _ptr(bias), float(alpha), float(beta),
+            _epi_code(epilogue))
+    s = _stream_handle(stream)
+    if plan is None:
+        _check(L.dg_gemm(*args, s))
+    else:
+        if isinstance(plan, dict):
+            p = TilePlan(**{k: v for k, v in plan.items() if k in dict(TilePlan._fields_)})
+        else:
+            p = plan
+        _check(L.dg_gemm_planned(*args, ctypes.byref(p), s))
+
+
+_TORCH_DTYPES = None
+
+
+def _expect(t, kinds, what):
+    import torch
+    global _TORCH_DTYPES
+    if _TORCH_DTYPES is None:
+        _TORCH_DTYPES = {"f16": torch.float16, "i8": torch.int8, "e2m1": torch.uint8,
+                         "i32": torch.int32}
+    if t.dtype != _TORCH_DTYPES[kinds]:
+        raise TypeError("%s must be %s, got %s" % (what, _TORCH_DTYPES[kinds], t.dtype))
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("%s must be 2-D with unit column stride" % what)
+
+
+def gemm(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none", dtype_b=None,
+         stream=None, plan=None):
+    """D = epilogue(alpha * A.B + beta * C), written into C.
+
+    A: [M, lda] (fp16 or int8); B: [N, ldb] (fp16/int8) or [N, ldb/2] uint8
+    packed E2M1 codes; C: [M, N] fp16 (int32 for int8); K defaults to
+    A.shape[1]; bias: [N] fp16.  The leading dimensions are the row strides.
+    """
+    import torch
+    dtype_a = "i8" if A.dtype == torch.int8 else "f16"
+    if dtype_b is None:
+        dtype_b = {torch.float16: "f16", torch.int8: "i8", torch.uint8: "e2m1"}[B.dtype]
+    _expect(A, dtype_a, "A")
+    _expect(B, dtype_b, "B")
+    _expect(C, "i32" if dtype_a == "i8" else "f16", "C")
+    M, N = C.shape
+    if A.shape[0] != M or B.shape[0] != N:
+        raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape),
+                                                               tuple(C.shape)))
+    if C.stride(0) != N:
+        raise ValueError("C must be dense row-major (leading dimension N)")
+    if K is None:
+        K = A.shape[1]
+    lda = A.stride(0)
+    ldb = B.stride(0) * (2 if dtype_b == "e2m1" else 1)
+    gemm_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue,
+             stream=stream, plan=plan)
+    return C
+
+
+def query_hw(device=0):
+    h = HwDesc()
+    _check(lib().dg_query_hw(int(device), ctypes.byref(h)))
+    return h
+
+
+def plan_tiles(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", hw=None,
+               target_occupancy=0.0, max_out=64):
+    """The planner's ranked candidates (list of dicts)."""
+    if isinstance(hw, dict):
+        h = HwDesc(**hw)
+        hw_p = ctypes.byref(h)
+    elif hw is not None:
+        hw_p = ctypes.byref(hw)
+    else:
+        hw_p = None
+    out = (TilePlan * max_out)()
+    n = ctypes.c_int(0)
+    _check(lib().dg_plan_tiles(int(M), int(N), int(K), _dtype_code(dtype_a), _dtype_code(dtype_b),
+                               _epi_code(epilogue), hw_p, float(target_occupancy), out,
+                               int(max_out), ctypes.byref(n)))
+    return [out[i].as_dict() for i in range(n.value)]
+
+
+def check_status(stream=None):
+    _check(lib().dg_check_status(_stream_handle(stream)))
+
+
+def set_wait_timeout_ns(ns):
+    _check(lib().dg_set_wait_timeout_ns(int(ns)))
+
+
+def selftest_wait_timeout(stream=None):
+    _check(lib().dg_selftest_wait_timeout(_stream_handle(stream)))
+
+
+def launch_count():
+    return int(lib().dg_launch_count())
+
+
+def shutdown():
+    _check(lib().dg_shutdown())

@@ -1,0 +1,440 @@
+// C ABI of libdg: argument validation, planning, dispatch and error state.
+//
+// Interface conventions taken from the "DeepGEMM" articles: a null/failure
+// return plus a last-error string (discosf.com/news/5532976, section 3.4 and
+// section 5.1 question 3: launches are asynchronous and their errors must be
+// checked), and positional GEMM arguments A, B, C, alpha, beta, m, n, k
+// (kwkr.cn/news/562171, section 3.2 step 4).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "dg.h"
+#include "internal.h"
+
+namespace dg {
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_timeout_ns{0};
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
+
+dg_status fail(dg_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+dg_status fail_cuda(cudaError_t e, const char* what) {
+  return fail(DG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceState {
+  bool ready = false;
+  dg_hw_desc hw{};
+  int* status = nullptr;  // device status word
+};
+
+struct Workspace {
+  float* partial = nullptr;
+  int64_t partial_elems = 0;
+  unsigned* counters = nullptr;
+  int64_t counter_elems = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+std::map<std::tuple<int, int64_t, int64_t, int64_t, int, int, int>, dg_tile_plan> g_plans;
+
+dg_status fill_hw(int device, dg_hw_desc* out) {
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess || count == 0) {
+    cudaGetLastError();
+    return fail(DG_ERR_INVALID_STATE, "no CUDA device available (%s)", cudaGetErrorName(e));
+  }
+  if (device < 0 || device >= count) return fail(DG_ERR_INVALID_STATE, "no device %d", device);
+  auto attr = [&](cudaDeviceAttr a) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, a, device);
+    return v;
+  };
+  dg_hw_desc h{};
+  h.sm_count = attr(cudaDevAttrMultiProcessorCount);
+  h.cc_major = attr(cudaDevAttrComputeCapabilityMajor);
+  h.cc_minor = attr(cudaDevAttrComputeCapabilityMinor);
+  h.smem_per_block_optin = attr(cudaDevAttrMaxSharedMemoryPerBlockOptin);
+  h.smem_per_sm = attr(cudaDevAttrMaxSharedMemoryPerMultiprocessor);
+  h.regs_per_sm = attr(cudaDevAttrMaxRegistersPerMultiprocessor);
+  h.regs_per_thread_max = 255;
+  h.max_threads_per_sm = attr(cudaDevAttrMaxThreadsPerMultiProcessor);
+  // Tensor memory (512 columns x 128 lanes per SM) exists on the sm_100 family.
+  h.tmem_cols = (h.cc_major == 10) ? 512 : 0;
+  h.l2_bytes = attr(cudaDevAttrL2CacheSize);
+  const double mem_khz = attr(cudaDevAttrMemoryClockRate);
+  const double bus_bits = attr(cudaDevAttrGlobalMemoryBusWidth);
+  h.hbm_gbps = mem_khz * 1e3 * 2.0 * bus_bits / 8.0 / 1e9;
+  h.clock_ghz = attr(cudaDevAttrClockRate) / 1e6;
+  // Dense FP16 tensor rate of an sm_100-family SM: 8192 FLOP per clock.
+  h.tc_f16_tflops = (h.cc_major == 10) ? h.sm_count * 8192.0 * h.clock_ghz * 1e9 / 1e12 : 0.0;
+  *out = h;
+  return DG_OK;
+}
+
+dg_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DG_ERR_INVALID_STATE, "no current CUDA device (%s)", cudaGetErrorName(e));
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    dg_status s = fill_hw(dev, &st.hw);
+    if (s != DG_OK) return s;
+    if (st.hw.cc_major != 10 || st.hw.cc_minor != 3) {
+      return fail(DG_ERR_INVALID_STATE,
+                  "device %d is sm_%d%d; libdg is built for sm_103a (GB300) only", dev,
+                  st.hw.cc_major, st.hw.cc_minor);
+    }
+    e = cudaMalloc(&st.status, sizeof(int));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(status word)");
+    e = cudaMemset(st.status, 0, sizeof(int));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemset(status word)");
+    st.ready = true;
+  }
+  *out = &st;
+  return DG_OK;
+}
+
+int elem_bits(dg_dtype t) {
+  switch (t) {
+    case DG_F16: return 16;
+    case DG_I8: return 8;
+    case DG_E2M1: return 4;
+  }
+  return 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dg_status validate(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const void* A,
+                   int64_t lda, const void* B, int64_t ldb, void* C, const void* bias,
+                   float alpha, float beta, dg_epilogue epi) {
+  const bool pair_ok = (da == DG_F16 && db == DG_F16) || (da == DG_I8 && db == DG_I8) ||
+                       (da == DG_F16 && db == DG_E2M1);
+  if (!pair_ok)
+    return fail(DG_ERR_UNSUPPORTED, "dtype pair (%d, %d) not supported: F16xF16, I8xI8, F16xE2M1",
+                static_cast<int>(da), static_cast<int>(db));
+  if (epi < DG_EPI_NONE || epi > DG_EPI_BIAS_GELU)
+    return fail(DG_ERR_INVALID_ARG, "unknown epilogue %d", static_cast<int>(epi));
+  if (M < 0 || N < 0 || K < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
+  if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30))
+    return fail(DG_ERR_INVALID_ARG, "size above 2^30");
+  if (M == 0 || N == 0) return DG_OK;
+  if (!C) return fail(DG_ERR_INVALID_ARG, "C/D is null");
+  if (!aligned16(C)) return fail(DG_ERR_INVALID_ARG, "C/D is not 16-byte aligned");
+  if (da == DG_I8) {
+    if (epi != DG_EPI_NONE)
+      return fail(DG_ERR_UNSUPPORTED, "the INT8 path has no bias/GELU epilogue");
+    if (!(isfinite(alpha) && isfinite(beta)) || alpha != floorf(alpha) || beta != floorf(beta) ||
+        fabsf(alpha) >= 2147483648.0f || fabsf(beta) >= 2147483648.0f)
+      return fail(DG_ERR_UNSUPPORTED, "the INT8 path takes integral alpha and beta below 2^31");
+  } else if (!(isfinite(alpha) && isfinite(beta))) {
+    return fail(DG_ERR_INVALID_ARG, "alpha and beta must be finite");
+  }
+  if ((epi == DG_EPI_BIAS || epi == DG_EPI_BIAS_GELU)) {
+    if (!bias) return fail(DG_ERR_INVALID_ARG, "bias epilogue with a null bias");
+    if (reinterpret_cast<uintptr_t>(bias) & 1u)
+      return fail(DG_ERR_INVALID_ARG, "bias is not 2-byte aligned");
+  }
+  if (K == 0) return DG_OK;
+  if (!A || !B) return fail(DG_ERR_INVALID_ARG, "A or B is null");
+  if (!aligned16(A) || !aligned16(B))
+    return fail(DG_ERR_INVALID_ARG, "A and B must be 16-byte aligned");
+  if (lda < K) return fail(DG_ERR_INVALID_ARG, "lda (%lld) < K (%lld)", (long long)lda, (long long)K);
+  if (ldb < K) return fail(DG_ERR_INVALID_ARG, "ldb (%lld) < K (%lld)", (long long)ldb, (long long)K);
+  if ((lda * elem_bits(da)) % 128 != 0)
+    return fail(DG_ERR_INVALID_ARG, "lda * element size must be a multiple of 16 bytes");
+  if (db == DG_E2M1 && (ldb % 2) != 0) return fail(DG_ERR_INVALID_ARG, "E2M1 ldb must be even");
+  if ((ldb * elem_bits(db)) % 128 != 0)
+    return fail(DG_ERR_INVALID_ARG, "ldb * element size must be a multiple of 16 bytes");
+  return DG_OK;
+}
+
+uint64_t timeout_ns() {
+  const uint64_t t = g_timeout_ns.load();
+  return t ? t : kDefaultTimeoutNs;
+}
+
+dg_status get_workspace(int dev, cudaStream_t stream, int64_t partial_elems, int64_t counter_elems,
+                        SplitKWorkspace* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+  if (w.partial_elems < partial_elems) {
+    if (w.partial) cudaFree(w.partial);  // synchronises the device: no kernel still uses it
+    w.partial = nullptr;
+    w.partial_elems = 0;
+    cudaError_t e = cudaMalloc(&w.partial, partial_elems * sizeof(float));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(split-K partials)");
+    w.partial_elems = partial_elems;
+  }
+  if (w.counter_elems < counter_elems) {
+    if (w.counters) cudaFree(w.counters);
+    w.counters = nullptr;
+    w.counter_elems = 0;
+    cudaError_t e = cudaMalloc(&w.counters, counter_elems * sizeof(unsigned));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(split-K counters)");
+    e = cudaMemset(w.counters, 0, counter_elems * sizeof(unsigned));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemset(split-K counters)");
+    w.counter_elems = counter_elems;
+  }
+  out->partial = w.partial;
+  out->partial_elems = w.partial_elems;
+  out->counters = w.counters;
+  out->counter_elems = w.counter_elems;
+  return DG_OK;
+}
+
+dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const void* A,
+              int64_t lda, const void* B, int64_t ldb, void* C, const void* bias, float alpha,
+              float beta, dg_epilogue epilogue, const dg_tile_plan* forced, cudaStream_t stream) {
+  g_last_error.clear();
+  dg_status s = validate(M, N, K, da, db, A, lda, B, ldb, C, bias, alpha, beta, epilogue);
+  if (s != DG_OK) return s;
+  if (M == 0 || N == 0) return DG_OK;
+  DeviceState* st = nullptr;
+  s = device_state(&st);
+  if (s != DG_OK) return s;
+  int dev = 0;
+  cudaGetDevice(&dev);
+
+  GemmArgs a;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.dtype_a = da;
+  a.dtype_b = db;
+  a.A = A;
+  a.lda = lda;
+  a.B = B;
+  a.ldb = ldb;
+  a.C = C;
+  a.bias = bias;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.epi = ((epilogue == DG_EPI_BIAS || epilogue == DG_EPI_BIAS_GELU) ? kEpiBias : 0) |
+          ((epilogue == DG_EPI_GELU || epilogue == DG_EPI_BIAS_GELU) ? kEpiGelu : 0);
+  a.stream = stream;
+  a.status = st->status;
+  a.timeout_ns = timeout_ns();
+  a.sm_count = st->hw.sm_count;
+
+  if (K == 0) {
+    cudaError_t e = launch_epilogue_only(a);
+    return e == cudaSuccess ? DG_OK : fail_cuda(e, "epilogue-only launch");
+  }
+
+  dg_tile_plan plan{};
+  if (forced) {
+    std::string why;
+    if (!plan_is_runnable(*forced, M, N, K, da, db, &why))
+      return fail(DG_ERR_INVALID_STATE, "plan not runnable: %s", why.c_str());
+    plan = *forced;
+  } else {
+    const auto key = std::make_tuple(dev, M, N, K, static_cast<int>(da), static_cast<int>(db),
+                                     static_cast<int>(epilogue));
+    bool have = false;
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      auto it = g_plans.find(key);
+      if (it != g_plans.end()) {
+        plan = it->second;
+        have = true;
+      }
+    }
+    if (!have) {
+      std::string why;
+      int n = 0;
+      s = plan_tiles(M, N, K, da, db, epilogue, st->hw, 0.0, &plan, 1, &n, &why);
+      if (s != DG_OK || n == 0)
+        return fail(DG_ERR_NO_VALID_CANDIDATE, "no valid candidate found after pruning: %s",
+                    why.c_str());
+      std::lock_guard<std::mutex> lock(g_mu);
+      g_plans[key] = plan;
+    }
+  }
+  if (getenv("DG_LOG")) {
+    fprintf(stderr,
+            "[dg] M=%lld N=%lld K=%lld kernel=%d tile=%dx%dx%d split_k=%d stages=%d grid=%d "
+            "est=%.2fus\n",
+            (long long)M, (long long)N, (long long)K, plan.kernel, plan.m_tile, plan.n_tile,
+            plan.k_tile, plan.split_k, plan.stages, plan.grid, plan.est_us);
+  }
+
+  cudaError_t e = cudaSuccess;
+  if (plan.kernel == DG_KERNEL_GEMV) {
+    SplitKWorkspace ws{nullptr, 0, nullptr, 0};
+    if (plan.split_k > 1) {
+      s = get_workspace(dev, stream, gemv_partial_elems(plan, M, N), gemv_counter_elems(plan, N),
+                        &ws);
+      if (s != DG_OK) return s;
+    }
+    e = launch_gemv(a, plan, ws);
+  } else if (plan.kernel == DG_KERNEL_TC) {
+    e = launch_tc(a, plan);
+  } else {
+    return fail(DG_ERR_INVALID_STATE, "plan names no kernel of this library");
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return DG_OK;
+}
+
+}  // namespace
+
+void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+dg_status dg_query_hw(int device, dg_hw_desc* out) {
+  g_last_error.clear();
+  if (!out) return fail(DG_ERR_INVALID_ARG, "out is null");
+  return fill_hw(device, out);
+}
+
+dg_status dg_plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                        dg_epilogue epilogue, const dg_hw_desc* hw, double target_occupancy,
+                        dg_tile_plan* out, int max_out, int* n_out) {
+  g_last_error.clear();
+  if (n_out) *n_out = 0;
+  if (M <= 0 || N <= 0 || K <= 0) return fail(DG_ERR_INVALID_ARG, "M, N and K must be >= 1");
+  if (max_out > 0 && !out) return fail(DG_ERR_INVALID_ARG, "out is null");
+  if (!(target_occupancy >= 0.0 && target_occupancy <= 1.0))
+    return fail(DG_ERR_INVALID_ARG, "target_occupancy must lie in [0, 1]");
+  const bool pair_ok = (dtype_a == DG_F16 && dtype_b == DG_F16) ||
+                       (dtype_a == DG_I8 && dtype_b == DG_I8) ||
+                       (dtype_a == DG_F16 && dtype_b == DG_E2M1);
+  if (!pair_ok) return fail(DG_ERR_UNSUPPORTED, "dtype pair not supported");
+  dg_hw_desc local{};
+  if (!hw) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(DG_ERR_INVALID_STATE, "hw is null and there is no current CUDA device");
+    }
+    dg_status s = fill_hw(dev, &local);
+    if (s != DG_OK) return s;
+    hw = &local;
+  }
+  if (hw->sm_count <= 0 || hw->smem_per_block_optin <= 0 || hw->regs_per_sm <= 0 ||
+      hw->max_threads_per_sm <= 0)
+    return fail(DG_ERR_INVALID_ARG, "hardware description has empty fields");
+  std::string why;
+  dg_status s = plan_tiles(M, N, K, dtype_a, dtype_b, epilogue, *hw, target_occupancy, out,
+                           max_out, n_out, &why);
+  if (s == DG_ERR_NO_VALID_CANDIDATE)
+    return fail(s, "no valid candidate found after pruning: %s", why.c_str());
+  return s;
+}
+
+dg_status dg_gemm(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                  const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                  const void* bias, float alpha, float beta, dg_epilogue epilogue,
+                  dg_stream_t stream) {
+  return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue, nullptr,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                          const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                          const void* bias, float alpha, float beta, dg_epilogue epilogue,
+                          const dg_tile_plan* plan, dg_stream_t stream) {
+  if (!plan) return fail(DG_ERR_INVALID_ARG, "plan is null");
+  return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue, plan,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* dg_last_error(void) { return g_last_error.c_str(); }
+
+dg_status dg_check_status(dg_stream_t stream) {
+  g_last_error.clear();
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, st->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e, "reading the status word");
+  if (word != 0) {
+    const int zero = 0;
+    cudaMemcpy(st->status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (word == static_cast<int>(DG_ERR_TIMEOUT))
+      return fail(DG_ERR_TIMEOUT, "a kernel gave up on a pipeline wait after its time limit");
+    return fail(DG_ERR_INVALID_STATE, "device status word %d", word);
+  }
+  return DG_OK;
+}
+
+dg_status dg_set_wait_timeout_ns(uint64_t ns) {
+  g_last_error.clear();
+  g_timeout_ns.store(ns);
+  return DG_OK;
+}
+
+dg_status dg_selftest_wait_timeout(dg_stream_t stream) {
+  g_last_error.clear();
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  cudaError_t e = launch_wait_selftest(reinterpret_cast<cudaStream_t>(stream), st->status,
+                                       timeout_ns());
+  return e == cudaSuccess ? DG_OK : fail_cuda(e, "self-test launch");
+}
+
+uint64_t dg_launch_count(void) { return g_launches.load(); }
+
+dg_status dg_shutdown(void) {
+  g_last_error.clear();
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  const bool have_dev = cudaGetDevice(&cur) == cudaSuccess;
+  for (auto& kv : g_workspaces) {
+    cudaSetDevice(kv.first.first);
+    if (kv.second.partial) cudaFree(kv.second.partial);
+    if (kv.second.counters) cudaFree(kv.second.counters);
+  }
+  g_workspaces.clear();
+  for (auto& kv : g_devices) {
+    if (kv.second.status) {
+      cudaSetDevice(kv.first);
+      cudaFree(kv.second.status);
+    }
+  }
+  g_devices.clear();
+  g_plans.clear();
+  if (have_dev) cudaSetDevice(cur);
+  cudaGetLastError();
+  return DG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,284 @@
+// Thin-M GEMM on the CUDA cores: y[m, j] = sum_k a[m, k] * B[j, k] for M <= 8.
+//
+// The "DeepGEMM" articles single out thin shapes that template libraries
+// handle badly: M=1 with N=4096, K=131072 and M=1, N=256, K=12800
+// (kwkr.cn/news/562171, section 2.1), and a small M=1 projection for which
+// plain FMA beats the tensor cores (discosf.com/news/5532976, section 5.3,
+// "use_hmma: false").  At M <= 8 the work is one pass over B, so this kernel
+// is built for HBM bandwidth:
+//   * one warp streams one row of B (one output column) over a K range with
+//     128-bit non-allocating loads, several in flight per lane;
+//   * each lane keeps FP32 partial sums in registers, then the warp reduces
+//     them with xor-shuffles (discosf.com article, section 4.1 stage 3: warp
+//     partial sums via shfl.sync rather than shared memory);
+//   * long K is split over grid.y (split-K).  Each split writes FP32 partials
+//     to a workspace; the last CTA of a row group to arrive adds the splits in
+//     index order (deterministic) and applies the fused epilogue.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "epilogue.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kGemvWarps = 8;     // warps (= B rows) per CTA
+constexpr int kGemvUnroll = 4;    // 16-byte loads in flight per lane per row
+constexpr int kGemvMaxM = 8;
+
+struct GemvParams {
+  int M, N, K;
+  const __half* A;
+  int64_t lda;
+  const __half* B;
+  int64_t ldb;
+  __half* CD;  // C in, D out (leading dimension N)
+  const __half* bias;
+  Epi epi;
+  int split_k;
+  int k_chunk;  // K elements per split (multiple of 8)
+  float* partial;       // [split_k][M][N] when split_k > 1
+  unsigned* counters;   // [gridDim.x] when split_k > 1, zero between launches
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void fma8(float& acc, const uint4& a, const uint4& b) {
+  const __half2* ah = reinterpret_cast<const __half2*>(&a);
+  const __half2* bh = reinterpret_cast<const __half2*>(&b);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = __half22float2(ah[i]);
+    const float2 fb = __half22float2(bh[i]);
+    acc = fmaf(fa.x, fb.x, acc);
+    acc = fmaf(fa.y, fb.y, acc);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void write_out(const GemvParams& p, int m, int j, float acc) {
+  const int64_t idx = static_cast<int64_t>(m) * p.N + j;
+  const float c = (p.epi.beta != 0.0f) ? __half2float(p.CD[idx]) : 0.0f;
+  const float b = (p.epi.flags & kEpiBias) ? __half2float(p.bias[j]) : 0.0f;
+  p.CD[idx] = __float2half_rn(epi_apply(acc, c, b, p.epi));
+}
+
+template <int MROWS>
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const GemvParams p) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x * kGemvWarps + warp;
+  const int split = blockIdx.y;
+  const int k0 = split * p.k_chunk;
+  const int k1 = min(p.K, k0 + p.k_chunk);
+
+  float acc[MROWS];
+#pragma unroll
+  for (int m = 0; m < MROWS; ++m) acc[m] = 0.0f;
+
+  if (j < p.N && k0 < k1) {
+    const __half* brow = p.B + static_cast<int64_t>(j) * p.ldb;
+    int k = k0 + lane * 8;
+    // Main body: kGemvUnroll full 256-element steps per iteration.
+    constexpr int kStep = 256;
+    for (; k + (kGemvUnroll - 1) * kStep + 8 <= k1; k += kGemvUnroll * kStep) {
+      uint4 bv[kGemvUnroll];
+#pragma unroll
+      for (int u = 0; u < kGemvUnroll; ++u) bv[u] = ld_stream(brow + k + u * kStep);
+#pragma unroll
+      for (int u = 0; u < kGemvUnroll; ++u) {
+#pragma unroll
+        for (int m = 0; m < MROWS; ++m) {
+          if (m < p.M) {
+            const uint4 av = __ldg(reinterpret_cast<const uint4*>(
+                p.A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
+            fma8(acc[m], av, bv[u]);
+          }
+        }
+      }
+    }
+    // Remaining whole 8-element groups.
+    for (; k + 8 <= k1; k += kStep) {
+      const uint4 bv = ld_stream(brow + k);
+#pragma unroll
+      for (int m = 0; m < MROWS; ++m) {
+        if (m < p.M) {
+          const uint4 av =
+              __ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(m) * p.lda + k));
+          fma8(acc[m], av, bv);
+        }
+      }
+    }
+    // Ragged tail (< 8 elements at the end of the K range), scalar.
+    if (k < k1) {
+      for (int kk = k; kk < k1; ++kk) {
+        const float bf = __half2float(brow[kk]);
+#pragma unroll
+        for (int m = 0; m < MROWS; ++m)
+          if (m < p.M)
+            acc[m] = fmaf(__half2float(p.A[static_cast<int64_t>(m) * p.lda + kk]), bf, acc[m]);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int m = 0; m < MROWS; ++m) acc[m] = warp_sum(acc[m]);
+
+  if (p.split_k == 1) {
+    if (lane == 0 && j < p.N) {
+#pragma unroll
+      for (int m = 0; m < MROWS; ++m)
+        if (m < p.M) write_out(p, m, j, acc[m]);
+    }
+    return;
+  }
+
+  // Split-K: publish this split's partial sums, then the last CTA of the
+  // row group reduces all splits in index order.
+  if (lane == 0 && j < p.N) {
+#pragma unroll
+    for (int m = 0; m < MROWS; ++m)
+      if (m < p.M)
+        p.partial[(static_cast<int64_t>(split) * p.M + m) * p.N + j] = acc[m];
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ unsigned s_is_last;
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&p.counters[blockIdx.x], 1u);
+    s_is_last = (prev == static_cast<unsigned>(p.split_k - 1)) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_is_last) return;
+  __threadfence();
+  // One thread per (m, row) of the group; splits added in order 0..split_k-1.
+  for (int t = threadIdx.x; t < kGemvWarps * p.M; t += blockDim.x) {
+    const int m = t / kGemvWarps;
+    const int jj = blockIdx.x * kGemvWarps + (t % kGemvWarps);
+    if (jj >= p.N) continue;
+    float s = 0.0f;
+    for (int sp = 0; sp < p.split_k; ++sp)
+      s += __ldcg(&p.partial[(static_cast<int64_t>(sp) * p.M + m) * p.N + jj]);
+    write_out(p, m, jj, s);
+  }
+  if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;  // ready for the next launch
+}
+
+// K == 0: D = epilogue(beta * C), no product term.
+__global__ void epilogue_only_kernel(int64_t M, int64_t N, __half* CD, const __half* bias,
+                                     Epi epi) {
+  const int64_t total = M * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t j = i % N;
+    const float c = (epi.beta != 0.0f) ? __half2float(CD[i]) : 0.0f;
+    const float b = (epi.flags & kEpiBias) ? __half2float(bias[j]) : 0.0f;
+    CD[i] = __float2half_rn(epi_apply(0.0f, c, b, epi));
+  }
+}
+
+// K == 0 on the integer path: D = beta * C (mod 2^32).
+__global__ void epilogue_only_i32_kernel(int64_t total, int32_t* CD, int32_t beta) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t c = (beta != 0) ? static_cast<uint32_t>(CD[i]) : 0u;
+    CD[i] = static_cast<int32_t>(static_cast<uint32_t>(beta) * c);
+  }
+}
+
+// One CTA waits on a barrier nobody arrives on; the bounded wait must give up,
+// record the timeout and let the kernel exit normally.
+__global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_wait(&bar, 0, timeout_ns, status);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N) {
+  return plan.split_k > 1 ? static_cast<int64_t>(plan.split_k) * M * N : 0;
+}
+
+int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N) {
+  return plan.split_k > 1 ? (N + kGemvWarps - 1) / kGemvWarps : 0;
+}
+
+cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws) {
+  GemvParams p;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.A = static_cast<const __half*>(a.A);
+  p.lda = a.lda;
+  p.B = static_cast<const __half*>(a.B);
+  p.ldb = a.ldb;
+  p.CD = static_cast<__half*>(a.C);
+  p.bias = static_cast<const __half*>(a.bias);
+  p.epi = Epi{a.alpha, a.beta, a.epi};
+  p.split_k = plan.split_k;
+  p.k_chunk = plan.k_tile;
+  p.partial = ws.partial;
+  p.counters = ws.counters;
+  const dim3 grid(static_cast<unsigned>((a.N + kGemvWarps - 1) / kGemvWarps),
+                  static_cast<unsigned>(plan.split_k));
+  const dim3 block(kGemvWarps * 32);
+  if (a.M <= 1)
+    gemv_splitk_kernel<1><<<grid, block, 0, a.stream>>>(p);
+  else if (a.M <= 2)
+    gemv_splitk_kernel<2><<<grid, block, 0, a.stream>>>(p);
+  else if (a.M <= 4)
+    gemv_splitk_kernel<4><<<grid, block, 0, a.stream>>>(p);
+  else
+    gemv_splitk_kernel<kGemvMaxM><<<grid, block, 0, a.stream>>>(p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_epilogue_only(const GemmArgs& a) {
+  const int64_t total = a.M * a.N;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(a.sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (a.dtype_a == DG_I8) {
+    epilogue_only_i32_kernel<<<static_cast<unsigned>(blocks), threads, 0, a.stream>>>(
+        total, static_cast<int32_t*>(a.C), static_cast<int32_t>(a.beta));
+  } else {
+    epilogue_only_kernel<<<static_cast<unsigned>(blocks), threads, 0, a.stream>>>(
+        a.M, a.N, static_cast<__half*>(a.C), static_cast<const __half*>(a.bias),
+        Epi{a.alpha, a.beta, a.epi});
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,64 @@
+// Declarations shared by the host translation units of libdg (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "dg.h"
+
+namespace dg {
+
+// Epilogue flags as the kernels see them.
+enum : int { kEpiBias = 1, kEpiGelu = 2 };
+
+// Everything a launcher needs to run one GEMM, already validated.
+struct GemmArgs {
+  int64_t M, N, K;
+  dg_dtype dtype_a, dtype_b;
+  const void* A;
+  int64_t lda;
+  const void* B;
+  int64_t ldb;
+  void* C;  // in: C (when beta != 0); out: D
+  const void* bias;
+  float alpha, beta;
+  int epi;  // kEpiBias | kEpiGelu
+  cudaStream_t stream;
+  int* status;          // per-device status word (device memory)
+  uint64_t timeout_ns;  // device-side wait limit
+  int sm_count;
+};
+
+// Planner (planner.cpp) -- host only.
+dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                     dg_epilogue epilogue, const dg_hw_desc& hw, double target_occupancy,
+                     dg_tile_plan* out, int max_out, int* n_out, std::string* why);
+
+// Whether the kernels shipped here can run `plan` for this problem.
+bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
+                      dg_dtype dtype_a, dg_dtype dtype_b, std::string* why);
+
+// Scratch for split-K reductions: FP32 partial sums and arrival counters.
+struct SplitKWorkspace {
+  float* partial;
+  int64_t partial_elems;
+  unsigned* counters;
+  int64_t counter_elems;
+};
+
+// Launchers (gemm_tc.cu, gemv.cu).  Each returns cudaSuccess or the launch error.
+cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);
+cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws);
+cudaError_t launch_epilogue_only(const GemmArgs& a);
+cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns);
+
+// Workspace sizes a GEMV plan needs.
+int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N);
+int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N);
+
+// Kernel-launch counter (api.cu).
+void count_launches(int n);
+
+}  // namespace dg

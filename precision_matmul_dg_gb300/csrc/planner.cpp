@@ -1,0 +1,303 @@
+// Tile planner: the constraint system of the "DeepGEMM" articles' first layer
+// (kwkr.cn/news/562171, section 2.2, "Hardware-Aware Tile Planner"):
+//
+//   SharedMemoryUsage(M_tile, N_tile, K_tile, dtype) <= available shared memory
+//   RegisterUsage(M_tile, N_tile, K_tile, dtype)     <= registers available
+//   Occupancy(M_tile, N_tile, K_tile)                >= target (e.g. 0.7)
+//
+// solved for one hardware description and one problem, returning the
+// surviving (M_tile, N_tile, K_tile, split-K, stages) candidates ranked by a
+// cost model (section 3.2 step 2 of the same article; discosf.com/news/5532976
+// section 4.1 stage 2 prunes an enumerated candidate space the same way).
+//
+// Two tile families are enumerated:
+//  * Blackwell (hw.tmem_cols > 0): the kernels compiled into this library --
+//    the tcgen05 tensor-core kernel (constraints add tensor-memory columns:
+//    two 128 x N_tile FP32 accumulators) and the split-K GEMV for thin M.
+//    These kernels are persistent with one CTA per SM by design, so
+//    "occupancy" is read as wave efficiency: work units / (waves * SMs).
+//  * Earlier GPUs (hw.tmem_cols == 0): a warp-level-MMA family in the pages'
+//    own ranges (M, N in [16, 128], K in [16, 64]) with warp occupancy
+//    (resident warps / maximum warps).  Planning only: this library has no
+//    kernel for it, and dg_gemm_planned rejects such plans.
+#include <math.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace dg {
+namespace {
+
+// Shapes of the tcgen05 kernel compiled into gemm_tc.cu: (N_tile, stages).
+struct TcVariant {
+  int n_tile, stages;
+};
+constexpr TcVariant kTcVariants[] = {{256, 4}, {128, 6}, {64, 8}};
+constexpr int kTcBlockM = 128;
+constexpr int kTcBlockK = 64;
+constexpr int kTcThreads = 256;
+constexpr int kTcRegsPerThread = 168;  // upper bound of what ptxas assigns these kernels
+constexpr int kTcBarrierBytes = 512;
+
+constexpr int kGemvWarps = 8;
+constexpr int kGemvThreads = kGemvWarps * 32;
+constexpr int kGemvRegsPerThread = 64;
+constexpr int kGemvMaxM = 8;
+constexpr int kGemvResidentWarpsPerSm = 64;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int tc_smem_bytes(int n_tile, int stages) {
+  return stages * (kTcBlockM * kTcBlockK * 2 + n_tile * kTcBlockK * 2) + kTcBarrierBytes + 1024;
+}
+
+double sm_rate_flops_per_us(const dg_hw_desc& hw) {
+  const double tflops = hw.tc_f16_tflops > 0 ? hw.tc_f16_tflops : 1900.0;
+  return tflops * 1e6 / std::max(1, hw.sm_count);  // FLOP per microsecond per SM
+}
+
+double hbm_bytes_per_us(const dg_hw_desc& hw) {
+  const double gbps = hw.hbm_gbps > 0 ? hw.hbm_gbps : 6800.0;
+  return gbps * 1e3;  // GB/s -> bytes per microsecond
+}
+
+// Fraction of the tensor rate a 128 x N_tile tcgen05 tile sustains: operand
+// bytes read from shared memory per MMA grow relative to the math as N_tile
+// shrinks.  A rough model, not a measurement.
+double tc_tile_efficiency(int n_tile) {
+  switch (n_tile) {
+    case 256: return 0.92;
+    case 128: return 0.80;
+    default: return 0.55;
+  }
+}
+
+void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+                       const dg_hw_desc& hw, double target, std::vector<dg_tile_plan>* out,
+                       std::string* why) {
+  if (!(da == DG_F16 && db == DG_F16)) {
+    if (why) *why += "tensor-core kernel: dtype pair not compiled; ";
+    return;
+  }
+  if (hw.cc_major < 10 || hw.tmem_cols <= 0) {
+    if (why) *why += "tensor-core kernel: needs tcgen05 / tensor memory; ";
+    return;
+  }
+  const double elem = 2.0;
+  for (const TcVariant& v : kTcVariants) {
+    const int smem = tc_smem_bytes(v.n_tile, v.stages);
+    if (smem > hw.smem_per_block_optin) {
+      if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": shared memory; ";
+      continue;
+    }
+    if (2 * v.n_tile > hw.tmem_cols) {
+      if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": tensor memory; ";
+      continue;
+    }
+    if (kTcRegsPerThread > hw.regs_per_thread_max ||
+        kTcRegsPerThread * kTcThreads > hw.regs_per_sm) {
+      if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": registers; ";
+      continue;
+    }
+    const int64_t tiles = ceil_div(M, kTcBlockM) * ceil_div(N, v.n_tile);
+    const int64_t waves = ceil_div(tiles, hw.sm_count);
+    const double occ = static_cast<double>(tiles) / static_cast<double>(waves * hw.sm_count);
+    if (occ < target) {
+      if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": occupancy; ";
+      continue;
+    }
+    const int64_t k_pad = ceil_div(K, kTcBlockK) * kTcBlockK;
+    const double tile_flops = 2.0 * kTcBlockM * v.n_tile * static_cast<double>(k_pad);
+    const double t_math =
+        waves * tile_flops / (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile));
+    const double bytes = elem * (M * K + N * K) + 2.0 * M * N * 2.0;
+    const double t_mem = bytes / hbm_bytes_per_us(hw);
+    const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
+    dg_tile_plan p{};
+    p.kernel = DG_KERNEL_TC;
+    p.m_tile = kTcBlockM;
+    p.n_tile = v.n_tile;
+    p.k_tile = kTcBlockK;
+    p.split_k = 1;
+    p.stages = v.stages;
+    p.cta_group = 1;
+    p.swap_ab = 0;
+    p.smem_bytes = smem;
+    p.threads = kTcThreads;
+    p.grid = static_cast<int>(std::min<int64_t>(tiles, hw.sm_count));
+    p.occupancy = occ;
+    p.est_us = std::max(t_math, t_mem) + t_epi + 2.0;
+    p.est_tflops = 2.0 * M * N * K / (p.est_us * 1e6);
+    out->push_back(p);
+  }
+}
+
+void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+                         const dg_hw_desc& hw, double target, std::vector<dg_tile_plan>* out,
+                         std::string* why) {
+  if (!(da == DG_F16 && db == DG_F16)) {
+    if (why) *why += "GEMV: dtype pair not compiled; ";
+    return;
+  }
+  if (M > kGemvMaxM) {
+    if (why) *why += "GEMV: M > 8; ";
+    return;
+  }
+  if (kGemvRegsPerThread * kGemvThreads > hw.regs_per_sm) {
+    if (why) *why += "GEMV: registers; ";
+    return;
+  }
+  const int64_t resident = static_cast<int64_t>(hw.sm_count) * kGemvResidentWarpsPerSm;
+  for (int split = 1; split <= 256; split *= 2) {
+    // K per split, a multiple of 256 (one warp-wide step of 8 elements per lane).
+    const int64_t chunk = ceil_div(ceil_div(K, split), 256) * 256;
+    if (split > 1 && chunk * (split - 1) >= K) break;  // last split would be empty
+    if (chunk > (int64_t(1) << 30)) continue;
+    const int64_t units = N * split;  // warps
+    const int64_t waves = ceil_div(units, resident);
+    const double occ = static_cast<double>(units) / static_cast<double>(waves * resident);
+    if (occ < target) {
+      if (why) *why += "GEMV split " + std::to_string(split) + ": occupancy; ";
+      continue;
+    }
+    // Bandwidth: each warp keeps about 2 KB in flight (~2 GB/s); HBM caps the total.
+    const double active = static_cast<double>(std::min(units, resident));
+    const double bw = std::min(hbm_bytes_per_us(hw), active * 2.0e3);
+    const double bytes = 2.0 * (N * K + M * K) + (split > 1 ? 8.0 * split * M * N : 0.0) +
+                         4.0 * M * N;
+    const double t = bytes / bw + (split > 1 ? 1.0 : 0.0) + 2.0;
+    dg_tile_plan p{};
+    p.kernel = DG_KERNEL_GEMV;
+    p.m_tile = static_cast<int>(M);
+    p.n_tile = kGemvWarps;
+    p.k_tile = static_cast<int>(chunk);
+    p.split_k = split;
+    p.stages = 1;
+    p.cta_group = 1;
+    p.swap_ab = 0;
+    p.smem_bytes = 0;
+    p.threads = kGemvThreads;
+    p.grid = static_cast<int>(ceil_div(N, kGemvWarps) * split);
+    p.occupancy = occ;
+    p.est_us = t;
+    p.est_tflops = 2.0 * M * N * K / (t * 1e6);
+    out->push_back(p);
+  }
+}
+
+// Warp-level-MMA tile family for GPUs without tensor memory (planning only).
+void add_warp_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, const dg_hw_desc& hw,
+                             double target, std::vector<dg_tile_plan>* out, std::string* why) {
+  const int elem = (da == DG_I8) ? 1 : 2;
+  const int max_warps = std::max(1, hw.max_threads_per_sm / 32);
+  const int sizes_mn[] = {16, 32, 48, 64, 80, 96, 112, 128};
+  const int sizes_k[] = {16, 32, 48, 64};
+  for (int mt : sizes_mn) {
+    for (int nt : sizes_mn) {
+      for (int kt : sizes_k) {
+        const int stages = 2;
+        // One warp per 32 x 32 block of outputs (at least one warp).
+        const int warps = std::max(1, (mt * nt) / 1024);
+        const int threads = warps * 32;
+        const int smem = stages * (mt + nt) * kt * elem;
+        const int acc_regs = (mt * nt) / threads;  // FP32 accumulators per thread
+        const int regs = 32 + acc_regs + (mt + nt) * kt * elem / (4 * threads) + 16;
+        if (smem > hw.smem_per_block_optin || regs > hw.regs_per_thread_max) continue;
+        int ctas = std::min(hw.smem_per_sm / std::max(1, smem), hw.max_threads_per_sm / threads);
+        ctas = std::min(ctas, hw.regs_per_sm / (regs * threads));
+        ctas = std::min(ctas, 32);
+        if (ctas < 1) continue;
+        const double occ = std::min(1.0, static_cast<double>(ctas * warps) / max_warps);
+        if (occ < target) continue;
+        const int64_t tiles = ceil_div(M, mt) * ceil_div(N, nt);
+        const int64_t slots = static_cast<int64_t>(hw.sm_count) * ctas;
+        const int64_t waves = ceil_div(tiles, slots);
+        // Operand re-reads from L2 per tile grow as tiles shrink.
+        const double l2_bytes = static_cast<double>(tiles) * (mt + nt) * K * elem;
+        const double rate = sm_rate_flops_per_us(hw) * hw.sm_count;
+        const double t_math = 2.0 * M * N * K / rate *
+                              static_cast<double>(waves * slots) / static_cast<double>(tiles);
+        const double t_l2 = l2_bytes / (4.0 * hbm_bytes_per_us(hw));
+        dg_tile_plan p{};
+        p.kernel = -1;  // no kernel in this library
+        p.m_tile = mt;
+        p.n_tile = nt;
+        p.k_tile = kt;
+        p.split_k = 1;
+        p.stages = stages;
+        p.cta_group = 1;
+        p.smem_bytes = smem;
+        p.threads = threads;
+        p.grid = static_cast<int>(std::min<int64_t>(tiles, slots));
+        p.occupancy = occ;
+        p.est_us = std::max(t_math, t_l2) + 2.0;
+        p.est_tflops = 2.0 * M * N * K / (p.est_us * 1e6);
+        out->push_back(p);
+      }
+    }
+  }
+  if (out->empty() && why) *why += "warp-MMA family: no tile meets every constraint; ";
+}
+
+}  // namespace
+
+dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                     dg_epilogue epilogue, const dg_hw_desc& hw, double target_occupancy,
+                     dg_tile_plan* out, int max_out, int* n_out, std::string* why) {
+  (void)epilogue;
+  if (n_out) *n_out = 0;
+  std::vector<dg_tile_plan> cands;
+  if (hw.tmem_cols > 0) {
+    add_tc_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
+    add_gemv_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
+  } else {
+    add_warp_mma_candidates(M, N, K, dtype_a, hw, target_occupancy, &cands, why);
+  }
+  if (cands.empty()) return DG_ERR_NO_VALID_CANDIDATE;
+  std::stable_sort(cands.begin(), cands.end(), [](const dg_tile_plan& a, const dg_tile_plan& b) {
+    return a.est_us < b.est_us;
+  });
+  const int n = std::min<int>(static_cast<int>(cands.size()), std::max(0, max_out));
+  for (int i = 0; i < n; ++i) out[i] = cands[i];
+  if (n_out) *n_out = (max_out <= 0) ? static_cast<int>(cands.size()) : n;
+  return DG_OK;
+}
+
+bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
+                      dg_dtype dtype_a, dg_dtype dtype_b, std::string* why) {
+  (void)N;
+  if (plan.kernel == DG_KERNEL_TC) {
+    if (!(dtype_a == DG_F16 && dtype_b == DG_F16)) {
+      if (why) *why = "tensor-core plan for a dtype pair it does not take";
+      return false;
+    }
+    if (plan.m_tile != kTcBlockM || plan.k_tile != kTcBlockK || plan.cta_group != 1 ||
+        plan.split_k != 1 || plan.swap_ab != 0) {
+      if (why) *why = "tensor-core plan shape not compiled";
+      return false;
+    }
+    for (const TcVariant& v : kTcVariants)
+      if (v.n_tile == plan.n_tile && v.stages == plan.stages) return true;
+    if (why) *why = "tensor-core N_tile/stages pair not compiled";
+    return false;
+  }
+  if (plan.kernel == DG_KERNEL_GEMV) {
+    if (!(dtype_a == DG_F16 && dtype_b == DG_F16) || M > kGemvMaxM) {
+      if (why) *why = "GEMV plan needs F16 x F16 and M <= 8";
+      return false;
+    }
+    if (plan.split_k < 1 || plan.k_tile <= 0 || plan.k_tile % 8 != 0 ||
+        static_cast<int64_t>(plan.k_tile) * plan.split_k < K) {
+      if (why) *why = "GEMV plan: K chunks do not cover K";
+      return false;
+    }
+    return true;
+  }
+  if (why) *why = "plan has no kernel in this library";
+  return false;
+}
+
+}  // namespace dg

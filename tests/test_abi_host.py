@@ -1,0 +1,153 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+symbol include/dg.h declares, its struct layouts match the binding, and
+invalid arguments are rejected synchronously (no GPU needed)."""
+
+import ctypes
+import os
+import re
+import subprocess
+import textwrap
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dg.h")
+
+
+@pytest.fixture(scope="module")
+def dg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import precision_matmul_dg_gb300 as dg
+    return dg
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports(dg):
+    assert _declared_functions() == sorted(dg.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(dg):
+    L = ctypes.CDLL(dg.lib_path())
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    nm = subprocess.run(["nm", "-D", "--defined-only", dg.lib_path()], capture_output=True,
+                        text=True)
+    if nm.returncode == 0:
+        defined = set(re.findall(r"\s[TW]\s+(\S+)", nm.stdout))
+        for name in _declared_functions():
+            assert name in defined, name
+
+
+def test_struct_layout_matches_c(dg, tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(textwrap.dedent("""
+        #include <stdio.h>
+        #include <stddef.h>
+        #include "dg.h"
+        #define F(T, f) printf(#T "." #f " %zu\\n", offsetof(T, f));
+        int main(void) {
+          printf("dg_hw_desc %zu\\n", sizeof(dg_hw_desc));
+          printf("dg_tile_plan %zu\\n", sizeof(dg_tile_plan));
+          F(dg_hw_desc, l2_bytes) F(dg_hw_desc, hbm_gbps) F(dg_hw_desc, clock_ghz)
+          F(dg_tile_plan, grid) F(dg_tile_plan, occupancy) F(dg_tile_plan, est_tflops)
+          return 0;
+        }
+    """))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = dict(line.rsplit(" ", 1) for line in subprocess.run(
+        [str(exe)], capture_output=True, text=True, check=True).stdout.split("\n") if line)
+    assert int(out["dg_hw_desc"]) == ctypes.sizeof(dg.HwDesc)
+    assert int(out["dg_tile_plan"]) == ctypes.sizeof(dg.TilePlan)
+    for key, val in out.items():
+        if "." in key:
+            struct, field = key.split(".")
+            cls = dg.HwDesc if struct == "dg_hw_desc" else dg.TilePlan
+            assert getattr(cls, field).offset == int(val), key
+
+
+# ---------------------------------------------------------------- validation
+# Pointers below are fake device addresses: every call must be rejected (or be
+# a no-op) before anything touches a GPU.
+
+GOOD = dict(M=64, N=64, K=64, dtype_a="f16", dtype_b="f16", A=0x10000, lda=64, B=0x20000, ldb=64,
+            C=0x30000, bias=None, alpha=1.0, beta=0.0, epilogue="none")
+
+
+def _call(dg, **over):
+    kw = dict(GOOD)
+    kw.update(over)
+    try:
+        dg.gemm_raw(kw["M"], kw["N"], kw["K"], kw["dtype_a"], kw["dtype_b"], kw["A"], kw["lda"],
+                    kw["B"], kw["ldb"], kw["C"], kw["bias"], kw["alpha"], kw["beta"],
+                    kw["epilogue"], stream=0)
+    except dg.DgError as e:
+        return e.name, str(e)
+    return "DG_OK", ""
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(A=None), "DG_ERR_INVALID_ARG"),
+    (dict(B=None), "DG_ERR_INVALID_ARG"),
+    (dict(C=None), "DG_ERR_INVALID_ARG"),
+    (dict(A=0x10008), "DG_ERR_INVALID_ARG"),           # not 16-byte aligned
+    (dict(C=0x30002), "DG_ERR_INVALID_ARG"),
+    (dict(lda=32), "DG_ERR_INVALID_ARG"),               # lda < K
+    (dict(ldb=63, K=60), "DG_ERR_INVALID_ARG"),         # ldb*2 bytes not a multiple of 16
+    (dict(M=-1), "DG_ERR_INVALID_ARG"),
+    (dict(K=-5), "DG_ERR_INVALID_ARG"),
+    (dict(epilogue="bias"), "DG_ERR_INVALID_ARG"),      # bias epilogue, null bias
+    (dict(bias=0x40001, epilogue="bias"), "DG_ERR_INVALID_ARG"),
+    (dict(dtype_a="i8", dtype_b="f16"), "DG_ERR_UNSUPPORTED"),
+    (dict(dtype_a="e2m1", dtype_b="f16"), "DG_ERR_UNSUPPORTED"),
+    (dict(dtype_a="i8", dtype_b="i8", epilogue="gelu"), "DG_ERR_UNSUPPORTED"),
+    (dict(dtype_a="i8", dtype_b="i8", alpha=1.5), "DG_ERR_UNSUPPORTED"),
+    (dict(dtype_a="i8", dtype_b="i8", beta=float("nan")), "DG_ERR_UNSUPPORTED"),
+    (dict(dtype_b="e2m1", ldb=63), "DG_ERR_INVALID_ARG"),   # odd E2M1 leading dimension
+    (dict(dtype_b="e2m1", ldb=80), "DG_ERR_INVALID_ARG"),   # 40-byte packed rows
+    (dict(alpha=float("inf")), "DG_ERR_INVALID_ARG"),
+])
+def test_invalid_arguments_rejected(dg, over, status):
+    got, msg = _call(dg, **over)
+    assert got == status, msg
+    assert msg  # a message is set
+
+
+def test_empty_problem_is_a_noop(dg):
+    assert _call(dg, M=0)[0] == "DG_OK"
+    assert _call(dg, N=0, A=None, B=None)[0] == "DG_OK"
+
+
+def test_valid_call_without_gpu_reports_state(dg):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    got, msg = _call(dg)
+    assert got == "DG_ERR_INVALID_STATE", msg
+
+
+def test_last_error_is_cleared_by_next_call(dg):
+    _call(dg, A=None)
+    assert dg.last_error()
+    dg.set_wait_timeout_ns(0)
+    assert dg.last_error() == ""
+
+
+def test_launch_count_readable(dg):
+    assert dg.launch_count() >= 0
+
+
+def test_product_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "precision_matmul_dg_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.replace("oracle-free", ""), f

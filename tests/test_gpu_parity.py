@@ -1,0 +1,167 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Floating point: every element within 2^-10 * (|A|.|B|)_ij + 2^-10 * |D_ref|_ij
+(plus the 2^-24 floor and the GELU factor, see oracle.error_bound).
+INT8: bit-exact.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import assert_parity, run_case, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import precision_matmul_dg_gb300 as dg
+    assert torch.cuda.is_available()
+    return dg
+
+
+# ------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name", ["f16_256", "f16_2048", "f16_4096", "f16_8192",
+                                  "thin_1x256x12800", "thin_1x4096x131072"])
+def test_workload_full_size(dg, name):
+    case = workloads.WORKLOADS[name]()
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+# ------------------------------------------------------- shapes and tails
+RANDOM = [
+    (128, 256, 64), (300, 520, 200), (129, 257, 72), (1000, 17, 99), (17, 1000, 130),
+    (512, 384, 1000), (640, 768, 4096), (77, 2000, 333), (1031, 263, 1),
+]
+
+
+@pytest.mark.parametrize("shape", RANDOM, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("epi", ["none", "bias", "gelu", "bias_gelu"])
+def test_random_shapes(dg, shape, epi):
+    M, N, K = shape
+    case = workloads.random_case(M, N, K, epilogue=epi, alpha=-0.75, beta=0.5,
+                                 seed=hash((M, N, K, epi)) % 1000, pad=float("nan"))
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("K", [8, 100, 256, 4097, 20000])
+def test_thin_m(dg, M, K):
+    case = workloads.random_case(M, 300, K, epilogue="bias", beta=-1.25, seed=M * 7 + K,
+                                 pad=float("nan"))
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+def _plans(dg, case):
+    return dg.plan_tiles(case.M, case.N, case.K, case.dtype_a, case.dtype_b, case.epilogue,
+                         target_occupancy=0.0)
+
+
+def test_every_tensor_core_plan(dg):
+    case = workloads.random_case(520, 1100, 700, epilogue="bias_gelu", alpha=1.5, beta=0.25,
+                                 seed=5)
+    tc = [p for p in _plans(dg, case) if p["kernel_name"] == "tc"]
+    assert {p["n_tile"] for p in tc} == {64, 128, 256}
+    for p in tc:
+        for grid in (p["grid"], 7, 1):   # persistent CTAs walking several tiles each
+            q = dict(p, grid=grid)
+            got, _ = run_case(dg, case, plan=q)
+            assert_parity(case, got)
+
+
+def test_every_gemv_split(dg):
+    case = workloads.random_case(3, 200, 30000, beta=0.5, epilogue="gelu", seed=9)
+    gv = [p for p in _plans(dg, case) if p["kernel_name"] == "gemv"]
+    assert {p["split_k"] for p in gv} >= {1, 2, 4, 8}
+    outs = []
+    for p in gv:
+        got, _ = run_case(dg, case, plan=p)
+        assert_parity(case, got)
+        outs.append(got)
+
+
+# ------------------------------------------------------- edge cases
+def test_k_zero(dg):
+    for epi in ("none", "bias_gelu"):
+        case = workloads.random_case(33, 70, 8, epilogue=epi, beta=0.5, seed=3)
+        case.K = 0
+        got, _ = run_case(dg, case)
+        assert_parity(case, got)
+
+
+def test_empty_m_or_n(dg):
+    A = torch.zeros(4, 8, dtype=torch.float16, device="cuda")
+    B = torch.zeros(4, 8, dtype=torch.float16, device="cuda")
+    C = torch.zeros(0, 4, dtype=torch.float16, device="cuda")
+    before = dg.launch_count()
+    dg.gemm_raw(0, 4, 8, "f16", "f16", A, 8, B, 8, A, None, 1.0, 0.0, "none")
+    dg.gemm_raw(4, 0, 8, "f16", "f16", A, 8, B, 8, A, None, 1.0, 0.0, "none")
+    assert dg.launch_count() == before
+    del C
+
+
+def test_output_canary_untouched(dg):
+    for shape in [(129, 257, 72), (1, 1000, 5000), (256, 256, 256), (5, 3, 17)]:
+        case = workloads.random_case(*shape, epilogue="gelu", beta=0.5, seed=1)
+        got, tail = run_case(dg, case, canary=64)
+        assert_parity(case, got)
+        assert np.all(tail == np.float16(-7.5))
+
+
+def test_padded_leading_dimensions(dg):
+    case = workloads.random_case(200, 300, 100, lda=160, ldb=136, beta=0.5, seed=4,
+                                 pad=float("nan"))
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+def test_deterministic(dg):
+    for shape in [(1000, 1000, 1000), (1, 4096, 65536)]:
+        case = workloads.random_case(*shape, beta=0.5, seed=2)
+        a, _ = run_case(dg, case)
+        b, _ = run_case(dg, case)
+        assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_closed_forms_on_device(dg):
+    # all-ones: D = K exactly;  identity B: D = A exactly
+    K = 4096
+    case = workloads.random_case(256, 256, K, seed=0)
+    case.A = np.ones_like(case.A)
+    case.B = np.ones_like(case.B)
+    got, _ = run_case(dg, case)
+    assert np.all(got == np.float16(K))
+    case = workloads.random_case(300, 192, 192, seed=6)
+    case.B = np.eye(192, dtype=np.float16)
+    got, _ = run_case(dg, case)
+    assert np.array_equal(got, case.A[:, :192])
+
+
+def test_side_stream(dg):
+    s = torch.cuda.Stream()
+    case = workloads.random_case(384, 640, 512, epilogue="bias", beta=0.5, seed=8)
+    with torch.cuda.stream(s):
+        got, _ = run_case(dg, case, stream=s)
+    assert_parity(case, got)
+
+
+def test_timeout_is_reported_and_context_survives(dg):
+    dg.set_wait_timeout_ns(2_000_000)  # 2 ms
+    try:
+        dg.selftest_wait_timeout()
+        with pytest.raises(dg.DgError) as ei:
+            dg.check_status()
+        assert ei.value.name == "DG_ERR_TIMEOUT"
+    finally:
+        dg.set_wait_timeout_ns(0)
+    dg.check_status()  # cleared
+    case = workloads.random_case(256, 256, 256, seed=1)
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)

@@ -1,0 +1,180 @@
+"""Planner properties (host only).
+
+The constraint system (kwkr.cn "DeepGEMM" article, section 2.2 first layer):
+shared memory <= available, registers <= available, occupancy >= target.
+Each returned plan is re-checked here against those constraints written out
+independently, and the returned set is compared with a brute-force
+enumeration of the compiled tile space.
+"""
+
+import math
+import os
+
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+# A GB300-like description (152 SMs, 227 KB per CTA, 512 TMEM columns).
+GB300 = dict(sm_count=152, cc_major=10, cc_minor=3, smem_per_block_optin=232448,
+             smem_per_sm=233472, regs_per_sm=65536, regs_per_thread_max=255,
+             max_threads_per_sm=2048, tmem_cols=512, l2_bytes=126 * 1024 * 1024,
+             hbm_gbps=6800.0, tc_f16_tflops=1900.0, clock_ghz=2.07)
+
+# Compiled tensor-core variants: (N_tile, stages); M_tile 128, K_tile 64, 256 threads.
+TC_VARIANTS = [(256, 4), (128, 6), (64, 8)]
+
+
+@pytest.fixture(scope="module")
+def dg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import precision_matmul_dg_gb300 as dg
+    return dg
+
+
+def tc_smem(n_tile, stages):
+    return stages * (128 * 64 * 2 + n_tile * 64 * 2) + 512 + 1024
+
+
+def tc_feasible(M, N, hw, target):
+    out = set()
+    for n_tile, stages in TC_VARIANTS:
+        if tc_smem(n_tile, stages) > hw["smem_per_block_optin"]:
+            continue
+        if 2 * n_tile > hw["tmem_cols"]:
+            continue
+        if 256 * 168 > hw["regs_per_sm"]:
+            continue
+        tiles = math.ceil(M / 128) * math.ceil(N / n_tile)
+        waves = math.ceil(tiles / hw["sm_count"])
+        if tiles / (waves * hw["sm_count"]) < target:
+            continue
+        out.add(("tc", n_tile, stages, 1))
+    return out
+
+
+def gemv_feasible(M, N, K, hw, target):
+    out = set()
+    if M > 8:
+        return out
+    resident = hw["sm_count"] * 64
+    split = 1
+    while split <= 256:
+        chunk = math.ceil(math.ceil(K / split) / 256) * 256
+        if split > 1 and chunk * (split - 1) >= K:
+            break
+        units = N * split
+        waves = math.ceil(units / resident)
+        if units / (waves * resident) >= target:
+            out.add(("gemv", 8, 1, split))
+        split *= 2
+    return out
+
+
+SHAPES = [(256, 256, 256), (4096, 4096, 4096), (2048, 2048, 2048), (8192, 8192, 8192),
+          (1, 4096, 131072), (1, 256, 12800), (7, 1000, 999), (300, 520, 200), (129, 17, 64)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("target", [0.0, 0.5, 0.7, 0.9])
+def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
+    M, N, K = shape
+    want = tc_feasible(M, N, GB300, target) | gemv_feasible(M, N, K, GB300, target)
+    if not want:
+        with pytest.raises(dg.DgError) as ei:
+            dg.plan_tiles(M, N, K, hw=GB300, target_occupancy=target)
+        assert ei.value.name == "DG_ERR_NO_VALID_CANDIDATE"
+        assert "no valid candidate" in str(ei.value)
+        return
+    plans = dg.plan_tiles(M, N, K, hw=GB300, target_occupancy=target)
+    got = set()
+    for p in plans:
+        assert p["occupancy"] >= target - 1e-12
+        if p["kernel_name"] == "tc":
+            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"])
+            assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
+            assert 2 * p["n_tile"] <= GB300["tmem_cols"]
+            assert p["threads"] * 168 <= GB300["regs_per_sm"]
+            tiles = math.ceil(M / 128) * math.ceil(N / p["n_tile"])
+            assert p["grid"] == min(tiles, GB300["sm_count"])
+            assert p["m_tile"] == 128 and p["k_tile"] == 64 and p["split_k"] == 1
+            got.add(("tc", p["n_tile"], p["stages"], 1))
+        else:
+            assert p["kernel_name"] == "gemv"
+            assert p["k_tile"] % 256 == 0
+            assert p["k_tile"] * p["split_k"] >= K
+            assert p["k_tile"] * (p["split_k"] - 1) < K      # no empty split
+            got.add(("gemv", p["n_tile"], p["stages"], p["split_k"]))
+    assert got == want
+    # ranked by estimated time
+    ests = [p["est_us"] for p in plans]
+    assert ests == sorted(ests)
+
+
+def test_resources_prune(dg):
+    tiny = dict(GB300, smem_per_block_optin=64 * 1024)
+    with pytest.raises(dg.DgError) as ei:
+        dg.plan_tiles(4096, 4096, 4096, hw=tiny)
+    assert ei.value.name == "DG_ERR_NO_VALID_CANDIDATE"
+    # every compiled variant needs tc_smem(...) bytes; one byte less prunes it
+    for n, s in TC_VARIANTS:
+        tight = dict(GB300, smem_per_block_optin=tc_smem(n, s) - 1)
+        got = {p["n_tile"] for p in dg.plan_tiles(4096, 4096, 4096, hw=tight)
+               if p["kernel_name"] == "tc"} if any(
+            tc_smem(n2, s2) < tc_smem(n, s) for n2, s2 in TC_VARIANTS) else set()
+        assert n not in got
+    small_tmem = dict(GB300, tmem_cols=256)
+    assert {p["n_tile"] for p in dg.plan_tiles(4096, 4096, 4096, hw=small_tmem)} == {64, 128}
+
+
+def test_dtype_pairs(dg):
+    with pytest.raises(dg.DgError) as ei:
+        dg.plan_tiles(64, 64, 64, "i8", "f16", hw=GB300)
+    assert ei.value.name == "DG_ERR_UNSUPPORTED"
+
+
+def test_bad_planner_arguments(dg):
+    for bad in [dict(M=0), dict(K=-1), dict(target_occupancy=1.5)]:
+        kw = dict(M=64, N=64, K=64, hw=GB300, target_occupancy=0.0)
+        kw.update(bad)
+        with pytest.raises(dg.DgError) as ei:
+            dg.plan_tiles(kw["M"], kw["N"], kw["K"], hw=kw["hw"],
+                          target_occupancy=kw["target_occupancy"])
+        assert ei.value.name == "DG_ERR_INVALID_ARG"
+
+
+def _golden_a100():
+    d, tiles = {}, []
+    for line in open(os.path.join(GOLDEN, "planner_a100_example.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, *v = line.split()
+        if k == "tile":
+            tiles.append(tuple(int(x) for x in v))
+        else:
+            d[k] = v
+    return d, tiles
+
+
+def test_worked_example_tiles_fit_the_a100_description(dg):
+    """The article's A100 example: its three printed tiles satisfy the shared
+    memory constraint of the printed hardware description and are among the
+    planner's warp-MMA candidates.  The printed GFLOPS estimates and the count
+    of 7 solutions rest on a cost model the article does not give and are not
+    reproduced (parity unpinned)."""
+    d, tiles = _golden_a100()
+    smem = int(d["shared_memory_per_sm_kb"][0]) * 1024
+    cc = d["compute_capability"][0].split(".")
+    hw = dict(sm_count=108, cc_major=int(cc[0]), cc_minor=int(cc[1]), smem_per_block_optin=smem,
+              smem_per_sm=smem, regs_per_sm=65536, regs_per_thread_max=255,
+              max_threads_per_sm=int(d["max_threads_per_sm"][0]), tmem_cols=0,
+              l2_bytes=int(d["l2_cache_size_kb"][0]) * 1024, hbm_gbps=1555.0,
+              tc_f16_tflops=312.0, clock_ghz=1.41)
+    M, N, K = (int(x) for x in d["shape"])
+    plans = dg.plan_tiles(M, N, K, hw=hw, target_occupancy=0.0, max_out=4096)
+    got = {(p["m_tile"], p["n_tile"], p["k_tile"]) for p in plans}
+    for t in tiles:
+        assert t in got, t
+        assert 2 * (t[0] + t[1]) * t[2] * 2 <= smem
+    assert all(p["kernel_name"] == "none" for p in plans)  # planning only: no kernel here

@@ -71,17 +71,17 @@ def _bytes(g, shape):
     return torch.randint(0, 256, shape, generator=g, dtype=torch.int16).to(torch.uint8).numpy()
 
 
-def _pad_cols(x, ld):
-    """Place x [rows, cols] in a zero-initialised [rows, ld] buffer."""
+def _pad_cols(x, ld, fill=0):
+    """Place x [rows, cols] in a [rows, ld] buffer whose extra columns hold `fill`."""
     if ld == x.shape[1]:
         return np.ascontiguousarray(x)
-    out = np.zeros((x.shape[0], ld), dtype=x.dtype)
+    out = np.full((x.shape[0], ld), fill, dtype=x.dtype)
     out[:, : x.shape[1]] = x
     return out
 
 
 def random_case(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", alpha=1.0,
-                beta=0.0, seed=0, dist="normal", lda=None, ldb=None, name=None):
+                beta=0.0, seed=0, dist="normal", lda=None, ldb=None, name=None, pad=0):
     """A general random case for parity tests.
 
     dist: "normal" -> N(0,1)/sqrt(K) operands (the square-GEMM recipe),
@@ -90,6 +90,8 @@ def random_case(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", alpha=1.
     epilogue has a bias.  lda/ldb default to the smallest legal padded
     leading dimension (K rounded up to 8 fp16 / 16 int8 elements, 32 codes
     for packed 4-bit), so every leading dimension is a 16-byte multiple.
+    pad: value stored in the columns between K and the leading dimension
+    (e.g. NaN, to show those columns are never read).
     """
     g = _gen(seed)
     if dtype_a == "f16":
@@ -106,20 +108,20 @@ def random_case(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", alpha=1.
     if dtype_b == "f16":
         ldb = ldb or _round_up(K, 8)
         B = _normal(g, (N, K), 1.0 / math.sqrt(K)) if dist == "normal" else _uniform_pm1(g, (N, K))
-        B = _pad_cols(B, ldb)
+        B = _pad_cols(B, ldb, pad)
     elif dtype_b == "i8":
         ldb = ldb or _round_up(K, 16)
-        B = _pad_cols(_int8(g, (N, K)), ldb)
+        B = _pad_cols(_int8(g, (N, K)), ldb, pad)
     elif dtype_b == "e2m1":
         ldb = ldb or _round_up(K, 32)
         nbytes = (K + 1) // 2
         Bp = _bytes(g, (N, nbytes))
         if K % 2:
             Bp[:, -1] &= 0x0F  # the unused high nibble of an odd row is left zero
-        B = _pad_cols(Bp, ldb // 2)
+        B = _pad_cols(Bp, ldb // 2, pad)
     else:
         raise ValueError(dtype_b)
-    A = _pad_cols(A, lda)
+    A = _pad_cols(A, lda, pad)
     C = None
     if beta != 0.0:
         C = _int32(g, (M, N)) if dtype_a == "i8" else _normal(g, (M, N), 1.0)
