@@ -153,6 +153,31 @@ dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_
                           const void *bias, float alpha, float beta, dg_epilogue epilogue,
                           const dg_tile_plan *plan, dg_stream_t stream);
 
+/* Thin-M GEMM that allocates nothing.  The pages have no counterpart: this
+ * entry point exists for callers that cannot let a library call cudaMalloc
+ * (code that runs while a CUDA graph is being captured, runtimes that own all
+ * device memory through their own pool, locked-down allocators).
+ * Computes exactly what dg_gemm computes, for F16 x F16 with M <= 8, through
+ * the split-K GEMV kernel with the same split choice; its FP32 partial sums
+ * and arrival counters live in a file-scope static device array of
+ * 2 MiB + 64 KiB that every GPU loading the library holds until exit.
+ *  - The first call on a device looks the array's device address up with
+ *    cudaGetSymbolAddress (once per device, that device current); make that
+ *    first call before any stream capture.
+ *  - Shapes whose split-K partials (split * M * N * 4 bytes) or counters
+ *    (ceil(N/8) * 4 bytes) exceed the array are rejected with
+ *    DG_ERR_INVALID_ARG and a message; other pairs or M > 8 give
+ *    DG_ERR_UNSUPPORTED.
+ *  - Every call shares the one array and it keeps the last call's contents:
+ *    the call clears the counters on `stream` first (cudaMemsetAsync), and
+ *    calls that overlap on the GPU (other streams, other host threads) race.
+ *  - Calls no cudaMalloc/cudaFree and no allocating routine.  Arguments,
+ *    layouts and errors otherwise as dg_gemm. */
+dg_status dg_gemm_thin_noalloc(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a,
+                               dg_dtype dtype_b, const void *A, int64_t lda, const void *B,
+                               int64_t ldb, void *C, const void *bias, float alpha, float beta,
+                               dg_epilogue epilogue, dg_stream_t stream);
+
 /* Message for the last failing call on this thread ("" if none).  Valid
  * until the next libdg call on the same thread. */
 const char *dg_last_error(void);

@@ -25,7 +25,8 @@ STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
 KERNELS = {0: "tc", 1: "gemv", -1: "none"}
 
 # Every symbol include/dg.h declares.
-EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_last_error",
+EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
+           "dg_gemm_thin_noalloc", "dg_last_error",
            "dg_check_status", "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout",
            "dg_launch_count", "dg_shutdown"]
 
@@ -89,6 +90,7 @@ def lib():
     gemm_args = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, vp, f32, f32, i32]
     L.dg_gemm.argtypes = gemm_args + [vp]
     L.dg_gemm_planned.argtypes = gemm_args + [ctypes.POINTER(TilePlan), vp]
+    L.dg_gemm_thin_noalloc.argtypes = gemm_args + [vp]
     L.dg_last_error.restype = ctypes.c_char_p
     L.dg_last_error.argtypes = []
     L.dg_check_status.argtypes = [vp]
@@ -97,7 +99,8 @@ def lib():
     L.dg_launch_count.restype = ctypes.c_uint64
     L.dg_launch_count.argtypes = []
     L.dg_shutdown.argtypes = []
-    for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_check_status",
+    for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
+                 "dg_gemm_thin_noalloc", "dg_check_status",
                  "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout", "dg_shutdown"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L

@@ -23,18 +23,17 @@
 namespace dg {
 namespace {
 
-thread_local std::string g_last_error;
+// Fixed-size per-thread message buffer: recording an error allocates nothing.
+thread_local char g_last_error[512];
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_timeout_ns{0};
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
 
 dg_status fail(dg_status s, const char* fmt, ...) {
-  char buf[512];
   va_list ap;
   va_start(ap, fmt);
-  vsnprintf(buf, sizeof buf, fmt, ap);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
   va_end(ap);
-  g_last_error = buf;
   return s;
 }
 
@@ -214,7 +213,7 @@ dg_status get_workspace(int dev, cudaStream_t stream, int64_t partial_elems, int
 dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const void* A,
               int64_t lda, const void* B, int64_t ldb, void* C, const void* bias, float alpha,
               float beta, dg_epilogue epilogue, const dg_tile_plan* forced, cudaStream_t stream) {
-  g_last_error.clear();
+  clear_error();
   dg_status s = validate(M, N, K, da, db, A, lda, B, ldb, C, bias, alpha, beta, epilogue);
   if (s != DG_OK) return s;
   if (M == 0 || N == 0) return DG_OK;
@@ -309,6 +308,18 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
 
 void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 
+void clear_error() { g_last_error[0] = '\0'; }
+
+dg_status set_error(dg_status s, const char* msg) { return fail(s, "%s", msg); }
+
+dg_status fill_hw_desc(int device, dg_hw_desc* out) { return fill_hw(device, out); }
+
+dg_status validate_gemm_args(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+                             const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                             const void* bias, float alpha, float beta, dg_epilogue epi) {
+  return validate(M, N, K, da, db, A, lda, B, ldb, C, bias, alpha, beta, epi);
+}
+
 }  // namespace dg
 
 using namespace dg;
@@ -316,7 +327,7 @@ using namespace dg;
 extern "C" {
 
 dg_status dg_query_hw(int device, dg_hw_desc* out) {
-  g_last_error.clear();
+  clear_error();
   if (!out) return fail(DG_ERR_INVALID_ARG, "out is null");
   return fill_hw(device, out);
 }
@@ -324,7 +335,7 @@ dg_status dg_query_hw(int device, dg_hw_desc* out) {
 dg_status dg_plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
                         dg_epilogue epilogue, const dg_hw_desc* hw, double target_occupancy,
                         dg_tile_plan* out, int max_out, int* n_out) {
-  g_last_error.clear();
+  clear_error();
   if (n_out) *n_out = 0;
   if (M <= 0 || N <= 0 || K <= 0) return fail(DG_ERR_INVALID_ARG, "M, N and K must be >= 1");
   if (max_out > 0 && !out) return fail(DG_ERR_INVALID_ARG, "out is null");
@@ -373,10 +384,10 @@ dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_
              reinterpret_cast<cudaStream_t>(stream));
 }
 
-const char* dg_last_error(void) { return g_last_error.c_str(); }
+const char* dg_last_error(void) { return g_last_error; }
 
 dg_status dg_check_status(dg_stream_t stream) {
-  g_last_error.clear();
+  clear_error();
   DeviceState* st = nullptr;
   dg_status s = device_state(&st);
   if (s != DG_OK) return s;
@@ -396,13 +407,13 @@ dg_status dg_check_status(dg_stream_t stream) {
 }
 
 dg_status dg_set_wait_timeout_ns(uint64_t ns) {
-  g_last_error.clear();
+  clear_error();
   g_timeout_ns.store(ns);
   return DG_OK;
 }
 
 dg_status dg_selftest_wait_timeout(dg_stream_t stream) {
-  g_last_error.clear();
+  clear_error();
   DeviceState* st = nullptr;
   dg_status s = device_state(&st);
   if (s != DG_OK) return s;
@@ -414,7 +425,7 @@ dg_status dg_selftest_wait_timeout(dg_stream_t stream) {
 uint64_t dg_launch_count(void) { return g_launches.load(); }
 
 dg_status dg_shutdown(void) {
-  g_last_error.clear();
+  clear_error();
   std::lock_guard<std::mutex> lock(g_mu);
   int cur = 0;
   const bool have_dev = cudaGetDevice(&cur) == cudaSuccess;

@@ -17,6 +17,9 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
+
+#include <mutex>
 
 #include "epilogue.cuh"
 #include "internal.h"
@@ -281,4 +284,139 @@ cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t time
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Split-K scratch for callers that cannot allocate device memory.
+//
+// dg_gemm grows a cudaMalloc'd workspace the first time a shape needs split-K
+// partials.  Some callers cannot let a library call cudaMalloc: code running
+// while a CUDA graph is being captured, inference runtimes that hand out every
+// byte of device memory from their own pool, or hosts whose allocator is
+// locked down.  dg_gemm_thin_noalloc runs the same GEMV kernel with its
+// partial sums and arrival counters in this fixed, file-scope device array
+// instead.  Every GPU that loads the library holds these bytes until the
+// process exits.
+constexpr size_t kNoAllocCounterBytes = 64 * 1024;        // 16384 row-group counters
+constexpr size_t kNoAllocPartialBytes = 2 * 1024 * 1024;  // 524288 FP32 partial sums
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocCounterBytes +
+                                                                 kNoAllocPartialBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on `dev` (which must be current).  The
+// host-side name of the array is only a stand-in, so the address is looked up
+// once per device with cudaGetSymbolAddress.
+dg_status noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return set_error(DG_ERR_INVALID_STATE, "device index beyond the scratch table");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      cudaGetLastError();
+      return set_error(DG_ERR_CUDA, "cudaGetSymbolAddress of the static split-K scratch failed");
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return DG_OK;
+}
+}  // namespace
+
 }  // namespace dg
+
+using namespace dg;
+
+extern "C" dg_status dg_gemm_thin_noalloc(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a,
+                                          dg_dtype dtype_b, const void* A, int64_t lda,
+                                          const void* B, int64_t ldb, void* C, const void* bias,
+                                          float alpha, float beta, dg_epilogue epilogue,
+                                          dg_stream_t stream) {
+  clear_error();
+  dg_status s = validate_gemm_args(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha,
+                                   beta, epilogue);
+  if (s != DG_OK) return s;
+  if (M == 0 || N == 0) return DG_OK;
+  if (dtype_a != DG_F16 || dtype_b != DG_F16 || M > kGemvMaxM)
+    return set_error(DG_ERR_UNSUPPORTED, "dg_gemm_thin_noalloc takes F16 x F16 with M <= 8");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(DG_ERR_INVALID_STATE, "no current CUDA device");
+  }
+  dg_hw_desc hw{};
+  s = fill_hw_desc(dev, &hw);
+  if (s != DG_OK) return s;
+  if (hw.cc_major != 10 || hw.cc_minor != 3)
+    return set_error(DG_ERR_INVALID_STATE, "libdg is built for sm_103a (GB300) only");
+
+  // Same split-K choice as the planner's GEMV candidates.
+  int64_t chunk = 0;
+  const int split = gemv_best_split(M, N, K, hw, &chunk);
+  const int64_t row_groups = (N + kGemvWarps - 1) / kGemvWarps;
+  const int64_t partial_bytes = split > 1 ? static_cast<int64_t>(split) * M * N * 4 : 0;
+  const int64_t counter_bytes = split > 1 ? row_groups * 4 : 0;
+  if (partial_bytes > static_cast<int64_t>(kNoAllocPartialBytes) ||
+      counter_bytes > static_cast<int64_t>(kNoAllocCounterBytes)) {
+    char msg[256];
+    snprintf(msg, sizeof msg,
+             "shape needs %lld bytes of split-K partials and %lld bytes of counters; the static "
+             "scratch holds %zu and %zu",
+             (long long)partial_bytes, (long long)counter_bytes, kNoAllocPartialBytes,
+             kNoAllocCounterBytes);
+    return set_error(DG_ERR_INVALID_ARG, msg);
+  }
+
+  void* scratch = nullptr;
+  s = noalloc_scratch(dev, &scratch);
+  if (s != DG_OK) return s;
+  unsigned* counters = static_cast<unsigned*>(scratch);
+  float* partial =
+      reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + kNoAllocCounterBytes);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (split > 1) {
+    // The array keeps the previous call's contents; counters must start at zero.
+    e = cudaMemsetAsync(counters, 0, static_cast<size_t>(counter_bytes), st);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return set_error(DG_ERR_CUDA, "cudaMemsetAsync of the scratch counters failed");
+    }
+  }
+
+  GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.dtype_a = dtype_a;
+  a.dtype_b = dtype_b;
+  a.A = A;
+  a.lda = lda;
+  a.B = B;
+  a.ldb = ldb;
+  a.C = C;
+  a.bias = bias;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.epi = ((epilogue == DG_EPI_BIAS || epilogue == DG_EPI_BIAS_GELU) ? kEpiBias : 0) |
+          ((epilogue == DG_EPI_GELU || epilogue == DG_EPI_BIAS_GELU) ? kEpiGelu : 0);
+  a.stream = st;
+  a.status = nullptr;
+  a.timeout_ns = 0;
+  a.sm_count = hw.sm_count;
+  dg_tile_plan plan{};
+  plan.kernel = DG_KERNEL_GEMV;
+  plan.split_k = split;
+  plan.k_tile = static_cast<int>(chunk);
+  SplitKWorkspace ws{partial, partial_bytes / 4, counters, counter_bytes / 4};
+  e = launch_gemv(a, plan, ws);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(DG_ERR_CUDA, "GEMV launch failed");
+  }
+  return DG_OK;
+}

@@ -58,7 +58,19 @@ cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t time
 int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N);
 int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N);
 
-// Kernel-launch counter (api.cu).
+// Kernel-launch counter and error state (api.cu).  None of these allocate.
 void count_launches(int n);
+void clear_error();
+dg_status set_error(dg_status s, const char* msg);
+dg_status fill_hw_desc(int device, dg_hw_desc* out);
+dg_status validate_gemm_args(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+                             const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                             const void* bias, float alpha, float beta, dg_epilogue epi);
+
+// Split-K choice of the GEMV kernel (planner.cpp): cost-model time of one
+// split count (negative when the split is not allowed), and the best split.
+double gemv_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_desc& hw,
+                        int64_t* chunk_out);
+int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out);
 
 }  // namespace dg

@@ -47,6 +47,7 @@ constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kGemvRegsPerThread = 64;
 constexpr int kGemvMaxM = 8;
 constexpr int kGemvResidentWarpsPerSm = 64;
+constexpr int kGemvMaxSplit = 256;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -151,11 +152,10 @@ void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype 
     return;
   }
   const int64_t resident = static_cast<int64_t>(hw.sm_count) * kGemvResidentWarpsPerSm;
-  for (int split = 1; split <= 256; split *= 2) {
-    // K per split, a multiple of 256 (one warp-wide step of 8 elements per lane).
-    const int64_t chunk = ceil_div(ceil_div(K, split), 256) * 256;
-    if (split > 1 && chunk * (split - 1) >= K) break;  // last split would be empty
-    if (chunk > (int64_t(1) << 30)) continue;
+  for (int split = 1; split <= kGemvMaxSplit; split *= 2) {
+    int64_t chunk = 0;
+    const double t = gemv_estimate_us(M, N, K, split, hw, &chunk);
+    if (t < 0) break;  // the last split would be empty
     const int64_t units = N * split;  // warps
     const int64_t waves = ceil_div(units, resident);
     const double occ = static_cast<double>(units) / static_cast<double>(waves * resident);
@@ -163,12 +163,6 @@ void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype 
       if (why) *why += "GEMV split " + std::to_string(split) + ": occupancy; ";
       continue;
     }
-    // Bandwidth: each warp keeps about 2 KB in flight (~2 GB/s); HBM caps the total.
-    const double active = static_cast<double>(std::min(units, resident));
-    const double bw = std::min(hbm_bytes_per_us(hw), active * 2.0e3);
-    const double bytes = 2.0 * (N * K + M * K) + (split > 1 ? 8.0 * split * M * N : 0.0) +
-                         4.0 * M * N;
-    const double t = bytes / bw + (split > 1 ? 1.0 : 0.0) + 2.0;
     dg_tile_plan p{};
     p.kernel = DG_KERNEL_GEMV;
     p.m_tile = static_cast<int>(M);
@@ -243,6 +237,41 @@ void add_warp_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, const
 }
 
 }  // namespace
+
+// Cost model of the split-K GEMV for one split count.  K per split is a
+// multiple of 256 (one warp-wide step of 8 elements per lane).  Each warp
+// keeps about 2 KB in flight (~2 GB/s); HBM caps the total.  Returns a
+// negative value when the last split would be empty.  Allocates nothing.
+double gemv_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_desc& hw,
+                        int64_t* chunk_out) {
+  const int64_t kk = K > 0 ? K : 1;
+  const int64_t chunk = ceil_div(ceil_div(kk, split), 256) * 256;
+  if (split > 1 && chunk * (split - 1) >= kk) return -1.0;
+  if (chunk_out) *chunk_out = chunk;
+  const int64_t resident = static_cast<int64_t>(hw.sm_count) * kGemvResidentWarpsPerSm;
+  const int64_t units = N * split;
+  const double active = static_cast<double>(std::min(units, resident));
+  const double bw = std::min(hbm_bytes_per_us(hw), active * 2.0e3);
+  const double bytes = 2.0 * (N * K + M * K) + (split > 1 ? 8.0 * split * M * N : 0.0) +
+                       4.0 * M * N;
+  return bytes / bw + (split > 1 ? 1.0 : 0.0) + 2.0;
+}
+
+int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out) {
+  int best = 1;
+  double best_t = -1.0;
+  for (int split = 1; split <= kGemvMaxSplit; split *= 2) {
+    int64_t chunk = 0;
+    const double t = gemv_estimate_us(M, N, K, split, hw, &chunk);
+    if (t < 0) break;
+    if (best_t < 0 || t < best_t) {
+      best_t = t;
+      best = split;
+      if (chunk_out) *chunk_out = chunk;
+    }
+  }
+  return best;
+}
 
 dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
                      dg_epilogue epilogue, const dg_hw_desc& hw, double target_occupancy,
