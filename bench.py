@@ -157,9 +157,15 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "gemm_f16_tc_kernel": ("gemm_tc.cu", "ptx.cuh", "epilogue.cuh"),
+    "gemv_splitk_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh"),
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "ptx.cuh", "epilogue.cuh", "gemv.cu"):
+    for f in KERNEL_SOURCES.get(kernel, ()):
         p = os.path.join(ROOT, "precision_matmul_dg_gb300", "csrc", f)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
@@ -168,14 +174,14 @@ def kernel_source_hash():
 
 def recorded_traffic(kernel):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
