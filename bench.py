@@ -158,7 +158,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "gemm_f16_tc_kernel": ("gemm_tc.cu", "ptx.cuh", "epilogue.cuh"),
+    "gemm_f16_tc_kernel": ("gemm_tc.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh"),
+    "gemm_conv_tc_kernel": ("gemm_conv.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh"),
     "gemv_splitk_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh"),
 }
 
@@ -195,18 +196,33 @@ def workload_info(name):
         "f16_256": ("FP16 GEMM M=N=K=256, A,B~U[-1,1)", "tensor"),
         "thin_1x4096x131072": ("FP16 GEMV M=1,N=4096,K=131072 split-K", "hbm"),
         "thin_1x256x12800": ("FP16 GEMV M=1,N=256,K=12800 split-K", "hbm"),
+        "i8_4096": ("INT8 GEMM M=N=K=4096, A,B uniform int8, exact INT32 out", "tensor"),
+        "w4a16_m16": ("W4A16 M=16,N=8960,K=1536, E2M1 weights x FP16, bias+erf-GELU", "hbm"),
+        "w4a16_m2048": ("W4A16 M=2048,N=8960,K=1536, E2M1 weights x FP16, bias+erf-GELU",
+                        "tensor"),
     }
     return info[name]
 
 
 def algorithmic_bytes(case):
-    eb = 2
-    b = case.M * case.K * eb + case.N * case.K * eb + case.M * case.N * 2
+    """Bytes the GEMM must move at least once: A, B, C (if read), bias, D."""
+    ea = 1 if case.dtype_a == "i8" else 2
+    eb = {"f16": 2, "i8": 1, "e2m1": 0.5}[case.dtype_b]
+    ed = 4 if case.dtype_a == "i8" else 2
+    b = case.M * case.K * ea + case.N * case.K * eb + case.M * case.N * ed
     if case.beta != 0:
-        b += case.M * case.N * 2
+        b += case.M * case.N * ed
     if case.bias is not None:
         b += case.N * 2
-    return b
+    return int(b)
+
+
+def kernel_name(plan, case):
+    if plan["kernel_name"] == "gemv":
+        return "gemv_splitk_kernel"
+    if case.dtype_a == "f16" and case.dtype_b == "f16":
+        return "gemm_f16_tc_kernel"
+    return "gemm_conv_tc_kernel"
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -219,24 +235,23 @@ def run_dg(args, world, rank, local):
     name = args.workload
     desc, bound = workload_info(name)
     base = workloads.WORKLOADS[name]()
-    set_bytes = base.A.nbytes + base.B.nbytes + base.M * base.N * 2
+    out_dtype = torch.int32 if base.dtype_a == "i8" else torch.float16
+    out_bytes = 4 if base.dtype_a == "i8" else 2
+    set_bytes = base.A.nbytes + base.B.nbytes + base.M * base.N * out_bytes
     nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes)) if set_bytes < 3 * L2_BYTES else 1
     nsets = min(nsets, 16)
     sets = []
-    g = torch.Generator(device=dev)
+    A0 = torch.from_numpy(base.A).to(dev)
+    B0 = torch.from_numpy(base.B).to(dev)
+    C0 = (torch.from_numpy(base.C).to(dev) if base.C is not None else
+          torch.zeros(base.M, base.N, dtype=out_dtype, device=dev))
+    bias = torch.from_numpy(base.bias).to(dev) if base.bias is not None else None
     for s in range(nsets):
-        A = torch.from_numpy(base.A).to(dev)
-        B = torch.from_numpy(base.B).to(dev)
-        C = (torch.from_numpy(base.C).to(dev) if base.C is not None else
-             torch.zeros(base.M, base.N, dtype=torch.float16, device=dev))
-        if s > 0:  # further sets: same recipe, seeded on the device
-            g.manual_seed(1000 + s)
-            A.normal_(0, 1.0 / math.sqrt(base.K), generator=g)
-            B.normal_(0, 1.0 / math.sqrt(base.K), generator=g)
-            if base.C is not None:
-                C.normal_(0, 1.0, generator=g)
-        bias = torch.from_numpy(base.bias).to(dev) if base.bias is not None else None
-        sets.append((A, B, C, bias))
+        # further sets: the same values with rows rotated (same distribution,
+        # different addresses), so no step finds its operands in L2
+        sh = 37 * s
+        sets.append((torch.roll(A0, sh, 0).contiguous(), torch.roll(B0, sh, 0).contiguous(),
+                     torch.roll(C0, sh, 0).contiguous(), bias))
     stream = torch.cuda.current_stream(dev)
     plan = dg.plan_tiles(base.M, base.N, base.K, base.dtype_a, base.dtype_b, base.epilogue)[0]
 
@@ -275,17 +290,23 @@ def run_dg(args, world, rank, local):
     kern_avg_ms = sum(kern_ms) / len(kern_ms)
 
     total_ms_max = max_over_ranks(total_ms, world)
+    # Throughput unit: TFLOP/s (TOPS for INT8) for tensor-bound workloads,
+    # algorithmic GB/s for the HBM-bound thin ones.
+    if bound == "hbm":
+        work, unit = algorithmic_bytes(base) * 1e3, "GB/s"   # so that work / s / 1e12 = GB/s
+    else:
+        work, unit = base.flops(), ("TOPS" if base.dtype_a == "i8" else "TFLOP/s")
     flops = base.flops()
-    total_flops = sum_over_ranks(flops * args.steps, world)
-    value = total_flops / (total_ms_max * 1e-3) / 1e12
+    total_work = sum_over_ranks(work * args.steps, world)
+    value = total_work / (total_ms_max * 1e-3) / 1e12
 
     # e2e: the same GEMM through the public API with pinned host buffers,
     # host->device copies of A, B, C and the device->host read of D timed.
     hA = torch.from_numpy(base.A).pin_memory()
     hB = torch.from_numpy(base.B).pin_memory()
     hC = (torch.from_numpy(base.C) if base.C is not None else
-          torch.zeros(base.M, base.N, dtype=torch.float16)).pin_memory()
-    hD = torch.empty(base.M, base.N, dtype=torch.float16).pin_memory()
+          torch.zeros(base.M, base.N, dtype=out_dtype)).pin_memory()
+    hD = torch.empty(base.M, base.N, dtype=out_dtype).pin_memory()
     dA, dB, dC, dbias = sets[0]
 
     def e2e_step():
@@ -308,7 +329,7 @@ def run_dg(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e_value = sum_over_ranks(flops * e2e_steps, world) / (e2e_ms * 1e-3) / 1e12
+    e2e_value = sum_over_ranks(work * e2e_steps, world) / (e2e_ms * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
     achieved = flops / (kern_avg_ms * 1e-3) / 1e12
@@ -317,20 +338,26 @@ def run_dg(args, world, rank, local):
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "peak_source": "%s bf16 dense burst (fp16 runs at the bf16 rate)" % peak_src}
+        if base.dtype_a == "i8":
+            roof["unit"] = "TOPS"
+            roof["peak_source"] += ("; INT8 runs on the FP16 tensor path (sm_103a has no "
+                                    "integer tcgen05 MMA), so its denominator is the FP16 peak")
     else:
         gbs = algorithmic_bytes(base) / (kern_avg_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(gbs / peak, 4), "peak_source": "%s copy bandwidth" % peak_src}
-    kname = "gemm_f16_tc_kernel" if plan["kernel_name"] == "tc" else "gemv_splitk_kernel"
+    kname = kernel_name(plan, base)
     roof["kernel"] = kname
     roof["kernel_avg_us"] = round(kern_avg_ms * 1e3, 2)
     roof["traffic"] = recorded_traffic(kname)
+    roof["algorithmic_bytes"] = algorithmic_bytes(base)
+    roof["algorithmic_flops"] = flops
 
     line = {
         "metric": "GEMM TFLOP/s (INT8 TOPS) and % of GB300 dense peak; GB/s vs HBM for M=1",
         "value": round(value, 2),
-        "unit": "TFLOP/s",
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -338,7 +365,7 @@ def run_dg(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
+        "dtype": "i8" if base.dtype_a == "i8" else "f16",
         "data": "synthetic (seeded, recipe in workloads.py)",
         "config": {"workload": desc, "name": name, "M": base.M, "N": base.N, "K": base.K,
                    "alpha": base.alpha, "beta": base.beta, "epilogue": base.epilogue,
@@ -348,7 +375,7 @@ def run_dg(args, world, rank, local):
                    "plan": {k: plan[k] for k in ("kernel_name", "m_tile", "n_tile", "k_tile",
                                                  "split_k", "stages", "grid")}},
         "roofline": roof,
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(e2e_value, 2), "unit": unit,
                 "h2d_bytes_per_step": int(hA.nbytes + hB.nbytes + hC.nbytes),
                 "d2h_bytes_per_step": int(hD.nbytes)},
         "gpu_launches": int(launches),
@@ -358,9 +385,19 @@ def run_dg(args, world, rank, local):
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_sample_rate(case, budget_s, rows_per_call):
+def work_unit(case, bound):
+    """(work per whole problem, unit): FLOPs -> TFLOP/s (TOPS for INT8) for
+    tensor-bound workloads, algorithmic bytes -> GB/s for HBM-bound ones; both
+    scaled so that work / seconds / 1e12 is the value in that unit."""
+    if bound == "hbm":
+        return algorithmic_bytes(case) * 1e3, "GB/s"
+    return case.flops(), ("TOPS" if case.dtype_a == "i8" else "TFLOP/s")
+
+
+def oracle_sample_rate(case, budget_s, rows_per_call, bound="tensor"):
     """Times the oracle (fp64 definition) on row samples of `case` for about
-    budget_s seconds; returns (TFLOP/s, seconds, rows done)."""
+    budget_s seconds; returns (value in the metric's unit, unit, seconds,
+    rows done)."""
     import oracle
     rng = np.random.default_rng(0)
     done_rows, t_total = 0, 0.0
@@ -372,8 +409,8 @@ def oracle_sample_rate(case, budget_s, rows_per_call):
                               epilogue=case.epilogue, rows=rows)
         t_total += time.perf_counter() - t
         done_rows += len(rows)
-    flops = 2.0 * done_rows * case.N * case.K
-    return flops / t_total / 1e12, t_total, done_rows
+    work, unit = work_unit(case, bound)
+    return work * done_rows / case.M / t_total / 1e12, unit, t_total, done_rows
 
 
 def cpu_cores():
@@ -403,21 +440,22 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t
-    flops = 2.0 * rows * case.N * case.K * args.steps
-    value = flops / dt / 1e12
+    work, unit = work_unit(case, workload_info(name)[1])
+    value = work * rows / case.M * args.steps / dt / 1e12
     sample = "%d random rows of the %dx%dx%d product per step (%s)" % (rows, case.M, case.N,
                                                                       case.K, name)
     return {
         "impl": "reference",
         "metric": "GEMM TFLOP/s (INT8 TOPS) and % of GB300 dense peak; GB/s vs HBM for M=1",
-        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, recipe in workloads.py)",
-        "config": {"workload": desc, "name": name, "M": case.M, "N": case.N, "K": case.K},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+        "config": {"workload": desc, "name": name, "M": case.M, "N": case.N, "K": case.K,
+                   "alpha": case.alpha, "beta": case.beta, "epilogue": case.epilogue},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 
@@ -450,9 +488,10 @@ def main():
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             case = workloads.WORKLOADS[args.workload]()
-            v, secs, rows = oracle_sample_rate(case, budget_s=10.0, rows_per_call=256)
+            v, u, secs, rows = oracle_sample_rate(case, budget_s=10.0, rows_per_call=256,
+                                                  bound=workload_info(args.workload)[1])
             line["cpu_baseline"] = {
-                "value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                "value": v, "unit": u, "cores": cpu_cores(), "kind": "oracle",
                 "sample": "%d rows of the %dx%dx%d product in %.1f s (fp64 numpy BLAS, "
                           "default threads)" % (rows, case.M, case.N, case.K, secs)}
         print(json.dumps(line), flush=True)

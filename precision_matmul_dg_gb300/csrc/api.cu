@@ -296,7 +296,7 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
     }
     e = launch_gemv(a, plan, ws);
   } else if (plan.kernel == DG_KERNEL_TC) {
-    e = launch_tc(a, plan);
+    e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);
   } else {
     return fail(DG_ERR_INVALID_STATE, "plan names no kernel of this library");
   }

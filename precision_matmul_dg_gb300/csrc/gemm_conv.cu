@@ -1,0 +1,511 @@
+// Tensor-core GEMM for operands that are not FP16 in memory: INT8 x INT8 with
+// an exact INT32 result, and FP16 activations x packed 4-bit E2M1 weights
+// (W4A16) with the fused FP16 epilogue.
+//
+// Sources: INT8 4096^3 GEMM with INT32 output (discosf.com/news/5532976,
+// section 1 and section 4.3); the {weight: int4_e2m1, activation: fp16,
+// output: fp16} precision triple with 2 exponent + 1 mantissa bits (same
+// article, section 2.2 layer 2) packed two codes per byte (section 4.3,
+// "pack_int4"); bias + GELU fused (kwkr.cn/news/562171, section 2.2 third
+// layer).
+//
+// sm_103a has no integer tcgen05.mma and no mixed FP16 x FP4 kind, and its
+// legacy mma.sync s8 path is slow, so both contractions run on the FP16
+// tensor-core path with the narrow operand widened in shared memory:
+//
+//   warp 0       TMA producer: raw int8 / packed-E2M1 tiles (no swizzle) and
+//                FP16 tiles (128-byte swizzle) into a ring of `Stages` slots;
+//   warps 8-11   converters: raw -> FP16 in the swizzled K-major layout the
+//                MMA reads (int8: exact via the 1024+u magic-number trick;
+//                E2M1: cvt.rn.f16x2.e2m1x2, exact), then a proxy fence;
+//   warp 1       MMA issuer: tcgen05.mma kind::f16 into TMEM (FP32);
+//   warp 2       TMEM allocation;  warps 4-7  epilogue.
+//
+// INT8 exactness: every product is an integer of magnitude <= 2^14, so any
+// partial sum of at most 1024 products is an integer of magnitude <= 2^24 and
+// exact in FP32.  The MMA therefore accumulates K in chunks of 1024 into one
+// of two FP32 TMEM buffers; the epilogue converts each finished chunk to INT32
+// (exact) and adds it into an INT32 running sum kept in a third TMEM region.
+// The last chunk produces D = alpha*sum + beta*C in INT32 (wrapping mod 2^32).
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tc_common.cuh"
+
+namespace dg {
+namespace {
+
+using tc::kBlockK;
+using tc::kBlockM;
+
+enum : int { kOpF16 = 0, kOpI8 = 1, kOpE2M1 = 2 };
+enum : int { kOutF16 = 0, kOutI32 = 1 };
+
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kConvWarp0 = 8;
+constexpr int kConvThreads = 128;
+constexpr int kI32ChunkKb = 16;  // 16 x 64 = 1024 K per exact FP32 chunk
+
+struct ConvParams {
+  int M, N, K;
+  int num_m_blocks, num_n_blocks, num_tiles, num_k_blocks;
+  int group_m;
+  Epi epi;
+  void* CD;
+  const __half* bias;
+  int32_t alpha_i, beta_i;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+template <int BN, int Stages, int OpA, int OpB>
+struct ConvSmem {
+  static constexpr int kOpA = kBlockM * kBlockK * 2;
+  static constexpr int kOpB = BN * kBlockK * 2;
+  static constexpr int kRawA = OpA == kOpI8 ? kBlockM * kBlockK : 0;
+  static constexpr int kRawB = OpB == kOpI8 ? BN * kBlockK : (OpB == kOpE2M1 ? BN * kBlockK / 2 : 0);
+  static constexpr int kOffOpA = 0;
+  static constexpr int kOffOpB = kOffOpA + Stages * kOpA;
+  static constexpr int kOffRawA = kOffOpB + Stages * kOpB;
+  static constexpr int kOffRawB = kOffRawA + Stages * kRawA;
+  static constexpr int kOffBar = kOffRawB + Stages * kRawB;
+  // full[S], conv[S], empty[S], tmem_full[2], tmem_empty[2], drain
+  static constexpr int kNumBars = 3 * Stages + 5;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kBytes = kOffAbort + 4;
+  static constexpr int kLaunchBytes = kBytes + 1024;
+  // bytes TMA delivers per stage
+  static constexpr uint32_t kTx = (OpA == kOpF16 ? kOpA : kRawA) + (OpB == kOpF16 ? kOpB : kRawB);
+  static_assert(kRawA % 1024 == 0 && kRawB % 1024 == 0, "raw tiles keep 1 KB alignment");
+};
+
+__device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Four int8 (one 32-bit word) -> four FP16 (two 32-bit words), exact:
+// byte b -> fp16 bits 0x6400 | (b ^ 0x80) = 1024 + (v + 128), minus 1152.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
+  uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// Eight E2M1 codes (one 32-bit word, code k in bits 4k..4k+3) -> eight FP16.
+__device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w) {
+  uint4 o;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
+      : "r"(w));
+  return o;
+}
+
+// Byte offset of the 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
+// K-major tile (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Widen one stage's raw tile of `rows` rows into the FP16 operand tile.
+template <int Op, int Rows>
+__device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* op, int ct) {
+  constexpr int kUnits = Rows * 8;  // 16-byte output chunks
+#pragma unroll 4
+  for (int u = ct; u < kUnits; u += kConvThreads) {
+    const int r = u >> 3, c = u & 7;
+    uint4 o;
+    if (Op == kOpI8) {
+      const uint2 w = *reinterpret_cast<const uint2*>(raw + r * 64 + c * 8);
+      i8x4_to_f16x4(w.x, o.x, o.y);
+      i8x4_to_f16x4(w.y, o.z, o.w);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + r * 32 + c * 4);
+      o = e2m1x8_to_f16x8(w);
+    }
+    *reinterpret_cast<uint4*>(op + sw128_offset(r, c)) = o;
+  }
+}
+
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// INT32 output of one 32-column chunk: D = alpha*sum + beta*C (mod 2^32).
+__device__ __forceinline__ void store_i32_chunk(const uint32_t (&s)[32], int row, int col0,
+                                                const ConvParams& p) {
+  if (row >= p.M) return;
+  int32_t* drow = static_cast<int32_t*>(p.CD) + static_cast<int64_t>(row) * p.N;
+  const uint32_t al = static_cast<uint32_t>(p.alpha_i), be = static_cast<uint32_t>(p.beta_i);
+  const bool full = (col0 + 32 <= p.N) && ((p.N & 3) == 0);
+  if (full) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint4 v;
+      if (be != 0u) v = *reinterpret_cast<const uint4*>(drow + col0 + q * 4);
+      else v = make_uint4(0, 0, 0, 0);
+      v.x = al * s[q * 4 + 0] + be * v.x;
+      v.y = al * s[q * 4 + 1] + be * v.y;
+      v.z = al * s[q * 4 + 2] + be * v.z;
+      v.w = al * s[q * 4 + 3] + be * v.w;
+      *reinterpret_cast<uint4*>(drow + col0 + q * 4) = v;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (col0 + i < p.N) {
+        const uint32_t c = be != 0u ? static_cast<uint32_t>(drow[col0 + i]) : 0u;
+        drow[col0 + i] = static_cast<int32_t>(al * s[i] + be * c);
+      }
+    }
+  }
+}
+
+template <int BN, int Stages, int OpA, int OpB, int Out>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_conv_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b, const ConvParams p) {
+  using L = ConvSmem<BN, Stages, OpA, OpB>;
+  constexpr bool kConvA = OpA != kOpF16;
+  constexpr bool kConvB = OpB != kOpF16;
+  // FP32 accumulators x2, plus the INT32 running sums on the integer path.
+  constexpr int kColsNeeded = Out == kOutI32 ? 3 * BN : 2 * BN;
+  constexpr int kTmemCols = kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512);
+  constexpr uint32_t kIdesc = idesc_f16_f32(kBlockM, BN);
+  static_assert(kColsNeeded <= 512, "tensor memory");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* full_bar = bars;
+  uint64_t* conv_bar = bars + Stages;
+  uint64_t* empty_bar = bars + 2 * Stages;
+  uint64_t* tmem_full = bars + 3 * Stages;
+  uint64_t* tmem_empty = bars + 3 * Stages + 2;
+  uint64_t* drain_bar = bars + 3 * Stages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // K blocks per accumulation chunk (one FP32 accumulator fill).
+  const int chunk_kb = Out == kOutI32 ? kI32ChunkKb : p.num_k_blocks;
+  const int num_chunks = (p.num_k_blocks + chunk_kb - 1) / chunk_kb;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&conv_bar[s], kConvThreads);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 4 * 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 2) tmem_alloc<kTmemCols>(tmem_slot);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one_lane()) {
+      const uint64_t pol = policy_evict_normal();
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int m_blk, n_blk;
+        tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (aborted(abort_flag) ||
+              !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], L::kTx);
+          if (OpA == kOpF16)
+            tma_load_2d(&tmap_a, &full_bar[stage], smem + L::kOffOpA + stage * L::kOpA,
+                        kb * kBlockK, m_blk * kBlockM, pol);
+          else
+            tma_load_2d(&tmap_a, &full_bar[stage], smem + L::kOffRawA + stage * L::kRawA,
+                        kb * kBlockK, m_blk * kBlockM, pol);
+          if (OpB == kOpF16)
+            tma_load_2d(&tmap_b, &full_bar[stage], smem + L::kOffOpB + stage * L::kOpB,
+                        kb * kBlockK, n_blk * BN, pol);
+          else if (OpB == kOpI8)
+            tma_load_2d(&tmap_b, &full_bar[stage], smem + L::kOffRawB + stage * L::kRawB,
+                        kb * kBlockK, n_blk * BN, pol);
+          else  // packed E2M1: 64 codes = 32 bytes per row
+            tma_load_2d(&tmap_b, &full_bar[stage], smem + L::kOffRawB + stage * L::kRawB,
+                        kb * (kBlockK / 2), n_blk * BN, pol);
+          ++issued;
+          if (++stage == Stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        const int64_t first = issued > Stages ? issued - Stages : 0;
+        for (int64_t i = first; i < issued; ++i)
+          mbar_wait(&full_bar[i % Stages], static_cast<uint32_t>((i / Stages) & 1), p.timeout_ns,
+                    p.status);
+      }
+    }
+  } else if (warp >= kConvWarp0) {
+    // ------------------------------------------------------------ converters
+    const int ct = threadIdx.x - kConvWarp0 * 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        if (aborted(abort_flag) || !mbar_wait(&full_bar[stage], phase, p.timeout_ns, p.status)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        if (kConvA)
+          convert_tile<OpA, kBlockM>(smem + L::kOffRawA + stage * L::kRawA,
+                                     smem + L::kOffOpA + stage * L::kOpA, ct);
+        if (kConvB)
+          convert_tile<OpB, BN>(smem + L::kOffRawB + stage * L::kRawB,
+                                smem + L::kOffOpB + stage * L::kOpB, ct);
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        mbar_arrive(&conv_bar[stage]);
+        if (++stage == Stages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one_lane()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        for (int ch = 0; ch < num_chunks && ok; ++ch) {
+          if (aborted(abort_flag) ||
+              !mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.timeout_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          const int kb0 = ch * chunk_kb;
+          const int kb1 = min(p.num_k_blocks, kb0 + chunk_kb);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            uint64_t* ready = (kConvA || kConvB) ? &conv_bar[stage] : &full_bar[stage];
+            if (aborted(abort_flag) || !mbar_wait(ready, phase, p.timeout_ns, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t a0 = smem_addr(smem + L::kOffOpA + stage * L::kOpA);
+            const uint32_t b0 = smem_addr(smem + L::kOffOpB + stage * L::kOpB);
+#pragma unroll
+            for (int k = 0; k < kBlockK / 16; ++k) {
+              tc_mma_f16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32),
+                         kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            }
+            tc_commit(&empty_bar[stage]);
+            if (++stage == Stages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          tc_commit(&tmem_full[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        tc_commit(drain_bar);
+        mbar_wait(drain_bar, 0, p.timeout_ns, p.status);
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - kEpiWarp0;
+    const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
+    const uint32_t sums = tmem_base + lane_base + 2 * BN;  // INT32 running sums
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      int m_blk, n_blk;
+      tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
+      const int row = m_blk * kBlockM + ew * 32 + lane;
+      for (int ch = 0; ch < num_chunks; ++ch) {
+        if (aborted(abort_flag) ||
+            !mbar_wait(&tmem_full[acc], acc_phase, p.timeout_ns, p.status)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t tacc = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(tacc + c * 32, r);
+          tc_wait_ld();
+          const int col0 = n_blk * BN + c * 32;
+          if (Out == kOutF16) {
+            if (col0 < p.N)
+              tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, static_cast<__half*>(p.CD),
+                                     p.bias);
+          } else {
+            // exact FP32 chunk sum -> INT32, added to the running sum
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+            if (ch > 0) {
+              uint32_t s[32];
+              tmem_ld_32cols(sums + c * 32, s);
+              tc_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] += s[i];
+            }
+            if (ch + 1 < num_chunks) {
+              tmem_st_32cols(sums + c * 32, r);
+              tc_wait_st();
+            } else if (col0 < p.N) {
+              store_i32_chunk(r, row, col0, p);
+            }
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&tmem_empty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc<kTmemCols>(tmem_base);
+  }
+}
+
+template <int BN, int Stages, int OpA, int OpB, int Out>
+cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
+  using L = ConvSmem<BN, Stages, OpA, OpB>;
+  CUtensorMap ta, tb;
+  cudaError_t e;
+  if (OpA == kOpF16)
+    e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, kBlockM);
+  else  // int8: rows of K bytes, 64-byte boxes, no swizzle
+    e = tc::make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.M, a.K, a.lda, kBlockM,
+                        kBlockK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  if (OpB == kOpF16)
+    e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, BN);
+  else if (OpB == kOpI8)
+    e = tc::make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.N, a.K, a.ldb, BN, kBlockK,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+  else  // E2M1: rows of ceil(K/2) bytes, pitch ldb/2 bytes, 32-byte boxes
+    e = tc::make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.N, (a.K + 1) / 2, a.ldb / 2,
+                        BN, kBlockK / 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+
+  ConvParams p;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.num_m_blocks = static_cast<int>((a.M + kBlockM - 1) / kBlockM);
+  p.num_n_blocks = static_cast<int>((a.N + BN - 1) / BN);
+  p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+  p.num_k_blocks = static_cast<int>((a.K + kBlockK - 1) / kBlockK);
+  p.group_m = 16;
+  p.epi = Epi{a.alpha, a.beta, a.epi};
+  p.CD = a.C;
+  p.bias = static_cast<const __half*>(a.bias);
+  p.alpha_i = static_cast<int32_t>(a.alpha);
+  p.beta_i = static_cast<int32_t>(a.beta);
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+
+  auto kern = gemm_conv_tc_kernel<BN, Stages, OpA, OpB, Out>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kLaunchBytes);
+  if (e != cudaSuccess) return e;
+  int grid = plan.grid > 0 ? plan.grid : a.sm_count;
+  if (grid > p.num_tiles) grid = p.num_tiles;
+  kern<<<grid, kThreads, L::kLaunchBytes, a.stream>>>(ta, tb, p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Shapes compiled for the converting kernels; the planner proposes only these.
+cudaError_t launch_conv(const GemmArgs& a, const dg_tile_plan& plan) {
+  if (a.dtype_a == DG_I8 && a.dtype_b == DG_I8) {
+    if (plan.n_tile == 128 && plan.stages == 4)
+      return run_conv<128, 4, kOpI8, kOpI8, kOutI32>(a, plan);
+  } else if (a.dtype_a == DG_F16 && a.dtype_b == DG_E2M1) {
+    if (plan.n_tile == 256 && plan.stages == 3)
+      return run_conv<256, 3, kOpF16, kOpE2M1, kOutF16>(a, plan);
+    if (plan.n_tile == 128 && plan.stages == 5)
+      return run_conv<128, 5, kOpF16, kOpE2M1, kOutF16>(a, plan);
+    if (plan.n_tile == 64 && plan.stages == 8)
+      return run_conv<64, 8, kOpF16, kOpE2M1, kOutF16>(a, plan);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace dg

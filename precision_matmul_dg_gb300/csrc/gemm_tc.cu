@@ -29,15 +29,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "epilogue.cuh"
-#include "internal.h"
-#include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace dg {
 namespace {
 
-constexpr int kBlockM = 128;
-constexpr int kBlockK = 64;  // 64 FP16 = 128 bytes: one swizzle row
+using tc::kBlockK;
+using tc::kBlockM;
 constexpr int kThreads = 256;
 constexpr int kEpiWarp0 = 4;
 constexpr int kTileBytesA = kBlockM * kBlockK * 2;
@@ -67,70 +65,7 @@ struct TcSmem {
   static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1 KB
 };
 
-__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& m_blk, int& n_blk) {
-  const int per_group = p.group_m * p.num_n_blocks;
-  const int g = t / per_group;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.num_m_blocks - first_m, p.group_m);
-  const int r = t - g * per_group;
-  m_blk = first_m + r % gm;
-  n_blk = r / gm;
-}
-
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
-
-// Epilogue of one 32-column chunk for this thread's row.
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const uint32_t (&r)[32], int row,
-                                               int col0) {
-  if (row >= p.M) return;
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = p.epi.alpha * __uint_as_float(r[i]);
-  __half* drow = p.CD + static_cast<int64_t>(row) * p.N;
-  const bool full = (col0 + 32 <= p.N) && ((p.N & 7) == 0);
-  if (p.epi.beta != 0.0f) {
-    if (full) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 cv = *reinterpret_cast<const uint4*>(drow + col0 + q * 8);
-        const __half2* ch = reinterpret_cast<const __half2*>(&cv);
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float2 f = __half22float2(ch[h]);
-          v[q * 8 + 2 * h] = fmaf(p.epi.beta, f.x, v[q * 8 + 2 * h]);
-          v[q * 8 + 2 * h + 1] = fmaf(p.epi.beta, f.y, v[q * 8 + 2 * h + 1]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (col0 + i < p.N) v[i] = fmaf(p.epi.beta, __half2float(drow[col0 + i]), v[i]);
-    }
-  }
-  if (p.epi.flags & kEpiBias) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < p.N) v[i] += __half2float(__ldg(p.bias + col0 + i));
-  }
-  if (p.epi.flags & kEpiGelu) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-  }
-  if (full) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 ov;
-      __half2* oh = reinterpret_cast<__half2*>(&ov);
-#pragma unroll
-      for (int h = 0; h < 4; ++h) oh[h] = __floats2half2_rn(v[q * 8 + 2 * h], v[q * 8 + 2 * h + 1]);
-      *reinterpret_cast<uint4*>(drow + col0 + q * 8) = ov;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < p.N) drow[col0 + i] = __float2half_rn(v[i]);
-  }
-}
 
 template <int BN, int Stages>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -191,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int m_blk, n_blk;
-        tile_coords(t, p, m_blk, n_blk);
+        tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (aborted(abort_flag) ||
               !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns, p.status)) {
@@ -276,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int m_blk, n_blk;
-      tile_coords(t, p, m_blk, n_blk);
+      tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
       if (aborted(abort_flag) ||
           !mbar_wait(&tmem_full[acc], acc_phase, p.timeout_ns, p.status)) {
         *abort_flag = 1;
@@ -292,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32cols(tbase + c * 32, r);
         tc_wait_ld();
         const int col0 = n_blk * BN + c * 32;
-        if (col0 < p.N) epilogue_chunk(p, r, row, col0);
+        if (col0 < p.N) tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, p.CD, p.bias);
       }
       tc_fence_before_sync();
       mbar_arrive(&tmem_empty[acc]);
@@ -311,49 +246,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ----------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = []() -> EncodeTiledFn {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<EncodeTiledFn>(f);
-  }();
-  return fn;
-}
-
-// 2-D K-major FP16 operand: `rows` rows of `k` elements, row pitch ld elements,
-// box of box_rows x 64, 128-byte swizzle, zero fill outside.
-cudaError_t make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, int64_t ld,
-                            int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int BN, int Stages>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   using L = TcSmem<BN, Stages>;
   CUtensorMap ta, tb;
-  cudaError_t e = make_kmajor_map(&ta, a.A, a.M, a.K, a.lda, kBlockM);
+  cudaError_t e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, kBlockM);
   if (e != cudaSuccess) return e;
-  e = make_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, BN);
+  e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, BN);
   if (e != cudaSuccess) return e;
 
   TcParams p;

@@ -49,7 +49,8 @@ struct SplitKWorkspace {
 };
 
 // Launchers (gemm_tc.cu, gemv.cu).  Each returns cudaSuccess or the launch error.
-cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);
+cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);    // F16 x F16
+cudaError_t launch_conv(const GemmArgs& a, const dg_tile_plan& plan);  // I8 x I8, F16 x E2M1
 cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws);
 cudaError_t launch_epilogue_only(const GemmArgs& a);
 cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns);

@@ -31,16 +31,47 @@
 namespace dg {
 namespace {
 
-// Shapes of the tcgen05 kernel compiled into gemm_tc.cu: (N_tile, stages).
+// Shapes of the tcgen05 kernels compiled into gemm_tc.cu (FP16 x FP16) and
+// gemm_conv.cu (INT8 x INT8, FP16 x E2M1): (N_tile, stages) per dtype pair.
 struct TcVariant {
   int n_tile, stages;
 };
-constexpr TcVariant kTcVariants[] = {{256, 4}, {128, 6}, {64, 8}};
+constexpr TcVariant kTcVariantsF16[] = {{256, 4}, {128, 6}, {64, 8}};
+constexpr TcVariant kTcVariantsI8[] = {{128, 4}};
+constexpr TcVariant kTcVariantsE2M1[] = {{256, 3}, {128, 5}, {64, 8}};
 constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 256;      // FP16 x FP16 kernel
+constexpr int kConvThreads = 384;    // converting kernel (adds four converter warps)
 constexpr int kTcRegsPerThread = 168;  // upper bound of what ptxas assigns these kernels
 constexpr int kTcBarrierBytes = 512;
+
+struct TcFamily {
+  const TcVariant* v;
+  int n;
+  int threads;
+};
+
+TcFamily tc_family(dg_dtype da, dg_dtype db) {
+  if (da == DG_F16 && db == DG_F16) return {kTcVariantsF16, 3, kTcThreads};
+  if (da == DG_I8 && db == DG_I8) return {kTcVariantsI8, 1, kConvThreads};
+  if (da == DG_F16 && db == DG_E2M1) return {kTcVariantsE2M1, 3, kConvThreads};
+  return {nullptr, 0, 0};
+}
+
+// Shared memory of one stage: FP16 operand tiles (128-byte swizzle) plus the
+// raw int8 / packed-E2M1 tiles the converters widen.
+int tc_stage_bytes(dg_dtype da, dg_dtype db, int n_tile) {
+  int b = kTcBlockM * kTcBlockK * 2 + n_tile * kTcBlockK * 2;
+  if (da == DG_I8) b += kTcBlockM * kTcBlockK;
+  if (db == DG_I8) b += n_tile * kTcBlockK;
+  if (db == DG_E2M1) b += n_tile * kTcBlockK / 2;
+  return b;
+}
+
+// Tensor-memory columns: two FP32 accumulators, plus INT32 running sums on
+// the integer path.
+int tc_tmem_cols(dg_dtype da, int n_tile) { return (da == DG_I8 ? 3 : 2) * n_tile; }
 
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
@@ -51,8 +82,8 @@ constexpr int kGemvMaxSplit = 256;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int tc_smem_bytes(int n_tile, int stages) {
-  return stages * (kTcBlockM * kTcBlockK * 2 + n_tile * kTcBlockK * 2) + kTcBarrierBytes + 1024;
+int tc_smem_bytes(dg_dtype da, dg_dtype db, int n_tile, int stages) {
+  return stages * tc_stage_bytes(da, db, n_tile) + kTcBarrierBytes + 1024;
 }
 
 double sm_rate_flops_per_us(const dg_hw_desc& hw) {
@@ -79,7 +110,8 @@ double tc_tile_efficiency(int n_tile) {
 void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
                        const dg_hw_desc& hw, double target, std::vector<dg_tile_plan>* out,
                        std::string* why) {
-  if (!(da == DG_F16 && db == DG_F16)) {
+  const TcFamily fam = tc_family(da, db);
+  if (!fam.v) {
     if (why) *why += "tensor-core kernel: dtype pair not compiled; ";
     return;
   }
@@ -87,19 +119,23 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     if (why) *why += "tensor-core kernel: needs tcgen05 / tensor memory; ";
     return;
   }
-  const double elem = 2.0;
-  for (const TcVariant& v : kTcVariants) {
-    const int smem = tc_smem_bytes(v.n_tile, v.stages);
+  // bytes per element read from HBM for A and B
+  const double elem_a = da == DG_I8 ? 1.0 : 2.0;
+  const double elem_b = db == DG_I8 ? 1.0 : (db == DG_E2M1 ? 0.5 : 2.0);
+  const double elem_d = da == DG_I8 ? 4.0 : 2.0;
+  for (int vi = 0; vi < fam.n; ++vi) {
+    const TcVariant& v = fam.v[vi];
+    const int smem = tc_smem_bytes(da, db, v.n_tile, v.stages);
     if (smem > hw.smem_per_block_optin) {
       if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": shared memory; ";
       continue;
     }
-    if (2 * v.n_tile > hw.tmem_cols) {
+    if (tc_tmem_cols(da, v.n_tile) > hw.tmem_cols) {
       if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": tensor memory; ";
       continue;
     }
     if (kTcRegsPerThread > hw.regs_per_thread_max ||
-        kTcRegsPerThread * kTcThreads > hw.regs_per_sm) {
+        kTcRegsPerThread * fam.threads > hw.regs_per_sm) {
       if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": registers; ";
       continue;
     }
@@ -112,9 +148,11 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     }
     const int64_t k_pad = ceil_div(K, kTcBlockK) * kTcBlockK;
     const double tile_flops = 2.0 * kTcBlockM * v.n_tile * static_cast<double>(k_pad);
-    const double t_math =
-        waves * tile_flops / (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile));
-    const double bytes = elem * (M * K + N * K) + 2.0 * M * N * 2.0;
+    // Converting kernels also spend shared-memory bandwidth widening operands.
+    const double conv_eff = (da == DG_I8) ? 0.5 : (db == DG_E2M1 ? 0.75 : 1.0);
+    const double t_math = waves * tile_flops /
+                          (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile) * conv_eff);
+    const double bytes = elem_a * M * K + elem_b * N * K + 2.0 * M * N * elem_d;
     const double t_mem = bytes / hbm_bytes_per_us(hw);
     const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
     dg_tile_plan p{};
@@ -127,7 +165,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     p.cta_group = 1;
     p.swap_ab = 0;
     p.smem_bytes = smem;
-    p.threads = kTcThreads;
+    p.threads = fam.threads;
     p.grid = static_cast<int>(std::min<int64_t>(tiles, hw.sm_count));
     p.occupancy = occ;
     p.est_us = std::max(t_math, t_mem) + t_epi + 2.0;
@@ -299,7 +337,8 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
                       dg_dtype dtype_a, dg_dtype dtype_b, std::string* why) {
   (void)N;
   if (plan.kernel == DG_KERNEL_TC) {
-    if (!(dtype_a == DG_F16 && dtype_b == DG_F16)) {
+    const TcFamily fam = tc_family(dtype_a, dtype_b);
+    if (!fam.v) {
       if (why) *why = "tensor-core plan for a dtype pair it does not take";
       return false;
     }
@@ -308,8 +347,8 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
       if (why) *why = "tensor-core plan shape not compiled";
       return false;
     }
-    for (const TcVariant& v : kTcVariants)
-      if (v.n_tile == plan.n_tile && v.stages == plan.stages) return true;
+    for (int vi = 0; vi < fam.n; ++vi)
+      if (fam.v[vi].n_tile == plan.n_tile && fam.v[vi].stages == plan.stages) return true;
     if (why) *why = "tensor-core N_tile/stages pair not compiled";
     return false;
   }

@@ -165,3 +165,101 @@ def test_timeout_is_reported_and_context_survives(dg):
     case = workloads.random_case(256, 256, 256, seed=1)
     got, _ = run_case(dg, case)
     assert_parity(case, got)
+
+
+# ------------------------------------------------------- INT8 (bit-exact)
+@pytest.mark.parametrize("name", ["i8_4096"])
+def test_int8_workload_full_size(dg, name):
+    case = workloads.WORKLOADS[name]()
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+@pytest.mark.parametrize("shape", [(128, 128, 64), (300, 520, 200), (129, 257, 72),
+                                   (1000, 17, 99), (17, 1000, 1030), (256, 384, 2049),
+                                   (640, 768, 4096), (7, 9, 5), (1031, 263, 1)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_int8_random_shapes(dg, shape):
+    M, N, K = shape
+    case = workloads.random_case(M, N, K, "i8", "i8", alpha=3, beta=-2, seed=M + N + K, pad=127)
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+def test_int8_extremes_and_wraparound(dg):
+    K = 4096
+    for a_val, b_val in [(-128, -128), (127, -128), (-128, 127), (127, 127)]:
+        case = workloads.random_case(130, 260, K, "i8", "i8", seed=1)
+        case.A = np.full_like(case.A, a_val)
+        case.B = np.full_like(case.B, b_val)
+        got, _ = run_case(dg, case)
+        assert np.all(got == a_val * b_val * K)
+    # alpha large enough to wrap modulo 2^32
+    case = workloads.random_case(64, 96, 3000, "i8", "i8", alpha=65537, beta=7, seed=2)
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+def test_int8_every_plan(dg):
+    case = workloads.random_case(300, 600, 2500, "i8", "i8", alpha=1, beta=1, seed=3)
+    tc = [p for p in _plans(dg, case) if p["kernel_name"] == "tc"]
+    assert tc
+    for p in tc:
+        for grid in (p["grid"], 3):
+            got, _ = run_case(dg, case, plan=dict(p, grid=grid))
+            assert_parity(case, got)
+
+
+# ------------------------------------------------------- W4A16
+@pytest.mark.parametrize("name", ["w4a16_m16", "w4a16_m2048"])
+def test_w4a16_workload_full_size(dg, name):
+    case = workloads.WORKLOADS[name]()
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+@pytest.mark.parametrize("shape", [(16, 8960, 1536), (300, 520, 200), (129, 257, 71),
+                                   (1000, 17, 99), (5, 1000, 1030), (640, 768, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("epi", ["none", "bias_gelu"])
+def test_w4a16_random_shapes(dg, shape, epi):
+    M, N, K = shape
+    case = workloads.random_case(M, N, K, "f16", "e2m1", epilogue=epi, alpha=0.5, beta=0.25,
+                                 seed=M * 3 + K, pad=255)
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+
+
+def test_w4a16_every_code_one_hot(dg):
+    """Column j of the weights holds code j % 16 at k = j % K and zeros elsewhere,
+    so D[:, j] = A[:, k] * value(code): every code's decoded value appears as a
+    product with an exact fp16 activation (table from the pinned golden file)."""
+    table = {}
+    import os
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "e2m1_codes.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            c, v = line.split()
+            table[int(c)] = float(v)
+    M, N, K = 64, 64, 64
+    case = workloads.random_case(M, N, K, "f16", "e2m1", seed=4)
+    case.A = np.ascontiguousarray(np.round(case.A * 8) / 8).astype(np.float16)
+    packed = np.zeros_like(case.B)
+    for j in range(N):
+        k, code = j % K, j % 16
+        packed[j, k // 2] |= np.uint8(code << (4 * (k % 2)))
+    case.B = packed
+    got, _ = run_case(dg, case)
+    for j in range(N):
+        want = case.A[:, j % K].astype(np.float64) * table[j % 16]
+        assert np.array_equal(got[:, j].astype(np.float64), want), j
+
+
+def test_w4a16_every_plan(dg):
+    case = workloads.random_case(200, 700, 600, "f16", "e2m1", epilogue="bias_gelu", beta=0.5,
+                                 seed=5)
+    tc = [p for p in _plans(dg, case) if p["kernel_name"] == "tc"]
+    assert {p["n_tile"] for p in tc} == {64, 128, 256}
+    for p in tc:
+        got, _ = run_case(dg, case, plan=p)
+        assert_parity(case, got)

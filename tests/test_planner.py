@@ -178,3 +178,33 @@ def test_worked_example_tiles_fit_the_a100_description(dg):
         assert t in got, t
         assert 2 * (t[0] + t[1]) * t[2] * 2 <= smem
     assert all(p["kernel_name"] == "none" for p in plans)  # planning only: no kernel here
+
+
+CONV_VARIANTS = {("i8", "i8"): [(128, 4)], ("f16", "e2m1"): [(256, 3), (128, 5), (64, 8)]}
+
+
+def conv_smem(da, db, n_tile, stages):
+    b = 128 * 64 * 2 + n_tile * 64 * 2
+    if da == "i8":
+        b += 128 * 64
+    if db == "i8":
+        b += n_tile * 64
+    if db == "e2m1":
+        b += n_tile * 32
+    return stages * b + 512 + 1024
+
+
+@pytest.mark.parametrize("pair", sorted(CONV_VARIANTS))
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (16, 8960, 1536), (2048, 8960, 1536),
+                                   (7, 9, 5)])
+def test_converting_kernel_plans(dg, pair, shape):
+    M, N, K = shape
+    plans = dg.plan_tiles(M, N, K, pair[0], pair[1], hw=GB300, target_occupancy=0.0)
+    got = {(p["n_tile"], p["stages"]) for p in plans}
+    assert got == set(CONV_VARIANTS[pair])
+    for p in plans:
+        assert p["kernel_name"] == "tc" and p["threads"] == 384
+        assert p["smem_bytes"] == conv_smem(pair[0], pair[1], p["n_tile"], p["stages"])
+        assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
+        cols = (3 if pair[0] == "i8" else 2) * p["n_tile"]
+        assert cols <= GB300["tmem_cols"]
