@@ -253,14 +253,16 @@ def run_dg(args, world, rank, local):
         sets.append((torch.roll(A0, sh, 0).contiguous(), torch.roll(B0, sh, 0).contiguous(),
                      torch.roll(C0, sh, 0).contiguous(), bias))
     stream = torch.cuda.current_stream(dev)
-    plan = dg.plan_tiles(base.M, base.N, base.K, base.dtype_a, base.dtype_b, base.epilogue)[0]
+    cands = dg.plan_tiles(base.M, base.N, base.K, base.dtype_a, base.dtype_b, base.epilogue)
+    plan = cands[min(args.plan_index, len(cands) - 1)]
+    forced = plan if args.plan_index > 0 else None  # index 0: dg_gemm's own choice
 
     def step(i, ev=None):
         A, B, C, bias = sets[i % nsets]
         if ev is not None:
             ev[0].record(stream)
         dg.gemm(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
-                epilogue=base.epilogue, stream=stream)
+                epilogue=base.epilogue, stream=stream, plan=forced)
         if ev is not None:
             ev[1].record(stream)
 
@@ -468,6 +470,8 @@ def main():
     ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
     ap.add_argument("--workload", default="f16_4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--plan-index", type=int, default=0,
+                    help="run the planner's i-th ranked candidate instead of its first")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -10,20 +10,28 @@
 // a single-thread-issued tcgen05.mma with the accumulator in tensor memory:
 //
 //   warp 0      TMA producer: a ring of `Stages` shared-memory slots, each a
-//               128 x 64 tile of A and a BN x 64 tile of B (128-byte swizzle);
-//   warp 1      MMA issuer: 4 x tcgen05.mma (K = 16 each) per slot into a
-//               128 x BN FP32 accumulator in TMEM; tcgen05.commit frees slots;
+//               128 x 64 tile of A and a B tile (128-byte swizzle);
+//   warp 1      MMA issuer: 4 x tcgen05.mma (K = 16 each) per slot into an
+//               FP32 accumulator in TMEM; tcgen05.commit frees slots;
 //   warp 2      allocates / frees the tensor memory (2 accumulators);
 //   warps 4-7   epilogue: tcgen05.ld of the accumulator (each warp owns 32 of
 //               the 128 TMEM lanes = rows), alpha/beta/bias/GELU in FP32,
 //               FP16 round-to-nearest-even, stored straight to D.
 //
-// The kernel is persistent (one CTA per SM walks the tile list), and the two
-// TMEM accumulators let the epilogue of tile i overlap the main loop of tile
-// i+1.  Out-of-range rows and K columns are zero-filled by TMA; the epilogue
-// masks rows >= M and columns >= N.  Every mbarrier wait is bounded: on a
-// timeout the CTA records it in the status word, drains its own copies and
-// MMAs, frees its tensor memory and exits.
+// CG = 1: one CTA computes a 128 x BN tile.
+// CG = 2: a cluster of two CTAs computes a 256 x BN tile with 256-row MMAs
+//   (cta_group::2).  Each CTA loads its own 128 rows of A and BN/2 rows of B;
+//   the even CTA issues the MMAs, which read both CTAs' shared memory, and its
+//   commits arrive on the barriers of both CTAs.  Every A and B tile is read
+//   from L2 once per pair instead of once per CTA, halving L2->SM traffic per
+//   FLOP, and each SM's shared memory feeds half of the B operand.
+//
+// The kernel is persistent (one CTA / pair per SM / SM pair walks the tile
+// list), and the two TMEM accumulators let the epilogue of tile i overlap the
+// main loop of tile i+1.  Out-of-range rows and K columns are zero-filled by
+// TMA; the epilogue masks rows >= M and columns >= N.  Every mbarrier wait is
+// bounded: on a timeout the CTA records it in the status word, drains its
+// own copies and MMAs, frees its tensor memory and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -51,9 +59,10 @@ struct TcParams {
   uint64_t timeout_ns;
 };
 
-template <int BN, int Stages>
+template <int BN, int Stages, int CG>
 struct TcSmem {
-  static constexpr int kTileBytesB = BN * kBlockK * 2;
+  static constexpr int kRowsB = BN / CG;  // B rows this CTA loads
+  static constexpr int kTileBytesB = kRowsB * kBlockK * 2;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + Stages * kTileBytesA;
   static constexpr int kOffBar = kOffB + Stages * kTileBytesB;
@@ -63,18 +72,20 @@ struct TcSmem {
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
   static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1 KB
+  static_assert(kTileBytesB % 1024 == 0, "B tiles keep 1 KB alignment");
 };
 
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
 
-template <int BN, int Stages>
+template <int BN, int Stages, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using L = TcSmem<BN, Stages>;
+  using L = TcSmem<BN, Stages, CG>;
   constexpr int kTmemCols = 2 * BN;
-  constexpr uint32_t kIdesc = idesc_f16_f32(kBlockM, BN);
-  constexpr uint32_t kStageTx = kTileBytesA + L::kTileBytesB;
+  constexpr int kTileM = kBlockM * CG;  // rows of D per tile
+  constexpr uint32_t kIdesc = idesc_f16_f32(kTileM, BN);
+  constexpr uint32_t kStageTx = CG * (kTileBytesA + L::kTileBytesB);  // both CTAs' bytes
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -92,6 +103,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit0 = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Stages; ++s) {
@@ -100,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], 4 * 32);
+      mbar_init(&tmem_empty[b], CG * 4 * 32);  // every epilogue thread of the pair
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -110,11 +125,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
   }
-  if (warp == 2) tmem_alloc<kTmemCols>(tmem_slot);
+  if (warp == 2) {
+    if (CG == 2)
+      tmem_alloc_pair<kTmemCols>(tmem_slot);
+    else
+      tmem_alloc<kTmemCols>(tmem_slot);
+  }
   tc_fence_before_sync();
   __syncthreads();
+  if (CG == 2) cluster_sync();  // peer barriers initialised before any remote arrive
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  bool ok = true;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -123,21 +145,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = unit0; t < p.num_tiles && ok; t += units) {
         int m_blk, n_blk;
         tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
+        const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBlockM;
+        const int b_row = n_blk * BN + static_cast<int>(rank) * L::kRowsB;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (aborted(abort_flag) ||
               !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], kStageTx);
-          tma_load_2d(&tmap_a, &full_bar[stage], smem_a + stage * kTileBytesA, kb * kBlockK,
-                      m_blk * kBlockM, pol);
-          tma_load_2d(&tmap_b, &full_bar[stage], smem_b + stage * L::kTileBytesB, kb * kBlockK,
-                      n_blk * BN, pol);
+          uint8_t* dst_a = smem_a + stage * kTileBytesA;
+          uint8_t* dst_b = smem_b + stage * L::kTileBytesB;
+          if (CG == 1) {
+            mbar_arrive_expect_tx(&full_bar[stage], kStageTx);
+            tma_load_2d(&tmap_a, &full_bar[stage], dst_a, kb * kBlockK, a_row, pol);
+            tma_load_2d(&tmap_b, &full_bar[stage], dst_b, kb * kBlockK, b_row, pol);
+          } else {
+            // both CTAs' copies complete on the even CTA's full barrier
+            if (leader) mbar_arrive_expect_tx(&full_bar[stage], kStageTx);
+            const uint32_t bar0 = mapa_shared(smem_addr(&full_bar[stage]), 0);
+            tma_load_2d_pair(&tmap_a, bar0, dst_a, kb * kBlockK, a_row, pol);
+            tma_load_2d_pair(&tmap_b, bar0, dst_b, kb * kBlockK, b_row, pol);
+          }
           ++issued;
           if (++stage == Stages) {
             stage = 0;
@@ -147,22 +178,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         *abort_flag = 1;
-        // Let the copies this thread started land before the CTA goes away.
-        const int64_t first = issued > Stages ? issued - Stages : 0;
-        for (int64_t i = first; i < issued; ++i)
-          mbar_wait(&full_bar[i % Stages], static_cast<uint32_t>((i / Stages) & 1), p.timeout_ns,
-                    p.status);
+        if (CG == 1 || leader) {
+          // Let the copies this thread started land before the CTA goes away.
+          const int64_t first = issued > Stages ? issued - Stages : 0;
+          for (int64_t i = first; i < issued; ++i)
+            mbar_wait(&full_bar[i % Stages], static_cast<uint32_t>((i / Stages) & 1),
+                      p.timeout_ns, p.status);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (elect_one_lane()) {
+    if (leader && elect_one_lane()) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = unit0; t < p.num_tiles && ok; t += units) {
         if (aborted(abort_flag) ||
             !mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.timeout_ns, p.status)) {
           ok = false;
@@ -181,17 +213,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = smem_addr(smem_b + stage * L::kTileBytesB);
 #pragma unroll
           for (int k = 0; k < kBlockK / 16; ++k) {
-            tc_mma_f16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), kIdesc,
-                       (kb | k) != 0 ? 1u : 0u);
+            const uint64_t da = smem_desc_sw128(a0 + k * 32), db = smem_desc_sw128(b0 + k * 32);
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            if (CG == 2)
+              tc_mma_f16_pair(d_tmem, da, db, kIdesc, accum);
+            else
+              tc_mma_f16(d_tmem, da, db, kIdesc, accum);
           }
-          tc_commit(&empty_bar[stage]);
+          if (CG == 2)
+            tc_commit_pair_multicast(&empty_bar[stage], 0x3);
+          else
+            tc_commit(&empty_bar[stage]);
           if (++stage == Stages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(&tmem_full[acc]);
+        if (CG == 2)
+          tc_commit_pair_multicast(&tmem_full[acc], 0x3);
+        else
+          tc_commit(&tmem_full[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
@@ -200,25 +242,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         *abort_flag = 1;
         // Wait for the MMAs already issued before the tensor memory is freed.
-        tc_commit(drain_bar);
+        if (CG == 2)
+          tc_commit_pair(drain_bar);
+        else
+          tc_commit(drain_bar);
         mbar_wait(drain_bar, 0, p.timeout_ns, p.status);
       }
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - kEpiWarp0;  // TMEM lanes 32*ew .. 32*ew+31
+    const uint32_t empty0 = CG == 2 ? mapa_shared(smem_addr(&tmem_empty[0]), 0) : 0u;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    for (int t = unit0; t < p.num_tiles; t += units) {
       int m_blk, n_blk;
       tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
       if (aborted(abort_flag) ||
           !mbar_wait(&tmem_full[acc], acc_phase, p.timeout_ns, p.status)) {
         *abort_flag = 1;
+        ok = false;
         break;
       }
       tc_fence_after_sync();
-      const int row = m_blk * kBlockM + ew * 32 + lane;
+      const int row = m_blk * kTileM + static_cast<int>(rank) * kBlockM + ew * 32 + lane;
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -230,7 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (col0 < p.N) tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, p.CD, p.bias);
       }
       tc_fence_before_sync();
-      mbar_arrive(&tmem_empty[acc]);
+      if (CG == 2)
+        mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc * 8));
+      else
+        mbar_arrive(&tmem_empty[acc]);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
@@ -240,44 +290,96 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if (CG == 2) {
+    if (aborted(abort_flag)) {
+      // Copies a peer issued against this pair's barriers may still be in
+      // flight after an abort; give them time to land before the pair exits.
+      if (threadIdx.x == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 100000) sleep_ns(1000);
+      }
+      __syncthreads();
+    }
+    cluster_sync();  // the peer no longer reads this CTA's shared memory or barriers
+  }
   if (warp == 2) {
     tc_fence_after_sync();
-    tmem_dealloc<kTmemCols>(tmem_base);
+    if (CG == 2)
+      tmem_dealloc_pair<kTmemCols>(tmem_base);
+    else
+      tmem_dealloc<kTmemCols>(tmem_base);
   }
 }
 
-template <int BN, int Stages>
+template <int BN, int Stages, int CG>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
-  using L = TcSmem<BN, Stages>;
+  using L = TcSmem<BN, Stages, CG>;
   CUtensorMap ta, tb;
   cudaError_t e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, kBlockM);
   if (e != cudaSuccess) return e;
-  e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, BN);
+  e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, L::kRowsB);
   if (e != cudaSuccess) return e;
 
   TcParams p;
   p.M = static_cast<int>(a.M);
   p.N = static_cast<int>(a.N);
   p.K = static_cast<int>(a.K);
-  p.num_m_blocks = static_cast<int>((a.M + kBlockM - 1) / kBlockM);
+  p.num_m_blocks = static_cast<int>((a.M + kBlockM * CG - 1) / (kBlockM * CG));
   p.num_n_blocks = static_cast<int>((a.N + BN - 1) / BN);
   p.num_tiles = p.num_m_blocks * p.num_n_blocks;
   p.num_k_blocks = static_cast<int>((a.K + kBlockK - 1) / kBlockK);
-  p.group_m = 16;
+  p.group_m = 16 / CG;
   p.epi = Epi{a.alpha, a.beta, a.epi};
   p.CD = static_cast<__half*>(a.C);
   p.bias = static_cast<const __half*>(a.bias);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
 
-  auto kern = gemm_f16_tc_kernel<BN, Stages>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kLaunchBytes);
-  if (e != cudaSuccess) return e;
-  int grid = plan.grid > 0 ? plan.grid : a.sm_count;
-  if (grid > p.num_tiles) grid = p.num_tiles;
-  kern<<<grid, kThreads, L::kLaunchBytes, a.stream>>>(ta, tb, p);
+  auto kern = gemm_f16_tc_kernel<BN, Stages, CG>;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  // One shared-memory opt-in and one co-residency query per variant and device.
+  static uint64_t attr_set = 0;
+  static int max_pairs[64] = {};
+  const uint64_t bit = 1ull << (dev & 63);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kLaunchBytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  cfg.numAttrs = 0;
+  if (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (!(attr_set & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kLaunchBytes);
+    if (e != cudaSuccess) return e;
+    if (CG == 2) {
+      // Pairs that fit at once: a persistent grid must not exceed it.
+      int n = 0;
+      cfg.gridDim = dim3(static_cast<unsigned>(a.sm_count & ~1));
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = a.sm_count / 2;
+      }
+      max_pairs[dev & 63] = n;
+    }
+    attr_set |= bit;
+  }
+  // grid: CTAs (pairs x 2 when CG == 2), never more units than tiles
+  int units = plan.grid > 0 ? plan.grid / CG : a.sm_count / CG;
+  if (CG == 2 && units > max_pairs[dev & 63]) units = max_pairs[dev & 63];
+  if (units > p.num_tiles) units = p.num_tiles;
+  if (units < 1) units = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -285,15 +387,20 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
 // Tile shapes compiled into the library; the planner only proposes these.
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (a.dtype_a != DG_F16 || a.dtype_b != DG_F16) return cudaErrorNotSupported;
+  if (plan.cta_group == 2) {
+    if (plan.n_tile == 256 && plan.stages == 6) return run_tc<256, 6, 2>(a, plan);
+    if (plan.n_tile == 128 && plan.stages == 8) return run_tc<128, 8, 2>(a, plan);
+    return cudaErrorNotSupported;
+  }
   switch (plan.n_tile) {
     case 256:
-      if (plan.stages == 4) return run_tc<256, 4>(a, plan);
+      if (plan.stages == 4) return run_tc<256, 4, 1>(a, plan);
       break;
     case 128:
-      if (plan.stages == 6) return run_tc<128, 6>(a, plan);
+      if (plan.stages == 6) return run_tc<128, 6, 1>(a, plan);
       break;
     case 64:
-      if (plan.stages == 8) return run_tc<64, 8>(a, plan);
+      if (plan.stages == 8) return run_tc<64, 8, 1>(a, plan);
       break;
   }
   return cudaErrorNotSupported;

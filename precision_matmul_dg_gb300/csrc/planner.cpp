@@ -34,11 +34,12 @@ namespace {
 // Shapes of the tcgen05 kernels compiled into gemm_tc.cu (FP16 x FP16) and
 // gemm_conv.cu (INT8 x INT8, FP16 x E2M1): (N_tile, stages) per dtype pair.
 struct TcVariant {
-  int n_tile, stages;
+  int n_tile, stages, cta_group;
 };
-constexpr TcVariant kTcVariantsF16[] = {{256, 4}, {128, 6}, {64, 8}};
-constexpr TcVariant kTcVariantsI8[] = {{128, 4}};
-constexpr TcVariant kTcVariantsE2M1[] = {{256, 3}, {128, 5}, {64, 8}};
+constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1}, {128, 6, 1}, {64, 8, 1}, {256, 6, 2},
+                                        {128, 8, 2}};
+constexpr TcVariant kTcVariantsI8[] = {{128, 4, 1}};
+constexpr TcVariant kTcVariantsE2M1[] = {{256, 3, 1}, {128, 5, 1}, {64, 8, 1}};
 constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;
 constexpr int kTcThreads = 256;      // FP16 x FP16 kernel
@@ -53,16 +54,17 @@ struct TcFamily {
 };
 
 TcFamily tc_family(dg_dtype da, dg_dtype db) {
-  if (da == DG_F16 && db == DG_F16) return {kTcVariantsF16, 3, kTcThreads};
+  if (da == DG_F16 && db == DG_F16) return {kTcVariantsF16, 5, kTcThreads};
   if (da == DG_I8 && db == DG_I8) return {kTcVariantsI8, 1, kConvThreads};
   if (da == DG_F16 && db == DG_E2M1) return {kTcVariantsE2M1, 3, kConvThreads};
   return {nullptr, 0, 0};
 }
 
-// Shared memory of one stage: FP16 operand tiles (128-byte swizzle) plus the
-// raw int8 / packed-E2M1 tiles the converters widen.
-int tc_stage_bytes(dg_dtype da, dg_dtype db, int n_tile) {
-  int b = kTcBlockM * kTcBlockK * 2 + n_tile * kTcBlockK * 2;
+// Shared memory of one stage of one CTA: FP16 operand tiles (128-byte
+// swizzle; a CTA of a pair holds half of the B tile) plus the raw int8 /
+// packed-E2M1 tiles the converters widen.
+int tc_stage_bytes(dg_dtype da, dg_dtype db, int n_tile, int cta_group = 1) {
+  int b = kTcBlockM * kTcBlockK * 2 + (n_tile / cta_group) * kTcBlockK * 2;
   if (da == DG_I8) b += kTcBlockM * kTcBlockK;
   if (db == DG_I8) b += n_tile * kTcBlockK;
   if (db == DG_E2M1) b += n_tile * kTcBlockK / 2;
@@ -82,8 +84,8 @@ constexpr int kGemvMaxSplit = 256;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int tc_smem_bytes(dg_dtype da, dg_dtype db, int n_tile, int stages) {
-  return stages * tc_stage_bytes(da, db, n_tile) + kTcBarrierBytes + 1024;
+int tc_smem_bytes(dg_dtype da, dg_dtype db, int n_tile, int stages, int cta_group) {
+  return stages * tc_stage_bytes(da, db, n_tile, cta_group) + kTcBarrierBytes + 1024;
 }
 
 double sm_rate_flops_per_us(const dg_hw_desc& hw) {
@@ -99,7 +101,8 @@ double hbm_bytes_per_us(const dg_hw_desc& hw) {
 // Fraction of the tensor rate a 128 x N_tile tcgen05 tile sustains: operand
 // bytes read from shared memory per MMA grow relative to the math as N_tile
 // shrinks.  A rough model, not a measurement.
-double tc_tile_efficiency(int n_tile) {
+double tc_tile_efficiency(int n_tile, int cta_group) {
+  if (cta_group == 2) return n_tile == 256 ? 0.97 : 0.90;  // half the operand bytes per FLOP
   switch (n_tile) {
     case 256: return 0.92;
     case 128: return 0.80;
@@ -125,48 +128,55 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
   const double elem_d = da == DG_I8 ? 4.0 : 2.0;
   for (int vi = 0; vi < fam.n; ++vi) {
     const TcVariant& v = fam.v[vi];
-    const int smem = tc_smem_bytes(da, db, v.n_tile, v.stages);
+    const std::string name =
+        "N_tile " + std::to_string(v.n_tile) + (v.cta_group == 2 ? " (CTA pair)" : "");
+    const int smem = tc_smem_bytes(da, db, v.n_tile, v.stages, v.cta_group);
     if (smem > hw.smem_per_block_optin) {
-      if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": shared memory; ";
+      if (why) *why += name + ": shared memory; ";
       continue;
     }
     if (tc_tmem_cols(da, v.n_tile) > hw.tmem_cols) {
-      if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": tensor memory; ";
+      if (why) *why += name + ": tensor memory; ";
       continue;
     }
     if (kTcRegsPerThread > hw.regs_per_thread_max ||
         kTcRegsPerThread * fam.threads > hw.regs_per_sm) {
-      if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": registers; ";
+      if (why) *why += name + ": registers; ";
       continue;
     }
-    const int64_t tiles = ceil_div(M, kTcBlockM) * ceil_div(N, v.n_tile);
-    const int64_t waves = ceil_div(tiles, hw.sm_count);
-    const double occ = static_cast<double>(tiles) / static_cast<double>(waves * hw.sm_count);
+    // A pair works on 256-row tiles with half the SMs as scheduling units.
+    const int tile_m = kTcBlockM * v.cta_group;
+    const int64_t units = std::max(1, hw.sm_count / v.cta_group);
+    const int64_t tiles = ceil_div(M, tile_m) * ceil_div(N, v.n_tile);
+    const int64_t waves = ceil_div(tiles, units);
+    const double occ = static_cast<double>(tiles) / static_cast<double>(waves * units);
     if (occ < target) {
-      if (why) *why += "N_tile " + std::to_string(v.n_tile) + ": occupancy; ";
+      if (why) *why += name + ": occupancy; ";
       continue;
     }
     const int64_t k_pad = ceil_div(K, kTcBlockK) * kTcBlockK;
+    // FLOPs of one tile per SM of its unit
     const double tile_flops = 2.0 * kTcBlockM * v.n_tile * static_cast<double>(k_pad);
     // Converting kernels also spend shared-memory bandwidth widening operands.
     const double conv_eff = (da == DG_I8) ? 0.5 : (db == DG_E2M1 ? 0.75 : 1.0);
-    const double t_math = waves * tile_flops /
-                          (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile) * conv_eff);
+    const double t_math =
+        waves * tile_flops /
+        (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile, v.cta_group) * conv_eff);
     const double bytes = elem_a * M * K + elem_b * N * K + 2.0 * M * N * elem_d;
     const double t_mem = bytes / hbm_bytes_per_us(hw);
     const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
     dg_tile_plan p{};
     p.kernel = DG_KERNEL_TC;
-    p.m_tile = kTcBlockM;
+    p.m_tile = tile_m;
     p.n_tile = v.n_tile;
     p.k_tile = kTcBlockK;
     p.split_k = 1;
     p.stages = v.stages;
-    p.cta_group = 1;
+    p.cta_group = v.cta_group;
     p.swap_ab = 0;
     p.smem_bytes = smem;
     p.threads = fam.threads;
-    p.grid = static_cast<int>(std::min<int64_t>(tiles, hw.sm_count));
+    p.grid = static_cast<int>(std::min<int64_t>(tiles, units) * v.cta_group);
     p.occupancy = occ;
     p.est_us = std::max(t_math, t_mem) + t_epi + 2.0;
     p.est_tflops = 2.0 * M * N * K / (p.est_us * 1e6);
@@ -342,13 +352,16 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
       if (why) *why = "tensor-core plan for a dtype pair it does not take";
       return false;
     }
-    if (plan.m_tile != kTcBlockM || plan.k_tile != kTcBlockK || plan.cta_group != 1 ||
+    if ((plan.cta_group != 1 && plan.cta_group != 2) ||
+        plan.m_tile != kTcBlockM * plan.cta_group || plan.k_tile != kTcBlockK ||
         plan.split_k != 1 || plan.swap_ab != 0) {
       if (why) *why = "tensor-core plan shape not compiled";
       return false;
     }
     for (int vi = 0; vi < fam.n; ++vi)
-      if (fam.v[vi].n_tile == plan.n_tile && fam.v[vi].stages == plan.stages) return true;
+      if (fam.v[vi].n_tile == plan.n_tile && fam.v[vi].stages == plan.stages &&
+          fam.v[vi].cta_group == plan.cta_group)
+        return true;
     if (why) *why = "tensor-core N_tile/stages pair not compiled";
     return false;
   }

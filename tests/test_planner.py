@@ -20,8 +20,9 @@ GB300 = dict(sm_count=152, cc_major=10, cc_minor=3, smem_per_block_optin=232448,
              max_threads_per_sm=2048, tmem_cols=512, l2_bytes=126 * 1024 * 1024,
              hbm_gbps=6800.0, tc_f16_tflops=1900.0, clock_ghz=2.07)
 
-# Compiled tensor-core variants: (N_tile, stages); M_tile 128, K_tile 64, 256 threads.
-TC_VARIANTS = [(256, 4), (128, 6), (64, 8)]
+# Compiled FP16 tensor-core variants: (N_tile, stages, CTAs per tile); M_tile
+# 128 per CTA, K_tile 64, 256 threads.  A CTA pair holds half of B per CTA.
+TC_VARIANTS = [(256, 4, 1), (128, 6, 1), (64, 8, 1), (256, 6, 2), (128, 8, 2)]
 
 
 @pytest.fixture(scope="module")
@@ -32,24 +33,25 @@ def dg():
     return dg
 
 
-def tc_smem(n_tile, stages):
-    return stages * (128 * 64 * 2 + n_tile * 64 * 2) + 512 + 1024
+def tc_smem(n_tile, stages, cg=1):
+    return stages * (128 * 64 * 2 + (n_tile // cg) * 64 * 2) + 512 + 1024
 
 
 def tc_feasible(M, N, hw, target):
     out = set()
-    for n_tile, stages in TC_VARIANTS:
-        if tc_smem(n_tile, stages) > hw["smem_per_block_optin"]:
+    for n_tile, stages, cg in TC_VARIANTS:
+        if tc_smem(n_tile, stages, cg) > hw["smem_per_block_optin"]:
             continue
         if 2 * n_tile > hw["tmem_cols"]:
             continue
         if 256 * 168 > hw["regs_per_sm"]:
             continue
-        tiles = math.ceil(M / 128) * math.ceil(N / n_tile)
-        waves = math.ceil(tiles / hw["sm_count"])
-        if tiles / (waves * hw["sm_count"]) < target:
+        units = hw["sm_count"] // cg
+        tiles = math.ceil(M / (128 * cg)) * math.ceil(N / n_tile)
+        waves = math.ceil(tiles / units)
+        if tiles / (waves * units) < target:
             continue
-        out.add(("tc", n_tile, stages, 1))
+        out.add(("tc", n_tile, stages, cg))
     return out
 
 
@@ -91,14 +93,15 @@ def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
     for p in plans:
         assert p["occupancy"] >= target - 1e-12
         if p["kernel_name"] == "tc":
-            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"])
+            cg = p["cta_group"]
+            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], cg)
             assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
             assert 2 * p["n_tile"] <= GB300["tmem_cols"]
             assert p["threads"] * 168 <= GB300["regs_per_sm"]
-            tiles = math.ceil(M / 128) * math.ceil(N / p["n_tile"])
-            assert p["grid"] == min(tiles, GB300["sm_count"])
-            assert p["m_tile"] == 128 and p["k_tile"] == 64 and p["split_k"] == 1
-            got.add(("tc", p["n_tile"], p["stages"], 1))
+            tiles = math.ceil(M / (128 * cg)) * math.ceil(N / p["n_tile"])
+            assert p["grid"] == cg * min(tiles, GB300["sm_count"] // cg)
+            assert p["m_tile"] == 128 * cg and p["k_tile"] == 64 and p["split_k"] == 1
+            got.add(("tc", p["n_tile"], p["stages"], cg))
         else:
             assert p["kernel_name"] == "gemv"
             assert p["k_tile"] % 256 == 0
@@ -117,12 +120,13 @@ def test_resources_prune(dg):
         dg.plan_tiles(4096, 4096, 4096, hw=tiny)
     assert ei.value.name == "DG_ERR_NO_VALID_CANDIDATE"
     # every compiled variant needs tc_smem(...) bytes; one byte less prunes it
-    for n, s in TC_VARIANTS:
-        tight = dict(GB300, smem_per_block_optin=tc_smem(n, s) - 1)
-        got = {p["n_tile"] for p in dg.plan_tiles(4096, 4096, 4096, hw=tight)
-               if p["kernel_name"] == "tc"} if any(
-            tc_smem(n2, s2) < tc_smem(n, s) for n2, s2 in TC_VARIANTS) else set()
-        assert n not in got
+    for n, s, cg in TC_VARIANTS:
+        tight = dict(GB300, smem_per_block_optin=tc_smem(n, s, cg) - 1)
+        try:
+            plans = dg.plan_tiles(4096, 4096, 4096, hw=tight)
+        except dg.DgError:
+            plans = []
+        assert (n, s, cg) not in {(p["n_tile"], p["stages"], p["cta_group"]) for p in plans}
     small_tmem = dict(GB300, tmem_cols=256)
     assert {p["n_tile"] for p in dg.plan_tiles(4096, 4096, 4096, hw=small_tmem)} == {64, 128}
 
