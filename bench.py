@@ -257,39 +257,67 @@ def run_dg(args, world, rank, local):
     plan = cands[min(args.plan_index, len(cands) - 1)]
     forced = plan if args.plan_index > 0 else None  # index 0: dg_gemm's own choice
 
-    def step(i, ev=None):
+    def step(i, ev=None, st=None):
+        st = st or stream
         A, B, C, bias = sets[i % nsets]
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(st)
         dg.gemm(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
-                epilogue=base.epilogue, stream=stream, plan=forced)
+                epilogue=base.epilogue, stream=st, plan=forced)
         if ev is not None:
-            ev[1].record(stream)
+            ev[1].record(st)
 
     for i in range(args.warmup):
         step(i)
     dg.check_status(stream)
     torch.cuda.synchronize(dev)
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
-    launches0 = dg.launch_count()
+    graph = None
+    if args.graph:
+        # The K timed steps captured once and replayed as one graph: the
+        # launches run back to back with no host work between them.  Warm up
+        # on the capture stream first: a split-K plan allocates its
+        # per-stream workspace on first use, which must not happen mid-capture.
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        for i in range(args.warmup):
+            step(i, st=cap)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        launches0 = dg.launch_count()
+        with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+            for i in range(args.steps):
+                step(i, st=cap)
+        launches = dg.launch_count() - launches0
+        graph.replay()  # one untimed replay
+        torch.cuda.synchronize(dev)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        launches0 = dg.launch_count()
     barrier(world)
     torch.cuda.synchronize(dev)
     with sampler:
         t0.record(stream)
-        for i in range(args.steps):
-            step(i, evs[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                step(i, evs[i])
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
-    launches = dg.launch_count() - launches0
+    if graph is None:
+        launches = dg.launch_count() - launches0
     dg.check_status(stream)
     total_ms = t0.elapsed_time(t1)
-    kern_ms = [a.elapsed_time(b) for a, b in evs]
-    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    if graph is None:
+        kern_ms = [a.elapsed_time(b) for a, b in evs]
+        kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    else:
+        kern_avg_ms = total_ms / args.steps  # back-to-back launches inside the graph
 
     total_ms_max = max_over_ranks(total_ms, world)
     # Throughput unit: TFLOP/s (TOPS for INT8) for tensor-bound workloads,
@@ -371,6 +399,8 @@ def run_dg(args, world, rank, local):
         "data": "synthetic (seeded, recipe in workloads.py)",
         "config": {"workload": desc, "name": name, "M": base.M, "N": base.N, "K": base.K,
                    "alpha": base.alpha, "beta": base.beta, "epilogue": base.epilogue,
+                   "timing": ("CUDA-graph replay of the K steps, per-launch = total / K"
+                              if args.graph else "eager launches, CUDA events per launch"),
                    "l2": "%d rotating input sets, %.0f MB > L2" % (nsets, nsets * set_bytes / 1e6)
                    if nsets > 1 else "inputs larger than L2",
                    "parallelism": "replicas" if world > 1 else "1 GPU",
@@ -472,6 +502,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--plan-index", type=int, default=0,
                     help="run the planner's i-th ranked candidate instead of its first")
+    ap.add_argument("--graph", action="store_true",
+                    help="time one CUDA-graph replay of the K steps (no host work between "
+                         "launches); per-launch time = total / K")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

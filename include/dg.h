@@ -140,7 +140,10 @@ dg_status dg_plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dt
  * epilogue, integral alpha and beta, wrap-around modulo 2^32).
  * M == 0 or N == 0 is a no-op; K == 0 gives epilogue(beta * C).
  * May grow a per-(device, stream) split-K workspace the first time a shape
- * needs it (cudaMalloc; libdg owns it until dg_shutdown). */
+ * needs it (cudaMalloc; libdg owns it until dg_shutdown).  Under CUDA-graph
+ * capture, make one call of the same shape on the capturing stream before
+ * capture begins (or use dg_gemm_thin_noalloc), so no allocation happens
+ * while capturing. */
 dg_status dg_gemm(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
                   const void *A, int64_t lda, const void *B, int64_t ldb, void *C,
                   const void *bias, float alpha, float beta, dg_epilogue epilogue,

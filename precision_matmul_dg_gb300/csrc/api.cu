@@ -278,7 +278,8 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
       g_plans[key] = plan;
     }
   }
-  if (getenv("DG_LOG")) {
+  static const bool log_plans = getenv("DG_LOG") != nullptr;
+  if (log_plans) {
     fprintf(stderr,
             "[dg] M=%lld N=%lld K=%lld kernel=%d tile=%dx%dx%d split_k=%d stages=%d grid=%d "
             "est=%.2fus\n",

@@ -13,13 +13,18 @@
 // legacy mma.sync s8 path is slow, so both contractions run on the FP16
 // tensor-core path with the narrow operand widened in shared memory:
 //
-//   warp 0       TMA producer: raw int8 / packed-E2M1 tiles (no swizzle) and
-//                FP16 tiles (128-byte swizzle) into a ring of `Stages` slots;
+//   warp 0       TMA producer into a deep input ring (`SIn` slots): raw int8
+//                / packed-E2M1 tiles (no swizzle) and FP16 A tiles (128-byte
+//                swizzle);
 //   warps 8-11   converters: raw -> FP16 in the swizzled K-major layout the
-//                MMA reads (int8: exact via the 1024+u magic-number trick;
-//                E2M1: cvt.rn.f16x2.e2m1x2, exact), then a proxy fence;
-//   warp 1       MMA issuer: tcgen05.mma kind::f16 into TMEM (FP32);
+//                MMA reads, into a short converted ring (`SCv` slots) (int8:
+//                exact via the 1024+u magic-number trick; E2M1:
+//                cvt.rn.f16x2.e2m1x2, exact), then a proxy fence;
+//   warp 1       MMA issuer: tcgen05.mma kind::f16 into TMEM (FP32); its
+//                commits free both the input and the converted slot;
 //   warp 2       TMEM allocation;  warps 4-7  epilogue.
+// The input ring is deep because it must cover the TMA latency; the wide
+// converted tiles need only cover the conversion latency.
 //
 // INT8 exactness: every product is an integer of magnitude <= 2^14, so any
 // partial sum of at most 1024 products is an integer of magnitude <= 2^24 and
@@ -59,28 +64,31 @@ struct ConvParams {
   int32_t alpha_i, beta_i;
   int* status;
   uint64_t timeout_ns;
+  uint32_t stage_tx;  // bytes TMA delivers per input slot
 };
 
-template <int BN, int Stages, int OpA, int OpB>
+template <int BN, int SIn, int SCv, int OpA, int OpB>
 struct ConvSmem {
-  static constexpr int kOpA = kBlockM * kBlockK * 2;
-  static constexpr int kOpB = BN * kBlockK * 2;
-  static constexpr int kRawA = OpA == kOpI8 ? kBlockM * kBlockK : 0;
-  static constexpr int kRawB = OpB == kOpI8 ? BN * kBlockK : (OpB == kOpE2M1 ? BN * kBlockK / 2 : 0);
-  static constexpr int kOffOpA = 0;
-  static constexpr int kOffOpB = kOffOpA + Stages * kOpA;
-  static constexpr int kOffRawA = kOffOpB + Stages * kOpB;
-  static constexpr int kOffRawB = kOffRawA + Stages * kRawA;
-  static constexpr int kOffBar = kOffRawB + Stages * kRawB;
-  // full[S], conv[S], empty[S], tmem_full[2], tmem_empty[2], drain
-  static constexpr int kNumBars = 3 * Stages + 5;
+  // input slot: A as loaded (FP16 tile or raw int8), B raw
+  static constexpr int kInA = OpA == kOpF16 ? kBlockM * kBlockK * 2 : kBlockM * kBlockK;
+  static constexpr int kInB = OpB == kOpI8 ? BN * kBlockK : BN * kBlockK / 2;
+  // converted slot: widened A (when A is not FP16) and widened B
+  static constexpr int kCvA = OpA == kOpF16 ? 0 : kBlockM * kBlockK * 2;
+  static constexpr int kCvB = BN * kBlockK * 2;
+  static constexpr int kOffInA = 0;
+  static constexpr int kOffInB = kOffInA + SIn * kInA;
+  static constexpr int kOffCvA = kOffInB + SIn * kInB;
+  static constexpr int kOffCvB = kOffCvA + SCv * kCvA;
+  static constexpr int kOffBar = kOffCvB + SCv * kCvB;
+  // in_full[SIn], in_empty[SIn], cv_full[SCv], cv_empty[SCv], tmem_full[2], tmem_empty[2], drain
+  static constexpr int kNumBars = 2 * SIn + 2 * SCv + 5;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
   static constexpr int kLaunchBytes = kBytes + 1024;
-  // bytes TMA delivers per stage
-  static constexpr uint32_t kTx = (OpA == kOpF16 ? kOpA : kRawA) + (OpB == kOpF16 ? kOpB : kRawB);
-  static_assert(kRawA % 1024 == 0 && kRawB % 1024 == 0, "raw tiles keep 1 KB alignment");
+  static_assert(kInA % 1024 == 0 && kInB % 1024 == 0 && kCvA % 1024 == 0 && kCvB % 1024 == 0,
+                "tiles keep 1 KB alignment");
+  static_assert(kLaunchBytes <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
@@ -122,23 +130,30 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// Widen one stage's raw tile of `rows` rows into the FP16 operand tile.
+// Widen one slot's raw tile of `Rows` rows into the FP16 operand tile.
+// Thread ct owns output chunk c = ct % 8 of rows ct / 8 + 16 i: its chunk and
+// swizzle phase (row % 8) are the same in every iteration, so each step is
+// one load, the conversion and one store at fixed strides.
 template <int Op, int Rows>
 __device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* op, int ct) {
-  constexpr int kUnits = Rows * 8;  // 16-byte output chunks
-#pragma unroll 4
-  for (int u = ct; u < kUnits; u += kConvThreads) {
-    const int r = u >> 3, c = u & 7;
+  constexpr int kRowsPerStep = kConvThreads / 8;  // 16
+  constexpr int kRawRow = Op == kOpI8 ? 64 : 32;  // raw bytes per row
+  constexpr int kRawChunk = Op == kOpI8 ? 8 : 4;  // raw bytes per output chunk
+  const int r0 = ct >> 3, c = ct & 7;
+  const uint8_t* src = raw + r0 * kRawRow + c * kRawChunk;
+  uint8_t* dst = op + sw128_offset(r0, c);  // (r0 + 16 i) % 8 == r0 % 8
+#pragma unroll
+  for (int i = 0; i < Rows / kRowsPerStep; ++i) {
     uint4 o;
     if (Op == kOpI8) {
-      const uint2 w = *reinterpret_cast<const uint2*>(raw + r * 64 + c * 8);
+      const uint2 w = *reinterpret_cast<const uint2*>(src + i * kRowsPerStep * kRawRow);
       i8x4_to_f16x4(w.x, o.x, o.y);
       i8x4_to_f16x4(w.y, o.z, o.w);
     } else {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + r * 32 + c * 4);
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(src + i * kRowsPerStep * kRawRow);
       o = e2m1x8_to_f16x8(w);
     }
-    *reinterpret_cast<uint4*>(op + sw128_offset(r, c)) = o;
+    *reinterpret_cast<uint4*>(dst + i * kRowsPerStep * 128) = o;
   }
 }
 
@@ -189,13 +204,31 @@ __device__ __forceinline__ void store_i32_chunk(const uint32_t (&s)[32], int row
   }
 }
 
-template <int BN, int Stages, int OpA, int OpB, int Out>
+// Position in the two rings of the i-th K block this CTA processes.
+struct RingPos {
+  int in, cv;
+  uint32_t in_phase, cv_phase;
+  __device__ __forceinline__ RingPos() : in(0), cv(0), in_phase(0), cv_phase(0) {}
+  template <int SIn, int SCv>
+  __device__ __forceinline__ void advance() {
+    if (++in == SIn) {
+      in = 0;
+      in_phase ^= 1;
+    }
+    if (++cv == SCv) {
+      cv = 0;
+      cv_phase ^= 1;
+    }
+  }
+};
+
+template <int BN, int SIn, int SCv, int OpA, int OpB, int Out>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_conv_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const ConvParams p) {
-  using L = ConvSmem<BN, Stages, OpA, OpB>;
+  using L = ConvSmem<BN, SIn, SCv, OpA, OpB>;
   constexpr bool kConvA = OpA != kOpF16;
-  constexpr bool kConvB = OpB != kOpF16;
+  static_assert(OpB != kOpF16, "B is always the widened operand here");
   // FP32 accumulators x2, plus the INT32 running sums on the integer path.
   constexpr int kColsNeeded = Out == kOutI32 ? 3 * BN : 2 * BN;
   constexpr int kTmemCols = kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512);
@@ -206,12 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-  uint64_t* full_bar = bars;
-  uint64_t* conv_bar = bars + Stages;
-  uint64_t* empty_bar = bars + 2 * Stages;
-  uint64_t* tmem_full = bars + 3 * Stages;
-  uint64_t* tmem_empty = bars + 3 * Stages + 2;
-  uint64_t* drain_bar = bars + 3 * Stages + 4;
+  uint64_t* in_full = bars;
+  uint64_t* in_empty = bars + SIn;
+  uint64_t* cv_full = bars + 2 * SIn;
+  uint64_t* cv_empty = bars + 2 * SIn + SCv;
+  uint64_t* tmem_full = bars + 2 * SIn + 2 * SCv;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* drain_bar = tmem_full + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
 
@@ -222,10 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_chunks = (p.num_k_blocks + chunk_kb - 1) / chunk_kb;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Stages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&conv_bar[s], kConvThreads);
-      mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < SIn; ++s) {
+      mbar_init(&in_full[s], 1);
+      mbar_init(&in_empty[s], 1);
+    }
+    for (int s = 0; s < SCv; ++s) {
+      mbar_init(&cv_full[s], kConvThreads);
+      mbar_init(&cv_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
@@ -258,28 +295,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (aborted(abort_flag) ||
-              !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns, p.status)) {
+              !mbar_wait(&in_empty[stage], phase ^ 1, p.timeout_ns, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], L::kTx);
-          if (OpA == kOpF16)
-            tma_load_2d(&tmap_a, &full_bar[stage], smem + L::kOffOpA + stage * L::kOpA,
-                        kb * kBlockK, m_blk * kBlockM, pol);
-          else
-            tma_load_2d(&tmap_a, &full_bar[stage], smem + L::kOffRawA + stage * L::kRawA,
-                        kb * kBlockK, m_blk * kBlockM, pol);
-          if (OpB == kOpF16)
-            tma_load_2d(&tmap_b, &full_bar[stage], smem + L::kOffOpB + stage * L::kOpB,
-                        kb * kBlockK, n_blk * BN, pol);
-          else if (OpB == kOpI8)
-            tma_load_2d(&tmap_b, &full_bar[stage], smem + L::kOffRawB + stage * L::kRawB,
-                        kb * kBlockK, n_blk * BN, pol);
-          else  // packed E2M1: 64 codes = 32 bytes per row
-            tma_load_2d(&tmap_b, &full_bar[stage], smem + L::kOffRawB + stage * L::kRawB,
-                        kb * (kBlockK / 2), n_blk * BN, pol);
+          mbar_arrive_expect_tx(&in_full[stage], p.stage_tx);
+          tma_load_2d(&tmap_a, &in_full[stage], smem + L::kOffInA + stage * L::kInA,
+                      kb * kBlockK, m_blk * kBlockM, pol);
+          // int8 rows carry 64 bytes per K block, packed E2M1 rows 32
+          tma_load_2d(&tmap_b, &in_full[stage], smem + L::kOffInB + stage * L::kInB,
+                      OpB == kOpI8 ? kb * kBlockK : kb * (kBlockK / 2), n_blk * BN, pol);
           ++issued;
-          if (++stage == Stages) {
+          if (++stage == SIn) {
             stage = 0;
             phase ^= 1;
           }
@@ -287,44 +314,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         *abort_flag = 1;
-        const int64_t first = issued > Stages ? issued - Stages : 0;
+        const int64_t first = issued > SIn ? issued - SIn : 0;
         for (int64_t i = first; i < issued; ++i)
-          mbar_wait(&full_bar[i % Stages], static_cast<uint32_t>((i / Stages) & 1), p.timeout_ns,
+          mbar_wait(&in_full[i % SIn], static_cast<uint32_t>((i / SIn) & 1), p.timeout_ns,
                     p.status);
       }
     }
   } else if (warp >= kConvWarp0) {
     // ------------------------------------------------------------ converters
     const int ct = threadIdx.x - kConvWarp0 * 32;
-    int stage = 0;
-    uint32_t phase = 0;
+    RingPos pos;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-        if (aborted(abort_flag) || !mbar_wait(&full_bar[stage], phase, p.timeout_ns, p.status)) {
+        if (aborted(abort_flag) ||
+            !mbar_wait(&in_full[pos.in], pos.in_phase, p.timeout_ns, p.status) ||
+            !mbar_wait(&cv_empty[pos.cv], pos.cv_phase ^ 1, p.timeout_ns, p.status)) {
           *abort_flag = 1;
           ok = false;
           break;
         }
         if (kConvA)
-          convert_tile<OpA, kBlockM>(smem + L::kOffRawA + stage * L::kRawA,
-                                     smem + L::kOffOpA + stage * L::kOpA, ct);
-        if (kConvB)
-          convert_tile<OpB, BN>(smem + L::kOffRawB + stage * L::kRawB,
-                                smem + L::kOffOpB + stage * L::kOpB, ct);
+          convert_tile<OpA, kBlockM>(smem + L::kOffInA + pos.in * L::kInA,
+                                     smem + L::kOffCvA + pos.cv * L::kCvA, ct);
+        convert_tile<OpB, BN>(smem + L::kOffInB + pos.in * L::kInB,
+                              smem + L::kOffCvB + pos.cv * L::kCvB, ct);
         fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-        mbar_arrive(&conv_bar[stage]);
-        if (++stage == Stages) {
-          stage = 0;
-          phase ^= 1;
-        }
+        mbar_arrive(&cv_full[pos.cv]);
+        pos.advance<SIn, SCv>();
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_lane()) {
-      int stage = 0;
-      uint32_t phase = 0;
+      RingPos pos;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -340,24 +363,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb0 = ch * chunk_kb;
           const int kb1 = min(p.num_k_blocks, kb0 + chunk_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
-            uint64_t* ready = (kConvA || kConvB) ? &conv_bar[stage] : &full_bar[stage];
-            if (aborted(abort_flag) || !mbar_wait(ready, phase, p.timeout_ns, p.status)) {
+            if (aborted(abort_flag) ||
+                !mbar_wait(&in_full[pos.in], pos.in_phase, p.timeout_ns, p.status) ||
+                !mbar_wait(&cv_full[pos.cv], pos.cv_phase, p.timeout_ns, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
-            const uint32_t a0 = smem_addr(smem + L::kOffOpA + stage * L::kOpA);
-            const uint32_t b0 = smem_addr(smem + L::kOffOpB + stage * L::kOpB);
+            const uint32_t a0 = smem_addr(kConvA ? smem + L::kOffCvA + pos.cv * L::kCvA
+                                                 : smem + L::kOffInA + pos.in * L::kInA);
+            const uint32_t b0 = smem_addr(smem + L::kOffCvB + pos.cv * L::kCvB);
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
               tc_mma_f16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32),
                          kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
             }
-            tc_commit(&empty_bar[stage]);
-            if (++stage == Stages) {
-              stage = 0;
-              phase ^= 1;
-            }
+            tc_commit(&in_empty[pos.in]);
+            tc_commit(&cv_empty[pos.cv]);
+            pos.advance<SIn, SCv>();
           }
           if (!ok) break;
           tc_commit(&tmem_full[acc]);
@@ -387,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = m_blk * kBlockM + ew * 32 + lane;
       for (int ch = 0; ch < num_chunks; ++ch) {
         if (aborted(abort_flag) ||
-            !mbar_wait(&tmem_full[acc], acc_phase, p.timeout_ns, p.status)) {
+            !mbar_wait_sleepy(&tmem_full[acc], acc_phase, p.timeout_ns, p.status, 256)) {
           *abort_flag = 1;
           ok = false;
           break;
@@ -442,20 +465,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int Stages, int OpA, int OpB, int Out>
+template <int BN, int SIn, int SCv, int OpA, int OpB, int Out>
 cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
-  using L = ConvSmem<BN, Stages, OpA, OpB>;
+  using L = ConvSmem<BN, SIn, SCv, OpA, OpB>;
+  // Fewer than 128 rows: load only those rows (rounded up to 8); the stale
+  // shared-memory rows below only feed accumulator rows >= M.
+  const int box_a = a.M < kBlockM ? static_cast<int>((a.M + 7) / 8 * 8) : kBlockM;
   CUtensorMap ta, tb;
   cudaError_t e;
   if (OpA == kOpF16)
-    e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, kBlockM);
+    e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, box_a);
   else  // int8: rows of K bytes, 64-byte boxes, no swizzle
-    e = tc::make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.M, a.K, a.lda, kBlockM,
-                        kBlockK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    e = tc::make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.M, a.K, a.lda, box_a, kBlockK,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  if (OpB == kOpF16)
-    e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, BN);
-  else if (OpB == kOpI8)
+  if (OpB == kOpI8)
     e = tc::make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.N, a.K, a.ldb, BN, kBlockK,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
   else  // E2M1: rows of ceil(K/2) bytes, pitch ldb/2 bytes, 32-byte boxes
@@ -479,10 +503,17 @@ cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
   p.beta_i = static_cast<int32_t>(a.beta);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
+  p.stage_tx = static_cast<uint32_t>(box_a * (OpA == kOpF16 ? kBlockK * 2 : kBlockK) + L::kInB);
 
-  auto kern = gemm_conv_tc_kernel<BN, Stages, OpA, OpB, Out>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kLaunchBytes);
-  if (e != cudaSuccess) return e;
+  auto kern = gemm_conv_tc_kernel<BN, SIn, SCv, OpA, OpB, Out>;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static uint64_t attr_set = 0;  // one shared-memory opt-in per variant and device
+  if (!(attr_set & (1ull << (dev & 63)))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kLaunchBytes);
+    if (e != cudaSuccess) return e;
+    attr_set |= 1ull << (dev & 63);
+  }
   int grid = plan.grid > 0 ? plan.grid : a.sm_count;
   if (grid > p.num_tiles) grid = p.num_tiles;
   kern<<<grid, kThreads, L::kLaunchBytes, a.stream>>>(ta, tb, p);
@@ -493,17 +524,18 @@ cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
 }  // namespace
 
 // Shapes compiled for the converting kernels; the planner proposes only these.
+// (N_tile, input slots, converted slots) per dtype pair.
 cudaError_t launch_conv(const GemmArgs& a, const dg_tile_plan& plan) {
   if (a.dtype_a == DG_I8 && a.dtype_b == DG_I8) {
-    if (plan.n_tile == 128 && plan.stages == 4)
-      return run_conv<128, 4, kOpI8, kOpI8, kOutI32>(a, plan);
+    if (plan.n_tile == 128 && plan.stages == 8)
+      return run_conv<128, 8, 3, kOpI8, kOpI8, kOutI32>(a, plan);
   } else if (a.dtype_a == DG_F16 && a.dtype_b == DG_E2M1) {
-    if (plan.n_tile == 256 && plan.stages == 3)
-      return run_conv<256, 3, kOpF16, kOpE2M1, kOutF16>(a, plan);
-    if (plan.n_tile == 128 && plan.stages == 5)
-      return run_conv<128, 5, kOpF16, kOpE2M1, kOutF16>(a, plan);
+    if (plan.n_tile == 256 && plan.stages == 6)
+      return run_conv<256, 6, 2, kOpF16, kOpE2M1, kOutF16>(a, plan);
+    if (plan.n_tile == 128 && plan.stages == 8)
+      return run_conv<128, 8, 3, kOpF16, kOpE2M1, kOutF16>(a, plan);
     if (plan.n_tile == 64 && plan.stages == 8)
-      return run_conv<64, 8, kOpF16, kOpE2M1, kOutF16>(a, plan);
+      return run_conv<64, 8, 4, kOpF16, kOpE2M1, kOutF16>(a, plan);
   }
   return cudaErrorNotSupported;
 }

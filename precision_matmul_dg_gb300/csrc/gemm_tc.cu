@@ -57,6 +57,7 @@ struct TcParams {
   const __half* bias;
   int* status;
   uint64_t timeout_ns;
+  uint32_t stage_tx;  // bytes TMA delivers per stage (both CTAs of a pair)
 };
 
 template <int BN, int Stages, int CG>
@@ -85,7 +86,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kTmemCols = 2 * BN;
   constexpr int kTileM = kBlockM * CG;  // rows of D per tile
   constexpr uint32_t kIdesc = idesc_f16_f32(kTileM, BN);
-  constexpr uint32_t kStageTx = CG * (kTileBytesA + L::kTileBytesB);  // both CTAs' bytes
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -159,12 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst_a = smem_a + stage * kTileBytesA;
           uint8_t* dst_b = smem_b + stage * L::kTileBytesB;
           if (CG == 1) {
-            mbar_arrive_expect_tx(&full_bar[stage], kStageTx);
+            mbar_arrive_expect_tx(&full_bar[stage], p.stage_tx);
             tma_load_2d(&tmap_a, &full_bar[stage], dst_a, kb * kBlockK, a_row, pol);
             tma_load_2d(&tmap_b, &full_bar[stage], dst_b, kb * kBlockK, b_row, pol);
           } else {
             // both CTAs' copies complete on the even CTA's full barrier
-            if (leader) mbar_arrive_expect_tx(&full_bar[stage], kStageTx);
+            if (leader) mbar_arrive_expect_tx(&full_bar[stage], p.stage_tx);
             const uint32_t bar0 = mapa_shared(smem_addr(&full_bar[stage]), 0);
             tma_load_2d_pair(&tmap_a, bar0, dst_a, kb * kBlockK, a_row, pol);
             tma_load_2d_pair(&tmap_b, bar0, dst_b, kb * kBlockK, b_row, pol);
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int m_blk, n_blk;
       tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
       if (aborted(abort_flag) ||
-          !mbar_wait(&tmem_full[acc], acc_phase, p.timeout_ns, p.status)) {
+          !mbar_wait_sleepy(&tmem_full[acc], acc_phase, p.timeout_ns, p.status, 256)) {
         *abort_flag = 1;
         ok = false;
         break;
@@ -315,7 +315,12 @@ template <int BN, int Stages, int CG>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   using L = TcSmem<BN, Stages, CG>;
   CUtensorMap ta, tb;
-  cudaError_t e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, kBlockM);
+  // A problem with fewer than 128 rows loads only its rows (rounded up to a
+  // swizzle atom of 8): TMA is slow on boxes that are mostly out of bounds,
+  // and the stale shared-memory rows below only feed accumulator rows >= M,
+  // which the epilogue never stores.
+  const int box_a = (CG == 1 && a.M < kBlockM) ? static_cast<int>((a.M + 7) / 8 * 8) : kBlockM;
+  cudaError_t e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, box_a);
   if (e != cudaSuccess) return e;
   e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, L::kRowsB);
   if (e != cudaSuccess) return e;
@@ -334,6 +339,7 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.bias = static_cast<const __half*>(a.bias);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
+  p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB));
 
   auto kern = gemm_f16_tc_kernel<BN, Stages, CG>;
   int dev = 0;

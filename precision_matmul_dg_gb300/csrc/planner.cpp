@@ -33,13 +33,15 @@ namespace {
 
 // Shapes of the tcgen05 kernels compiled into gemm_tc.cu (FP16 x FP16) and
 // gemm_conv.cu (INT8 x INT8, FP16 x E2M1): (N_tile, stages) per dtype pair.
+// `stages` is the TMA ring depth; the converting kernel adds a ring of
+// `cv_stages` widened-operand slots.
 struct TcVariant {
-  int n_tile, stages, cta_group;
+  int n_tile, stages, cta_group, cv_stages;
 };
-constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1}, {128, 6, 1}, {64, 8, 1}, {256, 6, 2},
-                                        {128, 8, 2}};
-constexpr TcVariant kTcVariantsI8[] = {{128, 4, 1}};
-constexpr TcVariant kTcVariantsE2M1[] = {{256, 3, 1}, {128, 5, 1}, {64, 8, 1}};
+constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1, 0}, {128, 6, 1, 0}, {64, 8, 1, 0},
+                                        {256, 6, 2, 0}, {128, 8, 2, 0}};
+constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
+constexpr TcVariant kTcVariantsE2M1[] = {{256, 6, 1, 2}, {128, 8, 1, 3}, {64, 8, 1, 4}};
 constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;
 constexpr int kTcThreads = 256;      // FP16 x FP16 kernel
@@ -60,15 +62,18 @@ TcFamily tc_family(dg_dtype da, dg_dtype db) {
   return {nullptr, 0, 0};
 }
 
-// Shared memory of one stage of one CTA: FP16 operand tiles (128-byte
-// swizzle; a CTA of a pair holds half of the B tile) plus the raw int8 /
-// packed-E2M1 tiles the converters widen.
-int tc_stage_bytes(dg_dtype da, dg_dtype db, int n_tile, int cta_group = 1) {
-  int b = kTcBlockM * kTcBlockK * 2 + (n_tile / cta_group) * kTcBlockK * 2;
-  if (da == DG_I8) b += kTcBlockM * kTcBlockK;
-  if (db == DG_I8) b += n_tile * kTcBlockK;
-  if (db == DG_E2M1) b += n_tile * kTcBlockK / 2;
-  return b;
+// Shared memory of one CTA.  FP16 x FP16: `stages` slots of FP16 tiles
+// (128-byte swizzle; a CTA of a pair holds half of the B tile).  Converting
+// kernel: `stages` input slots as loaded (FP16 A or raw int8 A; raw int8 /
+// packed-E2M1 B) plus `cv_stages` slots of widened FP16 operands.
+int tc_ring_bytes(dg_dtype da, dg_dtype db, const TcVariant& v) {
+  const int a16 = kTcBlockM * kTcBlockK * 2;
+  if (da == DG_F16 && db == DG_F16)
+    return v.stages * (a16 + (v.n_tile / v.cta_group) * kTcBlockK * 2);
+  const int in_a = da == DG_I8 ? kTcBlockM * kTcBlockK : a16;
+  const int in_b = db == DG_I8 ? v.n_tile * kTcBlockK : v.n_tile * kTcBlockK / 2;
+  const int cv = (da == DG_I8 ? a16 : 0) + v.n_tile * kTcBlockK * 2;
+  return v.stages * (in_a + in_b) + v.cv_stages * cv;
 }
 
 // Tensor-memory columns: two FP32 accumulators, plus INT32 running sums on
@@ -84,8 +89,8 @@ constexpr int kGemvMaxSplit = 256;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int tc_smem_bytes(dg_dtype da, dg_dtype db, int n_tile, int stages, int cta_group) {
-  return stages * tc_stage_bytes(da, db, n_tile, cta_group) + kTcBarrierBytes + 1024;
+int tc_smem_bytes(dg_dtype da, dg_dtype db, const TcVariant& v) {
+  return tc_ring_bytes(da, db, v) + kTcBarrierBytes + 1024;
 }
 
 double sm_rate_flops_per_us(const dg_hw_desc& hw) {
@@ -101,12 +106,15 @@ double hbm_bytes_per_us(const dg_hw_desc& hw) {
 // Fraction of the tensor rate a 128 x N_tile tcgen05 tile sustains: operand
 // bytes read from shared memory per MMA grow relative to the math as N_tile
 // shrinks.  A rough model, not a measurement.
+// Calibrated on GB300 at 4096^3 (tensor rate sustained per busy SM, measured
+// time x wave efficiency): wider tiles and CTA pairs move fewer operand bytes
+// through L2 and shared memory per FLOP.
 double tc_tile_efficiency(int n_tile, int cta_group) {
-  if (cta_group == 2) return n_tile == 256 ? 0.97 : 0.90;  // half the operand bytes per FLOP
+  if (cta_group == 2) return n_tile == 256 ? 0.86 : 0.63;
   switch (n_tile) {
-    case 256: return 0.92;
-    case 128: return 0.80;
-    default: return 0.55;
+    case 256: return 0.72;
+    case 128: return 0.57;
+    default: return 0.40;
   }
 }
 
@@ -130,7 +138,11 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     const TcVariant& v = fam.v[vi];
     const std::string name =
         "N_tile " + std::to_string(v.n_tile) + (v.cta_group == 2 ? " (CTA pair)" : "");
-    const int smem = tc_smem_bytes(da, db, v.n_tile, v.stages, v.cta_group);
+    if (v.cta_group == 2 && M <= kTcBlockM) {
+      if (why) *why += name + ": M fits one CTA; ";
+      continue;
+    }
+    const int smem = tc_smem_bytes(da, db, v);
     if (smem > hw.smem_per_block_optin) {
       if (why) *why += name + ": shared memory; ";
       continue;

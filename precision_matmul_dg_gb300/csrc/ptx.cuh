@@ -87,6 +87,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// As mbar_wait, for waits expected to last long (a whole main loop): between
+// polls the thread sleeps `sleep_ns`, leaving issue slots to working warps.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity,
+                                                 uint64_t timeout_ns, int* status,
+                                                 uint32_t sleep_ns) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    asm volatile("nanosleep.u32 %0;" ::"r"(sleep_ns));
+    if (mbar_try_wait(a, parity)) return true;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      if (status) atomicExch(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

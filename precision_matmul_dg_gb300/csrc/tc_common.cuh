@@ -109,9 +109,29 @@ inline EncodeTiledFn encode_fn() {
 
 // 2-D tensor map over `rows` rows of `inner` elements (row pitch `pitch_bytes`),
 // box of box_rows x box_inner elements, zero fill outside the tensor.
+// Encoded maps are kept in a small per-thread cache keyed by every argument
+// (a map holds only an address and a layout, so a hit is always valid).
 inline cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                                int64_t rows, int64_t inner, int64_t pitch_bytes, int box_rows,
                                int box_inner, CUtensorMapSwizzle swizzle) {
+  struct Entry {
+    const void* base;
+    int64_t rows, inner, pitch;
+    int box_rows, box_inner, dtype, swizzle;
+    CUtensorMap map;
+  };
+  constexpr int kCache = 16;
+  thread_local Entry cache[kCache];
+  thread_local int used = 0, next = 0;
+  for (int i = 0; i < used; ++i) {
+    const Entry& c = cache[i];
+    if (c.base == base && c.rows == rows && c.inner == inner && c.pitch == pitch_bytes &&
+        c.box_rows == box_rows && c.box_inner == box_inner && c.dtype == static_cast<int>(dtype) &&
+        c.swizzle == static_cast<int>(swizzle)) {
+      *map = c.map;
+      return cudaSuccess;
+    }
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
@@ -122,7 +142,20 @@ inline cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, cons
   const CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  Entry& e = cache[next];
+  e.base = base;
+  e.rows = rows;
+  e.inner = inner;
+  e.pitch = pitch_bytes;
+  e.box_rows = box_rows;
+  e.box_inner = box_inner;
+  e.dtype = static_cast<int>(dtype);
+  e.swizzle = static_cast<int>(swizzle);
+  e.map = *map;
+  next = (next + 1) % kCache;
+  if (used < kCache) ++used;
+  return cudaSuccess;
 }
 
 // K-major FP16 operand tile: box_rows x 64 elements, 128-byte swizzle.

@@ -40,6 +40,8 @@ def tc_smem(n_tile, stages, cg=1):
 def tc_feasible(M, N, hw, target):
     out = set()
     for n_tile, stages, cg in TC_VARIANTS:
+        if cg == 2 and M <= 128:      # a pair needs more than one CTA's rows
+            continue
         if tc_smem(n_tile, stages, cg) > hw["smem_per_block_optin"]:
             continue
         if 2 * n_tile > hw["tmem_cols"]:
@@ -184,18 +186,17 @@ def test_worked_example_tiles_fit_the_a100_description(dg):
     assert all(p["kernel_name"] == "none" for p in plans)  # planning only: no kernel here
 
 
-CONV_VARIANTS = {("i8", "i8"): [(128, 4)], ("f16", "e2m1"): [(256, 3), (128, 5), (64, 8)]}
+# converting kernel: (N_tile, input-ring slots) and the widened-operand slots
+CONV_VARIANTS = {("i8", "i8"): [(128, 8)], ("f16", "e2m1"): [(256, 6), (128, 8), (64, 8)]}
+CV_SLOTS = {("i8", "i8", 128): 3, ("f16", "e2m1", 256): 2, ("f16", "e2m1", 128): 3,
+            ("f16", "e2m1", 64): 4}
 
 
 def conv_smem(da, db, n_tile, stages):
-    b = 128 * 64 * 2 + n_tile * 64 * 2
-    if da == "i8":
-        b += 128 * 64
-    if db == "i8":
-        b += n_tile * 64
-    if db == "e2m1":
-        b += n_tile * 32
-    return stages * b + 512 + 1024
+    in_a = 128 * 64 if da == "i8" else 128 * 64 * 2
+    in_b = n_tile * 64 if db == "i8" else n_tile * 32
+    cv = (128 * 64 * 2 if da == "i8" else 0) + n_tile * 64 * 2
+    return stages * (in_a + in_b) + CV_SLOTS[(da, db, n_tile)] * cv + 512 + 1024
 
 
 @pytest.mark.parametrize("pair", sorted(CONV_VARIANTS))
