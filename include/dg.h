@@ -76,7 +76,10 @@ typedef enum {
 /* Kernel families a plan can select. */
 typedef enum {
   DG_KERNEL_TC = 0,    /* tensor-core pipeline: TMA -> SMEM ring -> tcgen05.mma -> TMEM -> fused epilogue */
-  DG_KERNEL_GEMV = 1   /* thin-M split-K streaming kernel on the CUDA cores */
+  DG_KERNEL_GEMV = 1,  /* thin-M split-K streaming kernel on the CUDA cores */
+  DG_KERNEL_TC_WIDENED = 2 /* int8 / E2M1 operands widened to FP16 by a streaming pre-pass into
+                              a library workspace, then the FP16 tensor-core kernel (INT8:
+                              exact INT32 output) -- for compute-bound shapes */
 } dg_kernel;
 
 /* Hardware description the planner solves against

@@ -52,6 +52,8 @@ struct Workspace {
   int64_t partial_elems = 0;
   unsigned* counters = nullptr;
   int64_t counter_elems = 0;
+  __half* wide = nullptr;  // FP16 copies of widened int8 / E2M1 operands
+  int64_t wide_elems = 0;
 };
 
 std::mutex g_mu;
@@ -210,6 +212,22 @@ dg_status get_workspace(int dev, cudaStream_t stream, int64_t partial_elems, int
   return DG_OK;
 }
 
+// FP16 buffer of at least `elems` halves for widened operands (per device and stream).
+dg_status get_wide_workspace(int dev, cudaStream_t stream, int64_t elems, __half** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+  if (w.wide_elems < elems) {
+    if (w.wide) cudaFree(w.wide);  // synchronises the device: no kernel still uses it
+    w.wide = nullptr;
+    w.wide_elems = 0;
+    cudaError_t e = cudaMalloc(&w.wide, elems * sizeof(__half));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(widened operands)");
+    w.wide_elems = elems;
+  }
+  *out = w.wide;
+  return DG_OK;
+}
+
 dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const void* A,
               int64_t lda, const void* B, int64_t ldb, void* C, const void* bias, float alpha,
               float beta, dg_epilogue epilogue, const dg_tile_plan* forced, cudaStream_t stream) {
@@ -243,6 +261,7 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
   a.status = st->status;
   a.timeout_ns = timeout_ns();
   a.sm_count = st->hw.sm_count;
+  a.exact_i32 = false;
 
   if (K == 0) {
     cudaError_t e = launch_epilogue_only(a);
@@ -298,6 +317,28 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
     e = launch_gemv(a, plan, ws);
   } else if (plan.kernel == DG_KERNEL_TC) {
     e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);
+  } else if (plan.kernel == DG_KERNEL_TC_WIDENED) {
+    // Widen the narrow operands into FP16 copies, then the FP16 kernel.
+    const int64_t ldw = widened_ld(K);
+    const int64_t a_elems = da == DG_I8 ? M * ldw : 0;
+    __half* wide = nullptr;
+    s = get_wide_workspace(dev, stream, a_elems + N * ldw, &wide);
+    if (s != DG_OK) return s;
+    GemmArgs w = a;
+    if (da == DG_I8) {
+      e = launch_widen(DG_I8, A, M, K, lda, wide, stream, a.sm_count);
+      if (e != cudaSuccess) return fail_cuda(e, "widening launch");
+      w.A = wide;
+      w.lda = ldw;
+    }
+    e = launch_widen(db, B, N, K, ldb, wide + a_elems, stream, a.sm_count);
+    if (e != cudaSuccess) return fail_cuda(e, "widening launch");
+    w.B = wide + a_elems;
+    w.ldb = ldw;
+    w.dtype_a = DG_F16;
+    w.dtype_b = DG_F16;
+    w.exact_i32 = da == DG_I8;
+    e = launch_tc(w, plan);
   } else {
     return fail(DG_ERR_INVALID_STATE, "plan names no kernel of this library");
   }
@@ -434,6 +475,7 @@ dg_status dg_shutdown(void) {
     cudaSetDevice(kv.first.first);
     if (kv.second.partial) cudaFree(kv.second.partial);
     if (kv.second.counters) cudaFree(kv.second.counters);
+    if (kv.second.wide) cudaFree(kv.second.wide);
   }
   g_workspaces.clear();
   for (auto& kv : g_devices) {

@@ -52,7 +52,7 @@ constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kConvWarp0 = 8;
 constexpr int kConvThreads = 128;
-constexpr int kI32ChunkKb = 16;  // 16 x 64 = 1024 K per exact FP32 chunk
+using tc::kI32ChunkKb;
 
 struct ConvParams {
   int M, N, K;
@@ -154,53 +154,6 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* op, in
       o = e2m1x8_to_f16x8(w);
     }
     *reinterpret_cast<uint4*>(dst + i * kRowsPerStep * 128) = o;
-  }
-}
-
-__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// INT32 output of one 32-column chunk: D = alpha*sum + beta*C (mod 2^32).
-__device__ __forceinline__ void store_i32_chunk(const uint32_t (&s)[32], int row, int col0,
-                                                const ConvParams& p) {
-  if (row >= p.M) return;
-  int32_t* drow = static_cast<int32_t*>(p.CD) + static_cast<int64_t>(row) * p.N;
-  const uint32_t al = static_cast<uint32_t>(p.alpha_i), be = static_cast<uint32_t>(p.beta_i);
-  const bool full = (col0 + 32 <= p.N) && ((p.N & 3) == 0);
-  if (full) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      uint4 v;
-      if (be != 0u) v = *reinterpret_cast<const uint4*>(drow + col0 + q * 4);
-      else v = make_uint4(0, 0, 0, 0);
-      v.x = al * s[q * 4 + 0] + be * v.x;
-      v.y = al * s[q * 4 + 1] + be * v.y;
-      v.z = al * s[q * 4 + 2] + be * v.z;
-      v.w = al * s[q * 4 + 3] + be * v.w;
-      *reinterpret_cast<uint4*>(drow + col0 + q * 4) = v;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (col0 + i < p.N) {
-        const uint32_t c = be != 0u ? static_cast<uint32_t>(drow[col0 + i]) : 0u;
-        drow[col0 + i] = static_cast<int32_t>(al * s[i] + be * c);
-      }
-    }
   }
 }
 
@@ -428,23 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, static_cast<__half*>(p.CD),
                                      p.bias);
           } else {
-            // exact FP32 chunk sum -> INT32, added to the running sum
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
-            if (ch > 0) {
-              uint32_t s[32];
-              tmem_ld_32cols(sums + c * 32, s);
-              tc_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] += s[i];
-            }
-            if (ch + 1 < num_chunks) {
-              tmem_st_32cols(sums + c * 32, r);
-              tc_wait_st();
-            } else if (col0 < p.N) {
-              store_i32_chunk(r, row, col0, p);
-            }
+            tc::flush_i32_piece(r, sums + c * 32, ch == 0, ch + 1 == num_chunks, row, col0, p.M,
+                                p.N, p.alpha_i, p.beta_i, p.CD);
           }
         }
         tc_fence_before_sync();

@@ -44,8 +44,9 @@ namespace {
 
 using tc::kBlockK;
 using tc::kBlockM;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 8;  // two warps per 32-lane TMEM quarter, each half of the columns
 constexpr int kTileBytesA = kBlockM * kBlockK * 2;
 
 struct TcParams {
@@ -53,12 +54,17 @@ struct TcParams {
   int num_m_blocks, num_n_blocks, num_tiles, num_k_blocks;
   int group_m;
   Epi epi;
-  __half* CD;  // C in / D out, leading dimension N
+  void* CD;  // C in / D out, leading dimension N (FP16, or INT32 when Out == kOutI32)
   const __half* bias;
+  int32_t alpha_i, beta_i;  // integer scalars of the INT32 output
   int* status;
   uint64_t timeout_ns;
   uint32_t stage_tx;  // bytes TMA delivers per stage (both CTAs of a pair)
 };
+
+// Output modes: FP16 with the fused epilogue, or exact INT32 for INT8 inputs
+// widened to FP16 (K accumulated in exact FP32 chunks, INT32 running sum).
+enum : int { kOutF16 = 0, kOutI32 = 1 };
 
 template <int BN, int Stages, int CG>
 struct TcSmem {
@@ -78,12 +84,18 @@ struct TcSmem {
 
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
 
-template <int BN, int Stages, int CG>
+template <int BN, int Stages, int CG, int Out>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
   using L = TcSmem<BN, Stages, CG>;
-  constexpr int kTmemCols = 2 * BN;
+  // two FP32 accumulators, plus the INT32 running sums in the integer mode
+  constexpr int kColsNeeded = (Out == kOutI32 ? 3 : 2) * BN;
+  constexpr int kTmemCols = kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512);
+  static_assert(kColsNeeded <= 512, "tensor memory");
+  // K blocks per accumulation chunk: the whole K, or exact-FP32 chunks
+  const int chunk_kb = Out == kOutI32 ? tc::kI32ChunkKb : p.num_k_blocks;
+  const int num_chunks = (p.num_k_blocks + chunk_kb - 1) / chunk_kb;
   constexpr int kTileM = kBlockM * CG;  // rows of D per tile
   constexpr uint32_t kIdesc = idesc_f16_f32(kTileM, BN);
 
@@ -115,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], CG * 4 * 32);  // every epilogue thread of the pair
+      mbar_init(&tmem_empty[b], CG * kEpiWarps * 32);  // every epilogue thread of the pair
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -195,48 +207,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int t = unit0; t < p.num_tiles && ok; t += units) {
-        if (aborted(abort_flag) ||
-            !mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.timeout_ns, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int ch = 0; ch < num_chunks && ok; ++ch) {
           if (aborted(abort_flag) ||
-              !mbar_wait(&full_bar[stage], phase, p.timeout_ns, p.status)) {
+              !mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.timeout_ns, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a0 = smem_addr(smem_a + stage * kTileBytesA);
-          const uint32_t b0 = smem_addr(smem_b + stage * L::kTileBytesB);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          const int kb0 = ch * chunk_kb;
+          const int kb1 = min(p.num_k_blocks, kb0 + chunk_kb);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (aborted(abort_flag) ||
+                !mbar_wait(&full_bar[stage], phase, p.timeout_ns, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t a0 = smem_addr(smem_a + stage * kTileBytesA);
+            const uint32_t b0 = smem_addr(smem_b + stage * L::kTileBytesB);
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k) {
-            const uint64_t da = smem_desc_sw128(a0 + k * 32), db = smem_desc_sw128(b0 + k * 32);
-            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            for (int k = 0; k < kBlockK / 16; ++k) {
+              const uint64_t da = smem_desc_sw128(a0 + k * 32), db = smem_desc_sw128(b0 + k * 32);
+              const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+              if (CG == 2)
+                tc_mma_f16_pair(d_tmem, da, db, kIdesc, accum);
+              else
+                tc_mma_f16(d_tmem, da, db, kIdesc, accum);
+            }
             if (CG == 2)
-              tc_mma_f16_pair(d_tmem, da, db, kIdesc, accum);
+              tc_commit_pair_multicast(&empty_bar[stage], 0x3);
             else
-              tc_mma_f16(d_tmem, da, db, kIdesc, accum);
+              tc_commit(&empty_bar[stage]);
+            if (++stage == Stages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
+          if (!ok) break;
           if (CG == 2)
-            tc_commit_pair_multicast(&empty_bar[stage], 0x3);
+            tc_commit_pair_multicast(&tmem_full[acc], 0x3);
           else
-            tc_commit(&empty_bar[stage]);
-          if (++stage == Stages) {
-            stage = 0;
-            phase ^= 1;
+            tc_commit(&tmem_full[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
           }
-        }
-        if (!ok) break;
-        if (CG == 2)
-          tc_commit_pair_multicast(&tmem_full[acc], 0x3);
-        else
-          tc_commit(&tmem_full[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1;
         }
       }
       if (!ok) {
@@ -251,39 +267,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - kEpiWarp0;  // TMEM lanes 32*ew .. 32*ew+31
+    // A warp may only access TMEM lanes 32*(warp % 4) .. +31: warps w and
+    // w + 4 share a lane quarter and take one half of the columns each.
+    const int ew = (warp - kEpiWarp0) & 3;
+    const int half = (warp - kEpiWarp0) >> 2;
+    constexpr int kChunksPerHalf = BN / 64;
     const uint32_t empty0 = CG == 2 ? mapa_shared(smem_addr(&tmem_empty[0]), 0) : 0u;
+    const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
+    const uint32_t sums = tmem_base + lane_base + 2 * BN;  // INT32 running sums (Out == I32)
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = unit0; t < p.num_tiles; t += units) {
+    for (int t = unit0; t < p.num_tiles && ok; t += units) {
       int m_blk, n_blk;
       tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
-      if (aborted(abort_flag) ||
-          !mbar_wait_sleepy(&tmem_full[acc], acc_phase, p.timeout_ns, p.status, 256)) {
-        *abort_flag = 1;
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
       const int row = m_blk * kTileM + static_cast<int>(rank) * kBlockM + ew * 32 + lane;
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      for (int ch = 0; ch < num_chunks; ++ch) {
+        if (aborted(abort_flag) ||
+            !mbar_wait_sleepy(&tmem_full[acc], acc_phase, p.timeout_ns, p.status, 256)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(tbase + c * 32, r);
-        tc_wait_ld();
-        const int col0 = n_blk * BN + c * 32;
-        if (col0 < p.N) tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, p.CD, p.bias);
-      }
-      tc_fence_before_sync();
-      if (CG == 2)
-        mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc * 8));
-      else
-        mbar_arrive(&tmem_empty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
+        for (int c = half * kChunksPerHalf; c < (half + 1) * kChunksPerHalf; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(tbase + c * 32, r);
+          tc_wait_ld();
+          const int col0 = n_blk * BN + c * 32;
+          if (Out == kOutF16) {
+            if (col0 < p.N)
+              tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, static_cast<__half*>(p.CD),
+                                     p.bias);
+          } else {
+            tc::flush_i32_piece(r, sums + c * 32, ch == 0, ch + 1 == num_chunks, row, col0, p.M,
+                                p.N, p.alpha_i, p.beta_i, p.CD);
+          }
+        }
+        tc_fence_before_sync();
+        if (CG == 2)
+          mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc * 8));
+        else
+          mbar_arrive(&tmem_empty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
     }
   }
@@ -311,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int Stages, int CG>
+template <int BN, int Stages, int CG, int Out>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   using L = TcSmem<BN, Stages, CG>;
   CUtensorMap ta, tb;
@@ -335,13 +365,15 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.num_k_blocks = static_cast<int>((a.K + kBlockK - 1) / kBlockK);
   p.group_m = 16 / CG;
   p.epi = Epi{a.alpha, a.beta, a.epi};
-  p.CD = static_cast<__half*>(a.C);
+  p.CD = a.C;
   p.bias = static_cast<const __half*>(a.bias);
+  p.alpha_i = static_cast<int32_t>(a.alpha);
+  p.beta_i = static_cast<int32_t>(a.beta);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
   p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB));
 
-  auto kern = gemm_f16_tc_kernel<BN, Stages, CG>;
+  auto kern = gemm_f16_tc_kernel<BN, Stages, CG, Out>;
   int dev = 0;
   cudaGetDevice(&dev);
   // One shared-memory opt-in and one co-residency query per variant and device.
@@ -391,22 +423,29 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
 }  // namespace
 
 // Tile shapes compiled into the library; the planner only proposes these.
+// `a` holds FP16 operands (the caller's, or widened copies); a.exact_i32
+// selects the exact INT32 output of widened INT8 operands.
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
-  if (a.dtype_a != DG_F16 || a.dtype_b != DG_F16) return cudaErrorNotSupported;
+  if (a.exact_i32) {
+    if (plan.n_tile != 128) return cudaErrorNotSupported;
+    if (plan.cta_group == 2 && plan.stages == 8) return run_tc<128, 8, 2, kOutI32>(a, plan);
+    if (plan.cta_group == 1 && plan.stages == 6) return run_tc<128, 6, 1, kOutI32>(a, plan);
+    return cudaErrorNotSupported;
+  }
   if (plan.cta_group == 2) {
-    if (plan.n_tile == 256 && plan.stages == 6) return run_tc<256, 6, 2>(a, plan);
-    if (plan.n_tile == 128 && plan.stages == 8) return run_tc<128, 8, 2>(a, plan);
+    if (plan.n_tile == 256 && plan.stages == 6) return run_tc<256, 6, 2, kOutF16>(a, plan);
+    if (plan.n_tile == 128 && plan.stages == 8) return run_tc<128, 8, 2, kOutF16>(a, plan);
     return cudaErrorNotSupported;
   }
   switch (plan.n_tile) {
     case 256:
-      if (plan.stages == 4) return run_tc<256, 4, 1>(a, plan);
+      if (plan.stages == 4) return run_tc<256, 4, 1, kOutF16>(a, plan);
       break;
     case 128:
-      if (plan.stages == 6) return run_tc<128, 6, 1>(a, plan);
+      if (plan.stages == 6) return run_tc<128, 6, 1, kOutF16>(a, plan);
       break;
     case 64:
-      if (plan.stages == 8) return run_tc<64, 8, 1>(a, plan);
+      if (plan.stages == 8) return run_tc<64, 8, 1, kOutF16>(a, plan);
       break;
   }
   return cudaErrorNotSupported;

@@ -96,8 +96,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
   if (j < p.N && k0 < k1) {
     const __half* brow = p.B + static_cast<int64_t>(j) * p.ldb;
     int k = k0 + lane * 8;
-    // Main body: kGemvUnroll full 256-element steps per iteration.
+    // Batches of kGemvUnroll 256-element steps: every load of a batch is in
+    // flight at once (one memory round trip per batch); steps past the end
+    // of the K range are predicated off.
     constexpr int kStep = 256;
+    // full batches: no predicates in the streaming loop
     for (; k + (kGemvUnroll - 1) * kStep + 8 <= k1; k += kGemvUnroll * kStep) {
       uint4 bv[kGemvUnroll];
 #pragma unroll
@@ -114,20 +117,32 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
         }
       }
     }
-    // Remaining whole 8-element groups.
-    for (; k + 8 <= k1; k += kStep) {
-      const uint4 bv = ld_stream(brow + k);
+    // at most one partial batch, predicated per step
+    if (k + 8 <= k1) {
+      uint4 bv[kGemvUnroll];
 #pragma unroll
-      for (int m = 0; m < MROWS; ++m) {
-        if (m < p.M) {
-          const uint4 av =
-              __ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(m) * p.lda + k));
-          fma8(acc[m], av, bv);
+      for (int u = 0; u < kGemvUnroll; ++u)
+        bv[u] = (k + u * kStep + 8 <= k1) ? ld_stream(brow + k + u * kStep)
+                                          : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kGemvUnroll; ++u) {
+        if (k + u * kStep + 8 <= k1) {
+#pragma unroll
+          for (int m = 0; m < MROWS; ++m) {
+            if (m < p.M) {
+              const uint4 av = __ldg(reinterpret_cast<const uint4*>(
+                  p.A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
+              fma8(acc[m], av, bv[u]);
+            }
+          }
         }
       }
     }
-    // Ragged tail (< 8 elements at the end of the K range), scalar.
-    if (k < k1) {
+    // k is now past the last whole 8-element group this lane owns; the
+    // ragged tail (< 8 elements at the end of the K range) is done by the
+    // lane whose next group would have started there.
+    k = k1 - ((k1 - k0) & 7);
+    if ((k - k0) % kStep == lane * 8 && k < k1) {
       for (int kk = k; kk < k1; ++kk) {
         const float bf = __half2float(brow[kk]);
 #pragma unroll
@@ -407,6 +422,7 @@ extern "C" dg_status dg_gemm_thin_noalloc(int64_t M, int64_t N, int64_t K, dg_dt
   a.stream = st;
   a.status = nullptr;
   a.timeout_ns = 0;
+  a.exact_i32 = false;
   a.sm_count = hw.sm_count;
   dg_tile_plan plan{};
   plan.kernel = DG_KERNEL_GEMV;

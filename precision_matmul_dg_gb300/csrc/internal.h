@@ -1,6 +1,7 @@
 // Declarations shared by the host translation units of libdg (not exported).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,6 +30,7 @@ struct GemmArgs {
   int* status;          // per-device status word (device memory)
   uint64_t timeout_ns;  // device-side wait limit
   int sm_count;
+  bool exact_i32;       // FP16 operands hold widened INT8 values: exact INT32 output
 };
 
 // Planner (planner.cpp) -- host only.
@@ -53,6 +55,12 @@ cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);    // F16 x 
 cudaError_t launch_conv(const GemmArgs& a, const dg_tile_plan& plan);  // I8 x I8, F16 x E2M1
 cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws);
 cudaError_t launch_epilogue_only(const GemmArgs& a);
+
+// Widening pre-pass (widen.cu): int8 or packed-E2M1 rows -> FP16 rows with
+// leading dimension widened_ld(K).
+int64_t widened_ld(int64_t K);
+cudaError_t launch_widen(dg_dtype dtype, const void* src, int64_t rows, int64_t K, int64_t ld_src,
+                         __half* dst, cudaStream_t stream, int sm_count);
 cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns);
 
 // Workspace sizes a GEMV plan needs.

@@ -41,10 +41,12 @@ struct TcVariant {
 constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1, 0}, {128, 6, 1, 0}, {64, 8, 1, 0},
                                         {256, 6, 2, 0}, {128, 8, 2, 0}};
 constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
+// FP16 kernel in its exact-INT32 mode (three 128-column TMEM regions)
+constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {128, 8, 2, 0}};
 constexpr TcVariant kTcVariantsE2M1[] = {{256, 6, 1, 2}, {128, 8, 1, 3}, {64, 8, 1, 4}};
 constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;
-constexpr int kTcThreads = 256;      // FP16 x FP16 kernel
+constexpr int kTcThreads = 384;      // FP16 x FP16 kernel (eight epilogue warps)
 constexpr int kConvThreads = 384;    // converting kernel (adds four converter warps)
 constexpr int kTcRegsPerThread = 168;  // upper bound of what ptxas assigns these kernels
 constexpr int kTcBarrierBytes = 512;
@@ -85,7 +87,10 @@ constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kGemvRegsPerThread = 64;
 constexpr int kGemvMaxM = 8;
 constexpr int kGemvResidentWarpsPerSm = 64;
-constexpr int kGemvMaxSplit = 256;
+// Split-K counts the GEMV may use: dense at the low end so that a warp's K
+// range can match one batch of in-flight loads (1024 K per lane group).
+constexpr int kGemvSplits[] = {1,  2,  3,  4,  5,  6,  7,  8,   10,  12,  13,  14,  16,
+                               20, 24, 28, 32, 40, 48, 64, 96, 128, 160, 192, 256};
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -103,12 +108,9 @@ double hbm_bytes_per_us(const dg_hw_desc& hw) {
   return gbps * 1e3;  // GB/s -> bytes per microsecond
 }
 
-// Fraction of the tensor rate a 128 x N_tile tcgen05 tile sustains: operand
-// bytes read from shared memory per MMA grow relative to the math as N_tile
-// shrinks.  A rough model, not a measurement.
-// Calibrated on GB300 at 4096^3 (tensor rate sustained per busy SM, measured
-// time x wave efficiency): wider tiles and CTA pairs move fewer operand bytes
-// through L2 and shared memory per FLOP.
+// Fraction of the tensor rate a tile shape sustains per busy SM, calibrated on
+// GB300 at 4096^3 (measured time x wave efficiency): wider tiles and CTA pairs
+// move fewer operand bytes through L2 and shared memory per FLOP.
 double tc_tile_efficiency(int n_tile, int cta_group) {
   if (cta_group == 2) return n_tile == 256 ? 0.86 : 0.63;
   switch (n_tile) {
@@ -118,10 +120,19 @@ double tc_tile_efficiency(int n_tile, int cta_group) {
   }
 }
 
-void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+// Tensor-core candidates.  widened == false: the kernel that reads the
+// operands as stored (FP16 x FP16, or the converting kernel that widens
+// int8 / E2M1 tiles in shared memory).  widened == true (int8 / E2M1 only):
+// a streaming pre-pass widens the narrow operands to FP16 in a workspace and
+// the FP16 kernel runs on the copies (INT8 with its exact INT32 output mode).
+void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, bool widened,
                        const dg_hw_desc& hw, double target, std::vector<dg_tile_plan>* out,
                        std::string* why) {
-  const TcFamily fam = tc_family(da, db);
+  const bool narrow = !(da == DG_F16 && db == DG_F16);
+  if (widened && !narrow) return;
+  TcFamily fam = widened ? (da == DG_I8 ? TcFamily{kTcVariantsI8Widened, 2, kTcThreads}
+                                        : TcFamily{kTcVariantsF16, 5, kTcThreads})
+                         : tc_family(da, db);
   if (!fam.v) {
     if (why) *why += "tensor-core kernel: dtype pair not compiled; ";
     return;
@@ -134,15 +145,23 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
   const double elem_a = da == DG_I8 ? 1.0 : 2.0;
   const double elem_b = db == DG_I8 ? 1.0 : (db == DG_E2M1 ? 0.5 : 2.0);
   const double elem_d = da == DG_I8 ? 4.0 : 2.0;
+  // the pre-pass reads the narrow operands and writes FP16 copies
+  const double pre_bytes =
+      widened ? (da == DG_I8 ? 3.0 * M * K : 0.0) + (elem_b + 2.0) * N * static_cast<double>(K)
+              : 0.0;
+  const double t_pre = widened ? pre_bytes / hbm_bytes_per_us(hw) + (da == DG_I8 ? 4.0 : 2.0)
+                               : 0.0;
+  // shared memory / tensor memory are those of the kernel that runs
+  const dg_dtype ka = widened ? DG_F16 : da, kb = widened ? DG_F16 : db;
   for (int vi = 0; vi < fam.n; ++vi) {
     const TcVariant& v = fam.v[vi];
-    const std::string name =
-        "N_tile " + std::to_string(v.n_tile) + (v.cta_group == 2 ? " (CTA pair)" : "");
+    const std::string name = std::string(widened ? "widened " : "") + "N_tile " +
+                             std::to_string(v.n_tile) + (v.cta_group == 2 ? " (CTA pair)" : "");
     if (v.cta_group == 2 && M <= kTcBlockM) {
       if (why) *why += name + ": M fits one CTA; ";
       continue;
     }
-    const int smem = tc_smem_bytes(da, db, v);
+    const int smem = tc_smem_bytes(ka, kb, v);
     if (smem > hw.smem_per_block_optin) {
       if (why) *why += name + ": shared memory; ";
       continue;
@@ -169,8 +188,9 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     const int64_t k_pad = ceil_div(K, kTcBlockK) * kTcBlockK;
     // FLOPs of one tile per SM of its unit
     const double tile_flops = 2.0 * kTcBlockM * v.n_tile * static_cast<double>(k_pad);
-    // Converting kernels also spend shared-memory bandwidth widening operands.
-    const double conv_eff = (da == DG_I8) ? 0.5 : (db == DG_E2M1 ? 0.75 : 1.0);
+    // The converting kernel spends shared-memory bandwidth and issue slots
+    // widening tiles (calibrated on GB300: INT8 4096^3, W4A16 2048x8960x1536).
+    const double conv_eff = (narrow && !widened) ? (da == DG_I8 ? 0.36 : 0.54) : 1.0;
     const double t_math =
         waves * tile_flops /
         (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile, v.cta_group) * conv_eff);
@@ -178,7 +198,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     const double t_mem = bytes / hbm_bytes_per_us(hw);
     const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
     dg_tile_plan p{};
-    p.kernel = DG_KERNEL_TC;
+    p.kernel = widened ? DG_KERNEL_TC_WIDENED : DG_KERNEL_TC;
     p.m_tile = tile_m;
     p.n_tile = v.n_tile;
     p.k_tile = kTcBlockK;
@@ -190,7 +210,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     p.threads = fam.threads;
     p.grid = static_cast<int>(std::min<int64_t>(tiles, units) * v.cta_group);
     p.occupancy = occ;
-    p.est_us = std::max(t_math, t_mem) + t_epi + 2.0;
+    p.est_us = std::max(t_math, t_mem) + t_epi + 2.0 + t_pre;
     p.est_tflops = 2.0 * M * N * K / (p.est_us * 1e6);
     out->push_back(p);
   }
@@ -212,10 +232,10 @@ void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype 
     return;
   }
   const int64_t resident = static_cast<int64_t>(hw.sm_count) * kGemvResidentWarpsPerSm;
-  for (int split = 1; split <= kGemvMaxSplit; split *= 2) {
+  for (int split : kGemvSplits) {
     int64_t chunk = 0;
     const double t = gemv_estimate_us(M, N, K, split, hw, &chunk);
-    if (t < 0) break;  // the last split would be empty
+    if (t < 0) continue;  // the last split would be empty
     const int64_t units = N * split;  // warps
     const int64_t waves = ceil_div(units, resident);
     const double occ = static_cast<double>(units) / static_cast<double>(waves * resident);
@@ -314,16 +334,19 @@ double gemv_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_
   const double bw = std::min(hbm_bytes_per_us(hw), active * 2.0e3);
   const double bytes = 2.0 * (N * K + M * K) + (split > 1 ? 8.0 * split * M * N : 0.0) +
                        4.0 * M * N;
-  return bytes / bw + (split > 1 ? 1.0 : 0.0) + 2.0;
+  // A warp streams its K range in batches of 4 x 256 elements, one memory
+  // round trip (~0.8 us) each; small problems are bound by that latency.
+  const double batches = static_cast<double>(ceil_div(chunk, 1024));
+  return std::max(bytes / bw, 0.8 * batches) + (split > 1 ? 1.0 : 0.0) + 2.0;
 }
 
 int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out) {
   int best = 1;
   double best_t = -1.0;
-  for (int split = 1; split <= kGemvMaxSplit; split *= 2) {
+  for (int split : kGemvSplits) {
     int64_t chunk = 0;
     const double t = gemv_estimate_us(M, N, K, split, hw, &chunk);
-    if (t < 0) break;
+    if (t < 0) continue;
     if (best_t < 0 || t < best_t) {
       best_t = t;
       best = split;
@@ -340,7 +363,8 @@ dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype
   if (n_out) *n_out = 0;
   std::vector<dg_tile_plan> cands;
   if (hw.tmem_cols > 0) {
-    add_tc_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
+    add_tc_candidates(M, N, K, dtype_a, dtype_b, false, hw, target_occupancy, &cands, why);
+    add_tc_candidates(M, N, K, dtype_a, dtype_b, true, hw, target_occupancy, &cands, why);
     add_gemv_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
   } else {
     add_warp_mma_candidates(M, N, K, dtype_a, hw, target_occupancy, &cands, why);
@@ -375,6 +399,28 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
           fam.v[vi].cta_group == plan.cta_group)
         return true;
     if (why) *why = "tensor-core N_tile/stages pair not compiled";
+    return false;
+  }
+  if (plan.kernel == DG_KERNEL_TC_WIDENED) {
+    const bool i8 = dtype_a == DG_I8 && dtype_b == DG_I8;
+    const bool e2m1 = dtype_a == DG_F16 && dtype_b == DG_E2M1;
+    if (!i8 && !e2m1) {
+      if (why) *why = "widened plans are for INT8 x INT8 and FP16 x E2M1";
+      return false;
+    }
+    if ((plan.cta_group != 1 && plan.cta_group != 2) ||
+        plan.m_tile != kTcBlockM * plan.cta_group || plan.k_tile != kTcBlockK ||
+        plan.split_k != 1 || plan.swap_ab != 0) {
+      if (why) *why = "widened plan shape not compiled";
+      return false;
+    }
+    const TcVariant* vs = i8 ? kTcVariantsI8Widened : kTcVariantsF16;
+    const int n = i8 ? 2 : 5;
+    for (int vi = 0; vi < n; ++vi)
+      if (vs[vi].n_tile == plan.n_tile && vs[vi].stages == plan.stages &&
+          vs[vi].cta_group == plan.cta_group)
+        return true;
+    if (why) *why = "widened N_tile/stages pair not compiled";
     return false;
   }
   if (plan.kernel == DG_KERNEL_GEMV) {

@@ -86,6 +86,84 @@ __device__ __forceinline__ void epilogue_f16_chunk(const uint32_t (&r)[32], int 
   }
 }
 
+// ------------------------------------------------- exact INT32 from FP32 chunks
+// An INT8 x INT8 product is an integer of magnitude <= 2^14, so a sum of at
+// most 1024 of them is an integer of magnitude <= 2^24, exact in FP32.  The
+// integer kernels accumulate K in chunks of this many 64-wide K blocks and
+// carry an INT32 running sum between chunks.
+constexpr int kI32ChunkKb = 16;  // 16 x 64 = 1024
+
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// INT32 output of one 32-column chunk: D = alpha*sum + beta*C (mod 2^32).
+__device__ __forceinline__ void store_i32_chunk(const uint32_t (&s)[32], int row, int col0, int M,
+                                                int N, int32_t alpha, int32_t beta, void* cd) {
+  if (row >= M) return;
+  int32_t* drow = static_cast<int32_t*>(cd) + static_cast<int64_t>(row) * N;
+  const uint32_t al = static_cast<uint32_t>(alpha), be = static_cast<uint32_t>(beta);
+  const bool full = (col0 + 32 <= N) && ((N & 3) == 0);
+  if (full) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint4 v;
+      if (be != 0u) v = *reinterpret_cast<const uint4*>(drow + col0 + q * 4);
+      else v = make_uint4(0, 0, 0, 0);
+      v.x = al * s[q * 4 + 0] + be * v.x;
+      v.y = al * s[q * 4 + 1] + be * v.y;
+      v.z = al * s[q * 4 + 2] + be * v.z;
+      v.w = al * s[q * 4 + 3] + be * v.w;
+      *reinterpret_cast<uint4*>(drow + col0 + q * 4) = v;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (col0 + i < N) {
+        const uint32_t c = be != 0u ? static_cast<uint32_t>(drow[col0 + i]) : 0u;
+        drow[col0 + i] = static_cast<int32_t>(al * s[i] + be * c);
+      }
+    }
+  }
+}
+
+// One 32-column piece of an INT8 accumulation chunk: convert the exact FP32
+// chunk sums `r` to INT32, add the running sum kept in TMEM at `sums` (all
+// chunks but the first), then either store the new running sum back (not the
+// last chunk) or write the result to D (last chunk).
+__device__ __forceinline__ void flush_i32_piece(uint32_t (&r)[32], uint32_t sums, bool first,
+                                                bool last, int row, int col0, int M, int N,
+                                                int32_t alpha, int32_t beta, void* cd) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+  if (!first) {
+    uint32_t s[32];
+    tmem_ld_32cols(sums, s);
+    tc_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] += s[i];
+  }
+  if (!last) {
+    tmem_st_32cols(sums, r);
+    tc_wait_st();
+  } else if (col0 < N) {
+    store_i32_chunk(r, row, col0, M, N, alpha, beta, cd);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -201,13 +201,30 @@ def test_int8_extremes_and_wraparound(dg):
 
 
 def test_int8_every_plan(dg):
+    # converting kernel and widened plans (1 CTA and CTA pair, exact INT32 mode);
+    # K = 2500 spans three exact-FP32 chunks of 1024 and a ragged tail
     case = workloads.random_case(300, 600, 2500, "i8", "i8", alpha=1, beta=1, seed=3)
-    tc = [p for p in _plans(dg, case) if p["kernel_name"] == "tc"]
-    assert tc
-    for p in tc:
+    plans = [p for p in _plans(dg, case) if p["kernel_name"] in ("tc", "tc_widened")]
+    assert {p["kernel_name"] for p in plans} == {"tc", "tc_widened"}
+    assert {p["cta_group"] for p in plans} == {1, 2}
+    for p in plans:
         for grid in (p["grid"], 3):
             got, _ = run_case(dg, case, plan=dict(p, grid=grid))
             assert_parity(case, got)
+
+
+def test_int8_widened_extremes(dg):
+    # adversarial exactness through the widened path: all -128 (chunk sums of
+    # exactly 2^24) and mixed extremes, at sizes where the planner widens
+    K = 4096
+    for a_val, b_val in [(-128, -128), (127, -128)]:
+        case = workloads.random_case(512, 512, K, "i8", "i8", seed=1)
+        case.A = np.full_like(case.A, a_val)
+        case.B = np.full_like(case.B, b_val)
+        for p in _plans(dg, case):
+            if p["kernel_name"] == "tc_widened":
+                got, _ = run_case(dg, case, plan=p)
+                assert np.all(got == a_val * b_val * K), p
 
 
 # ------------------------------------------------------- W4A16
@@ -258,8 +275,9 @@ def test_w4a16_every_code_one_hot(dg):
 def test_w4a16_every_plan(dg):
     case = workloads.random_case(200, 700, 600, "f16", "e2m1", epilogue="bias_gelu", beta=0.5,
                                  seed=5)
-    tc = [p for p in _plans(dg, case) if p["kernel_name"] == "tc"]
-    assert {p["n_tile"] for p in tc} == {64, 128, 256}
-    for p in tc:
+    plans = [p for p in _plans(dg, case) if p["kernel_name"] in ("tc", "tc_widened")]
+    assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc"} == {64, 128, 256}
+    assert {p["cta_group"] for p in plans if p["kernel_name"] == "tc_widened"} == {1, 2}
+    for p in plans:
         got, _ = run_case(dg, case, plan=p)
         assert_parity(case, got)

@@ -21,7 +21,7 @@ GB300 = dict(sm_count=152, cc_major=10, cc_minor=3, smem_per_block_optin=232448,
              hbm_gbps=6800.0, tc_f16_tflops=1900.0, clock_ghz=2.07)
 
 # Compiled FP16 tensor-core variants: (N_tile, stages, CTAs per tile); M_tile
-# 128 per CTA, K_tile 64, 256 threads.  A CTA pair holds half of B per CTA.
+# 128 per CTA, K_tile 64, 384 threads.  A CTA pair holds half of B per CTA.
 TC_VARIANTS = [(256, 4, 1), (128, 6, 1), (64, 8, 1), (256, 6, 2), (128, 8, 2)]
 
 
@@ -46,7 +46,7 @@ def tc_feasible(M, N, hw, target):
             continue
         if 2 * n_tile > hw["tmem_cols"]:
             continue
-        if 256 * 168 > hw["regs_per_sm"]:
+        if 384 * 168 > hw["regs_per_sm"]:
             continue
         units = hw["sm_count"] // cg
         tiles = math.ceil(M / (128 * cg)) * math.ceil(N / n_tile)
@@ -62,17 +62,19 @@ def gemv_feasible(M, N, K, hw, target):
     if M > 8:
         return out
     resident = hw["sm_count"] * 64
-    split = 1
-    while split <= 256:
+    for split in GEMV_SPLITS:
         chunk = math.ceil(math.ceil(K / split) / 256) * 256
         if split > 1 and chunk * (split - 1) >= K:
-            break
+            continue                      # the last split would be empty
         units = N * split
         waves = math.ceil(units / resident)
         if units / (waves * resident) >= target:
             out.add(("gemv", 8, 1, split))
-        split *= 2
     return out
+
+
+GEMV_SPLITS = [1, 2, 3, 4, 5, 6, 7, 8, 10, 12, 13, 14, 16, 20, 24, 28, 32, 40, 48, 64, 96, 128,
+               160, 192, 256]
 
 
 SHAPES = [(256, 256, 256), (4096, 4096, 4096), (2048, 2048, 2048), (8192, 8192, 8192),
@@ -205,11 +207,26 @@ def conv_smem(da, db, n_tile, stages):
 def test_converting_kernel_plans(dg, pair, shape):
     M, N, K = shape
     plans = dg.plan_tiles(M, N, K, pair[0], pair[1], hw=GB300, target_occupancy=0.0)
-    got = {(p["n_tile"], p["stages"]) for p in plans}
-    assert got == set(CONV_VARIANTS[pair])
-    for p in plans:
-        assert p["kernel_name"] == "tc" and p["threads"] == 384
+    assert {p["kernel_name"] for p in plans} == {"tc", "tc_widened"}
+    conv = [p for p in plans if p["kernel_name"] == "tc"]
+    assert {(p["n_tile"], p["stages"]) for p in conv} == set(CONV_VARIANTS[pair])
+    for p in conv:
+        assert p["threads"] == 384
         assert p["smem_bytes"] == conv_smem(pair[0], pair[1], p["n_tile"], p["stages"])
         assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
         cols = (3 if pair[0] == "i8" else 2) * p["n_tile"]
         assert cols <= GB300["tmem_cols"]
+    # widened: the FP16 kernel's variants (INT8: its exact-INT32 mode, N_tile 128)
+    wide = {(p["n_tile"], p["stages"], p["cta_group"]) for p in plans
+            if p["kernel_name"] == "tc_widened"}
+    if pair[0] == "i8":
+        want = {(128, 6, 1), (128, 8, 2)}
+    else:
+        want = set(TC_VARIANTS)
+    if M <= 128:
+        want = {w for w in want if w[2] == 1}
+    assert wide == want
+    for p in plans:
+        if p["kernel_name"] == "tc_widened":
+            assert p["threads"] == 384
+            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], p["cta_group"])
