@@ -14,9 +14,13 @@
 //   warp 1      MMA issuer: 4 x tcgen05.mma (K = 16 each) per slot into an
 //               FP32 accumulator in TMEM; tcgen05.commit frees slots;
 //   warp 2      allocates / frees the tensor memory (2 accumulators);
-//   warps 4-7   epilogue: tcgen05.ld of the accumulator (each warp owns 32 of
-//               the 128 TMEM lanes = rows), alpha/beta/bias/GELU in FP32,
-//               FP16 round-to-nearest-even, stored straight to D.
+//   warps 4-11  epilogue: tcgen05.ld of the accumulator (warps w and w + 4
+//               own TMEM lanes 32*(w % 4) .. +31 = rows, and half of the
+//               columns each), alpha/beta/bias/GELU in FP32, FP16
+//               round-to-nearest-even.  With N % 8 == 0 each warp moves C in
+//               and D out as 32 x 32 boxes through two shared-memory staging
+//               buffers with TMA (whole lines, C loaded ahead of use); other
+//               shapes store from registers.
 //
 // CG = 1: one CTA computes a 128 x BN tile.
 // CG = 2: a cluster of two CTAs computes a 256 x BN tile with 256-row MMAs
@@ -29,7 +33,11 @@
 // The kernel is persistent (one CTA / pair per SM / SM pair walks the tile
 // list), and the two TMEM accumulators let the epilogue of tile i overlap the
 // main loop of tile i+1.  Out-of-range rows and K columns are zero-filled by
-// TMA; the epilogue masks rows >= M and columns >= N.  Every mbarrier wait is
+// TMA; the epilogue masks (or the store's tensor map clips) rows >= M and
+// columns >= N.  Operand tiles are loaded with an L2 evict-last hint (they
+// are re-read by other tiles), C with evict-first.  Launches use programmatic
+// dependent launch: set-up overlaps the previous kernel's drain, and global
+// memory is touched only after griddepcontrol.wait.  Every mbarrier wait is
 // bounded: on a timeout the CTA records it in the status word, drains its
 // own copies and MMAs, frees its tensor memory and exits.
 #include <cuda.h>
@@ -60,21 +68,27 @@ struct TcParams {
   int* status;
   uint64_t timeout_ns;
   uint32_t stage_tx;  // bytes TMA delivers per stage (both CTAs of a pair)
+  int staged;         // FP16 out through shared-memory boxes and TMA (else direct stores)
 };
 
 // Output modes: FP16 with the fused epilogue, or exact INT32 for INT8 inputs
 // widened to FP16 (K accumulated in exact FP32 chunks, INT32 running sum).
 enum : int { kOutF16 = 0, kOutI32 = 1 };
 
-template <int BN, int Stages, int CG>
+// Shared memory: the operand ring, then (FP16 output) two staging boxes per
+// epilogue warp, then the barriers.
+template <int BN, int Stages, int CG, bool Staged>
 struct TcSmem {
   static constexpr int kRowsB = BN / CG;  // B rows this CTA loads
   static constexpr int kTileBytesB = kRowsB * kBlockK * 2;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + Stages * kTileBytesA;
-  static constexpr int kOffBar = kOffB + Stages * kTileBytesB;
-  // full[Stages], empty[Stages], tmem_full[2], tmem_empty[2], drain
-  static constexpr int kNumBars = 2 * Stages + 5;
+  static constexpr int kOffEpi = kOffB + Stages * kTileBytesB;
+  static constexpr int kEpiBytes = Staged ? kEpiWarps * 2 * tc::kEpiBoxBytes : 0;
+  static constexpr int kOffBar = kOffEpi + kEpiBytes;
+  // full[Stages], empty[Stages], tmem_full[2], tmem_empty[2], drain, then
+  // (Staged) one C-load barrier per staging box
+  static constexpr int kNumBars = 2 * Stages + 5 + (Staged ? 2 * kEpiWarps : 0);
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
@@ -84,11 +98,53 @@ struct TcSmem {
 
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
 
+// Staged epilogue: epilogue warp wi (0..7) owns TMEM lane quarter wi & 3 and
+// half wi >> 2 of the tile's 32-column chunks.  Its chunks form one stream over
+// the CTA's tiles; chunk j of the stream is the (j % n)-th chunk of the CTA's
+// (j / n)-th tile.  Returns the chunk's D coordinates, false past the end of
+// the stream or when the box lies wholly outside D.
+template <int BN, int CG>
+__device__ __forceinline__ bool epi_box(const TcParams& p, int unit0, int units, uint32_t rank,
+                                        int wi, int j, int& x, int& y) {
+  constexpr int kChunks = BN / 32;
+  const int half = wi >> 2;
+  const int lo = half == 0 ? 0 : (kChunks + 1) / 2;
+  const int n = half == 0 ? (kChunks + 1) / 2 : kChunks - (kChunks + 1) / 2;
+  const int t = unit0 + (j / n) * units;
+  if (t >= p.num_tiles) return false;
+  int mb, nb;
+  tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+  x = nb * BN + (lo + j % n) * 32;
+  y = mb * kBlockM * CG + static_cast<int>(rank) * kBlockM + (wi & 3) * 32;
+  return x < p.N && y < p.M;
+}
+
+// Loads C of stream chunk j of warp wi into its box j & 1 (arriving on that
+// box's barrier).  For the first chunk of a tile it also asks L2 for the
+// tile's chunks from the third on, which are loaded only during the
+// epilogue.  Box j & 1 must no longer feed a store.
+template <int BN, int CG>
+__device__ __forceinline__ void epi_load_c(const CUtensorMap* map, const TcParams& p, int unit0,
+                                           int units, uint32_t rank, int wi, int j,
+                                           uint8_t* boxes, uint64_t* cbar, uint64_t policy) {
+  constexpr int kChunks = BN / 32;
+  const int n = (wi >> 2) == 0 ? (kChunks + 1) / 2 : kChunks - (kChunks + 1) / 2;
+  int x, y;
+  if (!epi_box<BN, CG>(p, unit0, units, rank, wi, j, x, y)) return;
+  const int b = j & 1;
+  mbar_arrive_expect_tx(&cbar[b], tc::kEpiBoxBytes);
+  tma_load_2d(map, &cbar[b], boxes + b * tc::kEpiBoxBytes, x, y, policy);
+  if (j % n == 0)
+    for (int k = 2; k < n; ++k)
+      if (epi_box<BN, CG>(p, unit0, units, rank, wi, j + k, x, y)) tma_prefetch_l2_2d(map, x, y);
+}
+
 template <int BN, int Stages, int CG, int Out>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                       const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using L = TcSmem<BN, Stages, CG>;
+                       const __grid_constant__ CUtensorMap tmap_b,
+                       const __grid_constant__ CUtensorMap tmap_cd, const TcParams p) {
+  using L = TcSmem<BN, Stages, CG, Out == kOutF16>;
   // two FP32 accumulators, plus the INT32 running sums in the integer mode
   constexpr int kColsNeeded = (Out == kOutI32 ? 3 : 2) * BN;
   constexpr int kTmemCols = kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512);
@@ -110,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_full = bars + 2 * Stages;
   uint64_t* tmem_empty = bars + 2 * Stages + 2;
   uint64_t* drain_bar = bars + 2 * Stages + 4;
+  uint64_t* epi_bar = bars + 2 * Stages + 5;  // [kEpiWarps][2] when staged
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
 
@@ -130,12 +187,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tmem_empty[b], CG * kEpiWarps * 32);  // every epilogue thread of the pair
     }
     mbar_init(drain_bar, 1);
+    if (Out == kOutF16)
+      for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&epi_bar[b], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
+    if (Out == kOutF16 && p.staged) tma_prefetch_desc(&tmap_cd);
   }
   if (warp == 2) {
     if (CG == 2)
@@ -149,11 +209,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   bool ok = true;
+  // Launched with programmatic stream serialization: the kernel before this
+  // one in the stream may still be finishing.  Everything above touched only
+  // this CTA's (or pair's) own on-chip state; global memory waits for it.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (elect_one_lane()) {
-      const uint64_t pol = policy_evict_normal();
+      // Operand tiles are read again by other tiles: they outrank C and D in L2.
+      const uint64_t pol = policy_evict_last();
+      // The staged epilogue's first two C boxes per warp are loaded from here,
+      // behind the first ring of operand tiles, so they do not delay the first MMA.
+      const bool first_c = Out == kOutF16 && p.staged && p.epi.beta != 0.0f;
+      auto initial_c = [&]() {
+        const uint64_t pol_c = policy_evict_first();
+        for (int wi = 0; wi < kEpiWarps; ++wi)
+          for (int j = 0; j < 2; ++j)
+            epi_load_c<BN, CG>(&tmap_cd, p, unit0, units, rank, wi, j,
+                               smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes, epi_bar + wi * 2,
+                               pol_c);
+      };
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
@@ -182,12 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(&tmap_b, bar0, dst_b, kb * kBlockK, b_row, pol);
           }
           ++issued;
+          if (first_c && issued == Stages) initial_c();
           if (++stage == Stages) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
+      if (first_c && ok && issued < Stages) initial_c();
       if (!ok) {
         *abort_flag = 1;
         if (CG == 1 || leader) {
@@ -271,13 +350,123 @@ __global__ void __launch_bounds__(kThreads, 1)
     // w + 4 share a lane quarter and take one half of the columns each.
     const int ew = (warp - kEpiWarp0) & 3;
     const int half = (warp - kEpiWarp0) >> 2;
-    constexpr int kChunksPerHalf = BN / 64;
+    // 32-column chunks of this half: [0, ceil(n/2)) or [ceil(n/2), n)
+    constexpr int kChunks = BN / 32;
+    const int chunk_lo = half == 0 ? 0 : (kChunks + 1) / 2;
+    const int chunk_hi = half == 0 ? (kChunks + 1) / 2 : kChunks;
     const uint32_t empty0 = CG == 2 ? mapa_shared(smem_addr(&tmem_empty[0]), 0) : 0u;
     const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
     const uint32_t sums = tmem_base + lane_base + 2 * BN;  // INT32 running sums (Out == I32)
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = unit0; t < p.num_tiles && ok; t += units) {
+    if (Out == kOutF16 && p.staged) {
+      // Staged epilogue.  The warp's chunks form one stream over its tiles
+      // (epi_box); chunk j of the stream goes through box j & 1 of the warp's
+      // two boxes.  C of chunks 0 and 1 is loaded by the producer; lane 0
+      // loads C of chunk j + 2 as soon as chunk j's store has read its box,
+      // so it arrives while the warp finishes chunk j + 1 or, across tiles,
+      // during the next main loop.
+      const int wi = warp - kEpiWarp0;
+      uint8_t* boxes = smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes;
+      uint64_t* cbar = epi_bar + wi * 2;
+      const bool has_c = p.epi.beta != 0.0f;
+      const uint64_t pol_c = policy_evict_first();
+      uint32_t c_phase = 0;    // bit b: parity of box b's next C arrival
+      uint32_t c_pending = 0;  // bit b: a C load into box b not yet waited for
+      bool prev_stored = false;
+      auto box_at = [&](int jj, int& x, int& y) -> bool {
+        return epi_box<BN, CG>(p, unit0, units, rank, wi, jj, x, y);
+      };
+      auto load_c = [&](int jj) {
+        int x, y;
+        if (!has_c || !box_at(jj, x, y)) return;
+        c_pending |= 1u << (jj & 1);
+        if (lane == 0) {
+          bulk_wait_group_read<0>();  // the store that last used the box has read it
+          epi_load_c<BN, CG>(&tmap_cd, p, unit0, units, rank, wi, jj, boxes, cbar, pol_c);
+        }
+      };
+      for (int jj = 0; jj < 2; ++jj) {  // issued by the producer
+        int x, y;
+        if (has_c && box_at(jj, x, y)) c_pending |= 1u << jj;
+      }
+      int j = 0;
+      for (int t = unit0; t < p.num_tiles && ok; t += units) {
+        const bool ready =
+            !aborted(abort_flag) &&
+            mbar_wait_sleepy(&tmem_full[acc], acc_phase, p.timeout_ns, p.status, 256);
+        if (!__all_sync(0xffffffffu, ready)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+        for (int c = chunk_lo; c < chunk_hi; ++c, ++j) {
+          const int b = j & 1;
+          uint8_t* box = boxes + b * tc::kEpiBoxBytes;
+          int x, y;
+          const bool live = box_at(j, x, y);
+          if (live) {
+            uint32_t r[32];
+            tmem_ld_32cols(tbase + c * 32, r);
+            bool got = true;
+            if (has_c) {
+              got = mbar_wait(&cbar[b], (c_phase >> b) & 1u, p.timeout_ns, p.status);
+              if (got) {
+                c_phase ^= 1u << b;
+                c_pending &= ~(1u << b);
+              }
+            } else {
+              // box b was last read by the store of chunk j - 2
+              if (lane == 0) {
+                if (prev_stored)
+                  bulk_wait_group_read<1>();
+                else
+                  bulk_wait_group_read<0>();
+              }
+              __syncwarp();
+            }
+            got = __all_sync(0xffffffffu, got);
+            tc_wait_ld();
+            if (!got) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            tc::epilogue_f16_box(r, box, lane, x, p.N, p.epi, p.bias, has_c);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_cd, box, x, y);
+              bulk_commit_group();
+            }
+          }
+          prev_stored = live;
+          load_c(j + 2);
+        }
+        if (!ok) break;
+        tc_fence_before_sync();
+        if (CG == 2)
+          mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc * 8));
+        else
+          mbar_arrive(&tmem_empty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // Copies into and out of the boxes end before the CTA does.
+      if (lane == 0) {
+        for (int b = 0; b < 2; ++b)
+          if (c_pending & (1u << b))
+            mbar_wait(&cbar[b], (c_phase >> b) & 1u, p.timeout_ns, p.status);
+        bulk_wait_group<0>();
+      }
+      __syncwarp();
+    }
+    for (int t = unit0; t < p.num_tiles && ok && !(Out == kOutF16 && p.staged); t += units) {
       int m_blk, n_blk;
       tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
       const int row = m_blk * kTileM + static_cast<int>(rank) * kBlockM + ew * 32 + lane;
@@ -291,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-        for (int c = half * kChunksPerHalf; c < (half + 1) * kChunksPerHalf; ++c) {
+        for (int c = chunk_lo; c < chunk_hi; ++c) {
           uint32_t r[32];
           tmem_ld_32cols(tbase + c * 32, r);
           tc_wait_ld();
@@ -343,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int Stages, int CG, int Out>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
-  using L = TcSmem<BN, Stages, CG>;
-  CUtensorMap ta, tb;
+  using L = TcSmem<BN, Stages, CG, Out == kOutF16>;
+  CUtensorMap ta, tb, tcd;
   // A problem with fewer than 128 rows loads only its rows (rounded up to a
   // swizzle atom of 8): TMA is slow on boxes that are mostly out of bounds,
   // and the stale shared-memory rows below only feed accumulator rows >= M,
@@ -354,6 +543,16 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (e != cudaSuccess) return e;
   e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, L::kRowsB);
   if (e != cudaSuccess) return e;
+  // The staged epilogue moves C and D as 32 x 32 boxes, which needs 16-byte
+  // aligned rows (N % 8 == 0) and base; other shapes store straight from registers.
+  const bool staged = Out == kOutF16 && (a.N % 8) == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
+  if (staged) {
+    e = tc::make_f16_epi_map(&tcd, a.C, a.M, a.N);
+    if (e != cudaSuccess) return e;
+  } else {
+    tcd = ta;  // not read
+  }
 
   TcParams p;
   p.M = static_cast<int>(a.M);
@@ -372,6 +571,7 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
   p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB));
+  p.staged = staged ? 1 : 0;
 
   auto kern = gemm_f16_tc_kernel<BN, Stages, CG, Out>;
   int dev = 0;
@@ -384,7 +584,8 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L::kLaunchBytes;
   cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
   cfg.numAttrs = 0;
   if (CG == 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -415,7 +616,13 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (units > p.num_tiles) units = p.num_tiles;
   if (units < 1) units = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  // Programmatic dependent launch: this grid's CTAs may start (and set up
+  // barriers and tensor memory) while the previous kernel in the stream
+  // drains; the kernel waits for that kernel before touching global memory.
+  attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs += 1;
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tcd, p);
   count_launches(1);
   return e;
 }
@@ -434,6 +641,9 @@ cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   }
   if (plan.cta_group == 2) {
     if (plan.n_tile == 256 && plan.stages == 6) return run_tc<256, 6, 2, kOutF16>(a, plan);
+    // 224 columns: 19 column tiles cover N = 4096 (the last one partly), so a
+    // 4096^2 output is 16 x 19 = 304 pair tiles, four whole waves of 76 pairs
+    if (plan.n_tile == 224 && plan.stages == 6) return run_tc<224, 6, 2, kOutF16>(a, plan);
     if (plan.n_tile == 128 && plan.stages == 8) return run_tc<128, 8, 2, kOutF16>(a, plan);
     return cudaErrorNotSupported;
   }

@@ -39,7 +39,8 @@ struct TcVariant {
   int n_tile, stages, cta_group, cv_stages;
 };
 constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1, 0}, {128, 6, 1, 0}, {64, 8, 1, 0},
-                                        {256, 6, 2, 0}, {128, 8, 2, 0}};
+                                        {256, 6, 2, 0}, {224, 6, 2, 0}, {128, 8, 2, 0}};
+constexpr int kNumTcVariantsF16 = 6;
 constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
 // FP16 kernel in its exact-INT32 mode (three 128-column TMEM regions)
 constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {128, 8, 2, 0}};
@@ -58,7 +59,7 @@ struct TcFamily {
 };
 
 TcFamily tc_family(dg_dtype da, dg_dtype db) {
-  if (da == DG_F16 && db == DG_F16) return {kTcVariantsF16, 5, kTcThreads};
+  if (da == DG_F16 && db == DG_F16) return {kTcVariantsF16, kNumTcVariantsF16, kTcThreads};
   if (da == DG_I8 && db == DG_I8) return {kTcVariantsI8, 1, kConvThreads};
   if (da == DG_F16 && db == DG_E2M1) return {kTcVariantsE2M1, 3, kConvThreads};
   return {nullptr, 0, 0};
@@ -94,8 +95,12 @@ constexpr int kGemvSplits[] = {1,  2,  3,  4,  5,  6,  7,  8,   10,  12,  13,  1
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int tc_smem_bytes(dg_dtype da, dg_dtype db, const TcVariant& v) {
-  return tc_ring_bytes(da, db, v) + kTcBarrierBytes + 1024;
+// FP16-output runs of the FP16 x FP16 kernel add the staging boxes of its
+// epilogue: two 32 x 32 FP16 boxes for each of the eight epilogue warps.
+constexpr int kTcEpiStagingBytes = 8 * 2 * 32 * 32 * 2;
+
+int tc_smem_bytes(dg_dtype da, dg_dtype db, const TcVariant& v, bool staged) {
+  return tc_ring_bytes(da, db, v) + (staged ? kTcEpiStagingBytes : 0) + kTcBarrierBytes + 1024;
 }
 
 double sm_rate_flops_per_us(const dg_hw_desc& hw) {
@@ -112,7 +117,7 @@ double hbm_bytes_per_us(const dg_hw_desc& hw) {
 // GB300 at 4096^3 (measured time x wave efficiency): wider tiles and CTA pairs
 // move fewer operand bytes through L2 and shared memory per FLOP.
 double tc_tile_efficiency(int n_tile, int cta_group) {
-  if (cta_group == 2) return n_tile == 256 ? 0.86 : 0.63;
+  if (cta_group == 2) return n_tile >= 224 ? 0.86 : 0.63;
   switch (n_tile) {
     case 256: return 0.72;
     case 128: return 0.57;
@@ -131,7 +136,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
   const bool narrow = !(da == DG_F16 && db == DG_F16);
   if (widened && !narrow) return;
   TcFamily fam = widened ? (da == DG_I8 ? TcFamily{kTcVariantsI8Widened, 2, kTcThreads}
-                                        : TcFamily{kTcVariantsF16, 5, kTcThreads})
+                                        : TcFamily{kTcVariantsF16, kNumTcVariantsF16, kTcThreads})
                          : tc_family(da, db);
   if (!fam.v) {
     if (why) *why += "tensor-core kernel: dtype pair not compiled; ";
@@ -161,7 +166,9 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
       if (why) *why += name + ": M fits one CTA; ";
       continue;
     }
-    const int smem = tc_smem_bytes(ka, kb, v);
+    // the FP16 x FP16 kernel stages its FP16 output (not the INT32 mode)
+    const bool staged = ka == DG_F16 && kb == DG_F16 && da != DG_I8;
+    const int smem = tc_smem_bytes(ka, kb, v, staged);
     if (smem > hw.smem_per_block_optin) {
       if (why) *why += name + ": shared memory; ";
       continue;
@@ -415,7 +422,7 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
       return false;
     }
     const TcVariant* vs = i8 ? kTcVariantsI8Widened : kTcVariantsF16;
-    const int n = i8 ? 2 : 5;
+    const int n = i8 ? 2 : kNumTcVariantsF16;
     for (int vi = 0; vi < n; ++vi)
       if (vs[vi].n_tile == plan.n_tile && vs[vi].stages == plan.stages &&
           vs[vi].cta_group == plan.cta_group)

@@ -86,6 +86,64 @@ __device__ __forceinline__ void epilogue_f16_chunk(const uint32_t (&r)[32], int 
   }
 }
 
+// ------------------------------------------------------ staged (TMA) epilogue
+// A warp's 32 accumulator rows x 32 columns pass through a shared-memory box
+// that TMA fills with C and drains to D in whole lines, instead of each
+// thread touching 32 different rows of global memory per access.  The box is
+// 32 rows of 64 bytes in the 64-byte swizzle of the C/D tensor map: the
+// 16-byte piece q of row r sits at r*64 + ((q ^ ((r >> 1) & 3)) * 16).
+// Thread r of the warp touches row r only, and any 8 consecutive rows cover
+// all 32 banks, so its 16-byte accesses are free of bank conflicts.
+constexpr int kEpiBoxRows = 32;
+constexpr int kEpiBoxCols = 32;
+constexpr int kEpiBoxBytes = kEpiBoxRows * kEpiBoxCols * 2;
+
+__device__ __forceinline__ uint32_t epi_box_offset(int r, int q) {
+  return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+}
+
+// D = round_fp16(GELU?(alpha*acc + beta*C + bias)) for row `r` of a staged
+// box whose first column is D column col0; with `has_c` the box holds C on
+// entry.  D replaces C in the box.  Columns >= N (bias only) read 0; the
+// store's tensor map drops them.
+__device__ __forceinline__ void epilogue_f16_box(const uint32_t (&acc)[32], uint8_t* box, int r,
+                                                 int col0, int N, const Epi& epi,
+                                                 const __half* bias, bool has_c) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = epi.alpha * __uint_as_float(acc[i]);
+  if (has_c) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 cv = *reinterpret_cast<const uint4*>(box + epi_box_offset(r, q));
+      const __half2* ch = reinterpret_cast<const __half2*>(&cv);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float2 f = __half22float2(ch[h]);
+        v[q * 8 + 2 * h] = fmaf(epi.beta, f.x, v[q * 8 + 2 * h]);
+        v[q * 8 + 2 * h + 1] = fmaf(epi.beta, f.y, v[q * 8 + 2 * h + 1]);
+      }
+    }
+  }
+  if (epi.flags & kEpiBias) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < N) v[i] += __half2float(__ldg(bias + col0 + i));
+  }
+  if (epi.flags & kEpiGelu) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 ov;
+    __half2* oh = reinterpret_cast<__half2*>(&ov);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) oh[h] = __floats2half2_rn(v[q * 8 + 2 * h], v[q * 8 + 2 * h + 1]);
+    *reinterpret_cast<uint4*>(box + epi_box_offset(r, q)) = ov;
+  }
+}
+
 // ------------------------------------------------- exact INT32 from FP32 chunks
 // An INT8 x INT8 product is an integer of magnitude <= 2^14, so a sum of at
 // most 1024 of them is an integer of magnitude <= 2^24, exact in FP32.  The
@@ -198,7 +256,7 @@ inline cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, cons
     int box_rows, box_inner, dtype, swizzle;
     CUtensorMap map;
   };
-  constexpr int kCache = 16;
+  constexpr int kCache = 64;
   thread_local Entry cache[kCache];
   thread_local int used = 0, next = 0;
   for (int i = 0; i < used; ++i) {
@@ -234,6 +292,13 @@ inline cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, cons
   next = (next + 1) % kCache;
   if (used < kCache) ++used;
   return cudaSuccess;
+}
+
+// C / D of the staged epilogue: M x N FP16, row pitch N, boxes of 32 x 32 in
+// the 64-byte swizzle.  Needs N % 8 == 0 and a 16-byte aligned base.
+inline cudaError_t make_f16_epi_map(CUtensorMap* map, const void* base, int64_t M, int64_t N) {
+  return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, M, N, N * 2, kEpiBoxRows,
+                     kEpiBoxCols, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // K-major FP16 operand tile: box_rows x 64 elements, 128-byte swizzle.

@@ -68,7 +68,7 @@ def test_every_tensor_core_plan(dg):
     case = workloads.random_case(520, 1100, 700, epilogue="bias_gelu", alpha=1.5, beta=0.25,
                                  seed=5)
     tc = [p for p in _plans(dg, case) if p["kernel_name"] == "tc"]
-    assert {p["n_tile"] for p in tc} == {64, 128, 256}
+    assert {p["n_tile"] for p in tc} == {64, 128, 224, 256}
     for p in tc:
         for grid in (p["grid"], 7, 1):   # persistent CTAs walking several tiles each
             q = dict(p, grid=grid)
@@ -115,6 +115,41 @@ def test_output_canary_untouched(dg):
         assert np.all(tail == np.float16(-7.5))
 
 
+def _run_at_offset(dg, case, off, guard=64, plan=None):
+    """Runs `case` with C/D placed `off` elements into a larger buffer whose
+    `guard` elements before and after are filled with a canary."""
+    n = case.M * case.N
+    buf = torch.full((off + n + guard,), -7.5, dtype=torch.float16, device="cuda")
+    A, B, C0, bias, _ = to_device(case)
+    C = buf[off:off + n].view(case.M, case.N)
+    C.copy_(C0)
+    dg.gemm(A, B, C, K=case.K, bias=bias, alpha=case.alpha, beta=case.beta,
+            epilogue=case.epilogue, plan=plan)
+    dg.check_status()
+    host = buf.cpu().numpy()
+    assert np.all(host[:off] == np.float16(-7.5)) and np.all(host[off + n:] == np.float16(-7.5))
+    return C.cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", [(300, 520, 200), (256, 1000, 640), (129, 72, 1000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_staged_epilogue_at_offset(dg, shape):
+    # D 16 bytes into a larger buffer (aligned for TMA, not to a line): the
+    # boxes write exactly the M x N elements, none of the guards around them.
+    case = workloads.random_case(*shape, epilogue="bias_gelu", alpha=0.75, beta=-0.5, seed=11)
+    got = _run_at_offset(dg, case, 8)
+    assert_parity(case, got)
+
+
+def test_every_tensor_core_plan_without_c(dg):
+    # beta = 0: the staged epilogue stores only (no C loads)
+    case = workloads.random_case(700, 904, 520, epilogue="bias_gelu", alpha=-1.25, seed=12)
+    for p in [p for p in _plans(dg, case) if p["kernel_name"] == "tc"]:
+        got, tail = run_case(dg, case, plan=p, canary=64)
+        assert_parity(case, got)
+        assert np.all(tail == np.float16(-7.5))
+
+
 def test_padded_leading_dimensions(dg):
     case = workloads.random_case(200, 300, 100, lda=160, ldb=136, beta=0.5, seed=4,
                                  pad=float("nan"))
@@ -142,6 +177,35 @@ def test_closed_forms_on_device(dg):
     case.B = np.eye(192, dtype=np.float16)
     got, _ = run_case(dg, case)
     assert np.array_equal(got, case.A[:, :192])
+
+
+def test_back_to_back_kernels_keep_stream_order(dg):
+    # Tensor-core launches overlap the previous kernel's drain (programmatic
+    # dependent launch) and wait for it before touching global memory.  Three
+    # launches with no host synchronisation: step 2 reads step 1's output
+    # (read after write) and overwrites step 1's input (write after read);
+    # step 3 reads step 2's output and updates its own C in place.
+    M, K = 640, 1024
+    base = [workloads.random_case(M, K, K, seed=31 + i) for i in range(3)]
+    P0 = base[0].A.copy()
+    R0 = np.random.default_rng(7).standard_normal((M, K)).astype(np.float16)
+    dev = "cuda:0"
+    P = torch.from_numpy(P0).to(dev)
+    Q = torch.zeros(M, K, dtype=torch.float16, device=dev)
+    R = torch.from_numpy(R0).to(dev)
+    W = [torch.from_numpy(c.B).to(dev) for c in base]
+    for _ in range(3):   # repeated, so later launches also overlap earlier ones
+        P.copy_(torch.from_numpy(P0).to(dev))
+        R.copy_(torch.from_numpy(R0).to(dev))
+        dg.gemm(P, W[0], Q)                   # Q = P . W0^T
+        dg.gemm(Q, W[1], P)                   # P = Q . W1^T
+        dg.gemm(P, W[2], R, beta=0.5)         # R = P . W2^T + 0.5 R
+    dg.check_status()
+    q, p, r = Q.cpu().numpy(), P.cpu().numpy(), R.cpu().numpy()
+    steps = [(P0, q, None, 0.0), (q, p, None, 0.0), (p, r, R0, 0.5)]
+    for (a, got, c, beta), cs in zip(steps, base):
+        cs.A, cs.C, cs.beta = a, c, beta
+        assert_parity(cs, got)
 
 
 def test_side_stream(dg):
@@ -277,6 +341,7 @@ def test_w4a16_every_plan(dg):
                                  seed=5)
     plans = [p for p in _plans(dg, case) if p["kernel_name"] in ("tc", "tc_widened")]
     assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc"} == {64, 128, 256}
+    assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc_widened"} >= {128, 224, 256}
     assert {p["cta_group"] for p in plans if p["kernel_name"] == "tc_widened"} == {1, 2}
     for p in plans:
         got, _ = run_case(dg, case, plan=p)

@@ -22,7 +22,9 @@ GB300 = dict(sm_count=152, cc_major=10, cc_minor=3, smem_per_block_optin=232448,
 
 # Compiled FP16 tensor-core variants: (N_tile, stages, CTAs per tile); M_tile
 # 128 per CTA, K_tile 64, 384 threads.  A CTA pair holds half of B per CTA.
-TC_VARIANTS = [(256, 4, 1), (128, 6, 1), (64, 8, 1), (256, 6, 2), (128, 8, 2)]
+TC_VARIANTS = [(256, 4, 1), (128, 6, 1), (64, 8, 1), (256, 6, 2), (224, 6, 2), (128, 8, 2)]
+# FP16 output passes through two 32 x 32 FP16 staging boxes per epilogue warp (8 warps)
+EPI_STAGING = 8 * 2 * 32 * 32 * 2
 
 
 @pytest.fixture(scope="module")
@@ -33,8 +35,9 @@ def dg():
     return dg
 
 
-def tc_smem(n_tile, stages, cg=1):
-    return stages * (128 * 64 * 2 + (n_tile // cg) * 64 * 2) + 512 + 1024
+def tc_smem(n_tile, stages, cg=1, staged=True):
+    return (stages * (128 * 64 * 2 + (n_tile // cg) * 64 * 2) + (EPI_STAGING if staged else 0)
+            + 512 + 1024)
 
 
 def tc_feasible(M, N, hw, target):
@@ -229,4 +232,6 @@ def test_converting_kernel_plans(dg, pair, shape):
     for p in plans:
         if p["kernel_name"] == "tc_widened":
             assert p["threads"] == 384
-            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], p["cta_group"])
+            # INT8 runs the FP16 kernel in its exact INT32 mode, without staging
+            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], p["cta_group"],
+                                              staged=pair[0] != "i8")
