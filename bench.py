@@ -173,9 +173,9 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
+def recorded_traffic(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current sources of that kernel; else None."""
+    the current sources of that kernel and on this workload; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -183,6 +183,8 @@ def recorded_traffic(kernel):
         d = json.load(f)
     e = d.get(kernel)
     if not e or e.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    if e.get("workload") != workload:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -373,7 +375,7 @@ def run_dg(args, world, rank, local):
     kname = kernel_name(plan, base)
     roof["kernel"] = kname
     roof["kernel_avg_us"] = round(kern_avg_ms * 1e3, 2)
-    roof["traffic"] = recorded_traffic(kname)
+    roof["traffic"] = recorded_traffic(kname, name)
     roof["algorithmic_bytes"] = algorithmic_bytes(base)
     roof["algorithmic_flops"] = flops
 
