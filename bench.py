@@ -38,6 +38,7 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 L2_BYTES = 129 * 1000 * 1000
+RAMP_S = 0.2  # untimed clock ramp before the warm-up steps
 
 
 # --------------------------------------------------------------------------- clocks
@@ -265,6 +266,14 @@ def run_dg(args, world, rank, local):
         dg.gemm(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
                 epilogue=base.epilogue, stream=st, plan=forced)
 
+    # An idle GPU needs a few tens of milliseconds of load before its clocks
+    # settle: run the step untimed for RAMP_S before the W warm-up steps.
+    ramp_steps, t_ramp = 0, time.perf_counter()
+    while time.perf_counter() - t_ramp < RAMP_S:
+        for i in range(8):
+            step(i)
+        torch.cuda.synchronize(dev)
+        ramp_steps += 8
     for i in range(args.warmup):
         step(i)
     dg.check_status(stream)
@@ -394,6 +403,7 @@ def run_dg(args, world, rank, local):
         "data": "synthetic (seeded, recipe in workloads.py)",
         "config": {"workload": desc, "name": name, "M": base.M, "N": base.N, "K": base.K,
                    "alpha": base.alpha, "beta": base.beta, "epilogue": base.epilogue,
+                   "ramp": "%d untimed steps (%.1f s) before the warm-up" % (ramp_steps, RAMP_S),
                    "timing": ("CUDA-graph replay of the K steps" if args.graph else
                               "eager back-to-back launches") +
                    ", CUDA events around the K steps, per launch = total / K",
