@@ -325,13 +325,15 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
     s = get_wide_workspace(dev, stream, a_elems + N * ldw, &wide);
     if (s != DG_OK) return s;
     GemmArgs w = a;
+    WidenJob jobs[2];
+    int njobs = 0;
     if (da == DG_I8) {
-      e = launch_widen(DG_I8, A, M, K, lda, wide, stream, a.sm_count);
-      if (e != cudaSuccess) return fail_cuda(e, "widening launch");
+      jobs[njobs++] = WidenJob{DG_I8, A, M, lda, wide};
       w.A = wide;
       w.lda = ldw;
     }
-    e = launch_widen(db, B, N, K, ldb, wide + a_elems, stream, a.sm_count);
+    jobs[njobs++] = WidenJob{db, B, N, ldb, wide + a_elems};
+    e = launch_widen(jobs, njobs, K, stream, a.sm_count);
     if (e != cudaSuccess) return fail_cuda(e, "widening launch");
     w.B = wide + a_elems;
     w.ldb = ldw;

@@ -234,11 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a dependent of the previous kernel in the stream: the set-up
+  // above touched only on-chip state; global memory waits for that kernel.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (elect_one_lane()) {
-      const uint64_t pol = policy_evict_normal();
+      // operand tiles are read again by other tiles: they outrank C and D in L2
+      const uint64_t pol = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
@@ -265,6 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Every operand load is issued: a kernel launched after this one may be
+      // scheduled now (not earlier: its blocks could wait beside this CTA).
+      grid_launch_dependents();
       if (!ok) {
         *abort_flag = 1;
         const int64_t first = issued > SIn ? issued - SIn : 0;
@@ -454,9 +461,9 @@ cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
   }
   int grid = plan.grid > 0 ? plan.grid : a.sm_count;
   if (grid > p.num_tiles) grid = p.num_tiles;
-  kern<<<grid, kThreads, L::kLaunchBytes, a.stream>>>(ta, tb, p);
+  e = launch_dependent(kern, dim3(grid), dim3(kThreads), L::kLaunchBytes, a.stream, ta, tb, p);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

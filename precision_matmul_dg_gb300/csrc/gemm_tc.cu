@@ -75,20 +75,20 @@ struct TcParams {
 // widened to FP16 (K accumulated in exact FP32 chunks, INT32 running sum).
 enum : int { kOutF16 = 0, kOutI32 = 1 };
 
-// Shared memory: the operand ring, then (FP16 output) two staging boxes per
-// epilogue warp, then the barriers.
-template <int BN, int Stages, int CG, bool Staged>
+// Shared memory: the operand ring, then two staging boxes per epilogue warp,
+// then the barriers.
+template <int BN, int Stages, int CG>
 struct TcSmem {
   static constexpr int kRowsB = BN / CG;  // B rows this CTA loads
   static constexpr int kTileBytesB = kRowsB * kBlockK * 2;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + Stages * kTileBytesA;
   static constexpr int kOffEpi = kOffB + Stages * kTileBytesB;
-  static constexpr int kEpiBytes = Staged ? kEpiWarps * 2 * tc::kEpiBoxBytes : 0;
+  static constexpr int kEpiBytes = kEpiWarps * 2 * tc::kEpiBoxBytes;
   static constexpr int kOffBar = kOffEpi + kEpiBytes;
   // full[Stages], empty[Stages], tmem_full[2], tmem_empty[2], drain, then
-  // (Staged) one C-load barrier per staging box
-  static constexpr int kNumBars = 2 * Stages + 5 + (Staged ? 2 * kEpiWarps : 0);
+  // one C-load barrier per staging box
+  static constexpr int kNumBars = 2 * Stages + 5 + 2 * kEpiWarps;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
@@ -144,9 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_cd, const TcParams p) {
-  using L = TcSmem<BN, Stages, CG, Out == kOutF16>;
-  // two FP32 accumulators, plus the INT32 running sums in the integer mode
-  constexpr int kColsNeeded = (Out == kOutI32 ? 3 : 2) * BN;
+  using L = TcSmem<BN, Stages, CG>;
+  // two FP32 accumulators (the INT32 mode keeps its running sums in registers)
+  constexpr int kColsNeeded = 2 * BN;
   constexpr int kTmemCols = kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512);
   static_assert(kColsNeeded <= 512, "tensor memory");
   // K blocks per accumulation chunk: the whole K, or exact-FP32 chunks
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_full = bars + 2 * Stages;
   uint64_t* tmem_empty = bars + 2 * Stages + 2;
   uint64_t* drain_bar = bars + 2 * Stages + 4;
-  uint64_t* epi_bar = bars + 2 * Stages + 5;  // [kEpiWarps][2] when staged
+  uint64_t* epi_bar = bars + 2 * Stages + 5;  // [kEpiWarps][2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
 
@@ -187,15 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tmem_empty[b], CG * kEpiWarps * 32);  // every epilogue thread of the pair
     }
     mbar_init(drain_bar, 1);
-    if (Out == kOutF16)
-      for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&epi_bar[b], 1);
+    for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&epi_bar[b], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    if (Out == kOutF16 && p.staged) tma_prefetch_desc(&tmap_cd);
+    if (p.staged) tma_prefetch_desc(&tmap_cd);
   }
   if (warp == 2) {
     if (CG == 2)
@@ -213,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // one in the stream may still be finishing.  Everything above touched only
   // this CTA's (or pair's) own on-chip state; global memory waits for it.
   grid_dependency_wait();
-  if (threadIdx.x == 0) grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -267,6 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (first_c && ok && issued < Stages) initial_c();
+      // Every operand load is issued: a kernel launched after this one may be
+      // scheduled now (not earlier: small blocks of another kernel that fit
+      // beside this CTA would wait on its SM for the whole main loop).
+      grid_launch_dependents();
       if (!ok) {
         *abort_flag = 1;
         if (CG == 1 || leader) {
@@ -356,10 +358,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int chunk_hi = half == 0 ? (kChunks + 1) / 2 : kChunks;
     const uint32_t empty0 = CG == 2 ? mapa_shared(smem_addr(&tmem_empty[0]), 0) : 0u;
     const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
-    const uint32_t sums = tmem_base + lane_base + 2 * BN;  // INT32 running sums (Out == I32)
     int acc = 0;
     uint32_t acc_phase = 0;
-    if (Out == kOutF16 && p.staged) {
+    if (Out == kOutI32) {
+      // Exact INT32 (INT8 operands widened to FP16).  Each K chunk of at most
+      // 1024 accumulates exact integers in FP32 (|chunk sum| <= 1024 * 2^14 =
+      // 2^24); the warp converts them and adds them to running INT32 sums in
+      // registers (wrapping mod 2^32), and after the tile's last chunk writes
+      // D = alpha * sum + beta * C (mod 2^32) as 32 x 16 INT32 boxes through
+      // the staging buffers (or straight from registers without staging).
+      static_assert(Out != kOutI32 || BN % 64 == 0, "INT32 mode: equal chunks per warp");
+      constexpr int kCpw = BN / 64;  // 32-column chunks per warp
+      const int c_lo = half * kCpw;
+      const int wi = warp - kEpiWarp0;
+      uint8_t* boxes = smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes;
+      const uint32_t al = static_cast<uint32_t>(p.alpha_i), be = static_cast<uint32_t>(p.beta_i);
+      uint32_t sum[kCpw][32];
+      int nstores = 0;  // stores issued; store i goes through box i & 1
+      for (int t = unit0; t < p.num_tiles && ok; t += units) {
+        int m_blk, n_blk;
+        tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
+        const int y = m_blk * kTileM + static_cast<int>(rank) * kBlockM + ew * 32;
+        for (int ch = 0; ch < num_chunks; ++ch) {
+          const bool ready =
+              !aborted(abort_flag) &&
+              mbar_wait_sleepy(&tmem_full[acc], acc_phase, p.timeout_ns, p.status, 256);
+          if (!__all_sync(0xffffffffu, ready)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
+#pragma unroll
+          for (int cl = 0; cl < kCpw; ++cl) {
+            uint32_t r[32];
+            tmem_ld_32cols(tbase + (c_lo + cl) * 32, r);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t v = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+              sum[cl][i] = ch == 0 ? v : sum[cl][i] + v;
+            }
+          }
+          tc_fence_before_sync();
+          if (CG == 2)
+            mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc * 8));
+          else
+            mbar_arrive(&tmem_empty[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        const int row = y + lane;
+        const int32_t* crow = static_cast<const int32_t*>(p.CD) + static_cast<int64_t>(row) * p.N;
+#pragma unroll
+        for (int cl = 0; cl < kCpw; ++cl) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int x = n_blk * BN + (c_lo + cl) * 32 + hh * 16;
+            if (x >= p.N || y >= p.M) continue;  // warp-uniform: the box is wholly outside D
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = al * sum[cl][hh * 16 + i];
+            if (be != 0u && row < p.M) {
+              if (x + 16 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const uint4 c = *reinterpret_cast<const uint4*>(crow + x + q * 4);
+                  o[q * 4 + 0] += be * c.x;
+                  o[q * 4 + 1] += be * c.y;
+                  o[q * 4 + 2] += be * c.z;
+                  o[q * 4 + 3] += be * c.w;
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (x + i < p.N) o[i] += be * static_cast<uint32_t>(crow[x + i]);
+              }
+            }
+            if (p.staged) {
+              uint8_t* box = boxes + (nstores & 1) * tc::kEpiBoxBytes;
+              if (lane == 0) bulk_wait_group_read<1>();  // box's previous store has read it
+              __syncwarp();
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(box + tc::epi_box_offset(lane, q)) =
+                    make_uint4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmap_cd, box, x, y);
+                bulk_commit_group();
+              }
+              ++nstores;
+            } else if (row < p.M) {
+              int32_t* drow = static_cast<int32_t*>(p.CD) + static_cast<int64_t>(row) * p.N;
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (x + i < p.N) drow[x + i] = static_cast<int32_t>(o[i]);
+            }
+          }
+        }
+      }
+      if (lane == 0) bulk_wait_group<0>();  // stores end before the CTA does
+      __syncwarp();
+    } else if (p.staged) {
       // Staged epilogue.  The warp's chunks form one stream over its tiles
       // (epi_box); chunk j of the stream goes through box j & 1 of the warp's
       // two boxes.  C of chunks 0 and 1 is loaded by the producer; lane 0
@@ -466,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-    for (int t = unit0; t < p.num_tiles && ok && !(Out == kOutF16 && p.staged); t += units) {
+    for (int t = unit0; t < p.num_tiles && ok && Out == kOutF16 && !p.staged; t += units) {
       int m_blk, n_blk;
       tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
       const int row = m_blk * kTileM + static_cast<int>(rank) * kBlockM + ew * 32 + lane;
@@ -485,14 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32cols(tbase + c * 32, r);
           tc_wait_ld();
           const int col0 = n_blk * BN + c * 32;
-          if (Out == kOutF16) {
-            if (col0 < p.N)
-              tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, static_cast<__half*>(p.CD),
-                                     p.bias);
-          } else {
-            tc::flush_i32_piece(r, sums + c * 32, ch == 0, ch + 1 == num_chunks, row, col0, p.M,
-                                p.N, p.alpha_i, p.beta_i, p.CD);
-          }
+          if (col0 < p.N)
+            tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, static_cast<__half*>(p.CD),
+                                   p.bias);
         }
         tc_fence_before_sync();
         if (CG == 2)
@@ -532,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int Stages, int CG, int Out>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
-  using L = TcSmem<BN, Stages, CG, Out == kOutF16>;
+  using L = TcSmem<BN, Stages, CG>;
   CUtensorMap ta, tb, tcd;
   // A problem with fewer than 128 rows loads only its rows (rounded up to a
   // swizzle atom of 8): TMA is slow on boxes that are mostly out of bounds,
@@ -543,12 +644,14 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (e != cudaSuccess) return e;
   e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, L::kRowsB);
   if (e != cudaSuccess) return e;
-  // The staged epilogue moves C and D as 32 x 32 boxes, which needs 16-byte
-  // aligned rows (N % 8 == 0) and base; other shapes store straight from registers.
-  const bool staged = Out == kOutF16 && (a.N % 8) == 0 &&
+  // The staged epilogue moves D (and FP16 C) as boxes of 64-byte rows, which
+  // needs 16-byte aligned rows (N % 8 == 0 for FP16, N % 4 == 0 for INT32)
+  // and base; other shapes store straight from registers.
+  const bool staged = (a.N % (Out == kOutF16 ? 8 : 4)) == 0 &&
                       (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
   if (staged) {
-    e = tc::make_f16_epi_map(&tcd, a.C, a.M, a.N);
+    e = Out == kOutF16 ? tc::make_f16_epi_map(&tcd, a.C, a.M, a.N)
+                       : tc::make_i32_epi_map(&tcd, a.C, a.M, a.N);
     if (e != cudaSuccess) return e;
   } else {
     tcd = ta;  // not read
@@ -634,9 +737,10 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
 // selects the exact INT32 output of widened INT8 operands.
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (a.exact_i32) {
-    if (plan.n_tile != 128) return cudaErrorNotSupported;
-    if (plan.cta_group == 2 && plan.stages == 8) return run_tc<128, 8, 2, kOutI32>(a, plan);
-    if (plan.cta_group == 1 && plan.stages == 6) return run_tc<128, 6, 1, kOutI32>(a, plan);
+    if (plan.n_tile == 192 && plan.cta_group == 2 && plan.stages == 6)
+      return run_tc<192, 6, 2, kOutI32>(a, plan);
+    if (plan.n_tile == 128 && plan.cta_group == 1 && plan.stages == 6)
+      return run_tc<128, 6, 1, kOutI32>(a, plan);
     return cudaErrorNotSupported;
   }
   if (plan.cta_group == 2) {

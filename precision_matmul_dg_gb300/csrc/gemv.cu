@@ -82,6 +82,7 @@ __device__ __forceinline__ void write_out(const GemvParams& p, int m, int j, flo
 
 template <int MROWS>
 __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const GemvParams p) {
+  grid_dependency_wait();  // launched as a dependent of the previous kernel
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * kGemvWarps + warp;
@@ -155,6 +156,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
 
 #pragma unroll
   for (int m = 0; m < MROWS; ++m) acc[m] = warp_sum(acc[m]);
+  // The next kernel's blocks may be scheduled now.  Not earlier: they would
+  // share the SMs with this streaming pass while waiting for it to end.
+  grid_launch_dependents();
 
   if (p.split_k == 1) {
     if (lane == 0 && j < p.N) {
@@ -199,6 +203,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
 // K == 0: D = epilogue(beta * C), no product term.
 __global__ void epilogue_only_kernel(int64_t M, int64_t N, __half* CD, const __half* bias,
                                      Epi epi) {
+  grid_dependency_wait();  // launched as a dependent of the previous kernel
   const int64_t total = M * N;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -211,6 +216,7 @@ __global__ void epilogue_only_kernel(int64_t M, int64_t N, __half* CD, const __h
 
 // K == 0 on the integer path: D = beta * C (mod 2^32).
 __global__ void epilogue_only_i32_kernel(int64_t total, int32_t* CD, int32_t beta) {
+  grid_dependency_wait();  // launched as a dependent of the previous kernel
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint32_t c = (beta != 0) ? static_cast<uint32_t>(CD[i]) : 0u;
@@ -262,16 +268,13 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
   const dim3 grid(static_cast<unsigned>((a.N + kGemvWarps - 1) / kGemvWarps),
                   static_cast<unsigned>(plan.split_k));
   const dim3 block(kGemvWarps * 32);
-  if (a.M <= 1)
-    gemv_splitk_kernel<1><<<grid, block, 0, a.stream>>>(p);
-  else if (a.M <= 2)
-    gemv_splitk_kernel<2><<<grid, block, 0, a.stream>>>(p);
-  else if (a.M <= 4)
-    gemv_splitk_kernel<4><<<grid, block, 0, a.stream>>>(p);
-  else
-    gemv_splitk_kernel<kGemvMaxM><<<grid, block, 0, a.stream>>>(p);
+  auto kern = a.M <= 1   ? gemv_splitk_kernel<1>
+              : a.M <= 2 ? gemv_splitk_kernel<2>
+              : a.M <= 4 ? gemv_splitk_kernel<4>
+                         : gemv_splitk_kernel<kGemvMaxM>;
+  const cudaError_t e = launch_dependent(kern, grid, block, 0, a.stream, p);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_epilogue_only(const GemmArgs& a) {
@@ -281,16 +284,18 @@ cudaError_t launch_epilogue_only(const GemmArgs& a) {
   const int64_t cap = static_cast<int64_t>(a.sm_count) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  cudaError_t e;
   if (a.dtype_a == DG_I8) {
-    epilogue_only_i32_kernel<<<static_cast<unsigned>(blocks), threads, 0, a.stream>>>(
-        total, static_cast<int32_t*>(a.C), static_cast<int32_t>(a.beta));
+    e = launch_dependent(epilogue_only_i32_kernel, dim3(static_cast<unsigned>(blocks)),
+                         dim3(threads), 0, a.stream, total, static_cast<int32_t*>(a.C),
+                         static_cast<int32_t>(a.beta));
   } else {
-    epilogue_only_kernel<<<static_cast<unsigned>(blocks), threads, 0, a.stream>>>(
-        a.M, a.N, static_cast<__half*>(a.C), static_cast<const __half*>(a.bias),
-        Epi{a.alpha, a.beta, a.epi});
+    e = launch_dependent(epilogue_only_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads),
+                         0, a.stream, a.M, a.N, static_cast<__half*>(a.C),
+                         static_cast<const __half*>(a.bias), Epi{a.alpha, a.beta, a.epi});
   }
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns) {

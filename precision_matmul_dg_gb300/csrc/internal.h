@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "dg.h"
 
@@ -15,6 +16,27 @@ namespace dg {
 enum : int { kEpiBias = 1, kEpiGelu = 2 };
 
 // Everything a launcher needs to run one GEMM, already validated.
+// Launches `kern` with programmatic stream serialization: its CTAs may be
+// scheduled (and run their set-up) while the previous kernel in the stream
+// drains.  Every kernel launched this way executes griddepcontrol.wait
+// before its first global-memory access, which waits for that kernel to
+// complete and its memory to be visible.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 struct GemmArgs {
   int64_t M, N, K;
   dg_dtype dtype_a, dtype_b;
@@ -57,10 +79,17 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
 cudaError_t launch_epilogue_only(const GemmArgs& a);
 
 // Widening pre-pass (widen.cu): int8 or packed-E2M1 rows -> FP16 rows with
-// leading dimension widened_ld(K).
+// leading dimension widened_ld(K).  One or two operands (A and B of an INT8
+// product) per call, in one launch when both are dense and of one type.
 int64_t widened_ld(int64_t K);
-cudaError_t launch_widen(dg_dtype dtype, const void* src, int64_t rows, int64_t K, int64_t ld_src,
-                         __half* dst, cudaStream_t stream, int sm_count);
+struct WidenJob {
+  dg_dtype dtype;
+  const void* src;
+  int64_t rows, ld_src;  // ld_src in elements (codes for E2M1)
+  __half* dst;
+};
+cudaError_t launch_widen(const WidenJob* jobs, int njobs, int64_t K, cudaStream_t stream,
+                         int sm_count);
 cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns);
 
 // Workspace sizes a GEMV plan needs.

@@ -42,8 +42,9 @@ constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1, 0}, {128, 6, 1, 0}, {64, 8, 
                                         {256, 6, 2, 0}, {224, 6, 2, 0}, {128, 8, 2, 0}};
 constexpr int kNumTcVariantsF16 = 6;
 constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
-// FP16 kernel in its exact-INT32 mode (three 128-column TMEM regions)
-constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {128, 8, 2, 0}};
+// FP16 kernel in its exact-INT32 mode (two FP32 chunk accumulators in TMEM,
+// running INT32 sums in registers: N_tile a multiple of 64, at most 192)
+constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {192, 6, 2, 0}};
 constexpr TcVariant kTcVariantsE2M1[] = {{256, 6, 1, 2}, {128, 8, 1, 3}, {64, 8, 1, 4}};
 constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;
@@ -79,9 +80,9 @@ int tc_ring_bytes(dg_dtype da, dg_dtype db, const TcVariant& v) {
   return v.stages * (in_a + in_b) + v.cv_stages * cv;
 }
 
-// Tensor-memory columns: two FP32 accumulators, plus INT32 running sums on
-// the integer path.
-int tc_tmem_cols(dg_dtype da, int n_tile) { return (da == DG_I8 ? 3 : 2) * n_tile; }
+// Tensor-memory columns: two FP32 accumulators, plus INT32 running sums in the
+// converting INT8 kernel (the FP16 kernel's INT32 mode keeps them in registers).
+int tc_tmem_cols(bool conv_i8, int n_tile) { return (conv_i8 ? 3 : 2) * n_tile; }
 
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
@@ -117,7 +118,7 @@ double hbm_bytes_per_us(const dg_hw_desc& hw) {
 // GB300 at 4096^3 (measured time x wave efficiency): wider tiles and CTA pairs
 // move fewer operand bytes through L2 and shared memory per FLOP.
 double tc_tile_efficiency(int n_tile, int cta_group) {
-  if (cta_group == 2) return n_tile >= 224 ? 0.86 : 0.63;
+  if (cta_group == 2) return n_tile >= 224 ? 0.86 : (n_tile >= 192 ? 0.80 : 0.63);
   switch (n_tile) {
     case 256: return 0.72;
     case 128: return 0.57;
@@ -166,14 +167,14 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
       if (why) *why += name + ": M fits one CTA; ";
       continue;
     }
-    // the FP16 x FP16 kernel stages its FP16 output (not the INT32 mode)
-    const bool staged = ka == DG_F16 && kb == DG_F16 && da != DG_I8;
+    // the FP16 x FP16 kernel stages its output (FP16, or INT32 for widened INT8)
+    const bool staged = ka == DG_F16 && kb == DG_F16;
     const int smem = tc_smem_bytes(ka, kb, v, staged);
     if (smem > hw.smem_per_block_optin) {
       if (why) *why += name + ": shared memory; ";
       continue;
     }
-    if (tc_tmem_cols(da, v.n_tile) > hw.tmem_cols) {
+    if (tc_tmem_cols(da == DG_I8 && !widened, v.n_tile) > hw.tmem_cols) {
       if (why) *why += name + ": tensor memory; ";
       continue;
     }

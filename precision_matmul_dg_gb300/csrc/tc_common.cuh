@@ -30,6 +30,30 @@ __device__ __forceinline__ void tile_coords(int t, int num_m_blocks, int num_n_b
   n_blk = r / gm;
 }
 
+// v[i] += bias[col0 + i] for the columns < N: four 16-byte loads (the same
+// address across the warp) when the 32 values are in range and aligned.
+__device__ __forceinline__ void add_bias_chunk(float (&v)[32], const __half* bias, int col0,
+                                               int N) {
+  const __half* b = bias + col0;
+  if (col0 + 32 <= N && (reinterpret_cast<uintptr_t>(b) & 15) == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 bv = __ldg(reinterpret_cast<const uint4*>(b) + q);
+      const __half2* bh = reinterpret_cast<const __half2*>(&bv);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float2 f = __half22float2(bh[h]);
+        v[q * 8 + 2 * h] += f.x;
+        v[q * 8 + 2 * h + 1] += f.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < N) v[i] += __half2float(__ldg(b + i));
+  }
+}
+
 // Fused FP16 epilogue for one thread's row and 32 consecutive columns:
 // D = round_fp16(GELU?(alpha*acc + beta*C + bias)).  C and D share `cd`
 // (leading dimension N).  Rows >= M and columns >= N are skipped.
@@ -61,28 +85,25 @@ __device__ __forceinline__ void epilogue_f16_chunk(const uint32_t (&r)[32], int 
         if (col0 + i < N) v[i] = fmaf(epi.beta, __half2float(drow[col0 + i]), v[i]);
     }
   }
-  if (epi.flags & kEpiBias) {
+  if (epi.flags & kEpiBias) add_bias_chunk(v, bias, col0, N);
+  const bool gelu = (epi.flags & kEpiGelu) != 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < N) v[i] += __half2float(__ldg(bias + col0 + i));
-  }
-  if (epi.flags & kEpiGelu) {
+  for (int q = 0; q < 4; ++q) {  // 8 values at a time: activation, rounding, store
+    if (gelu) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-  }
-  if (full) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
+      for (int i = 0; i < 8; ++i) v[q * 8 + i] = gelu_erf(v[q * 8 + i]);
+    }
+    if (full) {
       uint4 ov;
       __half2* oh = reinterpret_cast<__half2*>(&ov);
 #pragma unroll
       for (int h = 0; h < 4; ++h) oh[h] = __floats2half2_rn(v[q * 8 + 2 * h], v[q * 8 + 2 * h + 1]);
       *reinterpret_cast<uint4*>(drow + col0 + q * 8) = ov;
-    }
-  } else {
+    } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < N) drow[col0 + i] = __float2half_rn(v[i]);
+      for (int i = 0; i < 8; ++i)
+        if (col0 + q * 8 + i < N) drow[col0 + q * 8 + i] = __float2half_rn(v[q * 8 + i]);
+    }
   }
 }
 
@@ -125,17 +146,14 @@ __device__ __forceinline__ void epilogue_f16_box(const uint32_t (&acc)[32], uint
       }
     }
   }
-  if (epi.flags & kEpiBias) {
+  if (epi.flags & kEpiBias) add_bias_chunk(v, bias, col0, N);
+  const bool gelu = (epi.flags & kEpiGelu) != 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < N) v[i] += __half2float(__ldg(bias + col0 + i));
-  }
-  if (epi.flags & kEpiGelu) {
+  for (int q = 0; q < 4; ++q) {  // 8 values at a time: activation, rounding, staging
+    if (gelu) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
-  }
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
+      for (int i = 0; i < 8; ++i) v[q * 8 + i] = gelu_erf(v[q * 8 + i]);
+    }
     uint4 ov;
     __half2* oh = reinterpret_cast<__half2*>(&ov);
 #pragma unroll
@@ -299,6 +317,14 @@ inline cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, cons
 inline cudaError_t make_f16_epi_map(CUtensorMap* map, const void* base, int64_t M, int64_t N) {
   return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, M, N, N * 2, kEpiBoxRows,
                      kEpiBoxCols, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// D of the INT32 output: M x N INT32, row pitch N, boxes of 32 rows x 16
+// columns (64-byte rows, the same 64-byte swizzle).  Needs N % 4 == 0 and a
+// 16-byte aligned base.
+inline cudaError_t make_i32_epi_map(CUtensorMap* map, const void* base, int64_t M, int64_t N) {
+  return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_INT32, base, M, N, N * 4, kEpiBoxRows,
+                     kEpiBoxCols / 2, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // K-major FP16 operand tile: box_rows x 64 elements, 128-byte swizzle.

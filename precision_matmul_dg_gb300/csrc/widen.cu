@@ -16,6 +16,7 @@
 #include <stdint.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dg {
 namespace {
@@ -37,57 +38,127 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return o;
 }
 
-// int8 [rows x ld_src] -> fp16 [rows x ld_dst]; 16 source bytes per thread step.
-// Reads whole 16-byte groups up to the row pitch (a multiple of 16 bytes);
-// columns >= K of the copy are never read by the GEMM.
-__global__ void widen_i8_kernel(const int8_t* __restrict__ src, int64_t rows, int64_t groups,
-                                int64_t ld_src, __half* __restrict__ dst, int64_t ld_dst) {
-  const int64_t total = rows * groups;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / groups, g = i - r * groups;
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src + r * ld_src + g * 16));
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    uint4 o[2];
-    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+// Streaming 16-byte load that does not allocate in L1 (each byte is read once).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Each thread issues kUnroll 16-byte loads before its first conversion, so
+// it keeps kUnroll loads in flight.  Whole 16-byte groups are read up to the
+// row pitch (a multiple of 16 bytes); columns >= K of the copy are never read
+// by the GEMM.
+constexpr int kWidenThreads = 256;
+constexpr int kUnroll = 4;
+
+// One 16-byte group of int8 (16 values) -> two 16-byte FP16 groups.
+__device__ __forceinline__ void widen_i8_group(const uint4& w, __half* d) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  uint4 o[2];
+  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      ow[2 * q] = i8x2_to_f16x2(ws[q] & 0xFFFFu);
-      ow[2 * q + 1] = i8x2_to_f16x2(ws[q] >> 16);
-    }
-    uint4* d = reinterpret_cast<uint4*>(dst + r * ld_dst + g * 16);
-    d[0] = o[0];
-    d[1] = o[1];
+  for (int q = 0; q < 4; ++q) {
+    ow[2 * q] = i8x2_to_f16x2(ws[q] & 0xFFFFu);
+    ow[2 * q + 1] = i8x2_to_f16x2(ws[q] >> 16);
+  }
+  uint4* dd = reinterpret_cast<uint4*>(d);
+  dd[0] = o[0];
+  dd[1] = o[1];
+}
+
+// One 16-byte group of packed E2M1 (32 codes) -> four 16-byte FP16 groups.
+__device__ __forceinline__ void widen_e2m1_group(const uint4& w, __half* d) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  uint4* dd = reinterpret_cast<uint4*>(d);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 o;
+    o.x = e2m1x2_to_f16x2(ws[q] & 0xFFu);
+    o.y = e2m1x2_to_f16x2((ws[q] >> 8) & 0xFFu);
+    o.z = e2m1x2_to_f16x2((ws[q] >> 16) & 0xFFu);
+    o.w = e2m1x2_to_f16x2(ws[q] >> 24);
+    dd[q] = o;
   }
 }
 
-// packed E2M1 [rows x ld_src bytes] -> fp16 [rows x ld_dst]; 16 bytes = 32
-// codes per thread step.
-__global__ void widen_e2m1_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t groups,
-                                  int64_t ld_src_bytes, __half* __restrict__ dst, int64_t ld_dst) {
-  const int64_t total = rows * groups;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / groups, g = i - r * groups;
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src + r * ld_src_bytes + g * 16));
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    uint4* d = reinterpret_cast<uint4*>(dst + r * ld_dst + g * 32);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 o;
-      o.x = e2m1x2_to_f16x2(ws[q] & 0xFFu);
-      o.y = e2m1x2_to_f16x2((ws[q] >> 8) & 0xFFu);
-      o.z = e2m1x2_to_f16x2((ws[q] >> 16) & 0xFFu);
-      o.w = e2m1x2_to_f16x2(ws[q] >> 24);
-      d[q] = o;
-    }
-  }
+// Source groups -> destination: kOut FP16 per group (16 for int8, 32 for E2M1).
+template <bool kE2M1>
+__device__ __forceinline__ void widen_group(const uint4& w, __half* d) {
+  if (kE2M1)
+    widen_e2m1_group(w, d);
+  else
+    widen_i8_group(w, d);
 }
 
+// Rows packed back to back in both source and copy (the usual case): an
+// operand is one run of groups.  One launch widens up to two operands (A and
+// B of an INT8 product): groups [0, total0) of the first, then total1 of the
+// second, taken kUnroll per thread step.
+template <bool kE2M1>
+__global__ void __launch_bounds__(kWidenThreads)
+    widen_dense_kernel(const uint8_t* __restrict__ src0, __half* __restrict__ dst0, int64_t total0,
+                       const uint8_t* __restrict__ src1, __half* __restrict__ dst1,
+                       int64_t total1) {
+  constexpr int kOut = kE2M1 ? 32 : 16;
+  const int64_t total = total0 + total1;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWidenThreads;
+  for (int64_t i0 = blockIdx.x * static_cast<int64_t>(kWidenThreads) + threadIdx.x; i0 < total;
+       i0 += stride * kUnroll) {
+    uint4 w[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < total) w[u] = ld_stream(i < total0 ? src0 + i * 16 : src1 + (i - total0) * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < total)
+        widen_group<kE2M1>(w[u], i < total0 ? dst0 + i * kOut : dst1 + (i - total0) * kOut);
+    }
+  }
+  // The GEMM launched next (a programmatic dependent) may be scheduled once
+  // every thread has issued its copies; it waits for their completion.
+  grid_launch_dependents();
+}
+
+// Padded rows: a block takes rows blockIdx.x, blockIdx.x + gridDim.x, ...;
+// in a row its threads take groups tx, tx + blockDim.x, ...
+template <bool kE2M1>
+__global__ void __launch_bounds__(kWidenThreads)
+    widen_rows_kernel(const uint8_t* __restrict__ src, int rows, int groups,
+                      int64_t ld_src_bytes, __half* __restrict__ dst, int64_t ld_dst) {
+  constexpr int kOut = kE2M1 ? 32 : 16;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint8_t* s = src + static_cast<int64_t>(r) * ld_src_bytes;
+    __half* d = dst + static_cast<int64_t>(r) * ld_dst;
+    for (int g0 = threadIdx.x; g0 < groups; g0 += kWidenThreads * kUnroll) {
+      uint4 w[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int g = g0 + u * kWidenThreads;
+        if (g < groups) w[u] = ld_stream(s + static_cast<int64_t>(g) * 16);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int g = g0 + u * kWidenThreads;
+        if (g < groups) widen_group<kE2M1>(w[u], d + static_cast<int64_t>(g) * kOut);
+      }
+    }
+  }
+  // The GEMM launched next (a programmatic dependent) may be scheduled once
+  // every thread has issued its copies; it waits for their completion.
+  grid_launch_dependents();
+}
+
+// Blocks: enough for `items` work items per thread step, capped at four
+// waves of eight resident blocks per SM.
 int grid_for(int64_t items, int sm_count) {
-  int64_t blocks = (items + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sm_count) * 16;
-  if (blocks > cap) blocks = cap;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8 * 4;
+  const int64_t blocks = items < cap ? items : cap;
   return static_cast<int>(blocks < 1 ? 1 : blocks);
 }
 
@@ -95,20 +166,74 @@ int grid_for(int64_t items, int sm_count) {
 
 int64_t widened_ld(int64_t K) { return (K + 31) / 32 * 32; }
 
-cudaError_t launch_widen(dg_dtype dtype, const void* src, int64_t rows, int64_t K, int64_t ld_src,
-                         __half* dst, cudaStream_t stream, int sm_count) {
-  const int64_t ld_dst = widened_ld(K);
-  if (dtype == DG_I8) {
-    const int64_t groups = (K + 15) / 16;  // 16 int8 per group; ld_src is a multiple of 16
-    widen_i8_kernel<<<grid_for(rows * groups, sm_count), 256, 0, stream>>>(
-        static_cast<const int8_t*>(src), rows, groups, ld_src, dst, ld_dst);
-  } else if (dtype == DG_E2M1) {
-    const int64_t groups = ((K + 1) / 2 + 15) / 16;  // 32 codes per group; pitch ld_src/2 bytes
-    widen_e2m1_kernel<<<grid_for(rows * groups, sm_count), 256, 0, stream>>>(
-        static_cast<const uint8_t*>(src), rows, groups, ld_src / 2, dst, ld_dst);
-  } else {
-    return cudaErrorInvalidValue;
+namespace {
+
+struct WidenShape {
+  int64_t groups, pitch, out_per_group;
+  bool dense;
+};
+
+WidenShape widen_shape(const WidenJob& j, int64_t K) {
+  const bool e2m1 = j.dtype == DG_E2M1;
+  WidenShape w;
+  // 16-byte source groups per row: 16 int8 or 32 E2M1 codes; the source row
+  // pitch (ld_src bytes, or ld_src / 2 for E2M1) is a multiple of 16
+  w.groups = e2m1 ? ((K + 1) / 2 + 15) / 16 : (K + 15) / 16;
+  w.pitch = e2m1 ? j.ld_src / 2 : j.ld_src;
+  w.out_per_group = e2m1 ? 32 : 16;
+  w.dense = w.pitch == w.groups * 16 && widened_ld(K) == w.groups * w.out_per_group;
+  return w;
+}
+
+cudaError_t launch_rows(const WidenJob& j, const WidenShape& w, int64_t K, cudaStream_t stream,
+                        int sm_count) {
+  if (j.rows > INT32_MAX || w.groups > INT32_MAX) return cudaErrorInvalidValue;
+  const int grid = grid_for(j.rows, sm_count);
+  const auto* s = static_cast<const uint8_t*>(j.src);
+  // An ordinary launch (see widen_dense_kernel)
+  (j.dtype == DG_E2M1 ? widen_rows_kernel<true> : widen_rows_kernel<false>)
+      <<<grid, kWidenThreads, 0, stream>>>(s, static_cast<int>(j.rows), static_cast<int>(w.groups),
+                                           w.pitch, j.dst, widened_ld(K));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_widen(const WidenJob* jobs, int njobs, int64_t K, cudaStream_t stream,
+                         int sm_count) {
+  if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
+  for (int i = 0; i < njobs; ++i)
+    if (jobs[i].dtype != DG_I8 && jobs[i].dtype != DG_E2M1) return cudaErrorInvalidValue;
+  const WidenShape w0 = widen_shape(jobs[0], K);
+  const WidenShape w1 = njobs == 2 ? widen_shape(jobs[1], K) : WidenShape{0, 0, 0, true};
+  const bool fused = w0.dense && w1.dense && (njobs == 1 || jobs[1].dtype == jobs[0].dtype);
+  if (!fused) {
+    for (int i = 0; i < njobs; ++i) {
+      const WidenShape& w = i == 0 ? w0 : w1;
+      cudaError_t e;
+      if (w.dense) {
+        const WidenJob one[1] = {jobs[i]};
+        e = launch_widen(one, 1, K, stream, sm_count);
+      } else {
+        e = launch_rows(jobs[i], w, K, stream, sm_count);
+      }
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   }
+  const int64_t t0 = jobs[0].rows * w0.groups;
+  const int64_t t1 = njobs == 2 ? jobs[1].rows * w1.groups : 0;
+  const auto* s0 = static_cast<const uint8_t*>(jobs[0].src);
+  const auto* s1 = njobs == 2 ? static_cast<const uint8_t*>(jobs[1].src) : s0;
+  __half* d1 = njobs == 2 ? jobs[1].dst : jobs[0].dst;
+  const int grid =
+      grid_for((t0 + t1 + kWidenThreads * kUnroll - 1) / (kWidenThreads * kUnroll), sm_count);
+  // An ordinary launch: as a programmatic dependent, its small blocks would
+  // wait beside the previous GEMM's CTAs through their last epilogue and slow
+  // it (measured: 6 us on a 2048 x 8960 x 1536 bias+GELU GEMM).
+  (jobs[0].dtype == DG_E2M1 ? widen_dense_kernel<true> : widen_dense_kernel<false>)
+      <<<grid, kWidenThreads, 0, stream>>>(s0, jobs[0].dst, t0, s1, d1, t1);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from gpu_util import assert_parity, run_case, to_device
 
@@ -208,6 +209,62 @@ def test_back_to_back_kernels_keep_stream_order(dg):
         assert_parity(cs, got)
 
 
+def test_back_to_back_widened_and_gemv_keep_stream_order(dg):
+    # Every kernel of the library is launched as a programmatic dependent.
+    # (1) Two widened INT8 GEMMs with no host synchronisation: the second one's
+    # widening pass overwrites the FP16 workspace the first one's tensor-core
+    # kernel reads (write after read).  (2) Thin GEMV launches each reading
+    # the previous one's output (read after write).
+    dev = "cuda:0"
+    cases = [workloads.random_case(640, 1024, 1024, "i8", "i8", seed=41 + i) for i in range(2)]
+    plan = [p for p in _plans(dg, cases[0]) if p["kernel_name"] == "tc_widened"][0]
+    outs = []
+    for _ in range(2):
+        outs = []
+        for cs in cases:
+            A = torch.from_numpy(cs.A).to(dev)
+            B = torch.from_numpy(cs.B).to(dev)
+            C = torch.zeros(cs.M, cs.N, dtype=torch.int32, device=dev)
+            dg.gemm(A, B, C, plan=plan)
+            outs.append(C)
+    dg.check_status()
+    for cs, C in zip(cases, outs):
+        assert_parity(cs, C.cpu().numpy())
+    K = 2048
+    chain = [workloads.random_case(2, K, K, seed=51 + i) for i in range(3)]
+    x0 = chain[0].A.copy()
+    X = [torch.from_numpy(x0).to(dev)] + [torch.zeros(2, K, dtype=torch.float16, device=dev)
+                                          for _ in chain]
+    W = [torch.from_numpy(c.B).to(dev) for c in chain]
+    for i in range(len(chain)):
+        dg.gemm(X[i], W[i], X[i + 1])          # X[i+1] = X[i] . W[i]^T
+    dg.check_status()
+    host = [x.cpu().numpy() for x in X]
+    for i, cs in enumerate(chain):
+        cs.A = host[i]
+        assert_parity(cs, host[i + 1])
+
+
+@pytest.mark.parametrize("m", [4096, 5])   # tensor-core kernel, thin GEMV
+def test_gelu_grid(dg, m):
+    # K = 1, B = 1: D = GELU(x) for a grid of FP16 x over [-12, 12].
+    case = workloads.random_case(m, 64, 1, epilogue="gelu", seed=3)
+    x = np.linspace(-12.0, 12.0, m).astype(np.float16)
+    case.A = np.zeros_like(case.A)
+    case.A[:, 0] = x
+    case.B = np.zeros_like(case.B)
+    case.B[:, 0] = 1.0
+    got, _ = run_case(dg, case)
+    assert_parity(case, got)
+    # where Phi(x) is not tiny the result is the correctly rounded FP16 value
+    # or a neighbour (the FP32 arithmetic carries ~1e-7 relative error)
+    ref = np.float16(oracle.gelu_erf(x.astype(np.float64)))
+    sel = x >= -2.0
+    ulp = np.abs(np.spacing(ref[sel]).astype(np.float64))
+    diff = np.abs(got[sel, 0].astype(np.float64) - ref[sel].astype(np.float64))
+    assert np.all(diff <= ulp)
+
+
 def test_side_stream(dg):
     s = torch.cuda.Stream()
     case = workloads.random_case(384, 640, 512, epilogue="bias", beta=0.5, seed=8)
@@ -274,6 +331,12 @@ def test_int8_every_plan(dg):
     for p in plans:
         for grid in (p["grid"], 3):
             got, _ = run_case(dg, case, plan=dict(p, grid=grid))
+            assert_parity(case, got)
+    # N % 4 != 0: INT32 rows are not 16-byte multiples, D is stored from registers
+    case = workloads.random_case(300, 603, 1100, "i8", "i8", alpha=-3, beta=-2, seed=4)
+    for p in _plans(dg, case):
+        if p["kernel_name"] == "tc_widened":
+            got, _ = run_case(dg, case, plan=p)
             assert_parity(case, got)
 
 

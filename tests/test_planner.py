@@ -23,7 +23,7 @@ GB300 = dict(sm_count=152, cc_major=10, cc_minor=3, smem_per_block_optin=232448,
 # Compiled FP16 tensor-core variants: (N_tile, stages, CTAs per tile); M_tile
 # 128 per CTA, K_tile 64, 384 threads.  A CTA pair holds half of B per CTA.
 TC_VARIANTS = [(256, 4, 1), (128, 6, 1), (64, 8, 1), (256, 6, 2), (224, 6, 2), (128, 8, 2)]
-# FP16 output passes through two 32 x 32 FP16 staging boxes per epilogue warp (8 warps)
+# The output passes through two 2 KB staging boxes per epilogue warp (8 warps)
 EPI_STAGING = 8 * 2 * 32 * 32 * 2
 
 
@@ -223,7 +223,7 @@ def test_converting_kernel_plans(dg, pair, shape):
     wide = {(p["n_tile"], p["stages"], p["cta_group"]) for p in plans
             if p["kernel_name"] == "tc_widened"}
     if pair[0] == "i8":
-        want = {(128, 6, 1), (128, 8, 2)}
+        want = {(128, 6, 1), (192, 6, 2)}
     else:
         want = set(TC_VARIANTS)
     if M <= 128:
@@ -232,6 +232,5 @@ def test_converting_kernel_plans(dg, pair, shape):
     for p in plans:
         if p["kernel_name"] == "tc_widened":
             assert p["threads"] == 384
-            # INT8 runs the FP16 kernel in its exact INT32 mode, without staging
-            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], p["cta_group"],
-                                              staged=pair[0] != "i8")
+            # INT8 runs the FP16 kernel in its exact INT32 mode (also staged)
+            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], p["cta_group"])
