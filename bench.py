@@ -182,10 +182,8 @@ def recorded_traffic(kernel, workload):
         return None
     with open(path) as f:
         d = json.load(f)
-    e = d.get(kernel)
+    e = d.get(kernel, {}).get(workload)
     if not e or e.get("source_hash") != kernel_source_hash(kernel):
-        return None
-    if e.get("workload") != workload:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -221,9 +219,11 @@ def algorithmic_bytes(case):
 
 
 def kernel_name(plan, case):
+    """The step's dominant kernel: the split-K GEMV, the FP16 tensor-core
+    kernel (also for widened INT8 / E2M1 operands) or the converting kernel."""
     if plan["kernel_name"] == "gemv":
         return "gemv_splitk_kernel"
-    if case.dtype_a == "f16" and case.dtype_b == "f16":
+    if plan["kernel_name"] == "tc_widened" or (case.dtype_a == "f16" and case.dtype_b == "f16"):
         return "gemm_f16_tc_kernel"
     return "gemm_conv_tc_kernel"
 
