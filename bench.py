@@ -162,6 +162,7 @@ KERNEL_SOURCES = {
     "gemm_f16_tc_kernel": ("gemm_tc.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh"),
     "gemm_conv_tc_kernel": ("gemm_conv.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh"),
     "gemv_splitk_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh"),
+    "skinny_w4a16_kernel": ("skinny.cu", "ptx.cuh", "epilogue.cuh"),
 }
 
 
@@ -223,6 +224,8 @@ def kernel_name(plan, case):
     kernel (also for widened INT8 / E2M1 operands) or the converting kernel."""
     if plan["kernel_name"] == "gemv":
         return "gemv_splitk_kernel"
+    if plan["kernel_name"] == "skinny":
+        return "skinny_w4a16_kernel"
     if plan["kernel_name"] == "tc_widened" or (case.dtype_a == "f16" and case.dtype_b == "f16"):
         return "gemm_f16_tc_kernel"
     return "gemm_conv_tc_kernel"

@@ -77,9 +77,11 @@ typedef enum {
 typedef enum {
   DG_KERNEL_TC = 0,    /* tensor-core pipeline: TMA -> SMEM ring -> tcgen05.mma -> TMEM -> fused epilogue */
   DG_KERNEL_GEMV = 1,  /* thin-M split-K streaming kernel on the CUDA cores */
-  DG_KERNEL_TC_WIDENED = 2 /* int8 / E2M1 operands widened to FP16 by a streaming pre-pass into
-                              a library workspace, then the FP16 tensor-core kernel (INT8:
-                              exact INT32 output) -- for compute-bound shapes */
+  DG_KERNEL_TC_WIDENED = 2, /* int8 / E2M1 operands widened to FP16 by a streaming pre-pass into
+                               a library workspace, then the FP16 tensor-core kernel (INT8:
+                               exact INT32 output) -- for compute-bound shapes */
+  DG_KERNEL_SKINNY = 3 /* FP16 x E2M1 with M <= 16 (HBM-bound): packed weights streamed into
+                          registers, widened there and fed to warp-level m16n8k16 MMAs */
 } dg_kernel;
 
 /* Hardware description the planner solves against

@@ -315,6 +315,8 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
       if (s != DG_OK) return s;
     }
     e = launch_gemv(a, plan, ws);
+  } else if (plan.kernel == DG_KERNEL_SKINNY) {
+    e = launch_skinny(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC) {
     e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC_WIDENED) {

@@ -76,6 +76,12 @@ struct SplitKWorkspace {
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);    // F16 x F16
 cudaError_t launch_conv(const GemmArgs& a, const dg_tile_plan& plan);  // I8 x I8, F16 x E2M1
 cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws);
+// Skinny W4A16 kernel (skinny.cu): FP16 A with M <= 16 x packed E2M1 B.
+cudaError_t launch_skinny(const GemmArgs& a, const dg_tile_plan& plan);
+int skinny_smem_bytes();
+int skinny_threads();
+int skinny_cols_per_block();
+int skinny_k_chunk();
 cudaError_t launch_epilogue_only(const GemmArgs& a);
 
 // Widening pre-pass (widen.cu): int8 or packed-E2M1 rows -> FP16 rows with

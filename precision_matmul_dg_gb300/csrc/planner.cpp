@@ -270,6 +270,69 @@ void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype 
   }
 }
 
+// Skinny W4A16 kernel: FP16 A with M <= 16 rows x packed E2M1 B, one block
+// of 512 threads per 64 columns, K in 2048-code chunks split between two warp
+// halves; the weights stream from HBM once.
+constexpr int kSkinnyMaxM = 16;
+constexpr int kSkinnyRegsPerThread = 80;
+
+void add_skinny_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+                           const dg_hw_desc& hw, double target, std::vector<dg_tile_plan>* out,
+                           std::string* why) {
+  if (!(da == DG_F16 && db == DG_E2M1)) return;
+  if (M > kSkinnyMaxM) {
+    if (why) *why += "skinny: M > 16; ";
+    return;
+  }
+  if (hw.cc_major < 8) {
+    if (why) *why += "skinny: needs m16n8k16 FP16 MMA; ";
+    return;
+  }
+  const int smem = skinny_smem_bytes();
+  if (smem > hw.smem_per_block_optin) {
+    if (why) *why += "skinny: shared memory; ";
+    return;
+  }
+  const int threads = skinny_threads();
+  if (kSkinnyRegsPerThread * threads > hw.regs_per_sm) {
+    if (why) *why += "skinny: registers; ";
+    return;
+  }
+  const int64_t blocks = ceil_div(N, skinny_cols_per_block());
+  const int64_t per_sm = std::max<int64_t>(
+      1, std::min<int64_t>(hw.smem_per_sm / smem, hw.max_threads_per_sm / threads));
+  const int64_t slots = per_sm * hw.sm_count;
+  const int64_t waves = ceil_div(blocks, slots);
+  const double occ = static_cast<double>(blocks) / static_cast<double>(waves * slots);
+  if (occ < target) {
+    if (why) *why += "skinny: occupancy; ";
+    return;
+  }
+  // Streaming time of the weights over the SMs that hold a block, plus a
+  // fixed latency (launch, activation load, one round trip per chunk).
+  const double busy = std::min(1.0, static_cast<double>(blocks) / hw.sm_count);
+  const double bytes = 0.5 * N * static_cast<double>(K) + 2.0 * M * K + 2.0 * M * N;
+  const int64_t chunks = ceil_div(K, skinny_k_chunk());
+  const double t = 2.0 + 1.0 * static_cast<double>(chunks) +
+                   bytes / (hbm_bytes_per_us(hw) * 0.8 * busy);
+  dg_tile_plan p{};
+  p.kernel = DG_KERNEL_SKINNY;
+  p.m_tile = kSkinnyMaxM;
+  p.n_tile = skinny_cols_per_block();
+  p.k_tile = skinny_k_chunk();
+  p.split_k = 2;
+  p.stages = 1;
+  p.cta_group = 1;
+  p.swap_ab = 0;
+  p.smem_bytes = smem;
+  p.threads = threads;
+  p.grid = static_cast<int>(blocks);
+  p.occupancy = occ;
+  p.est_us = t;
+  p.est_tflops = 2.0 * M * N * K / (t * 1e6);
+  out->push_back(p);
+}
+
 // Warp-level-MMA tile family for GPUs without tensor memory (planning only).
 void add_warp_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, const dg_hw_desc& hw,
                              double target, std::vector<dg_tile_plan>* out, std::string* why) {
@@ -374,6 +437,7 @@ dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype
     add_tc_candidates(M, N, K, dtype_a, dtype_b, false, hw, target_occupancy, &cands, why);
     add_tc_candidates(M, N, K, dtype_a, dtype_b, true, hw, target_occupancy, &cands, why);
     add_gemv_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
+    add_skinny_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
   } else {
     add_warp_mma_candidates(M, N, K, dtype_a, hw, target_occupancy, &cands, why);
   }
@@ -430,6 +494,18 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
         return true;
     if (why) *why = "widened N_tile/stages pair not compiled";
     return false;
+  }
+  if (plan.kernel == DG_KERNEL_SKINNY) {
+    if (!(dtype_a == DG_F16 && dtype_b == DG_E2M1) || M > kSkinnyMaxM) {
+      if (why) *why = "skinny plan needs F16 x E2M1 and M <= 16";
+      return false;
+    }
+    if (plan.n_tile != skinny_cols_per_block() || plan.k_tile != skinny_k_chunk() ||
+        plan.split_k != 2 || plan.cta_group != 1) {
+      if (why) *why = "skinny plan shape not compiled";
+      return false;
+    }
+    return true;
   }
   if (plan.kernel == DG_KERNEL_GEMV) {
     if (!(dtype_a == DG_F16 && dtype_b == DG_F16) || M > kGemvMaxM) {

@@ -1,0 +1,239 @@
+// Skinny W4A16 GEMM: D = epilogue(alpha * A . B + beta * C) for M <= 16 rows
+// of FP16 activations A against packed 4-bit E2M1 weights B (N rows of K
+// codes, two per byte, k = 2p in the low nibble of byte p; discosf.com/news/
+// 5532976, section 4.3 packing and section 3.2's W4A16 shapes with M = 16).
+//
+// At M <= 16 the product reads each weight once and does 16 multiply-adds
+// with it: the job is streaming N*K/2 bytes of weights from HBM.  The CUDA
+// cores cannot keep up (16 FMAs per 4-bit weight), and staging widened weight
+// tiles in shared memory for tcgen05 costs more than the MMA saves at this
+// size.  So the weights go from HBM straight into registers, are widened
+// there with cvt.rn.f16x2.e2m1x2 and fed to warp-level m16n8k16 MMAs (FP16 in,
+// FP32 accumulate), with the 16 activation rows (zero-padded) in shared memory.
+//
+// Layout.  A block of 16 warps owns 64 columns: warp w takes column group
+// w % 8 (8 columns, one B row per group of 4 lanes) and K half w / 8 (every
+// other pair of 128-code windows).  A warp reads a window pair of its 8 rows
+// (8 x 128 bytes) with two loads of 4 whole 128-byte lines each, all of its
+// pairs of a 2048-code chunk before the first MMA, then shuffles the bytes so
+// that lane (grp = lane / 4, tig = lane % 4) holds, per window, the 16 bytes
+// (32 codes) at window offset 32 * tig of B row n0 + grp (whole-line loads
+// take half the memory requests of per-lane 16-byte pieces of 8 rows).
+// For MMA step s (0..7) of a window it uses bytes 2s and 2s + 1 of those 16:
+// codes 4s .. 4s + 3, which fill the B fragment slots k = 2 tig, 2 tig + 1
+// and 2 tig + 8, 2 tig + 9.  The A fragment takes the same four K positions
+// of rows grp and grp + 8 from shared memory, so every MMA step covers 16
+// distinct K values of the window and the K order inside the dot product is
+// merely permuted.  The two K halves are summed in shared memory; the fused
+// epilogue (alpha, beta * C, bias, erf-GELU, FP16 rounding) runs on the MMA
+// fragments.  Columns >= N and rows >= M are computed on clamped or zero
+// inputs and never stored; codes at k >= K meet zeroed activations.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "epilogue.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kSkWarps = 16;     // 8 column groups x 2 K halves
+constexpr int kSkThreads = kSkWarps * 32;
+constexpr int kSkGroups = 8;     // column groups of 8 per block
+constexpr int kSkCols = kSkGroups * 8;
+constexpr int kSkWindow = 128;   // codes per window: 16 bytes per lane
+constexpr int kSkBatch = 8;      // windows per warp per chunk (all loads in flight)
+constexpr int kSkPairs = kSkBatch / 2;  // window pairs per warp per chunk
+constexpr int kSkChunk = 2 * kSkBatch * kSkWindow;  // K codes per activation chunk
+constexpr int kSkRowPad = 8;     // halves of padding per activation row
+constexpr int kSkStride = kSkChunk + kSkRowPad;
+constexpr int kSkSmemA = 16 * kSkStride * 2;
+constexpr int kSkSmemRed = kSkGroups * 32 * 4 * 4;
+constexpr int kSkSmem = kSkSmemA + kSkSmemRed;
+
+struct SkParams {
+  int M, N, K;
+  const __half* A;
+  int64_t lda;
+  const uint8_t* B;
+  int64_t ldb_bytes;  // packed row pitch
+  __half* CD;         // C in / D out, leading dimension N
+  const __half* bias;
+  Epi epi;
+};
+
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t o;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(o)
+      : "r"(byte));
+  return o;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// d += a (16 x 16, row-major fragment) . b (16 x 8, column-major fragment)
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(kSkThreads) skinny_w4a16_kernel(const SkParams p) {
+  extern __shared__ __align__(16) uint8_t sk_smem[];
+  __half* As = reinterpret_cast<__half*>(sk_smem);             // [16][kSkStride]
+  float* red = reinterpret_cast<float*>(sk_smem + kSkSmemA);   // [8 groups][32 lanes][4]
+  grid_dependency_wait();  // launched as a dependent of the previous kernel
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cg = warp % kSkGroups, kh = warp / kSkGroups;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int n0 = blockIdx.x * kSkCols + cg * 8;
+  // this lane's rows for the line loads: n0 + lane / 8 and n0 + 4 + lane / 8
+  // (rows >= N: clamped, results not stored)
+  const uint8_t* brow0 = p.B + static_cast<int64_t>(min(n0 + (lane >> 3), p.N - 1)) * p.ldb_bytes;
+  const uint8_t* brow1 =
+      p.B + static_cast<int64_t>(min(n0 + 4 + (lane >> 3), p.N - 1)) * p.ldb_bytes;
+  const int row_groups = (p.K + 31) / 32;  // 16-byte groups holding codes < K
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+
+  for (int kc0 = 0; kc0 < p.K; kc0 += kSkChunk) {
+    const int nwin = (min(kSkChunk, p.K - kc0) + kSkWindow - 1) / kSkWindow;
+    // this warp's weight loads for the chunk, issued before anything waits:
+    // window pair q = kh + 2i covers bytes [128 q, 128 q + 128) of each row
+    uint4 bl[kSkPairs][2];
+#pragma unroll
+    for (int i = 0; i < kSkPairs; ++i) {
+      const int q = kh + 2 * i;
+      const int g = kc0 / 32 + q * 8 + (lane & 7);
+      const bool in = 2 * q < nwin && g < row_groups;
+      bl[i][0] = in ? ld_stream16(brow0 + static_cast<int64_t>(g) * 16) : make_uint4(0u, 0u, 0u, 0u);
+      bl[i][1] = in ? ld_stream16(brow1 + static_cast<int64_t>(g) * 16) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // activation chunk -> shared memory; rows >= M and columns >= K are zero
+    __syncthreads();  // the previous chunk's reads are done
+    for (int idx = threadIdx.x; idx < 16 * (kSkChunk / 8); idx += kSkThreads) {
+      const int r = idx / (kSkChunk / 8), u = idx % (kSkChunk / 8);
+      const int k = kc0 + u * 8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < p.M && k < p.K) {
+        v = *reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(r) * p.lda + k);
+        if (k + 8 > p.K) {
+          __half* h = reinterpret_cast<__half*>(&v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (k + e >= p.K) h[e] = __ushort_as_half(0);
+        }
+      }
+      *reinterpret_cast<uint4*>(As + r * kSkStride + u * 8) = v;
+    }
+    __syncthreads();
+    // lane (grp, tig) takes, for window h of a pair, piece 4h + tig of row
+    // grp, held by lane 8 (grp % 4) + 4h + tig of load grp / 4
+#pragma unroll
+    for (int i = 0; i < kSkBatch; ++i) {
+      const int w = 2 * (kh + 2 * (i >> 1)) + (i & 1);
+      if (w >= nwin) break;  // the same for the whole warp
+      const int src = 8 * (grp & 3) + 4 * (i & 1) + tig;
+      const uint4 v0 = bl[i >> 1][0], v1 = bl[i >> 1][1];
+      // every lane takes part in both shuffles, then keeps the one for its row
+      const uint32_t s0[4] = {__shfl_sync(0xffffffffu, v0.x, src), __shfl_sync(0xffffffffu, v0.y, src),
+                              __shfl_sync(0xffffffffu, v0.z, src), __shfl_sync(0xffffffffu, v0.w, src)};
+      const uint32_t s1[4] = {__shfl_sync(0xffffffffu, v1.x, src), __shfl_sync(0xffffffffu, v1.y, src),
+                              __shfl_sync(0xffffffffu, v1.z, src), __shfl_sync(0xffffffffu, v1.w, src)};
+      uint32_t wv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wv[j] = grp < 4 ? s0[j] : s1[j];
+      const __half* a_lo = As + grp * kSkStride + w * kSkWindow + 32 * tig;
+      const __half* a_hi = a_lo + 8 * kSkStride;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t word = wv[s >> 1];
+        const int sh = 16 * (s & 1);
+        const uint32_t b0 = e2m1x2_to_f16x2((word >> sh) & 0xFFu);        // codes 4s, 4s+1
+        const uint32_t b1 = e2m1x2_to_f16x2((word >> (sh + 8)) & 0xFFu);  // codes 4s+2, 4s+3
+        const uint2 lo = *reinterpret_cast<const uint2*>(a_lo + 4 * s);
+        const uint2 hi = *reinterpret_cast<const uint2*>(a_hi + 4 * s);
+        const uint32_t a[4] = {lo.x, hi.x, lo.y, hi.y};
+        mma_m16n8k16(acc, a, b0, b1);
+      }
+    }
+  }
+
+  // the two K halves of each column group
+  if (kh == 1) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) red[(cg * 32 + lane) * 4 + j] = acc[j];
+  }
+  __syncthreads();
+  grid_launch_dependents();  // the weights have been streamed
+  if (kh != 0) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] += red[(cg * 32 + lane) * 4 + j];
+  // fragment: acc[0..1] at (row grp, columns n0 + 2 tig + {0,1}), acc[2..3] at row grp + 8
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int m = grp + 8 * h;
+    if (m >= p.M) continue;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int nn = n0 + 2 * tig + e;
+      if (nn >= p.N) continue;
+      const int64_t idx = static_cast<int64_t>(m) * p.N + nn;
+      const float c = p.epi.beta != 0.0f ? __half2float(p.CD[idx]) : 0.0f;
+      const float b = (p.epi.flags & kEpiBias) ? __half2float(p.bias[nn]) : 0.0f;
+      p.CD[idx] = __float2half_rn(epi_apply(acc[2 * h + e], c, b, p.epi));
+    }
+  }
+}
+
+}  // namespace
+
+int skinny_smem_bytes() { return kSkSmem; }
+int skinny_threads() { return kSkThreads; }
+int skinny_cols_per_block() { return kSkCols; }
+int skinny_k_chunk() { return kSkChunk; }
+
+cudaError_t launch_skinny(const GemmArgs& a, const dg_tile_plan& plan) {
+  (void)plan;
+  if (a.M > 16 || a.dtype_a != DG_F16 || a.dtype_b != DG_E2M1) return cudaErrorInvalidValue;
+  SkParams p;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.A = static_cast<const __half*>(a.A);
+  p.lda = a.lda;
+  p.B = static_cast<const uint8_t*>(a.B);
+  p.ldb_bytes = a.ldb / 2;
+  p.CD = static_cast<__half*>(a.C);
+  p.bias = static_cast<const __half*>(a.bias);
+  p.epi = Epi{a.alpha, a.beta, a.epi};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static uint64_t attr_set = 0;  // one shared-memory opt-in per device
+  if (!(attr_set & (1ull << (dev & 63)))) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(skinny_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSkSmem);
+    if (e != cudaSuccess) return e;
+    attr_set |= 1ull << (dev & 63);
+  }
+  const unsigned grid = static_cast<unsigned>((a.N + kSkCols - 1) / kSkCols);
+  const cudaError_t e = launch_dependent(skinny_w4a16_kernel, dim3(grid), dim3(kSkThreads),
+                                         kSkSmem, a.stream, p);
+  count_launches(1);
+  return e;
+}
+
+}  // namespace dg

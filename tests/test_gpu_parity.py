@@ -374,6 +374,37 @@ def test_w4a16_random_shapes(dg, shape, epi):
     assert_parity(case, got)
 
 
+def _skinny_plan(dg, case):
+    sk = [p for p in _plans(dg, case) if p["kernel_name"] == "skinny"]
+    assert len(sk) == 1
+    return sk[0]
+
+
+@pytest.mark.parametrize("shape", [(16, 8960, 1536), (1, 100, 64), (3, 777, 33), (9, 130, 4100),
+                                   (16, 64, 2048), (13, 1001, 6000), (2, 65, 1)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("epi", ["none", "bias_gelu"])
+def test_w4a16_skinny(dg, shape, epi):
+    # warp-MMA skinny kernel (M <= 16): ragged N (partial 64-column blocks and
+    # 8-column groups), K tails inside a 32-code group and across 2048-code
+    # chunks; the padding bytes (0xFF codes) past K must not contribute
+    M, N, K = shape
+    case = workloads.random_case(M, N, K, "f16", "e2m1", epilogue=epi, alpha=-0.75, beta=0.5,
+                                 seed=M * 7 + N + K, pad=255)
+    got, tail = run_case(dg, case, plan=_skinny_plan(dg, case), canary=64)
+    assert_parity(case, got)
+    assert np.all(tail == np.float16(-7.5))
+
+
+def test_w4a16_skinny_every_m(dg):
+    # every row count 1..16 through the same column layout
+    for M in range(1, 17):
+        case = workloads.random_case(M, 200, 700, "f16", "e2m1", epilogue="bias", beta=-1.0,
+                                     seed=100 + M, pad=255)
+        got, _ = run_case(dg, case, plan=_skinny_plan(dg, case))
+        assert_parity(case, got)
+
+
 def test_w4a16_every_code_one_hot(dg):
     """Column j of the weights holds code j % 16 at k = j % K and zeros elsewhere,
     so D[:, j] = A[:, k] * value(code): every code's decoded value appears as a

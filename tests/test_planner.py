@@ -210,7 +210,8 @@ def conv_smem(da, db, n_tile, stages):
 def test_converting_kernel_plans(dg, pair, shape):
     M, N, K = shape
     plans = dg.plan_tiles(M, N, K, pair[0], pair[1], hw=GB300, target_occupancy=0.0)
-    assert {p["kernel_name"] for p in plans} == {"tc", "tc_widened"}
+    skinny = pair == ("f16", "e2m1") and M <= 16
+    assert {p["kernel_name"] for p in plans} == {"tc", "tc_widened"} | ({"skinny"} if skinny else set())
     conv = [p for p in plans if p["kernel_name"] == "tc"]
     assert {(p["n_tile"], p["stages"]) for p in conv} == set(CONV_VARIANTS[pair])
     for p in conv:
@@ -234,3 +235,26 @@ def test_converting_kernel_plans(dg, pair, shape):
             assert p["threads"] == 384
             # INT8 runs the FP16 kernel in its exact INT32 mode (also staged)
             assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], p["cta_group"])
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 17])
+def test_skinny_plans(dg, M):
+    # FP16 x E2M1 with M <= 16: one 512-thread block per 64 columns, 2048-code
+    # activation chunks in shared memory split between two warp halves
+    N, K = 8960, 1536
+    plans = dg.plan_tiles(M, N, K, "f16", "e2m1", hw=GB300, target_occupancy=0.0)
+    sk = [p for p in plans if p["kernel_name"] == "skinny"]
+    if M > 16:
+        assert not sk
+        return
+    assert len(sk) == 1
+    p = sk[0]
+    assert (p["m_tile"], p["n_tile"], p["k_tile"], p["split_k"]) == (16, 64, 2048, 2)
+    assert p["threads"] == 512 and p["grid"] == math.ceil(N / 64)
+    assert p["smem_bytes"] == 16 * (2048 + 8) * 2 + 8 * 32 * 4 * 4
+    assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
+    # it streams the weights once: ranked first for the HBM-bound shape
+    assert plans[0]["kernel_name"] == "skinny"
+    # not for other dtype pairs
+    assert not [q for q in dg.plan_tiles(M, N, K, "f16", "f16", hw=GB300, target_occupancy=0.0)
+                if q["kernel_name"] == "skinny"]
