@@ -154,6 +154,32 @@ dg_status dg_gemm(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dt
                   const void *bias, float alpha, float beta, dg_epilogue epilogue,
                   dg_stream_t stream);
 
+/* D = epilogue(alpha * A.B + beta * C) on HOST buffers: the same operation
+ * and rules as dg_gemm, with the host-to-device and device-to-host copies
+ * inside the call.  This is the pages' calling pattern (discosf.com/news/
+ * 5532976, section 3.4: page-locked host matrices are bound to the GEMM, and
+ * the runtime allocates device memory on demand at the first launch and
+ * manages its lifetime; no cudaMalloc or cudaMemcpy in the caller).
+ *   A, B, bias: host inputs in dg_gemm's layouts (A: M rows of lda elements,
+ *     B: N rows of ldb elements / codes, bias: N FP16); C: host input (M x N,
+ *     leading dimension N; FP16, or INT32 for I8 x I8), read only when
+ *     beta != 0 and may then be NULL otherwise; D: host output of the same
+ *     layout as C (may equal C).
+ *   Copies and kernels are asynchronous and ordered on `stream`: the caller
+ *   synchronises that stream before reading D or reusing the inputs.  With
+ *   page-locked (pinned) host memory the copies overlap one another and the
+ *   kernels: B and bias are copied first, then row panels of A and C are
+ *   copied, multiplied and copied back on two internal streams joined back to
+ *   `stream`.  Pageable memory works, with copies that do not overlap.
+ *   Device copies of the operands live in a per-(device, stream) workspace
+ *   that grows with cudaMalloc and that libdg owns until dg_shutdown.
+ * Errors: as dg_gemm, plus DG_ERR_INVALID_ARG for a NULL D, or a NULL C with
+ * beta != 0, and DG_ERR_CUDA for a failed copy. */
+dg_status dg_gemm_host(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                       const void *A, int64_t lda, const void *B, int64_t ldb, const void *C,
+                       void *D, const void *bias, float alpha, float beta,
+                       dg_epilogue epilogue, dg_stream_t stream);
+
 /* As dg_gemm, but runs `plan` (one returned by dg_plan_tiles for the same
  * M, N, K and dtypes).  DG_ERR_INVALID_STATE when the plan does not fit. */
 dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,

@@ -12,6 +12,7 @@ import os
 
 __all__ = [
     "DgError", "F16", "I8", "E2M1", "EPILOGUES", "lib", "lib_path", "gemm", "gemm_raw",
+    "gemm_host", "gemm_host_raw",
     "plan_tiles", "query_hw", "last_error", "check_status", "set_wait_timeout_ns",
     "selftest_wait_timeout", "launch_count", "shutdown", "HwDesc", "TilePlan", "EXPORTS",
 ]
@@ -25,7 +26,7 @@ STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
 KERNELS = {0: "tc", 1: "gemv", 2: "tc_widened", 3: "skinny", -1: "none"}
 
 # Every symbol include/dg.h declares.
-EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
+EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_gemm_host",
            "dg_gemm_thin_noalloc", "dg_last_error",
            "dg_check_status", "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout",
            "dg_launch_count", "dg_shutdown"]
@@ -91,6 +92,8 @@ def lib():
     L.dg_gemm.argtypes = gemm_args + [vp]
     L.dg_gemm_planned.argtypes = gemm_args + [ctypes.POINTER(TilePlan), vp]
     L.dg_gemm_thin_noalloc.argtypes = gemm_args + [vp]
+    L.dg_gemm_host.argtypes = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, vp, vp, f32, f32,
+                               i32, vp]
     L.dg_last_error.restype = ctypes.c_char_p
     L.dg_last_error.argtypes = []
     L.dg_check_status.argtypes = [vp]
@@ -100,7 +103,7 @@ def lib():
     L.dg_launch_count.argtypes = []
     L.dg_shutdown.argtypes = []
     for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
-                 "dg_gemm_thin_noalloc", "dg_check_status",
+                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_check_status",
                  "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout", "dg_shutdown"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -203,6 +206,48 @@ def gemm(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none", dtype
     gemm_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue,
              stream=stream, plan=plan)
     return C
+
+
+def gemm_host_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, D, bias, alpha, beta, epilogue,
+                  stream=None):
+    """dg_gemm_host with the C argument order: A, B, C, D, bias are host
+    tensors (ideally pinned) or raw host addresses."""
+    args = (int(M), int(N), int(K), _dtype_code(dtype_a), _dtype_code(dtype_b), _ptr(A), int(lda),
+            _ptr(B), int(ldb), _ptr(C), _ptr(D), _ptr(bias), float(alpha), float(beta),
+            _epi_code(epilogue), _stream_handle(stream))
+    _check(lib().dg_gemm_host(*args))
+
+
+def gemm_host(A, B, D, C=None, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none",
+              dtype_b=None, stream=None):
+    """D = epilogue(alpha * A.B + beta * C) on host (CPU) tensors, copies
+    included: the call is asynchronous on `stream`, so synchronise it before
+    reading D.  Layouts as gemm(); C (read when beta != 0) and D are [M, N]."""
+    import torch
+    dtype_a = "i8" if A.dtype == torch.int8 else "f16"
+    if dtype_b is None:
+        dtype_b = {torch.float16: "f16", torch.int8: "i8", torch.uint8: "e2m1"}[B.dtype]
+    for t, what in ((A, "A"), (B, "B"), (D, "D"), (C, "C"), (bias, "bias")):
+        if t is not None and t.device.type != "cpu":
+            raise ValueError("%s must be a host tensor" % what)
+    _expect(A, dtype_a, "A")
+    _expect(B, dtype_b, "B")
+    out = "i32" if dtype_a == "i8" else "f16"
+    _expect(D, out, "D")
+    M, N = D.shape
+    if C is not None:
+        _expect(C, out, "C")
+        if tuple(C.shape) != (M, N) or C.stride(0) != N:
+            raise ValueError("C must be dense [M, N]")
+    if A.shape[0] != M or B.shape[0] != N or D.stride(0) != N:
+        raise ValueError("shape mismatch: A %s, B %s, D %s" % (tuple(A.shape), tuple(B.shape),
+                                                               tuple(D.shape)))
+    if K is None:
+        K = A.shape[1]
+    ldb = B.stride(0) * (2 if dtype_b == "e2m1" else 1)
+    gemm_host_raw(M, N, K, dtype_a, dtype_b, A, A.stride(0), B, ldb, C, D, bias, alpha, beta,
+                  epilogue, stream=stream)
+    return D
 
 
 def query_hw(device=0):

@@ -59,6 +59,17 @@ struct Workspace {
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+// Device copies of host operands for dg_gemm_host, and the two internal
+// streams (with their events) that overlap panel copies with the kernels.
+struct HostWorkspace {
+  void* buf[4] = {nullptr, nullptr, nullptr, nullptr};  // A, B, C/D, bias
+  int64_t bytes[4] = {0, 0, 0, 0};
+  cudaStream_t aux[2] = {nullptr, nullptr};
+  cudaEvent_t ev_b = nullptr;
+  cudaEvent_t ev_done[2] = {nullptr, nullptr};
+};
+std::map<std::pair<int, cudaStream_t>, HostWorkspace> g_host_ws;
 std::map<std::tuple<int, int64_t, int64_t, int64_t, int, int, int>, dg_tile_plan> g_plans;
 
 dg_status fill_hw(int device, dg_hw_desc* out) {
@@ -358,6 +369,97 @@ void clear_error() { g_last_error[0] = '\0'; }
 
 dg_status set_error(dg_status s, const char* msg) { return fail(s, "%s", msg); }
 
+// Host-buffer GEMM (dg_gemm_host in dg.h).
+dg_status run_host(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const void* A,
+                   int64_t lda, const void* B, int64_t ldb, const void* C, void* D,
+                   const void* bias, float alpha, float beta, dg_epilogue epilogue,
+                   cudaStream_t stream) {
+  clear_error();
+  if (!D) return fail(DG_ERR_INVALID_ARG, "D is null");
+  if (beta != 0.0f && !C) return fail(DG_ERR_INVALID_ARG, "beta != 0 with a null C");
+  dg_status s = validate(M, N, K, da, db, A, lda, B, ldb, D, bias, alpha, beta, epilogue);
+  if (s != DG_OK) return s;
+  if (M == 0 || N == 0) return DG_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DG_ERR_INVALID_STATE, "no current CUDA device");
+  }
+  const int64_t a_row = lda * elem_bits(da) / 8, b_row = ldb * elem_bits(db) / 8;
+  const int64_t o_elem = da == DG_I8 ? 4 : 2;
+  const bool has_bias = epilogue == DG_EPI_BIAS || epilogue == DG_EPI_BIAS_GELU;
+  const int64_t need[4] = {K > 0 ? M * a_row : 0, K > 0 ? N * b_row : 0, M * N * o_elem,
+                           has_bias ? N * 2 : 0};
+  HostWorkspace* hw = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    hw = &g_host_ws[std::make_pair(dev, stream)];
+    for (int i = 0; i < 4; ++i) {
+      if (hw->bytes[i] >= need[i]) continue;
+      if (hw->buf[i]) cudaFree(hw->buf[i]);  // synchronises the device: nothing still uses it
+      hw->buf[i] = nullptr;
+      hw->bytes[i] = 0;
+      const cudaError_t e = cudaMalloc(&hw->buf[i], need[i]);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(host-call workspace)");
+      hw->bytes[i] = need[i];
+    }
+    if (!hw->aux[0]) {
+      for (int i = 0; i < 2; ++i) {
+        cudaError_t e = cudaStreamCreateWithFlags(&hw->aux[i], cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hw->ev_done[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) return fail_cuda(e, "stream / event creation");
+      }
+      const cudaError_t e = cudaEventCreateWithFlags(&hw->ev_b, cudaEventDisableTiming);
+      if (e != cudaSuccess) return fail_cuda(e, "event creation");
+    }
+  }
+  auto* dA = static_cast<uint8_t*>(hw->buf[0]);
+  auto* dB = static_cast<uint8_t*>(hw->buf[1]);
+  auto* dC = static_cast<uint8_t*>(hw->buf[2]);
+  auto* dbias = static_cast<uint8_t*>(hw->buf[3]);
+  auto copy = [&](void* dst, const void* src, int64_t n, cudaMemcpyKind kind,
+                  cudaStream_t st) -> dg_status {
+    if (n <= 0) return DG_OK;
+    const cudaError_t e = cudaMemcpyAsync(dst, src, n, kind, st);
+    return e == cudaSuccess ? DG_OK : fail_cuda(e, "host-call copy");
+  };
+  // B and bias first, on the caller's stream (after whatever it already holds).
+  if ((s = copy(dB, B, need[1], cudaMemcpyHostToDevice, stream)) != DG_OK) return s;
+  if ((s = copy(dbias, bias, need[3], cudaMemcpyHostToDevice, stream)) != DG_OK) return s;
+  cudaError_t e = cudaEventRecord(hw->ev_b, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "event record");
+  // Row panels of A and C: copy in, multiply, copy out, alternating between
+  // the two internal streams so that one panel's copies overlap the other's.
+  const int64_t panel = M >= 512 ? (((M + 3) / 4 + 255) / 256) * 256 : M;
+  const int64_t npanels = (M + panel - 1) / panel;
+  for (int64_t i = 0; i < npanels; ++i) {
+    cudaStream_t st = hw->aux[i % 2];
+    if (i < 2 && (e = cudaStreamWaitEvent(st, hw->ev_b, 0)) != cudaSuccess)
+      return fail_cuda(e, "stream wait");
+    const int64_t r0 = i * panel, mr = std::min(panel, M - r0);
+    if ((s = copy(dA + r0 * a_row, static_cast<const uint8_t*>(A) + r0 * a_row, mr * a_row,
+                  cudaMemcpyHostToDevice, st)) != DG_OK)
+      return s;
+    if (beta != 0.0f &&
+        (s = copy(dC + r0 * N * o_elem, static_cast<const uint8_t*>(C) + r0 * N * o_elem,
+                  mr * N * o_elem, cudaMemcpyHostToDevice, st)) != DG_OK)
+      return s;
+    s = run(mr, N, K, da, db, dA + r0 * a_row, lda, dB, ldb, dC + r0 * N * o_elem,
+            has_bias ? dbias : nullptr, alpha, beta, epilogue, nullptr, st);
+    if (s != DG_OK) return s;
+    if ((s = copy(static_cast<uint8_t*>(D) + r0 * N * o_elem, dC + r0 * N * o_elem,
+                  mr * N * o_elem, cudaMemcpyDeviceToHost, st)) != DG_OK)
+      return s;
+  }
+  // The caller's stream continues after both internal streams.
+  for (int i = 0; i < 2 && i < npanels; ++i) {
+    if ((e = cudaEventRecord(hw->ev_done[i], hw->aux[i])) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, hw->ev_done[i], 0)) != cudaSuccess)
+      return fail_cuda(e, "stream join");
+  }
+  return DG_OK;
+}
+
 dg_status fill_hw_desc(int device, dg_hw_desc* out) { return fill_hw(device, out); }
 
 dg_status validate_gemm_args(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
@@ -411,6 +513,14 @@ dg_status dg_plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dt
   if (s == DG_ERR_NO_VALID_CANDIDATE)
     return fail(s, "no valid candidate found after pruning: %s", why.c_str());
   return s;
+}
+
+dg_status dg_gemm_host(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                       const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+                       void* D, const void* bias, float alpha, float beta,
+                       dg_epilogue epilogue, dg_stream_t stream) {
+  return run_host(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, D, bias, alpha, beta, epilogue,
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_gemm(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
@@ -482,6 +592,18 @@ dg_status dg_shutdown(void) {
     if (kv.second.wide) cudaFree(kv.second.wide);
   }
   g_workspaces.clear();
+  for (auto& kv : g_host_ws) {
+    cudaSetDevice(kv.first.first);
+    HostWorkspace& h = kv.second;
+    for (int i = 0; i < 4; ++i)
+      if (h.buf[i]) cudaFree(h.buf[i]);
+    for (int i = 0; i < 2; ++i) {
+      if (h.aux[i]) cudaStreamDestroy(h.aux[i]);
+      if (h.ev_done[i]) cudaEventDestroy(h.ev_done[i]);
+    }
+    if (h.ev_b) cudaEventDestroy(h.ev_b);
+  }
+  g_host_ws.clear();
   for (auto& kv : g_devices) {
     if (kv.second.status) {
       cudaSetDevice(kv.first);

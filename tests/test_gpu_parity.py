@@ -440,3 +440,68 @@ def test_w4a16_every_plan(dg):
     for p in plans:
         got, _ = run_case(dg, case, plan=p)
         assert_parity(case, got)
+
+
+# ------------------------------------------------------- host-buffer entry point
+def _run_host(dg, case, pinned=True, in_place=False, stream=None):
+    def host(x):
+        t = torch.from_numpy(np.array(x, copy=True))  # never alias the case's own arrays
+        return t.pin_memory() if pinned else t
+    A, B = host(case.A), host(case.B)
+    out_dtype = torch.int32 if case.dtype_a == "i8" else torch.float16
+    C = host(case.C) if case.C is not None else None
+    if in_place:
+        assert C is not None
+        D = C
+    else:
+        D = torch.full((case.M, case.N), 3, dtype=out_dtype)
+        D = D.pin_memory() if pinned else D
+    bias = host(case.bias) if case.bias is not None else None
+    dg.gemm_host(A, B, D, C=C, K=case.K, bias=bias, alpha=case.alpha, beta=case.beta,
+                 epilogue=case.epilogue, dtype_b=case.dtype_b, stream=stream)
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    dg.check_status()
+    return D.numpy().copy()
+
+
+@pytest.mark.parametrize("spec", [
+    ("f16", "f16", (1100, 700, 900), "bias_gelu", 0.5),     # tensor cores, 3 row panels
+    ("f16", "f16", (4096, 4096, 4096), "none", 0.5),        # the square workload
+    ("f16", "f16", (5, 3000, 2000), "bias", -1.0),          # thin GEMV
+    ("i8", "i8", (600, 520, 700), "none", 2.0),             # exact INT32
+    ("f16", "e2m1", (16, 900, 1536), "bias_gelu", 0.0),     # skinny
+    ("f16", "e2m1", (520, 1000, 400), "gelu", 0.25),        # converting / widened
+], ids=lambda s: "%s_%s_%dx%dx%d_%s" % (s[0], s[1], *s[2], s[3]))
+def test_gemm_host(dg, spec):
+    da, db, (M, N, K), epi, beta = spec
+    case = workloads.random_case(M, N, K, da, db, epilogue=epi, beta=beta,
+                                 alpha=1 if da == "i8" else 0.75, seed=M + N + K, pad=0)
+    got = _run_host(dg, case)
+    assert_parity(case, got)
+
+
+def test_gemm_host_pageable_in_place_and_reuse(dg):
+    # pageable host memory; D == C; shapes that grow and shrink the workspace;
+    # back-to-back calls on one stream with no synchronisation between them
+    cases = [workloads.random_case(300, 256, 512, epilogue="bias", beta=0.5, seed=61),
+             workloads.random_case(1500, 520, 640, beta=-0.5, seed=62),
+             workloads.random_case(40, 100, 64, epilogue="gelu", beta=1.0, seed=63)]
+    for cs in cases:
+        assert_parity(cs, _run_host(dg, cs, pinned=False, in_place=True))
+    s = torch.cuda.Stream()
+    outs = []
+    hosts = []
+    for cs in cases:
+        A = torch.from_numpy(cs.A).pin_memory()
+        B = torch.from_numpy(cs.B).pin_memory()
+        C = torch.from_numpy(cs.C).pin_memory()
+        D = torch.empty(cs.M, cs.N, dtype=torch.float16).pin_memory()
+        bias = torch.from_numpy(cs.bias).pin_memory() if cs.bias is not None else None
+        dg.gemm_host(A, B, D, C=C, bias=bias, alpha=cs.alpha, beta=cs.beta,
+                     epilogue=cs.epilogue, stream=s)
+        hosts.append((A, B, C, bias))
+        outs.append(D)
+    s.synchronize()
+    dg.check_status(s)
+    for cs, D in zip(cases, outs):
+        assert_parity(cs, D.numpy())
