@@ -27,5 +27,7 @@ from .gemm_ref import (  # noqa: F401
     gelu_erf,
     gemm_reference,
     error_bound,
+    apply_program,
+    PROGRAM_OPS,
     GELU_LIPSCHITZ,
 )

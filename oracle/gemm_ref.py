@@ -27,10 +27,20 @@ Functions and what each follows:
       kwkr.cn section 2.2 third layer + section 3.2 step 3.  Pinned by closed
       forms (identity, permutation, all-ones, rank-1, int8 extremes) and by
       exact rational brute force on tiny shapes.
+  apply_program -- an epilogue program: ops applied in order to t (the
+      op_type registry of the fused epilogue, kwkr.cn section 2.2 third layer:
+      bias add, ReLU, quantization-style scale and saturation; discosf.com
+      section 6.1: GELU chosen by op type).  Reading taken: each op is the
+      plain real function (t + bias_j, max(t, 0), GELU, a * t, min(max(t, lo),
+      hi)); the op operands a, lo, hi are binary32 numbers, the type the C ABI
+      passes them in.  Pinned by hand-computed values and order-sensitivity
+      cases.
   error_bound -- the floating-point acceptance bound
       2^-10 * (|A|.|B|)_ij + 2^-10 * |D_ref|_ij, with (|A|.|B|) read as the
       magnitude of every term that enters t, a 2^-24 floor, and a GELU
-      Lipschitz factor.  Pinned by direct checks on hand-computed cases.
+      Lipschitz factor; for a program, the input error carried through each
+      op by its Lipschitz constant.  Pinned by direct checks on hand-computed
+      cases.
 """
 
 import math
@@ -44,6 +54,9 @@ E2M1_BITS = (1, 2, 1)
 GELU_LIPSCHITZ = 1.13
 
 _EPILOGUES = ("none", "bias", "gelu", "bias_gelu")
+
+# Ops of an epilogue program and the number of operands each takes.
+PROGRAM_OPS = {"bias": 0, "relu": 0, "gelu": 0, "scale": 1, "clamp": 2}
 
 
 def e2m1_value(code):
@@ -107,6 +120,50 @@ def gelu_erf(t):
     return 0.5 * t * (1.0 + _erf(t / math.sqrt(2.0)))
 
 
+def _normalise_program(program):
+    """[(name, operands...)] with binary32-rounded operands, validated."""
+    out = []
+    for op in program:
+        if isinstance(op, str):
+            op = (op,)
+        name, args = op[0], tuple(op[1:])
+        if name not in PROGRAM_OPS:
+            raise ValueError("unknown epilogue op %r" % (name,))
+        if len(args) != PROGRAM_OPS[name]:
+            raise ValueError("op %r takes %d operands" % (name, PROGRAM_OPS[name]))
+        args = tuple(float(np.float32(x)) for x in args)
+        if name == "clamp" and not args[0] <= args[1]:
+            raise ValueError("clamp needs lo <= hi")
+        out.append((name,) + args)
+    return out
+
+
+def apply_program(t, program, bias=None):
+    """The epilogue program's ops, in order, on t (float64, [rows, N]).
+
+    bias (float16 [N]) is read by the "bias" op: t_ij + bias_j.
+    """
+    t = np.asarray(t, dtype=np.float64)
+    for op in _normalise_program(program):
+        name = op[0]
+        if name == "bias":
+            if bias is None:
+                raise ValueError("a bias op needs a bias vector")
+            bias = np.asarray(bias)
+            if bias.dtype != np.float16:
+                raise TypeError("bias must be float16")
+            t = t + bias.astype(np.float64)[None, :]
+        elif name == "relu":
+            t = np.where(t > 0.0, t, 0.0)
+        elif name == "gelu":
+            t = gelu_erf(t)
+        elif name == "scale":
+            t = op[1] * t
+        else:  # clamp
+            t = np.minimum(np.maximum(t, op[1]), op[2])
+    return t
+
+
 def _operand_a(A, dtype_a):
     if dtype_a == "f16":
         A = np.asarray(A)
@@ -148,16 +205,20 @@ def _wrap_int32(x_u64):
 
 
 def gemm_reference(A, B, K, dtype_a="f16", dtype_b="f16", C=None, bias=None,
-                   alpha=1.0, beta=0.0, epilogue="none", rows=None):
+                   alpha=1.0, beta=0.0, epilogue="none", rows=None, program=None):
     """D_ref for every row (or only for ``rows``) of the output.
 
     Floating-point pairs return float64 (no output rounding).  The int8 pair
     returns int64 values in the int32 range: the exact integer sum, then
     alpha*acc + beta*C taken modulo 2^32 (alpha and beta must be integers).
+    ``program`` (a list of ops, see apply_program) replaces ``epilogue``:
+    D = program(alpha*acc + beta*C).
     """
     _check_pair(dtype_a, dtype_b)
     if epilogue not in _EPILOGUES:
         raise ValueError("unknown epilogue %r" % (epilogue,))
+    if program and epilogue != "none":
+        raise ValueError("give an epilogue or a program, not both")
     A = np.asarray(A)
     if rows is not None:
         rows = np.asarray(rows, dtype=np.int64)
@@ -172,8 +233,8 @@ def gemm_reference(A, B, K, dtype_a="f16", dtype_b="f16", C=None, bias=None,
     acc = a @ b.T
 
     if dtype_a == "i8":
-        if epilogue != "none" or bias is not None:
-            raise ValueError("the int8 path has no bias/GELU epilogue")
+        if epilogue != "none" or bias is not None or program:
+            raise ValueError("the int8 path has no bias/GELU epilogue or program")
         if float(alpha) != int(alpha) or float(beta) != int(beta):
             raise ValueError("the int8 path takes integral alpha and beta")
         # |acc| <= K * 2^14, an integer below 2^53 for K < 2^39, hence exact.
@@ -195,6 +256,8 @@ def gemm_reference(A, B, K, dtype_a="f16", dtype_b="f16", C=None, bias=None,
         if C.dtype != np.float16:
             raise TypeError("C must be float16 on the floating-point paths")
         t = t + float(beta) * C.astype(np.float64)
+    if program:
+        return apply_program(t, program, bias)
     if epilogue in ("bias", "bias_gelu"):
         if bias is None:
             raise ValueError("bias epilogue needs a bias vector")
@@ -208,7 +271,7 @@ def gemm_reference(A, B, K, dtype_a="f16", dtype_b="f16", C=None, bias=None,
 
 
 def error_bound(A, B, K, D_ref, dtype_a="f16", dtype_b="f16", C=None, bias=None,
-                alpha=1.0, beta=0.0, epilogue="none", rows=None):
+                alpha=1.0, beta=0.0, epilogue="none", rows=None, program=None):
     """Per-element acceptance bound for floating-point results.
 
     bound = g * 2^-10 * P_ij + 2^-10 * |D_ref|_ij + 2^-24, where
@@ -217,6 +280,12 @@ def error_bound(A, B, K, D_ref, dtype_a="f16", dtype_b="f16", C=None, bias=None,
     without GELU and g = GELU_LIPSCHITZ with it (an error in t moves GELU(t)
     by at most that factor), and 2^-24 (the smallest fp16 subnormal) lets
     exact zeros and fp16-subnormal outputs compare.
+
+    With a program, E = 2^-10 * P_0 (P_0 without the bias) is the error
+    allowed in t on entry and each op carries it forward: a bias op adds
+    2^-10 |bias_j|, GELU multiplies it by GELU_LIPSCHITZ, scale by |a|, ReLU
+    and clamp (Lipschitz 1) keep it; every op adds 2^-20 |t| after it for the
+    binary32 rounding of that op.  bound = E + 2^-10 |D_ref| + 2^-24.
     """
     _check_pair(dtype_a, dtype_b)
     A = np.asarray(A)
@@ -230,6 +299,23 @@ def error_bound(A, B, K, D_ref, dtype_a="f16", dtype_b="f16", C=None, bias=None,
     P = abs(float(alpha)) * (a @ b.T)
     if beta != 0.0 and C is not None:
         P = P + abs(float(beta)) * np.abs(np.asarray(C).astype(np.float64))
+    if program:
+        # t on entry, recomputed from its definition to track |t| per op
+        t = float(alpha) * (_operand_a(A[:, :K], dtype_a) @ _operand_b(B, dtype_b, K).T)
+        if beta != 0.0 and C is not None:
+            t = t + float(beta) * np.asarray(C).astype(np.float64)
+        E = 2.0 ** -10 * P
+        for op in _normalise_program(program):
+            name = op[0]
+            if name == "bias":
+                E = E + 2.0 ** -10 * np.abs(np.asarray(bias).astype(np.float64))[None, :]
+            elif name == "gelu":
+                E = GELU_LIPSCHITZ * E
+            elif name == "scale":
+                E = abs(op[1]) * E
+            t = apply_program(t, [op], bias)
+            E = E + 2.0 ** -20 * np.abs(t)
+        return E + 2.0 ** -10 * np.abs(D_ref) + 2.0 ** -24
     if epilogue in ("bias", "bias_gelu") and bias is not None:
         P = P + np.abs(np.asarray(bias).astype(np.float64))[None, :]
     g = GELU_LIPSCHITZ if epilogue in ("gelu", "bias_gelu") else 1.0

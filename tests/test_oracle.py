@@ -302,10 +302,61 @@ def check_rows_subset(fn):
     return np.array_equal(part, full[rows])
 
 
+# Epilogue programs.  acc = [-3, 0.5, 2, 7] from a K = 1 product; every
+# expected row below is worked out by hand from the op definitions (t + b_j,
+# max(t, 0), GELU(t) = t Phi(t), a t, min(max(t, lo), hi)), applied in order.
+_PROG_A = _f16([[1.0]])
+_PROG_B = _f16([[-3.0], [0.5], [2.0], [7.0]])
+_PROG_BIAS = _f16([1.0, -1.0, 0.5, -8.0])
+_PROG_CASES = [
+    ([], 1.0, [-3.0, 0.5, 2.0, 7.0]),
+    (["relu"], 1.0, [0.0, 0.5, 2.0, 7.0]),
+    ([("scale", -0.5)], 1.0, [1.5, -0.25, -1.0, -3.5]),
+    ([("clamp", -1.0, 2.5)], 1.0, [-1.0, 0.5, 2.0, 2.5]),
+    (["relu", ("scale", -1.0)], 1.0, [0.0, -0.5, -2.0, -7.0]),
+    ([("scale", -1.0), "relu"], 1.0, [3.0, 0.0, 0.0, 0.0]),
+    (["bias", "relu"], 1.0, [0.0, 0.0, 2.5, 0.0]),
+    (["relu", "bias"], 1.0, [1.0, -0.5, 2.5, -1.0]),
+    (["relu", ("clamp", 0.25, 1.0), ("scale", 4.0)], 2.0, [1.0, 4.0, 4.0, 4.0]),
+]
+
+
+def check_program_by_hand(fn):
+    for prog, alpha, want in _PROG_CASES:
+        got = fn(_PROG_A, _PROG_B, 1, bias=_PROG_BIAS, alpha=alpha, program=prog)
+        if not np.array_equal(got, np.array([want])):
+            return False
+    return True
+
+
+def check_program_after_alpha_beta(fn):
+    # t = 2 acc - C = [-7, 0, 3, 13], then clamp to [-5, 5]
+    C = _f16([[1.0, 1.0, 1.0, 1.0]])
+    got = fn(_PROG_A, _PROG_B, 1, C=C, alpha=2.0, beta=-1.0, program=[("clamp", -5.0, 5.0)])
+    return np.array_equal(got, np.array([[-5.0, 0.0, 3.0, 5.0]]))
+
+
+def check_program_gelu_table(fn):
+    # GELU(x) = x Phi(x) with Phi from the printed normal-CDF table (10 digits),
+    # after a bias op that moves acc = [-3, 0.5, 2, 7] to [-2, -0.5, 2.5, -1]
+    phi = {float(x): float(p) for x, p in _read_pairs("normal_cdf.txt")}
+    got = fn(_PROG_A, _PROG_B, 1, bias=_PROG_BIAS, program=["bias", "gelu"])
+    want = [-2.0 * phi[-2.0], -0.5 * (1.0 - phi[0.5]), 2.5 * phi[2.5], -1.0 * phi[-1.0]]
+    return np.allclose(got, np.array([want]), rtol=0, atol=1e-9)
+
+
+def check_program_operands_are_binary32(fn):
+    # 0.1 is passed as the binary32 number 13421773 / 2^27, not the decimal 0.1
+    got = fn(_PROG_A, _f16([[1.0]]), 1, program=[("scale", 0.1)])
+    return got[0, 0] == 13421773 / 2.0 ** 27
+
+
 ALL_CHECKS = [check_identity, check_permutation, check_all_ones, check_rank1,
               check_rectangular_orientation, check_epilogue_alpha_beta_bias,
               check_gelu_after_bias, check_int8_extremes, check_int8_wrap,
-              check_e2m1_one_hot, check_brute_force, check_rows_subset]
+              check_e2m1_one_hot, check_brute_force, check_rows_subset,
+              check_program_by_hand, check_program_after_alpha_beta, check_program_gelu_table,
+              check_program_operands_are_binary32]
 
 
 def _ref(A, B, K, dtype_a="f16", dtype_b="f16", **kw):
@@ -416,18 +467,58 @@ class _BiasBeforeAlpha:
         old = self.old
 
         def patched(A, B, K, dtype_a="f16", dtype_b="f16", C=None, bias=None, alpha=1.0,
-                    beta=0.0, epilogue="none", rows=None):
-            if bias is not None and epilogue in ("bias", "bias_gelu"):
+                    beta=0.0, epilogue="none", rows=None, program=None):
+            if bias is not None and (epilogue in ("bias", "bias_gelu") or program):
                 bias = (np.asarray(bias, dtype=np.float64) * alpha).astype(np.float16)
             return old(A, B, K, dtype_a, dtype_b, C=C, bias=bias, alpha=alpha, beta=beta,
-                       epilogue=epilogue, rows=rows)
+                       epilogue=epilogue, rows=rows, program=program)
         oracle.gemm_reference = patched
 
     def __exit__(self, *a):
         oracle.gemm_reference = self.old
 
 
+_ORIG_APPLY_PROGRAM = gemm_ref.apply_program
+
+
+def _mut_program_reversed(t, program, bias=None):
+    return _ORIG_APPLY_PROGRAM(t, list(program)[::-1], bias)
+
+
+def _mut_relu_abs(t, program, bias=None):
+    for op in program:
+        if op == "relu" or (isinstance(op, tuple) and op[0] == "relu"):
+            t = np.abs(np.asarray(t, dtype=np.float64))
+        else:
+            t = _ORIG_APPLY_PROGRAM(t, [op], bias)
+    return t
+
+
+def _mut_clamp_order(t, program, bias=None):
+    # the bounds swapped: max(min(t, lo), hi)
+    for op in program:
+        if isinstance(op, tuple) and op[0] == "clamp":
+            t = np.maximum(np.minimum(t, op[1]), op[2])
+        else:
+            t = _ORIG_APPLY_PROGRAM(t, [op], bias)
+    return t
+
+
+def _mut_scale_decimal(t, program, bias=None):
+    # scale operand kept as the decimal (binary64) value, not binary32
+    for op in program:
+        if isinstance(op, tuple) and op[0] == "scale":
+            t = op[1] * np.asarray(t, dtype=np.float64)
+        else:
+            t = _ORIG_APPLY_PROGRAM(t, [op], bias)
+    return t
+
+
 MUTANTS = {
+    "program_reversed": _Swap("apply_program", _mut_program_reversed),
+    "relu_as_abs": _Swap("apply_program", _mut_relu_abs),
+    "clamp_order": _Swap("apply_program", _mut_clamp_order),
+    "scale_binary64": _Swap("apply_program", _mut_scale_decimal),
     "transposed_B": _Swap("_operand_b", _mut_transpose_b),
     "swapped_nibbles": _Swap("unpack_e2m1", _mut_nibbles),
     "tanh_gelu": _Swap("gelu_erf", _mut_tanh_gelu),
@@ -485,3 +576,35 @@ def test_fp16_rounding_fits_in_bound():
     rounded = vals.astype(np.float16).astype(np.float64)
     bound = 2.0 ** -10 * np.abs(vals) + 2.0 ** -24
     assert np.all(np.abs(rounded - vals) <= bound)
+
+
+def test_error_bound_program_terms():
+    # acc = [2, 1], t = 2 acc = [4, 2], P_0 = 2 (|A|.|B|) = [8, 6]
+    A = _f16([[1.0, -2.0]])
+    B = _f16([[3.0, 0.5], [-1.0, -1.0]])
+    prog = [("scale", -0.5), "relu", "gelu"]
+    D = oracle.gemm_reference(A, B, 2, alpha=2.0, program=prog)
+    assert np.array_equal(D, np.array([[0.0, 0.0]]))  # scale -> [-2, -1], relu -> 0, GELU(0) = 0
+    bnd = oracle.error_bound(A, B, 2, D, alpha=2.0, program=prog)
+    # scale: 0.5 * 2^-10 [8, 6] + 2^-20 [2, 1]; relu: + 0; GELU: * 1.13, + 0
+    want = 1.13 * (2.0 ** -10 * np.array([[4.0, 3.0]]) + 2.0 ** -20 * np.array([[2.0, 1.0]]))
+    assert np.allclose(bnd, want + 2.0 ** -24, rtol=1e-15, atol=0)
+    bias = _f16([0.5, -4.0])
+    prog = ["bias", ("clamp", -1.0, 1.0)]
+    D = oracle.gemm_reference(A, B, 2, bias=bias, alpha=2.0, program=prog)
+    assert np.array_equal(D, np.array([[1.0, -1.0]]))  # t + bias = [4.5, -2]
+    bnd = oracle.error_bound(A, B, 2, D, bias=bias, alpha=2.0, program=prog)
+    want = (2.0 ** -10 * np.array([[8.5, 10.0]]) + 2.0 ** -20 * np.array([[4.5, 2.0]])
+            + 2.0 ** -20 * np.array([[1.0, 1.0]]) + 2.0 ** -10 * np.array([[1.0, 1.0]]) + 2.0 ** -24)
+    assert np.allclose(bnd, want, rtol=1e-15, atol=0)
+
+
+def test_program_rejects_bad_ops():
+    A, B = _PROG_A, _PROG_B
+    for prog in (["tanh"], [("scale",)], [("clamp", 2.0, 1.0)], [("relu", 1.0)]):
+        with pytest.raises(ValueError):
+            oracle.gemm_reference(A, B, 1, program=prog)
+    with pytest.raises(ValueError):
+        oracle.gemm_reference(A, B, 1, program=["bias"])  # no bias vector
+    with pytest.raises(ValueError):
+        oracle.gemm_reference(A, B, 1, epilogue="gelu", program=["relu"])
