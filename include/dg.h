@@ -73,6 +73,32 @@ typedef enum {
   DG_EPI_BIAS_GELU = 3
 } dg_epilogue;
 
+/* Epilogue programs: the op_type registry of the pages' epilogue generator
+ * (kwkr.cn/news/562171, section 2.2 third layer: post-processing such as
+ * bias add, ReLU and quantization fused into the GEMM; discosf.com/news/
+ * 5532976, section 6.1: an epilogue chosen by op_type, e.g. "gelu").  A
+ * program is up to DG_MAX_EPILOGUE_OPS ops applied in order to
+ * t = alpha*acc + beta*C, in FP32, before the single rounding to FP16. */
+#define DG_MAX_EPILOGUE_OPS 8
+typedef enum {
+  DG_OP_BIAS = 1,  /* t += bias[j] (FP16 [N]) */
+  DG_OP_RELU = 2,  /* t = max(t, 0); a NaN t becomes 0 */
+  DG_OP_GELU = 3,  /* t = 0.5*t*(1 + erf(t/sqrt(2))) */
+  DG_OP_SCALE = 4, /* t = t * a (e.g. a dequantization or output scale) */
+  DG_OP_CLAMP = 5  /* t = min(max(t, a), b), a <= b (saturation before a narrow output);
+                      a NaN t becomes a */
+} dg_op_type;
+
+typedef struct {
+  int type;    /* dg_op_type */
+  float a, b;  /* operands of DG_OP_SCALE (a) and DG_OP_CLAMP (a, b); ignored otherwise */
+} dg_epilogue_op;
+
+typedef struct {
+  int n_ops; /* 0 .. DG_MAX_EPILOGUE_OPS */
+  dg_epilogue_op ops[DG_MAX_EPILOGUE_OPS];
+} dg_epilogue_program;
+
 /* Kernel families a plan can select. */
 typedef enum {
   DG_KERNEL_TC = 0,    /* tensor-core pipeline: TMA -> SMEM ring -> tcgen05.mma -> TMEM -> fused epilogue */
@@ -179,6 +205,27 @@ dg_status dg_gemm_host(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dty
                        const void *A, int64_t lda, const void *B, int64_t ldb, const void *C,
                        void *D, const void *bias, float alpha, float beta,
                        dg_epilogue epilogue, dg_stream_t stream);
+
+/* D = program(alpha * A.B + beta * C) with separate C and D buffers.
+ * The general form of dg_gemm (kwkr.cn/news/562171, section 3.2 step 3: the
+ * generated kernel takes A, B, C, alpha, beta; section 2.2 third layer: the
+ * fused post-processing ops), BLAS-style: C is read, D is written.
+ *   C: M x N, leading dimension ldc >= N, read only when beta != 0 (may then
+ *     be NULL otherwise); D: M x N, leading dimension ldd >= N.  Both FP16,
+ *     or INT32 for I8 x I8; both 16-byte aligned.  C and D are the same
+ *     buffer with ldc == ldd (in place) or do not overlap; columns N .. ld-1
+ *     of D are never written.
+ *   program: NULL or n_ops == 0 for none.  For I8 x I8 (exact INT32 output)
+ *     it must be empty.  DG_OP_BIAS needs bias (FP16 [N]), which is read
+ *     only by that op.
+ *   Plan, kernels, workspaces and errors as dg_gemm; DG_ERR_INVALID_ARG for
+ *   ldc < N (with beta != 0), ldd < N, a NULL D, more than
+ *   DG_MAX_EPILOGUE_OPS ops, an unknown op type or a clamp with a > b (or a
+ *   NaN bound); DG_ERR_UNSUPPORTED for a program on I8 x I8. */
+dg_status dg_gemm_ex(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                     const void *A, int64_t lda, const void *B, int64_t ldb, const void *C,
+                     int64_t ldc, void *D, int64_t ldd, const void *bias, float alpha, float beta,
+                     const dg_epilogue_program *program, dg_stream_t stream);
 
 /* As dg_gemm, but runs `plan` (one returned by dg_plan_tiles for the same
  * M, N, K and dtypes).  DG_ERR_INVALID_STATE when the plan does not fit. */

@@ -12,7 +12,8 @@ import os
 
 __all__ = [
     "DgError", "F16", "I8", "E2M1", "EPILOGUES", "lib", "lib_path", "gemm", "gemm_raw",
-    "gemm_host", "gemm_host_raw",
+    "gemm_host", "gemm_host_raw", "gemm_ex", "gemm_ex_raw", "OPS", "MAX_EPILOGUE_OPS",
+    "EpilogueOp", "EpilogueProgram", "make_program",
     "plan_tiles", "query_hw", "last_error", "check_status", "set_wait_timeout_ns",
     "selftest_wait_timeout", "launch_count", "shutdown", "HwDesc", "TilePlan", "EXPORTS",
 ]
@@ -20,6 +21,8 @@ __all__ = [
 F16, I8, E2M1 = 0, 1, 2
 DTYPES = {"f16": F16, "i8": I8, "e2m1": E2M1}
 EPILOGUES = {"none": 0, "bias": 1, "gelu": 2, "bias_gelu": 3}
+OPS = {"bias": 1, "relu": 2, "gelu": 3, "scale": 4, "clamp": 5}
+MAX_EPILOGUE_OPS = 8
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
           3: "DG_ERR_NO_VALID_CANDIDATE", 4: "DG_ERR_CUDA", 5: "DG_ERR_TIMEOUT",
           6: "DG_ERR_INVALID_STATE"}
@@ -27,6 +30,7 @@ KERNELS = {0: "tc", 1: "gemv", 2: "tc_widened", 3: "skinny", -1: "none"}
 
 # Every symbol include/dg.h declares.
 EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_gemm_host",
+           "dg_gemm_ex",
            "dg_gemm_thin_noalloc", "dg_last_error",
            "dg_check_status", "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout",
            "dg_launch_count", "dg_shutdown"]
@@ -74,6 +78,31 @@ class TilePlan(ctypes.Structure):
 _lib = None
 
 
+class EpilogueOp(ctypes.Structure):
+    _fields_ = [("type", ctypes.c_int), ("a", ctypes.c_float), ("b", ctypes.c_float)]
+
+
+class EpilogueProgram(ctypes.Structure):
+    _fields_ = [("n_ops", ctypes.c_int), ("ops", EpilogueOp * MAX_EPILOGUE_OPS)]
+
+
+def make_program(ops):
+    """EpilogueProgram from a list of ops: "relu", "gelu", "bias",
+    ("scale", a), ("clamp", lo, hi), or (type_code, a, b)."""
+    ops = list(ops)
+    if len(ops) > MAX_EPILOGUE_OPS:
+        raise ValueError("at most %d epilogue ops" % MAX_EPILOGUE_OPS)
+    prog = EpilogueProgram()
+    prog.n_ops = len(ops)
+    for k, op in enumerate(ops):
+        if isinstance(op, str):
+            op = (op,)
+        code = OPS[op[0]] if isinstance(op[0], str) else int(op[0])
+        args = [float(x) for x in op[1:]] + [0.0, 0.0]
+        prog.ops[k] = EpilogueOp(code, args[0], args[1])
+    return prog
+
+
 def lib():
     """The loaded libdg.so (raises if it has not been built)."""
     global _lib
@@ -94,6 +123,8 @@ def lib():
     L.dg_gemm_thin_noalloc.argtypes = gemm_args + [vp]
     L.dg_gemm_host.argtypes = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, vp, vp, f32, f32,
                                i32, vp]
+    L.dg_gemm_ex.argtypes = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, f32,
+                             f32, ctypes.POINTER(EpilogueProgram), vp]
     L.dg_last_error.restype = ctypes.c_char_p
     L.dg_last_error.argtypes = []
     L.dg_check_status.argtypes = [vp]
@@ -103,7 +134,7 @@ def lib():
     L.dg_launch_count.argtypes = []
     L.dg_shutdown.argtypes = []
     for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
-                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_check_status",
+                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_gemm_ex", "dg_check_status",
                  "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout", "dg_shutdown"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -206,6 +237,54 @@ def gemm(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none", dtype
     gemm_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue,
              stream=stream, plan=plan)
     return C
+
+
+def gemm_ex_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, ldc, D, ldd, bias, alpha, beta,
+                program=None, stream=None):
+    """dg_gemm_ex with the C argument order.  program: None, an
+    EpilogueProgram, or a list of ops for make_program."""
+    if program is not None and not isinstance(program, EpilogueProgram):
+        program = make_program(program)
+    args = (int(M), int(N), int(K), _dtype_code(dtype_a), _dtype_code(dtype_b), _ptr(A), int(lda),
+            _ptr(B), int(ldb), _ptr(C), int(ldc), _ptr(D), int(ldd), _ptr(bias), float(alpha),
+            float(beta), ctypes.byref(program) if program is not None else None,
+            _stream_handle(stream))
+    _check(lib().dg_gemm_ex(*args))
+
+
+def gemm_ex(A, B, D, C=None, K=None, bias=None, alpha=1.0, beta=0.0, program=(), dtype_b=None,
+            stream=None):
+    """D = program(alpha * A.B + beta * C) with C read and D written.
+
+    A and B as in gemm(); C and D are [M, N] views with unit column stride
+    and any row stride (leading dimension) >= N, e.g. column slices of wider
+    buffers; C may be D itself.  program: list of ops, applied in order
+    ("bias", "relu", "gelu", ("scale", a), ("clamp", lo, hi)).
+    """
+    import torch
+    dtype_a = "i8" if A.dtype == torch.int8 else "f16"
+    if dtype_b is None:
+        dtype_b = {torch.float16: "f16", torch.int8: "i8", torch.uint8: "e2m1"}[B.dtype]
+    _expect(A, dtype_a, "A")
+    _expect(B, dtype_b, "B")
+    out = "i32" if dtype_a == "i8" else "f16"
+    _expect(D, out, "D")
+    M, N = D.shape
+    ldc = D.stride(0)
+    if C is not None:
+        _expect(C, out, "C")
+        if tuple(C.shape) != (M, N):
+            raise ValueError("C must be [M, N] like D")
+        ldc = C.stride(0)
+    if A.shape[0] != M or B.shape[0] != N:
+        raise ValueError("shape mismatch: A %s, B %s, D %s" % (tuple(A.shape), tuple(B.shape),
+                                                               tuple(D.shape)))
+    if K is None:
+        K = A.shape[1]
+    ldb = B.stride(0) * (2 if dtype_b == "e2m1" else 1)
+    gemm_ex_raw(M, N, K, dtype_a, dtype_b, A, A.stride(0), B, ldb, C, ldc, D, D.stride(0), bias,
+                alpha, beta, program=make_program(program or []), stream=stream)
+    return D
 
 
 def gemm_host_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, D, bias, alpha, beta, epilogue,

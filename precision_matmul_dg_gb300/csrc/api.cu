@@ -145,32 +145,79 @@ int elem_bits(dg_dtype t) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A call's epilogue as the kernels take it: kEpiBias | kEpiGelu for the
+// fixed forms, kEpiProgram (+ kEpiBias when an op reads the bias) for a
+// program.
+struct EpiSpec {
+  int flags = 0;
+  int n_ops = 0;
+  EpiOp ops[kMaxEpiOps] = {};
+};
+
+dg_status fixed_epilogue(dg_epilogue e, EpiSpec* out) {
+  if (e < DG_EPI_NONE || e > DG_EPI_BIAS_GELU)
+    return fail(DG_ERR_INVALID_ARG, "unknown epilogue %d", static_cast<int>(e));
+  *out = EpiSpec{};
+  out->flags = ((e == DG_EPI_BIAS || e == DG_EPI_BIAS_GELU) ? kEpiBias : 0) |
+               ((e == DG_EPI_GELU || e == DG_EPI_BIAS_GELU) ? kEpiGelu : 0);
+  return DG_OK;
+}
+
+dg_status program_epilogue(const dg_epilogue_program* prog, EpiSpec* out) {
+  *out = EpiSpec{};
+  if (!prog || prog->n_ops == 0) return DG_OK;
+  if (prog->n_ops < 0 || prog->n_ops > kMaxEpiOps)
+    return fail(DG_ERR_INVALID_ARG, "epilogue program of %d ops (0 .. %d)", prog->n_ops,
+                kMaxEpiOps);
+  out->flags = kEpiProgram;
+  out->n_ops = prog->n_ops;
+  for (int k = 0; k < prog->n_ops; ++k) {
+    const dg_epilogue_op& op = prog->ops[k];
+    switch (op.type) {
+      case DG_OP_BIAS:
+        out->flags |= kEpiBias;
+        break;
+      case DG_OP_RELU:
+      case DG_OP_GELU:
+        break;
+      case DG_OP_SCALE:
+        if (!isfinite(op.a)) return fail(DG_ERR_INVALID_ARG, "op %d: scale is not finite", k);
+        break;
+      case DG_OP_CLAMP:
+        if (!(op.a <= op.b)) return fail(DG_ERR_INVALID_ARG, "op %d: clamp needs a <= b", k);
+        break;
+      default:
+        return fail(DG_ERR_INVALID_ARG, "op %d: unknown op type %d", k, op.type);
+    }
+    out->ops[k] = op;
+  }
+  return DG_OK;
+}
+
 dg_status validate(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const void* A,
-                   int64_t lda, const void* B, int64_t ldb, void* C, const void* bias,
-                   float alpha, float beta, dg_epilogue epi) {
+                   int64_t lda, const void* B, int64_t ldb, void* D, const void* bias,
+                   float alpha, float beta, int epi_flags) {
   const bool pair_ok = (da == DG_F16 && db == DG_F16) || (da == DG_I8 && db == DG_I8) ||
                        (da == DG_F16 && db == DG_E2M1);
   if (!pair_ok)
     return fail(DG_ERR_UNSUPPORTED, "dtype pair (%d, %d) not supported: F16xF16, I8xI8, F16xE2M1",
                 static_cast<int>(da), static_cast<int>(db));
-  if (epi < DG_EPI_NONE || epi > DG_EPI_BIAS_GELU)
-    return fail(DG_ERR_INVALID_ARG, "unknown epilogue %d", static_cast<int>(epi));
   if (M < 0 || N < 0 || K < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
   if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30))
     return fail(DG_ERR_INVALID_ARG, "size above 2^30");
   if (M == 0 || N == 0) return DG_OK;
-  if (!C) return fail(DG_ERR_INVALID_ARG, "C/D is null");
-  if (!aligned16(C)) return fail(DG_ERR_INVALID_ARG, "C/D is not 16-byte aligned");
+  if (!D) return fail(DG_ERR_INVALID_ARG, "C/D is null");
+  if (!aligned16(D)) return fail(DG_ERR_INVALID_ARG, "C/D is not 16-byte aligned");
   if (da == DG_I8) {
-    if (epi != DG_EPI_NONE)
-      return fail(DG_ERR_UNSUPPORTED, "the INT8 path has no bias/GELU epilogue");
+    if (epi_flags != 0)
+      return fail(DG_ERR_UNSUPPORTED, "the INT8 path has no bias/GELU epilogue or program");
     if (!(isfinite(alpha) && isfinite(beta)) || alpha != floorf(alpha) || beta != floorf(beta) ||
         fabsf(alpha) >= 2147483648.0f || fabsf(beta) >= 2147483648.0f)
       return fail(DG_ERR_UNSUPPORTED, "the INT8 path takes integral alpha and beta below 2^31");
   } else if (!(isfinite(alpha) && isfinite(beta))) {
     return fail(DG_ERR_INVALID_ARG, "alpha and beta must be finite");
   }
-  if ((epi == DG_EPI_BIAS || epi == DG_EPI_BIAS_GELU)) {
+  if (epi_flags & kEpiBias) {
     if (!bias) return fail(DG_ERR_INVALID_ARG, "bias epilogue with a null bias");
     if (reinterpret_cast<uintptr_t>(bias) & 1u)
       return fail(DG_ERR_INVALID_ARG, "bias is not 2-byte aligned");
@@ -239,13 +286,27 @@ dg_status get_wide_workspace(int dev, cudaStream_t stream, int64_t elems, __half
   return DG_OK;
 }
 
+// D (leading dimension ldd) = epilogue(alpha * A.B + beta * C (ldc)).  The
+// caller has validated the epilogue; C and D are checked here.
 dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const void* A,
-              int64_t lda, const void* B, int64_t ldb, void* C, const void* bias, float alpha,
-              float beta, dg_epilogue epilogue, const dg_tile_plan* forced, cudaStream_t stream) {
-  clear_error();
-  dg_status s = validate(M, N, K, da, db, A, lda, B, ldb, C, bias, alpha, beta, epilogue);
+              int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc, void* D,
+              int64_t ldd, const void* bias, float alpha, float beta, const EpiSpec& epi,
+              const dg_tile_plan* forced, cudaStream_t stream) {
+  dg_status s = validate(M, N, K, da, db, A, lda, B, ldb, D, bias, alpha, beta, epi.flags);
   if (s != DG_OK) return s;
   if (M == 0 || N == 0) return DG_OK;
+  if (ldd < N) return fail(DG_ERR_INVALID_ARG, "ldd (%lld) < N (%lld)", (long long)ldd, (long long)N);
+  if (beta != 0.0f) {
+    if (!C) return fail(DG_ERR_INVALID_ARG, "beta != 0 with a null C");
+    if (!aligned16(C)) return fail(DG_ERR_INVALID_ARG, "C is not 16-byte aligned");
+    if (ldc < N)
+      return fail(DG_ERR_INVALID_ARG, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
+    if (C == D && ldc != ldd)
+      return fail(DG_ERR_INVALID_ARG, "C and D share a buffer with ldc != ldd");
+  } else {
+    C = D;  // never read
+    ldc = ldd;
+  }
   DeviceState* st = nullptr;
   s = device_state(&st);
   if (s != DG_OK) return s;
@@ -263,11 +324,15 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
   a.B = B;
   a.ldb = ldb;
   a.C = C;
+  a.ldc = ldc;
+  a.D = D;
+  a.ldd = ldd;
   a.bias = bias;
   a.alpha = alpha;
   a.beta = beta;
-  a.epi = ((epilogue == DG_EPI_BIAS || epilogue == DG_EPI_BIAS_GELU) ? kEpiBias : 0) |
-          ((epilogue == DG_EPI_GELU || epilogue == DG_EPI_BIAS_GELU) ? kEpiGelu : 0);
+  a.epi = epi.flags;
+  a.n_ops = epi.n_ops;
+  for (int k = 0; k < kMaxEpiOps; ++k) a.ops[k] = epi.ops[k];
   a.stream = stream;
   a.status = st->status;
   a.timeout_ns = timeout_ns();
@@ -286,8 +351,8 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
       return fail(DG_ERR_INVALID_STATE, "plan not runnable: %s", why.c_str());
     plan = *forced;
   } else {
-    const auto key = std::make_tuple(dev, M, N, K, static_cast<int>(da), static_cast<int>(db),
-                                     static_cast<int>(epilogue));
+    // The planner's choice does not depend on the epilogue.
+    const auto key = std::make_tuple(dev, M, N, K, static_cast<int>(da), static_cast<int>(db), 0);
     bool have = false;
     {
       std::lock_guard<std::mutex> lock(g_mu);
@@ -300,7 +365,7 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
     if (!have) {
       std::string why;
       int n = 0;
-      s = plan_tiles(M, N, K, da, db, epilogue, st->hw, 0.0, &plan, 1, &n, &why);
+      s = plan_tiles(M, N, K, da, db, DG_EPI_NONE, st->hw, 0.0, &plan, 1, &n, &why);
       if (s != DG_OK || n == 0)
         return fail(DG_ERR_NO_VALID_CANDIDATE, "no valid candidate found after pruning: %s",
                     why.c_str());
@@ -377,7 +442,10 @@ dg_status run_host(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, co
   clear_error();
   if (!D) return fail(DG_ERR_INVALID_ARG, "D is null");
   if (beta != 0.0f && !C) return fail(DG_ERR_INVALID_ARG, "beta != 0 with a null C");
-  dg_status s = validate(M, N, K, da, db, A, lda, B, ldb, D, bias, alpha, beta, epilogue);
+  EpiSpec epi;
+  dg_status s = fixed_epilogue(epilogue, &epi);
+  if (s != DG_OK) return s;
+  s = validate(M, N, K, da, db, A, lda, B, ldb, D, bias, alpha, beta, epi.flags);
   if (s != DG_OK) return s;
   if (M == 0 || N == 0) return DG_OK;
   int dev = 0;
@@ -444,8 +512,9 @@ dg_status run_host(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, co
         (s = copy(dC + r0 * N * o_elem, static_cast<const uint8_t*>(C) + r0 * N * o_elem,
                   mr * N * o_elem, cudaMemcpyHostToDevice, st)) != DG_OK)
       return s;
-    s = run(mr, N, K, da, db, dA + r0 * a_row, lda, dB, ldb, dC + r0 * N * o_elem,
-            has_bias ? dbias : nullptr, alpha, beta, epilogue, nullptr, st);
+    uint8_t* cd = dC + r0 * N * o_elem;
+    s = run(mr, N, K, da, db, dA + r0 * a_row, lda, dB, ldb, cd, N, cd, N,
+            has_bias ? dbias : nullptr, alpha, beta, epi, nullptr, st);
     if (s != DG_OK) return s;
     if ((s = copy(static_cast<uint8_t*>(D) + r0 * N * o_elem, dC + r0 * N * o_elem,
                   mr * N * o_elem, cudaMemcpyDeviceToHost, st)) != DG_OK)
@@ -465,7 +534,10 @@ dg_status fill_hw_desc(int device, dg_hw_desc* out) { return fill_hw(device, out
 dg_status validate_gemm_args(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
                              const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                              const void* bias, float alpha, float beta, dg_epilogue epi) {
-  return validate(M, N, K, da, db, A, lda, B, ldb, C, bias, alpha, beta, epi);
+  EpiSpec e;
+  const dg_status s = fixed_epilogue(epi, &e);
+  if (s != DG_OK) return s;
+  return validate(M, N, K, da, db, A, lda, B, ldb, C, bias, alpha, beta, e.flags);
 }
 
 }  // namespace dg
@@ -527,16 +599,36 @@ dg_status dg_gemm(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dt
                   const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                   const void* bias, float alpha, float beta, dg_epilogue epilogue,
                   dg_stream_t stream) {
-  return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue, nullptr,
-             reinterpret_cast<cudaStream_t>(stream));
+  clear_error();
+  EpiSpec epi;
+  const dg_status s = fixed_epilogue(epilogue, &epi);
+  if (s != DG_OK) return s;
+  return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, N, C, N, bias, alpha, beta, epi,
+             nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_gemm_ex(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
+                     const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+                     int64_t ldc, void* D, int64_t ldd, const void* bias, float alpha, float beta,
+                     const dg_epilogue_program* program, dg_stream_t stream) {
+  clear_error();
+  EpiSpec epi;
+  const dg_status s = program_epilogue(program, &epi);
+  if (s != DG_OK) return s;
+  return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, ldc, D, ldd, bias, alpha, beta, epi,
+             nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
                           const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                           const void* bias, float alpha, float beta, dg_epilogue epilogue,
                           const dg_tile_plan* plan, dg_stream_t stream) {
+  clear_error();
   if (!plan) return fail(DG_ERR_INVALID_ARG, "plan is null");
-  return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue, plan,
+  EpiSpec epi;
+  const dg_status s = fixed_epilogue(epilogue, &epi);
+  if (s != DG_OK) return s;
+  return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, N, C, N, bias, alpha, beta, epi, plan,
              reinterpret_cast<cudaStream_t>(stream));
 }
 

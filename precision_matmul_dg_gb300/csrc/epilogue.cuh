@@ -1,4 +1,5 @@
-// Fused epilogue of the GEMM: t = alpha*acc + beta*C + bias, then GELU.
+// Fused epilogue of the GEMM: t = alpha*acc + beta*C + bias, then GELU; or
+// t = alpha*acc + beta*C, then a program of ops.
 //
 // Order and form follow the "DeepGEMM" articles' epilogue generator
 // (kwkr.cn/news/562171, section 2.2 third layer: alpha * gemm_out + beta * ...,
@@ -10,6 +11,8 @@
 #pragma once
 
 #include <cuda_fp16.h>
+
+#include "internal.h"
 
 namespace dg {
 
@@ -31,18 +34,63 @@ __device__ __forceinline__ float gelu_erf(float t) {
   return t * (t >= 0.0f ? 1.0f - q : q);
 }
 
+// Epilogue ops of a program (dg_epilogue_op in dg.h), applied in order to
+// t = alpha * acc + beta * C: the post-processing steps the pages' epilogue
+// generator fuses into the GEMM (kwkr.cn/news/562171, section 2.2 third
+// layer: bias add, ReLU, quantize-style scaling; GELU as op_type "gelu",
+// discosf.com/news/5532976, section 6.1).
+// Kept to 16 bytes: every kernel carries it in its parameter struct, and
+// those structs stay within 128 bytes (measured on GB300: a by-value
+// parameter struct above 128 bytes slowed the streaming GEMV by 10% and the
+// tensor-core kernel by 8%).  The ops travel in their own parameter.
 struct Epi {
   float alpha, beta;
-  int flags;  // kEpiBias | kEpiGelu
+  int flags;  // kEpiBias | kEpiGelu (bias, then GELU), or kEpiProgram (+ kEpiBias if a bias op)
+  int n_ops;  // kEpiProgram: the program's ops [0, n_ops) in order
 };
 
+// A program's ops: a kernel parameter of its own (__grid_constant__).
+struct EpiProgram {
+  EpiOp ops[kMaxEpiOps];
+};
+
+// The program's ops on t; b is the column's bias (0 without a bias op).
+// ReLU and clamp ignore NaN the way fmaxf / fminf do.
+__device__ __forceinline__ float epi_program(float t, float b, const Epi& e,
+                                             const EpiProgram& prog) {
+#pragma unroll 1
+  for (int k = 0; k < e.n_ops; ++k) {
+    const EpiOp op = prog.ops[k];
+    switch (op.type) {  // kOpScale: t *= a; kOpClamp: t = min(max(t, a), b)
+      case kOpBias: t += b; break;
+      case kOpRelu: t = t > 0.0f ? t : 0.0f; break;
+      case kOpGelu: t = gelu_erf(t); break;
+      case kOpScale: t *= op.a; break;
+      case kOpClamp: t = fminf(fmaxf(t, op.a), op.b); break;
+      default: break;
+    }
+  }
+  return t;
+}
+
 // t for one element; c and b are the C and bias values (0 when unused).
-__device__ __forceinline__ float epi_apply(float acc, float c, float b, const Epi& e) {
+__device__ __forceinline__ float epi_apply(float acc, float c, float b, const Epi& e,
+                                           const EpiProgram& prog) {
   float t = e.alpha * acc;
   t = fmaf(e.beta, c, t);
+  if (e.flags & kEpiProgram) return epi_program(t, b, e, prog);
   t += b;
-  if (e.flags & 2) t = gelu_erf(t);
+  if (e.flags & kEpiGelu) t = gelu_erf(t);
   return t;
+}
+
+// The kernels' view of a call's scalars and epilogue.
+inline Epi make_epi(const GemmArgs& a) { return Epi{a.alpha, a.beta, a.epi, a.n_ops}; }
+
+inline EpiProgram make_program(const GemmArgs& a) {
+  EpiProgram p;
+  for (int k = 0; k < kMaxEpiOps; ++k) p.ops[k] = k < a.n_ops ? a.ops[k] : EpiOp{0, 0.0f, 0.0f};
+  return p;
 }
 
 }  // namespace dg

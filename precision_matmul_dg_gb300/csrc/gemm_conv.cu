@@ -59,13 +59,17 @@ struct ConvParams {
   int num_m_blocks, num_n_blocks, num_tiles, num_k_blocks;
   int group_m;
   Epi epi;
-  void* CD;
+  const void* C;  // read when beta != 0 (FP16, or INT32 when Out == kOutI32)
+  int64_t ldc;
+  void* D;
+  int64_t ldd;
   const __half* bias;
   int32_t alpha_i, beta_i;
   int* status;
   uint64_t timeout_ns;
   uint32_t stage_tx;  // bytes TMA delivers per input slot
 };
+static_assert(sizeof(ConvParams) <= 128, "parameter struct within 128 bytes (see Epi)");
 
 template <int BN, int SIn, int SCv, int OpA, int OpB>
 struct ConvSmem {
@@ -178,7 +182,8 @@ struct RingPos {
 template <int BN, int SIn, int SCv, int OpA, int OpB, int Out>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_conv_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                        const __grid_constant__ CUtensorMap tmap_b, const ConvParams p) {
+                        const __grid_constant__ CUtensorMap tmap_b, const ConvParams p,
+                        const __grid_constant__ EpiProgram prog) {
   using L = ConvSmem<BN, SIn, SCv, OpA, OpB>;
   constexpr bool kConvA = OpA != kOpF16;
   static_assert(OpB != kOpF16, "B is always the widened operand here");
@@ -385,11 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int col0 = n_blk * BN + c * 32;
           if (Out == kOutF16) {
             if (col0 < p.N)
-              tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, static_cast<__half*>(p.CD),
-                                     p.bias);
+              tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, prog,
+                                     static_cast<const __half*>(p.C), p.ldc,
+                                     static_cast<__half*>(p.D), p.ldd, p.bias);
           } else {
             tc::flush_i32_piece(r, sums + c * 32, ch == 0, ch + 1 == num_chunks, row, col0, p.M,
-                                p.N, p.alpha_i, p.beta_i, p.CD);
+                                p.N, p.alpha_i, p.beta_i,
+                                tc::I32Out{static_cast<const int32_t*>(p.C), p.ldc,
+                                           static_cast<int32_t*>(p.D), p.ldd});
           }
         }
         tc_fence_before_sync();
@@ -441,8 +449,11 @@ cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
   p.num_tiles = p.num_m_blocks * p.num_n_blocks;
   p.num_k_blocks = static_cast<int>((a.K + kBlockK - 1) / kBlockK);
   p.group_m = 16;
-  p.epi = Epi{a.alpha, a.beta, a.epi};
-  p.CD = a.C;
+  p.epi = make_epi(a);
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.D = a.D;
+  p.ldd = a.ldd;
   p.bias = static_cast<const __half*>(a.bias);
   p.alpha_i = static_cast<int32_t>(a.alpha);
   p.beta_i = static_cast<int32_t>(a.beta);
@@ -461,7 +472,8 @@ cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
   }
   int grid = plan.grid > 0 ? plan.grid : a.sm_count;
   if (grid > p.num_tiles) grid = p.num_tiles;
-  e = launch_dependent(kern, dim3(grid), dim3(kThreads), L::kLaunchBytes, a.stream, ta, tb, p);
+  e = launch_dependent(kern, dim3(grid), dim3(kThreads), L::kLaunchBytes, a.stream, ta, tb, p,
+                       make_program(a));
   count_launches(1);
   return e;
 }

@@ -62,7 +62,10 @@ struct TcParams {
   int num_m_blocks, num_n_blocks, num_tiles, num_k_blocks;
   int group_m;
   Epi epi;
-  void* CD;  // C in / D out, leading dimension N (FP16, or INT32 when Out == kOutI32)
+  const void* C;  // read when beta != 0 (FP16, or INT32 when Out == kOutI32)
+  int64_t ldc;
+  void* D;
+  int64_t ldd;
   const __half* bias;
   int32_t alpha_i, beta_i;  // integer scalars of the INT32 output
   int* status;
@@ -70,6 +73,7 @@ struct TcParams {
   uint32_t stage_tx;  // bytes TMA delivers per stage (both CTAs of a pair)
   int staged;         // FP16 out through shared-memory boxes and TMA (else direct stores)
 };
+static_assert(sizeof(TcParams) <= 128, "parameter struct within 128 bytes (see Epi)");
 
 // Output modes: FP16 with the fused epilogue, or exact INT32 for INT8 inputs
 // widened to FP16 (K accumulated in exact FP32 chunks, INT32 running sum).
@@ -143,7 +147,9 @@ template <int BN, int Stages, int CG, int Out>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b,
-                       const __grid_constant__ CUtensorMap tmap_cd, const TcParams p) {
+                       const __grid_constant__ CUtensorMap tmap_c,
+                       const __grid_constant__ CUtensorMap tmap_d, const TcParams p,
+                       const __grid_constant__ EpiProgram prog) {
   using L = TcSmem<BN, Stages, CG>;
   // two FP32 accumulators (the INT32 mode keeps its running sums in registers)
   constexpr int kColsNeeded = 2 * BN;
@@ -194,7 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    if (p.staged) tma_prefetch_desc(&tmap_cd);
+    if (p.staged) {
+      tma_prefetch_desc(&tmap_d);
+      if (Out == kOutF16 && p.epi.beta != 0.0f) tma_prefetch_desc(&tmap_c);
+    }
   }
   if (warp == 2) {
     if (CG == 2)
@@ -225,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_c = policy_evict_first();
         for (int wi = 0; wi < kEpiWarps; ++wi)
           for (int j = 0; j < 2; ++j)
-            epi_load_c<BN, CG>(&tmap_cd, p, unit0, units, rank, wi, j,
+            epi_load_c<BN, CG>(&tmap_c, p, unit0, units, rank, wi, j,
                                smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes, epi_bar + wi * 2,
                                pol_c);
       };
@@ -413,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         const int row = y + lane;
-        const int32_t* crow = static_cast<const int32_t*>(p.CD) + static_cast<int64_t>(row) * p.N;
+        const int32_t* crow = static_cast<const int32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
         for (int cl = 0; cl < kCpw; ++cl) {
 #pragma unroll
@@ -424,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = al * sum[cl][hh * 16 + i];
             if (be != 0u && row < p.M) {
-              if (x + 16 <= p.N && (p.N & 3) == 0) {
+              if (x + 16 <= p.N && (p.ldc & 3) == 0) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                   const uint4 c = *reinterpret_cast<const uint4*>(crow + x + q * 4);
@@ -450,12 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmap_cd, box, x, y);
+                tma_store_2d(&tmap_d, box, x, y);
                 bulk_commit_group();
               }
               ++nstores;
             } else if (row < p.M) {
-              int32_t* drow = static_cast<int32_t*>(p.CD) + static_cast<int64_t>(row) * p.N;
+              int32_t* drow = static_cast<int32_t*>(p.D) + static_cast<int64_t>(row) * p.ldd;
 #pragma unroll
               for (int i = 0; i < 16; ++i)
                 if (x + i < p.N) drow[x + i] = static_cast<int32_t>(o[i]);
@@ -489,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         c_pending |= 1u << (jj & 1);
         if (lane == 0) {
           bulk_wait_group_read<0>();  // the store that last used the box has read it
-          epi_load_c<BN, CG>(&tmap_cd, p, unit0, units, rank, wi, jj, boxes, cbar, pol_c);
+          epi_load_c<BN, CG>(&tmap_c, p, unit0, units, rank, wi, jj, boxes, cbar, pol_c);
         }
       };
       for (int jj = 0; jj < 2; ++jj) {  // issued by the producer
@@ -541,11 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            tc::epilogue_f16_box(r, box, lane, x, p.N, p.epi, p.bias, has_c);
+            tc::epilogue_f16_box(r, box, lane, x, p.N, p.epi, prog, p.bias, has_c);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmap_cd, box, x, y);
+              tma_store_2d(&tmap_d, box, x, y);
               bulk_commit_group();
             }
           }
@@ -592,8 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_wait_ld();
           const int col0 = n_blk * BN + c * 32;
           if (col0 < p.N)
-            tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, static_cast<__half*>(p.CD),
-                                   p.bias);
+            tc::epilogue_f16_chunk(r, row, col0, p.M, p.N, p.epi, prog,
+                                   static_cast<const __half*>(p.C), p.ldc,
+                                   static_cast<__half*>(p.D), p.ldd, p.bias);
         }
         tc_fence_before_sync();
         if (CG == 2)
@@ -634,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int Stages, int CG, int Out>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   using L = TcSmem<BN, Stages, CG>;
-  CUtensorMap ta, tb, tcd;
+  CUtensorMap ta, tb;
   // A problem with fewer than 128 rows loads only its rows (rounded up to a
   // swizzle atom of 8): TMA is slow on boxes that are mostly out of bounds,
   // and the stale shared-memory rows below only feed accumulator rows >= M,
@@ -645,16 +655,22 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, L::kRowsB);
   if (e != cudaSuccess) return e;
   // The staged epilogue moves D (and FP16 C) as boxes of 64-byte rows, which
-  // needs 16-byte aligned rows (N % 8 == 0 for FP16, N % 4 == 0 for INT32)
-  // and base; other shapes store straight from registers.
-  const bool staged = (a.N % (Out == kOutF16 ? 8 : 4)) == 0 &&
-                      (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
+  // needs 16-byte aligned rows (ld % 8 == 0 for FP16, ld % 4 == 0 for INT32)
+  // and bases; other layouts store straight from registers.  The INT32 mode
+  // reads C with plain loads.
+  const int64_t vec = Out == kOutF16 ? 8 : 4;
+  const bool c_tma = Out == kOutF16 && a.beta != 0.0f;
+  const bool staged = a.ldd % vec == 0 && (reinterpret_cast<uintptr_t>(a.D) & 15) == 0 &&
+                      (!c_tma || (a.ldc % vec == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0));
+  CUtensorMap tc_map = ta, td_map = ta;  // copies of a map that the kernel does not use
   if (staged) {
-    e = Out == kOutF16 ? tc::make_f16_epi_map(&tcd, a.C, a.M, a.N)
-                       : tc::make_i32_epi_map(&tcd, a.C, a.M, a.N);
+    e = Out == kOutF16 ? tc::make_f16_epi_map(&td_map, a.D, a.M, a.N, a.ldd)
+                       : tc::make_i32_epi_map(&td_map, a.D, a.M, a.N, a.ldd);
     if (e != cudaSuccess) return e;
-  } else {
-    tcd = ta;  // not read
+    if (c_tma) {
+      e = tc::make_f16_epi_map(&tc_map, a.C, a.M, a.N, a.ldc);
+      if (e != cudaSuccess) return e;
+    }
   }
 
   TcParams p;
@@ -666,8 +682,11 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.num_tiles = p.num_m_blocks * p.num_n_blocks;
   p.num_k_blocks = static_cast<int>((a.K + kBlockK - 1) / kBlockK);
   p.group_m = 16 / CG;
-  p.epi = Epi{a.alpha, a.beta, a.epi};
-  p.CD = a.C;
+  p.epi = make_epi(a);
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.D = a.D;
+  p.ldd = a.ldd;
   p.bias = static_cast<const __half*>(a.bias);
   p.alpha_i = static_cast<int32_t>(a.alpha);
   p.beta_i = static_cast<int32_t>(a.beta);
@@ -725,7 +744,7 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs += 1;
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tcd, p);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc_map, td_map, p, make_program(a));
   count_launches(1);
   return e;
 }

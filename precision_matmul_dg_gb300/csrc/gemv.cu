@@ -38,7 +38,10 @@ struct GemvParams {
   int64_t lda;
   const __half* B;
   int64_t ldb;
-  __half* CD;  // C in, D out (leading dimension N)
+  const __half* C;  // read when beta != 0
+  int64_t ldc;
+  __half* D;
+  int64_t ldd;
   const __half* bias;
   Epi epi;
   int split_k;
@@ -46,6 +49,7 @@ struct GemvParams {
   float* partial;       // [split_k][M][N] when split_k > 1
   unsigned* counters;   // [gridDim.x] when split_k > 1, zero between launches
 };
+static_assert(sizeof(GemvParams) <= 128, "parameter struct within 128 bytes (see Epi)");
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 v;
@@ -73,15 +77,16 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ void write_out(const GemvParams& p, int m, int j, float acc) {
-  const int64_t idx = static_cast<int64_t>(m) * p.N + j;
-  const float c = (p.epi.beta != 0.0f) ? __half2float(p.CD[idx]) : 0.0f;
+__device__ __forceinline__ void write_out(const GemvParams& p, const EpiProgram& prog, int m,
+                                          int j, float acc) {
+  const float c = (p.epi.beta != 0.0f) ? __half2float(p.C[static_cast<int64_t>(m) * p.ldc + j])
+                                        : 0.0f;
   const float b = (p.epi.flags & kEpiBias) ? __half2float(p.bias[j]) : 0.0f;
-  p.CD[idx] = __float2half_rn(epi_apply(acc, c, b, p.epi));
+  p.D[static_cast<int64_t>(m) * p.ldd + j] = __float2half_rn(epi_apply(acc, c, b, p.epi, prog));
 }
 
 template <int MROWS>
-__global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const GemvParams p, const __grid_constant__ EpiProgram prog) {
   grid_dependency_wait();  // launched as a dependent of the previous kernel
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -164,7 +169,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
     if (lane == 0 && j < p.N) {
 #pragma unroll
       for (int m = 0; m < MROWS; ++m)
-        if (m < p.M) write_out(p, m, j, acc[m]);
+        if (m < p.M) write_out(p, prog, m, j, acc[m]);
     }
     return;
   }
@@ -195,32 +200,37 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
     float s = 0.0f;
     for (int sp = 0; sp < p.split_k; ++sp)
       s += __ldcg(&p.partial[(static_cast<int64_t>(sp) * p.M + m) * p.N + jj]);
-    write_out(p, m, jj, s);
+    write_out(p, prog, m, jj, s);
   }
   if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;  // ready for the next launch
 }
 
-// K == 0: D = epilogue(beta * C), no product term.
-__global__ void epilogue_only_kernel(int64_t M, int64_t N, __half* CD, const __half* bias,
-                                     Epi epi) {
+// K == 0: D = epilogue(beta * C), no product term.  Element i of the M x N
+// result is row i / N, column i % N.
+__global__ void epilogue_only_kernel(int64_t M, int64_t N, const __half* C, int64_t ldc,
+                                     __half* D, int64_t ldd, const __half* bias,
+                                     const Epi epi, const __grid_constant__ EpiProgram prog) {
   grid_dependency_wait();  // launched as a dependent of the previous kernel
   const int64_t total = M * N;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t j = i % N;
-    const float c = (epi.beta != 0.0f) ? __half2float(CD[i]) : 0.0f;
+    const int64_t m = i / N, j = i - m * N;
+    const float c = (epi.beta != 0.0f) ? __half2float(C[m * ldc + j]) : 0.0f;
     const float b = (epi.flags & kEpiBias) ? __half2float(bias[j]) : 0.0f;
-    CD[i] = __float2half_rn(epi_apply(0.0f, c, b, epi));
+    D[m * ldd + j] = __float2half_rn(epi_apply(0.0f, c, b, epi, prog));
   }
 }
 
 // K == 0 on the integer path: D = beta * C (mod 2^32).
-__global__ void epilogue_only_i32_kernel(int64_t total, int32_t* CD, int32_t beta) {
+__global__ void epilogue_only_i32_kernel(int64_t M, int64_t N, const int32_t* C, int64_t ldc,
+                                         int32_t* D, int64_t ldd, int32_t beta) {
   grid_dependency_wait();  // launched as a dependent of the previous kernel
+  const int64_t total = M * N;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint32_t c = (beta != 0) ? static_cast<uint32_t>(CD[i]) : 0u;
-    CD[i] = static_cast<int32_t>(static_cast<uint32_t>(beta) * c);
+    const int64_t m = i / N, j = i - m * N;
+    const uint32_t c = (beta != 0) ? static_cast<uint32_t>(C[m * ldc + j]) : 0u;
+    D[m * ldd + j] = static_cast<int32_t>(static_cast<uint32_t>(beta) * c);
   }
 }
 
@@ -258,9 +268,12 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
   p.lda = a.lda;
   p.B = static_cast<const __half*>(a.B);
   p.ldb = a.ldb;
-  p.CD = static_cast<__half*>(a.C);
+  p.C = static_cast<const __half*>(a.C);
+  p.ldc = a.ldc;
+  p.D = static_cast<__half*>(a.D);
+  p.ldd = a.ldd;
   p.bias = static_cast<const __half*>(a.bias);
-  p.epi = Epi{a.alpha, a.beta, a.epi};
+  p.epi = make_epi(a);
   p.split_k = plan.split_k;
   p.k_chunk = plan.k_tile;
   p.partial = ws.partial;
@@ -272,7 +285,7 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
               : a.M <= 2 ? gemv_splitk_kernel<2>
               : a.M <= 4 ? gemv_splitk_kernel<4>
                          : gemv_splitk_kernel<kGemvMaxM>;
-  const cudaError_t e = launch_dependent(kern, grid, block, 0, a.stream, p);
+  const cudaError_t e = launch_dependent(kern, grid, block, 0, a.stream, p, make_program(a));
   count_launches(1);
   return e;
 }
@@ -287,12 +300,13 @@ cudaError_t launch_epilogue_only(const GemmArgs& a) {
   cudaError_t e;
   if (a.dtype_a == DG_I8) {
     e = launch_dependent(epilogue_only_i32_kernel, dim3(static_cast<unsigned>(blocks)),
-                         dim3(threads), 0, a.stream, total, static_cast<int32_t*>(a.C),
-                         static_cast<int32_t>(a.beta));
+                         dim3(threads), 0, a.stream, a.M, a.N, static_cast<const int32_t*>(a.C),
+                         a.ldc, static_cast<int32_t*>(a.D), a.ldd, static_cast<int32_t>(a.beta));
   } else {
     e = launch_dependent(epilogue_only_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads),
-                         0, a.stream, a.M, a.N, static_cast<__half*>(a.C),
-                         static_cast<const __half*>(a.bias), Epi{a.alpha, a.beta, a.epi});
+                         0, a.stream, a.M, a.N, static_cast<const __half*>(a.C), a.ldc,
+                         static_cast<__half*>(a.D), a.ldd, static_cast<const __half*>(a.bias),
+                         make_epi(a), make_program(a));
   }
   count_launches(1);
   return e;
@@ -419,11 +433,15 @@ extern "C" dg_status dg_gemm_thin_noalloc(int64_t M, int64_t N, int64_t K, dg_dt
   a.B = B;
   a.ldb = ldb;
   a.C = C;
+  a.ldc = N;
+  a.D = C;
+  a.ldd = N;
   a.bias = bias;
   a.alpha = alpha;
   a.beta = beta;
   a.epi = ((epilogue == DG_EPI_BIAS || epilogue == DG_EPI_BIAS_GELU) ? kEpiBias : 0) |
           ((epilogue == DG_EPI_GELU || epilogue == DG_EPI_BIAS_GELU) ? kEpiGelu : 0);
+  a.n_ops = 0;
   a.stream = st;
   a.status = nullptr;
   a.timeout_ns = 0;

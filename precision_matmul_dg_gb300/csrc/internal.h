@@ -13,9 +13,19 @@
 namespace dg {
 
 // Epilogue flags as the kernels see them.
-enum : int { kEpiBias = 1, kEpiGelu = 2 };
+enum : int { kEpiBias = 1, kEpiGelu = 2, kEpiProgram = 4 };
 
-// Everything a launcher needs to run one GEMM, already validated.
+// Epilogue-program ops (dg_epilogue_op of dg.h).
+using EpiOp = dg_epilogue_op;
+constexpr int kMaxEpiOps = DG_MAX_EPILOGUE_OPS;
+enum : int {
+  kOpBias = DG_OP_BIAS,
+  kOpRelu = DG_OP_RELU,
+  kOpGelu = DG_OP_GELU,
+  kOpScale = DG_OP_SCALE,
+  kOpClamp = DG_OP_CLAMP
+};
+
 // Launches `kern` with programmatic stream serialization: its CTAs may be
 // scheduled (and run their set-up) while the previous kernel in the stream
 // drains.  Every kernel launched this way executes griddepcontrol.wait
@@ -37,6 +47,7 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Everything a launcher needs to run one GEMM, already validated.
 struct GemmArgs {
   int64_t M, N, K;
   dg_dtype dtype_a, dtype_b;
@@ -44,10 +55,15 @@ struct GemmArgs {
   int64_t lda;
   const void* B;
   int64_t ldb;
-  void* C;  // in: C (when beta != 0); out: D
+  const void* C;  // read when beta != 0; else equal to D
+  int64_t ldc;    // row pitches in elements (N for dg_gemm, where C == D)
+  void* D;        // C and D are one buffer (ldc == ldd) or do not overlap
+  int64_t ldd;
   const void* bias;
   float alpha, beta;
-  int epi;  // kEpiBias | kEpiGelu
+  int epi;    // kEpiBias | kEpiGelu, or kEpiProgram (+ kEpiBias)
+  int n_ops;  // kEpiProgram: the ops, in order
+  EpiOp ops[kMaxEpiOps];
   cudaStream_t stream;
   int* status;          // per-device status word (device memory)
   uint64_t timeout_ns;  // device-side wait limit

@@ -59,10 +59,14 @@ struct SkParams {
   int64_t lda;
   const uint8_t* B;
   int64_t ldb_bytes;  // packed row pitch
-  __half* CD;         // C in / D out, leading dimension N
+  const __half* C;    // read when beta != 0
+  int64_t ldc;
+  __half* D;
+  int64_t ldd;
   const __half* bias;
   Epi epi;
 };
+static_assert(sizeof(SkParams) <= 128, "parameter struct within 128 bytes (see Epi)");
 
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t o;
@@ -90,7 +94,8 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__global__ void __launch_bounds__(kSkThreads) skinny_w4a16_kernel(const SkParams p) {
+__global__ void __launch_bounds__(kSkThreads)
+    skinny_w4a16_kernel(const SkParams p, const __grid_constant__ EpiProgram prog) {
   extern __shared__ __align__(16) uint8_t sk_smem[];
   __half* As = reinterpret_cast<__half*>(sk_smem);             // [16][kSkStride]
   float* red = reinterpret_cast<float*>(sk_smem + kSkSmemA);   // [8 groups][32 lanes][4]
@@ -190,10 +195,11 @@ __global__ void __launch_bounds__(kSkThreads) skinny_w4a16_kernel(const SkParams
     for (int e = 0; e < 2; ++e) {
       const int nn = n0 + 2 * tig + e;
       if (nn >= p.N) continue;
-      const int64_t idx = static_cast<int64_t>(m) * p.N + nn;
-      const float c = p.epi.beta != 0.0f ? __half2float(p.CD[idx]) : 0.0f;
+      const float c =
+          p.epi.beta != 0.0f ? __half2float(p.C[static_cast<int64_t>(m) * p.ldc + nn]) : 0.0f;
       const float b = (p.epi.flags & kEpiBias) ? __half2float(p.bias[nn]) : 0.0f;
-      p.CD[idx] = __float2half_rn(epi_apply(acc[2 * h + e], c, b, p.epi));
+      p.D[static_cast<int64_t>(m) * p.ldd + nn] =
+          __float2half_rn(epi_apply(acc[2 * h + e], c, b, p.epi, prog));
     }
   }
 }
@@ -216,9 +222,12 @@ cudaError_t launch_skinny(const GemmArgs& a, const dg_tile_plan& plan) {
   p.lda = a.lda;
   p.B = static_cast<const uint8_t*>(a.B);
   p.ldb_bytes = a.ldb / 2;
-  p.CD = static_cast<__half*>(a.C);
+  p.C = static_cast<const __half*>(a.C);
+  p.ldc = a.ldc;
+  p.D = static_cast<__half*>(a.D);
+  p.ldd = a.ldd;
   p.bias = static_cast<const __half*>(a.bias);
-  p.epi = Epi{a.alpha, a.beta, a.epi};
+  p.epi = make_epi(a);
   int dev = 0;
   cudaGetDevice(&dev);
   static uint64_t attr_set = 0;  // one shared-memory opt-in per device
@@ -231,7 +240,7 @@ cudaError_t launch_skinny(const GemmArgs& a, const dg_tile_plan& plan) {
   }
   const unsigned grid = static_cast<unsigned>((a.N + kSkCols - 1) / kSkCols);
   const cudaError_t e = launch_dependent(skinny_w4a16_kernel, dim3(grid), dim3(kSkThreads),
-                                         kSkSmem, a.stream, p);
+                                         kSkSmem, a.stream, p, make_program(a));
   count_launches(1);
   return e;
 }

@@ -54,23 +54,84 @@ __device__ __forceinline__ void add_bias_chunk(float (&v)[32], const __half* bia
   }
 }
 
+// An epilogue program's ops, in order, on 32 consecutive columns of one row
+// (op-outer, so each op's kind is decided once per chunk, uniformly across
+// the warp).  Columns >= N take a zero bias; their values are never stored.
+__device__ __forceinline__ void apply_program_chunk(float (&v)[32], const __half* bias, int col0,
+                                                    int N, const Epi& epi,
+                                                    const EpiProgram& prog) {
+#pragma unroll 1
+  for (int k = 0; k < epi.n_ops; ++k) {
+    const EpiOp op = prog.ops[k];
+    switch (op.type) {
+      case kOpBias:
+        add_bias_chunk(v, bias, col0, N);
+        break;
+      case kOpRelu:
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = v[i] > 0.0f ? v[i] : 0.0f;
+        break;
+      case kOpGelu:
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+        break;
+      case kOpScale:
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= op.a;
+        break;
+      case kOpClamp:
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = fminf(fmaxf(v[i], op.a), op.b);
+        break;
+      default:
+        break;
+    }
+  }
+}
+
+// Rounds 32 values to FP16 and stores the columns < N of them at drow + col0
+// (16-byte stores when `full`: all 32 in range and 16-byte aligned).
+__device__ __forceinline__ void store_f16_32(const float (&v)[32], __half* drow, int col0, int N,
+                                             bool full) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (full) {
+      uint4 ov;
+      __half2* oh = reinterpret_cast<__half2*>(&ov);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) oh[h] = __floats2half2_rn(v[q * 8 + 2 * h], v[q * 8 + 2 * h + 1]);
+      *reinterpret_cast<uint4*>(drow + col0 + q * 8) = ov;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (col0 + q * 8 + i < N) drow[col0 + q * 8 + i] = __float2half_rn(v[q * 8 + i]);
+    }
+  }
+}
+
 // Fused FP16 epilogue for one thread's row and 32 consecutive columns:
-// D = round_fp16(GELU?(alpha*acc + beta*C + bias)).  C and D share `cd`
-// (leading dimension N).  Rows >= M and columns >= N are skipped.
+// D = round_fp16(epilogue(alpha*acc + beta*C)), the epilogue being bias then
+// GELU (flags) or a program.  C (read only when beta != 0) has leading
+// dimension ldc, D has ldd; they are one buffer or do not overlap.  Rows >= M
+// and columns >= N are skipped.
 __device__ __forceinline__ void epilogue_f16_chunk(const uint32_t (&r)[32], int row, int col0,
-                                                   int M, int N, const Epi& epi, __half* cd,
+                                                   int M, int N, const Epi& epi,
+                                                   const EpiProgram& prog, const __half* c,
+                                                   int64_t ldc, __half* d, int64_t ldd,
                                                    const __half* bias) {
   if (row >= M) return;
   float v[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = epi.alpha * __uint_as_float(r[i]);
-  __half* drow = cd + static_cast<int64_t>(row) * N;
-  const bool full = (col0 + 32 <= N) && ((N & 7) == 0);
+  __half* drow = d + static_cast<int64_t>(row) * ldd;
+  const bool in_range = col0 + 32 <= N;
+  const bool full = in_range && ((ldd & 7) == 0);
   if (epi.beta != 0.0f) {
-    if (full) {
+    const __half* crow = c + static_cast<int64_t>(row) * ldc;
+    if (in_range && (ldc & 7) == 0) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 cv = *reinterpret_cast<const uint4*>(drow + col0 + q * 8);
+        const uint4 cv = *reinterpret_cast<const uint4*>(crow + col0 + q * 8);
         const __half2* ch = reinterpret_cast<const __half2*>(&cv);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -82,8 +143,13 @@ __device__ __forceinline__ void epilogue_f16_chunk(const uint32_t (&r)[32], int 
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (col0 + i < N) v[i] = fmaf(epi.beta, __half2float(drow[col0 + i]), v[i]);
+        if (col0 + i < N) v[i] = fmaf(epi.beta, __half2float(crow[col0 + i]), v[i]);
     }
+  }
+  if (epi.flags & kEpiProgram) {
+    apply_program_chunk(v, bias, col0, N, epi, prog);
+    store_f16_32(v, drow, col0, N, full);
+    return;
   }
   if (epi.flags & kEpiBias) add_bias_chunk(v, bias, col0, N);
   const bool gelu = (epi.flags & kEpiGelu) != 0;
@@ -123,13 +189,14 @@ __device__ __forceinline__ uint32_t epi_box_offset(int r, int q) {
   return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
 }
 
-// D = round_fp16(GELU?(alpha*acc + beta*C + bias)) for row `r` of a staged
+// D = round_fp16(epilogue(alpha*acc + beta*C)) for row `r` of a staged
 // box whose first column is D column col0; with `has_c` the box holds C on
 // entry.  D replaces C in the box.  Columns >= N (bias only) read 0; the
 // store's tensor map drops them.
 __device__ __forceinline__ void epilogue_f16_box(const uint32_t (&acc)[32], uint8_t* box, int r,
                                                  int col0, int N, const Epi& epi,
-                                                 const __half* bias, bool has_c) {
+                                                 const EpiProgram& prog, const __half* bias,
+                                                 bool has_c) {
   float v[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = epi.alpha * __uint_as_float(acc[i]);
@@ -146,8 +213,12 @@ __device__ __forceinline__ void epilogue_f16_box(const uint32_t (&acc)[32], uint
       }
     }
   }
-  if (epi.flags & kEpiBias) add_bias_chunk(v, bias, col0, N);
-  const bool gelu = (epi.flags & kEpiGelu) != 0;
+  const bool program = (epi.flags & kEpiProgram) != 0;
+  if (program)
+    apply_program_chunk(v, bias, col0, N, epi, prog);
+  else if (epi.flags & kEpiBias)
+    add_bias_chunk(v, bias, col0, N);
+  const bool gelu = !program && (epi.flags & kEpiGelu) != 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {  // 8 values at a time: activation, rounding, staging
     if (gelu) {
@@ -186,18 +257,29 @@ __device__ __forceinline__ void tc_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// C and D of an INT32 output: C read when beta != 0, leading dimensions in
+// elements; the two are one buffer or do not overlap.
+struct I32Out {
+  const int32_t* c;
+  int64_t ldc;
+  int32_t* d;
+  int64_t ldd;
+};
+
 // INT32 output of one 32-column chunk: D = alpha*sum + beta*C (mod 2^32).
 __device__ __forceinline__ void store_i32_chunk(const uint32_t (&s)[32], int row, int col0, int M,
-                                                int N, int32_t alpha, int32_t beta, void* cd) {
+                                                int N, int32_t alpha, int32_t beta,
+                                                const I32Out& o) {
   if (row >= M) return;
-  int32_t* drow = static_cast<int32_t*>(cd) + static_cast<int64_t>(row) * N;
+  const int32_t* crow = o.c + static_cast<int64_t>(row) * o.ldc;
+  int32_t* drow = o.d + static_cast<int64_t>(row) * o.ldd;
   const uint32_t al = static_cast<uint32_t>(alpha), be = static_cast<uint32_t>(beta);
-  const bool full = (col0 + 32 <= N) && ((N & 3) == 0);
+  const bool full = (col0 + 32 <= N) && (((o.ldc | o.ldd) & 3) == 0);
   if (full) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       uint4 v;
-      if (be != 0u) v = *reinterpret_cast<const uint4*>(drow + col0 + q * 4);
+      if (be != 0u) v = *reinterpret_cast<const uint4*>(crow + col0 + q * 4);
       else v = make_uint4(0, 0, 0, 0);
       v.x = al * s[q * 4 + 0] + be * v.x;
       v.y = al * s[q * 4 + 1] + be * v.y;
@@ -209,7 +291,7 @@ __device__ __forceinline__ void store_i32_chunk(const uint32_t (&s)[32], int row
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       if (col0 + i < N) {
-        const uint32_t c = be != 0u ? static_cast<uint32_t>(drow[col0 + i]) : 0u;
+        const uint32_t c = be != 0u ? static_cast<uint32_t>(crow[col0 + i]) : 0u;
         drow[col0 + i] = static_cast<int32_t>(al * s[i] + be * c);
       }
     }
@@ -222,7 +304,7 @@ __device__ __forceinline__ void store_i32_chunk(const uint32_t (&s)[32], int row
 // last chunk) or write the result to D (last chunk).
 __device__ __forceinline__ void flush_i32_piece(uint32_t (&r)[32], uint32_t sums, bool first,
                                                 bool last, int row, int col0, int M, int N,
-                                                int32_t alpha, int32_t beta, void* cd) {
+                                                int32_t alpha, int32_t beta, const I32Out& o) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
   if (!first) {
@@ -236,7 +318,7 @@ __device__ __forceinline__ void flush_i32_piece(uint32_t (&r)[32], uint32_t sums
     tmem_st_32cols(sums, r);
     tc_wait_st();
   } else if (col0 < N) {
-    store_i32_chunk(r, row, col0, M, N, alpha, beta, cd);
+    store_i32_chunk(r, row, col0, M, N, alpha, beta, o);
   }
 }
 
@@ -312,18 +394,21 @@ inline cudaError_t make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, cons
   return cudaSuccess;
 }
 
-// C / D of the staged epilogue: M x N FP16, row pitch N, boxes of 32 x 32 in
-// the 64-byte swizzle.  Needs N % 8 == 0 and a 16-byte aligned base.
-inline cudaError_t make_f16_epi_map(CUtensorMap* map, const void* base, int64_t M, int64_t N) {
-  return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, M, N, N * 2, kEpiBoxRows,
+// C or D of the staged epilogue: M x N FP16, row pitch ld elements, boxes
+// of 32 x 32 in the 64-byte swizzle.  Needs ld % 8 == 0 and a 16-byte
+// aligned base.
+inline cudaError_t make_f16_epi_map(CUtensorMap* map, const void* base, int64_t M, int64_t N,
+                                    int64_t ld) {
+  return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, M, N, ld * 2, kEpiBoxRows,
                      kEpiBoxCols, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// D of the INT32 output: M x N INT32, row pitch N, boxes of 32 rows x 16
-// columns (64-byte rows, the same 64-byte swizzle).  Needs N % 4 == 0 and a
-// 16-byte aligned base.
-inline cudaError_t make_i32_epi_map(CUtensorMap* map, const void* base, int64_t M, int64_t N) {
-  return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_INT32, base, M, N, N * 4, kEpiBoxRows,
+// D of the INT32 output: M x N INT32, row pitch ld elements, boxes of 32
+// rows x 16 columns (64-byte rows, the same 64-byte swizzle).  Needs
+// ld % 4 == 0 and a 16-byte aligned base.
+inline cudaError_t make_i32_epi_map(CUtensorMap* map, const void* base, int64_t M, int64_t N,
+                                    int64_t ld) {
+  return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_INT32, base, M, N, ld * 4, kEpiBoxRows,
                      kEpiBoxCols / 2, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 

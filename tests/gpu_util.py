@@ -38,10 +38,46 @@ def run_case(dg, case, plan=None, stream=None, canary=0):
     return out, tail
 
 
+def run_case_ex(dg, case, ldc=None, ldd=None, inplace=False, stream=None):
+    """Runs `case` through dg_gemm_ex with C and D in separate buffers of
+    leading dimensions ldc and ldd (default N), or with D = C in place.  The
+    columns between N and each leading dimension hold a canary; asserts that
+    D's stay untouched and that C (with its padding) is unchanged."""
+    dev = "cuda:0"
+    M, N = case.M, case.N
+    A = torch.from_numpy(np.ascontiguousarray(case.A)).to(dev)
+    B = torch.from_numpy(np.ascontiguousarray(case.B)).to(dev)
+    out_dtype = torch.int32 if case.dtype_a == "i8" else torch.float16
+    fill = 12345 if out_dtype == torch.int32 else -7.5
+    ldd = ldd or N
+    Dbuf = torch.full((M, ldd), fill, dtype=out_dtype, device=dev)
+    D = Dbuf[:, :N]
+    Cbuf = C = None
+    if case.C is not None:
+        if inplace:
+            D.copy_(torch.from_numpy(case.C).to(dev))
+            C = D
+        else:
+            Cbuf = torch.full((M, ldc or N), fill, dtype=out_dtype, device=dev)
+            Cbuf[:, :N] = torch.from_numpy(case.C).to(dev)
+            C = Cbuf[:, :N]
+    c_before = Cbuf.cpu().numpy() if Cbuf is not None else None
+    bias = torch.from_numpy(case.bias).to(dev) if case.bias is not None else None
+    dg.gemm_ex(A, B, D, C=C, K=case.K, bias=bias, alpha=case.alpha, beta=case.beta,
+               program=case.program or [], dtype_b=case.dtype_b, stream=stream)
+    dg.check_status(stream)
+    host = Dbuf.cpu().numpy()
+    assert np.all(host[:, N:] == np.array(fill, dtype=host.dtype)), "D padding was written"
+    if Cbuf is not None:
+        assert np.array_equal(Cbuf.cpu().numpy().view(np.uint8), c_before.view(np.uint8)), \
+            "C was modified"
+    return host[:, :N]
+
+
 def reference(case, rows=None):
     return oracle.gemm_reference(case.A, case.B, case.K, case.dtype_a, case.dtype_b, C=case.C,
                                  bias=case.bias, alpha=case.alpha, beta=case.beta,
-                                 epilogue=case.epilogue, rows=rows)
+                                 epilogue=case.epilogue, rows=rows, program=case.program)
 
 
 def assert_parity(case, got, rows=None):
@@ -56,7 +92,7 @@ def assert_parity(case, got, rows=None):
         return
     bound = oracle.error_bound(case.A, case.B, case.K, ref, case.dtype_a, case.dtype_b, C=case.C,
                                bias=case.bias, alpha=case.alpha, beta=case.beta,
-                               epilogue=case.epilogue, rows=rows)
+                               epilogue=case.epilogue, rows=rows, program=case.program)
     g = got.astype(np.float64)
     err = np.abs(g - ref)
     ok = err <= bound

@@ -54,8 +54,13 @@ def test_struct_layout_matches_c(dg, tmp_path):
         int main(void) {
           printf("dg_hw_desc %zu\\n", sizeof(dg_hw_desc));
           printf("dg_tile_plan %zu\\n", sizeof(dg_tile_plan));
+          printf("dg_epilogue_op %zu\\n", sizeof(dg_epilogue_op));
+          printf("dg_epilogue_program %zu\\n", sizeof(dg_epilogue_program));
+          printf("ops %d,%d,%d,%d,%d,%d\\n", DG_MAX_EPILOGUE_OPS, DG_OP_BIAS, DG_OP_RELU,
+                 DG_OP_GELU, DG_OP_SCALE, DG_OP_CLAMP);
           F(dg_hw_desc, l2_bytes) F(dg_hw_desc, hbm_gbps) F(dg_hw_desc, clock_ghz)
           F(dg_tile_plan, grid) F(dg_tile_plan, occupancy) F(dg_tile_plan, est_tflops)
+          F(dg_epilogue_op, a) F(dg_epilogue_op, b) F(dg_epilogue_program, ops)
           return 0;
         }
     """))
@@ -66,11 +71,17 @@ def test_struct_layout_matches_c(dg, tmp_path):
         [str(exe)], capture_output=True, text=True, check=True).stdout.split("\n") if line)
     assert int(out["dg_hw_desc"]) == ctypes.sizeof(dg.HwDesc)
     assert int(out["dg_tile_plan"]) == ctypes.sizeof(dg.TilePlan)
+    assert int(out["dg_epilogue_op"]) == ctypes.sizeof(dg.EpilogueOp)
+    assert int(out["dg_epilogue_program"]) == ctypes.sizeof(dg.EpilogueProgram)
+    ops = [int(x) for x in out.pop("ops").split(",")]
+    assert ops == [dg.MAX_EPILOGUE_OPS] + [dg.OPS[k] for k in ("bias", "relu", "gelu", "scale",
+                                                               "clamp")]
+    classes = {"dg_hw_desc": dg.HwDesc, "dg_tile_plan": dg.TilePlan,
+               "dg_epilogue_op": dg.EpilogueOp, "dg_epilogue_program": dg.EpilogueProgram}
     for key, val in out.items():
         if "." in key:
             struct, field = key.split(".")
-            cls = dg.HwDesc if struct == "dg_hw_desc" else dg.TilePlan
-            assert getattr(cls, field).offset == int(val), key
+            assert getattr(classes[struct], field).offset == int(val), key
 
 
 # ---------------------------------------------------------------- validation
@@ -118,6 +129,74 @@ def test_invalid_arguments_rejected(dg, over, status):
     got, msg = _call(dg, **over)
     assert got == status, msg
     assert msg  # a message is set
+
+
+GOOD_EX = dict(M=64, N=64, K=64, dtype_a="f16", dtype_b="f16", A=0x10000, lda=64, B=0x20000,
+               ldb=64, C=0x30000, ldc=64, D=0x50000, ldd=72, bias=None, alpha=1.0, beta=1.0,
+               program=[])
+
+
+def _call_ex(dg, **over):
+    kw = dict(GOOD_EX)
+    kw.update(over)
+    prog = kw["program"]
+    try:
+        dg.gemm_ex_raw(kw["M"], kw["N"], kw["K"], kw["dtype_a"], kw["dtype_b"], kw["A"],
+                       kw["lda"], kw["B"], kw["ldb"], kw["C"], kw["ldc"], kw["D"], kw["ldd"],
+                       kw["bias"], kw["alpha"], kw["beta"], program=prog, stream=0)
+    except dg.DgError as e:
+        return e.name, str(e)
+    return "DG_OK", ""
+
+
+def _nine_ops(dg):
+    p = dg.make_program(["relu"] * 8)
+    p.n_ops = 9
+    return p
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(D=None), "DG_ERR_INVALID_ARG"),
+    (dict(D=0x50004), "DG_ERR_INVALID_ARG"),
+    (dict(C=None), "DG_ERR_INVALID_ARG"),                  # beta != 0 needs C
+    (dict(C=0x30008), "DG_ERR_INVALID_ARG"),
+    (dict(ldc=63), "DG_ERR_INVALID_ARG"),                  # ldc < N
+    (dict(ldd=32), "DG_ERR_INVALID_ARG"),                  # ldd < N
+    (dict(C=0x50000, ldc=64), "DG_ERR_INVALID_ARG"),       # C == D with ldc != ldd
+    (dict(program=["bias"]), "DG_ERR_INVALID_ARG"),        # bias op, null bias
+    (dict(program=[("clamp", 1.0, -1.0)]), "DG_ERR_INVALID_ARG"),
+    (dict(program=[("clamp", float("nan"), 1.0)]), "DG_ERR_INVALID_ARG"),
+    (dict(program=[("scale", float("inf"))]), "DG_ERR_INVALID_ARG"),
+    (dict(program=[(9, 0.0, 0.0)]), "DG_ERR_INVALID_ARG"),  # unknown op type
+    (dict(program=[(0, 0.0, 0.0)]), "DG_ERR_INVALID_ARG"),
+    (dict(program="nine"), "DG_ERR_INVALID_ARG"),          # n_ops above the maximum
+    (dict(dtype_a="i8", dtype_b="i8", program=["relu"]), "DG_ERR_UNSUPPORTED"),
+])
+def test_gemm_ex_invalid_arguments_rejected(dg, over, status):
+    if over.get("program") == "nine":
+        over = dict(over, program=_nine_ops(dg))
+    got, msg = _call_ex(dg, **over)
+    assert got == status, msg
+    assert msg
+
+
+def test_gemm_ex_unused_c_may_be_null(dg):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # beta == 0: C is not read, so a null C (and any ldc) passes validation and
+    # the call reaches the device check
+    got, msg = _call_ex(dg, C=None, ldc=0, beta=0.0, program=["relu", ("scale", 2.0)])
+    assert got == "DG_ERR_INVALID_STATE", msg
+
+
+def test_make_program_limits(dg):
+    with pytest.raises(ValueError):
+        dg.make_program(["relu"] * 9)
+    p = dg.make_program(["bias", ("scale", 0.5), ("clamp", -1, 1), "gelu"])
+    assert p.n_ops == 4
+    assert [p.ops[k].type for k in range(4)] == [1, 4, 5, 3]
+    assert (p.ops[1].a, p.ops[2].a, p.ops[2].b) == (0.5, -1.0, 1.0)
 
 
 def test_empty_problem_is_a_noop(dg):

@@ -39,6 +39,7 @@ class Case:
     lda: int = 0
     ldb: int = 0
     meta: dict = field(default_factory=dict)
+    program: Optional[list] = None  # epilogue ops in order (replaces `epilogue`)
 
     def flops(self):
         return 2.0 * self.M * self.N * self.K
@@ -81,13 +82,14 @@ def _pad_cols(x, ld, fill=0):
 
 
 def random_case(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", alpha=1.0,
-                beta=0.0, seed=0, dist="normal", lda=None, ldb=None, name=None, pad=0):
+                beta=0.0, seed=0, dist="normal", lda=None, ldb=None, name=None, pad=0,
+                program=None):
     """A general random case for parity tests.
 
     dist: "normal" -> N(0,1)/sqrt(K) operands (the square-GEMM recipe),
           "uniform" -> U[-1,1) operands.
     C ~ N(0,1) fp16 whenever beta != 0; bias ~ N(0, 0.1) fp16 when the
-    epilogue has a bias.  lda/ldb default to the smallest legal padded
+    epilogue (or the program) has a bias.  lda/ldb default to the smallest legal padded
     leading dimension (K rounded up to 8 fp16 / 16 int8 elements, 32 codes
     for packed 4-bit), so every leading dimension is a 16-byte multiple.
     pad: value stored in the columns between K and the leading dimension
@@ -126,10 +128,12 @@ def random_case(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", alpha=1.
     if beta != 0.0:
         C = _int32(g, (M, N)) if dtype_a == "i8" else _normal(g, (M, N), 1.0)
     bias = None
-    if epilogue in ("bias", "bias_gelu"):
+    if epilogue in ("bias", "bias_gelu") or any(
+            op == "bias" or (isinstance(op, tuple) and op[0] == "bias") for op in program or []):
         bias = _normal(g, (N,), 0.1)
     return Case(name or "random_%s_%s_%dx%dx%d" % (dtype_a, dtype_b, M, N, K), M, N, K,
-                dtype_a, dtype_b, A, B, C, bias, float(alpha), float(beta), epilogue, lda, ldb)
+                dtype_a, dtype_b, A, B, C, bias, float(alpha), float(beta), epilogue, lda, ldb,
+                program=list(program) if program else None)
 
 
 def _int32(g, shape):
