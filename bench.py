@@ -202,6 +202,8 @@ def workload_info(name):
         "w4a16_m16": ("W4A16 M=16,N=8960,K=1536, E2M1 weights x FP16, bias+erf-GELU", "hbm"),
         "w4a16_m2048": ("W4A16 M=2048,N=8960,K=1536, E2M1 weights x FP16, bias+erf-GELU",
                         "tensor"),
+        "qkv_1x128x4096_b96": ("96 FP16 GEMMs M=1,N=128,K=4096 in one strided-batched call "
+                               "(QKV projections of 32 heads)", "hbm"),
     }
     return info[name]
 
@@ -216,7 +218,7 @@ def algorithmic_bytes(case):
         b += case.M * case.N * ed
     if case.bias is not None:
         b += case.N * 2
-    return int(b)
+    return int(b * case.batch)
 
 
 def kernel_name(plan, case):
@@ -241,20 +243,23 @@ def run_dg(args, world, rank, local):
     name = args.workload
     desc, bound = workload_info(name)
     base = workloads.WORKLOADS[name]()
+    batch = base.batch
     out_dtype = torch.int32 if base.dtype_a == "i8" else torch.float16
     out_bytes = 4 if base.dtype_a == "i8" else 2
-    set_bytes = base.A.nbytes + base.B.nbytes + base.M * base.N * out_bytes
+    out_shape = (batch, base.M, base.N) if batch > 1 else (base.M, base.N)
+    set_bytes = base.A.nbytes + base.B.nbytes + batch * base.M * base.N * out_bytes
     nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes)) if set_bytes < 3 * L2_BYTES else 1
     nsets = min(nsets, 16)
     sets = []
     A0 = torch.from_numpy(base.A).to(dev)
     B0 = torch.from_numpy(base.B).to(dev)
     C0 = (torch.from_numpy(base.C).to(dev) if base.C is not None else
-          torch.zeros(base.M, base.N, dtype=out_dtype, device=dev))
+          torch.zeros(*out_shape, dtype=out_dtype, device=dev))
     bias = torch.from_numpy(base.bias).to(dev) if base.bias is not None else None
     for s in range(nsets):
-        # further sets: the same values with rows rotated (same distribution,
-        # different addresses), so no step finds its operands in L2
+        # further sets: the same values with rows (problems, for a batch)
+        # rotated (same distribution, different addresses), so no step finds
+        # its operands in L2
         sh = 37 * s
         sets.append((torch.roll(A0, sh, 0).contiguous(), torch.roll(B0, sh, 0).contiguous(),
                      torch.roll(C0, sh, 0).contiguous(), bias))
@@ -266,6 +271,10 @@ def run_dg(args, world, rank, local):
     def step(i, st=None):
         st = st or stream
         A, B, C, bias = sets[i % nsets]
+        if batch > 1:
+            dg.gemm_batched(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
+                            epilogue=base.epilogue, stream=st)
+            return
         dg.gemm(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
                 epilogue=base.epilogue, stream=st, plan=forced)
 
@@ -344,9 +353,31 @@ def run_dg(args, world, rank, local):
     hB = torch.from_numpy(base.B).pin_memory()
     hC = torch.from_numpy(base.C).pin_memory() if base.C is not None else None
     hbias = torch.from_numpy(base.bias).pin_memory() if base.bias is not None else None
-    hD = torch.empty(base.M, base.N, dtype=out_dtype).pin_memory()
+    hD = torch.empty(*out_shape, dtype=out_dtype).pin_memory()
+    e2e_call = "dg_gemm_host on pinned host buffers"
+    if batch > 1:
+        # The batched call takes device buffers: the step copies the pinned
+        # inputs in, runs dg_gemm_strided_batched and copies D back.
+        e2e_call = "pinned host-to-device copies, dg_gemm_strided_batched, device-to-host copy"
+        dA, dB = torch.empty_like(A0), torch.empty_like(B0)
+        dD = torch.empty(*out_shape, dtype=out_dtype, device=dev)
+        dC = torch.empty_like(dD) if hC is not None else None
+        dbias = torch.empty_like(bias) if hbias is not None else None
 
     def e2e_step():
+        if batch > 1:
+            with torch.cuda.stream(stream):
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                if dC is not None:
+                    dC.copy_(hC, non_blocking=True)
+                    dD.copy_(dC)
+                if dbias is not None:
+                    dbias.copy_(hbias, non_blocking=True)
+                dg.gemm_batched(dA, dB, dD, K=base.K, bias=dbias, alpha=base.alpha,
+                                beta=base.beta, epilogue=base.epilogue, stream=stream)
+                hD.copy_(dD, non_blocking=True)
+            return
         dg.gemm_host(hA, hB, hD, C=hC, K=base.K, bias=hbias, alpha=base.alpha, beta=base.beta,
                      epilogue=base.epilogue, dtype_b=base.dtype_b, stream=stream)
 
@@ -401,7 +432,8 @@ def run_dg(args, world, rank, local):
         "dtype": "i8" if base.dtype_a == "i8" else "f16",
         "data": "synthetic (seeded, recipe in workloads.py)",
         "config": {"workload": desc, "name": name, "M": base.M, "N": base.N, "K": base.K,
-                   "alpha": base.alpha, "beta": base.beta, "epilogue": base.epilogue,
+                   "batch": batch, "alpha": base.alpha, "beta": base.beta,
+                   "epilogue": base.epilogue,
                    "ramp": "%d untimed steps (%.1f s) before the warm-up" % (ramp_steps, RAMP_S),
                    "timing": ("CUDA-graph replay of the K steps" if args.graph else
                               "eager back-to-back launches") +
@@ -410,14 +442,16 @@ def run_dg(args, world, rank, local):
                    if nsets > 1 else "inputs larger than L2",
                    "parallelism": "replicas" if world > 1 else "1 GPU",
                    "plan": {k: plan[k] for k in ("kernel_name", "m_tile", "n_tile", "k_tile",
-                                                 "split_k", "stages", "grid")}},
+                                                 "split_k", "stages", "grid")},
+                   "plan_note": ("the single problem's plan; a batched GEMV picks its split-K "
+                                 "for the whole batch" if batch > 1 else "")},
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": unit,
                 "h2d_bytes_per_step": int(hA.nbytes + hB.nbytes +
                                           (hC.nbytes if hC is not None else 0) +
                                           (hbias.nbytes if hbias is not None else 0)),
                 "d2h_bytes_per_step": int(hD.nbytes),
-                "call": "dg_gemm_host on pinned host buffers, %d steps" % e2e_steps},
+                "call": "%s, %d steps" % (e2e_call, e2e_steps)},
         "gpu_launches": int(launches),
         "clocks": sampler.summary(),
     }
@@ -441,6 +475,16 @@ def oracle_sample_rate(case, budget_s, rows_per_call, bound="tensor"):
     import oracle
     rng = np.random.default_rng(0)
     done_rows, t_total = 0, 0.0
+    if case.batch > 1:  # whole problems, chosen at random
+        while t_total < budget_s and done_rows < case.batch * case.M:
+            z = int(rng.integers(case.batch))
+            t = time.perf_counter()
+            oracle.gemm_reference(case.A[z], case.B[z], case.K, case.dtype_a, case.dtype_b,
+                                  alpha=case.alpha, beta=case.beta, epilogue=case.epilogue)
+            t_total += time.perf_counter() - t
+            done_rows += case.M
+        work, unit = work_unit(case, bound)
+        return work * done_rows / (case.M * case.batch) / t_total / 1e12, unit, t_total, done_rows
     while t_total < budget_s and done_rows < 64 * case.M:
         rows = rng.choice(case.M, size=min(rows_per_call, case.M), replace=False)
         t = time.perf_counter()
@@ -469,6 +513,11 @@ def run_reference(args):
     rng = np.random.default_rng(1)
 
     def step():
+        if case.batch > 1:  # one whole problem per step
+            z = int(rng.integers(case.batch))
+            oracle.gemm_reference(case.A[z], case.B[z], case.K, case.dtype_a, case.dtype_b,
+                                  alpha=case.alpha, beta=case.beta, epilogue=case.epilogue)
+            return
         r = rng.choice(case.M, size=rows, replace=False)
         oracle.gemm_reference(case.A, case.B, case.K, case.dtype_a, case.dtype_b, C=case.C,
                               bias=case.bias, alpha=case.alpha, beta=case.beta,
@@ -481,9 +530,13 @@ def run_reference(args):
         step()
     dt = time.perf_counter() - t
     work, unit = work_unit(case, workload_info(name)[1])
-    value = work * rows / case.M * args.steps / dt / 1e12
-    sample = "%d random rows of the %dx%dx%d product per step (%s)" % (rows, case.M, case.N,
-                                                                      case.K, name)
+    if case.batch > 1:
+        value = work / case.batch * args.steps / dt / 1e12
+        sample = "one random problem of the %d per step (%s)" % (case.batch, name)
+    else:
+        value = work * rows / case.M * args.steps / dt / 1e12
+        sample = "%d random rows of the %dx%dx%d product per step (%s)" % (rows, case.M, case.N,
+                                                                          case.K, name)
     return {
         "impl": "reference",
         "metric": "GEMM TFLOP/s (INT8 TOPS) and % of GB300 dense peak; GB/s vs HBM for M=1",
@@ -537,8 +590,9 @@ def main():
                                                   bound=workload_info(args.workload)[1])
             line["cpu_baseline"] = {
                 "value": v, "unit": u, "cores": cpu_cores(), "kind": "oracle",
-                "sample": "%d rows of the %dx%dx%d product in %.1f s (fp64 numpy BLAS, "
-                          "default threads)" % (rows, case.M, case.N, case.K, secs)}
+                "sample": "%d rows of the %s%dx%dx%d product in %.1f s (fp64 numpy BLAS, "
+                          "default threads)" % (rows, "%d x " % case.batch if case.batch > 1
+                                                else "", case.M, case.N, case.K, secs)}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -227,6 +227,32 @@ dg_status dg_gemm_ex(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype
                      int64_t ldc, void *D, int64_t ldd, const void *bias, float alpha, float beta,
                      const dg_epilogue_program *program, dg_stream_t stream);
 
+/* A strided batch of independent problems of one shape:
+ *   D_z = epilogue(alpha * A_z.B_z + beta * C_z),  z = 0 .. batch-1,
+ * with A_z = A + z*stride_a, B_z = B + z*stride_b, C_z (= D_z) = C + z*stride_c
+ * and bias_z = bias + z*stride_bias.  For the pages' many small GEMMs of one
+ * shape, e.g. the attention QKV projections M=1, N=128, K=4096
+ * (discosf.com/news/5532976, section 5.3, third stage).
+ *   Strides are element counts (codes for E2M1 B), >= 0; 0 shares the
+ *   operand between problems (e.g. one bias for all).  With batch > 1,
+ *   stride_c >= M*N (outputs may not overlap) and stride_a and stride_b span
+ *   multiples of 16 bytes, so every problem's A and B keep dg_gemm's
+ *   alignment; stride_c may be any such count (C and D of problem z > 0 need
+ *   only their element alignment).  Each problem otherwise follows dg_gemm's
+ *   layouts and rules.
+ *   When the planner picks the thin split-K GEMV for the shape (FP16, M <= 8)
+ *   the whole batch is one launch; otherwise each problem is launched in
+ *   turn on `stream`.  The GEMV's split-K workspace grows with the batch.
+ *   batch == 0 is a no-op.
+ * Errors: as dg_gemm, plus DG_ERR_INVALID_ARG for a negative batch or
+ * stride, overlapping outputs or a misaligned stride_a / stride_b. */
+dg_status dg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                  dg_dtype dtype_a, dg_dtype dtype_b, const void *A, int64_t lda,
+                                  int64_t stride_a, const void *B, int64_t ldb, int64_t stride_b,
+                                  void *C, int64_t stride_c, const void *bias,
+                                  int64_t stride_bias, float alpha, float beta,
+                                  dg_epilogue epilogue, dg_stream_t stream);
+
 /* As dg_gemm, but runs `plan` (one returned by dg_plan_tiles for the same
  * M, N, K and dtypes).  DG_ERR_INVALID_STATE when the plan does not fit. */
 dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,

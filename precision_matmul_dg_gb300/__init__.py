@@ -12,7 +12,8 @@ import os
 
 __all__ = [
     "DgError", "F16", "I8", "E2M1", "EPILOGUES", "lib", "lib_path", "gemm", "gemm_raw",
-    "gemm_host", "gemm_host_raw", "gemm_ex", "gemm_ex_raw", "OPS", "MAX_EPILOGUE_OPS",
+    "gemm_host", "gemm_host_raw", "gemm_ex", "gemm_ex_raw", "gemm_batched",
+    "gemm_strided_batched_raw", "OPS", "MAX_EPILOGUE_OPS",
     "EpilogueOp", "EpilogueProgram", "make_program",
     "plan_tiles", "query_hw", "last_error", "check_status", "set_wait_timeout_ns",
     "selftest_wait_timeout", "launch_count", "shutdown", "HwDesc", "TilePlan", "EXPORTS",
@@ -30,7 +31,7 @@ KERNELS = {0: "tc", 1: "gemv", 2: "tc_widened", 3: "skinny", -1: "none"}
 
 # Every symbol include/dg.h declares.
 EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_gemm_host",
-           "dg_gemm_ex",
+           "dg_gemm_ex", "dg_gemm_strided_batched",
            "dg_gemm_thin_noalloc", "dg_last_error",
            "dg_check_status", "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout",
            "dg_launch_count", "dg_shutdown"]
@@ -123,6 +124,8 @@ def lib():
     L.dg_gemm_thin_noalloc.argtypes = gemm_args + [vp]
     L.dg_gemm_host.argtypes = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, vp, vp, f32, f32,
                                i32, vp]
+    L.dg_gemm_strided_batched.argtypes = [i64, i64, i64, i64, i32, i32, vp, i64, i64, vp, i64,
+                                          i64, vp, i64, vp, i64, f32, f32, i32, vp]
     L.dg_gemm_ex.argtypes = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, f32,
                              f32, ctypes.POINTER(EpilogueProgram), vp]
     L.dg_last_error.restype = ctypes.c_char_p
@@ -134,7 +137,7 @@ def lib():
     L.dg_launch_count.argtypes = []
     L.dg_shutdown.argtypes = []
     for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
-                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_gemm_ex", "dg_check_status",
+                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_gemm_ex", "dg_gemm_strided_batched", "dg_check_status",
                  "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout", "dg_shutdown"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -285,6 +288,56 @@ def gemm_ex(A, B, D, C=None, K=None, bias=None, alpha=1.0, beta=0.0, program=(),
     gemm_ex_raw(M, N, K, dtype_a, dtype_b, A, A.stride(0), B, ldb, C, ldc, D, D.stride(0), bias,
                 alpha, beta, program=make_program(program or []), stream=stream)
     return D
+
+
+def gemm_strided_batched_raw(batch, M, N, K, dtype_a, dtype_b, A, lda, stride_a, B, ldb, stride_b,
+                             C, stride_c, bias, stride_bias, alpha, beta, epilogue, stream=None):
+    """dg_gemm_strided_batched with the C argument order."""
+    args = (int(batch), int(M), int(N), int(K), _dtype_code(dtype_a), _dtype_code(dtype_b),
+            _ptr(A), int(lda), int(stride_a), _ptr(B), int(ldb), int(stride_b), _ptr(C),
+            int(stride_c), _ptr(bias), int(stride_bias), float(alpha), float(beta),
+            _epi_code(epilogue), _stream_handle(stream))
+    _check(lib().dg_gemm_strided_batched(*args))
+
+
+def gemm_batched(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none",
+                 dtype_b=None, stream=None):
+    """D_z = epilogue(alpha * A_z.B_z + beta * C_z) for every z, written into C.
+
+    A: [batch, M, lda]; B: [batch, N, ldb] or [N, ldb] (shared by all
+    problems; uint8 packed codes for E2M1); C: [batch, M, N], each [M, N]
+    dense; bias: [batch, N] or [N] (shared).  The batch strides are the
+    tensors' first-dimension strides.
+    """
+    import torch
+    dtype_a = "i8" if A.dtype == torch.int8 else "f16"
+    if dtype_b is None:
+        dtype_b = {torch.float16: "f16", torch.int8: "i8", torch.uint8: "e2m1"}[B.dtype]
+    if A.dim() != 3 or C.dim() != 3 or B.dim() not in (2, 3):
+        raise ValueError("A and C must be 3-D, B 2-D or 3-D")
+    batch, M, N = C.shape
+    _expect(A[0], dtype_a, "A")
+    B0 = B[0] if B.dim() == 3 else B
+    _expect(B0, dtype_b, "B")
+    _expect(C[0], "i32" if dtype_a == "i8" else "f16", "C")
+    if A.shape[0] != batch or A.shape[1] != M or B0.shape[0] != N or \
+            (B.dim() == 3 and B.shape[0] != batch):
+        raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape),
+                                                               tuple(C.shape)))
+    if C.stride(1) != N:
+        raise ValueError("each C[z] must be dense row-major (leading dimension N)")
+    if K is None:
+        K = A.shape[2]
+    codes = 2 if dtype_b == "e2m1" else 1
+    ldb = B0.stride(0) * codes
+    stride_b = B.stride(0) * codes if B.dim() == 3 else 0
+    stride_bias = 0
+    if bias is not None and bias.dim() == 2:
+        stride_bias = bias.stride(0)
+    gemm_strided_batched_raw(batch, M, N, K, dtype_a, dtype_b, A, A.stride(1), A.stride(0), B,
+                             ldb, stride_b, C, C.stride(0), bias, stride_bias, alpha, beta,
+                             epilogue, stream=stream)
+    return C
 
 
 def gemm_host_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, D, bias, alpha, beta, epilogue,

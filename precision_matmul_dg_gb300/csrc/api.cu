@@ -286,12 +286,24 @@ dg_status get_wide_workspace(int dev, cudaStream_t stream, int64_t elems, __half
   return DG_OK;
 }
 
-// D (leading dimension ldd) = epilogue(alpha * A.B + beta * C (ldc)).  The
-// caller has validated the epilogue; C and D are checked here.
+dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev);
+
+// Strided batch of one problem shape (dg_gemm_strided_batched): problem z
+// at A + z sa, B + z sb, C/D + z sc, bias + z sbias (elements; codes for
+// E2M1).  Validated by the caller.
+struct BatchSpec {
+  int64_t count = 1;
+  int64_t sa = 0, sb = 0, sc = 0, sbias = 0;
+};
+
+// D (leading dimension ldd) = epilogue(alpha * A.B + beta * C (ldc)), for
+// one problem or a strided batch.  The caller has validated the epilogue
+// (and the batch strides); C and D are checked here.
 dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const void* A,
               int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc, void* D,
               int64_t ldd, const void* bias, float alpha, float beta, const EpiSpec& epi,
-              const dg_tile_plan* forced, cudaStream_t stream) {
+              const dg_tile_plan* forced, cudaStream_t stream,
+              const BatchSpec& batch = BatchSpec()) {
   dg_status s = validate(M, N, K, da, db, A, lda, B, ldb, D, bias, alpha, beta, epi.flags);
   if (s != DG_OK) return s;
   if (M == 0 || N == 0) return DG_OK;
@@ -338,10 +350,27 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
   a.timeout_ns = timeout_ns();
   a.sm_count = st->hw.sm_count;
   a.exact_i32 = false;
+  a.batch = 1;
+  a.stride_a = a.stride_b = a.stride_c = a.stride_d = a.stride_bias = 0;
+
+  // Problem z of the batch as a single problem.
+  const int64_t out_bytes = da == DG_I8 ? 4 : 2;
+  auto problem = [&](int64_t z) {
+    GemmArgs w = a;
+    w.A = static_cast<const uint8_t*>(A) + z * batch.sa * elem_bits(da) / 8;
+    w.B = static_cast<const uint8_t*>(B) + z * batch.sb * elem_bits(db) / 8;
+    w.C = static_cast<const uint8_t*>(C) + z * batch.sc * out_bytes;
+    w.D = static_cast<uint8_t*>(D) + z * batch.sc * out_bytes;
+    w.bias = bias ? static_cast<const uint8_t*>(bias) + z * batch.sbias * 2 : nullptr;
+    return w;
+  };
 
   if (K == 0) {
-    cudaError_t e = launch_epilogue_only(a);
-    return e == cudaSuccess ? DG_OK : fail_cuda(e, "epilogue-only launch");
+    for (int64_t z = 0; z < batch.count; ++z) {
+      cudaError_t e = launch_epilogue_only(problem(z));
+      if (e != cudaSuccess) return fail_cuda(e, "epilogue-only launch");
+    }
+    return DG_OK;
   }
 
   dg_tile_plan plan{};
@@ -382,16 +411,44 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
             plan.k_tile, plan.split_k, plan.stages, plan.grid, plan.est_us);
   }
 
-  cudaError_t e = cudaSuccess;
   if (plan.kernel == DG_KERNEL_GEMV) {
+    // The GEMV kernel takes the whole batch in one launch (grid.z).
+    if (batch.count > 1 && !forced) {
+      int64_t chunk = 0;
+      plan.split_k = gemv_best_split(M, N, K, st->hw, &chunk, batch.count);
+      plan.k_tile = static_cast<int>(chunk);
+    }
     SplitKWorkspace ws{nullptr, 0, nullptr, 0};
     if (plan.split_k > 1) {
-      s = get_workspace(dev, stream, gemv_partial_elems(plan, M, N), gemv_counter_elems(plan, N),
-                        &ws);
+      s = get_workspace(dev, stream, gemv_partial_elems(plan, M, N, batch.count),
+                        gemv_counter_elems(plan, N, batch.count), &ws);
       if (s != DG_OK) return s;
     }
-    e = launch_gemv(a, plan, ws);
-  } else if (plan.kernel == DG_KERNEL_SKINNY) {
+    a.batch = batch.count;
+    a.stride_a = batch.sa;
+    a.stride_b = batch.sb;
+    a.stride_c = batch.sc;
+    a.stride_d = batch.sc;
+    a.stride_bias = batch.sbias;
+    const cudaError_t e = launch_gemv(a, plan, ws);
+    return e == cudaSuccess ? DG_OK : fail_cuda(e, "kernel launch");
+  }
+  // Other kernels: one launch (or widening + launch) per problem.
+  for (int64_t z = 0; z < batch.count; ++z) {
+    s = dispatch(problem(z), plan, dev);
+    if (s != DG_OK) return s;
+  }
+  return DG_OK;
+}
+
+// Launches `plan` (not the GEMV) for the single problem `a`.
+dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev) {
+  const int64_t M = a.M, N = a.N, K = a.K;
+  const dg_dtype da = a.dtype_a, db = a.dtype_b;
+  const cudaStream_t stream = a.stream;
+  dg_status s = DG_OK;
+  cudaError_t e = cudaSuccess;
+  if (plan.kernel == DG_KERNEL_SKINNY) {
     e = launch_skinny(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC) {
     e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);
@@ -406,11 +463,11 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
     WidenJob jobs[2];
     int njobs = 0;
     if (da == DG_I8) {
-      jobs[njobs++] = WidenJob{DG_I8, A, M, lda, wide};
+      jobs[njobs++] = WidenJob{DG_I8, a.A, M, a.lda, wide};
       w.A = wide;
       w.lda = ldw;
     }
-    jobs[njobs++] = WidenJob{db, B, N, ldb, wide + a_elems};
+    jobs[njobs++] = WidenJob{db, a.B, N, a.ldb, wide + a_elems};
     e = launch_widen(jobs, njobs, K, stream, a.sm_count);
     if (e != cudaSuccess) return fail_cuda(e, "widening launch");
     w.B = wide + a_elems;
@@ -617,6 +674,37 @@ dg_status dg_gemm_ex(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype
   if (s != DG_OK) return s;
   return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, ldc, D, ldd, bias, alpha, beta, epi,
              nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                  dg_dtype dtype_a, dg_dtype dtype_b, const void* A, int64_t lda,
+                                  int64_t stride_a, const void* B, int64_t ldb, int64_t stride_b,
+                                  void* C, int64_t stride_c, const void* bias,
+                                  int64_t stride_bias, float alpha, float beta,
+                                  dg_epilogue epilogue, dg_stream_t stream) {
+  clear_error();
+  EpiSpec epi;
+  dg_status s = fixed_epilogue(epilogue, &epi);
+  if (s != DG_OK) return s;
+  if (batch < 0) return fail(DG_ERR_INVALID_ARG, "negative batch");
+  if (batch == 0) return DG_OK;
+  if (stride_a < 0 || stride_b < 0 || stride_c < 0 || stride_bias < 0)
+    return fail(DG_ERR_INVALID_ARG, "negative batch stride");
+  if (batch > 1) {
+    if (M > 0 && N > 0 && stride_c < M * N)
+      return fail(DG_ERR_INVALID_ARG, "stride_c (%lld) < M * N: the problems' outputs overlap",
+                  (long long)stride_c);
+    if ((stride_a * elem_bits(dtype_a)) % 128 != 0 || (stride_b * elem_bits(dtype_b)) % 128 != 0)
+      return fail(DG_ERR_INVALID_ARG, "stride_a and stride_b must span multiples of 16 bytes");
+  }
+  BatchSpec bs;
+  bs.count = batch;
+  bs.sa = stride_a;
+  bs.sb = stride_b;
+  bs.sc = stride_c;
+  bs.sbias = stride_bias;
+  return run(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, N, C, N, bias, alpha, beta, epi,
+             nullptr, reinterpret_cast<cudaStream_t>(stream), bs);
 }
 
 dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,

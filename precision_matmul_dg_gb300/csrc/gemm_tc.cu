@@ -433,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = al * sum[cl][hh * 16 + i];
             if (be != 0u && row < p.M) {
-              if (x + 16 <= p.N && (p.ldc & 3) == 0) {
+              if (x + 16 <= p.N && (p.ldc & 3) == 0 &&
+                  (reinterpret_cast<uintptr_t>(p.C) & 15) == 0) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                   const uint4 c = *reinterpret_cast<const uint4*>(crow + x + q * 4);

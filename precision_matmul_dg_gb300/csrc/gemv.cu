@@ -19,6 +19,7 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "epilogue.cuh"
@@ -51,6 +52,13 @@ struct GemvParams {
 };
 static_assert(sizeof(GemvParams) <= 128, "parameter struct within 128 bytes (see Epi)");
 
+// Strided batch: problem z (blockIdx.z) reads A + z sa, B + z sb, C + z sc
+// and bias + z sbias and writes D + z sd (elements); its split-K partials
+// and counters follow those of problem z - 1.
+struct GemvBatch {
+  int64_t sa, sb, sc, sd, sbias;
+};
+
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -77,17 +85,29 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ void write_out(const GemvParams& p, const EpiProgram& prog, int m,
-                                          int j, float acc) {
-  const float c = (p.epi.beta != 0.0f) ? __half2float(p.C[static_cast<int64_t>(m) * p.ldc + j])
+// One problem's output side: C, D and bias already offset to the problem.
+struct GemvOut {
+  const __half* C;
+  __half* D;
+  const __half* bias;
+};
+
+__device__ __forceinline__ void write_out(const GemvParams& p, const GemvOut& o,
+                                          const EpiProgram& prog, int m, int j, float acc) {
+  const float c = (p.epi.beta != 0.0f) ? __half2float(o.C[static_cast<int64_t>(m) * p.ldc + j])
                                         : 0.0f;
-  const float b = (p.epi.flags & kEpiBias) ? __half2float(p.bias[j]) : 0.0f;
-  p.D[static_cast<int64_t>(m) * p.ldd + j] = __float2half_rn(epi_apply(acc, c, b, p.epi, prog));
+  const float b = (p.epi.flags & kEpiBias) ? __half2float(o.bias[j]) : 0.0f;
+  o.D[static_cast<int64_t>(m) * p.ldd + j] = __float2half_rn(epi_apply(acc, c, b, p.epi, prog));
 }
 
 template <int MROWS>
-__global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const GemvParams p, const __grid_constant__ EpiProgram prog) {
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const GemvParams p, const __grid_constant__ EpiProgram prog,
+                       const GemvBatch bt) {
   grid_dependency_wait();  // launched as a dependent of the previous kernel
+  const int64_t z = blockIdx.z;
+  const __half* A = p.A + z * bt.sa;
+  const __half* B = p.B + z * bt.sb;
+  const GemvOut out{p.C + z * bt.sc, p.D + z * bt.sd, p.bias ? p.bias + z * bt.sbias : nullptr};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * kGemvWarps + warp;
@@ -100,7 +120,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
   for (int m = 0; m < MROWS; ++m) acc[m] = 0.0f;
 
   if (j < p.N && k0 < k1) {
-    const __half* brow = p.B + static_cast<int64_t>(j) * p.ldb;
+    const __half* brow = B + static_cast<int64_t>(j) * p.ldb;
     int k = k0 + lane * 8;
     // Batches of kGemvUnroll 256-element steps: every load of a batch is in
     // flight at once (one memory round trip per batch); steps past the end
@@ -117,7 +137,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
         for (int m = 0; m < MROWS; ++m) {
           if (m < p.M) {
             const uint4 av = __ldg(reinterpret_cast<const uint4*>(
-                p.A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
+                A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
             fma8(acc[m], av, bv[u]);
           }
         }
@@ -137,7 +157,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
           for (int m = 0; m < MROWS; ++m) {
             if (m < p.M) {
               const uint4 av = __ldg(reinterpret_cast<const uint4*>(
-                  p.A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
+                  A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
               fma8(acc[m], av, bv[u]);
             }
           }
@@ -154,7 +174,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
 #pragma unroll
         for (int m = 0; m < MROWS; ++m)
           if (m < p.M)
-            acc[m] = fmaf(__half2float(p.A[static_cast<int64_t>(m) * p.lda + kk]), bf, acc[m]);
+            acc[m] = fmaf(__half2float(A[static_cast<int64_t>(m) * p.lda + kk]), bf, acc[m]);
       }
     }
   }
@@ -169,24 +189,26 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
     if (lane == 0 && j < p.N) {
 #pragma unroll
       for (int m = 0; m < MROWS; ++m)
-        if (m < p.M) write_out(p, prog, m, j, acc[m]);
+        if (m < p.M) write_out(p, out, prog, m, j, acc[m]);
     }
     return;
   }
 
   // Split-K: publish this split's partial sums, then the last CTA of the
   // row group reduces all splits in index order.
+  float* partial = p.partial + z * p.split_k * p.M * static_cast<int64_t>(p.N);
+  unsigned* counters = p.counters + z * gridDim.x;
   if (lane == 0 && j < p.N) {
 #pragma unroll
     for (int m = 0; m < MROWS; ++m)
       if (m < p.M)
-        p.partial[(static_cast<int64_t>(split) * p.M + m) * p.N + j] = acc[m];
+        partial[(static_cast<int64_t>(split) * p.M + m) * p.N + j] = acc[m];
   }
   __threadfence();
   __syncthreads();
   __shared__ unsigned s_is_last;
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(&p.counters[blockIdx.x], 1u);
+    const unsigned prev = atomicAdd(&counters[blockIdx.x], 1u);
     s_is_last = (prev == static_cast<unsigned>(p.split_k - 1)) ? 1u : 0u;
   }
   __syncthreads();
@@ -199,10 +221,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const Gemv
     if (jj >= p.N) continue;
     float s = 0.0f;
     for (int sp = 0; sp < p.split_k; ++sp)
-      s += __ldcg(&p.partial[(static_cast<int64_t>(sp) * p.M + m) * p.N + jj]);
-    write_out(p, prog, m, jj, s);
+      s += __ldcg(&partial[(static_cast<int64_t>(sp) * p.M + m) * p.N + jj]);
+    write_out(p, out, prog, m, jj, s);
   }
-  if (threadIdx.x == 0) p.counters[blockIdx.x] = 0u;  // ready for the next launch
+  if (threadIdx.x == 0) counters[blockIdx.x] = 0u;  // ready for the next launch
 }
 
 // K == 0: D = epilogue(beta * C), no product term.  Element i of the M x N
@@ -251,12 +273,12 @@ __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 
 }  // namespace
 
-int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N) {
-  return plan.split_k > 1 ? static_cast<int64_t>(plan.split_k) * M * N : 0;
+int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t batch) {
+  return plan.split_k > 1 ? static_cast<int64_t>(plan.split_k) * M * N * batch : 0;
 }
 
-int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N) {
-  return plan.split_k > 1 ? (N + kGemvWarps - 1) / kGemvWarps : 0;
+int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N, int64_t batch) {
+  return plan.split_k > 1 ? (N + kGemvWarps - 1) / kGemvWarps * batch : 0;
 }
 
 cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws) {
@@ -285,9 +307,26 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
               : a.M <= 2 ? gemv_splitk_kernel<2>
               : a.M <= 4 ? gemv_splitk_kernel<4>
                          : gemv_splitk_kernel<kGemvMaxM>;
-  const cudaError_t e = launch_dependent(kern, grid, block, 0, a.stream, p, make_program(a));
-  count_launches(1);
-  return e;
+  // grid.z takes at most 65535 problems per launch
+  constexpr int64_t kMaxZ = 65535;
+  const int64_t groups = (a.N + kGemvWarps - 1) / kGemvWarps;
+  const GemvBatch bt{a.stride_a, a.stride_b, a.stride_c, a.stride_d, a.stride_bias};
+  for (int64_t z0 = 0; z0 < a.batch; z0 += kMaxZ) {
+    const int64_t nz = std::min(kMaxZ, a.batch - z0);
+    GemvParams q = p;
+    q.A += z0 * bt.sa;
+    q.B += z0 * bt.sb;
+    q.C += z0 * bt.sc;
+    q.D += z0 * bt.sd;
+    if (q.bias) q.bias += z0 * bt.sbias;
+    if (q.partial) q.partial += z0 * plan.split_k * a.M * a.N;
+    if (q.counters) q.counters += z0 * groups;
+    const dim3 g(grid.x, grid.y, static_cast<unsigned>(nz));
+    const cudaError_t e = launch_dependent(kern, g, block, 0, a.stream, q, make_program(a), bt);
+    count_launches(1);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_epilogue_only(const GemmArgs& a) {
@@ -442,6 +481,8 @@ extern "C" dg_status dg_gemm_thin_noalloc(int64_t M, int64_t N, int64_t K, dg_dt
   a.epi = ((epilogue == DG_EPI_BIAS || epilogue == DG_EPI_BIAS_GELU) ? kEpiBias : 0) |
           ((epilogue == DG_EPI_GELU || epilogue == DG_EPI_BIAS_GELU) ? kEpiGelu : 0);
   a.n_ops = 0;
+  a.batch = 1;
+  a.stride_a = a.stride_b = a.stride_c = a.stride_d = a.stride_bias = 0;
   a.stream = st;
   a.status = nullptr;
   a.timeout_ns = 0;

@@ -64,6 +64,11 @@ struct GemmArgs {
   int epi;    // kEpiBias | kEpiGelu, or kEpiProgram (+ kEpiBias)
   int n_ops;  // kEpiProgram: the ops, in order
   EpiOp ops[kMaxEpiOps];
+  // Strided batch (GEMV kernel only): `batch` problems, problem z at
+  // A + z stride_a, B + z stride_b, C + z stride_c, D + z stride_d,
+  // bias + z stride_bias (elements).  1 for a single problem.
+  int64_t batch;
+  int64_t stride_a, stride_b, stride_c, stride_d, stride_bias;
   cudaStream_t stream;
   int* status;          // per-device status word (device memory)
   uint64_t timeout_ns;  // device-side wait limit
@@ -114,9 +119,9 @@ cudaError_t launch_widen(const WidenJob* jobs, int njobs, int64_t K, cudaStream_
                          int sm_count);
 cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns);
 
-// Workspace sizes a GEMV plan needs.
-int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N);
-int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N);
+// Workspace sizes a GEMV plan needs for `batch` problems.
+int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t batch);
+int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N, int64_t batch);
 
 // Kernel-launch counter and error state (api.cu).  None of these allocate.
 void count_launches(int n);
@@ -129,8 +134,10 @@ dg_status validate_gemm_args(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dt
 
 // Split-K choice of the GEMV kernel (planner.cpp): cost-model time of one
 // split count (negative when the split is not allowed), and the best split.
+// `batch` independent problems of the shape share one launch.
 double gemv_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_desc& hw,
-                        int64_t* chunk_out);
-int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out);
+                        int64_t* chunk_out, int64_t batch = 1);
+int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out,
+                    int64_t batch = 1);
 
 }  // namespace dg

@@ -394,29 +394,30 @@ void add_warp_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, const
 // keeps about 2 KB in flight (~2 GB/s); HBM caps the total.  Returns a
 // negative value when the last split would be empty.  Allocates nothing.
 double gemv_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_desc& hw,
-                        int64_t* chunk_out) {
+                        int64_t* chunk_out, int64_t batch) {
   const int64_t kk = K > 0 ? K : 1;
   const int64_t chunk = ceil_div(ceil_div(kk, split), 256) * 256;
   if (split > 1 && chunk * (split - 1) >= kk) return -1.0;
   if (chunk_out) *chunk_out = chunk;
   const int64_t resident = static_cast<int64_t>(hw.sm_count) * kGemvResidentWarpsPerSm;
-  const int64_t units = N * split;
+  const int64_t units = N * split * batch;
   const double active = static_cast<double>(std::min(units, resident));
   const double bw = std::min(hbm_bytes_per_us(hw), active * 2.0e3);
-  const double bytes = 2.0 * (N * K + M * K) + (split > 1 ? 8.0 * split * M * N : 0.0) +
-                       4.0 * M * N;
+  const double bytes = batch * (2.0 * (N * K + M * K) + (split > 1 ? 8.0 * split * M * N : 0.0) +
+                                4.0 * M * N);
   // A warp streams its K range in batches of 4 x 256 elements, one memory
   // round trip (~0.8 us) each; small problems are bound by that latency.
   const double batches = static_cast<double>(ceil_div(chunk, 1024));
   return std::max(bytes / bw, 0.8 * batches) + (split > 1 ? 1.0 : 0.0) + 2.0;
 }
 
-int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out) {
+int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out,
+                    int64_t batch) {
   int best = 1;
   double best_t = -1.0;
   for (int split : kGemvSplits) {
     int64_t chunk = 0;
-    const double t = gemv_estimate_us(M, N, K, split, hw, &chunk);
+    const double t = gemv_estimate_us(M, N, K, split, hw, &chunk, batch);
     if (t < 0) continue;
     if (best_t < 0 || t < best_t) {
       best_t = t;

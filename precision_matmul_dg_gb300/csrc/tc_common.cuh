@@ -113,7 +113,9 @@ __device__ __forceinline__ void store_f16_32(const float (&v)[32], __half* drow,
 // D = round_fp16(epilogue(alpha*acc + beta*C)), the epilogue being bias then
 // GELU (flags) or a program.  C (read only when beta != 0) has leading
 // dimension ldc, D has ldd; they are one buffer or do not overlap.  Rows >= M
-// and columns >= N are skipped.
+// and columns >= N are skipped.  16-byte accesses need a 16-byte aligned
+// base and a pitch of a multiple of 8 (a batched problem's C and D may start
+// anywhere 2-byte aligned); otherwise the chunk takes one element at a time.
 __device__ __forceinline__ void epilogue_f16_chunk(const uint32_t (&r)[32], int row, int col0,
                                                    int M, int N, const Epi& epi,
                                                    const EpiProgram& prog, const __half* c,
@@ -125,10 +127,10 @@ __device__ __forceinline__ void epilogue_f16_chunk(const uint32_t (&r)[32], int 
   for (int i = 0; i < 32; ++i) v[i] = epi.alpha * __uint_as_float(r[i]);
   __half* drow = d + static_cast<int64_t>(row) * ldd;
   const bool in_range = col0 + 32 <= N;
-  const bool full = in_range && ((ldd & 7) == 0);
+  const bool full = in_range && ((ldd & 7) == 0) && ((reinterpret_cast<uintptr_t>(d) & 15) == 0);
   if (epi.beta != 0.0f) {
     const __half* crow = c + static_cast<int64_t>(row) * ldc;
-    if (in_range && (ldc & 7) == 0) {
+    if (in_range && (ldc & 7) == 0 && (reinterpret_cast<uintptr_t>(c) & 15) == 0) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 cv = *reinterpret_cast<const uint4*>(crow + col0 + q * 8);
@@ -274,7 +276,8 @@ __device__ __forceinline__ void store_i32_chunk(const uint32_t (&s)[32], int row
   const int32_t* crow = o.c + static_cast<int64_t>(row) * o.ldc;
   int32_t* drow = o.d + static_cast<int64_t>(row) * o.ldd;
   const uint32_t al = static_cast<uint32_t>(alpha), be = static_cast<uint32_t>(beta);
-  const bool full = (col0 + 32 <= N) && (((o.ldc | o.ldd) & 3) == 0);
+  const bool full = (col0 + 32 <= N) && (((o.ldc | o.ldd) & 3) == 0) &&
+                    (((reinterpret_cast<uintptr_t>(o.c) | reinterpret_cast<uintptr_t>(o.d)) & 15) == 0);
   if (full) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {

@@ -199,6 +199,50 @@ def test_make_program_limits(dg):
     assert (p.ops[1].a, p.ops[2].a, p.ops[2].b) == (0.5, -1.0, 1.0)
 
 
+def _call_batched(dg, **over):
+    kw = dict(batch=4, M=1, N=128, K=4096, dtype_a="f16", dtype_b="f16", A=0x10000, lda=4096,
+              sa=4096, B=0x20000, ldb=4096, sb=128 * 4096, C=0x30000, sc=128, bias=None,
+              sbias=0, alpha=1.0, beta=0.0, epilogue="none")
+    kw.update(over)
+    try:
+        dg.gemm_strided_batched_raw(kw["batch"], kw["M"], kw["N"], kw["K"], kw["dtype_a"],
+                                    kw["dtype_b"], kw["A"], kw["lda"], kw["sa"], kw["B"],
+                                    kw["ldb"], kw["sb"], kw["C"], kw["sc"], kw["bias"],
+                                    kw["sbias"], kw["alpha"], kw["beta"], kw["epilogue"],
+                                    stream=0)
+    except dg.DgError as e:
+        return e.name, str(e)
+    return "DG_OK", ""
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(batch=-1), "DG_ERR_INVALID_ARG"),
+    (dict(sa=-8), "DG_ERR_INVALID_ARG"),
+    (dict(sbias=-1), "DG_ERR_INVALID_ARG"),
+    (dict(sc=120), "DG_ERR_INVALID_ARG"),            # outputs overlap
+    (dict(sa=4100), "DG_ERR_INVALID_ARG"),           # 8200 bytes: not a multiple of 16
+    (dict(dtype_b="e2m1", sb=16), "DG_ERR_INVALID_ARG"),   # 8 bytes of codes
+    (dict(epilogue="bias"), "DG_ERR_INVALID_ARG"),   # null bias
+    (dict(epilogue="sigmoid"), "DG_ERR_INVALID_ARG"),
+    (dict(C=None), "DG_ERR_INVALID_ARG"),
+])
+def test_batched_invalid_arguments_rejected(dg, over, status):
+    if over.get("epilogue") == "sigmoid":
+        over = dict(over, epilogue=7)
+    got, msg = _call_batched(dg, **over)
+    assert got == status, msg
+    assert msg
+
+
+def test_batched_empty_is_a_noop(dg):
+    assert _call_batched(dg, batch=0, A=None, B=None, C=None)[0] == "DG_OK"
+    assert _call_batched(dg, M=0)[0] == "DG_OK"
+    # one problem: any stride, as the strides are never applied
+    import torch
+    if not torch.cuda.is_available():
+        assert _call_batched(dg, batch=1, sc=3, sa=1)[0] == "DG_ERR_INVALID_STATE"
+
+
 def test_empty_problem_is_a_noop(dg):
     assert _call(dg, M=0)[0] == "DG_OK"
     assert _call(dg, N=0, A=None, B=None)[0] == "DG_OK"

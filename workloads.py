@@ -40,9 +40,10 @@ class Case:
     ldb: int = 0
     meta: dict = field(default_factory=dict)
     program: Optional[list] = None  # epilogue ops in order (replaces `epilogue`)
+    batch: int = 1  # > 1: A [batch, M, lda], B [batch, N, ldb], C [batch, M, N]
 
     def flops(self):
-        return 2.0 * self.M * self.N * self.K
+        return 2.0 * self.M * self.N * self.K * self.batch
 
 
 def _gen(seed):
@@ -177,6 +178,17 @@ def w4a16(M, N=8960, K=1536, seed=0):
                        name="w4a16_m%d" % M)
 
 
+def batched_thin(batch, N, K, seed=0):
+    """`batch` independent M=1 FP16 GEMMs of one shape, e.g. the Q, K and V
+    projections of 32 attention heads (96 problems of 1 x 128 x 4096); a and
+    every B ~ N(0,1)/sqrt(K), alpha=1, beta=0."""
+    g = _gen(seed)
+    A = _normal(g, (batch, 1, K), 1.0 / math.sqrt(K))
+    B = _normal(g, (batch, N, K), 1.0 / math.sqrt(K))
+    return Case("qkv_1x%dx%d_b%d" % (N, K, batch), 1, N, K, "f16", "f16", A, B, lda=K, ldb=K,
+                batch=batch)
+
+
 WORKLOADS = {
     "f16_256": lambda: f16_256(),
     "f16_2048": lambda: f16_square(2048),
@@ -187,4 +199,5 @@ WORKLOADS = {
     "thin_1x256x12800": lambda: thin(256, 12800),
     "w4a16_m16": lambda: w4a16(16),
     "w4a16_m2048": lambda: w4a16(2048),
+    "qkv_1x128x4096_b96": lambda: batched_thin(96, 128, 4096),
 }
