@@ -228,6 +228,8 @@ def kernel_name(plan, case):
         return "gemv_splitk_kernel"
     if plan["kernel_name"] == "skinny":
         return "skinny_w4a16_kernel"
+    if plan["kernel_name"] == "gemv_mma":
+        return "gemv_mma_kernel"
     if plan["kernel_name"] == "tc_widened" or (case.dtype_a == "f16" and case.dtype_b == "f16"):
         return "gemm_f16_tc_kernel"
     return "gemm_conv_tc_kernel"

@@ -106,8 +106,10 @@ typedef enum {
   DG_KERNEL_TC_WIDENED = 2, /* int8 / E2M1 operands widened to FP16 by a streaming pre-pass into
                                a library workspace, then the FP16 tensor-core kernel (INT8:
                                exact INT32 output) -- for compute-bound shapes */
-  DG_KERNEL_SKINNY = 3 /* FP16 x E2M1 with M <= 16 (HBM-bound): packed weights streamed into
-                          registers, widened there and fed to warp-level m16n8k16 MMAs */
+  DG_KERNEL_SKINNY = 3, /* FP16 x E2M1 with M <= 16 (HBM-bound): packed weights streamed into
+                           registers, widened there and fed to warp-level m16n8k16 MMAs */
+  DG_KERNEL_GEMV_MMA = 4 /* FP16 x FP16 with 2 <= M <= 16 (HBM-bound): the split-K GEMV's
+                            streaming of B rows, multiplied on warp-level m16n8k16 MMAs */
 } dg_kernel;
 
 /* Hardware description the planner solves against

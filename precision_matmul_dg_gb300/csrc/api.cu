@@ -411,11 +411,13 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
             plan.k_tile, plan.split_k, plan.stages, plan.grid, plan.est_us);
   }
 
-  if (plan.kernel == DG_KERNEL_GEMV) {
-    // The GEMV kernel takes the whole batch in one launch (grid.z).
+  if (plan.kernel == DG_KERNEL_GEMV || plan.kernel == DG_KERNEL_GEMV_MMA) {
+    // The GEMV kernels take the whole batch in one launch (grid.z).
+    const bool mma = plan.kernel == DG_KERNEL_GEMV_MMA;
     if (batch.count > 1 && !forced) {
       int64_t chunk = 0;
-      plan.split_k = gemv_best_split(M, N, K, st->hw, &chunk, batch.count);
+      plan.split_k = mma ? gemv_mma_best_split(M, N, K, st->hw, &chunk, batch.count)
+                         : gemv_best_split(M, N, K, st->hw, &chunk, batch.count);
       plan.k_tile = static_cast<int>(chunk);
     }
     SplitKWorkspace ws{nullptr, 0, nullptr, 0};
@@ -430,7 +432,7 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
     a.stride_c = batch.sc;
     a.stride_d = batch.sc;
     a.stride_bias = batch.sbias;
-    const cudaError_t e = launch_gemv(a, plan, ws);
+    const cudaError_t e = mma ? launch_gemv_mma(a, plan, ws) : launch_gemv(a, plan, ws);
     return e == cudaSuccess ? DG_OK : fail_cuda(e, "kernel launch");
   }
   // Other kernels: one launch (or widening + launch) per problem.

@@ -101,7 +101,8 @@ __device__ __forceinline__ void write_out(const GemvParams& p, const GemvOut& o,
 }
 
 template <int MROWS>
-__global__ void __launch_bounds__(kGemvWarps * 32) gemv_splitk_kernel(const GemvParams p, const __grid_constant__ EpiProgram prog,
+__global__ void __launch_bounds__(kGemvWarps * 32)
+    gemv_splitk_kernel(const GemvParams p, const __grid_constant__ EpiProgram prog,
                        const GemvBatch bt) {
   grid_dependency_wait();  // launched as a dependent of the previous kernel
   const int64_t z = blockIdx.z;
@@ -256,6 +257,158 @@ __global__ void epilogue_only_i32_kernel(int64_t M, int64_t N, const int32_t* C,
   }
 }
 
+// ------------------------------------------------------------ warp-MMA GEMV
+// For 2 <= M <= 16 the FMA kernel above runs out of issue slots before HBM
+// runs out of bandwidth (every B element meets M multiply-adds plus its
+// conversion).  This variant feeds the same stream of B rows to warp-level
+// m16n8k16 tensor-core MMAs: a warp owns 8 output columns (the MMA's n = 8)
+// and up to 16 rows of A (its m = 16; rows >= M are zero), a CTA owns 64
+// columns, and K is split over grid.y with the FMA kernel's deterministic
+// last-CTA reduction.
+//
+// Fragments without shuffles: lane (g = lane / 4, t = lane % 4) loads 16
+// bytes of B row n0 + g and of A rows g and g + 8 at k = k_step + 8t.  The
+// m16n8k16 fragment wants, at lane (g, t), B[k][g] and A[g][k] for MMA-k
+// 2t, 2t+1 (first register) and 2t+8, 2t+9 (second); taking MMA-k
+// {2t, 2t+1, 2t+8, 2t+9} to mean k_step + 8t + {0, 1, 2, 3} in the first MMA
+// and + {4, 5, 6, 7} in the second is one permutation of the 32 k of the step,
+// the same for A and B, so the sum over k is unchanged.
+constexpr int kMmaWarps = 8;
+constexpr int kMmaCols = kMmaWarps * 8;  // output columns per CTA
+constexpr int kMmaUnroll = 8;            // 32-wide k steps per batch
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Both MMAs of one 32-wide k step: A rows g (av) and g + 8 (av8), B row (bv).
+__device__ __forceinline__ void mma_step(float (&d)[4], const uint4& av, const uint4& av8,
+                                         const uint4& bv) {
+  mma_16816(d, av.x, av8.x, av.y, av8.y, bv.x, bv.y);
+  mma_16816(d, av.z, av8.z, av.w, av8.w, bv.z, bv.w);
+}
+
+// The 8 halves at row + k .. k + 7 that lie below k1, zeros above.
+__device__ __forceinline__ uint4 load8_tail(const __half* row, int k, int k1) {
+  uint4 v = make_uint4(0, 0, 0, 0);
+  __half* h = reinterpret_cast<__half*>(&v);
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (k + e < k1) h[e] = row[k + e];
+  return v;
+}
+
+template <int MROWS>  // 8: rows g only; 16: rows g and g + 8
+__global__ void __launch_bounds__(kMmaWarps * 32)
+    gemv_mma_kernel(const GemvParams p, const __grid_constant__ EpiProgram prog,
+                    const GemvBatch bt) {
+  grid_dependency_wait();  // launched as a dependent of the previous kernel
+  const int64_t z = blockIdx.z;
+  const __half* A = p.A + z * bt.sa;
+  const __half* B = p.B + z * bt.sb;
+  const GemvOut out{p.C + z * bt.sc, p.D + z * bt.sd, p.bias ? p.bias + z * bt.sbias : nullptr};
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int n0 = (blockIdx.x * kMmaWarps + warp) * 8;
+  const int split = blockIdx.y;
+  const int k0 = split * p.k_chunk;
+  const int k1 = min(p.K, k0 + p.k_chunk);
+
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // Lanes past the last column read row N - 1 (in bounds) and discard it.
+  const __half* brow = B + static_cast<int64_t>(min(n0 + g, p.N - 1)) * p.ldb;
+  const bool has_a0 = g < p.M, has_a8 = MROWS == 16 && g + 8 < p.M;
+  const __half* arow0 = A + static_cast<int64_t>(has_a0 ? g : 0) * p.lda;
+  const __half* arow8 = A + static_cast<int64_t>(has_a8 ? g + 8 : 0) * p.lda;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+
+  if (n0 < p.N && k0 < k1) {  // warp-uniform: every lane reaches every MMA
+    constexpr int kStep = 32;
+    int kw = k0;  // the warp's k; this lane's 8 elements start at kw + 8t
+    for (; kw + kMmaUnroll * kStep <= k1; kw += kMmaUnroll * kStep) {
+      uint4 bv[kMmaUnroll], av[kMmaUnroll], av8[kMmaUnroll];
+#pragma unroll
+      for (int u = 0; u < kMmaUnroll; ++u) bv[u] = ld_stream(brow + kw + u * kStep + 8 * t);
+#pragma unroll
+      for (int u = 0; u < kMmaUnroll; ++u) {
+        av[u] = has_a0 ? __ldg(reinterpret_cast<const uint4*>(arow0 + kw + u * kStep + 8 * t))
+                       : zero;
+        av8[u] = has_a8 ? __ldg(reinterpret_cast<const uint4*>(arow8 + kw + u * kStep + 8 * t))
+                        : zero;
+      }
+#pragma unroll
+      for (int u = 0; u < kMmaUnroll; ++u) mma_step(acc, av[u], av8[u], bv[u]);
+    }
+    // whole 32-wide steps left
+    for (; kw + kStep <= k1; kw += kStep) {
+      const uint4 bv = ld_stream(brow + kw + 8 * t);
+      const uint4 av =
+          has_a0 ? __ldg(reinterpret_cast<const uint4*>(arow0 + kw + 8 * t)) : zero;
+      const uint4 av8 =
+          has_a8 ? __ldg(reinterpret_cast<const uint4*>(arow8 + kw + 8 * t)) : zero;
+      mma_step(acc, av, av8, bv);
+    }
+    // a last partial step: elements at or past k1 read as zero
+    if (kw < k1) {
+      const int kl = kw + 8 * t;
+      const uint4 bv = load8_tail(brow, kl, k1);
+      const uint4 av = has_a0 ? load8_tail(arow0, kl, k1) : zero;
+      const uint4 av8 = has_a8 ? load8_tail(arow8, kl, k1) : zero;
+      mma_step(acc, av, av8, bv);
+    }
+  }
+  // The next kernel's blocks may be scheduled now (see the FMA kernel).
+  grid_launch_dependents();
+
+  // acc[0..1]: row g, columns n0 + 2t + {0, 1}; acc[2..3]: row g + 8.
+  const int col = n0 + 2 * t;
+  if (p.split_k == 1) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (g + 8 * h < p.M && col + e < p.N)
+          write_out(p, out, prog, g + 8 * h, col + e, acc[2 * h + e]);
+    return;
+  }
+
+  // Split-K: partials, then the last CTA of the column group reduces.
+  float* partial = p.partial + z * p.split_k * p.M * static_cast<int64_t>(p.N);
+  unsigned* counters = p.counters + z * gridDim.x;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      if (g + 8 * h < p.M && col + e < p.N)
+        partial[(static_cast<int64_t>(split) * p.M + g + 8 * h) * p.N + col + e] = acc[2 * h + e];
+  __threadfence();
+  __syncthreads();
+  __shared__ unsigned s_is_last;
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&counters[blockIdx.x], 1u);
+    s_is_last = (prev == static_cast<unsigned>(p.split_k - 1)) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_is_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < kMmaCols * p.M; i += blockDim.x) {
+    const int m = i / kMmaCols;
+    const int jj = blockIdx.x * kMmaCols + (i % kMmaCols);
+    if (jj >= p.N) continue;
+    float s = 0.0f;
+    for (int sp = 0; sp < p.split_k; ++sp)
+      s += __ldcg(&partial[(static_cast<int64_t>(sp) * p.M + m) * p.N + jj]);
+    write_out(p, out, prog, m, jj, s);
+  }
+  if (threadIdx.x == 0) counters[blockIdx.x] = 0u;  // ready for the next launch
+}
+
 // One CTA waits on a barrier nobody arrives on; the bounded wait must give up,
 // record the timeout and let the kernel exit normally.
 __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
@@ -323,6 +476,50 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
     if (q.counters) q.counters += z0 * groups;
     const dim3 g(grid.x, grid.y, static_cast<unsigned>(nz));
     const cudaError_t e = launch_dependent(kern, g, block, 0, a.stream, q, make_program(a), bt);
+    count_launches(1);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_gemv_mma(const GemmArgs& a, const dg_tile_plan& plan,
+                            const SplitKWorkspace& ws) {
+  if (a.M < 1 || a.M > 16) return cudaErrorInvalidValue;
+  GemvParams p;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.A = static_cast<const __half*>(a.A);
+  p.lda = a.lda;
+  p.B = static_cast<const __half*>(a.B);
+  p.ldb = a.ldb;
+  p.C = static_cast<const __half*>(a.C);
+  p.ldc = a.ldc;
+  p.D = static_cast<__half*>(a.D);
+  p.ldd = a.ldd;
+  p.bias = static_cast<const __half*>(a.bias);
+  p.epi = make_epi(a);
+  p.split_k = plan.split_k;
+  p.k_chunk = plan.k_tile;
+  p.partial = ws.partial;
+  p.counters = ws.counters;
+  const unsigned gx = static_cast<unsigned>((a.N + kMmaCols - 1) / kMmaCols);
+  auto kern = a.M <= 8 ? gemv_mma_kernel<8> : gemv_mma_kernel<16>;
+  constexpr int64_t kMaxZ = 65535;
+  const GemvBatch bt{a.stride_a, a.stride_b, a.stride_c, a.stride_d, a.stride_bias};
+  for (int64_t z0 = 0; z0 < a.batch; z0 += kMaxZ) {
+    const int64_t nz = std::min(kMaxZ, a.batch - z0);
+    GemvParams q = p;
+    q.A += z0 * bt.sa;
+    q.B += z0 * bt.sb;
+    q.C += z0 * bt.sc;
+    q.D += z0 * bt.sd;
+    if (q.bias) q.bias += z0 * bt.sbias;
+    if (q.partial) q.partial += z0 * plan.split_k * a.M * a.N;
+    if (q.counters) q.counters += z0 * gx;
+    const dim3 grid(gx, static_cast<unsigned>(plan.split_k), static_cast<unsigned>(nz));
+    const cudaError_t e = launch_dependent(kern, grid, dim3(kMmaWarps * 32), 0, a.stream, q,
+                                           make_program(a), bt);
     count_launches(1);
     if (e != cudaSuccess) return e;
   }

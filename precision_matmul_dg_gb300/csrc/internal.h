@@ -97,6 +97,9 @@ struct SplitKWorkspace {
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);    // F16 x F16
 cudaError_t launch_conv(const GemmArgs& a, const dg_tile_plan& plan);  // I8 x I8, F16 x E2M1
 cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws);
+// Warp-MMA GEMV (gemv.cu): F16 x F16 with M <= 16 on m16n8k16 tensor-core MMAs.
+cudaError_t launch_gemv_mma(const GemmArgs& a, const dg_tile_plan& plan,
+                            const SplitKWorkspace& ws);
 // Skinny W4A16 kernel (skinny.cu): FP16 A with M <= 16 x packed E2M1 B.
 cudaError_t launch_skinny(const GemmArgs& a, const dg_tile_plan& plan);
 int skinny_smem_bytes();
@@ -139,5 +142,10 @@ double gemv_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_
                         int64_t* chunk_out, int64_t batch = 1);
 int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out,
                     int64_t batch = 1);
+// The same for the warp-MMA GEMV (2 <= M <= 16).
+double gemv_mma_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_desc& hw,
+                            int64_t* chunk_out, int64_t batch = 1);
+int gemv_mma_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw,
+                        int64_t* chunk_out, int64_t batch = 1);
 
 }  // namespace dg

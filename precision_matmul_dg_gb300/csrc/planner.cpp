@@ -270,6 +270,57 @@ void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype 
   }
 }
 
+// Warp-MMA GEMV (FP16 x FP16, 2 <= M <= 16): CTAs of 8 warps, a warp owns 8
+// output columns and streams their 8 rows of B in batches of 8 x 32 K.
+constexpr int kGemvMmaMinM = 2;
+constexpr int kGemvMmaMaxM = 16;
+constexpr int kGemvMmaCols = 64;
+constexpr int kGemvMmaThreads = 256;
+constexpr int kGemvMmaRegsPerThread = 80;  // upper bound of what ptxas assigns the kernel
+
+void add_gemv_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+                             const dg_hw_desc& hw, double target, std::vector<dg_tile_plan>* out,
+                             std::string* why) {
+  if (!(da == DG_F16 && db == DG_F16)) return;
+  if (M < kGemvMmaMinM || M > kGemvMmaMaxM) {
+    if (why) *why += "warp-MMA GEMV: M outside [2, 16]; ";
+    return;
+  }
+  const int ctas = hw.regs_per_sm / (kGemvMmaRegsPerThread * kGemvMmaThreads);
+  if (ctas < 1) {
+    if (why) *why += "warp-MMA GEMV: registers; ";
+    return;
+  }
+  const int64_t resident = static_cast<int64_t>(hw.sm_count) * ctas * (kGemvMmaThreads / 32);
+  for (int split : kGemvSplits) {
+    int64_t chunk = 0;
+    const double t = gemv_mma_estimate_us(M, N, K, split, hw, &chunk);
+    if (t < 0) continue;
+    const int64_t units = ceil_div(N, 8) * split;  // warps
+    const int64_t waves = ceil_div(units, resident);
+    const double occ = static_cast<double>(units) / static_cast<double>(waves * resident);
+    if (occ < target) {
+      if (why) *why += "warp-MMA GEMV split " + std::to_string(split) + ": occupancy; ";
+      continue;
+    }
+    dg_tile_plan p{};
+    p.kernel = DG_KERNEL_GEMV_MMA;
+    p.m_tile = kGemvMmaMaxM;
+    p.n_tile = kGemvMmaCols;
+    p.k_tile = static_cast<int>(chunk);
+    p.split_k = split;
+    p.stages = 1;
+    p.cta_group = 1;
+    p.smem_bytes = 0;
+    p.threads = kGemvMmaThreads;
+    p.grid = static_cast<int>(ceil_div(N, kGemvMmaCols) * split);
+    p.occupancy = occ;
+    p.est_us = t;
+    p.est_tflops = 2.0 * M * N * K / (t * 1e6);
+    out->push_back(p);
+  }
+}
+
 // Skinny W4A16 kernel: FP16 A with M <= 16 rows x packed E2M1 B, one block
 // of 512 threads per 64 columns, K in 2048-code chunks split between two warp
 // halves; the weights stream from HBM once.
@@ -408,7 +459,52 @@ double gemv_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_
   // A warp streams its K range in batches of 4 x 256 elements, one memory
   // round trip (~0.8 us) each; small problems are bound by that latency.
   const double batches = static_cast<double>(ceil_div(chunk, 1024));
-  return std::max(bytes / bw, 0.8 * batches) + (split > 1 ? 1.0 : 0.0) + 2.0;
+  // Each further row of A costs the FMA loop about 0.65 of the one-row time
+  // (measured on GB300 at M = 2..8: 1.7x, 3.0x, 5.8x at M = 2, 4, 8).
+  const double rows = 1.0 + 0.65 * static_cast<double>(M - 1);
+  return std::max(bytes / bw, 0.8 * batches) * rows + (split > 1 ? 1.0 : 0.0) + 2.0;
+}
+
+double gemv_mma_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_desc& hw,
+                            int64_t* chunk_out, int64_t batch) {
+  const int64_t kk = K > 0 ? K : 1;
+  const int64_t chunk = ceil_div(ceil_div(kk, split), 256) * 256;
+  if (split > 1 && chunk * (split - 1) >= kk) return -1.0;
+  if (chunk_out) *chunk_out = chunk;
+  const int ctas = std::max(1, hw.regs_per_sm / (kGemvMmaRegsPerThread * kGemvMmaThreads));
+  const int64_t resident = static_cast<int64_t>(hw.sm_count) * ctas * (kGemvMmaThreads / 32);
+  const int64_t units = ceil_div(N, 8) * split * batch;  // warps
+  // A warp keeps 8 rows x 8 steps x 64 bytes = 4 KB in flight; measured on
+  // GB300 it moves about 2 KB per us.  Warps beyond one resident wave run in
+  // later waves.
+  const int64_t waves = ceil_div(units, resident);
+  const double per_wave = static_cast<double>(std::min(units, resident));
+  const double bw = std::min(hbm_bytes_per_us(hw), per_wave * 2.0e3);
+  const double bytes = batch * (2.0 * (N * K + M * K) + (split > 1 ? 8.0 * split * M * N : 0.0) +
+                                4.0 * M * N);
+  const double t_mem = waves * (bytes * per_wave / static_cast<double>(units)) / bw;
+  const double batches = static_cast<double>(ceil_div(chunk, 256));
+  // Fixed costs measured on GB300: about 6 us of launch, ramp and tail; the
+  // 16-row variant (M > 8) streams about 1.2x slower than the 8-row one.
+  const double rows = M > 8 ? 1.2 : 1.0;
+  return std::max(t_mem, 0.8 * batches * waves) * rows + (split > 1 ? 1.0 : 0.0) + 6.0;
+}
+
+int gemv_mma_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw,
+                        int64_t* chunk_out, int64_t batch) {
+  int best = 1;
+  double best_t = -1.0;
+  for (int split : kGemvSplits) {
+    int64_t chunk = 0;
+    const double t = gemv_mma_estimate_us(M, N, K, split, hw, &chunk, batch);
+    if (t < 0) continue;
+    if (best_t < 0 || t < best_t) {
+      best_t = t;
+      best = split;
+      if (chunk_out) *chunk_out = chunk;
+    }
+  }
+  return best;
 }
 
 int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64_t* chunk_out,
@@ -438,6 +534,7 @@ dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype
     add_tc_candidates(M, N, K, dtype_a, dtype_b, false, hw, target_occupancy, &cands, why);
     add_tc_candidates(M, N, K, dtype_a, dtype_b, true, hw, target_occupancy, &cands, why);
     add_gemv_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
+    add_gemv_mma_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
     add_skinny_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
   } else {
     add_warp_mma_candidates(M, N, K, dtype_a, hw, target_occupancy, &cands, why);
@@ -516,6 +613,18 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
     if (plan.split_k < 1 || plan.k_tile <= 0 || plan.k_tile % 8 != 0 ||
         static_cast<int64_t>(plan.k_tile) * plan.split_k < K) {
       if (why) *why = "GEMV plan: K chunks do not cover K";
+      return false;
+    }
+    return true;
+  }
+  if (plan.kernel == DG_KERNEL_GEMV_MMA) {
+    if (!(dtype_a == DG_F16 && dtype_b == DG_F16) || M < 1 || M > kGemvMmaMaxM) {
+      if (why) *why = "warp-MMA GEMV plan needs F16 x F16 and M <= 16";
+      return false;
+    }
+    if (plan.split_k < 1 || plan.k_tile <= 0 || plan.k_tile % 8 != 0 ||
+        static_cast<int64_t>(plan.k_tile) * plan.split_k < K) {
+      if (why) *why = "warp-MMA GEMV plan: K chunks do not cover K";
       return false;
     }
     return true;

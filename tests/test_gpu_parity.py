@@ -88,6 +88,27 @@ def test_every_gemv_split(dg):
         outs.append(got)
 
 
+@pytest.mark.parametrize("M", [2, 7, 8, 9, 15, 16])
+@pytest.mark.parametrize("K", [1, 8, 31, 100, 4097, 20000])
+def test_gemv_mma(dg, M, K):
+    # warp-MMA GEMV: ragged N (not a multiple of the 64-column CTA), K tails
+    # shorter than one 32-wide step, padding columns holding NaN
+    case = workloads.random_case(M, 300, K, epilogue="bias_gelu", alpha=0.75, beta=-1.25,
+                                 seed=M * 31 + K, pad=float("nan"))
+    plan = [p for p in _plans(dg, case) if p["kernel_name"] == "gemv_mma"][0]
+    got, _ = run_case(dg, case, plan=plan)
+    assert_parity(case, got)
+
+
+def test_every_gemv_mma_split(dg):
+    case = workloads.random_case(12, 200, 30000, beta=0.5, epilogue="gelu", seed=19)
+    gm = [p for p in _plans(dg, case) if p["kernel_name"] == "gemv_mma"]
+    assert {p["split_k"] for p in gm} >= {1, 2, 4, 8, 14}
+    for p in gm:
+        got, _ = run_case(dg, case, plan=p)
+        assert_parity(case, got)
+
+
 # ------------------------------------------------------- edge cases
 def test_k_zero(dg):
     for epi in ("none", "bias_gelu"):

@@ -80,6 +80,25 @@ GEMV_SPLITS = [1, 2, 3, 4, 5, 6, 7, 8, 10, 12, 13, 14, 16, 20, 24, 28, 32, 40, 4
                160, 192, 256]
 
 
+def gemv_mma_feasible(M, N, K, hw, target):
+    # warp-MMA GEMV: 2 <= M <= 16; CTAs of 256 threads at 80 registers, a
+    # warp per 8 columns
+    out = set()
+    if not 2 <= M <= 16:
+        return out
+    ctas = hw["regs_per_sm"] // (80 * 256)
+    resident = hw["sm_count"] * ctas * 8
+    for split in GEMV_SPLITS:
+        chunk = math.ceil(math.ceil(K / split) / 256) * 256
+        if split > 1 and chunk * (split - 1) >= K:
+            continue
+        units = math.ceil(N / 8) * split
+        waves = math.ceil(units / resident)
+        if units / (waves * resident) >= target:
+            out.add(("gemv_mma", 64, 1, split))
+    return out
+
+
 SHAPES = [(256, 256, 256), (4096, 4096, 4096), (2048, 2048, 2048), (8192, 8192, 8192),
           (1, 4096, 131072), (1, 256, 12800), (7, 1000, 999), (300, 520, 200), (129, 17, 64)]
 
@@ -88,7 +107,8 @@ SHAPES = [(256, 256, 256), (4096, 4096, 4096), (2048, 2048, 2048), (8192, 8192, 
 @pytest.mark.parametrize("target", [0.0, 0.5, 0.7, 0.9])
 def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
     M, N, K = shape
-    want = tc_feasible(M, N, GB300, target) | gemv_feasible(M, N, K, GB300, target)
+    want = (tc_feasible(M, N, GB300, target) | gemv_feasible(M, N, K, GB300, target) |
+            gemv_mma_feasible(M, N, K, GB300, target))
     if not want:
         with pytest.raises(dg.DgError) as ei:
             dg.plan_tiles(M, N, K, hw=GB300, target_occupancy=target)
@@ -110,11 +130,11 @@ def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
             assert p["m_tile"] == 128 * cg and p["k_tile"] == 64 and p["split_k"] == 1
             got.add(("tc", p["n_tile"], p["stages"], cg))
         else:
-            assert p["kernel_name"] == "gemv"
+            assert p["kernel_name"] in ("gemv", "gemv_mma")
             assert p["k_tile"] % 256 == 0
             assert p["k_tile"] * p["split_k"] >= K
             assert p["k_tile"] * (p["split_k"] - 1) < K      # no empty split
-            got.add(("gemv", p["n_tile"], p["stages"], p["split_k"]))
+            got.add((p["kernel_name"], p["n_tile"], p["stages"], p["split_k"]))
     assert got == want
     # ranked by estimated time
     ests = [p["est_us"] for p in plans]
