@@ -159,10 +159,13 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "gemm_f16_tc_kernel": ("gemm_tc.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh"),
-    "gemm_conv_tc_kernel": ("gemm_conv.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh"),
-    "gemv_splitk_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh"),
-    "skinny_w4a16_kernel": ("skinny.cu", "ptx.cuh", "epilogue.cuh"),
+    "gemm_f16_tc_kernel": ("gemm_tc.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh",
+                           "internal.h"),
+    "gemm_conv_tc_kernel": ("gemm_conv.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh",
+                            "internal.h"),
+    "gemv_splitk_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
+    "gemv_mma_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
+    "skinny_w4a16_kernel": ("skinny.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
 }
 
 
