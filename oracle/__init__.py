@@ -28,6 +28,7 @@ from .gemm_ref import (  # noqa: F401
     gemm_reference,
     error_bound,
     apply_program,
+    quantize_i8,
     PROGRAM_OPS,
     GELU_LIPSCHITZ,
 )

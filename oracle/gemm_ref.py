@@ -33,14 +33,17 @@ Functions and what each follows:
       section 6.1: GELU chosen by op type).  Reading taken: each op is the
       plain real function (t + bias_j, max(t, 0), GELU, a * t, min(max(t, lo),
       hi)); the op operands a, lo, hi are binary32 numbers, the type the C ABI
-      passes them in.  Pinned by hand-computed values and order-sensitivity
-      cases.
+      passes them in.  "quant_i8" (last op only) is the output quantization of
+      the same passage: D becomes int8, round-half-to-even(a * t) saturated to
+      [-128, 127], NaN to 0.  Pinned by hand-computed values and
+      order-sensitivity cases.
   error_bound -- the floating-point acceptance bound
       2^-10 * (|A|.|B|)_ij + 2^-10 * |D_ref|_ij, with (|A|.|B|) read as the
       magnitude of every term that enters t, a 2^-24 floor, and a GELU
       Lipschitz factor; for a program, the input error carried through each
-      op by its Lipschitz constant.  Pinned by direct checks on hand-computed
-      cases.
+      op by its Lipschitz constant, and |a| E + 1 for an int8 quantization
+      (the error of a * t, plus half a unit for each side's rounding).  Pinned
+      by direct checks on hand-computed cases.
 """
 
 import math
@@ -56,7 +59,7 @@ GELU_LIPSCHITZ = 1.13
 _EPILOGUES = ("none", "bias", "gelu", "bias_gelu")
 
 # Ops of an epilogue program and the number of operands each takes.
-PROGRAM_OPS = {"bias": 0, "relu": 0, "gelu": 0, "scale": 1, "clamp": 2}
+PROGRAM_OPS = {"bias": 0, "relu": 0, "gelu": 0, "scale": 1, "clamp": 2, "quant_i8": 1}
 
 
 def e2m1_value(code):
@@ -135,7 +138,16 @@ def _normalise_program(program):
         if name == "clamp" and not args[0] <= args[1]:
             raise ValueError("clamp needs lo <= hi")
         out.append((name,) + args)
+    if any(op[0] == "quant_i8" for op in out[:-1]):
+        raise ValueError("quant_i8 must be the last op")
     return out
+
+
+def quantize_i8(x):
+    """Round half to even, saturate to [-128, 127]; NaN to 0 (float64 codes)."""
+    x = np.asarray(x, dtype=np.float64)
+    q = np.clip(np.rint(np.nan_to_num(x, nan=0.0, posinf=np.inf, neginf=-np.inf)), -128, 127)
+    return np.where(np.isnan(x), 0.0, q)
 
 
 def apply_program(t, program, bias=None):
@@ -159,8 +171,10 @@ def apply_program(t, program, bias=None):
             t = gelu_erf(t)
         elif name == "scale":
             t = op[1] * t
-        else:  # clamp
+        elif name == "clamp":
             t = np.minimum(np.maximum(t, op[1]), op[2])
+        else:  # quant_i8
+            t = quantize_i8(op[1] * t)
     return t
 
 
@@ -313,8 +327,11 @@ def error_bound(A, B, K, D_ref, dtype_a="f16", dtype_b="f16", C=None, bias=None,
                 E = GELU_LIPSCHITZ * E
             elif name == "scale":
                 E = abs(op[1]) * E
+            elif name == "quant_i8":
+                E = abs(op[1]) * E + 1.0
             t = apply_program(t, [op], bias)
-            E = E + 2.0 ** -20 * np.abs(t)
+            if name != "quant_i8":
+                E = E + 2.0 ** -20 * np.abs(t)
         return E + 2.0 ** -10 * np.abs(D_ref) + 2.0 ** -24
     if epilogue in ("bias", "bias_gelu") and bias is not None:
         P = P + np.abs(np.asarray(bias).astype(np.float64))[None, :]

@@ -318,6 +318,12 @@ _PROG_CASES = [
     (["bias", "relu"], 1.0, [0.0, 0.0, 2.5, 0.0]),
     (["relu", "bias"], 1.0, [1.0, -0.5, 2.5, -1.0]),
     (["relu", ("clamp", 0.25, 1.0), ("scale", 4.0)], 2.0, [1.0, 4.0, 4.0, 4.0]),
+    # int8 output: round half to even, then saturate
+    ([("quant_i8", 2.0)], 1.0, [-6.0, 1.0, 4.0, 14.0]),
+    ([("quant_i8", 0.25)], 1.0, [-1.0, 0.0, 0.0, 2.0]),     # -0.75, 0.125, 0.5, 1.75
+    ([("quant_i8", 0.75)], 1.0, [-2.0, 0.0, 2.0, 5.0]),     # -2.25, 0.375, 1.5, 5.25
+    ([("scale", 100.0), ("quant_i8", 1.0)], 1.0, [-128.0, 50.0, 127.0, 127.0]),
+    (["bias", ("quant_i8", -1.0)], 1.0, [2.0, 0.0, -2.0, 1.0]),   # -(t + bias) = 2, .5, -2.5, 1
 ]
 
 
@@ -504,6 +510,28 @@ def _mut_clamp_order(t, program, bias=None):
     return t
 
 
+def _mut_round_half_up(t, program, bias=None):
+    # quantization rounding half away from zero instead of half to even
+    for op in program:
+        if isinstance(op, tuple) and op[0] == "quant_i8":
+            x = float(np.float32(op[1])) * np.asarray(t, dtype=np.float64)
+            t = np.clip(np.sign(x) * np.floor(np.abs(x) + 0.5), -128, 127)
+        else:
+            t = _ORIG_APPLY_PROGRAM(t, [op], bias)
+    return t
+
+
+def _mut_wrap_i8(t, program, bias=None):
+    # quantization wrapping modulo 256 instead of saturating
+    for op in program:
+        if isinstance(op, tuple) and op[0] == "quant_i8":
+            x = np.rint(float(np.float32(op[1])) * np.asarray(t, dtype=np.float64))
+            t = ((x + 128) % 256) - 128
+        else:
+            t = _ORIG_APPLY_PROGRAM(t, [op], bias)
+    return t
+
+
 def _mut_scale_decimal(t, program, bias=None):
     # scale operand kept as the decimal (binary64) value, not binary32
     for op in program:
@@ -519,6 +547,8 @@ MUTANTS = {
     "relu_as_abs": _Swap("apply_program", _mut_relu_abs),
     "clamp_order": _Swap("apply_program", _mut_clamp_order),
     "scale_binary64": _Swap("apply_program", _mut_scale_decimal),
+    "quant_round_half_up": _Swap("apply_program", _mut_round_half_up),
+    "quant_wraps": _Swap("apply_program", _mut_wrap_i8),
     "transposed_B": _Swap("_operand_b", _mut_transpose_b),
     "swapped_nibbles": _Swap("unpack_e2m1", _mut_nibbles),
     "tanh_gelu": _Swap("gelu_erf", _mut_tanh_gelu),
@@ -599,9 +629,28 @@ def test_error_bound_program_terms():
     assert np.allclose(bnd, want, rtol=1e-15, atol=0)
 
 
+def test_error_bound_quant_terms():
+    # t = 2 acc = [4, 2], E = 2^-10 [8, 6]; quant a = 3: |a| E + 1, then no
+    # per-op rounding term; D = [12, 6]
+    A = _f16([[1.0, -2.0]])
+    B = _f16([[3.0, 0.5], [-1.0, -1.0]])
+    prog = [("quant_i8", 3.0)]
+    D = oracle.gemm_reference(A, B, 2, alpha=2.0, program=prog)
+    assert np.array_equal(D, np.array([[12.0, 6.0]]))
+    bnd = oracle.error_bound(A, B, 2, D, alpha=2.0, program=prog)
+    want = 3.0 * 2.0 ** -10 * np.array([[8.0, 6.0]]) + 1.0 + 2.0 ** -10 * np.array([[12.0, 6.0]])
+    assert np.allclose(bnd, want + 2.0 ** -24, rtol=1e-15, atol=0)
+
+
+def test_quantize_special_values():
+    q = oracle.quantize_i8(np.array([np.nan, np.inf, -np.inf, 127.5, -128.5, 2.5, -2.5, 0.49999]))
+    assert q.tolist() == [0.0, 127.0, -128.0, 127.0, -128.0, 2.0, -2.0, 0.0]
+
+
 def test_program_rejects_bad_ops():
     A, B = _PROG_A, _PROG_B
-    for prog in (["tanh"], [("scale",)], [("clamp", 2.0, 1.0)], [("relu", 1.0)]):
+    for prog in (["tanh"], [("scale",)], [("clamp", 2.0, 1.0)], [("relu", 1.0)],
+                 [("quant_i8", 1.0), "relu"]):
         with pytest.raises(ValueError):
             oracle.gemm_reference(A, B, 1, program=prog)
     with pytest.raises(ValueError):
