@@ -85,8 +85,10 @@ typedef enum {
   DG_OP_RELU = 2,  /* t = max(t, 0); a NaN t becomes 0 */
   DG_OP_GELU = 3,  /* t = 0.5*t*(1 + erf(t/sqrt(2))) */
   DG_OP_SCALE = 4, /* t = t * a (e.g. a dequantization or output scale) */
-  DG_OP_CLAMP = 5  /* t = min(max(t, a), b), a <= b (saturation before a narrow output);
+  DG_OP_CLAMP = 5, /* t = min(max(t, a), b), a <= b (saturation before a narrow output);
                       a NaN t becomes a */
+  DG_OP_QUANT_I8 = 6 /* last op only: D is int8, D = round-half-to-even(a * t) saturated to
+                        [-128, 127], a NaN to 0 (output quantization); ldd counts bytes */
 } dg_op_type;
 
 typedef struct {
@@ -219,11 +221,13 @@ dg_status dg_gemm_host(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dty
  *     of D are never written.
  *   program: NULL or n_ops == 0 for none.  For I8 x I8 (exact INT32 output)
  *     it must be empty.  DG_OP_BIAS needs bias (FP16 [N]), which is read
- *     only by that op.
+ *     only by that op.  A program ending in DG_OP_QUANT_I8 makes D int8 (C,
+ *     when read, stays FP16), so C and D must then be different buffers.
  *   Plan, kernels, workspaces and errors as dg_gemm; DG_ERR_INVALID_ARG for
  *   ldc < N (with beta != 0), ldd < N, a NULL D, more than
- *   DG_MAX_EPILOGUE_OPS ops, an unknown op type or a clamp with a > b (or a
- *   NaN bound); DG_ERR_UNSUPPORTED for a program on I8 x I8. */
+ *   DG_MAX_EPILOGUE_OPS ops, an unknown op type, a clamp with a > b (or a
+ *   NaN bound), a non-finite scale, DG_OP_QUANT_I8 before the last op, or an
+ *   int8 D that is also C; DG_ERR_UNSUPPORTED for a program on I8 x I8. */
 dg_status dg_gemm_ex(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
                      const void *A, int64_t lda, const void *B, int64_t ldb, const void *C,
                      int64_t ldc, void *D, int64_t ldd, const void *bias, float alpha, float beta,

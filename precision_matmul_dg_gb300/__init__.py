@@ -22,7 +22,7 @@ __all__ = [
 F16, I8, E2M1 = 0, 1, 2
 DTYPES = {"f16": F16, "i8": I8, "e2m1": E2M1}
 EPILOGUES = {"none": 0, "bias": 1, "gelu": 2, "bias_gelu": 3}
-OPS = {"bias": 1, "relu": 2, "gelu": 3, "scale": 4, "clamp": 5}
+OPS = {"bias": 1, "relu": 2, "gelu": 3, "scale": 4, "clamp": 5, "quant_i8": 6}
 MAX_EPILOGUE_OPS = 8
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
           3: "DG_ERR_NO_VALID_CANDIDATE", 4: "DG_ERR_CUDA", 5: "DG_ERR_TIMEOUT",
@@ -89,7 +89,8 @@ class EpilogueProgram(ctypes.Structure):
 
 def make_program(ops):
     """EpilogueProgram from a list of ops: "relu", "gelu", "bias",
-    ("scale", a), ("clamp", lo, hi), or (type_code, a, b)."""
+    ("scale", a), ("clamp", lo, hi), ("quant_i8", a) (last op: int8 D), or
+    (type_code, a, b)."""
     ops = list(ops)
     if len(ops) > MAX_EPILOGUE_OPS:
         raise ValueError("at most %d epilogue ops" % MAX_EPILOGUE_OPS)
@@ -262,7 +263,8 @@ def gemm_ex(A, B, D, C=None, K=None, bias=None, alpha=1.0, beta=0.0, program=(),
     A and B as in gemm(); C and D are [M, N] views with unit column stride
     and any row stride (leading dimension) >= N, e.g. column slices of wider
     buffers; C may be D itself.  program: list of ops, applied in order
-    ("bias", "relu", "gelu", ("scale", a), ("clamp", lo, hi)).
+    ("bias", "relu", "gelu", ("scale", a), ("clamp", lo, hi)); a program
+    ending in ("quant_i8", a) writes an int8 D (C, when given, stays fp16).
     """
     import torch
     dtype_a = "i8" if A.dtype == torch.int8 else "f16"
@@ -271,7 +273,10 @@ def gemm_ex(A, B, D, C=None, K=None, bias=None, alpha=1.0, beta=0.0, program=(),
     _expect(A, dtype_a, "A")
     _expect(B, dtype_b, "B")
     out = "i32" if dtype_a == "i8" else "f16"
-    _expect(D, out, "D")
+    ops = list(program or [])
+    last = ops[-1] if ops else None
+    quant = last is not None and (last[0] if isinstance(last, tuple) else last) in ("quant_i8", 6)
+    _expect(D, "i8" if quant else out, "D")
     M, N = D.shape
     ldc = D.stride(0)
     if C is not None:
@@ -286,7 +291,7 @@ def gemm_ex(A, B, D, C=None, K=None, bias=None, alpha=1.0, beta=0.0, program=(),
         K = A.shape[1]
     ldb = B.stride(0) * (2 if dtype_b == "e2m1" else 1)
     gemm_ex_raw(M, N, K, dtype_a, dtype_b, A, A.stride(0), B, ldb, C, ldc, D, D.stride(0), bias,
-                alpha, beta, program=make_program(program or []), stream=stream)
+                alpha, beta, program=make_program(ops), stream=stream)
     return D
 
 

@@ -186,6 +186,13 @@ dg_status program_epilogue(const dg_epilogue_program* prog, EpiSpec* out) {
       case DG_OP_CLAMP:
         if (!(op.a <= op.b)) return fail(DG_ERR_INVALID_ARG, "op %d: clamp needs a <= b", k);
         break;
+      case DG_OP_QUANT_I8:
+        if (k != prog->n_ops - 1)
+          return fail(DG_ERR_INVALID_ARG, "op %d: the int8 quantization must be the last op", k);
+        if (!isfinite(op.a))
+          return fail(DG_ERR_INVALID_ARG, "op %d: quantization scale is not finite", k);
+        out->flags |= kEpiOutI8;
+        break;
       default:
         return fail(DG_ERR_INVALID_ARG, "op %d: unknown op type %d", k, op.type);
     }
@@ -315,6 +322,8 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
       return fail(DG_ERR_INVALID_ARG, "ldc (%lld) < N (%lld)", (long long)ldc, (long long)N);
     if (C == D && ldc != ldd)
       return fail(DG_ERR_INVALID_ARG, "C and D share a buffer with ldc != ldd");
+    if (C == D && (epi.flags & kEpiOutI8))
+      return fail(DG_ERR_INVALID_ARG, "an int8 D cannot also be the FP16 C");
   } else {
     C = D;  // never read
     ldc = ldd;

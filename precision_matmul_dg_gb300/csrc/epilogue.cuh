@@ -34,6 +34,13 @@ __device__ __forceinline__ float gelu_erf(float t) {
   return t * (t >= 0.0f ? 1.0f - q : q);
 }
 
+// Output quantization (kOpQuantI8, the program's last op): x = a * t rounded
+// half to even and saturated to [-128, 127]; NaN gives 0.
+__device__ __forceinline__ int8_t quant_i8(float x) {
+  if (x != x) return 0;
+  return static_cast<int8_t>(__float2int_rn(fminf(fmaxf(x, -128.0f), 127.0f)));
+}
+
 // Epilogue ops of a program (dg_epilogue_op in dg.h), applied in order to
 // t = alpha * acc + beta * C: the post-processing steps the pages' epilogue
 // generator fuses into the GEMM (kwkr.cn/news/562171, section 2.2 third
@@ -67,7 +74,7 @@ __device__ __forceinline__ float epi_program(float t, float b, const Epi& e,
       case kOpGelu: t = gelu_erf(t); break;
       case kOpScale: t *= op.a; break;
       case kOpClamp: t = fminf(fmaxf(t, op.a), op.b); break;
-      default: break;
+      default: break;  // kOpQuantI8 is applied by the store (epi_store)
     }
   }
   return t;
@@ -82,6 +89,16 @@ __device__ __forceinline__ float epi_apply(float acc, float c, float b, const Ep
   t += b;
   if (e.flags & kEpiGelu) t = gelu_erf(t);
   return t;
+}
+
+// Stores t as element idx of D: FP16 (round to nearest even), or the int8
+// code of the program's closing quantization.
+__device__ __forceinline__ void epi_store(void* D, int64_t idx, float t, const Epi& e,
+                                          const EpiProgram& prog) {
+  if (e.flags & kEpiOutI8)
+    static_cast<int8_t*>(D)[idx] = quant_i8(prog.ops[e.n_ops - 1].a * t);
+  else
+    static_cast<__half*>(D)[idx] = __float2half_rn(t);
 }
 
 // The kernels' view of a call's scalars and epilogue.

@@ -661,7 +661,9 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   // reads C with plain loads.
   const int64_t vec = Out == kOutF16 ? 8 : 4;
   const bool c_tma = Out == kOutF16 && a.beta != 0.0f;
-  const bool staged = a.ldd % vec == 0 && (reinterpret_cast<uintptr_t>(a.D) & 15) == 0 &&
+  // An int8 D (output quantization) takes the direct path.
+  const bool staged = !(a.epi & kEpiOutI8) && a.ldd % vec == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.D) & 15) == 0 &&
                       (!c_tma || (a.ldc % vec == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0));
   CUtensorMap tc_map = ta, td_map = ta;  // copies of a map that the kernel does not use
   if (staged) {

@@ -97,7 +97,8 @@ __device__ __forceinline__ void write_out(const GemvParams& p, const GemvOut& o,
   const float c = (p.epi.beta != 0.0f) ? __half2float(o.C[static_cast<int64_t>(m) * p.ldc + j])
                                         : 0.0f;
   const float b = (p.epi.flags & kEpiBias) ? __half2float(o.bias[j]) : 0.0f;
-  o.D[static_cast<int64_t>(m) * p.ldd + j] = __float2half_rn(epi_apply(acc, c, b, p.epi, prog));
+  epi_store(o.D, static_cast<int64_t>(m) * p.ldd + j, epi_apply(acc, c, b, p.epi, prog), p.epi,
+            prog);
 }
 
 template <int MROWS>
@@ -240,7 +241,7 @@ __global__ void epilogue_only_kernel(int64_t M, int64_t N, const __half* C, int6
     const int64_t m = i / N, j = i - m * N;
     const float c = (epi.beta != 0.0f) ? __half2float(C[m * ldc + j]) : 0.0f;
     const float b = (epi.flags & kEpiBias) ? __half2float(bias[j]) : 0.0f;
-    D[m * ldd + j] = __float2half_rn(epi_apply(0.0f, c, b, epi, prog));
+    epi_store(D, m * ldd + j, epi_apply(0.0f, c, b, epi, prog), epi, prog);
   }
 }
 

@@ -13,7 +13,8 @@
 namespace dg {
 
 // Epilogue flags as the kernels see them.
-enum : int { kEpiBias = 1, kEpiGelu = 2, kEpiProgram = 4 };
+// kEpiOutI8: the program ends in an int8 quantization and D is int8.
+enum : int { kEpiBias = 1, kEpiGelu = 2, kEpiProgram = 4, kEpiOutI8 = 8 };
 
 // Epilogue-program ops (dg_epilogue_op of dg.h).
 using EpiOp = dg_epilogue_op;
@@ -23,7 +24,8 @@ enum : int {
   kOpRelu = DG_OP_RELU,
   kOpGelu = DG_OP_GELU,
   kOpScale = DG_OP_SCALE,
-  kOpClamp = DG_OP_CLAMP
+  kOpClamp = DG_OP_CLAMP,
+  kOpQuantI8 = DG_OP_QUANT_I8
 };
 
 // Launches `kern` with programmatic stream serialization: its CTAs may be

@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(kSkThreads)
       const float c =
           p.epi.beta != 0.0f ? __half2float(p.C[static_cast<int64_t>(m) * p.ldc + nn]) : 0.0f;
       const float b = (p.epi.flags & kEpiBias) ? __half2float(p.bias[nn]) : 0.0f;
-      p.D[static_cast<int64_t>(m) * p.ldd + nn] =
-          __float2half_rn(epi_apply(acc[2 * h + e], c, b, p.epi, prog));
+      const float t = epi_apply(acc[2 * h + e], c, b, p.epi, prog);
+      epi_store(p.D, static_cast<int64_t>(m) * p.ldd + nn, t, p.epi, prog);
     }
   }
 }

@@ -83,7 +83,7 @@ __device__ __forceinline__ void apply_program_chunk(float (&v)[32], const __half
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = fminf(fmaxf(v[i], op.a), op.b);
         break;
-      default:
+      default:  // kOpQuantI8: applied by the store
         break;
     }
   }
@@ -106,6 +106,29 @@ __device__ __forceinline__ void store_f16_32(const float (&v)[32], __half* drow,
       for (int i = 0; i < 8; ++i)
         if (col0 + q * 8 + i < N) drow[col0 + q * 8 + i] = __float2half_rn(v[q * 8 + i]);
     }
+  }
+}
+
+// int8 codes of 32 values (the program's closing quantization by `scale`),
+// stored at qrow + col0 for the columns < N (two 16-byte stores when `full`).
+__device__ __forceinline__ void store_i8_32(const float (&v)[32], int8_t* qrow, int col0, int N,
+                                           float scale, bool full) {
+  if (full) {
+    uint32_t w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      w[q] = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        w[q] |= static_cast<uint32_t>(static_cast<uint8_t>(quant_i8(scale * v[q * 4 + b])))
+                << (8 * b);
+    }
+    reinterpret_cast<uint4*>(qrow + col0)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(qrow + col0)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < N) qrow[col0 + i] = quant_i8(scale * v[i]);
   }
 }
 
@@ -150,6 +173,13 @@ __device__ __forceinline__ void epilogue_f16_chunk(const uint32_t (&r)[32], int 
   }
   if (epi.flags & kEpiProgram) {
     apply_program_chunk(v, bias, col0, N, epi, prog);
+    if (epi.flags & kEpiOutI8) {  // D is int8: ldd counts bytes
+      int8_t* qrow = reinterpret_cast<int8_t*>(d) + static_cast<int64_t>(row) * ldd;
+      const bool full8 = in_range && ((ldd & 15) == 0) &&
+                         ((reinterpret_cast<uintptr_t>(d) & 15) == 0);
+      store_i8_32(v, qrow, col0, N, prog.ops[epi.n_ops - 1].a, full8);
+      return;
+    }
     store_f16_32(v, drow, col0, N, full);
     return;
   }

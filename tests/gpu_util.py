@@ -49,9 +49,13 @@ def run_case_ex(dg, case, ldc=None, ldd=None, inplace=False, stream=None):
     B = torch.from_numpy(np.ascontiguousarray(case.B)).to(dev)
     out_dtype = torch.int32 if case.dtype_a == "i8" else torch.float16
     fill = 12345 if out_dtype == torch.int32 else -7.5
+    last = (case.program or [None])[-1]
+    quant = isinstance(last, tuple) and last[0] == "quant_i8"
     ldd = ldd or N
-    Dbuf = torch.full((M, ldd), fill, dtype=out_dtype, device=dev)
+    Dbuf = torch.full((M, ldd), 77 if quant else fill, dtype=torch.int8 if quant else out_dtype,
+                      device=dev)
     D = Dbuf[:, :N]
+    fill_d = 77 if quant else fill
     Cbuf = C = None
     if case.C is not None:
         if inplace:
@@ -67,7 +71,7 @@ def run_case_ex(dg, case, ldc=None, ldd=None, inplace=False, stream=None):
                program=case.program or [], dtype_b=case.dtype_b, stream=stream)
     dg.check_status(stream)
     host = Dbuf.cpu().numpy()
-    assert np.all(host[:, N:] == np.array(fill, dtype=host.dtype)), "D padding was written"
+    assert np.all(host[:, N:] == np.array(fill_d, dtype=host.dtype)), "D padding was written"
     if Cbuf is not None:
         assert np.array_equal(Cbuf.cpu().numpy().view(np.uint8), c_before.view(np.uint8)), \
             "C was modified"

@@ -171,6 +171,9 @@ def _nine_ops(dg):
     (dict(program=[(0, 0.0, 0.0)]), "DG_ERR_INVALID_ARG"),
     (dict(program="nine"), "DG_ERR_INVALID_ARG"),          # n_ops above the maximum
     (dict(dtype_a="i8", dtype_b="i8", program=["relu"]), "DG_ERR_UNSUPPORTED"),
+    (dict(program=[("quant_i8", 1.0), "relu"]), "DG_ERR_INVALID_ARG"),   # quantization not last
+    (dict(program=[("quant_i8", float("inf"))]), "DG_ERR_INVALID_ARG"),
+    (dict(C=0x50000, ldc=72, program=[("quant_i8", 1.0)]), "DG_ERR_INVALID_ARG"),  # int8 D is C
 ])
 def test_gemm_ex_invalid_arguments_rejected(dg, over, status):
     if over.get("program") == "nine":

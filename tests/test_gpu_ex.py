@@ -118,6 +118,40 @@ def test_program_extremes(dg):
     assert (got == 0).mean() > 0.3 and (got == np.float16(2000.0)).mean() > 0.05
 
 
+QUANT_PROGRAMS = {
+    "quant": [("quant_i8", 40.0)],
+    "bias_gelu_quant": ["bias", "gelu", ("quant_i8", 60.0)],
+    "relu_clamp_quant": ["relu", ("clamp", 0.0, 1.5), ("quant_i8", 84.6)],
+    "saturating": [("scale", 7.0), ("quant_i8", 100.0)],
+}
+
+
+@pytest.mark.parametrize("fam", FAMILIES, ids=lambda f: f[2])
+@pytest.mark.parametrize("prog", sorted(QUANT_PROGRAMS))
+def test_int8_output_every_family(dg, fam, prog):
+    # int8 D (program ending in a quantization): codes within |a| E + 1 of
+    # the oracle's, where E bounds the error of t; D padding untouched
+    dtypes, shape, _ = fam
+    case = _case(dtypes, shape, QUANT_PROGRAMS[prog], 0.5, hash((shape, prog)) % 997)
+    N = case.N
+    layout = dict(ldc=N + 8, ldd=N + 16) if "bias" in prog else dict(ldc=N, ldd=N + 5)
+    got = run_case_ex(dg, case, **layout)
+    assert got.dtype == np.int8
+    assert_parity(case, got.astype(np.float64), _rows(case))
+    if prog == "saturating":
+        assert (got == 127).any() and (got == -128).any()
+
+
+def test_int8_output_rejects_in_place(dg):
+    case = _case(("f16", "f16"), (64, 128, 64), [("quant_i8", 1.0)], 0.5, 3)
+    A = torch.from_numpy(case.A).cuda()
+    B = torch.from_numpy(case.B).cuda()
+    C = torch.from_numpy(case.C).cuda()
+    with pytest.raises(dg.DgError):
+        dg.gemm_ex_raw(64, 128, 64, "f16", "f16", A, case.lda, B, case.ldb, C, 128, C, 128, None,
+                       1.0, 0.5, program=[("quant_i8", 1.0)])
+
+
 def test_fixed_epilogue_equals_program(dg):
     # dg_gemm's bias+GELU form and the program ["bias", "gelu"] are the same
     # function: both must meet the oracle on the same inputs
