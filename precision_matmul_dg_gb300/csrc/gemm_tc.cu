@@ -770,6 +770,9 @@ cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
     // 224 columns: 19 column tiles cover N = 4096 (the last one partly), so a
     // 4096^2 output is 16 x 19 = 304 pair tiles, four whole waves of 76 pairs
     if (plan.n_tile == 224 && plan.stages == 6) return run_tc<224, 6, 2, kOutF16>(a, plan);
+    // 192 columns: N = 8960 is 47 column tiles, so M = 2048 gives 376 pair
+    // tiles, 4.95 waves of 76 pairs (256 columns: 280 tiles, 3.68 waves)
+    if (plan.n_tile == 192 && plan.stages == 6) return run_tc<192, 6, 2, kOutF16>(a, plan);
     if (plan.n_tile == 128 && plan.stages == 8) return run_tc<128, 8, 2, kOutF16>(a, plan);
     return cudaErrorNotSupported;
   }

@@ -39,8 +39,9 @@ struct TcVariant {
   int n_tile, stages, cta_group, cv_stages;
 };
 constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1, 0}, {128, 6, 1, 0}, {64, 8, 1, 0},
-                                        {256, 6, 2, 0}, {224, 6, 2, 0}, {128, 8, 2, 0}};
-constexpr int kNumTcVariantsF16 = 6;
+                                        {256, 6, 2, 0}, {224, 6, 2, 0}, {192, 6, 2, 0},
+                                        {128, 8, 2, 0}};
+constexpr int kNumTcVariantsF16 = 7;
 constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
 // FP16 kernel in its exact-INT32 mode (two FP32 chunk accumulators in TMEM,
 // running INT32 sums in registers: N_tile a multiple of 64, at most 192)

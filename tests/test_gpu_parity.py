@@ -69,7 +69,7 @@ def test_every_tensor_core_plan(dg):
     case = workloads.random_case(520, 1100, 700, epilogue="bias_gelu", alpha=1.5, beta=0.25,
                                  seed=5)
     tc = [p for p in _plans(dg, case) if p["kernel_name"] == "tc"]
-    assert {p["n_tile"] for p in tc} == {64, 128, 224, 256}
+    assert {p["n_tile"] for p in tc} == {64, 128, 192, 224, 256}
     for p in tc:
         for grid in (p["grid"], 7, 1):   # persistent CTAs walking several tiles each
             q = dict(p, grid=grid)

@@ -22,7 +22,8 @@ GB300 = dict(sm_count=152, cc_major=10, cc_minor=3, smem_per_block_optin=232448,
 
 # Compiled FP16 tensor-core variants: (N_tile, stages, CTAs per tile); M_tile
 # 128 per CTA, K_tile 64, 384 threads.  A CTA pair holds half of B per CTA.
-TC_VARIANTS = [(256, 4, 1), (128, 6, 1), (64, 8, 1), (256, 6, 2), (224, 6, 2), (128, 8, 2)]
+TC_VARIANTS = [(256, 4, 1), (128, 6, 1), (64, 8, 1), (256, 6, 2), (224, 6, 2), (192, 6, 2),
+               (128, 8, 2)]
 # The output passes through two 2 KB staging boxes per epilogue warp (8 warps)
 EPI_STAGING = 8 * 2 * 32 * 32 * 2
 
