@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBlockM;
         const int b_row = n_blk * BN + static_cast<int>(rank) * L::kRowsB;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (aborted(abort_flag) ||
-              !mbar_wait(&empty_bar[stage], phase ^ 1, p.timeout_ns, p.status)) {
+          if (!mbar_wait_abortable(&empty_bar[stage], phase ^ 1, p.timeout_ns, p.status,
+                                   abort_flag)) {
             ok = false;
             break;
           }
@@ -298,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       for (int t = unit0; t < p.num_tiles && ok; t += units) {
         for (int ch = 0; ch < num_chunks && ok; ++ch) {
-          if (aborted(abort_flag) ||
-              !mbar_wait(&tmem_empty[acc], acc_phase ^ 1, p.timeout_ns, p.status)) {
+          if (!mbar_wait_abortable(&tmem_empty[acc], acc_phase ^ 1, p.timeout_ns, p.status,
+                                   abort_flag)) {
             ok = false;
             break;
           }
@@ -308,17 +308,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb0 = ch * chunk_kb;
           const int kb1 = min(p.num_k_blocks, kb0 + chunk_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (aborted(abort_flag) ||
-                !mbar_wait(&full_bar[stage], phase, p.timeout_ns, p.status)) {
+            if (!mbar_wait_abortable(&full_bar[stage], phase, p.timeout_ns, p.status,
+                                     abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
-            const uint32_t a0 = smem_addr(smem_a + stage * kTileBytesA);
-            const uint32_t b0 = smem_addr(smem_b + stage * L::kTileBytesB);
+            // K step k of the stage starts 32 bytes further into the swizzled
+            // rows: +2 in the descriptor's 16-byte address field
+            const uint64_t da0 = smem_desc_sw128(smem_addr(smem_a + stage * kTileBytesA));
+            const uint64_t db0 = smem_desc_sw128(smem_addr(smem_b + stage * L::kTileBytesB));
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
-              const uint64_t da = smem_desc_sw128(a0 + k * 32), db = smem_desc_sw128(b0 + k * 32);
+              const uint64_t da = da0 + 2 * k, db = db0 + 2 * k;
               const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
               if (CG == 2)
                 tc_mma_f16_pair(d_tmem, da, db, kIdesc, accum);

@@ -87,6 +87,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// As mbar_wait, and gives up (false) once *abort is set.  The flag is read
+// only while the phase is still incomplete, so a pipeline whose barriers are
+// ready pays nothing for it.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity,
+                                                    uint64_t timeout_ns, int* status,
+                                                    volatile int* abort) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      if (status) atomicExch(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // As mbar_wait, for waits expected to last long (a whole main loop): between
 // polls the thread sleeps `sleep_ns`, leaving issue slots to working warps.
 __device__ __forceinline__ bool mbar_wait_sleepy(uint64_t* bar, uint32_t parity,
