@@ -46,3 +46,21 @@ def test_gelu_form_matches_erf_gelu():
     form = t * np.where(t >= 0, 1.0 - q, q)
     exact = 0.5 * t * (1.0 + scipy_special.erf(t / np.sqrt(2.0)))
     assert np.allclose(form, exact, rtol=1e-12, atol=1e-15)
+
+
+def test_folded_form_is_the_same_function():
+    # The kernel folds 1/sqrt 2 into p, 1/2 into a1..a5 and evaluates
+    # exp(-z^2) as 2^(-t^2 log2(e) / 2): in float64 this is the same value.
+    c = kernel_constants()
+    t = np.linspace(-12.0, 12.0, 48001)
+    z = np.abs(t) / np.sqrt(2.0)
+    s = 1.0 / (1.0 + c["p"] * z)
+    poly = ((((c["a5"] * s + c["a4"]) * s + c["a3"]) * s + c["a2"]) * s + c["a1"]) * s
+    q = 0.5 * poly * np.exp(-z * z)
+    kp, ke = c["p"] * 0.70710678118654752, -0.72134752044448170
+    s2 = 1.0 / (1.0 + kp * np.abs(t))
+    half_poly = ((((0.5 * c["a5"] * s2 + 0.5 * c["a4"]) * s2 + 0.5 * c["a3"]) * s2
+                  + 0.5 * c["a2"]) * s2 + 0.5 * c["a1"]) * s2
+    q2 = half_poly * np.exp2(t * t * ke)
+    assert np.allclose(q2, q, rtol=1e-13, atol=1e-300)
+    assert abs(ke + np.log2(np.e) / 2) < 1e-16
