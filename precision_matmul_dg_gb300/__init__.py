@@ -213,6 +213,18 @@ def _expect(t, kinds, what):
         raise ValueError("%s must be 2-D with unit column stride" % what)
 
 
+_TD = None  # (torch, B dtype -> code, code -> torch dtype), built on first use
+
+
+def _td():
+    global _TD
+    if _TD is None:
+        import torch
+        _TD = (torch, {torch.float16: F16, torch.int8: I8, torch.uint8: E2M1},
+               (torch.float16, torch.int8, torch.uint8))
+    return _TD
+
+
 def gemm(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none", dtype_b=None,
          stream=None, plan=None):
     """D = epilogue(alpha * A.B + beta * C), written into C.
@@ -220,26 +232,36 @@ def gemm(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none", dtype
     A: [M, lda] (fp16 or int8); B: [N, ldb] (fp16/int8) or [N, ldb/2] uint8
     packed E2M1 codes; C: [M, N] fp16 (int32 for int8); K defaults to
     A.shape[1]; bias: [N] fp16.  The leading dimensions are the row strides.
+    (Written for a short host path: small GEMMs are bound by it.)
     """
-    import torch
-    dtype_a = "i8" if A.dtype == torch.int8 else "f16"
-    if dtype_b is None:
-        dtype_b = {torch.float16: "f16", torch.int8: "i8", torch.uint8: "e2m1"}[B.dtype]
-    _expect(A, dtype_a, "A")
-    _expect(B, dtype_b, "B")
-    _expect(C, "i32" if dtype_a == "i8" else "f16", "C")
+    torch, b_code, code_dt = _TD or _td()
+    da = I8 if A.dtype is torch.int8 else F16
+    db = b_code[B.dtype] if dtype_b is None else _dtype_code(dtype_b)
+    sa, sb, sc = A.stride(), B.stride(), C.stride()
+    names = ("f16", "i8", "e2m1")
+    if A.dtype is not code_dt[da] or len(sa) != 2 or sa[1] != 1:
+        _expect(A, names[da], "A")
+    if B.dtype is not code_dt[db] or len(sb) != 2 or sb[1] != 1:
+        _expect(B, names[db], "B")
+    if C.dtype is not (torch.int32 if da == I8 else torch.float16) or len(sc) != 2 or sc[1] != 1:
+        _expect(C, "i32" if da == I8 else "f16", "C")
     M, N = C.shape
     if A.shape[0] != M or B.shape[0] != N:
         raise ValueError("shape mismatch: A %s, B %s, C %s" % (tuple(A.shape), tuple(B.shape),
                                                                tuple(C.shape)))
-    if C.stride(0) != N:
+    if sc[0] != N:
         raise ValueError("C must be dense row-major (leading dimension N)")
     if K is None:
         K = A.shape[1]
-    lda = A.stride(0)
-    ldb = B.stride(0) * (2 if dtype_b == "e2m1" else 1)
-    gemm_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, epilogue,
-             stream=stream, plan=plan)
+    ldb = sb[0] * (2 if db == E2M1 else 1)
+    if plan is not None:
+        gemm_raw(M, N, K, da, db, A, sa[0], B, ldb, C, bias, alpha, beta, epilogue,
+                 stream=stream, plan=plan)
+        return C
+    s = _stream_handle(stream)
+    _check(lib().dg_gemm(M, N, K, da, db, A.data_ptr(), sa[0], B.data_ptr(), ldb, C.data_ptr(),
+                         None if bias is None else bias.data_ptr(), alpha, beta,
+                         EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue), s))
     return C
 
 
