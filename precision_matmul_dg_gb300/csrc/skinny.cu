@@ -50,6 +50,8 @@ constexpr int kSkChunk = 2 * kSkBatch * kSkWindow;  // K codes per activation ch
 constexpr int kSkRowPad = 8;     // halves of padding per activation row
 constexpr int kSkStride = kSkChunk + kSkRowPad;
 constexpr int kSkSmemA = 16 * kSkStride * 2;
+constexpr int kSkAPer = 16 * (kSkChunk / 8) / kSkThreads;  // 16-byte pieces per thread
+static_assert(kSkAPer * kSkThreads == 16 * (kSkChunk / 8), "whole pieces per thread");
 constexpr int kSkSmemRed = kSkGroups * 32 * 4 * 4;
 constexpr int kSkSmem = kSkSmemA + kSkSmemRed;
 
@@ -126,22 +128,34 @@ __global__ void __launch_bounds__(kSkThreads)
       bl[i][0] = in ? ld_stream16(brow0 + static_cast<int64_t>(g) * 16) : make_uint4(0u, 0u, 0u, 0u);
       bl[i][1] = in ? ld_stream16(brow1 + static_cast<int64_t>(g) * 16) : make_uint4(0u, 0u, 0u, 0u);
     }
-    // activation chunk -> shared memory; rows >= M and columns >= K are zero
+    // activation chunk -> shared memory; rows >= M and columns >= K are zero.
+    // A thread's kSkAPer 16-byte pieces are all loaded before any is stored,
+    // so the chunk costs one round trip to L2 rather than one per piece.
     __syncthreads();  // the previous chunk's reads are done
-    for (int idx = threadIdx.x; idx < 16 * (kSkChunk / 8); idx += kSkThreads) {
-      const int r = idx / (kSkChunk / 8), u = idx % (kSkChunk / 8);
-      const int k = kc0 + u * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (r < p.M && k < p.K) {
-        v = *reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(r) * p.lda + k);
-        if (k + 8 > p.K) {
-          __half* h = reinterpret_cast<__half*>(&v);
+    {
+      uint4 v[kSkAPer];
+#pragma unroll
+      for (int i = 0; i < kSkAPer; ++i) {
+        const int idx = threadIdx.x + i * kSkThreads;
+        const int r = idx / (kSkChunk / 8), u = idx % (kSkChunk / 8);
+        const int k = kc0 + u * 8;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.M && k < p.K)
+          v[i] = __ldg(reinterpret_cast<const uint4*>(p.A + static_cast<int64_t>(r) * p.lda + k));
+      }
+#pragma unroll
+      for (int i = 0; i < kSkAPer; ++i) {
+        const int idx = threadIdx.x + i * kSkThreads;
+        const int r = idx / (kSkChunk / 8), u = idx % (kSkChunk / 8);
+        const int k = kc0 + u * 8;
+        if (k < p.K && k + 8 > p.K) {
+          __half* h = reinterpret_cast<__half*>(&v[i]);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             if (k + e >= p.K) h[e] = __ushort_as_half(0);
         }
+        *reinterpret_cast<uint4*>(As + r * kSkStride + u * 8) = v[i];
       }
-      *reinterpret_cast<uint4*>(As + r * kSkStride + u * 8) = v;
     }
     __syncthreads();
     // lane (grp, tig) takes, for window h of a pair, piece 4h + tig of row
