@@ -259,6 +259,28 @@ dg_status dg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K
                                   int64_t stride_bias, float alpha, float beta,
                                   dg_epilogue epilogue, dg_stream_t stream);
 
+/* A group of independent problems that share N, K, the dtypes, scalars and
+ * epilogue but not M or their buffers, e.g. the experts of a mixture-of-
+ * experts layer, each with the rows routed to it (a grouped form of the many
+ * small GEMMs of discosf.com/news/5532976, section 5.3, third stage):
+ *   D_g = epilogue(alpha * A_g.B_g + beta * C_g),  g = 0 .. count-1.
+ *   Ms, A, B, C and bias are HOST arrays of count entries: row counts (0
+ *   skips the problem) and device pointers in dg_gemm's layouts (lda, ldb
+ *   shared; C_g / D_g leading dimension N).  bias may be NULL without a bias
+ *   epilogue; entries of a problem with M = 0 are not read.
+ *   FP16 x FP16 groups whose largest M is at most 16 run as ONE launch of the
+ *   warp-MMA GEMV: a table of the problems is copied (cudaMemcpyAsync from
+ *   pageable memory, so not under CUDA-graph capture) to a per-(device,
+ *   stream) workspace, with the split-K workspace sized for the group.  Other
+ *   groups launch each problem in turn on `stream`.
+ * Errors: as dg_gemm for each problem (the message names the problem), plus
+ * DG_ERR_INVALID_ARG for a negative count or M or a NULL array. */
+dg_status dg_gemm_grouped(int64_t count, const int64_t *Ms, int64_t N, int64_t K,
+                          dg_dtype dtype_a, dg_dtype dtype_b, const void *const *A, int64_t lda,
+                          const void *const *B, int64_t ldb, void *const *C,
+                          const void *const *bias, float alpha, float beta,
+                          dg_epilogue epilogue, dg_stream_t stream);
+
 /* As dg_gemm, but runs `plan` (one returned by dg_plan_tiles for the same
  * M, N, K and dtypes).  DG_ERR_INVALID_STATE when the plan does not fit. */
 dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,

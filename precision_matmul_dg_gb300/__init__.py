@@ -12,7 +12,7 @@ import os
 
 __all__ = [
     "DgError", "F16", "I8", "E2M1", "EPILOGUES", "lib", "lib_path", "gemm", "gemm_raw",
-    "gemm_host", "gemm_host_raw", "gemm_ex", "gemm_ex_raw", "gemm_batched",
+    "gemm_host", "gemm_host_raw", "gemm_ex", "gemm_ex_raw", "gemm_batched", "gemm_grouped",
     "gemm_strided_batched_raw", "OPS", "MAX_EPILOGUE_OPS",
     "EpilogueOp", "EpilogueProgram", "make_program",
     "plan_tiles", "query_hw", "last_error", "check_status", "set_wait_timeout_ns",
@@ -31,7 +31,7 @@ KERNELS = {0: "tc", 1: "gemv", 2: "tc_widened", 3: "skinny", 4: "gemv_mma", -1: 
 
 # Every symbol include/dg.h declares.
 EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_gemm_host",
-           "dg_gemm_ex", "dg_gemm_strided_batched",
+           "dg_gemm_ex", "dg_gemm_strided_batched", "dg_gemm_grouped",
            "dg_gemm_thin_noalloc", "dg_last_error",
            "dg_check_status", "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout",
            "dg_launch_count", "dg_shutdown"]
@@ -127,6 +127,9 @@ def lib():
                                i32, vp]
     L.dg_gemm_strided_batched.argtypes = [i64, i64, i64, i64, i32, i32, vp, i64, i64, vp, i64,
                                           i64, vp, i64, vp, i64, f32, f32, i32, vp]
+    L.dg_gemm_grouped.argtypes = [i64, ctypes.POINTER(ctypes.c_int64), i64, i64, i32, i32,
+                                  ctypes.POINTER(vp), i64, ctypes.POINTER(vp), i64,
+                                  ctypes.POINTER(vp), ctypes.POINTER(vp), f32, f32, i32, vp]
     L.dg_gemm_ex.argtypes = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, f32,
                              f32, ctypes.POINTER(EpilogueProgram), vp]
     L.dg_last_error.restype = ctypes.c_char_p
@@ -138,7 +141,8 @@ def lib():
     L.dg_launch_count.argtypes = []
     L.dg_shutdown.argtypes = []
     for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
-                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_gemm_ex", "dg_gemm_strided_batched", "dg_check_status",
+                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_gemm_ex", "dg_gemm_strided_batched", "dg_gemm_grouped",
+                 "dg_check_status",
                  "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout", "dg_shutdown"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -365,6 +369,55 @@ def gemm_batched(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none
                              ldb, stride_b, C, C.stride(0), bias, stride_bias, alpha, beta,
                              epilogue, stream=stream)
     return C
+
+
+def gemm_grouped(As, Bs, Cs, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none",
+                 stream=None):
+    """D_g = epilogue(alpha * A_g.B_g + beta * C_g) for every g, written into Cs[g].
+
+    As: list of [M_g, lda] tensors (one lda, M_g may differ, 0 skips); Bs: a
+    list of [N, ldb] tensors or one tensor shared by all; Cs: list of [M_g, N]
+    dense tensors; bias: None, one [N] tensor or a list.  All problems share
+    N, K, the dtypes, scalars and epilogue.
+    """
+    import torch
+    count = len(As)
+    if not isinstance(Bs, (list, tuple)):
+        Bs = [Bs] * count
+    if bias is not None and not isinstance(bias, (list, tuple)):
+        bias = [bias] * count
+    if len(Bs) != count or len(Cs) != count or (bias is not None and len(bias) != count):
+        raise ValueError("As, Bs, Cs (and bias) must have one entry per problem")
+    if count == 0:
+        return Cs
+    A0, B0 = As[0], Bs[0]
+    dtype_a = "i8" if A0.dtype == torch.int8 else "f16"
+    dtype_b = {torch.float16: "f16", torch.int8: "i8", torch.uint8: "e2m1"}[B0.dtype]
+    N = Cs[0].shape[1]
+    if K is None:
+        K = A0.shape[1]
+    lda = A0.stride(0)
+    ldb = B0.stride(0) * (2 if dtype_b == "e2m1" else 1)
+    for g in range(count):
+        _expect(As[g], dtype_a, "A[%d]" % g)
+        _expect(Bs[g], dtype_b, "B[%d]" % g)
+        _expect(Cs[g], "i32" if dtype_a == "i8" else "f16", "C[%d]" % g)
+        if As[g].stride(0) != lda or Bs[g].stride(0) * (2 if dtype_b == "e2m1" else 1) != ldb:
+            raise ValueError("every problem must share lda and ldb")
+        if Cs[g].shape[1] != N or Cs[g].shape[0] != As[g].shape[0] or Bs[g].shape[0] != N or \
+                (Cs[g].shape[0] and Cs[g].stride(0) != N):
+            raise ValueError("problem %d: shapes or C layout do not match" % g)
+    vp = ctypes.c_void_p
+    Ms = (ctypes.c_int64 * count)(*[int(a.shape[0]) for a in As])
+    pa = (vp * count)(*[a.data_ptr() for a in As])
+    pb = (vp * count)(*[b.data_ptr() for b in Bs])
+    pc = (vp * count)(*[c.data_ptr() for c in Cs])
+    pbias = None if bias is None else (vp * count)(*[b.data_ptr() for b in bias])
+    _check(lib().dg_gemm_grouped(count, Ms, int(N), int(K), _dtype_code(dtype_a),
+                                 _dtype_code(dtype_b), pa, int(lda), pb, int(ldb), pc, pbias,
+                                 float(alpha), float(beta), _epi_code(epilogue),
+                                 _stream_handle(stream)))
+    return Cs
 
 
 def gemm_host_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, D, bias, alpha, beta, epilogue,

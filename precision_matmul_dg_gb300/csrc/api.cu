@@ -11,11 +11,13 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
 #include <tuple>
+#include <vector>
 
 #include "dg.h"
 #include "internal.h"
@@ -54,6 +56,8 @@ struct Workspace {
   int64_t counter_elems = 0;
   __half* wide = nullptr;  // FP16 copies of widened int8 / E2M1 operands
   int64_t wide_elems = 0;
+  void* table = nullptr;   // problem descriptors of a grouped launch
+  int64_t table_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -274,6 +278,23 @@ dg_status get_workspace(int dev, cudaStream_t stream, int64_t partial_elems, int
   out->partial_elems = w.partial_elems;
   out->counters = w.counters;
   out->counter_elems = w.counter_elems;
+  return DG_OK;
+}
+
+// Device buffer of at least `bytes` for a grouped launch's problem table (per
+// device and stream).
+dg_status get_table_workspace(int dev, cudaStream_t stream, int64_t bytes, void** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+  if (w.table_bytes < bytes) {
+    if (w.table) cudaFree(w.table);  // synchronises the device: no kernel still reads it
+    w.table = nullptr;
+    w.table_bytes = 0;
+    const cudaError_t e = cudaMalloc(&w.table, bytes);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(group table)");
+    w.table_bytes = bytes;
+  }
+  *out = w.table;
   return DG_OK;
 }
 
@@ -718,6 +739,99 @@ dg_status dg_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K
              nullptr, reinterpret_cast<cudaStream_t>(stream), bs);
 }
 
+dg_status dg_gemm_grouped(int64_t count, const int64_t* Ms, int64_t N, int64_t K,
+                          dg_dtype dtype_a, dg_dtype dtype_b, const void* const* A, int64_t lda,
+                          const void* const* B, int64_t ldb, void* const* C,
+                          const void* const* bias, float alpha, float beta,
+                          dg_epilogue epilogue, dg_stream_t stream) {
+  clear_error();
+  EpiSpec epi;
+  dg_status s = fixed_epilogue(epilogue, &epi);
+  if (s != DG_OK) return s;
+  if (count < 0) return fail(DG_ERR_INVALID_ARG, "negative count");
+  if (count == 0) return DG_OK;
+  if (!Ms || !A || !B || !C)
+    return fail(DG_ERR_INVALID_ARG, "Ms, A, B and C must be host arrays of count entries");
+  if ((epi.flags & kEpiBias) && !bias)
+    return fail(DG_ERR_INVALID_ARG, "bias epilogue with a null bias array");
+  int64_t max_m = 0;
+  for (int64_t g = 0; g < count; ++g) {
+    if (Ms[g] < 0) return fail(DG_ERR_INVALID_ARG, "problem %lld: negative M", (long long)g);
+    max_m = std::max(max_m, Ms[g]);
+  }
+  for (int64_t g = 0; g < count; ++g) {
+    if (Ms[g] == 0) continue;
+    s = validate(Ms[g], N, K, dtype_a, dtype_b, A[g], lda, B[g], ldb, C[g],
+                 bias ? bias[g] : nullptr, alpha, beta, epi.flags);
+    if (s != DG_OK) {
+      std::string msg = g_last_error;
+      return fail(s, "problem %lld: %s", (long long)g, msg.c_str());
+    }
+  }
+  if (max_m == 0 || N == 0) return DG_OK;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool one_launch = dtype_a == DG_F16 && dtype_b == DG_F16 && max_m <= 16 && K > 0;
+  if (!one_launch) {  // each problem in turn, as dg_gemm
+    for (int64_t g = 0; g < count; ++g) {
+      if (Ms[g] == 0) continue;
+      s = run(Ms[g], N, K, dtype_a, dtype_b, A[g], lda, B[g], ldb, C[g], N, C[g], N,
+              bias ? bias[g] : nullptr, alpha, beta, epi, nullptr, st);
+      if (s != DG_OK) return s;
+    }
+    return DG_OK;
+  }
+  DeviceState* dst = nullptr;
+  s = device_state(&dst);
+  if (s != DG_OK) return s;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  // One launch of the warp-MMA GEMV over the group: split-K chosen for the
+  // whole group, problem descriptors in a device table.
+  dg_tile_plan plan{};
+  int64_t chunk = 0;
+  plan.kernel = DG_KERNEL_GEMV_MMA;
+  plan.split_k = gemv_mma_best_split(max_m, N, K, dst->hw, &chunk, count);
+  plan.k_tile = static_cast<int>(chunk);
+  SplitKWorkspace ws{nullptr, 0, nullptr, 0};
+  if (plan.split_k > 1) {
+    s = get_workspace(dev, st, static_cast<int64_t>(plan.split_k) * max_m * N * count,
+                      (N + 7) / 8 * count, &ws);
+    if (s != DG_OK) return s;
+  }
+  const int64_t entry = gemv_group_entry_bytes();
+  void* table = nullptr;
+  s = get_table_workspace(dev, st, entry * count, &table);
+  if (s != DG_OK) return s;
+  std::vector<unsigned char> host(static_cast<size_t>(entry * count));
+  for (int64_t g = 0; g < count; ++g)
+    gemv_group_entry(host.data(), g, A[g], B[g], C[g], bias ? bias[g] : nullptr, Ms[g]);
+  // From pageable memory the call returns once `host` has been staged; the
+  // copy runs in stream order, after the kernels that read the table before.
+  cudaError_t e = cudaMemcpyAsync(table, host.data(), host.size(), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return fail_cuda(e, "group table copy");
+  GemmArgs a{};
+  a.M = max_m;
+  a.N = N;
+  a.K = K;
+  a.dtype_a = dtype_a;
+  a.dtype_b = dtype_b;
+  a.lda = lda;
+  a.ldb = ldb;
+  a.ldc = N;
+  a.ldd = N;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.epi = epi.flags;
+  a.n_ops = 0;
+  a.batch = count;
+  a.stream = st;
+  a.status = dst->status;
+  a.timeout_ns = timeout_ns();
+  a.sm_count = dst->hw.sm_count;
+  e = launch_gemv_mma_grouped(a, table, count, max_m, plan, ws);
+  return e == cudaSuccess ? DG_OK : fail_cuda(e, "kernel launch");
+}
+
 dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
                           const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                           const void* bias, float alpha, float beta, dg_epilogue epilogue,
@@ -781,6 +895,7 @@ dg_status dg_shutdown(void) {
     if (kv.second.partial) cudaFree(kv.second.partial);
     if (kv.second.counters) cudaFree(kv.second.counters);
     if (kv.second.wide) cudaFree(kv.second.wide);
+    if (kv.second.table) cudaFree(kv.second.table);
   }
   g_workspaces.clear();
   for (auto& kv : g_host_ws) {

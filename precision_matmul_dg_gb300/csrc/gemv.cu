@@ -57,6 +57,18 @@ static_assert(sizeof(GemvParams) <= 128, "parameter struct within 128 bytes (see
 // and counters follow those of problem z - 1.
 struct GemvBatch {
   int64_t sa, sb, sc, sd, sbias;
+  const struct GemvGroupProblem* group;  // grouped launch: problem z is group[z] instead
+};
+
+// One problem of a grouped launch (dg_gemm_grouped): its rows and buffers
+// (C and D one buffer of leading dimension N).  The launch's p.M is the
+// largest M of the group, which sizes each problem's split-K partials.
+struct GemvGroupProblem {
+  const __half* A;
+  const __half* B;
+  __half* CD;
+  const __half* bias;
+  int64_t M;
 };
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -326,9 +338,14 @@ __global__ void __launch_bounds__(kMmaWarps * 32)
                     const GemvBatch bt) {
   grid_dependency_wait();  // launched as a dependent of the previous kernel
   const int64_t z = blockIdx.z;
-  const __half* A = p.A + z * bt.sa;
-  const __half* B = p.B + z * bt.sb;
-  const GemvOut out{p.C + z * bt.sc, p.D + z * bt.sd, p.bias ? p.bias + z * bt.sbias : nullptr};
+  const GemvGroupProblem* gp = bt.group ? bt.group + z : nullptr;
+  const int M = gp ? static_cast<int>(gp->M) : p.M;
+  if (M == 0) return;  // an empty problem of a group (the whole block)
+  const __half* A = gp ? gp->A : p.A + z * bt.sa;
+  const __half* B = gp ? gp->B : p.B + z * bt.sb;
+  const GemvOut out = gp ? GemvOut{gp->CD, gp->CD, gp->bias}
+                         : GemvOut{p.C + z * bt.sc, p.D + z * bt.sd,
+                                   p.bias ? p.bias + z * bt.sbias : nullptr};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -340,7 +357,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32)
   float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   // Lanes past the last column read row N - 1 (in bounds) and discard it.
   const __half* brow = B + static_cast<int64_t>(min(n0 + g, p.N - 1)) * p.ldb;
-  const bool has_a0 = g < p.M, has_a8 = MROWS == 16 && g + 8 < p.M;
+  const bool has_a0 = g < M, has_a8 = MROWS == 16 && g + 8 < M;
   const __half* arow0 = A + static_cast<int64_t>(has_a0 ? g : 0) * p.lda;
   const __half* arow8 = A + static_cast<int64_t>(has_a8 ? g + 8 : 0) * p.lda;
   const uint4 zero = make_uint4(0, 0, 0, 0);
@@ -390,20 +407,21 @@ __global__ void __launch_bounds__(kMmaWarps * 32)
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int e = 0; e < 2; ++e)
-        if (g + 8 * h < p.M && col + e < p.N)
+        if (g + 8 * h < M && col + e < p.N)
           write_out(p, out, prog, g + 8 * h, col + e, acc[2 * h + e]);
     return;
   }
 
   // Split-K: partials, then the last CTA of the column group reduces.
+  // problem z's partials: [split][M][N] inside a slot of split x p.M x N
   float* partial = p.partial + z * p.split_k * p.M * static_cast<int64_t>(p.N);
   unsigned* counters = p.counters + z * gridDim.x;
 #pragma unroll
   for (int h = 0; h < 2; ++h)
 #pragma unroll
     for (int e = 0; e < 2; ++e)
-      if (g + 8 * h < p.M && col + e < p.N)
-        partial[(static_cast<int64_t>(split) * p.M + g + 8 * h) * p.N + col + e] = acc[2 * h + e];
+      if (g + 8 * h < M && col + e < p.N)
+        partial[(static_cast<int64_t>(split) * M + g + 8 * h) * p.N + col + e] = acc[2 * h + e];
   __threadfence();
   __syncthreads();
   __shared__ unsigned s_is_last;
@@ -414,12 +432,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32)
   __syncthreads();
   if (!s_is_last) return;
   __threadfence();
-  for (int i = threadIdx.x; i < kMmaCols * p.M; i += blockDim.x) {
+  for (int i = threadIdx.x; i < kMmaCols * M; i += blockDim.x) {
     const int m = i / kMmaCols;
     const int jj = blockIdx.x * kMmaCols + (i % kMmaCols);
     if (jj >= p.N) continue;
     const float s = sum_splits(partial + static_cast<int64_t>(m) * p.N + jj,
-                               static_cast<int64_t>(p.M) * p.N, p.split_k);
+                               static_cast<int64_t>(M) * p.N, p.split_k);
     write_out(p, out, prog, m, jj, s);
   }
   if (threadIdx.x == 0) counters[blockIdx.x] = 0u;  // ready for the next launch
@@ -540,6 +558,51 @@ cudaError_t launch_gemv_mma(const GemmArgs& a, const dg_tile_plan& plan,
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_gemv_mma_grouped(const GemmArgs& a, const void* table, int64_t count,
+                                    int64_t max_m, const dg_tile_plan& plan,
+                                    const SplitKWorkspace& ws) {
+  if (max_m < 1 || max_m > 16 || count < 1) return cudaErrorInvalidValue;
+  GemvParams p{};
+  p.M = static_cast<int>(max_m);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.lda = a.lda;
+  p.ldb = a.ldb;
+  p.ldc = a.N;
+  p.ldd = a.N;
+  p.epi = make_epi(a);
+  p.split_k = plan.split_k;
+  p.k_chunk = plan.k_tile;
+  p.partial = ws.partial;
+  p.counters = ws.counters;
+  const unsigned gx = static_cast<unsigned>((a.N + kMmaCols - 1) / kMmaCols);
+  auto kern = max_m <= 8 ? gemv_mma_kernel<8> : gemv_mma_kernel<16>;
+  constexpr int64_t kMaxZ = 65535;
+  const auto* group = static_cast<const GemvGroupProblem*>(table);
+  for (int64_t z0 = 0; z0 < count; z0 += kMaxZ) {
+    const int64_t nz = std::min(kMaxZ, count - z0);
+    GemvParams q = p;
+    if (q.partial) q.partial += z0 * plan.split_k * max_m * a.N;
+    if (q.counters) q.counters += z0 * gx;
+    const GemvBatch bt{0, 0, 0, 0, 0, group + z0};
+    const dim3 grid(gx, static_cast<unsigned>(plan.split_k), static_cast<unsigned>(nz));
+    const cudaError_t e = launch_dependent(kern, grid, dim3(kMmaWarps * 32), 0, a.stream, q,
+                                           make_program(a), bt);
+    count_launches(1);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+int64_t gemv_group_entry_bytes() { return sizeof(GemvGroupProblem); }
+
+void gemv_group_entry(void* table, int64_t i, const void* A, const void* B, void* CD,
+                      const void* bias, int64_t M) {
+  static_cast<GemvGroupProblem*>(table)[i] =
+      GemvGroupProblem{static_cast<const __half*>(A), static_cast<const __half*>(B),
+                       static_cast<__half*>(CD), static_cast<const __half*>(bias), M};
 }
 
 cudaError_t launch_epilogue_only(const GemmArgs& a) {

@@ -102,6 +102,15 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
 // Warp-MMA GEMV (gemv.cu): F16 x F16 with M <= 16 on m16n8k16 tensor-core MMAs.
 cudaError_t launch_gemv_mma(const GemmArgs& a, const dg_tile_plan& plan,
                             const SplitKWorkspace& ws);
+// The same over a group of problems of one N and K (dg_gemm_grouped): `table`
+// is a device array of `count` entries written by gemv_group_entry, max_m the
+// largest M.  a.N, a.K, a.lda, a.ldb, the epilogue and the stream apply to all.
+cudaError_t launch_gemv_mma_grouped(const GemmArgs& a, const void* table, int64_t count,
+                                    int64_t max_m, const dg_tile_plan& plan,
+                                    const SplitKWorkspace& ws);
+int64_t gemv_group_entry_bytes();
+void gemv_group_entry(void* table, int64_t i, const void* A, const void* B, void* CD,
+                      const void* bias, int64_t M);
 // Skinny W4A16 kernel (skinny.cu): FP16 A with M <= 16 x packed E2M1 B.
 cudaError_t launch_skinny(const GemmArgs& a, const dg_tile_plan& plan);
 int skinny_smem_bytes();

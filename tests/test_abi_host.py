@@ -246,6 +246,35 @@ def test_batched_empty_is_a_noop(dg):
         assert _call_batched(dg, batch=1, sc=3, sa=1)[0] == "DG_ERR_INVALID_STATE"
 
 
+def _call_grouped(dg, Ms, A=0x10000, B=0x20000, C=0x30000, bias=None, N=128, K=256,
+                  epilogue=0, arrays=True, count=None):
+    import ctypes
+    n = len(Ms) if count is None else count
+    vp = ctypes.c_void_p
+    size = max(len(Ms), 1)
+    ms = (ctypes.c_int64 * size)(*Ms) if arrays else None
+    pa = (vp * size)(*[A] * len(Ms)) if arrays else None
+    pb = (vp * size)(*[B] * len(Ms)) if arrays else None
+    pc = (vp * size)(*[C] * len(Ms)) if arrays else None
+    pbias = None if bias is None else (vp * size)(*[bias] * len(Ms))
+    st = dg.lib().dg_gemm_grouped(n, ms, N, K, 0, 0, pa, 256, pb, 256, pc, pbias, 1.0, 0.0,
+                                  epilogue, None)
+    return st, dg.last_error()
+
+
+def test_grouped_invalid_arguments_rejected(dg):
+    assert _call_grouped(dg, [1, 2], count=-1)[0] == 1
+    assert _call_grouped(dg, [1, 2], arrays=False)[0] == 1
+    st, msg = _call_grouped(dg, [1, -3])
+    assert st == 1 and "negative M" in msg
+    st, msg = _call_grouped(dg, [1, 2], epilogue=1)     # bias epilogue, no bias array
+    assert st == 1 and "bias" in msg
+    st, msg = _call_grouped(dg, [4, 2], A=0x10008)      # misaligned A, reported per problem
+    assert st == 1 and msg.startswith("problem 0:")
+    assert _call_grouped(dg, [], count=0)[0] == 0
+    assert _call_grouped(dg, [0, 0])[0] == 0            # nothing to do
+
+
 def test_empty_problem_is_a_noop(dg):
     assert _call(dg, M=0)[0] == "DG_OK"
     assert _call(dg, N=0, A=None, B=None)[0] == "DG_OK"
