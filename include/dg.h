@@ -28,6 +28,12 @@
  *  - A and B must be 16-byte aligned and lda/ldb must span a multiple of 16
  *    bytes (the tensor-memory-access engine reads them in tiles); C must be
  *    16-byte aligned; bias 2-byte aligned.
+ *  - Any host thread may call.  The library's own state (device
+ *    descriptors, cached plans, scratch buffers kept per device and stream,
+ *    one-time kernel set-up) is guarded internally, so calls on different
+ *    streams from different threads are independent.  Calls on one stream
+ *    must not overlap on the host: a call may grow that stream's scratch
+ *    and free the buffer another call is about to launch with.
  *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *    Invalid arguments are rejected synchronously, before any launch, with a
  *    status and a message in dg_last_error().  Faults in a launched kernel

@@ -464,12 +464,12 @@ cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
   auto kern = gemm_conv_tc_kernel<BN, SIn, SCv, OpA, OpB, Out>;
   int dev = 0;
   cudaGetDevice(&dev);
-  static uint64_t attr_set = 0;  // one shared-memory opt-in per variant and device
-  if (!(attr_set & (1ull << (dev & 63)))) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kLaunchBytes);
-    if (e != cudaSuccess) return e;
-    attr_set |= 1ull << (dev & 63);
-  }
+  static std::atomic<uint64_t> attr_set{0};  // one shared-memory opt-in per variant and device
+  e = once_per_device(attr_set, dev, [&]() {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                L::kLaunchBytes);
+  });
+  if (e != cudaSuccess) return e;
   int grid = plan.grid > 0 ? plan.grid : a.sm_count;
   if (grid > p.num_tiles) grid = p.num_tiles;
   e = launch_dependent(kern, dim3(grid), dim3(kThreads), L::kLaunchBytes, a.stream, ta, tb, p,

@@ -704,9 +704,8 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   int dev = 0;
   cudaGetDevice(&dev);
   // One shared-memory opt-in and one co-residency query per variant and device.
-  static uint64_t attr_set = 0;
+  static std::atomic<uint64_t> attr_set{0};
   static int max_pairs[64] = {};
-  const uint64_t bit = 1ull << (dev & 63);
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L::kLaunchBytes;
@@ -722,9 +721,10 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  if (!(attr_set & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kLaunchBytes);
-    if (e != cudaSuccess) return e;
+  e = once_per_device(attr_set, dev, [&]() {
+    cudaError_t r =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kLaunchBytes);
+    if (r != cudaSuccess) return r;
     if (CG == 2) {
       // Pairs that fit at once: a persistent grid must not exceed it.
       int n = 0;
@@ -735,8 +735,9 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
       }
       max_pairs[dev & 63] = n;
     }
-    attr_set |= bit;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   // grid: CTAs (pairs x 2 when CG == 2), never more units than tiles
   int units = plan.grid > 0 ? plan.grid / CG : a.sm_count / CG;
   if (CG == 2 && units > max_pairs[dev & 63]) units = max_pairs[dev & 63];

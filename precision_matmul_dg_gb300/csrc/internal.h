@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
 #include <string>
 #include <utility>
 
@@ -47,6 +49,23 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// One-time set-up of a kernel on a device (shared-memory opt-in, occupancy
+// query), safe when several host threads make their first call at once:
+// `init` runs under a lock, at most once per device and flag word (retried
+// after a failure), and what it wrote is visible to every later caller that
+// finds the device's bit set.
+template <typename F>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, int dev, F&& init) {
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+  const cudaError_t e = init();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 // Everything a launcher needs to run one GEMM, already validated.

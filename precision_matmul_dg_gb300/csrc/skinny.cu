@@ -244,14 +244,12 @@ cudaError_t launch_skinny(const GemmArgs& a, const dg_tile_plan& plan) {
   p.epi = make_epi(a);
   int dev = 0;
   cudaGetDevice(&dev);
-  static uint64_t attr_set = 0;  // one shared-memory opt-in per device
-  if (!(attr_set & (1ull << (dev & 63)))) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(skinny_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSkSmem);
-    if (e != cudaSuccess) return e;
-    attr_set |= 1ull << (dev & 63);
-  }
+  static std::atomic<uint64_t> attr_set{0};  // one shared-memory opt-in per device
+  const cudaError_t ea = once_per_device(attr_set, dev, []() {
+    return cudaFuncSetAttribute(skinny_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSkSmem);
+  });
+  if (ea != cudaSuccess) return ea;
   const unsigned grid = static_cast<unsigned>((a.N + kSkCols - 1) / kSkCols);
   const cudaError_t e = launch_dependent(skinny_w4a16_kernel, dim3(grid), dim3(kSkThreads),
                                          kSkSmem, a.stream, p, make_program(a));
