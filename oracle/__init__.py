@@ -16,7 +16,12 @@ Sources (cited by page address and section):
     (epilogue generator: alpha * gemm_out + beta * ..., bias + GELU fused),
     section 3.2 step 3 (epilogue "alpha * C + beta * D").
 
-Parity status of each function is listed in ``oracle.gemm_ref.__doc__``.
+Block-scaled 4-bit operands (MXFP4: E2M1 codes with one E8M0 scale per 32
+values along K) and the GEMM on them are in ``oracle.mx_ref``; the pages fix
+no block format, and that module's docstring states the reading taken.
+
+Parity status of each function is listed in ``oracle.gemm_ref.__doc__`` and
+``oracle.mx_ref.__doc__``.
 """
 
 from .gemm_ref import (  # noqa: F401
@@ -31,4 +36,16 @@ from .gemm_ref import (  # noqa: F401
     quantize_i8,
     PROGRAM_OPS,
     GELU_LIPSCHITZ,
+)
+from .mx_ref import (  # noqa: F401
+    MX_BLOCK,
+    e8m0_value,
+    e8m0_decode,
+    e2m1_round,
+    shared_exponent,
+    mxfp4_quantize,
+    mxfp4_dequantize,
+    pack_e2m1,
+    gemm_mx_reference,
+    error_bound_mx,
 )

@@ -262,6 +262,16 @@ def gemm_reference(A, B, K, dtype_a="f16", dtype_b="f16", C=None, bias=None,
             t = t + np.uint64(int(beta) % mod) * c_u
         return _wrap_int32(t)
 
+    return fp_epilogue(acc, C, bias, alpha, beta, epilogue, program)
+
+
+def fp_epilogue(acc, C, bias, alpha, beta, epilogue, program):
+    """The floating-point epilogue on the exact products' sums acc (float64):
+    t = alpha*acc + beta*C, then the program, or bias and GELU."""
+    if epilogue not in _EPILOGUES:
+        raise ValueError("unknown epilogue %r" % (epilogue,))
+    if program and epilogue != "none":
+        raise ValueError("give an epilogue or a program, not both")
     t = float(alpha) * acc
     if beta != 0.0:
         if C is None:
@@ -308,14 +318,18 @@ def error_bound(A, B, K, D_ref, dtype_a="f16", dtype_b="f16", C=None, bias=None,
         A = A[rows]
         if C is not None:
             C = np.asarray(C)[rows]
-    a = np.abs(_operand_a(A[:, :K], dtype_a))
-    b = np.abs(_operand_b(B, dtype_b, K))
-    P = abs(float(alpha)) * (a @ b.T)
+    return fp_bound(_operand_a(A[:, :K], dtype_a), _operand_b(B, dtype_b, K), D_ref, C, bias,
+                    alpha, beta, epilogue, program)
+
+
+def fp_bound(a, b, D_ref, C, bias, alpha, beta, epilogue, program):
+    """error_bound's formula on decoded operands a [rows, K] and b [N, K]."""
+    P = abs(float(alpha)) * (np.abs(a) @ np.abs(b).T)
     if beta != 0.0 and C is not None:
         P = P + abs(float(beta)) * np.abs(np.asarray(C).astype(np.float64))
     if program:
         # t on entry, recomputed from its definition to track |t| per op
-        t = float(alpha) * (_operand_a(A[:, :K], dtype_a) @ _operand_b(B, dtype_b, K).T)
+        t = float(alpha) * (a @ b.T)
         if beta != 0.0 and C is not None:
             t = t + float(beta) * np.asarray(C).astype(np.float64)
         E = 2.0 ** -10 * P
