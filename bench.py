@@ -207,14 +207,17 @@ def workload_info(name):
                         "tensor"),
         "qkv_1x128x4096_b96": ("96 FP16 GEMMs M=1,N=128,K=4096 in one strided-batched call "
                                "(QKV projections of 32 heads)", "hbm"),
+        "mxf4_4096": ("MXFP4 GEMM M=N=K=4096 (E2M1 codes, one E8M0 scale per 32 along K), "
+                      "D=1.0*A.B+0.5*C, FP16 C/D", "tensor"),
     }
     return info[name]
 
 
 def algorithmic_bytes(case):
     """Bytes the GEMM must move at least once: A, B, C (if read), bias, D."""
-    ea = 1 if case.dtype_a == "i8" else 2
-    eb = {"f16": 2, "i8": 1, "e2m1": 0.5}[case.dtype_b]
+    mx = 0.5 + 1.0 / 32  # a code and a 32nd of a scale byte
+    ea = {"f16": 2, "i8": 1, "mxf4": mx}[case.dtype_a]
+    eb = {"f16": 2, "i8": 1, "e2m1": 0.5, "mxf4": mx}[case.dtype_b]
     ed = 4 if case.dtype_a == "i8" else 2
     b = case.M * case.K * ea + case.N * case.K * eb + case.M * case.N * ed
     if case.beta != 0:
@@ -252,7 +255,10 @@ def run_dg(args, world, rank, local):
     out_dtype = torch.int32 if base.dtype_a == "i8" else torch.float16
     out_bytes = 4 if base.dtype_a == "i8" else 2
     out_shape = (batch, base.M, base.N) if batch > 1 else (base.M, base.N)
+    is_mx = base.dtype_a == "mxf4"
     set_bytes = base.A.nbytes + base.B.nbytes + batch * base.M * base.N * out_bytes
+    if is_mx:
+        set_bytes += base.scale_a.nbytes + base.scale_b.nbytes
     nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes)) if set_bytes < 3 * L2_BYTES else 1
     nsets = min(nsets, 16)
     sets = []
@@ -261,13 +267,15 @@ def run_dg(args, world, rank, local):
     C0 = (torch.from_numpy(base.C).to(dev) if base.C is not None else
           torch.zeros(*out_shape, dtype=out_dtype, device=dev))
     bias = torch.from_numpy(base.bias).to(dev) if base.bias is not None else None
+    SA0 = torch.from_numpy(base.scale_a).to(dev) if is_mx else None
+    SB0 = torch.from_numpy(base.scale_b).to(dev) if is_mx else None
     for s in range(nsets):
         # further sets: the same values with rows (problems, for a batch)
         # rotated (same distribution, different addresses), so no step finds
-        # its operands in L2
+        # its operands in L2; scale rows move with their code rows
         sh = 37 * s
-        sets.append((torch.roll(A0, sh, 0).contiguous(), torch.roll(B0, sh, 0).contiguous(),
-                     torch.roll(C0, sh, 0).contiguous(), bias))
+        roll = (lambda t: torch.roll(t, sh, 0).contiguous() if t is not None else None)
+        sets.append((roll(A0), roll(B0), roll(C0), bias, roll(SA0), roll(SB0)))
     stream = torch.cuda.current_stream(dev)
     cands = dg.plan_tiles(base.M, base.N, base.K, base.dtype_a, base.dtype_b, base.epilogue)
     plan = cands[min(args.plan_index, len(cands) - 1)]
@@ -275,7 +283,11 @@ def run_dg(args, world, rank, local):
 
     def step(i, st=None):
         st = st or stream
-        A, B, C, bias = sets[i % nsets]
+        A, B, C, bias, SA, SB = sets[i % nsets]
+        if is_mx:
+            dg.gemm_mxf4(A, SA, B, SB, C, base.K, bias=bias, alpha=base.alpha, beta=base.beta,
+                         epilogue=base.epilogue, stream=st)
+            return
         if batch > 1:
             dg.gemm_batched(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
                             epilogue=base.epilogue, stream=st)
@@ -360,6 +372,16 @@ def run_dg(args, world, rank, local):
     hbias = torch.from_numpy(base.bias).pin_memory() if base.bias is not None else None
     hD = torch.empty(*out_shape, dtype=out_dtype).pin_memory()
     e2e_call = "dg_gemm_host on pinned host buffers"
+    h_scales = []
+    if is_mx:
+        # No host-buffer form of the MXFP4 call: the step copies the pinned
+        # codes, scales and C in, runs dg_gemm_mxf4 and copies D back.
+        e2e_call = "pinned host-to-device copies, dg_gemm_mxf4, device-to-host copy"
+        h_scales = [torch.from_numpy(base.scale_a).pin_memory(),
+                    torch.from_numpy(base.scale_b).pin_memory()]
+        dA, dB = torch.empty_like(A0), torch.empty_like(B0)
+        dSA, dSB = torch.empty_like(SA0), torch.empty_like(SB0)
+        dD = torch.empty(*out_shape, dtype=out_dtype, device=dev)
     if batch > 1:
         # The batched call takes device buffers: the step copies the pinned
         # inputs in, runs dg_gemm_strided_batched and copies D back.
@@ -370,6 +392,18 @@ def run_dg(args, world, rank, local):
         dbias = torch.empty_like(bias) if hbias is not None else None
 
     def e2e_step():
+        if is_mx:
+            with torch.cuda.stream(stream):
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                dSA.copy_(h_scales[0], non_blocking=True)
+                dSB.copy_(h_scales[1], non_blocking=True)
+                if hC is not None:
+                    dD.copy_(hC, non_blocking=True)
+                dg.gemm_mxf4(dA, dSA, dB, dSB, dD, base.K, bias=bias, alpha=base.alpha,
+                             beta=base.beta, epilogue=base.epilogue, stream=stream)
+                hD.copy_(dD, non_blocking=True)
+            return
         if batch > 1:
             with torch.cuda.stream(stream):
                 dA.copy_(hA, non_blocking=True)
@@ -434,7 +468,7 @@ def run_dg(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "i8" if base.dtype_a == "i8" else "f16",
+        "dtype": base.dtype_a,
         "data": "synthetic (seeded, recipe in workloads.py)",
         "config": {"workload": desc, "name": name, "M": base.M, "N": base.N, "K": base.K,
                    "batch": batch, "alpha": base.alpha, "beta": base.beta,
@@ -453,6 +487,7 @@ def run_dg(args, world, rank, local):
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": unit,
                 "h2d_bytes_per_step": int(hA.nbytes + hB.nbytes +
+                                          sum(t.nbytes for t in h_scales) +
                                           (hC.nbytes if hC is not None else 0) +
                                           (hbias.nbytes if hbias is not None else 0)),
                 "d2h_bytes_per_step": int(hD.nbytes),
@@ -471,6 +506,15 @@ def work_unit(case, bound):
     if bound == "hbm":
         return algorithmic_bytes(case) * 1e3, "GB/s"
     return case.flops(), ("TOPS" if case.dtype_a == "i8" else "TFLOP/s")
+
+
+def oracle_rows(oracle, case, rows):
+    """The oracle's D on the given rows of a single-problem case."""
+    kw = dict(C=case.C, bias=case.bias, alpha=case.alpha, beta=case.beta,
+              epilogue=case.epilogue, rows=rows)
+    if case.dtype_a == "mxf4":
+        return oracle.gemm_mx_reference(case.A, case.scale_a, case.B, case.scale_b, case.K, **kw)
+    return oracle.gemm_reference(case.A, case.B, case.K, case.dtype_a, case.dtype_b, **kw)
 
 
 def oracle_sample_rate(case, budget_s, rows_per_call, bound="tensor"):
@@ -493,9 +537,7 @@ def oracle_sample_rate(case, budget_s, rows_per_call, bound="tensor"):
     while t_total < budget_s and done_rows < 64 * case.M:
         rows = rng.choice(case.M, size=min(rows_per_call, case.M), replace=False)
         t = time.perf_counter()
-        oracle.gemm_reference(case.A, case.B, case.K, case.dtype_a, case.dtype_b, C=case.C,
-                              bias=case.bias, alpha=case.alpha, beta=case.beta,
-                              epilogue=case.epilogue, rows=rows)
+        oracle_rows(oracle, case, rows)
         t_total += time.perf_counter() - t
         done_rows += len(rows)
     work, unit = work_unit(case, bound)
@@ -524,9 +566,7 @@ def run_reference(args):
                                   alpha=case.alpha, beta=case.beta, epilogue=case.epilogue)
             return
         r = rng.choice(case.M, size=rows, replace=False)
-        oracle.gemm_reference(case.A, case.B, case.K, case.dtype_a, case.dtype_b, C=case.C,
-                              bias=case.bias, alpha=case.alpha, beta=case.beta,
-                              epilogue=case.epilogue, rows=r)
+        oracle_rows(oracle, case, r)
 
     for _ in range(args.warmup):
         step()

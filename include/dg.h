@@ -67,7 +67,10 @@ typedef enum {
 typedef enum {
   DG_F16 = 0,   /* IEEE binary16 */
   DG_I8 = 1,    /* two's-complement int8 */
-  DG_E2M1 = 2   /* 4-bit float: sign | 2-bit exponent (bias 1) | 1-bit mantissa */
+  DG_E2M1 = 2,  /* 4-bit float: sign | 2-bit exponent (bias 1) | 1-bit mantissa */
+  DG_MXF4 = 3   /* block-scaled E2M1 (MXFP4): E2M1 codes packed as for DG_E2M1, plus one
+                   E8M0 scale byte (2^(e - 127); 255 = NaN) per 32 codes along K.  Taken by
+                   dg_quantize_mxf4, dg_gemm_mxf4 and dg_plan_tiles (pair DG_MXF4 x DG_MXF4) */
 } dg_dtype;
 
 /* Fused epilogue applied to t = alpha*acc + beta*C:  bias adds bias[j] to t,
@@ -113,7 +116,8 @@ typedef enum {
   DG_KERNEL_GEMV = 1,  /* thin-M split-K streaming kernel on the CUDA cores */
   DG_KERNEL_TC_WIDENED = 2, /* int8 / E2M1 operands widened to FP16 by a streaming pre-pass into
                                a library workspace, then the FP16 tensor-core kernel (INT8:
-                               exact INT32 output) -- for compute-bound shapes */
+                               exact INT32 output) -- for compute-bound shapes; MXFP4
+                               operands are widened to BF16 with their block scales */
   DG_KERNEL_SKINNY = 3, /* FP16 x E2M1 with M <= 16 (HBM-bound): packed weights streamed into
                            registers, widened there and fed to warp-level m16n8k16 MMAs */
   DG_KERNEL_GEMV_MMA = 4 /* FP16 x FP16 with 2 <= M <= 16 (HBM-bound): the split-K GEMV's
@@ -286,6 +290,56 @@ dg_status dg_gemm_grouped(int64_t count, const int64_t *Ms, int64_t N, int64_t K
                           const void *const *B, int64_t ldb, void *const *C,
                           const void *const *bias, float alpha, float beta,
                           dg_epilogue epilogue, dg_stream_t stream);
+
+/* Block quantization of an FP16 matrix to MXFP4, row by row along K: for
+ * each block of 32 values (the last block of a row holds K mod 32 when K is
+ * not a multiple of 32) the scale is X = 2^s with s = floor(log2(amax)) - 2
+ * (amax the block's largest magnitude; an all-zero block takes s = -127),
+ * stored as the E8M0 byte s + 127, and each value becomes the E2M1 code
+ * nearest to v / X (ties to the code with mantissa bit 0, magnitudes above 6
+ * saturated to 6, the sign kept, so a negative value that rounds to 0 gives
+ * code 8).  A block holding a NaN or an infinity gets the scale byte 255 and
+ * codes 0.  The pages ask for low-bit operands in the tensor cores' own
+ * formats (discosf.com/news/5532976, section 2.2 layer 2 and section 4.3)
+ * without fixing a block format; this is the MX block format those
+ * tensor cores' block-scaled MMAs consume.
+ *   X: rows x K FP16, leading dimension ldx >= K elements, ldx * 2 a multiple
+ *     of 16 bytes, X 16-byte aligned.
+ *   codes: rows x K codes packed two per byte (byte p of a row: k = 2p in the
+ *     low nibble, k = 2p + 1 in the high nibble), leading dimension ldq
+ *     codes: ldq >= K and a multiple of 32 (16-byte rows), 16-byte aligned.
+ *     Bytes of a row past ceil(K / 2) are not written; with K odd, the high
+ *     nibble of the last byte is written as 0.
+ *   scales: rows x ceil(K / 32) bytes, leading dimension lds >= ceil(K / 32)
+ *     bytes; bytes past ceil(K / 32) are not written.
+ *   One launch on `stream`; rows == 0 or K == 0 is a no-op.  Every pointer is
+ *   caller-owned device memory.
+ * Errors: DG_ERR_INVALID_ARG for negative sizes, NULL or misaligned pointers
+ * and leading dimensions that break the rules above. */
+dg_status dg_quantize_mxf4(int64_t rows, int64_t K, const void *X, int64_t ldx, void *codes,
+                           int64_t ldq, void *scales, int64_t lds, dg_stream_t stream);
+
+/* D = epilogue(alpha * A.B + beta * C) for MXFP4 operands: A (M x K) and B
+ * (N rows of K), each as packed E2M1 codes (layout of dg_quantize_mxf4's
+ * output; lda, ldb in codes, >= K and multiples of 32) plus E8M0 scale bytes
+ * (scale_a: M rows of lds_a >= ceil(K / 32) bytes; scale_b: N rows of
+ * lds_b bytes).  Element k of a row stands for e2m1(code) * 2^(e - 127), with
+ * e the scale byte of block k / 32 (255: NaN for the whole block).
+ * Products are summed in FP32; C, D (one buffer, M x N, leading dimension N,
+ * FP16), bias, the epilogue, alpha and beta are as in dg_gemm.
+ * Runs the plan dg_plan_tiles gives for the pair DG_MXF4 x DG_MXF4: both
+ * operands are widened with their scales into a BF16 copy in a
+ * per-(device, stream) workspace (exact: each value has at most two
+ * significant bits and BF16 keeps FP32's exponent range; scale bytes above
+ * 251 may overflow to an infinity), then the tensor-core kernel multiplies
+ * the BF16 copies with kind::f16 MMAs and FP32 accumulation.
+ * M == 0 or N == 0 is a no-op; K == 0 gives epilogue(beta * C).
+ * Errors: as dg_gemm, plus DG_ERR_INVALID_ARG for NULL or misaligned scale
+ * pointers and leading dimensions that break the rules above. */
+dg_status dg_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                       const void *scale_a, int64_t lds_a, const void *B, int64_t ldb,
+                       const void *scale_b, int64_t lds_b, void *C, const void *bias, float alpha,
+                       float beta, dg_epilogue epilogue, dg_stream_t stream);
 
 /* As dg_gemm, but runs `plan` (one returned by dg_plan_tiles for the same
  * M, N, K and dtypes).  DG_ERR_INVALID_STATE when the plan does not fit. */

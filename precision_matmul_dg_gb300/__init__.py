@@ -13,14 +13,15 @@ import os
 __all__ = [
     "DgError", "F16", "I8", "E2M1", "EPILOGUES", "lib", "lib_path", "gemm", "gemm_raw",
     "gemm_host", "gemm_host_raw", "gemm_ex", "gemm_ex_raw", "gemm_batched", "gemm_grouped",
-    "gemm_strided_batched_raw", "OPS", "MAX_EPILOGUE_OPS",
+    "gemm_strided_batched_raw", "OPS", "MAX_EPILOGUE_OPS", "MXF4", "quantize_mxf4",
+    "quantize_mxf4_raw", "gemm_mxf4", "gemm_mxf4_raw",
     "EpilogueOp", "EpilogueProgram", "make_program",
     "plan_tiles", "query_hw", "last_error", "check_status", "set_wait_timeout_ns",
     "selftest_wait_timeout", "launch_count", "shutdown", "HwDesc", "TilePlan", "EXPORTS",
 ]
 
-F16, I8, E2M1 = 0, 1, 2
-DTYPES = {"f16": F16, "i8": I8, "e2m1": E2M1}
+F16, I8, E2M1, MXF4 = 0, 1, 2, 3
+DTYPES = {"f16": F16, "i8": I8, "e2m1": E2M1, "mxf4": MXF4}
 EPILOGUES = {"none": 0, "bias": 1, "gelu": 2, "bias_gelu": 3}
 OPS = {"bias": 1, "relu": 2, "gelu": 3, "scale": 4, "clamp": 5, "quant_i8": 6}
 MAX_EPILOGUE_OPS = 8
@@ -32,6 +33,7 @@ KERNELS = {0: "tc", 1: "gemv", 2: "tc_widened", 3: "skinny", 4: "gemv_mma", -1: 
 # Every symbol include/dg.h declares.
 EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_gemm_host",
            "dg_gemm_ex", "dg_gemm_strided_batched", "dg_gemm_grouped",
+           "dg_quantize_mxf4", "dg_gemm_mxf4",
            "dg_gemm_thin_noalloc", "dg_last_error",
            "dg_check_status", "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout",
            "dg_launch_count", "dg_shutdown"]
@@ -132,6 +134,9 @@ def lib():
                                   ctypes.POINTER(vp), ctypes.POINTER(vp), f32, f32, i32, vp]
     L.dg_gemm_ex.argtypes = [i64, i64, i64, i32, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, f32,
                              f32, ctypes.POINTER(EpilogueProgram), vp]
+    L.dg_quantize_mxf4.argtypes = [i64, i64, vp, i64, vp, i64, vp, i64, vp]
+    L.dg_gemm_mxf4.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, f32,
+                               f32, i32, vp]
     L.dg_last_error.restype = ctypes.c_char_p
     L.dg_last_error.argtypes = []
     L.dg_check_status.argtypes = [vp]
@@ -141,7 +146,8 @@ def lib():
     L.dg_launch_count.argtypes = []
     L.dg_shutdown.argtypes = []
     for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
-                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_gemm_ex", "dg_gemm_strided_batched", "dg_gemm_grouped",
+                 "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_gemm_ex", "dg_gemm_strided_batched",
+                 "dg_gemm_grouped", "dg_quantize_mxf4", "dg_gemm_mxf4",
                  "dg_check_status",
                  "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout", "dg_shutdown"):
         getattr(L, name).restype = ctypes.c_int
@@ -266,6 +272,60 @@ def gemm(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none", dtype
     _check(lib().dg_gemm(M, N, K, da, db, A.data_ptr(), sa[0], B.data_ptr(), ldb, C.data_ptr(),
                          None if bias is None else bias.data_ptr(), alpha, beta,
                          EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue), s))
+    return C
+
+
+def quantize_mxf4_raw(rows, K, X, ldx, codes, ldq, scales, lds, stream=None):
+    """dg_quantize_mxf4 with the C argument order (ldq in codes, lds in bytes)."""
+    _check(lib().dg_quantize_mxf4(int(rows), int(K), _ptr(X), int(ldx), _ptr(codes), int(ldq),
+                                  _ptr(scales), int(lds), _stream_handle(stream)))
+
+
+def quantize_mxf4(X, K=None, stream=None):
+    """MXFP4 block quantization of the fp16 rows X [rows, >= K] along K.
+
+    Returns (codes, scales): codes uint8 [rows, ldq / 2] (two E2M1 codes per
+    byte, ldq = K rounded up to 32), scales uint8 [rows, ceil(K / 32)] (E8M0).
+    """
+    import torch
+    _expect(X, "f16", "X")
+    rows = X.shape[0]
+    K = X.shape[1] if K is None else int(K)
+    ldq = (K + 31) // 32 * 32
+    nblk = (K + 31) // 32
+    codes = torch.zeros((rows, ldq // 2), dtype=torch.uint8, device=X.device)
+    scales = torch.zeros((rows, nblk), dtype=torch.uint8, device=X.device)
+    quantize_mxf4_raw(rows, K, X, X.stride(0), codes, ldq, scales, nblk, stream)
+    return codes, scales
+
+
+def gemm_mxf4_raw(M, N, K, A, lda, scale_a, lds_a, B, ldb, scale_b, lds_b, C, bias, alpha, beta,
+                  epilogue="none", stream=None):
+    """dg_gemm_mxf4 with the C argument order (lda, ldb in codes)."""
+    epi = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+    _check(lib().dg_gemm_mxf4(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(scale_a),
+                              int(lds_a), _ptr(B), int(ldb), _ptr(scale_b), int(lds_b), _ptr(C),
+                              _ptr(bias), float(alpha), float(beta), epi,
+                              _stream_handle(stream)))
+
+
+def gemm_mxf4(A, scale_a, B, scale_b, C, K, bias=None, alpha=1.0, beta=0.0, epilogue="none",
+              stream=None):
+    """D = epilogue(alpha * A.B + beta * C) for MXFP4 A and B, written into C.
+
+    A: uint8 [M, lda / 2] packed codes with scale_a uint8 [M, >= ceil(K/32)];
+    B: uint8 [N, ldb / 2] with scale_b [N, ...]; C: fp16 [M, N] dense.
+    """
+    for t, what in ((A, "A"), (B, "B"), (scale_a, "scale_a"), (scale_b, "scale_b")):
+        _expect(t, "e2m1", what)
+    _expect(C, "f16", "C")
+    M, N = C.shape
+    if A.shape[0] != M or B.shape[0] != N or scale_a.shape[0] != M or scale_b.shape[0] != N:
+        raise ValueError("shape mismatch")
+    if C.stride(0) != N:
+        raise ValueError("C must be dense row-major (leading dimension N)")
+    gemm_mxf4_raw(M, N, K, A, 2 * A.stride(0), scale_a, scale_a.stride(0), B, 2 * B.stride(0),
+                  scale_b, scale_b.stride(0), C, bias, alpha, beta, epilogue, stream)
     return C
 
 

@@ -143,6 +143,7 @@ int elem_bits(dg_dtype t) {
     case DG_F16: return 16;
     case DG_I8: return 8;
     case DG_E2M1: return 4;
+    case DG_MXF4: return 4;  // codes; the scales are a separate array
   }
   return 0;
 }
@@ -316,6 +317,40 @@ dg_status get_wide_workspace(int dev, cudaStream_t stream, int64_t elems, __half
 
 dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev);
 
+// The planner's best plan for a shape and dtype pair on device `dev`, cached
+// (the choice does not depend on the epilogue).  DG_LOG=1 prints each plan.
+dg_status cached_plan(int dev, int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+                      const dg_hw_desc& hw, dg_tile_plan* out) {
+  const auto key = std::make_tuple(dev, M, N, K, static_cast<int>(da), static_cast<int>(db), 0);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+      *out = it->second;
+      return DG_OK;
+    }
+  }
+  std::string why;
+  int n = 0;
+  dg_tile_plan plan{};
+  const dg_status s = plan_tiles(M, N, K, da, db, DG_EPI_NONE, hw, 0.0, &plan, 1, &n, &why);
+  if (s != DG_OK || n == 0)
+    return fail(DG_ERR_NO_VALID_CANDIDATE, "no valid candidate found after pruning: %s",
+                why.c_str());
+  static const bool log_plans = getenv("DG_LOG") != nullptr;
+  if (log_plans) {
+    fprintf(stderr,
+            "[dg] M=%lld N=%lld K=%lld kernel=%d tile=%dx%dx%d split_k=%d stages=%d grid=%d "
+            "est=%.2fus\n",
+            (long long)M, (long long)N, (long long)K, plan.kernel, plan.m_tile, plan.n_tile,
+            plan.k_tile, plan.split_k, plan.stages, plan.grid, plan.est_us);
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_plans[key] = plan;
+  *out = plan;
+  return DG_OK;
+}
+
 // Strided batch of one problem shape (dg_gemm_strided_batched): problem z
 // at A + z sa, B + z sb, C/D + z sc, bias + z sbias (elements; codes for
 // E2M1).  Validated by the caller.
@@ -410,35 +445,8 @@ dg_status run(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db, const v
       return fail(DG_ERR_INVALID_STATE, "plan not runnable: %s", why.c_str());
     plan = *forced;
   } else {
-    // The planner's choice does not depend on the epilogue.
-    const auto key = std::make_tuple(dev, M, N, K, static_cast<int>(da), static_cast<int>(db), 0);
-    bool have = false;
-    {
-      std::lock_guard<std::mutex> lock(g_mu);
-      auto it = g_plans.find(key);
-      if (it != g_plans.end()) {
-        plan = it->second;
-        have = true;
-      }
-    }
-    if (!have) {
-      std::string why;
-      int n = 0;
-      s = plan_tiles(M, N, K, da, db, DG_EPI_NONE, st->hw, 0.0, &plan, 1, &n, &why);
-      if (s != DG_OK || n == 0)
-        return fail(DG_ERR_NO_VALID_CANDIDATE, "no valid candidate found after pruning: %s",
-                    why.c_str());
-      std::lock_guard<std::mutex> lock(g_mu);
-      g_plans[key] = plan;
-    }
-  }
-  static const bool log_plans = getenv("DG_LOG") != nullptr;
-  if (log_plans) {
-    fprintf(stderr,
-            "[dg] M=%lld N=%lld K=%lld kernel=%d tile=%dx%dx%d split_k=%d stages=%d grid=%d "
-            "est=%.2fus\n",
-            (long long)M, (long long)N, (long long)K, plan.kernel, plan.m_tile, plan.n_tile,
-            plan.k_tile, plan.split_k, plan.stages, plan.grid, plan.est_us);
+    s = cached_plan(dev, M, N, K, da, db, st->hw, &plan);
+    if (s != DG_OK) return s;
   }
 
   if (plan.kernel == DG_KERNEL_GEMV || plan.kernel == DG_KERNEL_GEMV_MMA) {
@@ -484,6 +492,26 @@ dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev) {
     e = launch_skinny(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC) {
     e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);
+  } else if (plan.kernel == DG_KERNEL_TC_WIDENED && da == DG_MXF4) {
+    // Widen both MXFP4 operands with their block scales into BF16 copies
+    // (exact), then the tensor-core kernel on BF16 operands.
+    const int64_t ldw = widened_ld(K);
+    __half* wide = nullptr;
+    s = get_wide_workspace(dev, stream, (M + N) * ldw, &wide);
+    if (s != DG_OK) return s;
+    const MxWidenJob jobs[2] = {{a.A, M, a.lda, a.scale_a, a.lds_a, wide},
+                                {a.B, N, a.ldb, a.scale_b, a.lds_b, wide + M * ldw}};
+    e = launch_widen_mxf4(jobs, 2, K, stream, a.sm_count);
+    if (e != cudaSuccess) return fail_cuda(e, "widening launch");
+    GemmArgs w = a;
+    w.A = wide;
+    w.lda = ldw;
+    w.B = wide + M * ldw;
+    w.ldb = ldw;
+    w.dtype_a = DG_F16;
+    w.dtype_b = DG_F16;
+    w.bf16_ab = true;
+    e = launch_tc(w, plan);
   } else if (plan.kernel == DG_KERNEL_TC_WIDENED) {
     // Widen the narrow operands into FP16 copies, then the FP16 kernel.
     const int64_t ldw = widened_ld(K);
@@ -513,6 +541,116 @@ dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev) {
   }
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
   return DG_OK;
+}
+
+// Rules shared by the MXFP4 entry points for one packed operand: rows of
+// `ld` codes (>= K, a multiple of 32, so 16-byte rows) at a 16-byte aligned
+// base, and `lds` >= ceil(K / 32) scale bytes per row.
+dg_status check_mx_operand(const char* name, int64_t K, const void* codes, int64_t ld,
+                           const void* scales, int64_t lds) {
+  if (!codes || !scales) return fail(DG_ERR_INVALID_ARG, "%s or its scales is null", name);
+  if (!aligned16(codes)) return fail(DG_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  if (ld < K || ld % 32 != 0)
+    return fail(DG_ERR_INVALID_ARG,
+                "%s: leading dimension %lld codes must be >= K (%lld) and a multiple of 32", name,
+                (long long)ld, (long long)K);
+  if (lds < (K + 31) / 32)
+    return fail(DG_ERR_INVALID_ARG, "%s: %lld scale bytes per row, need %lld", name,
+                (long long)lds, (long long)((K + 31) / 32));
+  return DG_OK;
+}
+
+// dg_quantize_mxf4 (dg.h).
+dg_status run_quantize_mxf4(int64_t rows, int64_t K, const void* X, int64_t ldx, void* codes,
+                            int64_t ldq, void* scales, int64_t lds, cudaStream_t stream) {
+  if (rows < 0 || K < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
+  if (rows > (int64_t(1) << 30) || K > (int64_t(1) << 30))
+    return fail(DG_ERR_INVALID_ARG, "size above 2^30");
+  if (rows == 0 || K == 0) return DG_OK;
+  if (!X) return fail(DG_ERR_INVALID_ARG, "X is null");
+  if (!aligned16(X) || ldx % 8 != 0 || ldx < K)
+    return fail(DG_ERR_INVALID_ARG,
+                "X must be 16-byte aligned with ldx >= K and ldx a multiple of 8 elements");
+  dg_status s = check_mx_operand("the codes", K, codes, ldq, scales, lds);
+  if (s != DG_OK) return s;
+  DeviceState* st = nullptr;
+  s = device_state(&st);
+  if (s != DG_OK) return s;
+  const cudaError_t e =
+      launch_quantize_mxf4(rows, K, X, ldx, codes, ldq, scales, lds, stream, st->hw.sm_count);
+  return e == cudaSuccess ? DG_OK : fail_cuda(e, "quantization launch");
+}
+
+// dg_gemm_mxf4 (dg.h): C and D one buffer of leading dimension N.
+dg_status run_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                        const void* scale_a, int64_t lds_a, const void* B, int64_t ldb,
+                        const void* scale_b, int64_t lds_b, void* C, const void* bias,
+                        float alpha, float beta, dg_epilogue epilogue, cudaStream_t stream) {
+  EpiSpec epi;
+  dg_status s = fixed_epilogue(epilogue, &epi);
+  if (s != DG_OK) return s;
+  if (M < 0 || N < 0 || K < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
+  if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30))
+    return fail(DG_ERR_INVALID_ARG, "size above 2^30");
+  if (M == 0 || N == 0) return DG_OK;
+  if (!C) return fail(DG_ERR_INVALID_ARG, "C/D is null");
+  if (!aligned16(C)) return fail(DG_ERR_INVALID_ARG, "C/D is not 16-byte aligned");
+  if (!(isfinite(alpha) && isfinite(beta)))
+    return fail(DG_ERR_INVALID_ARG, "alpha and beta must be finite");
+  if (epi.flags & kEpiBias) {
+    if (!bias) return fail(DG_ERR_INVALID_ARG, "bias epilogue with a null bias");
+    if (reinterpret_cast<uintptr_t>(bias) & 1u)
+      return fail(DG_ERR_INVALID_ARG, "bias is not 2-byte aligned");
+  }
+  if (K > 0) {
+    if ((s = check_mx_operand("A", K, A, lda, scale_a, lds_a)) != DG_OK) return s;
+    if ((s = check_mx_operand("B", K, B, ldb, scale_b, lds_b)) != DG_OK) return s;
+  }
+  DeviceState* st = nullptr;
+  s = device_state(&st);
+  if (s != DG_OK) return s;
+  int dev = 0;
+  cudaGetDevice(&dev);
+
+  GemmArgs a;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.dtype_a = DG_MXF4;
+  a.dtype_b = DG_MXF4;
+  a.A = A;
+  a.lda = lda;
+  a.B = B;
+  a.ldb = ldb;
+  a.C = C;
+  a.ldc = N;
+  a.D = C;
+  a.ldd = N;
+  a.bias = bias;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.epi = epi.flags;
+  a.n_ops = 0;
+  for (int k = 0; k < kMaxEpiOps; ++k) a.ops[k] = EpiOp{};
+  a.batch = 1;
+  a.stride_a = a.stride_b = a.stride_c = a.stride_d = a.stride_bias = 0;
+  a.stream = stream;
+  a.status = st->status;
+  a.timeout_ns = timeout_ns();
+  a.sm_count = st->hw.sm_count;
+  a.exact_i32 = false;
+  a.scale_a = scale_a;
+  a.lds_a = lds_a;
+  a.scale_b = scale_b;
+  a.lds_b = lds_b;
+  if (K == 0) {
+    const cudaError_t e = launch_epilogue_only(a);
+    return e == cudaSuccess ? DG_OK : fail_cuda(e, "epilogue-only launch");
+  }
+  dg_tile_plan plan{};
+  s = cached_plan(dev, M, N, K, DG_MXF4, DG_MXF4, st->hw, &plan);
+  if (s != DG_OK) return s;
+  return dispatch(a, plan, dev);
 }
 
 }  // namespace
@@ -652,7 +790,8 @@ dg_status dg_plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dt
     return fail(DG_ERR_INVALID_ARG, "target_occupancy must lie in [0, 1]");
   const bool pair_ok = (dtype_a == DG_F16 && dtype_b == DG_F16) ||
                        (dtype_a == DG_I8 && dtype_b == DG_I8) ||
-                       (dtype_a == DG_F16 && dtype_b == DG_E2M1);
+                       (dtype_a == DG_F16 && dtype_b == DG_E2M1) ||
+                       (dtype_a == DG_MXF4 && dtype_b == DG_MXF4);
   if (!pair_ok) return fail(DG_ERR_UNSUPPORTED, "dtype pair not supported");
   dg_hw_desc local{};
   if (!hw) {
@@ -830,6 +969,22 @@ dg_status dg_gemm_grouped(int64_t count, const int64_t* Ms, int64_t N, int64_t K
   a.sm_count = dst->hw.sm_count;
   e = launch_gemv_mma_grouped(a, table, count, max_m, plan, ws);
   return e == cudaSuccess ? DG_OK : fail_cuda(e, "kernel launch");
+}
+
+dg_status dg_quantize_mxf4(int64_t rows, int64_t K, const void* X, int64_t ldx, void* codes,
+                           int64_t ldq, void* scales, int64_t lds, dg_stream_t stream) {
+  clear_error();
+  return run_quantize_mxf4(rows, K, X, ldx, codes, ldq, scales, lds,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                       const void* scale_a, int64_t lds_a, const void* B, int64_t ldb,
+                       const void* scale_b, int64_t lds_b, void* C, const void* bias, float alpha,
+                       float beta, dg_epilogue epilogue, dg_stream_t stream) {
+  clear_error();
+  return run_gemm_mxf4(M, N, K, A, lda, scale_a, lds_a, B, ldb, scale_b, lds_b, C, bias, alpha,
+                       beta, epilogue, reinterpret_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,

@@ -72,6 +72,7 @@ struct TcParams {
   uint64_t timeout_ns;
   uint32_t stage_tx;  // bytes TMA delivers per stage (both CTAs of a pair)
   int staged;         // FP16 out through shared-memory boxes and TMA (else direct stores)
+  uint32_t idesc_ab;  // instruction-descriptor bits of the operand type (0: FP16; BF16 bits)
 };
 static_assert(sizeof(TcParams) <= 128, "parameter struct within 128 bytes (see Epi)");
 
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int chunk_kb = Out == kOutI32 ? tc::kI32ChunkKb : p.num_k_blocks;
   const int num_chunks = (p.num_k_blocks + chunk_kb - 1) / chunk_kb;
   constexpr int kTileM = kBlockM * CG;  // rows of D per tile
-  constexpr uint32_t kIdesc = idesc_f16_f32(kTileM, BN);
+  const uint32_t idesc = idesc_f16_f32(kTileM, BN) | p.idesc_ab;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -323,9 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t da = da0 + 2 * k, db = db0 + 2 * k;
               const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
               if (CG == 2)
-                tc_mma_f16_pair(d_tmem, da, db, kIdesc, accum);
+                tc_mma_f16_pair(d_tmem, da, db, idesc, accum);
               else
-                tc_mma_f16(d_tmem, da, db, kIdesc, accum);
+                tc_mma_f16(d_tmem, da, db, idesc, accum);
             }
             if (CG == 2)
               tc_commit_pair_multicast(&empty_bar[stage], 0x3);
@@ -699,6 +700,7 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.timeout_ns = a.timeout_ns;
   p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB));
   p.staged = staged ? 1 : 0;
+  p.idesc_ab = a.bf16_ab ? idesc_ab_bf16() : 0u;
 
   auto kern = gemm_f16_tc_kernel<BN, Stages, CG, Out>;
   int dev = 0;
@@ -758,8 +760,9 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
 }  // namespace
 
 // Tile shapes compiled into the library; the planner only proposes these.
-// `a` holds FP16 operands (the caller's, or widened copies); a.exact_i32
-// selects the exact INT32 output of widened INT8 operands.
+// `a` holds FP16 operands (the caller's, or widened copies) or, with
+// a.bf16_ab, BF16 ones (widened MXFP4); a.exact_i32 selects the exact INT32
+// output of widened INT8 operands.
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (a.exact_i32) {
     if (plan.n_tile == 192 && plan.cta_group == 2 && plan.stages == 6)

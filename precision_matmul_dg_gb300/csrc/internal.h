@@ -95,6 +95,12 @@ struct GemmArgs {
   uint64_t timeout_ns;  // device-side wait limit
   int sm_count;
   bool exact_i32;       // FP16 operands hold widened INT8 values: exact INT32 output
+  bool bf16_ab = false;  // A and B are BF16 (widened MXFP4 operands), not FP16
+  // MXFP4 operands (dtype DG_MXF4): E8M0 scale bytes, row pitches in bytes
+  const void* scale_a = nullptr;
+  int64_t lds_a = 0;
+  const void* scale_b = nullptr;
+  int64_t lds_b = 0;
 };
 
 // Planner (planner.cpp) -- host only.
@@ -150,6 +156,21 @@ struct WidenJob {
 };
 cudaError_t launch_widen(const WidenJob* jobs, int njobs, int64_t K, cudaStream_t stream,
                          int sm_count);
+// MXFP4 (mx.cu): block quantization of FP16 rows (ldq in codes), and the
+// exact widening of MXFP4 rows (codes + E8M0 scales) to BF16 rows of
+// widened_ld(K) values, one or two operands per launch.
+cudaError_t launch_quantize_mxf4(int64_t rows, int64_t K, const void* X, int64_t ldx,
+                                 void* codes, int64_t ldq, void* scales, int64_t lds,
+                                 cudaStream_t stream, int sm_count);
+struct MxWidenJob {
+  const void* codes;
+  int64_t rows, ld;  // ld in codes (a multiple of 32)
+  const void* scales;
+  int64_t lds;       // bytes
+  __half* dst;       // holds BF16 bits
+};
+cudaError_t launch_widen_mxf4(const MxWidenJob* jobs, int njobs, int64_t K, cudaStream_t stream,
+                              int sm_count);
 cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns);
 
 // Workspace sizes a GEMV plan needs for `batch` problems.

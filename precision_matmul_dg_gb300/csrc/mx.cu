@@ -1,0 +1,276 @@
+// Block-scaled 4-bit operands (MXFP4): quantization of FP16 rows, and the
+// exact widening of MXFP4 operands to BF16 for the tensor-core kernel.
+//
+// Format (the MX block format; the pages -- discosf.com/news/5532976,
+// section 2.2 layer 2 and section 4.3 -- ask for low-bit operands in the
+// tensor cores' own formats but fix no block layout): along K, each block of
+// 32 values shares one E8M0 scale byte e (X = 2^(e - 127), e = 255 is NaN)
+// and each value is an E2M1 code, packed two per byte with k = 2p in the low
+// nibble of byte p (the packing of the E2M1 weights).
+//
+// Quantization (one block, 4 threads of 8 values each):
+//   amax   -- the largest magnitude, taken on the FP16 bit patterns (sign
+//             cleared; an unsigned maximum orders finite values by magnitude
+//             and puts infinities and NaNs above all of them);
+//   scale  -- s = floor(log2(amax)) - 2, read off amax's exponent field (or,
+//             for an FP16 subnormal, its leading mantissa bit); e = s + 127;
+//             an all-zero block takes s = -127; a block with an infinity or
+//             a NaN takes e = 255 and codes 0;
+//   codes  -- v * 2^-s, exact in FP32, rounded to E2M1 by the conversion
+//             instruction (nearest, ties to even, saturating at 6) on the
+//             magnitude, with the sign bit of v put back, so that -0 and
+//             negative values that round to 0 keep their sign.
+//
+// Widening: e2m1(code) has at most two significant bits and e spans 2^-127 ..
+// 2^127, so e2m1(code) * X is exact in FP32 and again in BF16 (FP32's
+// exponent range; BF16 subnormals reach 2^-133) up to e = 251; above that the
+// largest codes overflow to infinities.  The copy is laid out as the FP16
+// widening's copies are: rows of widened_ld(K) = 32 * ceil(K / 32) values.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kMxThreads = 256;
+constexpr int kMxBlock = 32;  // values per scale
+constexpr int kQuantLanes = kMxBlock / 8;  // quantizer threads per block, 8 values each
+
+// ---------------------------------------------------------------------------
+// Quantization
+// ---------------------------------------------------------------------------
+
+// Two non-negative FP32 values -> one byte of two E2M1 codes (lo in the low
+// nibble), nearest with ties to even, saturated to the largest finite code.
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 q;\n\tcvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\tcvt.u32.u8 %0, q;\n\t}"
+      : "=r"(out)
+      : "f"(hi), "f"(lo));
+  return out;
+}
+
+// 16-byte read-only load.
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Each group of 4 consecutive threads quantizes one block of 32 values: a
+// thread loads 8 values (one 16-byte load), the 4-lane maximum of the
+// magnitudes gives the scale, and the thread writes its 4 bytes of codes.
+// Blocks are numbered row-major (row, block of the row); the grid strides
+// over them.  All 4 threads of a group take the same loop trips, so the
+// 4-lane shuffles run converged.
+__global__ void __launch_bounds__(kMxThreads)
+    quantize_mxf4_kernel(const __half* __restrict__ X, int64_t ldx, int64_t K, int64_t nblk,
+                         int64_t units, uint8_t* __restrict__ codes, int64_t ldq_bytes,
+                         uint8_t* __restrict__ scales, int64_t lds) {
+  const int lane4 = threadIdx.x & 3;
+  const unsigned group_mask = 0xFu << (threadIdx.x & 28);
+  const int64_t step = static_cast<int64_t>(gridDim.x) * (kMxThreads / kQuantLanes);
+  for (int64_t u = (static_cast<int64_t>(blockIdx.x) * kMxThreads + threadIdx.x) / kQuantLanes;
+       u < units; u += step) {
+    const int64_t r = u / nblk, b = u - r * nblk;
+    const int64_t k0 = b * kMxBlock + lane4 * 8;
+    const __half* src = X + r * ldx + k0;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (k0 + 8 <= K) {
+      const uint4 v = ld_nc16(src);
+      w[0] = v.x;
+      w[1] = v.y;
+      w[2] = v.z;
+      w[3] = v.w;
+    } else {
+      // the row's last values: element loads, zeros past K
+      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+      for (int i = 0; i < 8 && k0 + i < K; ++i)
+        w[i >> 1] |= static_cast<uint32_t>(s16[i]) << (16 * (i & 1));
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m = __vmaxu2(m, w[q] & 0x7FFF7FFFu);
+    uint32_t amax = max(m & 0xFFFFu, m >> 16);
+    amax = max(amax, __shfl_xor_sync(group_mask, amax, 1));
+    amax = max(amax, __shfl_xor_sync(group_mask, amax, 2));
+
+    uint32_t scale_byte, packed = 0;
+    if (amax >= 0x7C00u) {
+      scale_byte = 255;  // infinity or NaN in the block: codes 0
+    } else {
+      int s = -127;  // all-zero block
+      if (amax != 0) {
+        const int e = static_cast<int>(amax >> 10);
+        const int fl = e != 0 ? e - 15 : (31 - __clz(static_cast<int>(amax))) - 24;
+        s = fl - 2;
+      }
+      scale_byte = static_cast<uint32_t>(s + 127);
+      // 2^-s as FP32 bits (s in [-26, 13] for a non-zero block; 2^127 for
+      // the all-zero block, whose products are zero anyway)
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[q])))) * inv;
+        const float hi =
+            fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[q] >> 16)))) * inv;
+        uint32_t byte = e2m1x2_from_f32(lo, hi);
+        byte |= ((w[q] >> 12) & 0x8u) | ((w[q] >> 24) & 0x80u);  // the two sign bits
+        packed |= byte << (8 * q);
+      }
+    }
+    uint8_t* dst = codes + r * ldq_bytes + k0 / 2;
+    if (k0 + 8 <= K) {
+      *reinterpret_cast<uint32_t*>(dst) = packed;
+    } else if (k0 < K) {
+      const int nbytes = static_cast<int>((K - k0 + 1) / 2);
+      for (int i = 0; i < nbytes; ++i) dst[i] = static_cast<uint8_t>(packed >> (8 * i));
+    }
+    if (lane4 == 0) scales[r * lds + b] = static_cast<uint8_t>(scale_byte);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Widening to BF16
+// ---------------------------------------------------------------------------
+
+// One byte of two E2M1 codes -> two FP16 values (low nibble in the low half).
+__device__ __forceinline__ __half2 e2m1x2_to_half2(uint32_t byte) {
+  uint32_t o;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(o)
+      : "r"(byte));
+  return *reinterpret_cast<__half2*>(&o);
+}
+
+// FP32 value of an E8M0 scale byte: 2^(e - 127); e = 0 is the FP32
+// subnormal 2^-127; e = 255 is NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
+  const uint32_t bits = e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : e << 23);
+  return __uint_as_float(bits);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (each byte is read once).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+struct MxOperand {
+  const uint8_t* codes;
+  int64_t ld_bytes;  // row pitch of the codes (a multiple of 16)
+  const uint8_t* scales;
+  int64_t lds;       // row pitch of the scales
+  int64_t units;     // rows * nblk
+  uint16_t* dst;     // BF16 rows of nblk * 32 values
+};
+
+// One unit = one block of one row: 16 bytes of codes and a scale byte in,
+// 32 BF16 values (64 bytes) out.  Units of the first operand, then of the
+// second; each thread issues its kUnroll loads before converting.
+constexpr int kWidenUnroll = 4;
+
+__global__ void __launch_bounds__(kMxThreads)
+    widen_mxf4_kernel(MxOperand op0, MxOperand op1, int64_t nblk) {
+  const int64_t total = op0.units + op1.units;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kMxThreads;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kMxThreads + threadIdx.x; i0 < total;
+       i0 += stride * kWidenUnroll) {
+    uint4 w[kWidenUnroll];
+    uint32_t sc[kWidenUnroll];
+#pragma unroll
+    for (int t = 0; t < kWidenUnroll; ++t) {
+      const int64_t i = i0 + t * stride;
+      if (i < total) {
+        const MxOperand& op = i < op0.units ? op0 : op1;
+        const int64_t u = i < op0.units ? i : i - op0.units;
+        const int64_t r = u / nblk, b = u - r * nblk;
+        w[t] = ld_stream16(op.codes + r * op.ld_bytes + b * 16);
+        sc[t] = op.scales[r * op.lds + b];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kWidenUnroll; ++t) {
+      const int64_t i = i0 + t * stride;
+      if (i < total) {
+        const MxOperand& op = i < op0.units ? op0 : op1;
+        const int64_t u = i < op0.units ? i : i - op0.units;
+        const float x = e8m0_to_f32(sc[t]);
+        const uint32_t ws[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
+        uint4* d = reinterpret_cast<uint4*>(op.dst + u * kMxBlock);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(e2m1x2_to_half2((ws[q] >> (8 * j)) & 0xFFu));
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f.x * x, f.y * x);
+            o[j] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          d[q] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+  // The GEMM launched next may be scheduled once every thread has issued its
+  // copies (it waits for their completion before reading them).
+  grid_launch_dependents();
+}
+
+int grid_for_units(int64_t units_per_thread_step, int sm_count) {
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8 * 4;
+  const int64_t blocks = units_per_thread_step < cap ? units_per_thread_step : cap;
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_mxf4(int64_t rows, int64_t K, const void* X, int64_t ldx,
+                                 void* codes, int64_t ldq, void* scales, int64_t lds,
+                                 cudaStream_t stream, int sm_count) {
+  const int64_t nblk = (K + kMxBlock - 1) / kMxBlock;
+  const int64_t units = rows * nblk;
+  if (units <= 0) return cudaSuccess;
+  const int per_cta = kMxThreads / kQuantLanes;
+  const int grid = grid_for_units((units + per_cta - 1) / per_cta, sm_count);
+  quantize_mxf4_kernel<<<grid, kMxThreads, 0, stream>>>(
+      static_cast<const __half*>(X), ldx, K, nblk, units, static_cast<uint8_t*>(codes), ldq / 2,
+      static_cast<uint8_t*>(scales), lds);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_widen_mxf4(const MxWidenJob* jobs, int njobs, int64_t K, cudaStream_t stream,
+                              int sm_count) {
+  if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
+  const int64_t nblk = (K + kMxBlock - 1) / kMxBlock;
+  MxOperand ops[2] = {};
+  for (int i = 0; i < njobs; ++i) {
+    ops[i].codes = static_cast<const uint8_t*>(jobs[i].codes);
+    ops[i].ld_bytes = jobs[i].ld / 2;
+    ops[i].scales = static_cast<const uint8_t*>(jobs[i].scales);
+    ops[i].lds = jobs[i].lds;
+    ops[i].units = jobs[i].rows * nblk;
+    ops[i].dst = reinterpret_cast<uint16_t*>(jobs[i].dst);
+  }
+  const int64_t total = ops[0].units + ops[1].units;
+  if (total <= 0) return cudaSuccess;
+  const int grid =
+      grid_for_units((total + kMxThreads * kWidenUnroll - 1) / (kMxThreads * kWidenUnroll),
+                     sm_count);
+  widen_mxf4_kernel<<<grid, kMxThreads, 0, stream>>>(ops[0], ops[1], nblk);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

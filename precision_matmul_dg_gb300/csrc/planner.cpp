@@ -137,6 +137,8 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
                        std::string* why) {
   const bool narrow = !(da == DG_F16 && db == DG_F16);
   if (widened && !narrow) return;
+  // MXFP4 operands run only widened (to BF16, on the FP16 kernel's tiles)
+  if ((da == DG_MXF4) != (db == DG_MXF4)) return;
   TcFamily fam = widened ? (da == DG_I8 ? TcFamily{kTcVariantsI8Widened, 2, kTcThreads}
                                         : TcFamily{kTcVariantsF16, kNumTcVariantsF16, kTcThreads})
                          : tc_family(da, db);
@@ -148,13 +150,18 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     if (why) *why += "tensor-core kernel: needs tcgen05 / tensor memory; ";
     return;
   }
-  // bytes per element read from HBM for A and B
-  const double elem_a = da == DG_I8 ? 1.0 : 2.0;
-  const double elem_b = db == DG_I8 ? 1.0 : (db == DG_E2M1 ? 0.5 : 2.0);
+  // bytes per element read from HBM for A and B (MXFP4: half a byte of code
+  // and a 32nd of a scale byte)
+  const double mx_elem = 0.5 + 1.0 / 32.0;
+  const double elem_a = da == DG_I8 ? 1.0 : (da == DG_MXF4 ? mx_elem : 2.0);
+  const double elem_b =
+      db == DG_I8 ? 1.0 : (db == DG_E2M1 ? 0.5 : (db == DG_MXF4 ? mx_elem : 2.0));
   const double elem_d = da == DG_I8 ? 4.0 : 2.0;
-  // the pre-pass reads the narrow operands and writes FP16 copies
+  // the pre-pass reads the narrow operands and writes 16-bit copies (an FP16
+  // A is used as it is)
   const double pre_bytes =
-      widened ? (da == DG_I8 ? 3.0 * M * K : 0.0) + (elem_b + 2.0) * N * static_cast<double>(K)
+      widened ? (da == DG_F16 ? 0.0 : (elem_a + 2.0) * M * static_cast<double>(K)) +
+                    (elem_b + 2.0) * N * static_cast<double>(K)
               : 0.0;
   const double t_pre = widened ? pre_bytes / hbm_bytes_per_us(hw) + (da == DG_I8 ? 4.0 : 2.0)
                                : 0.0;
@@ -575,8 +582,9 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
   if (plan.kernel == DG_KERNEL_TC_WIDENED) {
     const bool i8 = dtype_a == DG_I8 && dtype_b == DG_I8;
     const bool e2m1 = dtype_a == DG_F16 && dtype_b == DG_E2M1;
-    if (!i8 && !e2m1) {
-      if (why) *why = "widened plans are for INT8 x INT8 and FP16 x E2M1";
+    const bool mxf4 = dtype_a == DG_MXF4 && dtype_b == DG_MXF4;
+    if (!i8 && !e2m1 && !mxf4) {
+      if (why) *why = "widened plans are for INT8 x INT8, FP16 x E2M1 and MXF4 x MXF4";
       return false;
     }
     if ((plan.cta_group != 1 && plan.cta_group != 2) ||

@@ -398,4 +398,8 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
          | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
 }
 
+// Operand-type bits of that descriptor for BF16 A and B (format 1 in both
+// the A and the B field); OR-ed into idesc_f16_f32's value.
+__host__ __device__ constexpr uint32_t idesc_ab_bf16() { return (1u << 7) | (1u << 10); }
+
 }  // namespace dg

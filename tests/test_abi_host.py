@@ -306,3 +306,58 @@ def test_product_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.replace("oracle-free", ""), f
+
+
+# ---------------------------------------------------------------- MXFP4 entry points
+
+QGOOD = dict(rows=64, K=64, X=0x10000, ldx=64, codes=0x20000, ldq=64, scales=0x30000, lds=2)
+
+
+@pytest.mark.parametrize("over", [
+    dict(rows=-1), dict(K=-3), dict(X=None), dict(X=0x10008), dict(ldx=68), dict(ldx=32),
+    dict(codes=None), dict(codes=0x20004), dict(ldq=80), dict(ldq=32), dict(scales=None),
+    dict(lds=1),
+], ids=lambda o: ",".join("%s=%s" % kv for kv in o.items()))
+def test_quantize_mxf4_invalid_arguments_rejected(dg, over):
+    kw = dict(QGOOD)
+    kw.update(over)
+    with pytest.raises(dg.DgError) as ei:
+        dg.quantize_mxf4_raw(stream=0, **kw)
+    assert ei.value.name == "DG_ERR_INVALID_ARG"
+
+
+def test_quantize_mxf4_empty_is_a_noop(dg):
+    dg.quantize_mxf4_raw(0, 64, None, 64, None, 64, None, 2, stream=0)
+    dg.quantize_mxf4_raw(64, 0, None, 64, None, 64, None, 2, stream=0)
+
+
+MGOOD = dict(M=64, N=64, K=64, A=0x10000, lda=64, scale_a=0x11000, lds_a=2, B=0x20000, ldb=64,
+             scale_b=0x21000, lds_b=2, C=0x30000, bias=None, alpha=1.0, beta=0.0,
+             epilogue="none")
+
+
+@pytest.mark.parametrize("over", [
+    dict(M=-1), dict(A=None), dict(scale_a=None), dict(B=None), dict(scale_b=None),
+    dict(C=None), dict(C=0x30002), dict(A=0x10008), dict(lda=80), dict(lda=32), dict(ldb=104),
+    dict(lds_a=1), dict(lds_b=1), dict(epilogue="bias"), dict(alpha=float("nan")),
+    dict(bias=0x40001, epilogue="bias_gelu"),
+], ids=lambda o: ",".join("%s=%s" % kv for kv in o.items()))
+def test_gemm_mxf4_invalid_arguments_rejected(dg, over):
+    kw = dict(MGOOD)
+    kw.update(over)
+    with pytest.raises(dg.DgError) as ei:
+        dg.gemm_mxf4_raw(stream=0, **kw)
+    assert ei.value.name == "DG_ERR_INVALID_ARG"
+
+
+def test_gemm_mxf4_empty_is_a_noop(dg):
+    for M, N in ((0, 64), (64, 0)):
+        dg.gemm_mxf4_raw(M, N, 64, None, 64, None, 2, None, 64, None, 2, None, None, 1.0, 0.0,
+                         stream=0)
+
+
+def test_mxf4_pair_is_for_its_own_entry_point(dg):
+    # dg_gemm and dg_gemm_ex take no scales: the MXF4 pair is refused there
+    for pair in (("mxf4", "mxf4"), ("f16", "mxf4"), ("mxf4", "f16")):
+        got, _ = _call(dg, dtype_a=pair[0], dtype_b=pair[1])
+        assert got == "DG_ERR_UNSUPPORTED", pair

@@ -279,3 +279,15 @@ def test_skinny_plans(dg, M):
     # not for other dtype pairs
     assert not [q for q in dg.plan_tiles(M, N, K, "f16", "f16", hw=GB300, target_occupancy=0.0)
                 if q["kernel_name"] == "skinny"]
+
+
+def test_mxf4_plans_are_widened(dg):
+    # MXFP4 operands run only through the widening pre-pass and the FP16
+    # kernel's tiles; mixed pairs are refused
+    for shape in [(1, 4096, 4096), (16, 8960, 1536), (4096, 4096, 4096), (130, 1000, 1000)]:
+        plans = dg.plan_tiles(*shape, "mxf4", "mxf4", hw=GB300, max_out=64)
+        assert plans and {p["kernel_name"] for p in plans} == {"tc_widened"}, shape
+    for pair in (("f16", "mxf4"), ("mxf4", "e2m1")):
+        with pytest.raises(dg.DgError) as ei:
+            dg.plan_tiles(64, 64, 64, *pair, hw=GB300)
+        assert ei.value.name == "DG_ERR_UNSUPPORTED"

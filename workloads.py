@@ -41,6 +41,10 @@ class Case:
     meta: dict = field(default_factory=dict)
     program: Optional[list] = None  # epilogue ops in order (replaces `epilogue`)
     batch: int = 1  # > 1: A [batch, M, lda], B [batch, N, ldb], C [batch, M, N]
+    # dtype "mxf4": A [M, lda/2] and B [N, ldb/2] packed codes, with E8M0
+    # scale bytes [M, ceil(K/32)] and [N, ceil(K/32)]
+    scale_a: Optional[np.ndarray] = None
+    scale_b: Optional[np.ndarray] = None
 
     def flops(self):
         return 2.0 * self.M * self.N * self.K * self.batch
@@ -137,6 +141,41 @@ def random_case(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", alpha=1.
                 program=list(program) if program else None)
 
 
+def mxf4_case(M, N, K, alpha=1.0, beta=0.0, epilogue="none", seed=0, scale_lo=119,
+              scale_hi=123, name=None):
+    """MXFP4 operands drawn directly in their stored form: packed code bytes
+    uniform over 0..255 (so every code of a row, including the ones past K in
+    its last bytes, is uniform over the 16 E2M1 codes), and E8M0 scale bytes
+    uniform over [scale_lo, scale_hi] (default 2^-8 .. 2^-4: the block scales
+    of N(0,1)/sqrt(K) data at K of a few thousand); lda = ldb = K rounded up
+    to 32 codes.  C ~ N(0,1) when beta != 0, bias ~ N(0, 0.1) for a bias
+    epilogue."""
+    g = _gen(seed)
+    ld = _round_up(max(K, 1), 32)
+    nblk = (K + 31) // 32
+    A = _bytes(g, (M, ld // 2))
+    B = _bytes(g, (N, ld // 2))
+    sa = torch.randint(scale_lo, scale_hi + 1, (M, max(nblk, 1)), generator=g,
+                       dtype=torch.int16).to(torch.uint8).numpy()
+    sb = torch.randint(scale_lo, scale_hi + 1, (N, max(nblk, 1)), generator=g,
+                       dtype=torch.int16).to(torch.uint8).numpy()
+    C = _normal(g, (M, N), 1.0) if beta != 0.0 else None
+    bias = _normal(g, (N,), 0.1) if epilogue in ("bias", "bias_gelu") else None
+    return Case(name or "mxf4_%dx%dx%d" % (M, N, K), M, N, K, "mxf4", "mxf4", A, B, C, bias,
+                float(alpha), float(beta), epilogue, ld, ld, scale_a=sa, scale_b=sb)
+
+
+def mx_activations(rows, K, seed=0, lo=-20, hi=12):
+    """FP16 rows for block quantization: N(0,1) values times 2^e with e drawn
+    per row uniformly in [lo, hi] (so the rows reach from FP16 subnormals to
+    the thousands), ld = K rounded up to 8."""
+    g = _gen(seed)
+    x = torch.randn(rows, K, generator=g, dtype=torch.float32)
+    e = torch.randint(lo, hi + 1, (rows, 1), generator=g, dtype=torch.int32).to(torch.float32)
+    x = (x * torch.exp2(e)).to(torch.float16).numpy()
+    return _pad_cols(x, _round_up(max(K, 1), 8))
+
+
 def _int32(g, shape):
     return torch.randint(-(1 << 20), 1 << 20, shape, generator=g, dtype=torch.int32).numpy()
 
@@ -200,4 +239,5 @@ WORKLOADS = {
     "w4a16_m16": lambda: w4a16(16),
     "w4a16_m2048": lambda: w4a16(2048),
     "qkv_1x128x4096_b96": lambda: batched_thin(96, 128, 4096),
+    "mxf4_4096": lambda: mxf4_case(4096, 4096, 4096, beta=0.5, name="mxf4_4096"),
 }
