@@ -207,7 +207,8 @@ def workload_info(name):
                         "tensor"),
         "qkv_1x128x4096_b96": ("96 FP16 GEMMs M=1,N=128,K=4096 in one strided-batched call "
                                "(QKV projections of 32 heads)", "hbm"),
-        "mxf4_4096": ("MXFP4 GEMM M=N=K=4096 (E2M1 codes, one E8M0 scale per 32 along K), "
+        "mxf4_4096": ("MXFP4 GEMM M=N=K=4096: FP16 activations quantized to MXFP4 (E2M1 codes, "
+                      "one E8M0 scale per 32 along K) every step, times MXFP4 weights, "
                       "D=1.0*A.B+0.5*C, FP16 C/D", "tensor"),
     }
     return info[name]
@@ -217,6 +218,8 @@ def algorithmic_bytes(case):
     """Bytes the GEMM must move at least once: A, B, C (if read), bias, D."""
     mx = 0.5 + 1.0 / 32  # a code and a 32nd of a scale byte
     ea = {"f16": 2, "i8": 1, "mxf4": mx}[case.dtype_a]
+    if case.a_fp16 is not None:
+        ea = 2  # FP16 activations, quantized inside the step
     eb = {"f16": 2, "i8": 1, "e2m1": 0.5, "mxf4": mx}[case.dtype_b]
     ed = 4 if case.dtype_a == "i8" else 2
     b = case.M * case.K * ea + case.N * case.K * eb + case.M * case.N * ed
@@ -256,9 +259,12 @@ def run_dg(args, world, rank, local):
     out_bytes = 4 if base.dtype_a == "i8" else 2
     out_shape = (batch, base.M, base.N) if batch > 1 else (base.M, base.N)
     is_mx = base.dtype_a == "mxf4"
+    if is_mx:
+        # the FP16 activations stand in the A slot; the step quantizes them
+        base.A, base.scale_a = base.a_fp16, np.zeros((base.M, 1), np.uint8)
     set_bytes = base.A.nbytes + base.B.nbytes + batch * base.M * base.N * out_bytes
     if is_mx:
-        set_bytes += base.scale_a.nbytes + base.scale_b.nbytes
+        set_bytes += base.scale_b.nbytes
     nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes)) if set_bytes < 3 * L2_BYTES else 1
     nsets = min(nsets, 16)
     sets = []
@@ -267,8 +273,14 @@ def run_dg(args, world, rank, local):
     C0 = (torch.from_numpy(base.C).to(dev) if base.C is not None else
           torch.zeros(*out_shape, dtype=out_dtype, device=dev))
     bias = torch.from_numpy(base.bias).to(dev) if base.bias is not None else None
-    SA0 = torch.from_numpy(base.scale_a).to(dev) if is_mx else None
+    SA0 = None
     SB0 = torch.from_numpy(base.scale_b).to(dev) if is_mx else None
+    if is_mx:
+        # the quantized activations: one buffer, rewritten by every step
+        nblk = (base.K + 31) // 32
+        ldq = nblk * 32
+        QA = torch.empty((base.M, ldq // 2), dtype=torch.uint8, device=dev)
+        QS = torch.empty((base.M, nblk), dtype=torch.uint8, device=dev)
     for s in range(nsets):
         # further sets: the same values with rows (problems, for a batch)
         # rotated (same distribution, different addresses), so no step finds
@@ -285,7 +297,8 @@ def run_dg(args, world, rank, local):
         st = st or stream
         A, B, C, bias, SA, SB = sets[i % nsets]
         if is_mx:
-            dg.gemm_mxf4(A, SA, B, SB, C, base.K, bias=bias, alpha=base.alpha, beta=base.beta,
+            dg.quantize_mxf4_raw(base.M, base.K, A, A.stride(0), QA, ldq, QS, nblk, stream=st)
+            dg.gemm_mxf4(QA, QS, B, SB, C, base.K, bias=bias, alpha=base.alpha, beta=base.beta,
                          epilogue=base.epilogue, stream=st)
             return
         if batch > 1:
@@ -376,11 +389,11 @@ def run_dg(args, world, rank, local):
     if is_mx:
         # No host-buffer form of the MXFP4 call: the step copies the pinned
         # codes, scales and C in, runs dg_gemm_mxf4 and copies D back.
-        e2e_call = "pinned host-to-device copies, dg_gemm_mxf4, device-to-host copy"
-        h_scales = [torch.from_numpy(base.scale_a).pin_memory(),
-                    torch.from_numpy(base.scale_b).pin_memory()]
+        e2e_call = ("pinned host-to-device copies of the FP16 activations and the MXFP4 "
+                    "weights, dg_quantize_mxf4 + dg_gemm_mxf4, device-to-host copy")
+        h_scales = [torch.from_numpy(base.scale_b).pin_memory()]
         dA, dB = torch.empty_like(A0), torch.empty_like(B0)
-        dSA, dSB = torch.empty_like(SA0), torch.empty_like(SB0)
+        dSB = torch.empty_like(SB0)
         dD = torch.empty(*out_shape, dtype=out_dtype, device=dev)
     if batch > 1:
         # The batched call takes device buffers: the step copies the pinned
@@ -396,11 +409,12 @@ def run_dg(args, world, rank, local):
             with torch.cuda.stream(stream):
                 dA.copy_(hA, non_blocking=True)
                 dB.copy_(hB, non_blocking=True)
-                dSA.copy_(h_scales[0], non_blocking=True)
-                dSB.copy_(h_scales[1], non_blocking=True)
+                dSB.copy_(h_scales[0], non_blocking=True)
                 if hC is not None:
                     dD.copy_(hC, non_blocking=True)
-                dg.gemm_mxf4(dA, dSA, dB, dSB, dD, base.K, bias=bias, alpha=base.alpha,
+                dg.quantize_mxf4_raw(base.M, base.K, dA, dA.stride(0), QA, ldq, QS, nblk,
+                                     stream=stream)
+                dg.gemm_mxf4(QA, QS, dB, dSB, dD, base.K, bias=bias, alpha=base.alpha,
                              beta=base.beta, epilogue=base.epilogue, stream=stream)
                 hD.copy_(dD, non_blocking=True)
             return
@@ -512,6 +526,12 @@ def oracle_rows(oracle, case, rows):
     """The oracle's D on the given rows of a single-problem case."""
     kw = dict(C=case.C, bias=case.bias, alpha=case.alpha, beta=case.beta,
               epilogue=case.epilogue, rows=rows)
+    if case.dtype_a == "mxf4" and case.a_fp16 is not None:
+        # quantize the activation rows, then multiply
+        codes, scales = oracle.mxfp4_quantize(case.a_fp16[rows], case.K)
+        kw.update(rows=None, C=case.C[rows] if case.C is not None else None)
+        return oracle.gemm_mx_reference(oracle.pack_e2m1(codes), scales, case.B, case.scale_b,
+                                        case.K, **kw)
     if case.dtype_a == "mxf4":
         return oracle.gemm_mx_reference(case.A, case.scale_a, case.B, case.scale_b, case.K, **kw)
     return oracle.gemm_reference(case.A, case.B, case.K, case.dtype_a, case.dtype_b, **kw)

@@ -39,7 +39,6 @@ namespace {
 
 constexpr int kMxThreads = 256;
 constexpr int kMxBlock = 32;  // values per scale
-constexpr int kQuantLanes = kMxBlock / 8;  // quantizer threads per block, 8 values each
 
 // ---------------------------------------------------------------------------
 // Quantization
@@ -64,76 +63,108 @@ __device__ __forceinline__ uint4 ld_nc16(const void* p) {
   return v;
 }
 
-// Each group of 4 consecutive threads quantizes one block of 32 values: a
-// thread loads 8 values (one 16-byte load), the 4-lane maximum of the
-// magnitudes gives the scale, and the thread writes its 4 bytes of codes.
-// Blocks are numbered row-major (row, block of the row); the grid strides
-// over them.  All 4 threads of a group take the same loop trips, so the
-// 4-lane shuffles run converged.
-__global__ void __launch_bounds__(kMxThreads)
-    quantize_mxf4_kernel(const __half* __restrict__ X, int64_t ldx, int64_t K, int64_t nblk,
-                         int64_t units, uint8_t* __restrict__ codes, int64_t ldq_bytes,
-                         uint8_t* __restrict__ scales, int64_t lds) {
-  const int lane4 = threadIdx.x & 3;
-  const unsigned group_mask = 0xFu << (threadIdx.x & 28);
-  const int64_t step = static_cast<int64_t>(gridDim.x) * (kMxThreads / kQuantLanes);
-  for (int64_t u = (static_cast<int64_t>(blockIdx.x) * kMxThreads + threadIdx.x) / kQuantLanes;
-       u < units; u += step) {
-    const int64_t r = u / nblk, b = u - r * nblk;
-    const int64_t k0 = b * kMxBlock + lane4 * 8;
-    const __half* src = X + r * ldx + k0;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (k0 + 8 <= K) {
-      const uint4 v = ld_nc16(src);
-      w[0] = v.x;
-      w[1] = v.y;
-      w[2] = v.z;
-      w[3] = v.w;
-    } else {
-      // the row's last values: element loads, zeros past K
-      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
-      for (int i = 0; i < 8 && k0 + i < K; ++i)
-        w[i >> 1] |= static_cast<uint32_t>(s16[i]) << (16 * (i & 1));
-    }
-    uint32_t m = 0;
+// Quantizes one block: `w` holds this thread's 8 FP16 values (zeros past
+// K), `group_mask` the 4 lanes of the block.  Returns the thread's 4 bytes
+// of codes and sets the block's scale byte.
+__device__ __forceinline__ uint32_t quantize_block(const uint32_t (&w)[4], unsigned group_mask,
+                                                   uint32_t& scale_byte) {
+  uint32_t m = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) m = __vmaxu2(m, w[q] & 0x7FFF7FFFu);
-    uint32_t amax = max(m & 0xFFFFu, m >> 16);
-    amax = max(amax, __shfl_xor_sync(group_mask, amax, 1));
-    amax = max(amax, __shfl_xor_sync(group_mask, amax, 2));
+  for (int q = 0; q < 4; ++q) m = __vmaxu2(m, w[q] & 0x7FFF7FFFu);
+  uint32_t amax = max(m & 0xFFFFu, m >> 16);
+  amax = max(amax, __shfl_xor_sync(group_mask, amax, 1));
+  amax = max(amax, __shfl_xor_sync(group_mask, amax, 2));
+  if (amax >= 0x7C00u) {
+    scale_byte = 255;  // infinity or NaN in the block: codes 0
+    return 0;
+  }
+  int s = -127;  // all-zero block
+  if (amax != 0) {
+    const int e = static_cast<int>(amax >> 10);
+    const int fl = e != 0 ? e - 15 : (31 - __clz(static_cast<int>(amax))) - 24;
+    s = fl - 2;
+  }
+  scale_byte = static_cast<uint32_t>(s + 127);
+  // 2^-s as FP32 bits (s in [-26, 13] for a non-zero block; 2^127 for the
+  // all-zero block, whose products are zero anyway)
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float lo = fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[q])))) * inv;
+    const float hi = fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[q] >> 16)))) * inv;
+    uint32_t byte = e2m1x2_from_f32(lo, hi);
+    byte |= ((w[q] >> 12) & 0x8u) | ((w[q] >> 24) & 0x80u);  // the two sign bits
+    packed |= byte << (8 * q);
+  }
+  return packed;
+}
 
-    uint32_t scale_byte, packed = 0;
-    if (amax >= 0x7C00u) {
-      scale_byte = 255;  // infinity or NaN in the block: codes 0
-    } else {
-      int s = -127;  // all-zero block
-      if (amax != 0) {
-        const int e = static_cast<int>(amax >> 10);
-        const int fl = e != 0 ? e - 15 : (31 - __clz(static_cast<int>(amax))) - 24;
-        s = fl - 2;
-      }
-      scale_byte = static_cast<uint32_t>(s + 127);
-      // 2^-s as FP32 bits (s in [-26, 13] for a non-zero block; 2^127 for
-      // the all-zero block, whose products are zero anyway)
-      const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+// Threads are laid out by rows: a row is shared by lpr = 2^log2_lpr lanes
+// (4 <= lpr <= the block size; the CTA takes kMxThreads / lpr rows at once),
+// and each group of 4 consecutive lanes quantizes one block of 32 values at
+// a time (a thread: one 16-byte load of 8 values, a 4-lane maximum for the
+// scale, 4 bytes of codes), stepping by lpr / 4 blocks.  Each thread loads
+// kQuantUnroll blocks before working on the first, so that many 16-byte
+// loads are in flight; lpr is chosen so that a row takes one such trip when
+// it can.  All lanes of a group take the same loop trips, so the 4-lane
+// shuffles run converged; every index is a shift, not a division.
+constexpr int kQuantUnroll = 4;
+
+// Four CTAs of 256 threads per SM (up to 64 registers a thread): the launch
+// sizes its grid as one wave of four, so that no CTA waits for another.
+constexpr int kQuantCtasPerSm = 4;
+
+__global__ void __launch_bounds__(kMxThreads, kQuantCtasPerSm)
+    quantize_mxf4_kernel(const __half* __restrict__ X, int64_t ldx, int64_t K, int64_t nblk,
+                         int64_t rows, int log2_lpr, uint8_t* __restrict__ codes,
+                         int64_t ldq_bytes, uint8_t* __restrict__ scales, int64_t lds) {
+  const int lane = threadIdx.x & ((1 << log2_lpr) - 1);
+  const int lane4 = lane & 3;
+  const unsigned group_mask = 0xFu << (threadIdx.x & 28);
+  const int rows_per_cta = kMxThreads >> log2_lpr;
+  const int64_t bstep = (1 << log2_lpr) >> 2;  // blocks a row's lanes cover at once
+  const int64_t row_step = static_cast<int64_t>(gridDim.x) * rows_per_cta;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * rows_per_cta + (threadIdx.x >> log2_lpr);
+       r < rows; r += row_step) {
+    const __half* xrow = X + r * ldx;
+    uint8_t* qrow = codes + r * ldq_bytes;
+    for (int64_t b0 = lane >> 2; b0 < nblk; b0 += kQuantUnroll * bstep) {
+      uint32_t w[kQuantUnroll][4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float lo = fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[q])))) * inv;
-        const float hi =
-            fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[q] >> 16)))) * inv;
-        uint32_t byte = e2m1x2_from_f32(lo, hi);
-        byte |= ((w[q] >> 12) & 0x8u) | ((w[q] >> 24) & 0x80u);  // the two sign bits
-        packed |= byte << (8 * q);
+      for (int t = 0; t < kQuantUnroll; ++t) {
+        const int64_t k0 = (b0 + t * bstep) * kMxBlock + lane4 * 8;
+        w[t][0] = w[t][1] = w[t][2] = w[t][3] = 0u;
+        if (k0 + 8 <= K) {
+          const uint4 v = ld_nc16(xrow + k0);
+          w[t][0] = v.x;
+          w[t][1] = v.y;
+          w[t][2] = v.z;
+          w[t][3] = v.w;
+        } else if (k0 < K) {
+          // the row's last values: element loads, zeros past K
+          const uint16_t* s16 = reinterpret_cast<const uint16_t*>(xrow + k0);
+          for (int i = 0; i < 8 && k0 + i < K; ++i)
+            w[t][i >> 1] |= static_cast<uint32_t>(s16[i]) << (16 * (i & 1));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kQuantUnroll; ++t) {
+        const int64_t b = b0 + t * bstep;
+        if (b >= nblk) break;  // the same for the 4 lanes of the block
+        const int64_t k0 = b * kMxBlock + lane4 * 8;
+        uint32_t scale_byte;
+        const uint32_t packed = quantize_block(w[t], group_mask, scale_byte);
+        uint8_t* dst = qrow + k0 / 2;
+        if (k0 + 8 <= K) {
+          *reinterpret_cast<uint32_t*>(dst) = packed;
+        } else if (k0 < K) {
+          const int nbytes = static_cast<int>((K - k0 + 1) / 2);
+          for (int i = 0; i < nbytes; ++i) dst[i] = static_cast<uint8_t>(packed >> (8 * i));
+        }
+        if (lane4 == 0) scales[r * lds + b] = static_cast<uint8_t>(scale_byte);
       }
     }
-    uint8_t* dst = codes + r * ldq_bytes + k0 / 2;
-    if (k0 + 8 <= K) {
-      *reinterpret_cast<uint32_t*>(dst) = packed;
-    } else if (k0 < K) {
-      const int nbytes = static_cast<int>((K - k0 + 1) / 2);
-      for (int i = 0; i < nbytes; ++i) dst[i] = static_cast<uint8_t>(packed >> (8 * i));
-    }
-    if (lane4 == 0) scales[r * lds + b] = static_cast<uint8_t>(scale_byte);
   }
 }
 
@@ -171,54 +202,67 @@ struct MxOperand {
   int64_t ld_bytes;  // row pitch of the codes (a multiple of 16)
   const uint8_t* scales;
   int64_t lds;       // row pitch of the scales
-  int64_t units;     // rows * nblk
+  int64_t units;     // rows * nblk: blocks of 32 values
   uint16_t* dst;     // BF16 rows of nblk * 32 values
+  int dense;         // ld_bytes == 16 * nblk and lds == nblk: unit u at codes + 16 u, scales + u
 };
 
-// One unit = one block of one row: 16 bytes of codes and a scale byte in,
-// 32 BF16 values (64 bytes) out.  Units of the first operand, then of the
-// second; each thread issues its kUnroll loads before converting.
+// A unit (one block of one row: 16 bytes of codes and a scale byte in, 32
+// BF16 values = 64 bytes out) is taken by 4 consecutive threads, each
+// turning 4 code bytes into 16 output bytes: a warp reads 128 contiguous
+// bytes of codes and writes 512 contiguous bytes.  Quarter-units of the
+// first operand, then of the second; each thread issues kWidenUnroll loads
+// before converting.
 constexpr int kWidenUnroll = 4;
+
+__device__ __forceinline__ const uint8_t* unit_codes(const MxOperand& op, int64_t u, int64_t nblk,
+                                                     const uint8_t** scale) {
+  if (op.dense) {
+    *scale = op.scales + u;
+    return op.codes + u * 16;
+  }
+  const int64_t r = u / nblk, b = u - r * nblk;
+  *scale = op.scales + r * op.lds + b;
+  return op.codes + r * op.ld_bytes + b * 16;
+}
 
 __global__ void __launch_bounds__(kMxThreads)
     widen_mxf4_kernel(MxOperand op0, MxOperand op1, int64_t nblk) {
-  const int64_t total = op0.units + op1.units;
+  const int64_t total = 4 * (op0.units + op1.units);  // quarter-units
+  const int64_t q0 = 4 * op0.units;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kMxThreads;
   for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kMxThreads + threadIdx.x; i0 < total;
        i0 += stride * kWidenUnroll) {
-    uint4 w[kWidenUnroll];
-    uint32_t sc[kWidenUnroll];
+    uint32_t w[kWidenUnroll], sc[kWidenUnroll];
 #pragma unroll
     for (int t = 0; t < kWidenUnroll; ++t) {
       const int64_t i = i0 + t * stride;
       if (i < total) {
-        const MxOperand& op = i < op0.units ? op0 : op1;
-        const int64_t u = i < op0.units ? i : i - op0.units;
-        const int64_t r = u / nblk, b = u - r * nblk;
-        w[t] = ld_stream16(op.codes + r * op.ld_bytes + b * 16);
-        sc[t] = op.scales[r * op.lds + b];
+        const bool first = i < q0;
+        const int64_t qi = first ? i : i - q0;
+        const uint8_t* sp;
+        const uint8_t* cp = unit_codes(first ? op0 : op1, qi >> 2, nblk, &sp);
+        w[t] = __ldg(reinterpret_cast<const unsigned int*>(cp) + (qi & 3));
+        sc[t] = *sp;
       }
     }
 #pragma unroll
     for (int t = 0; t < kWidenUnroll; ++t) {
       const int64_t i = i0 + t * stride;
       if (i < total) {
-        const MxOperand& op = i < op0.units ? op0 : op1;
-        const int64_t u = i < op0.units ? i : i - op0.units;
+        const bool first = i < q0;
+        const int64_t qi = first ? i : i - q0;
         const float x = e8m0_to_f32(sc[t]);
-        const uint32_t ws[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
-        uint4* d = reinterpret_cast<uint4*>(op.dst + u * kMxBlock);
+        uint32_t o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t o[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(e2m1x2_to_half2((ws[q] >> (8 * j)) & 0xFFu));
-            const __nv_bfloat162 h = __floats2bfloat162_rn(f.x * x, f.y * x);
-            o[j] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-          d[q] = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(e2m1x2_to_half2((w[t] >> (8 * j)) & 0xFFu));
+          const __nv_bfloat162 h = __floats2bfloat162_rn(f.x * x, f.y * x);
+          o[j] = *reinterpret_cast<const uint32_t*>(&h);
         }
+        // quarter qi: output values 8 qi .. 8 qi + 7 of the operand's copy
+        *reinterpret_cast<uint4*>((first ? op0.dst : op1.dst) + qi * 8) =
+            make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
@@ -239,13 +283,18 @@ cudaError_t launch_quantize_mxf4(int64_t rows, int64_t K, const void* X, int64_t
                                  void* codes, int64_t ldq, void* scales, int64_t lds,
                                  cudaStream_t stream, int sm_count) {
   const int64_t nblk = (K + kMxBlock - 1) / kMxBlock;
-  const int64_t units = rows * nblk;
-  if (units <= 0) return cudaSuccess;
-  const int per_cta = kMxThreads / kQuantLanes;
-  const int grid = grid_for_units((units + per_cta - 1) / per_cta, sm_count);
+  if (rows <= 0 || nblk <= 0) return cudaSuccess;
+  // lanes per row: 4 lanes per block, kQuantUnroll blocks per lane group,
+  // rounded up to a power of two between one block's 4 and the whole CTA
+  int log2_lpr = 2;
+  while (log2_lpr < 8 && (int64_t(1) << log2_lpr) * kQuantUnroll < 4 * nblk) ++log2_lpr;
+  const int64_t rows_per_cta = kMxThreads >> log2_lpr;
+  const int64_t ctas = (rows + rows_per_cta - 1) / rows_per_cta;
+  const int64_t cap = static_cast<int64_t>(sm_count) * kQuantCtasPerSm;  // one wave
+  const int grid = static_cast<int>(ctas < cap ? ctas : cap);
   quantize_mxf4_kernel<<<grid, kMxThreads, 0, stream>>>(
-      static_cast<const __half*>(X), ldx, K, nblk, units, static_cast<uint8_t*>(codes), ldq / 2,
-      static_cast<uint8_t*>(scales), lds);
+      static_cast<const __half*>(X), ldx, K, nblk, rows, log2_lpr, static_cast<uint8_t*>(codes),
+      ldq / 2, static_cast<uint8_t*>(scales), lds);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -262,8 +311,9 @@ cudaError_t launch_widen_mxf4(const MxWidenJob* jobs, int njobs, int64_t K, cuda
     ops[i].lds = jobs[i].lds;
     ops[i].units = jobs[i].rows * nblk;
     ops[i].dst = reinterpret_cast<uint16_t*>(jobs[i].dst);
+    ops[i].dense = ops[i].ld_bytes == 16 * nblk && ops[i].lds == nblk;
   }
-  const int64_t total = ops[0].units + ops[1].units;
+  const int64_t total = 4 * (ops[0].units + ops[1].units);
   if (total <= 0) return cudaSuccess;
   const int grid =
       grid_for_units((total + kMxThreads * kWidenUnroll - 1) / (kMxThreads * kWidenUnroll),

@@ -178,11 +178,24 @@ def test_gemm_mxf4_k_zero(dg):
 
 
 def test_gemm_mxf4_full_size_sampled(dg):
-    # the bench configuration (4096^3, beta = 0.5), rows sampled for the oracle
+    # the bench configuration (4096^3, beta = 0.5) as bench.py runs it: the
+    # FP16 activations quantized on the GPU, then the MXFP4 GEMM; the oracle
+    # quantizes and multiplies a sample of the rows
     case = workloads.WORKLOADS["mxf4_4096"]()
-    got = _run_gemm(dg, case)
-    rows = np.unique(np.concatenate([np.arange(0, case.M, 257), [case.M - 1]]))
-    _assert_gemm_parity(case, got, rows)
+    M, K = case.M, case.K
+    Qa, Sa = dg.quantize_mxf4(torch.from_numpy(case.a_fp16).cuda(), K)
+    C = torch.from_numpy(case.C).cuda()
+    dg.gemm_mxf4(Qa, Sa, torch.from_numpy(case.B).cuda(), torch.from_numpy(case.scale_b).cuda(),
+                 C, K, alpha=case.alpha, beta=case.beta, epilogue=case.epilogue)
+    dg.check_status()
+    rows = np.unique(np.concatenate([np.arange(0, M, 257), [M - 1]]))
+    codes, scales = oracle.mxfp4_quantize(case.a_fp16[rows], K)
+    np.testing.assert_array_equal(oracle.gemm_ref.unpack_e2m1(Qa.cpu().numpy()[rows], K), codes)
+    np.testing.assert_array_equal(Sa.cpu().numpy()[rows], scales)
+    sampled = workloads.Case(case.name, len(rows), case.N, K, "mxf4", "mxf4",
+                             oracle.pack_e2m1(codes), case.B, case.C[rows], None, case.alpha,
+                             case.beta, case.epilogue, scale_a=scales, scale_b=case.scale_b)
+    _assert_gemm_parity(sampled, C.cpu().numpy()[rows])
 
 
 def test_quantize_then_gemm(dg):

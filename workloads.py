@@ -45,6 +45,9 @@ class Case:
     # scale bytes [M, ceil(K/32)] and [N, ceil(K/32)]
     scale_a: Optional[np.ndarray] = None
     scale_b: Optional[np.ndarray] = None
+    # dtype "mxf4" with A given as FP16 activations [M, lda16] that the step
+    # quantizes (A and scale_a are then None)
+    a_fp16: Optional[np.ndarray] = None
 
     def flops(self):
         return 2.0 * self.M * self.N * self.K * self.batch
@@ -142,14 +145,15 @@ def random_case(M, N, K, dtype_a="f16", dtype_b="f16", epilogue="none", alpha=1.
 
 
 def mxf4_case(M, N, K, alpha=1.0, beta=0.0, epilogue="none", seed=0, scale_lo=119,
-              scale_hi=123, name=None):
+              scale_hi=123, name=None, fp16_a=False):
     """MXFP4 operands drawn directly in their stored form: packed code bytes
     uniform over 0..255 (so every code of a row, including the ones past K in
     its last bytes, is uniform over the 16 E2M1 codes), and E8M0 scale bytes
     uniform over [scale_lo, scale_hi] (default 2^-8 .. 2^-4: the block scales
     of N(0,1)/sqrt(K) data at K of a few thousand); lda = ldb = K rounded up
     to 32 codes.  C ~ N(0,1) when beta != 0, bias ~ N(0, 0.1) for a bias
-    epilogue."""
+    epilogue.  With fp16_a, A is instead FP16 activations ~ N(0,1)/sqrt(K)
+    (ld = K rounded up to 8) for the step to quantize."""
     g = _gen(seed)
     ld = _round_up(max(K, 1), 32)
     nblk = (K + 31) // 32
@@ -161,8 +165,12 @@ def mxf4_case(M, N, K, alpha=1.0, beta=0.0, epilogue="none", seed=0, scale_lo=11
                        dtype=torch.int16).to(torch.uint8).numpy()
     C = _normal(g, (M, N), 1.0) if beta != 0.0 else None
     bias = _normal(g, (N,), 0.1) if epilogue in ("bias", "bias_gelu") else None
+    a16 = None
+    if fp16_a:
+        a16 = _pad_cols(_normal(g, (M, K), 1.0 / math.sqrt(max(K, 1))), _round_up(max(K, 1), 8))
+        A, sa = None, None
     return Case(name or "mxf4_%dx%dx%d" % (M, N, K), M, N, K, "mxf4", "mxf4", A, B, C, bias,
-                float(alpha), float(beta), epilogue, ld, ld, scale_a=sa, scale_b=sb)
+                float(alpha), float(beta), epilogue, ld, ld, scale_a=sa, scale_b=sb, a_fp16=a16)
 
 
 def mx_activations(rows, K, seed=0, lo=-20, hi=12):
@@ -239,5 +247,5 @@ WORKLOADS = {
     "w4a16_m16": lambda: w4a16(16),
     "w4a16_m2048": lambda: w4a16(2048),
     "qkv_1x128x4096_b96": lambda: batched_thin(96, 128, 4096),
-    "mxf4_4096": lambda: mxf4_case(4096, 4096, 4096, beta=0.5, name="mxf4_4096"),
+    "mxf4_4096": lambda: mxf4_case(4096, 4096, 4096, beta=0.5, name="mxf4_4096", fp16_a=True),
 }
