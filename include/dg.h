@@ -394,7 +394,13 @@ dg_status dg_selftest_wait_timeout(dg_stream_t stream);
 /* Kernels launched by this process through libdg so far. */
 uint64_t dg_launch_count(void);
 
-/* Frees the split-K workspaces and cached state of every device. */
+/* Frees what libdg allocated on every device (split-K, widened-operand,
+ * group-table and host-call workspaces, internal streams and events, status
+ * words) and forgets the cached plans; the next call sets them up again.
+ * Not to be called while another thread is inside libdg or while its kernels
+ * may still run.  Each kernel's shared-memory opt-in is made once per device
+ * and process and is not undone: a process that resets a device
+ * (cudaDeviceReset) cannot use libdg on that device afterwards. */
 dg_status dg_shutdown(void);
 
 #ifdef __cplusplus

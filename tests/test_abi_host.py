@@ -58,6 +58,9 @@ def test_struct_layout_matches_c(dg, tmp_path):
           printf("dg_epilogue_program %zu\\n", sizeof(dg_epilogue_program));
           printf("ops %d,%d,%d,%d,%d,%d\\n", DG_MAX_EPILOGUE_OPS, DG_OP_BIAS, DG_OP_RELU,
                  DG_OP_GELU, DG_OP_SCALE, DG_OP_CLAMP);
+          printf("dtypes %d,%d,%d,%d\\n", DG_F16, DG_I8, DG_E2M1, DG_MXF4);
+          printf("kernels %d,%d,%d,%d,%d\\n", DG_KERNEL_TC, DG_KERNEL_GEMV, DG_KERNEL_TC_WIDENED,
+                 DG_KERNEL_SKINNY, DG_KERNEL_GEMV_MMA);
           F(dg_hw_desc, l2_bytes) F(dg_hw_desc, hbm_gbps) F(dg_hw_desc, clock_ghz)
           F(dg_tile_plan, grid) F(dg_tile_plan, occupancy) F(dg_tile_plan, est_tflops)
           F(dg_epilogue_op, a) F(dg_epilogue_op, b) F(dg_epilogue_program, ops)
@@ -74,6 +77,10 @@ def test_struct_layout_matches_c(dg, tmp_path):
     assert int(out["dg_epilogue_op"]) == ctypes.sizeof(dg.EpilogueOp)
     assert int(out["dg_epilogue_program"]) == ctypes.sizeof(dg.EpilogueProgram)
     ops = [int(x) for x in out.pop("ops").split(",")]
+    assert [int(x) for x in out.pop("dtypes").split(",")] == [dg.DTYPES[k] for k in
+                                                              ("f16", "i8", "e2m1", "mxf4")]
+    kernels = [int(x) for x in out.pop("kernels").split(",")]
+    assert [dg.KERNELS[k] for k in kernels] == ["tc", "gemv", "tc_widened", "skinny", "gemv_mma"]
     assert ops == [dg.MAX_EPILOGUE_OPS] + [dg.OPS[k] for k in ("bias", "relu", "gelu", "scale",
                                                                "clamp")]
     classes = {"dg_hw_desc": dg.HwDesc, "dg_tile_plan": dg.TilePlan,
