@@ -214,3 +214,39 @@ def test_quantize_then_gemm(dg):
     case = workloads.Case("quantized", M, N, K, "mxf4", "mxf4", oracle.pack_e2m1(ca),
                           oracle.pack_e2m1(cb), scale_a=sa, scale_b=sb)
     _assert_gemm_parity(case, C.cpu().numpy())
+
+
+def test_quantize_padded_rows_not_read(dg):
+    # X rows padded with NaN past K: a quantizer that read them would give
+    # NaN scales (255) to the last blocks
+    for K in (40, 100, 4096):
+        x = workloads.mx_activations(9, K, seed=K)
+        xp = np.full((9, (K + 7) // 8 * 8 + 24), np.nan, dtype=np.float16)
+        xp[:, :K] = x[:, :K]
+        _assert_quantize_parity(dg, xp, K)
+
+
+@pytest.mark.parametrize("shape", [(70, 130, 100), (256, 300, 1024), (3, 40, 33)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gemm_mxf4_padded_operands(dg, shape):
+    # leading dimensions wider than the packed rows (the widening's general,
+    # non-packed path): code padding holds random bytes, scale padding holds
+    # NaN scales (255), so reading either would show in D
+    M, N, K = shape
+    case = workloads.mxf4_case(M, N, K, alpha=1.5, beta=0.5, epilogue="bias", seed=M * N + K)
+    nblk = (K + 31) // 32
+    rng = np.random.default_rng(7)
+
+    def pad(codes, scales, extra_codes, extra_scales):
+        rows = codes.shape[0]
+        c = rng.integers(0, 256, (rows, codes.shape[1] + extra_codes // 2)).astype(np.uint8)
+        c[:, :codes.shape[1]] = codes
+        s = np.full((rows, nblk + extra_scales), 255, dtype=np.uint8)
+        s[:, :nblk] = scales[:, :nblk]
+        return c, s
+
+    case.A, case.scale_a = pad(case.A, case.scale_a, 64, 5)
+    case.B, case.scale_b = pad(case.B, case.scale_b, 32, 1)
+    got = _run_gemm(dg, case)
+    assert not np.isnan(got).any()
+    _assert_gemm_parity(case, got)
