@@ -207,6 +207,8 @@ def workload_info(name):
                         "tensor"),
         "qkv_1x128x4096_b96": ("96 FP16 GEMMs M=1,N=128,K=4096 in one strided-batched call "
                                "(QKV projections of 32 heads)", "hbm"),
+        "moe_64x4096x2048": ("64 FP16 expert GEMMs N=4096, K=2048 with M uniform in 1..16, in one "
+                             "grouped call (a mixture-of-experts layer)", "hbm"),
         "mxf4_4096": ("MXFP4 GEMM M=N=K=4096: FP16 activations quantized to MXFP4 (E2M1 codes, "
                       "one E8M0 scale per 32 along K) every step, times MXFP4 weights, "
                       "D=1.0*A.B+0.5*C, FP16 C/D", "tensor"),
@@ -222,6 +224,9 @@ def algorithmic_bytes(case):
         ea = 2  # FP16 activations, quantized inside the step
     eb = {"f16": 2, "i8": 1, "e2m1": 0.5, "mxf4": mx}[case.dtype_b]
     ed = 4 if case.dtype_a == "i8" else 2
+    if case.group_ms is not None:  # every expert's weights, its own rows of A and D
+        rows = sum(case.group_ms)
+        return int(case.batch * case.N * case.K * eb + rows * (case.K * ea + case.N * ed))
     b = case.M * case.K * ea + case.N * case.K * eb + case.M * case.N * ed
     if case.beta != 0:
         b += case.M * case.N * ed
@@ -291,10 +296,28 @@ def run_dg(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     cands = dg.plan_tiles(base.M, base.N, base.K, base.dtype_a, base.dtype_b, base.epilogue)
     plan = cands[min(args.plan_index, len(cands) - 1)]
+    if base.group_ms is not None and base.dtype_a == "f16" and base.dtype_b == "f16" and \
+            base.M <= 16:
+        # an FP16 group whose largest M is at most 16 runs as one warp-MMA
+        # GEMV launch over the problem table, whatever one problem's plan is
+        plan = next(p for p in cands if p["kernel_name"] == "gemv_mma")
     forced = plan if args.plan_index > 0 else None  # index 0: dg_gemm's own choice
+
+    if base.group_ms is not None:
+        # one prepared group per input set: the experts' rows of A and C
+        # (the pointer arrays are built once, outside the timed steps)
+        group_runs = [dg.prepare_grouped([A[g, :m] for g, m in enumerate(base.group_ms)],
+                                         [B[g] for g in range(batch)],
+                                         [C[g, :m] for g, m in enumerate(base.group_ms)],
+                                         K=base.K, alpha=base.alpha, beta=base.beta,
+                                         epilogue=base.epilogue)
+                      for A, B, C, _, _, _ in sets]
 
     def step(i, st=None):
         st = st or stream
+        if base.group_ms is not None:
+            group_runs[i % nsets](st)
+            return
         A, B, C, bias, SA, SB = sets[i % nsets]
         if is_mx:
             dg.quantize_mxf4_raw(base.M, base.K, A, A.stride(0), QA, ldq, QS, nblk, stream=st)
@@ -404,7 +427,24 @@ def run_dg(args, world, rank, local):
         dC = torch.empty_like(dD) if hC is not None else None
         dbias = torch.empty_like(bias) if hbias is not None else None
 
+    if base.group_ms is not None:
+        e2e_call = "pinned host-to-device copies, dg_gemm_grouped, device-to-host copy"
+        dA, dB = torch.empty_like(A0), torch.empty_like(B0)
+        dD = torch.empty(*out_shape, dtype=out_dtype, device=dev)
+        e2e_group = dg.prepare_grouped([dA[g, :m] for g, m in enumerate(base.group_ms)],
+                                       [dB[g] for g in range(batch)],
+                                       [dD[g, :m] for g, m in enumerate(base.group_ms)],
+                                       K=base.K, alpha=base.alpha, beta=base.beta,
+                                       epilogue=base.epilogue)
+
     def e2e_step():
+        if base.group_ms is not None:
+            with torch.cuda.stream(stream):
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                e2e_group(stream)
+                hD.copy_(dD, non_blocking=True)
+            return
         if is_mx:
             with torch.cuda.stream(stream):
                 dA.copy_(hA, non_blocking=True)
@@ -496,7 +536,9 @@ def run_dg(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "1 GPU",
                    "plan": {k: plan[k] for k in ("kernel_name", "m_tile", "n_tile", "k_tile",
                                                  "split_k", "stages", "grid")},
-                   "plan_note": ("the single problem's plan; a batched GEMV picks its split-K "
+                   "plan_note": ("the warp-MMA GEMV over the group's problem table (split-K "
+                                 "chosen for the largest M)" if base.group_ms is not None else
+                                 "the single problem's plan; a batched GEMV picks its split-K "
                                  "for the whole batch" if batch > 1 else "")},
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": unit,
@@ -545,15 +587,17 @@ def oracle_sample_rate(case, budget_s, rows_per_call, bound="tensor"):
     rng = np.random.default_rng(0)
     done_rows, t_total = 0, 0.0
     if case.batch > 1:  # whole problems, chosen at random
-        while t_total < budget_s and done_rows < case.batch * case.M:
+        total_rows = sum(case.group_ms) if case.group_ms is not None else case.M * case.batch
+        while t_total < budget_s and done_rows < total_rows:
             z = int(rng.integers(case.batch))
+            m = case.group_ms[z] if case.group_ms is not None else case.M
             t = time.perf_counter()
-            oracle.gemm_reference(case.A[z], case.B[z], case.K, case.dtype_a, case.dtype_b,
+            oracle.gemm_reference(case.A[z][:m], case.B[z], case.K, case.dtype_a, case.dtype_b,
                                   alpha=case.alpha, beta=case.beta, epilogue=case.epilogue)
             t_total += time.perf_counter() - t
-            done_rows += case.M
+            done_rows += m
         work, unit = work_unit(case, bound)
-        return work * done_rows / (case.M * case.batch) / t_total / 1e12, unit, t_total, done_rows
+        return work * done_rows / total_rows / t_total / 1e12, unit, t_total, done_rows
     while t_total < budget_s and done_rows < 64 * case.M:
         rows = rng.choice(case.M, size=min(rows_per_call, case.M), replace=False)
         t = time.perf_counter()
@@ -578,11 +622,14 @@ def run_reference(args):
     rows = max(1, min(case.M, 64))
     import oracle
     rng = np.random.default_rng(1)
+    done = []  # rows of each whole-problem step
 
     def step():
         if case.batch > 1:  # one whole problem per step
             z = int(rng.integers(case.batch))
-            oracle.gemm_reference(case.A[z], case.B[z], case.K, case.dtype_a, case.dtype_b,
+            m = case.group_ms[z] if case.group_ms is not None else case.M
+            done.append(m)
+            oracle.gemm_reference(case.A[z][:m], case.B[z], case.K, case.dtype_a, case.dtype_b,
                                   alpha=case.alpha, beta=case.beta, epilogue=case.epilogue)
             return
         r = rng.choice(case.M, size=rows, replace=False)
@@ -596,7 +643,8 @@ def run_reference(args):
     dt = time.perf_counter() - t
     work, unit = work_unit(case, workload_info(name)[1])
     if case.batch > 1:
-        value = work / case.batch * args.steps / dt / 1e12
+        total_rows = sum(case.group_ms) if case.group_ms is not None else case.M * case.batch
+        value = work * sum(done[args.warmup:]) / total_rows / dt / 1e12
         sample = "one random problem of the %d per step (%s)" % (case.batch, name)
     else:
         value = work * rows / case.M * args.steps / dt / 1e12

@@ -13,7 +13,7 @@ import os
 __all__ = [
     "DgError", "F16", "I8", "E2M1", "EPILOGUES", "lib", "lib_path", "gemm", "gemm_raw",
     "gemm_host", "gemm_host_raw", "gemm_ex", "gemm_ex_raw", "gemm_batched", "gemm_grouped",
-    "gemm_strided_batched_raw", "OPS", "MAX_EPILOGUE_OPS", "MXF4", "quantize_mxf4",
+    "gemm_strided_batched_raw", "prepare_grouped", "OPS", "MAX_EPILOGUE_OPS", "MXF4", "quantize_mxf4",
     "quantize_mxf4_raw", "gemm_mxf4", "gemm_mxf4_raw",
     "EpilogueOp", "EpilogueProgram", "make_program",
     "plan_tiles", "query_hw", "last_error", "check_status", "set_wait_timeout_ns",
@@ -431,15 +431,12 @@ def gemm_batched(A, B, C, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none
     return C
 
 
-def gemm_grouped(As, Bs, Cs, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none",
-                 stream=None):
-    """D_g = epilogue(alpha * A_g.B_g + beta * C_g) for every g, written into Cs[g].
-
-    As: list of [M_g, lda] tensors (one lda, M_g may differ, 0 skips); Bs: a
-    list of [N, ldb] tensors or one tensor shared by all; Cs: list of [M_g, N]
-    dense tensors; bias: None, one [N] tensor or a list.  All problems share
-    N, K, the dtypes, scalars and epilogue.
-    """
+def prepare_grouped(As, Bs, Cs, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none"):
+    """Checks a group of problems once and returns run(stream=None), which
+    issues dg_gemm_grouped on them with the prepared pointer arrays (for a
+    group that is run again and again, e.g. one mixture-of-experts layer).
+    The tensors must stay alive and keep their storage.  Arguments as
+    gemm_grouped."""
     import torch
     count = len(As)
     if not isinstance(Bs, (list, tuple)):
@@ -449,7 +446,50 @@ def gemm_grouped(As, Bs, Cs, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="n
     if len(Bs) != count or len(Cs) != count or (bias is not None and len(bias) != count):
         raise ValueError("As, Bs, Cs (and bias) must have one entry per problem")
     if count == 0:
+        return lambda stream=None: Cs
+    A0, B0 = As[0], Bs[0]
+    dtype_a = "i8" if A0.dtype == torch.int8 else "f16"
+    dtype_b = {torch.float16: "f16", torch.int8: "i8", torch.uint8: "e2m1"}[B0.dtype]
+    N = Cs[0].shape[1]
+    if K is None:
+        K = A0.shape[1]
+    lda = A0.stride(0)
+    ldb = B0.stride(0) * (2 if dtype_b == "e2m1" else 1)
+    for g in range(count):
+        _expect(As[g], dtype_a, "A[%d]" % g)
+        _expect(Bs[g], dtype_b, "B[%d]" % g)
+        _expect(Cs[g], "i32" if dtype_a == "i8" else "f16", "C[%d]" % g)
+        if As[g].stride(0) != lda or Bs[g].stride(0) * (2 if dtype_b == "e2m1" else 1) != ldb:
+            raise ValueError("every problem must share lda and ldb")
+        if Cs[g].shape[1] != N or Cs[g].shape[0] != As[g].shape[0] or Bs[g].shape[0] != N or \
+                (Cs[g].shape[0] and Cs[g].stride(0) != N):
+            raise ValueError("problem %d: shapes or C layout do not match" % g)
+    vp = ctypes.c_void_p
+    Ms = (ctypes.c_int64 * count)(*[int(a.shape[0]) for a in As])
+    pa = (vp * count)(*[a.data_ptr() for a in As])
+    pb = (vp * count)(*[b.data_ptr() for b in Bs])
+    pc = (vp * count)(*[c.data_ptr() for c in Cs])
+    pbias = None if bias is None else (vp * count)(*[b.data_ptr() for b in bias])
+    args = (count, Ms, int(N), int(K), _dtype_code(dtype_a), _dtype_code(dtype_b), pa, int(lda),
+            pb, int(ldb), pc, pbias, float(alpha), float(beta), _epi_code(epilogue))
+    fn = lib().dg_gemm_grouped
+
+    def run(stream=None):
+        _check(fn(*args, _stream_handle(stream)))
         return Cs
+    return run
+
+
+def gemm_grouped(As, Bs, Cs, K=None, bias=None, alpha=1.0, beta=0.0, epilogue="none",
+                 stream=None):
+    """D_g = epilogue(alpha * A_g.B_g + beta * C_g) for every g, written into Cs[g].
+
+    As: list of [M_g, lda] tensors (one lda, M_g may differ, 0 skips); Bs: a
+    list of [N, ldb] tensors or one tensor shared by all; Cs: list of [M_g, N]
+    dense tensors; bias: None, one [N] tensor or a list.  All problems share
+    N, K, the dtypes, scalars and epilogue.
+    """
+    return prepare_grouped(As, Bs, Cs, K, bias, alpha, beta, epilogue)(stream)
     A0, B0 = As[0], Bs[0]
     dtype_a = "i8" if A0.dtype == torch.int8 else "f16"
     dtype_b = {torch.float16: "f16", torch.int8: "i8", torch.uint8: "e2m1"}[B0.dtype]

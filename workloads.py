@@ -48,8 +48,13 @@ class Case:
     # dtype "mxf4" with A given as FP16 activations [M, lda16] that the step
     # quantizes (A and scale_a are then None)
     a_fp16: Optional[np.ndarray] = None
+    # a group of `batch` problems with their own row counts (A [batch, M, lda]
+    # holds M = the largest count; problem g uses its first group_ms[g] rows)
+    group_ms: Optional[list] = None
 
     def flops(self):
+        if self.group_ms is not None:
+            return 2.0 * sum(self.group_ms) * self.N * self.K
         return 2.0 * self.M * self.N * self.K * self.batch
 
 
@@ -236,6 +241,19 @@ def batched_thin(batch, N, K, seed=0):
                 batch=batch)
 
 
+def grouped_experts(count, N, K, m_hi=16, seed=0):
+    """A mixture-of-experts layer: `count` experts with their own FP16
+    weights B_g [N, K] ~ N(0,1)/sqrt(K) and row counts M_g uniform in
+    [1, m_hi] (the tokens routed to each), activations ~ N(0,1)/sqrt(K),
+    alpha=1, beta=0."""
+    g = _gen(seed)
+    ms = [int(x) for x in torch.randint(1, m_hi + 1, (count,), generator=g)]
+    A = _normal(g, (count, m_hi, K), 1.0 / math.sqrt(K))
+    B = _normal(g, (count, N, K), 1.0 / math.sqrt(K))
+    return Case("moe_%dx%dx%d" % (count, N, K), m_hi, N, K, "f16", "f16", A, B, lda=K, ldb=K,
+                batch=count, group_ms=ms)
+
+
 WORKLOADS = {
     "f16_256": lambda: f16_256(),
     "f16_2048": lambda: f16_square(2048),
@@ -248,4 +266,5 @@ WORKLOADS = {
     "w4a16_m2048": lambda: w4a16(2048),
     "qkv_1x128x4096_b96": lambda: batched_thin(96, 128, 4096),
     "mxf4_4096": lambda: mxf4_case(4096, 4096, 4096, beta=0.5, name="mxf4_4096", fp16_a=True),
+    "moe_64x4096x2048": lambda: grouped_experts(64, 4096, 2048),
 }
