@@ -334,6 +334,9 @@ dg_status dg_quantize_mxf4(int64_t rows, int64_t K, const void *X, int64_t ldx, 
  * 251 may overflow to an infinity), then the tensor-core kernel multiplies
  * the BF16 copies with kind::f16 MMAs and FP32 accumulation.
  * M == 0 or N == 0 is a no-op; K == 0 gives epilogue(beta * C).
+ * The BF16 workspace grows with cudaMalloc the first time a shape needs it:
+ * under CUDA-graph capture, make one call of the same shape on the
+ * capturing stream before capture begins.
  * Errors: as dg_gemm, plus DG_ERR_INVALID_ARG for NULL or misaligned scale
  * pointers and leading dimensions that break the rules above. */
 dg_status dg_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
