@@ -15,6 +15,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -38,86 +40,79 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return o;
 }
 
-// Streaming 16-byte load that does not allocate in L1 (each byte is read once).
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+// Streaming loads that do not allocate in L1 (each byte is read once).
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
                : "l"(p));
   return v;
 }
+__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
 
-// Each thread issues kUnroll 16-byte loads before its first conversion, so
-// it keeps kUnroll loads in flight.  Whole 16-byte groups are read up to the
-// row pitch (a multiple of 16 bytes); columns >= K of the copy are never read
-// by the GEMM.
+// The copy is written in chunks of 16 bytes (8 FP16 values), each made from
+// 8 int8 bytes or 4 bytes of packed E2M1 codes.  Consecutive threads take
+// consecutive chunks, so a warp reads one contiguous run of 256 or 128 bytes
+// and writes 512 contiguous bytes.  Each thread issues kUnroll loads before
+// its first conversion.  Whole 16-byte source groups are read up to the row
+// pitch (a multiple of 16 bytes); columns >= K of the copy are never read by
+// the GEMM.
 constexpr int kWidenThreads = 256;
 constexpr int kUnroll = 4;
 
-// One 16-byte group of int8 (16 values) -> two 16-byte FP16 groups.
-__device__ __forceinline__ void widen_i8_group(const uint4& w, __half* d) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  uint4 o[2];
-  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    ow[2 * q] = i8x2_to_f16x2(ws[q] & 0xFFFFu);
-    ow[2 * q + 1] = i8x2_to_f16x2(ws[q] >> 16);
-  }
-  uint4* dd = reinterpret_cast<uint4*>(d);
-  dd[0] = o[0];
-  dd[1] = o[1];
-}
-
-// One 16-byte group of packed E2M1 (32 codes) -> four 16-byte FP16 groups.
-__device__ __forceinline__ void widen_e2m1_group(const uint4& w, __half* d) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  uint4* dd = reinterpret_cast<uint4*>(d);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 o;
-    o.x = e2m1x2_to_f16x2(ws[q] & 0xFFu);
-    o.y = e2m1x2_to_f16x2((ws[q] >> 8) & 0xFFu);
-    o.z = e2m1x2_to_f16x2((ws[q] >> 16) & 0xFFu);
-    o.w = e2m1x2_to_f16x2(ws[q] >> 24);
-    dd[q] = o;
-  }
-}
-
-// Source groups -> destination: kOut FP16 per group (16 for int8, 32 for E2M1).
 template <bool kE2M1>
-__device__ __forceinline__ void widen_group(const uint4& w, __half* d) {
-  if (kE2M1)
-    widen_e2m1_group(w, d);
-  else
-    widen_i8_group(w, d);
-}
+struct WidenChunk {
+  static constexpr int kInBytes = kE2M1 ? 4 : 8;   // source bytes per chunk
+  static constexpr int kPerGroup = 16 / kInBytes;  // chunks per 16-byte source group
+  using In = typename std::conditional<kE2M1, uint32_t, uint2>::type;
+  static __device__ __forceinline__ In load(const uint8_t* p) {
+    if constexpr (kE2M1)
+      return ld_stream4(p);
+    else
+      return ld_stream8(p);
+  }
+  static __device__ __forceinline__ uint4 convert(const In& w) {
+    if constexpr (kE2M1) {
+      return make_uint4(e2m1x2_to_f16x2(w & 0xFFu), e2m1x2_to_f16x2((w >> 8) & 0xFFu),
+                        e2m1x2_to_f16x2((w >> 16) & 0xFFu), e2m1x2_to_f16x2(w >> 24));
+    } else {
+      return make_uint4(i8x2_to_f16x2(w.x & 0xFFFFu), i8x2_to_f16x2(w.x >> 16),
+                        i8x2_to_f16x2(w.y & 0xFFFFu), i8x2_to_f16x2(w.y >> 16));
+    }
+  }
+};
 
 // Rows packed back to back in both source and copy (the usual case): an
-// operand is one run of groups.  One launch widens up to two operands (A and
-// B of an INT8 product): groups [0, total0) of the first, then total1 of the
+// operand is one run of chunks.  One launch widens up to two operands (A and
+// B of an INT8 product): chunks [0, total0) of the first, then total1 of the
 // second, taken kUnroll per thread step.
 template <bool kE2M1>
 __global__ void __launch_bounds__(kWidenThreads)
     widen_dense_kernel(const uint8_t* __restrict__ src0, __half* __restrict__ dst0, int64_t total0,
                        const uint8_t* __restrict__ src1, __half* __restrict__ dst1,
                        int64_t total1) {
-  constexpr int kOut = kE2M1 ? 32 : 16;
+  using C = WidenChunk<kE2M1>;
   const int64_t total = total0 + total1;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kWidenThreads;
   for (int64_t i0 = blockIdx.x * static_cast<int64_t>(kWidenThreads) + threadIdx.x; i0 < total;
        i0 += stride * kUnroll) {
-    uint4 w[kUnroll];
+    typename C::In w[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = i0 + u * stride;
-      if (i < total) w[u] = ld_stream(i < total0 ? src0 + i * 16 : src1 + (i - total0) * 16);
+      if (i < total)
+        w[u] = C::load(i < total0 ? src0 + i * C::kInBytes : src1 + (i - total0) * C::kInBytes);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t i = i0 + u * stride;
       if (i < total)
-        widen_group<kE2M1>(w[u], i < total0 ? dst0 + i * kOut : dst1 + (i - total0) * kOut);
+        *reinterpret_cast<uint4*>(i < total0 ? dst0 + i * 8 : dst1 + (i - total0) * 8) =
+            C::convert(w[u]);
     }
   }
   // The GEMM launched next (a programmatic dependent) may be scheduled once
@@ -126,26 +121,28 @@ __global__ void __launch_bounds__(kWidenThreads)
 }
 
 // Padded rows: a block takes rows blockIdx.x, blockIdx.x + gridDim.x, ...;
-// in a row its threads take groups tx, tx + blockDim.x, ...
+// in a row its threads take chunks tx, tx + blockDim.x, ...
 template <bool kE2M1>
 __global__ void __launch_bounds__(kWidenThreads)
     widen_rows_kernel(const uint8_t* __restrict__ src, int rows, int groups,
                       int64_t ld_src_bytes, __half* __restrict__ dst, int64_t ld_dst) {
-  constexpr int kOut = kE2M1 ? 32 : 16;
+  using C = WidenChunk<kE2M1>;
+  const int chunks = groups * C::kPerGroup;
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const uint8_t* s = src + static_cast<int64_t>(r) * ld_src_bytes;
     __half* d = dst + static_cast<int64_t>(r) * ld_dst;
-    for (int g0 = threadIdx.x; g0 < groups; g0 += kWidenThreads * kUnroll) {
-      uint4 w[kUnroll];
+    for (int c0 = threadIdx.x; c0 < chunks; c0 += kWidenThreads * kUnroll) {
+      typename C::In w[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int g = g0 + u * kWidenThreads;
-        if (g < groups) w[u] = ld_stream(s + static_cast<int64_t>(g) * 16);
+        const int c = c0 + u * kWidenThreads;
+        if (c < chunks) w[u] = C::load(s + static_cast<int64_t>(c) * C::kInBytes);
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int g = g0 + u * kWidenThreads;
-        if (g < groups) widen_group<kE2M1>(w[u], d + static_cast<int64_t>(g) * kOut);
+        const int c = c0 + u * kWidenThreads;
+        if (c < chunks)
+          *reinterpret_cast<uint4*>(d + static_cast<int64_t>(c) * 8) = C::convert(w[u]);
       }
     }
   }
@@ -222,8 +219,10 @@ cudaError_t launch_widen(const WidenJob* jobs, int njobs, int64_t K, cudaStream_
     }
     return cudaSuccess;
   }
-  const int64_t t0 = jobs[0].rows * w0.groups;
-  const int64_t t1 = njobs == 2 ? jobs[1].rows * w1.groups : 0;
+  // chunks of 16 output bytes: 2 per source group of int8, 4 of E2M1
+  const int64_t per_group = jobs[0].dtype == DG_E2M1 ? 4 : 2;
+  const int64_t t0 = jobs[0].rows * w0.groups * per_group;
+  const int64_t t1 = njobs == 2 ? jobs[1].rows * w1.groups * per_group : 0;
   const auto* s0 = static_cast<const uint8_t*>(jobs[0].src);
   const auto* s1 = njobs == 2 ? static_cast<const uint8_t*>(jobs[1].src) : s0;
   __half* d1 = njobs == 2 ? jobs[1].dst : jobs[0].dst;
