@@ -1,14 +1,21 @@
 """Throughput of the dg GEMM path on GB300 (one JSON line on rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dg|reference]
-                  [--workload NAME] [--all]
+                  [--workload NAME] [--configs default|all|none|NAME,...]
 
 A step is one dg_gemm call: planning (cached), the tcgen05 main loop and the
 fused alpha/beta/bias/GELU epilogue over one batch of synthetic inputs.  The
-default workload is the FP16 GEMM M = N = K = 4096 with D = 1.0*A.B + 0.5*C,
+headline workload is the FP16 GEMM M = N = K = 4096 with D = 1.0*A.B + 0.5*C,
 A, B ~ N(0,1)/sqrt(K), C ~ N(0,1) (seed 0).  Steps rotate over several input
 sets whose total size is several times the 129 MB L2, so no step reads
 operands another step left in L2.
+
+After the headline (which also carries the end-to-end number through the
+host-buffer call and the CPU oracle's rate), the same line holds a
+`configs` object: every other configuration the library is measured on
+(FP16 256^3, 2048^3 and 8192^3, INT8 4096^3, the thin M = 1 shapes, W4A16
+at M = 16 and 2048, MXFP4 4096^3), each timed with the same K and W, with
+its own value, roofline and clock record.  --configs none skips them.
 
 --impl reference times the CPU oracle (fp64 definition of the same GEMM) on
 the host cores, one bounded row sample of the same workload per step.
@@ -37,6 +44,7 @@ import torch  # noqa: E402
 
 import workloads  # noqa: E402
 
+METRIC = "GEMM TFLOP/s (INT8 TOPS) and % of GB300 dense peak; GB/s vs HBM for M=1"
 L2_BYTES = 129 * 1000 * 1000
 RAMP_S = 0.2  # untimed clock ramp before the warm-up steps
 
@@ -44,17 +52,20 @@ RAMP_S = 0.2  # untimed clock ramp before the warm-up steps
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     """Samples SM clock and clock-event reasons of one GPU through NVML
-    (read-only queries) in a background thread."""
+    (read-only queries) in a background thread, about once a millisecond,
+    from the ramp through the timed region; samples taken while the timed
+    region runs are marked as such."""
 
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x100: "display_clock_setting"}
 
-    def __init__(self, index, period_s=0.005):
+    def __init__(self, index, period_s=0.0005):
         self.index, self.period = index, period_s
-        self.samples = []
+        self.samples = []  # (mhz, reasons, timed)
         self.ok = False
+        self.timed = False
         self._stop = threading.Event()
         try:
             self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
@@ -66,6 +77,8 @@ class ClockSampler:
             mx = ctypes.c_uint()
             self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))  # 1 = SM
             self.max_mhz = int(mx.value)
+            self.reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) \
+                or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
             self.ok = True
         except OSError:
             pass
@@ -73,15 +86,18 @@ class ClockSampler:
     def _read(self):
         mhz, reasons = ctypes.c_uint(), ctypes.c_ulonglong()
         self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz))
-        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
-        fn(self.handle, ctypes.byref(reasons))
+        self.reasons_fn(self.handle, ctypes.byref(reasons))
         return int(mhz.value), int(reasons.value)
 
     def _run(self):
         while not self._stop.is_set():
-            self.samples.append(self._read())
+            timed = self.timed
+            m, r = self._read()
+            self.samples.append((m, r, timed and self.timed))
             time.sleep(self.period)
+
+    def mark_timed(self, on):
+        self.timed = on
 
     def __enter__(self):
         if self.ok:
@@ -98,13 +114,19 @@ class ClockSampler:
         if not self.ok:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "source": "unavailable"}
-        busy = [m for m, r in self.samples if not (r & 0x1)] or [m for m, _ in self.samples]
+        timed = [(m, r) for m, r, t in self.samples if t]
+        # the median of the timed region's busy samples when it has a few,
+        # else of every busy sample from the ramp on (a short timed region)
+        use = timed if len(timed) >= 5 else [(m, r) for m, r, _ in self.samples]
+        busy = [m for m, r in use if not (r & 0x1)] or [m for m, _ in use]
         seen = 0
-        for _, r in self.samples:
+        for _, r in use:
             seen |= r
         return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": self.max_mhz,
                 "reasons": [n for b, n in self.REASONS.items() if seen & b and b != 0x1],
-                "samples": len(self.samples), "source": "nvml"}
+                "samples": len(self.samples), "samples_timed": len(timed),
+                "over": "timed region" if use is timed else "ramp, warm-up and timed region",
+                "source": "nvml"}
 
 
 # --------------------------------------------------------------------------- helpers
@@ -250,187 +272,226 @@ def kernel_name(plan, case):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def run_dg(args, world, rank, local):
-    import precision_matmul_dg_gb300 as dg
-    from precision_matmul_dg_gb300 import build as dg_build
-    if rank == 0 or world > 1:
-        dg_build.build()
-    dev = torch.device("cuda", local)
-    name = args.workload
-    desc, bound = workload_info(name)
-    base = workloads.WORKLOADS[name]()
-    batch = base.batch
-    out_dtype = torch.int32 if base.dtype_a == "i8" else torch.float16
-    out_bytes = 4 if base.dtype_a == "i8" else 2
-    out_shape = (batch, base.M, base.N) if batch > 1 else (base.M, base.N)
-    is_mx = base.dtype_a == "mxf4"
-    if is_mx:
-        # the FP16 activations stand in the A slot; the step quantizes them
-        base.A, base.scale_a = base.a_fp16, np.zeros((base.M, 1), np.uint8)
-    set_bytes = base.A.nbytes + base.B.nbytes + batch * base.M * base.N * out_bytes
-    if is_mx:
-        set_bytes += base.scale_b.nbytes
-    nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes)) if set_bytes < 3 * L2_BYTES else 1
-    nsets = min(nsets, 16)
-    sets = []
-    A0 = torch.from_numpy(base.A).to(dev)
-    B0 = torch.from_numpy(base.B).to(dev)
-    C0 = (torch.from_numpy(base.C).to(dev) if base.C is not None else
-          torch.zeros(*out_shape, dtype=out_dtype, device=dev))
-    bias = torch.from_numpy(base.bias).to(dev) if base.bias is not None else None
-    SA0 = None
-    SB0 = torch.from_numpy(base.scale_b).to(dev) if is_mx else None
-    if is_mx:
-        # the quantized activations: one buffer, rewritten by every step
-        nblk = (base.K + 31) // 32
-        ldq = nblk * 32
-        QA = torch.empty((base.M, ldq // 2), dtype=torch.uint8, device=dev)
-        QS = torch.empty((base.M, nblk), dtype=torch.uint8, device=dev)
-    for s in range(nsets):
-        # further sets: the same values with rows (problems, for a batch)
-        # rotated (same distribution, different addresses), so no step finds
-        # its operands in L2; scale rows move with their code rows
-        sh = 37 * s
-        roll = (lambda t: torch.roll(t, sh, 0).contiguous() if t is not None else None)
-        sets.append((roll(A0), roll(B0), roll(C0), bias, roll(SA0), roll(SB0)))
-    stream = torch.cuda.current_stream(dev)
-    cands = dg.plan_tiles(base.M, base.N, base.K, base.dtype_a, base.dtype_b, base.epilogue)
-    plan = cands[min(args.plan_index, len(cands) - 1)]
-    if base.group_ms is not None and base.dtype_a == "f16" and base.dtype_b == "f16" and \
-            base.M <= 16:
-        # an FP16 group whose largest M is at most 16 runs as one warp-MMA
-        # GEMV launch over the problem table, whatever one problem's plan is
-        plan = next(p for p in cands if p["kernel_name"] == "gemv_mma")
-    forced = plan if args.plan_index > 0 else None  # index 0: dg_gemm's own choice
+class Workload:
+    """One workload resident on the device: its input sets (rotated so that
+    no step finds its operands in L2), its plan and the step that runs it."""
 
-    if base.group_ms is not None:
-        # one prepared group per input set: the experts' rows of A and C
-        # (the pointer arrays are built once, outside the timed steps)
-        group_runs = [dg.prepare_grouped([A[g, :m] for g, m in enumerate(base.group_ms)],
-                                         [B[g] for g in range(batch)],
-                                         [C[g, :m] for g, m in enumerate(base.group_ms)],
-                                         K=base.K, alpha=base.alpha, beta=base.beta,
-                                         epilogue=base.epilogue)
-                      for A, B, C, _, _, _ in sets]
-
-    def step(i, st=None):
-        st = st or stream
+    def __init__(self, dg, name, dev, plan_index=0):
+        self.dg, self.name, self.dev = dg, name, dev
+        self.desc, self.bound = workload_info(name)
+        base = self.base = workloads.WORKLOADS[name]()
+        batch = base.batch
+        self.out_dtype = torch.int32 if base.dtype_a == "i8" else torch.float16
+        out_bytes = 4 if base.dtype_a == "i8" else 2
+        self.out_shape = (batch, base.M, base.N) if batch > 1 else (base.M, base.N)
+        self.is_mx = base.dtype_a == "mxf4"
+        if self.is_mx:
+            # the FP16 activations stand in the A slot; the step quantizes them
+            base.A, base.scale_a = base.a_fp16, np.zeros((base.M, 1), np.uint8)
+        set_bytes = base.A.nbytes + base.B.nbytes + batch * base.M * base.N * out_bytes
+        if self.is_mx:
+            set_bytes += base.scale_b.nbytes
+        nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes)) if set_bytes < 3 * L2_BYTES else 1
+        self.nsets = min(nsets, 16)
+        self.set_bytes = set_bytes
+        self.A0 = torch.from_numpy(base.A).to(dev)
+        self.B0 = torch.from_numpy(base.B).to(dev)
+        C0 = (torch.from_numpy(base.C).to(dev) if base.C is not None else
+              torch.zeros(*self.out_shape, dtype=self.out_dtype, device=dev))
+        bias = torch.from_numpy(base.bias).to(dev) if base.bias is not None else None
+        self.bias = bias
+        self.SB0 = torch.from_numpy(base.scale_b).to(dev) if self.is_mx else None
+        if self.is_mx:
+            # the quantized activations: one buffer, rewritten by every step
+            self.nblk = (base.K + 31) // 32
+            self.ldq = self.nblk * 32
+            self.QA = torch.empty((base.M, self.ldq // 2), dtype=torch.uint8, device=dev)
+            self.QS = torch.empty((base.M, self.nblk), dtype=torch.uint8, device=dev)
+        self.sets = []
+        for s in range(self.nsets):
+            # further sets: the same values with rows (problems, for a batch)
+            # rotated (same distribution, different addresses), so no step finds
+            # its operands in L2; scale rows move with their code rows
+            sh = 37 * s
+            roll = (lambda t: torch.roll(t, sh, 0).contiguous() if t is not None else None)
+            self.sets.append((roll(self.A0), roll(self.B0), roll(C0), bias, roll(self.SB0)))
+        cands = dg.plan_tiles(base.M, base.N, base.K, base.dtype_a, base.dtype_b, base.epilogue)
+        plan = cands[min(plan_index, len(cands) - 1)]
+        if base.group_ms is not None and base.dtype_a == "f16" and base.dtype_b == "f16" and \
+                base.M <= 16:
+            # an FP16 group whose largest M is at most 16 runs as one warp-MMA
+            # GEMV launch over the problem table, whatever one problem's plan is
+            plan = next(p for p in cands if p["kernel_name"] == "gemv_mma")
+        self.plan = plan
+        self.forced = plan if plan_index > 0 else None  # index 0: dg_gemm's own choice
+        self.group_runs = None
         if base.group_ms is not None:
-            group_runs[i % nsets](st)
+            # one prepared group per input set: the experts' rows of A and C
+            # (the pointer arrays are built once, outside the timed steps)
+            self.group_runs = [
+                dg.prepare_grouped([A[g, :m] for g, m in enumerate(base.group_ms)],
+                                   [B[g] for g in range(batch)],
+                                   [C[g, :m] for g, m in enumerate(base.group_ms)],
+                                   K=base.K, alpha=base.alpha, beta=base.beta,
+                                   epilogue=base.epilogue)
+                for A, B, C, _, _ in self.sets]
+
+    def step(self, i, st):
+        dg, base = self.dg, self.base
+        if self.group_runs is not None:
+            self.group_runs[i % self.nsets](st)
             return
-        A, B, C, bias, SA, SB = sets[i % nsets]
-        if is_mx:
-            dg.quantize_mxf4_raw(base.M, base.K, A, A.stride(0), QA, ldq, QS, nblk, stream=st)
-            dg.gemm_mxf4(QA, QS, B, SB, C, base.K, bias=bias, alpha=base.alpha, beta=base.beta,
-                         epilogue=base.epilogue, stream=st)
+        A, B, C, bias, SB = self.sets[i % self.nsets]
+        if self.is_mx:
+            dg.quantize_mxf4_raw(base.M, base.K, A, A.stride(0), self.QA, self.ldq, self.QS,
+                                 self.nblk, stream=st)
+            dg.gemm_mxf4(self.QA, self.QS, B, SB, C, base.K, bias=bias, alpha=base.alpha,
+                         beta=base.beta, epilogue=base.epilogue, stream=st)
             return
-        if batch > 1:
+        if base.batch > 1:
             dg.gemm_batched(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
                             epilogue=base.epilogue, stream=st)
             return
         dg.gemm(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,
-                epilogue=base.epilogue, stream=st, plan=forced)
+                epilogue=base.epilogue, stream=st, plan=self.forced)
 
-    # An idle GPU needs a few tens of milliseconds of load before its clocks
-    # settle: run the step untimed for RAMP_S before the W warm-up steps.
-    ramp_steps, t_ramp = 0, time.perf_counter()
-    while time.perf_counter() - t_ramp < RAMP_S:
-        for i in range(8):
-            step(i)
-        torch.cuda.synchronize(dev)
-        ramp_steps += 8
-    for i in range(args.warmup):
-        step(i)
-    dg.check_status(stream)
-    torch.cuda.synchronize(dev)
+    def work_unit(self):
+        return work_unit(self.base, self.bound)
 
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+def time_workload(w, args, world, local, stream):
+    """Ramp, W warm-up steps, then K timed steps between barriers and
+    synchronizations (CUDA events on the launching stream).  Returns (total
+    ms of the K steps, kernel launches inside them, the clock summary, the
+    number of untimed ramp steps)."""
+    dg, dev = w.dg, w.dev
     sampler = ClockSampler(local)
-    graph = None
-    if args.graph:
-        # The K timed steps captured once and replayed as one graph: the
-        # launches run back to back with no host work between them.  Warm up
-        # on the capture stream first: a split-K plan allocates its
-        # per-stream workspace on first use, which must not happen mid-capture.
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        for i in range(args.warmup):
-            step(i, st=cap)
-        torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        launches0 = dg.launch_count()
-        with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
-            for i in range(args.steps):
-                step(i, st=cap)
-        launches = dg.launch_count() - launches0
-        graph.replay()  # one untimed replay
-        torch.cuda.synchronize(dev)
-    else:
-        launches0 = dg.launch_count()
-    barrier(world)
-    torch.cuda.synchronize(dev)
     with sampler:
+        # An idle GPU needs a few tens of milliseconds of load before its
+        # clocks settle: run the step untimed for RAMP_S before the warm-up.
+        ramp_steps, t_ramp = 0, time.perf_counter()
+        while time.perf_counter() - t_ramp < RAMP_S:
+            for i in range(8):
+                w.step(i, stream)
+            torch.cuda.synchronize(dev)
+            ramp_steps += 8
+        for i in range(args.warmup):
+            w.step(i, stream)
+        dg.check_status(stream)
+        torch.cuda.synchronize(dev)
+
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        graph = None
+        if args.graph:
+            # The K timed steps captured once and replayed as one graph: the
+            # launches run back to back with no host work between them.  Warm
+            # up on the capture stream first: a split-K plan allocates its
+            # per-stream workspace on first use, which must not happen
+            # mid-capture.
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            for i in range(args.warmup):
+                w.step(i, cap)
+            torch.cuda.synchronize(dev)
+            graph = torch.cuda.CUDAGraph()
+            launches0 = dg.launch_count()
+            with torch.cuda.graph(graph, stream=cap, capture_error_mode="thread_local"):
+                for i in range(args.steps):
+                    w.step(i, cap)
+            launches = dg.launch_count() - launches0
+            graph.replay()  # one untimed replay
+            torch.cuda.synchronize(dev)
+        else:
+            launches0 = dg.launch_count()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        sampler.mark_timed(True)
         t0.record(stream)
         if graph is not None:
             graph.replay()
         else:
             for i in range(args.steps):
-                step(i)
+                w.step(i, stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
-    barrier(world)
+        sampler.mark_timed(False)
+        barrier(world)
     if graph is None:
         launches = dg.launch_count() - launches0
     dg.check_status(stream)
-    total_ms = t0.elapsed_time(t1)
-    # The K launches run back to back on one stream (eager or replayed from a
-    # graph), each overlapping the previous one's drain; a launch's average
-    # duration is the timed region over K.
-    kern_avg_ms = total_ms / args.steps
+    return t0.elapsed_time(t1), launches, sampler.summary(), ramp_steps
 
-    total_ms_max = max_over_ranks(total_ms, world)
-    # Throughput unit: TFLOP/s (TOPS for INT8) for tensor-bound workloads,
-    # algorithmic GB/s for the HBM-bound thin ones.
-    if bound == "hbm":
-        work, unit = algorithmic_bytes(base) * 1e3, "GB/s"   # so that work / s / 1e12 = GB/s
-    else:
-        work, unit = base.flops(), ("TOPS" if base.dtype_a == "i8" else "TFLOP/s")
+
+def roofline(w, kern_avg_ms, peaks, peak_src):
+    """The dominant kernel's roofline: algorithmic FLOPs (tensor-bound) or
+    bytes (HBM-bound) per launch over the launch's average duration."""
+    base = w.base
     flops = base.flops()
-    total_work = sum_over_ranks(work * args.steps, world)
-    value = total_work / (total_ms_max * 1e-3) / 1e12
+    if w.bound == "tensor":
+        achieved = flops / (kern_avg_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": "%s bf16 dense burst (fp16 runs at the bf16 rate)" % peak_src}
+        if base.dtype_a == "i8":
+            roof["unit"] = "TOPS"
+            roof["peak_source"] += ("; INT8 runs on the FP16 tensor path (sm_103a has no "
+                                    "integer tcgen05 MMA), so its denominator is the FP16 peak")
+        if base.dtype_a == "mxf4":
+            roof["peak_source"] += "; the MXFP4 step is measured against the 16-bit peak"
+    else:
+        gbs = algorithmic_bytes(base) / (kern_avg_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(gbs / peak, 4), "peak_source": "%s copy bandwidth" % peak_src}
+    kname = kernel_name(w.plan, base)
+    roof["kernel"] = kname
+    roof["kernel_avg_us"] = round(kern_avg_ms * 1e3, 2)
+    roof["traffic"] = recorded_traffic(kname, w.name)
+    roof["algorithmic_bytes"] = algorithmic_bytes(base)
+    roof["algorithmic_flops"] = flops
+    return roof
 
-    # e2e: the same GEMM through the C ABI's host-buffer call (dg_gemm_host)
-    # on pinned host buffers: every step copies A, B, C (when beta != 0) and
-    # bias to the device and reads D back, inside the timed region.
+
+def plan_summary(plan):
+    return {k: plan[k] for k in ("kernel_name", "m_tile", "n_tile", "k_tile", "split_k", "stages",
+                                 "grid")}
+
+
+def measure_e2e(w, args, world, stream):
+    """The same metric end to end: every step copies its inputs from pinned
+    host memory to the device and its result back, inside the timed region."""
+    dg, dev, base = w.dg, w.dev, w.base
+    batch = base.batch
     hA = torch.from_numpy(base.A).pin_memory()
     hB = torch.from_numpy(base.B).pin_memory()
     hC = torch.from_numpy(base.C).pin_memory() if base.C is not None else None
     hbias = torch.from_numpy(base.bias).pin_memory() if base.bias is not None else None
-    hD = torch.empty(*out_shape, dtype=out_dtype).pin_memory()
-    e2e_call = "dg_gemm_host on pinned host buffers"
+    hD = torch.empty(*w.out_shape, dtype=w.out_dtype).pin_memory()
+    call = "dg_gemm_host on pinned host buffers"
     h_scales = []
-    if is_mx:
+    if w.is_mx:
         # No host-buffer form of the MXFP4 call: the step copies the pinned
-        # codes, scales and C in, runs dg_gemm_mxf4 and copies D back.
-        e2e_call = ("pinned host-to-device copies of the FP16 activations and the MXFP4 "
-                    "weights, dg_quantize_mxf4 + dg_gemm_mxf4, device-to-host copy")
+        # activations, codes, scales and C in, runs dg_quantize_mxf4 +
+        # dg_gemm_mxf4 and copies D back.
+        call = ("pinned host-to-device copies of the FP16 activations and the MXFP4 "
+                "weights, dg_quantize_mxf4 + dg_gemm_mxf4, device-to-host copy")
         h_scales = [torch.from_numpy(base.scale_b).pin_memory()]
-        dA, dB = torch.empty_like(A0), torch.empty_like(B0)
-        dSB = torch.empty_like(SB0)
-        dD = torch.empty(*out_shape, dtype=out_dtype, device=dev)
+        dA, dB = torch.empty_like(w.A0), torch.empty_like(w.B0)
+        dSB = torch.empty_like(w.SB0)
+        dD = torch.empty(*w.out_shape, dtype=w.out_dtype, device=dev)
     if batch > 1:
         # The batched call takes device buffers: the step copies the pinned
         # inputs in, runs dg_gemm_strided_batched and copies D back.
-        e2e_call = "pinned host-to-device copies, dg_gemm_strided_batched, device-to-host copy"
-        dA, dB = torch.empty_like(A0), torch.empty_like(B0)
-        dD = torch.empty(*out_shape, dtype=out_dtype, device=dev)
+        call = "pinned host-to-device copies, dg_gemm_strided_batched, device-to-host copy"
+        dA, dB = torch.empty_like(w.A0), torch.empty_like(w.B0)
+        dD = torch.empty(*w.out_shape, dtype=w.out_dtype, device=dev)
         dC = torch.empty_like(dD) if hC is not None else None
-        dbias = torch.empty_like(bias) if hbias is not None else None
-
+        dbias = torch.empty_like(w.bias) if hbias is not None else None
     if base.group_ms is not None:
-        e2e_call = "pinned host-to-device copies, dg_gemm_grouped, device-to-host copy"
-        dA, dB = torch.empty_like(A0), torch.empty_like(B0)
-        dD = torch.empty(*out_shape, dtype=out_dtype, device=dev)
+        call = "pinned host-to-device copies, dg_gemm_grouped, device-to-host copy"
+        dA, dB = torch.empty_like(w.A0), torch.empty_like(w.B0)
+        dD = torch.empty(*w.out_shape, dtype=w.out_dtype, device=dev)
         e2e_group = dg.prepare_grouped([dA[g, :m] for g, m in enumerate(base.group_ms)],
                                        [dB[g] for g in range(batch)],
                                        [dD[g, :m] for g, m in enumerate(base.group_ms)],
@@ -445,16 +506,16 @@ def run_dg(args, world, rank, local):
                 e2e_group(stream)
                 hD.copy_(dD, non_blocking=True)
             return
-        if is_mx:
+        if w.is_mx:
             with torch.cuda.stream(stream):
                 dA.copy_(hA, non_blocking=True)
                 dB.copy_(hB, non_blocking=True)
                 dSB.copy_(h_scales[0], non_blocking=True)
                 if hC is not None:
                     dD.copy_(hC, non_blocking=True)
-                dg.quantize_mxf4_raw(base.M, base.K, dA, dA.stride(0), QA, ldq, QS, nblk,
-                                     stream=stream)
-                dg.gemm_mxf4(QA, QS, dB, dSB, dD, base.K, bias=bias, alpha=base.alpha,
+                dg.quantize_mxf4_raw(base.M, base.K, dA, dA.stride(0), w.QA, w.ldq, w.QS,
+                                     w.nblk, stream=stream)
+                dg.gemm_mxf4(w.QA, w.QS, dB, dSB, dD, base.K, bias=w.bias, alpha=base.alpha,
                              beta=base.beta, epilogue=base.epilogue, stream=stream)
                 hD.copy_(dD, non_blocking=True)
             return
@@ -486,33 +547,66 @@ def run_dg(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e_value = sum_over_ranks(work * e2e_steps, world) / (e2e_ms * 1e-3) / 1e12
+    work, unit = w.work_unit()
+    value = sum_over_ranks(work * e2e_steps, world) / (e2e_ms * 1e-3) / 1e12
+    return {"value": round(value, 2), "unit": unit,
+            "h2d_bytes_per_step": int(hA.nbytes + hB.nbytes +
+                                      sum(t.nbytes for t in h_scales) +
+                                      (hC.nbytes if hC is not None else 0) +
+                                      (hbias.nbytes if hbias is not None else 0)),
+            "d2h_bytes_per_step": int(hD.nbytes),
+            "call": "%s, %d steps" % (call, e2e_steps)}
 
+
+def measure_config(dg, name, args, world, local, dev, stream, peaks, peak_src):
+    """One further workload, timed exactly like the headline (same K and W,
+    its own ramp, rotating inputs above L2): device-timed value, roofline and
+    clocks.  Its buffers are freed before the next one."""
+    w = Workload(dg, name, dev)
+    total_ms, launches, clocks, _ = time_workload(w, args, world, local, stream)
+    total_ms_max = max_over_ranks(total_ms, world)
+    work, unit = w.work_unit()
+    value = sum_over_ranks(work * args.steps, world) / (total_ms_max * 1e-3) / 1e12
+    kern_avg_ms = total_ms / args.steps
+    out = {"workload": w.desc, "value": round(value, 2), "unit": unit,
+           "ms_per_step": round(total_ms_max / args.steps, 5),
+           "kernel_avg_us": round(kern_avg_ms * 1e3, 2),
+           "roofline": roofline(w, kern_avg_ms, peaks, peak_src),
+           "plan": plan_summary(w.plan), "gpu_launches": int(launches), "clocks": clocks,
+           "l2": ("%d rotating input sets, %.0f MB > L2" % (w.nsets, w.nsets * w.set_bytes / 1e6)
+                  if w.nsets > 1 else "inputs larger than L2")}
+    del w
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_dg(args, world, rank, local):
+    import precision_matmul_dg_gb300 as dg
+    from precision_matmul_dg_gb300 import build as dg_build
+    if rank == 0 or world > 1:
+        dg_build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
-    achieved = flops / (kern_avg_ms * 1e-3) / 1e12
-    if bound == "tensor":
-        peak = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "peak_source": "%s bf16 dense burst (fp16 runs at the bf16 rate)" % peak_src}
-        if base.dtype_a == "i8":
-            roof["unit"] = "TOPS"
-            roof["peak_source"] += ("; INT8 runs on the FP16 tensor path (sm_103a has no "
-                                    "integer tcgen05 MMA), so its denominator is the FP16 peak")
-    else:
-        gbs = algorithmic_bytes(base) / (kern_avg_ms * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(gbs / peak, 4), "peak_source": "%s copy bandwidth" % peak_src}
-    kname = kernel_name(plan, base)
-    roof["kernel"] = kname
-    roof["kernel_avg_us"] = round(kern_avg_ms * 1e3, 2)
-    roof["traffic"] = recorded_traffic(kname, name)
-    roof["algorithmic_bytes"] = algorithmic_bytes(base)
-    roof["algorithmic_flops"] = flops
+    name = args.workload
+    w = Workload(dg, name, dev, args.plan_index)
+    base = w.base
+    total_ms, launches, clocks, ramp_steps = time_workload(w, args, world, local, stream)
+    # The K launches run back to back on one stream (eager or replayed from a
+    # graph), each overlapping the previous one's drain; a launch's average
+    # duration is the timed region over K.
+    kern_avg_ms = total_ms / args.steps
+    total_ms_max = max_over_ranks(total_ms, world)
+    # Throughput unit: TFLOP/s (TOPS for INT8) for tensor-bound workloads,
+    # algorithmic GB/s for the HBM-bound thin ones.
+    work, unit = w.work_unit()
+    value = sum_over_ranks(work * args.steps, world) / (total_ms_max * 1e-3) / 1e12
+    e2e = measure_e2e(w, args, world, stream)
+    roof = roofline(w, kern_avg_ms, peaks, peak_src)
 
     line = {
-        "metric": "GEMM TFLOP/s (INT8 TOPS) and % of GB300 dense peak; GB/s vs HBM for M=1",
+        "metric": METRIC,
         "value": round(value, 2),
         "unit": unit,
         "n_gpus": world,
@@ -524,34 +618,57 @@ def run_dg(args, world, rank, local):
         "vs_baseline": None,
         "dtype": base.dtype_a,
         "data": "synthetic (seeded, recipe in workloads.py)",
-        "config": {"workload": desc, "name": name, "M": base.M, "N": base.N, "K": base.K,
-                   "batch": batch, "alpha": base.alpha, "beta": base.beta,
+        "config": {"workload": w.desc, "name": name, "M": base.M, "N": base.N, "K": base.K,
+                   "batch": base.batch, "alpha": base.alpha, "beta": base.beta,
                    "epilogue": base.epilogue,
                    "ramp": "%d untimed steps (%.1f s) before the warm-up" % (ramp_steps, RAMP_S),
                    "timing": ("CUDA-graph replay of the K steps" if args.graph else
                               "eager back-to-back launches") +
                    ", CUDA events around the K steps, per launch = total / K",
-                   "l2": "%d rotating input sets, %.0f MB > L2" % (nsets, nsets * set_bytes / 1e6)
-                   if nsets > 1 else "inputs larger than L2",
+                   "l2": "%d rotating input sets, %.0f MB > L2" % (w.nsets,
+                                                                   w.nsets * w.set_bytes / 1e6)
+                   if w.nsets > 1 else "inputs larger than L2",
                    "parallelism": "replicas" if world > 1 else "1 GPU",
-                   "plan": {k: plan[k] for k in ("kernel_name", "m_tile", "n_tile", "k_tile",
-                                                 "split_k", "stages", "grid")},
+                   "plan": plan_summary(w.plan),
                    "plan_note": ("the warp-MMA GEMV over the group's problem table (split-K "
                                  "chosen for the largest M)" if base.group_ms is not None else
                                  "the single problem's plan; a batched GEMV picks its split-K "
-                                 "for the whole batch" if batch > 1 else "")},
+                                 "for the whole batch" if base.batch > 1 else "")},
         "roofline": roof,
-        "e2e": {"value": round(e2e_value, 2), "unit": unit,
-                "h2d_bytes_per_step": int(hA.nbytes + hB.nbytes +
-                                          sum(t.nbytes for t in h_scales) +
-                                          (hC.nbytes if hC is not None else 0) +
-                                          (hbias.nbytes if hbias is not None else 0)),
-                "d2h_bytes_per_step": int(hD.nbytes),
-                "call": "%s, %d steps" % (e2e_call, e2e_steps)},
+        "e2e": e2e,
         "gpu_launches": int(launches),
-        "clocks": sampler.summary(),
+        "clocks": clocks,
     }
+    del w
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    names = config_names(args, name)
+    if names:
+        line["configs"] = {}
+        for n in names:
+            line["configs"][n] = measure_config(dg, n, args, world, local, dev, stream, peaks,
+                                                peak_src)
     return line
+
+
+# The further workloads the default run measures after its headline, each
+# with its own value, roofline and clocks: every configuration of the GEMM
+# the library is measured on (square FP16 at three sizes and 256^3, INT8,
+# the two thin M = 1 shapes, W4A16 at M = 16 and 2048, block-scaled FP4).
+DEFAULT_CONFIGS = ("f16_256", "f16_2048", "f16_8192", "i8_4096", "thin_1x4096x131072",
+                   "thin_1x256x12800", "w4a16_m16", "w4a16_m2048", "mxf4_4096")
+
+
+def config_names(args, headline):
+    if args.configs == "none":
+        return []
+    names = DEFAULT_CONFIGS if args.configs == "default" else \
+        tuple(sorted(workloads.WORKLOADS)) if args.configs == "all" else \
+        tuple(n for n in args.configs.split(",") if n)
+    for n in names:
+        if n not in workloads.WORKLOADS:
+            raise SystemExit("unknown workload in --configs: %s" % n)
+    return [n for n in names if n != headline]
 
 
 # --------------------------------------------------------------------------- CPU oracle
@@ -652,7 +769,7 @@ def run_reference(args):
                                                                           case.K, name)
     return {
         "impl": "reference",
-        "metric": "GEMM TFLOP/s (INT8 TOPS) and % of GB300 dense peak; GB/s vs HBM for M=1",
+        "metric": METRIC,
         "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -674,6 +791,10 @@ def main():
     ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
     ap.add_argument("--workload", default="f16_4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", default="default",
+                    help="further workloads measured after the headline into the line's "
+                         "`configs` object: default (every measured configuration), all, "
+                         "none, or a comma-separated list of names")
     ap.add_argument("--plan-index", type=int, default=0,
                     help="run the planner's i-th ranked candidate instead of its first")
     ap.add_argument("--graph", action="store_true",

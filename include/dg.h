@@ -157,6 +157,9 @@ typedef struct {
   int swap_ab;      /* 1: the kernel computes D^T = B^T.A^T (thin-M tensor path) */
   int smem_bytes;   /* dynamic shared memory of the launch */
   int threads;      /* threads per CTA */
+  int regs_per_thread; /* registers per thread the register constraint was checked with: the
+                          kernel's own figure (cudaFuncGetAttributes) when a device is present,
+                          else the planner's upper bound for that kernel */
   int grid;         /* CTAs launched */
   double occupancy; /* wave efficiency: work units / (waves * SMs) */
   double est_us;    /* cost-model time */
@@ -355,17 +358,23 @@ dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_
  * entry point exists for callers that cannot let a library call cudaMalloc
  * (code that runs while a CUDA graph is being captured, runtimes that own all
  * device memory through their own pool, locked-down allocators).
- * Computes exactly what dg_gemm computes, for F16 x F16 with M <= 8, through
- * the split-K GEMV kernel with the same split choice; its FP32 partial sums
- * and arrival counters live in a file-scope static device array of
- * 2 MiB + 64 KiB that every GPU loading the library holds until exit.
+ * Computes the same GEMM as dg_gemm, for F16 x F16 with M <= 8, within the
+ * same error bound, but always through the split-K GEMV kernel on the CUDA
+ * cores with that kernel's own best split.  dg_gemm may choose another
+ * kernel (the warp-MMA GEMV or a tensor-core plan for 2 <= M <= 8) or another
+ * split for the same shape, so the two agree within the bound, not bit for
+ * bit.  The FP32 partial sums and arrival counters live in a file-scope
+ * static device array of 2 MiB + 64 KiB that every GPU loading the library
+ * holds until exit.
  *  - The first call on a device looks the array's device address up with
- *    cudaGetSymbolAddress (once per device, that device current); make that
- *    first call before any stream capture.
+ *    cudaGetSymbolAddress and reads the device's attributes (once per
+ *    device, that device current); make that first call before any stream
+ *    capture.
  *  - Shapes whose split-K partials (split * M * N * 4 bytes) or counters
  *    (ceil(N/8) * 4 bytes) exceed the array are rejected with
- *    DG_ERR_INVALID_ARG and a message; other pairs or M > 8 give
- *    DG_ERR_UNSUPPORTED.
+ *    DG_ERR_INVALID_ARG and a message (a guard: the GEMV's split choice
+ *    stays far below both limits for every M <= 8); other pairs or M > 8
+ *    give DG_ERR_UNSUPPORTED.
  *  - Every call shares the one array and it keeps the last call's contents:
  *    the call clears the counters on `stream` first (cudaMemsetAsync), and
  *    calls that overlap on the GPU (other streams, other host threads) race.

@@ -68,7 +68,8 @@ class TilePlan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("m_tile", ctypes.c_int), ("n_tile", ctypes.c_int),
                 ("k_tile", ctypes.c_int), ("split_k", ctypes.c_int), ("stages", ctypes.c_int),
                 ("cta_group", ctypes.c_int), ("swap_ab", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int), ("grid", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
+                ("regs_per_thread", ctypes.c_int), ("grid", ctypes.c_int),
                 ("occupancy", ctypes.c_double), ("est_us", ctypes.c_double),
                 ("est_tflops", ctypes.c_double)]
 

@@ -71,7 +71,7 @@ def build(force=False, verbose_ptxas=False, quiet=True):
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(r[0] for r in failed))
     tmp = LIB + ".tmp"
-    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + [r[1] for r in results] + ["-lcuda"] * 0
+    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + [r[1] for r in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)

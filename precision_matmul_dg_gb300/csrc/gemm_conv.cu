@@ -482,6 +482,25 @@ cudaError_t run_conv(const GemmArgs& a, const dg_tile_plan& plan) {
 
 // Shapes compiled for the converting kernels; the planner proposes only these.
 // (N_tile, input slots, converted slots) per dtype pair.
+namespace {
+template <int BN, int Stages, int CvStages, int OpA, int OpB, int Out>
+int conv_regs_of() {
+  static std::atomic<int> slot{-1};
+  return kernel_regs(gemm_conv_tc_kernel<BN, Stages, CvStages, OpA, OpB, Out>, slot);
+}
+}  // namespace
+
+int conv_kernel_regs(dg_dtype da, dg_dtype db, int n_tile, int stages) {
+  if (da == DG_I8 && db == DG_I8) {
+    if (n_tile == 128 && stages == 8) return conv_regs_of<128, 8, 3, kOpI8, kOpI8, kOutI32>();
+  } else if (da == DG_F16 && db == DG_E2M1) {
+    if (n_tile == 256 && stages == 6) return conv_regs_of<256, 6, 2, kOpF16, kOpE2M1, kOutF16>();
+    if (n_tile == 128 && stages == 8) return conv_regs_of<128, 8, 3, kOpF16, kOpE2M1, kOutF16>();
+    if (n_tile == 64 && stages == 8) return conv_regs_of<64, 8, 4, kOpF16, kOpE2M1, kOutF16>();
+  }
+  return 0;
+}
+
 cudaError_t launch_conv(const GemmArgs& a, const dg_tile_plan& plan) {
   if (a.dtype_a == DG_I8 && a.dtype_b == DG_I8) {
     if (plan.n_tile == 128 && plan.stages == 8)

@@ -757,7 +757,32 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   return e;
 }
 
+template <int BN, int Stages, int CG, int Out>
+int regs_of() {
+  static std::atomic<int> slot{-1};
+  return kernel_regs(gemm_f16_tc_kernel<BN, Stages, CG, Out>, slot);
+}
+
 }  // namespace
+
+int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32) {
+  if (exact_i32) {
+    if (n_tile == 192 && cta_group == 2 && stages == 6) return regs_of<192, 6, 2, kOutI32>();
+    if (n_tile == 128 && cta_group == 1 && stages == 6) return regs_of<128, 6, 1, kOutI32>();
+    return 0;
+  }
+  if (cta_group == 2) {
+    if (n_tile == 256 && stages == 6) return regs_of<256, 6, 2, kOutF16>();
+    if (n_tile == 224 && stages == 6) return regs_of<224, 6, 2, kOutF16>();
+    if (n_tile == 192 && stages == 6) return regs_of<192, 6, 2, kOutF16>();
+    if (n_tile == 128 && stages == 8) return regs_of<128, 8, 2, kOutF16>();
+    return 0;
+  }
+  if (n_tile == 256 && stages == 4) return regs_of<256, 4, 1, kOutF16>();
+  if (n_tile == 128 && stages == 6) return regs_of<128, 6, 1, kOutF16>();
+  if (n_tile == 64 && stages == 8) return regs_of<64, 8, 1, kOutF16>();
+  return 0;
+}
 
 // Tile shapes compiled into the library; the planner only proposes these.
 // `a` holds FP16 operands (the caller's, or widened copies) or, with

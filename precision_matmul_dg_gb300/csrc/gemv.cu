@@ -468,6 +468,20 @@ int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N, int64_t batch) {
   return plan.split_k > 1 ? (N + kGemvWarps - 1) / kGemvWarps * batch : 0;
 }
 
+int gemv_kernel_regs(int64_t M) {
+  static std::atomic<int> slot[4] = {{-1}, {-1}, {-1}, {-1}};
+  if (M <= 1) return kernel_regs(gemv_splitk_kernel<1>, slot[0]);
+  if (M <= 2) return kernel_regs(gemv_splitk_kernel<2>, slot[1]);
+  if (M <= 4) return kernel_regs(gemv_splitk_kernel<4>, slot[2]);
+  return kernel_regs(gemv_splitk_kernel<kGemvMaxM>, slot[3]);
+}
+
+int gemv_mma_kernel_regs(int64_t M) {
+  static std::atomic<int> slot[2] = {{-1}, {-1}};
+  return M <= 8 ? kernel_regs(gemv_mma_kernel<8>, slot[0])
+                : kernel_regs(gemv_mma_kernel<16>, slot[1]);
+}
+
 cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws) {
   GemvParams p;
   p.M = static_cast<int>(a.M);
@@ -654,24 +668,34 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocCounter
 namespace {
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+dg_hw_desc g_noalloc_hw[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch array on `dev` (which must be current).  The
-// host-side name of the array is only a stand-in, so the address is looked up
-// once per device with cudaGetSymbolAddress.
-dg_status noalloc_scratch(int dev, void** out) {
+// Device address of the scratch array on `dev` (which must be current) and
+// that device's description.  The host-side name of the array is only a
+// stand-in, so the address is looked up once per device with
+// cudaGetSymbolAddress; the description (a dozen attribute queries) is
+// filled at the same time, so later calls make no query at all.
+dg_status noalloc_setup(int dev, void** out, dg_hw_desc* hw) {
   if (dev < 0 || dev >= kNoAllocMaxDevices)
     return set_error(DG_ERR_INVALID_STATE, "device index beyond the scratch table");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_addr[dev]) {
+    dg_hw_desc h{};
+    const dg_status s = fill_hw_desc(dev, &h);
+    if (s != DG_OK) return s;
+    if (h.cc_major != 10 || h.cc_minor != 3)
+      return set_error(DG_ERR_INVALID_STATE, "libdg is built for sm_103a (GB300) only");
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p) {
       cudaGetLastError();
       return set_error(DG_ERR_CUDA, "cudaGetSymbolAddress of the static split-K scratch failed");
     }
+    g_noalloc_hw[dev] = h;
     g_noalloc_addr[dev] = p;
   }
   *out = g_noalloc_addr[dev];
+  *hw = g_noalloc_hw[dev];
   return DG_OK;
 }
 }  // namespace
@@ -699,12 +723,12 @@ extern "C" dg_status dg_gemm_thin_noalloc(int64_t M, int64_t N, int64_t K, dg_dt
     return set_error(DG_ERR_INVALID_STATE, "no current CUDA device");
   }
   dg_hw_desc hw{};
-  s = fill_hw_desc(dev, &hw);
+  void* scratch = nullptr;
+  s = noalloc_setup(dev, &scratch, &hw);
   if (s != DG_OK) return s;
-  if (hw.cc_major != 10 || hw.cc_minor != 3)
-    return set_error(DG_ERR_INVALID_STATE, "libdg is built for sm_103a (GB300) only");
 
-  // Same split-K choice as the planner's GEMV candidates.
+  // The split-K GEMV's own best split (the fastest GEMV candidate of the
+  // planner; dg_gemm may pick another kernel or split for the same shape).
   int64_t chunk = 0;
   const int split = gemv_best_split(M, N, K, hw, &chunk);
   const int64_t row_groups = (N + kGemvWarps - 1) / kGemvWarps;
@@ -721,9 +745,6 @@ extern "C" dg_status dg_gemm_thin_noalloc(int64_t M, int64_t N, int64_t K, dg_dt
     return set_error(DG_ERR_INVALID_ARG, msg);
   }
 
-  void* scratch = nullptr;
-  s = noalloc_scratch(dev, &scratch);
-  if (s != DG_OK) return s;
   unsigned* counters = static_cast<unsigned*>(scratch);
   float* partial =
       reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + kNoAllocCounterBytes);

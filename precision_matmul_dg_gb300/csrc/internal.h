@@ -68,6 +68,24 @@ cudaError_t once_per_device(std::atomic<uint64_t>& done, int dev, F&& init) {
   return e;
 }
 
+// Registers per thread that ptxas gave `kern`, read once with
+// cudaFuncGetAttributes and kept in `slot` (which starts at -1).  0 when no
+// device is present to read them from; the planner then uses its bound.
+template <typename Kern>
+int kernel_regs(Kern kern, std::atomic<int>& slot) {
+  int v = slot.load(std::memory_order_acquire);
+  if (v >= 0) return v;
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(kern)) == cudaSuccess) {
+    v = fa.numRegs;
+  } else {
+    cudaGetLastError();
+    v = 0;
+  }
+  slot.store(v, std::memory_order_release);
+  return v;
+}
+
 // Everything a launcher needs to run one GEMM, already validated.
 struct GemmArgs {
   int64_t M, N, K;
@@ -102,6 +120,17 @@ struct GemmArgs {
   const void* scale_b = nullptr;
   int64_t lds_b = 0;
 };
+
+// Measured registers per thread of the kernel a plan would launch (0 when
+// they cannot be read: no device).  FP16 tensor-core kernel (gemm_tc.cu;
+// exact_i32: its INT32 output mode), converting kernel (gemm_conv.cu),
+// split-K GEMV and warp-MMA GEMV for M rows (gemv.cu), skinny W4A16 kernel
+// (skinny.cu).  0 too for a variant that is not compiled.
+int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32);
+int conv_kernel_regs(dg_dtype da, dg_dtype db, int n_tile, int stages);
+int gemv_kernel_regs(int64_t M);
+int gemv_mma_kernel_regs(int64_t M);
+int skinny_kernel_regs();
 
 // Planner (planner.cpp) -- host only.
 dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,

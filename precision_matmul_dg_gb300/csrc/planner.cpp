@@ -51,7 +51,10 @@ constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;
 constexpr int kTcThreads = 384;      // FP16 x FP16 kernel (eight epilogue warps)
 constexpr int kConvThreads = 384;    // converting kernel (adds four converter warps)
-constexpr int kTcRegsPerThread = 168;  // upper bound of what ptxas assigns these kernels
+// Registers per thread: the kernels' own figures (cudaFuncGetAttributes) when
+// a device is present to read them from, else these upper bounds of what
+// ptxas assigns them.
+constexpr int kTcRegsPerThread = 168;
 constexpr int kTcBarrierBytes = 512;
 
 struct TcFamily {
@@ -186,8 +189,12 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
       if (why) *why += name + ": tensor memory; ";
       continue;
     }
-    if (kTcRegsPerThread > hw.regs_per_thread_max ||
-        kTcRegsPerThread * fam.threads > hw.regs_per_sm) {
+    const int measured = (ka == DG_F16 && kb == DG_F16)
+                             ? tc_kernel_regs(v.n_tile, v.stages, v.cta_group,
+                                              widened && da == DG_I8)
+                             : conv_kernel_regs(ka, kb, v.n_tile, v.stages);
+    const int regs = measured > 0 ? measured : kTcRegsPerThread;
+    if (regs > hw.regs_per_thread_max || regs * fam.threads > hw.regs_per_sm) {
       if (why) *why += name + ": registers; ";
       continue;
     }
@@ -224,6 +231,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     p.swap_ab = 0;
     p.smem_bytes = smem;
     p.threads = fam.threads;
+    p.regs_per_thread = regs;
     p.grid = static_cast<int>(std::min<int64_t>(tiles, units) * v.cta_group);
     p.occupancy = occ;
     p.est_us = std::max(t_math, t_mem) + t_epi + 2.0 + t_pre;
@@ -243,7 +251,9 @@ void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype 
     if (why) *why += "GEMV: M > 8; ";
     return;
   }
-  if (kGemvRegsPerThread * kGemvThreads > hw.regs_per_sm) {
+  const int measured = gemv_kernel_regs(M);
+  const int regs = measured > 0 ? measured : kGemvRegsPerThread;
+  if (regs * kGemvThreads > hw.regs_per_sm) {
     if (why) *why += "GEMV: registers; ";
     return;
   }
@@ -270,6 +280,7 @@ void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype 
     p.swap_ab = 0;
     p.smem_bytes = 0;
     p.threads = kGemvThreads;
+    p.regs_per_thread = regs;
     p.grid = static_cast<int>(ceil_div(N, kGemvWarps) * split);
     p.occupancy = occ;
     p.est_us = t;
@@ -286,6 +297,11 @@ constexpr int kGemvMmaCols = 64;
 constexpr int kGemvMmaThreads = 256;
 constexpr int kGemvMmaRegsPerThread = 80;  // upper bound of what ptxas assigns the kernel
 
+int gemv_mma_regs(int64_t M) {
+  const int measured = gemv_mma_kernel_regs(M);
+  return measured > 0 ? measured : kGemvMmaRegsPerThread;
+}
+
 void add_gemv_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
                              const dg_hw_desc& hw, double target, std::vector<dg_tile_plan>* out,
                              std::string* why) {
@@ -294,7 +310,8 @@ void add_gemv_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dt
     if (why) *why += "warp-MMA GEMV: M outside [2, 16]; ";
     return;
   }
-  const int ctas = hw.regs_per_sm / (kGemvMmaRegsPerThread * kGemvMmaThreads);
+  const int regs = gemv_mma_regs(M);
+  const int ctas = hw.regs_per_sm / (regs * kGemvMmaThreads);
   if (ctas < 1) {
     if (why) *why += "warp-MMA GEMV: registers; ";
     return;
@@ -321,6 +338,7 @@ void add_gemv_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dt
     p.cta_group = 1;
     p.smem_bytes = 0;
     p.threads = kGemvMmaThreads;
+    p.regs_per_thread = regs;
     p.grid = static_cast<int>(ceil_div(N, kGemvMmaCols) * split);
     p.occupancy = occ;
     p.est_us = t;
@@ -353,7 +371,9 @@ void add_skinny_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtyp
     return;
   }
   const int threads = skinny_threads();
-  if (kSkinnyRegsPerThread * threads > hw.regs_per_sm) {
+  const int measured = skinny_kernel_regs();
+  const int regs = measured > 0 ? measured : kSkinnyRegsPerThread;
+  if (regs * threads > hw.regs_per_sm) {
     if (why) *why += "skinny: registers; ";
     return;
   }
@@ -385,6 +405,7 @@ void add_skinny_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtyp
   p.swap_ab = 0;
   p.smem_bytes = smem;
   p.threads = threads;
+  p.regs_per_thread = regs;
   p.grid = static_cast<int>(blocks);
   p.occupancy = occ;
   p.est_us = t;
@@ -435,6 +456,7 @@ void add_warp_mma_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, const
         p.cta_group = 1;
         p.smem_bytes = smem;
         p.threads = threads;
+        p.regs_per_thread = regs;
         p.grid = static_cast<int>(std::min<int64_t>(tiles, slots));
         p.occupancy = occ;
         p.est_us = std::max(t_math, t_l2) + 2.0;
@@ -479,7 +501,7 @@ double gemv_mma_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg
   const int64_t chunk = ceil_div(ceil_div(kk, split), 256) * 256;
   if (split > 1 && chunk * (split - 1) >= kk) return -1.0;
   if (chunk_out) *chunk_out = chunk;
-  const int ctas = std::max(1, hw.regs_per_sm / (kGemvMmaRegsPerThread * kGemvMmaThreads));
+  const int ctas = std::max(1, hw.regs_per_sm / (gemv_mma_regs(M) * kGemvMmaThreads));
   const int64_t resident = static_cast<int64_t>(hw.sm_count) * ctas * (kGemvMmaThreads / 32);
   const int64_t units = ceil_div(N, 8) * split * batch;  // warps
   // A warp keeps 8 rows x 8 steps x 64 bytes = 4 KB in flight; measured on

@@ -224,6 +224,10 @@ int skinny_smem_bytes() { return kSkSmem; }
 int skinny_threads() { return kSkThreads; }
 int skinny_cols_per_block() { return kSkCols; }
 int skinny_k_chunk() { return kSkChunk; }
+int skinny_kernel_regs() {
+  static std::atomic<int> slot{-1};
+  return kernel_regs(skinny_w4a16_kernel, slot);
+}
 
 cudaError_t launch_skinny(const GemmArgs& a, const dg_tile_plan& plan) {
   (void)plan;

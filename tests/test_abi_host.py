@@ -62,7 +62,7 @@ def test_struct_layout_matches_c(dg, tmp_path):
           printf("kernels %d,%d,%d,%d,%d\\n", DG_KERNEL_TC, DG_KERNEL_GEMV, DG_KERNEL_TC_WIDENED,
                  DG_KERNEL_SKINNY, DG_KERNEL_GEMV_MMA);
           F(dg_hw_desc, l2_bytes) F(dg_hw_desc, hbm_gbps) F(dg_hw_desc, clock_ghz)
-          F(dg_tile_plan, grid) F(dg_tile_plan, occupancy) F(dg_tile_plan, est_tflops)
+          F(dg_tile_plan, regs_per_thread) F(dg_tile_plan, grid) F(dg_tile_plan, occupancy) F(dg_tile_plan, est_tflops)
           F(dg_epilogue_op, a) F(dg_epilogue_op, b) F(dg_epilogue_program, ops)
           return 0;
         }

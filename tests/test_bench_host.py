@@ -40,3 +40,22 @@ def test_oracle_rows_of_the_mxf4_step():
     full = oracle.gemm_mx_reference(oracle.pack_e2m1(codes), scales, case.B, case.scale_b,
                                     case.K, C=case.C, alpha=case.alpha, beta=case.beta)
     np.testing.assert_array_equal(got, full[rows])
+
+
+def test_default_configs_cover_every_measured_configuration():
+    # the default line measures the headline plus every configuration of the
+    # GEMM (square FP16 at four sizes, INT8, both thin shapes, W4A16 at both
+    # M, MXFP4), each once
+    class A:
+        configs = "default"
+    names = bench.config_names(A, "f16_4096")
+    assert sorted(names + ["f16_4096"]) == sorted(
+        ["f16_256", "f16_2048", "f16_4096", "f16_8192", "i8_4096", "thin_1x4096x131072",
+         "thin_1x256x12800", "w4a16_m16", "w4a16_m2048", "mxf4_4096"])
+    A.configs = "none"
+    assert bench.config_names(A, "f16_4096") == []
+    A.configs = "thin_1x256x12800,f16_4096"
+    assert bench.config_names(A, "f16_4096") == ["thin_1x256x12800"]
+    A.configs = "nonesuch"
+    with pytest.raises(SystemExit):
+        bench.config_names(A, "f16_4096")

@@ -125,7 +125,9 @@ def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
             assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], cg)
             assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
             assert 2 * p["n_tile"] <= GB300["tmem_cols"]
-            assert p["threads"] * 168 <= GB300["regs_per_sm"]
+            # the kernel's measured registers with a device, else the bound 168
+            assert 0 < p["regs_per_thread"] <= 168
+            assert p["threads"] * p["regs_per_thread"] <= GB300["regs_per_sm"]
             tiles = math.ceil(M / (128 * cg)) * math.ceil(N / p["n_tile"])
             assert p["grid"] == cg * min(tiles, GB300["sm_count"] // cg)
             assert p["m_tile"] == 128 * cg and p["k_tile"] == 64 and p["split_k"] == 1
@@ -291,3 +293,21 @@ def test_mxf4_plans_are_widened(dg):
         with pytest.raises(dg.DgError) as ei:
             dg.plan_tiles(64, 64, 64, *pair, hw=GB300)
         assert ei.value.name == "DG_ERR_UNSUPPORTED"
+
+
+def test_noalloc_scratch_covers_every_gemv_split(dg):
+    # dg_gemm_thin_noalloc keeps its split-K partials (split * M * N * 4 bytes)
+    # and counters (ceil(N / 8) * 4 bytes) in a static array of 2 MiB + 64 KiB
+    # and rejects shapes beyond it.  The GEMV's best split (its fastest
+    # candidate) stays far below both limits over thin shapes from tiny to huge.
+    worst = 0.0
+    for M in (1, 2, 4, 8):
+        for N in (8, 64, 256, 1024, 4096, 16384, 65536, 131072, 262144):
+            for K in (256, 4096, 65536, 1048576, 4194304):
+                cands = [p for p in dg.plan_tiles(M, N, K, hw=GB300, target_occupancy=0.0)
+                         if p["kernel"] == 1]  # DG_KERNEL_GEMV
+                best = min(cands, key=lambda p: p["est_us"])
+                if best["split_k"] > 1:
+                    worst = max(worst, best["split_k"] * M * N * 4 / (2 << 20))
+                    assert (N + 7) // 8 * 4 <= 64 << 10
+    assert worst <= 0.25
