@@ -181,7 +181,7 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "gemm_f16_tc_kernel": ("gemm_tc.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh",
+    "gemm_tc_kernel": ("gemm_tc.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh",
                            "internal.h"),
     "gemm_conv_tc_kernel": ("gemm_conv.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh",
                             "internal.h"),
@@ -258,16 +258,18 @@ def algorithmic_bytes(case):
 
 
 def kernel_name(plan, case):
-    """The step's dominant kernel: the split-K GEMV, the FP16 tensor-core
-    kernel (also for widened INT8 / E2M1 operands) or the converting kernel."""
+    """The step's dominant kernel: the split-K GEMV, the tensor-core kernel
+    (FP16; widened INT8 / E2M1 / MXFP4 operands; MXFP4 on the block-scaled
+    MMA) or the converting kernel."""
     if plan["kernel_name"] == "gemv":
         return "gemv_splitk_kernel"
     if plan["kernel_name"] == "skinny":
         return "skinny_w4a16_kernel"
     if plan["kernel_name"] == "gemv_mma":
         return "gemv_mma_kernel"
-    if plan["kernel_name"] == "tc_widened" or (case.dtype_a == "f16" and case.dtype_b == "f16"):
-        return "gemm_f16_tc_kernel"
+    if plan["kernel_name"] == "tc_widened" or case.dtype_a == "mxf4" or \
+            (case.dtype_a == "f16" and case.dtype_b == "f16"):
+        return "gemm_tc_kernel"
     return "gemm_conv_tc_kernel"
 
 
@@ -346,7 +348,7 @@ class Workload:
             dg.quantize_mxf4_raw(base.M, base.K, A, A.stride(0), self.QA, self.ldq, self.QS,
                                  self.nblk, stream=st)
             dg.gemm_mxf4(self.QA, self.QS, B, SB, C, base.K, bias=bias, alpha=base.alpha,
-                         beta=base.beta, epilogue=base.epilogue, stream=st)
+                         beta=base.beta, epilogue=base.epilogue, stream=st, plan=self.forced)
             return
         if base.batch > 1:
             dg.gemm_batched(A, B, C, K=base.K, bias=bias, alpha=base.alpha, beta=base.beta,

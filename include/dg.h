@@ -112,7 +112,8 @@ typedef struct {
 
 /* Kernel families a plan can select. */
 typedef enum {
-  DG_KERNEL_TC = 0,    /* tensor-core pipeline: TMA -> SMEM ring -> tcgen05.mma -> TMEM -> fused epilogue */
+  DG_KERNEL_TC = 0,    /* tensor-core pipeline: TMA -> SMEM ring -> tcgen05.mma -> TMEM -> fused
+                          epilogue (MXFP4: packed codes on the block-scaled kind::mxf4 MMA) */
   DG_KERNEL_GEMV = 1,  /* thin-M split-K streaming kernel on the CUDA cores */
   DG_KERNEL_TC_WIDENED = 2, /* int8 / E2M1 operands widened to FP16 by a streaming pre-pass into
                                a library workspace, then the FP16 tensor-core kernel (INT8:
@@ -330,14 +331,20 @@ dg_status dg_quantize_mxf4(int64_t rows, int64_t K, const void *X, int64_t ldx, 
  * e the scale byte of block k / 32 (255: NaN for the whole block).
  * Products are summed in FP32; C, D (one buffer, M x N, leading dimension N,
  * FP16), bias, the epilogue, alpha and beta are as in dg_gemm.
- * Runs the plan dg_plan_tiles gives for the pair DG_MXF4 x DG_MXF4: both
- * operands are widened with their scales into a BF16 copy in a
- * per-(device, stream) workspace (exact: each value has at most two
- * significant bits and BF16 keeps FP32's exponent range; scale bytes above
- * 251 may overflow to an infinity), then the tensor-core kernel multiplies
- * the BF16 copies with kind::f16 MMAs and FP32 accumulation.
+ * Runs the plan dg_plan_tiles gives for the pair DG_MXF4 x DG_MXF4:
+ *  - DG_KERNEL_TC (K even): the codes go to the tensor cores as stored, on
+ *    block-scaled kind::mxf4 MMAs with FP32 accumulation; one small launch
+ *    first packs both operands' scales into the order the kernel copies into
+ *    tensor memory (a per-(device, stream) workspace of about
+ *    (M + N) * K / 256 bytes).  Codes past K (and, for the scales, blocks
+ *    past ceil(K / 32)) are never read.
+ *  - DG_KERNEL_TC_WIDENED (any K; the only plan for odd K): both operands
+ *    are widened with their scales into a BF16 copy in that workspace (exact:
+ *    each value has at most two significant bits and BF16 keeps FP32's
+ *    exponent range; scale bytes above 251 may overflow to an infinity),
+ *    then kind::f16 MMAs multiply the copies.
  * M == 0 or N == 0 is a no-op; K == 0 gives epilogue(beta * C).
- * The BF16 workspace grows with cudaMalloc the first time a shape needs it:
+ * The workspace grows with cudaMalloc the first time a shape needs it:
  * under CUDA-graph capture, make one call of the same shape on the
  * capturing stream before capture begins.
  * Errors: as dg_gemm, plus DG_ERR_INVALID_ARG for NULL or misaligned scale
@@ -346,6 +353,20 @@ dg_status dg_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void *A, int64_t l
                        const void *scale_a, int64_t lds_a, const void *B, int64_t ldb,
                        const void *scale_b, int64_t lds_b, void *C, const void *bias, float alpha,
                        float beta, dg_epilogue epilogue, dg_stream_t stream);
+
+/* As dg_gemm_mxf4, but runs `plan` (one returned by dg_plan_tiles for the
+ * same M, N, K and the pair DG_MXF4 x DG_MXF4): DG_KERNEL_TC is the
+ * block-scaled MMA on the packed codes, DG_KERNEL_TC_WIDENED the BF16
+ * widening.  The pages' planner hands its chosen tile to the generated
+ * kernel the same way (kwkr.cn/news/562171, section 3.2 steps 2 and 4).
+ * DG_ERR_INVALID_STATE when the plan does not fit (e.g. a DG_KERNEL_TC plan
+ * with an odd K); DG_ERR_INVALID_ARG for a NULL plan; otherwise as
+ * dg_gemm_mxf4. */
+dg_status dg_gemm_mxf4_planned(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                               const void *scale_a, int64_t lds_a, const void *B, int64_t ldb,
+                               const void *scale_b, int64_t lds_b, void *C, const void *bias,
+                               float alpha, float beta, dg_epilogue epilogue,
+                               const dg_tile_plan *plan, dg_stream_t stream);
 
 /* As dg_gemm, but runs `plan` (one returned by dg_plan_tiles for the same
  * M, N, K and dtypes).  DG_ERR_INVALID_STATE when the plan does not fit. */

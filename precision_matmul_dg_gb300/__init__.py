@@ -33,7 +33,7 @@ KERNELS = {0: "tc", 1: "gemv", 2: "tc_widened", 3: "skinny", 4: "gemv_mma", -1: 
 # Every symbol include/dg.h declares.
 EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_gemm_host",
            "dg_gemm_ex", "dg_gemm_strided_batched", "dg_gemm_grouped",
-           "dg_quantize_mxf4", "dg_gemm_mxf4",
+           "dg_quantize_mxf4", "dg_gemm_mxf4", "dg_gemm_mxf4_planned",
            "dg_gemm_thin_noalloc", "dg_last_error",
            "dg_check_status", "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout",
            "dg_launch_count", "dg_shutdown"]
@@ -138,6 +138,8 @@ def lib():
     L.dg_quantize_mxf4.argtypes = [i64, i64, vp, i64, vp, i64, vp, i64, vp]
     L.dg_gemm_mxf4.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, f32,
                                f32, i32, vp]
+    L.dg_gemm_mxf4_planned.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, vp,
+                                       f32, f32, i32, ctypes.POINTER(TilePlan), vp]
     L.dg_last_error.restype = ctypes.c_char_p
     L.dg_last_error.argtypes = []
     L.dg_check_status.argtypes = [vp]
@@ -148,7 +150,7 @@ def lib():
     L.dg_shutdown.argtypes = []
     for name in ("dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned",
                  "dg_gemm_thin_noalloc", "dg_gemm_host", "dg_gemm_ex", "dg_gemm_strided_batched",
-                 "dg_gemm_grouped", "dg_quantize_mxf4", "dg_gemm_mxf4",
+                 "dg_gemm_grouped", "dg_quantize_mxf4", "dg_gemm_mxf4", "dg_gemm_mxf4_planned",
                  "dg_check_status",
                  "dg_set_wait_timeout_ns", "dg_selftest_wait_timeout", "dg_shutdown"):
         getattr(L, name).restype = ctypes.c_int
@@ -202,11 +204,7 @@ def gemm_raw(M, N, K, dtype_a, dtype_b, A, lda, B, ldb, C, bias, alpha, beta, ep
     if plan is None:
         _check(L.dg_gemm(*args, s))
     else:
-        if isinstance(plan, dict):
-            p = TilePlan(**{k: v for k, v in plan.items() if k in dict(TilePlan._fields_)})
-        else:
-            p = plan
-        _check(L.dg_gemm_planned(*args, ctypes.byref(p), s))
+        _check(L.dg_gemm_planned(*args, ctypes.byref(_as_plan(plan)), s))
 
 
 _TORCH_DTYPES = None
@@ -300,22 +298,35 @@ def quantize_mxf4(X, K=None, stream=None):
     return codes, scales
 
 
+def _as_plan(plan):
+    if isinstance(plan, dict):
+        return TilePlan(**{k: v for k, v in plan.items() if k in dict(TilePlan._fields_)})
+    return plan
+
+
 def gemm_mxf4_raw(M, N, K, A, lda, scale_a, lds_a, B, ldb, scale_b, lds_b, C, bias, alpha, beta,
-                  epilogue="none", stream=None):
-    """dg_gemm_mxf4 with the C argument order (lda, ldb in codes)."""
+                  epilogue="none", stream=None, plan=None):
+    """dg_gemm_mxf4 (dg_gemm_mxf4_planned with a plan) with the C argument
+    order (lda, ldb in codes)."""
     epi = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
-    _check(lib().dg_gemm_mxf4(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(scale_a),
-                              int(lds_a), _ptr(B), int(ldb), _ptr(scale_b), int(lds_b), _ptr(C),
-                              _ptr(bias), float(alpha), float(beta), epi,
-                              _stream_handle(stream)))
+    args = (int(M), int(N), int(K), _ptr(A), int(lda), _ptr(scale_a), int(lds_a), _ptr(B),
+            int(ldb), _ptr(scale_b), int(lds_b), _ptr(C), _ptr(bias), float(alpha), float(beta),
+            epi)
+    if plan is None:
+        _check(lib().dg_gemm_mxf4(*args, _stream_handle(stream)))
+    else:
+        _check(lib().dg_gemm_mxf4_planned(*args, ctypes.byref(_as_plan(plan)),
+                                          _stream_handle(stream)))
 
 
 def gemm_mxf4(A, scale_a, B, scale_b, C, K, bias=None, alpha=1.0, beta=0.0, epilogue="none",
-              stream=None):
+              stream=None, plan=None):
     """D = epilogue(alpha * A.B + beta * C) for MXFP4 A and B, written into C.
 
     A: uint8 [M, lda / 2] packed codes with scale_a uint8 [M, >= ceil(K/32)];
     B: uint8 [N, ldb / 2] with scale_b [N, ...]; C: fp16 [M, N] dense.
+    plan: a dg_plan_tiles candidate for (M, N, K, "mxf4", "mxf4") to run
+    instead of the planner's first.
     """
     for t, what in ((A, "A"), (B, "B"), (scale_a, "scale_a"), (scale_b, "scale_b")):
         _expect(t, "e2m1", what)
@@ -326,7 +337,7 @@ def gemm_mxf4(A, scale_a, B, scale_b, C, K, bias=None, alpha=1.0, beta=0.0, epil
     if C.stride(0) != N:
         raise ValueError("C must be dense row-major (leading dimension N)")
     gemm_mxf4_raw(M, N, K, A, 2 * A.stride(0), scale_a, scale_a.stride(0), B, 2 * B.stride(0),
-                  scale_b, scale_b.stride(0), C, bias, alpha, beta, epilogue, stream)
+                  scale_b, scale_b.stride(0), C, bias, alpha, beta, epilogue, stream, plan)
     return C
 
 

@@ -490,6 +490,20 @@ dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev) {
   cudaError_t e = cudaSuccess;
   if (plan.kernel == DG_KERNEL_SKINNY) {
     e = launch_skinny(a, plan);
+  } else if (plan.kernel == DG_KERNEL_TC && da == DG_MXF4) {
+    // MXFP4 on the block-scaled MMA: the codes go to the tensor cores as
+    // they are; the scales are first packed into the order the kernel
+    // copies into tensor memory.
+    const int64_t bytes = pack_mx_scales_bytes(M, N, K, plan.n_tile);
+    __half* packed = nullptr;
+    s = get_wide_workspace(dev, stream, (bytes + 1) / 2, &packed);
+    if (s != DG_OK) return s;
+    e = launch_pack_mx_scales(M, N, K, plan.n_tile, a.scale_a, a.lds_a, a.scale_b, a.lds_b,
+                              packed, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "scale packing launch");
+    GemmArgs w = a;
+    w.sf_packed = packed;
+    e = launch_tc_mx(w, plan);
   } else if (plan.kernel == DG_KERNEL_TC) {
     e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC_WIDENED && da == DG_MXF4) {
@@ -585,7 +599,8 @@ dg_status run_quantize_mxf4(int64_t rows, int64_t K, const void* X, int64_t ldx,
 dg_status run_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                         const void* scale_a, int64_t lds_a, const void* B, int64_t ldb,
                         const void* scale_b, int64_t lds_b, void* C, const void* bias,
-                        float alpha, float beta, dg_epilogue epilogue, cudaStream_t stream) {
+                        float alpha, float beta, dg_epilogue epilogue, const dg_tile_plan* forced,
+                        cudaStream_t stream) {
   EpiSpec epi;
   dg_status s = fixed_epilogue(epilogue, &epi);
   if (s != DG_OK) return s;
@@ -648,8 +663,15 @@ dg_status run_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     return e == cudaSuccess ? DG_OK : fail_cuda(e, "epilogue-only launch");
   }
   dg_tile_plan plan{};
-  s = cached_plan(dev, M, N, K, DG_MXF4, DG_MXF4, st->hw, &plan);
-  if (s != DG_OK) return s;
+  if (forced) {
+    std::string why;
+    if (!plan_is_runnable(*forced, M, N, K, DG_MXF4, DG_MXF4, &why))
+      return fail(DG_ERR_INVALID_STATE, "plan not runnable: %s", why.c_str());
+    plan = *forced;
+  } else {
+    s = cached_plan(dev, M, N, K, DG_MXF4, DG_MXF4, st->hw, &plan);
+    if (s != DG_OK) return s;
+  }
   return dispatch(a, plan, dev);
 }
 
@@ -984,7 +1006,18 @@ dg_status dg_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                        float beta, dg_epilogue epilogue, dg_stream_t stream) {
   clear_error();
   return run_gemm_mxf4(M, N, K, A, lda, scale_a, lds_a, B, ldb, scale_b, lds_b, C, bias, alpha,
-                       beta, epilogue, reinterpret_cast<cudaStream_t>(stream));
+                       beta, epilogue, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_gemm_mxf4_planned(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                               const void* scale_a, int64_t lds_a, const void* B, int64_t ldb,
+                               const void* scale_b, int64_t lds_b, void* C, const void* bias,
+                               float alpha, float beta, dg_epilogue epilogue,
+                               const dg_tile_plan* plan, dg_stream_t stream) {
+  clear_error();
+  if (!plan) return fail(DG_ERR_INVALID_ARG, "plan is null");
+  return run_gemm_mxf4(M, N, K, A, lda, scale_a, lds_a, B, ldb, scale_b, lds_b, C, bias, alpha,
+                       beta, epilogue, plan, reinterpret_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_gemm_planned(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,

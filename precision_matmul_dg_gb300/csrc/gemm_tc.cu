@@ -1,4 +1,6 @@
-// Dense FP16 GEMM on the 5th-generation tensor cores (tcgen05) of sm_103a.
+// Dense GEMM on the 5th-generation tensor cores (tcgen05) of sm_103a: FP16
+// (or BF16) operands on kind::f16, and block-scaled 4-bit operands (MXFP4:
+// E2M1 codes with an E8M0 scale per 32 values along K) on kind::mxf4.
 //
 //   D[M x N] = epilogue(alpha * A[M x K] . B[N x K]^T + beta * C)
 //
@@ -29,6 +31,17 @@
 //   commits arrive on the barriers of both CTAs.  Every A and B tile is read
 //   from L2 once per pair instead of once per CTA, halving L2->SM traffic per
 //   FLOP, and each SM's shared memory feeds half of the B operand.
+//
+// MXFP4 (single CTAs): a stage holds 128 bytes of packed codes per row (256
+// values of K, as 16-bit stages hold 64), loaded by TMA as bytes into the
+// same swizzled slots, plus the stage's E8M0 scales, which a pre-pass packed
+// into 16-byte lines and one bulk copy per operand brings in.  The MMA
+// thread copies the scales into tensor memory (tcgen05.cp, in issue order
+// with its MMAs) and issues four block-scaled MMAs of K = 64 per stage: the
+// 4-bit codes reach the tensor cores as they are stored, with no 16-bit
+// copy (discosf.com/news/5532976, section 4.3: packed 4-bit weights instead
+// of an FP16 emulation; section 2.2, layer 2: each precision in the tensor
+// core's own format).
 //
 // The kernel is persistent (one CTA / pair per SM / SM pair walks the tile
 // list), and the two TMEM accumulators let the epilogue of tile i overlap the
@@ -67,7 +80,14 @@ struct TcParams {
   void* D;
   int64_t ldd;
   const __half* bias;
-  int32_t alpha_i, beta_i;  // integer scalars of the INT32 output
+  union {
+    struct {
+      int32_t alpha_i, beta_i;  // integer scalars of the INT32 output
+    };
+    // MXFP4 operands: the block scales of A, then of B, packed per tile and
+    // K block in the layout the scale copies into tensor memory read
+    const uint8_t* sf;
+  };
   int* status;
   uint64_t timeout_ns;
   uint32_t stage_tx;  // bytes TMA delivers per stage (both CTAs of a pair)
@@ -80,15 +100,31 @@ static_assert(sizeof(TcParams) <= 128, "parameter struct within 128 bytes (see E
 // widened to FP16 (K accumulated in exact FP32 chunks, INT32 running sum).
 enum : int { kOutF16 = 0, kOutI32 = 1 };
 
+// Operand kinds: 16-bit (FP16, or BF16 with the BF16 operand bits), or
+// packed E2M1 with E8M0 block scales (MXFP4) on the block-scaled MMA.  An
+// MXFP4 stage holds the same 128 bytes per row as a 16-bit stage (256 codes
+// instead of 64 values), so the ring, the TMA boxes and the shared-memory
+// descriptors are the same; each stage adds the scales of its 256-wide K
+// block: 8 bytes per row, as two 512-byte images of 32 lines x 16 bytes for
+// each 128 rows (line r, word i, byte k: the scale of row 32 i + r for the
+// K block's 32-value block 4 j + k, image j).
+enum : int { kKind16 = 0, kKindMx = 1 };
+constexpr int kMxSfImage = 512;           // one image: 128 rows x 4 scales
+constexpr int kMxSfRowBlock = 2 * kMxSfImage;  // 128 rows x the 8 scales of a stage
+
 // Shared memory: the operand ring, then two staging boxes per epilogue warp,
 // then the barriers.
-template <int BN, int Stages, int CG>
+template <int BN, int Stages, int CG, int Kind = kKind16>
 struct TcSmem {
   static constexpr int kRowsB = BN / CG;  // B rows this CTA loads
   static constexpr int kTileBytesB = kRowsB * kBlockK * 2;
+  // MXFP4: scale images of a stage, A's 128 rows then B's rows in 128-row blocks
+  static constexpr int kSfBlocksB = (kRowsB + 127) / 128;
+  static constexpr int kSfBytes = Kind == kKindMx ? kMxSfRowBlock * (1 + kSfBlocksB) : 0;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + Stages * kTileBytesA;
-  static constexpr int kOffEpi = kOffB + Stages * kTileBytesB;
+  static constexpr int kOffSf = kOffB + Stages * kTileBytesB;
+  static constexpr int kOffEpi = kOffSf + Stages * kSfBytes;
   static constexpr int kEpiBytes = kEpiWarps * 2 * tc::kEpiBoxBytes;
   static constexpr int kOffBar = kOffEpi + kEpiBytes;
   // full[Stages], empty[Stages], tmem_full[2], tmem_empty[2], drain, then
@@ -144,16 +180,24 @@ __device__ __forceinline__ void epi_load_c(const CUtensorMap* map, const TcParam
       if (epi_box<BN, CG>(p, unit0, units, rank, wi, j + k, x, y)) tma_prefetch_l2_2d(map, x, y);
 }
 
-template <int BN, int Stages, int CG, int Out>
+template <int BN, int Stages, int CG, int Out, int Kind>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c,
                        const __grid_constant__ CUtensorMap tmap_d, const TcParams p,
                        const __grid_constant__ EpiProgram prog) {
-  using L = TcSmem<BN, Stages, CG>;
-  // two FP32 accumulators (the INT32 mode keeps its running sums in registers)
-  constexpr int kColsNeeded = 2 * BN;
+  using L = TcSmem<BN, Stages, CG, Kind>;
+  constexpr bool kMx = Kind == kKindMx;
+  static_assert(!kMx || (CG == 1 && Out == kOutF16), "MXFP4: single CTAs, FP16 output");
+  // two FP32 accumulators (the INT32 mode keeps its running sums in registers);
+  // MXFP4 adds two buffers of scale words after them: A's 128 rows (4
+  // columns per scale word, one per 32-row group) and B's rows (one column
+  // per 32 rows) for the two words of a stage
+  constexpr int kSfColsA = 8;
+  constexpr int kSfColsB = 8 * L::kSfBlocksB;
+  constexpr int kSfCols = kSfColsA + kSfColsB;
+  constexpr int kColsNeeded = 2 * BN + (kMx ? 2 * kSfCols : 0);
   constexpr int kTmemCols = kColsNeeded <= 128 ? 128 : (kColsNeeded <= 256 ? 256 : 512);
   static_assert(kColsNeeded <= 512, "tensor memory");
   // K blocks per accumulation chunk: the whole K, or exact-FP32 chunks
@@ -167,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* smem_a = smem + L::kOffA;
   uint8_t* smem_b = smem + L::kOffB;
+  uint8_t* smem_sf = smem + L::kOffSf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + Stages;
@@ -257,8 +302,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst_b = smem_b + stage * L::kTileBytesB;
           if (CG == 1) {
             mbar_arrive_expect_tx(&full_bar[stage], p.stage_tx);
-            tma_load_2d(&tmap_a, &full_bar[stage], dst_a, kb * kBlockK, a_row, pol);
-            tma_load_2d(&tmap_b, &full_bar[stage], dst_b, kb * kBlockK, b_row, pol);
+            // x counts elements of the map: FP16 values, or bytes of two codes
+            tma_load_2d(&tmap_a, &full_bar[stage], dst_a, kb * (kMx ? 128 : kBlockK), a_row, pol);
+            tma_load_2d(&tmap_b, &full_bar[stage], dst_b, kb * (kMx ? 128 : kBlockK), b_row, pol);
+            if (kMx) {
+              // this stage's scale images: A's row block, then B's tile
+              uint8_t* dst_sf = smem_sf + stage * L::kSfBytes;
+              const uint8_t* sfa =
+                  p.sf + (static_cast<int64_t>(m_blk) * p.num_k_blocks + kb) * kMxSfRowBlock;
+              const uint8_t* sfb =
+                  p.sf + static_cast<int64_t>(p.num_m_blocks) * p.num_k_blocks * kMxSfRowBlock +
+                  (static_cast<int64_t>(n_blk) * p.num_k_blocks + kb) * kMxSfRowBlock *
+                      L::kSfBlocksB;
+              bulk_load_g2s(dst_sf, sfa, kMxSfRowBlock, &full_bar[stage], pol);
+              bulk_load_g2s(dst_sf + kMxSfRowBlock, sfb, kMxSfRowBlock * L::kSfBlocksB,
+                            &full_bar[stage], pol);
+            }
           } else {
             // both CTAs' copies complete on the even CTA's full barrier
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], p.stage_tx);
@@ -297,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      int sf_buf = 0;  // MXFP4: scale buffer of the next stage
       for (int t = unit0; t < p.num_tiles && ok; t += units) {
         for (int ch = 0; ch < num_chunks && ok; ++ch) {
           if (!mbar_wait_abortable(&tmem_empty[acc], acc_phase ^ 1, p.timeout_ns, p.status,
@@ -319,14 +379,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             // rows: +2 in the descriptor's 16-byte address field
             const uint64_t da0 = smem_desc_sw128(smem_addr(smem_a + stage * kTileBytesA));
             const uint64_t db0 = smem_desc_sw128(smem_addr(smem_b + stage * L::kTileBytesB));
+            if (kMx) {
+              // The stage's scale images into scale buffer sf_buf: A's two
+              // words (4 columns each), then B's (one column per 32 rows of
+              // each 128-row block, 8 columns per block and word).  The copies
+              // run before this thread's later MMAs, in issue order; the MMAs
+              // of the stage before read the other buffer.
+              const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(2 * BN + sf_buf * kSfCols);
+              const uint32_t sfb_t = sfa_t + kSfColsA;
+              const uint32_t src = smem_addr(smem_sf + stage * L::kSfBytes);
 #pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k) {
-              const uint64_t da = da0 + 2 * k, db = db0 + 2 * k;
-              const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-              if (CG == 2)
-                tc_mma_f16_pair(d_tmem, da, db, idesc, accum);
-              else
-                tc_mma_f16(d_tmem, da, db, idesc, accum);
+              for (int w = 0; w < 2; ++w) {
+                tc_cp_32x128b_warpx4(sfa_t + 4 * w, smem_desc_rows16(src + w * kMxSfImage));
+#pragma unroll
+                for (int h = 0; h < L::kSfBlocksB; ++h)
+                  tc_cp_32x128b_warpx4(
+                      sfb_t + w * 4 * L::kSfBlocksB + 4 * h,
+                      smem_desc_rows16(src + kMxSfRowBlock * (1 + h) + w * kMxSfImage));
+              }
+              // MMA k (K = 64, scale blocks 2k and 2k + 1) reads word k / 2
+              // at byte 2 (k % 2)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+                tc_mma_mxf4(d_tmem, da0 + 2 * k, db0 + 2 * k,
+                            idesc_mxf4(kBlockM, BN, 2u * (k & 1)),
+                            sfa_t + 4 * (k >> 1), sfb_t + (k >> 1) * 4 * L::kSfBlocksB, accum);
+              }
+              sf_buf ^= 1;
+            } else {
+#pragma unroll
+              for (int k = 0; k < kBlockK / 16; ++k) {
+                const uint64_t da = da0 + 2 * k, db = db0 + 2 * k;
+                const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+                if (CG == 2)
+                  tc_mma_f16_pair(d_tmem, da, db, idesc, accum);
+                else
+                  tc_mma_f16(d_tmem, da, db, idesc, accum);
+              }
             }
             if (CG == 2)
               tc_commit_pair_multicast(&empty_bar[stage], 0x3);
@@ -479,38 +569,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) bulk_wait_group<0>();  // stores end before the CTA does
       __syncwarp();
     } else if (p.staged) {
-      // Staged epilogue.  The warp's chunks form one stream over its tiles
-      // (epi_box); chunk j of the stream goes through box j & 1 of the warp's
-      // two boxes.  C of chunks 0 and 1 is loaded by the producer; lane 0
-      // loads C of chunk j + 2 as soon as chunk j's store has read its box,
-      // so it arrives while the warp finishes chunk j + 1 or, across tiles,
-      // during the next main loop.
+      // Staged epilogue.  The warp's chunks form one stream over its tiles:
+      // chunk j of the stream is chunk j % n of the warp's (j / n)-th tile
+      // (n = the warp's chunks per tile) and goes through box j & 1 of its two
+      // boxes.  C of chunks 0 and 1 is loaded by the producer; lane 0 loads C
+      // of chunk j + 2 as soon as chunk j's store has read its box, so it
+      // arrives while the warp finishes chunk j + 1 or, across tiles, during
+      // the next main loop.  Tile coordinates are worked out once per tile (a
+      // second cursor runs two chunks ahead for the C loads).  Reading chunk
+      // j + 1's accumulator columns while chunk j is converted was measured
+      // and not kept: it took the registers to the 168 limit and the FP16
+      // 2048^3 and W4A16 M = 2048 GEMMs 5-7% slower.
       const int wi = warp - kEpiWarp0;
       uint8_t* boxes = smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes;
       uint64_t* cbar = epi_bar + wi * 2;
       const bool has_c = p.epi.beta != 0.0f;
       const uint64_t pol_c = policy_evict_first();
+      const int n_mine = chunk_hi - chunk_lo;
+      const int row_off = static_cast<int>(rank) * kBlockM + ew * 32;
+      // A stream position: tile t, chunk k of the warp's share of it, the
+      // share's first D column x0 and the warp's first D row y.
+      struct Cursor {
+        int t, k, x0, y;
+      };
+      auto set_tile = [&](Cursor& q) {
+        if (q.t < p.num_tiles) {
+          int mb, nb;
+          tc::tile_coords(q.t, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+          q.x0 = nb * BN + chunk_lo * 32;
+          q.y = mb * kTileM + row_off;
+        }
+      };
+      auto advance = [&](Cursor& q) {
+        if (++q.k == n_mine) {
+          q.k = 0;
+          q.t += units;
+          set_tile(q);
+        }
+      };
+      auto live_at = [&](const Cursor& q) {
+        return q.t < p.num_tiles && q.x0 + q.k * 32 < p.N && q.y < p.M;
+      };
       uint32_t c_phase = 0;    // bit b: parity of box b's next C arrival
       uint32_t c_pending = 0;  // bit b: a C load into box b not yet waited for
       bool prev_stored = false;
-      auto box_at = [&](int jj, int& x, int& y) -> bool {
-        return epi_box<BN, CG>(p, unit0, units, rank, wi, jj, x, y);
-      };
-      auto load_c = [&](int jj) {
-        int x, y;
-        if (!has_c || !box_at(jj, x, y)) return;
-        c_pending |= 1u << (jj & 1);
-        if (lane == 0) {
-          bulk_wait_group_read<0>();  // the store that last used the box has read it
-          epi_load_c<BN, CG>(&tmap_c, p, unit0, units, rank, wi, jj, boxes, cbar, pol_c);
-        }
-      };
-      for (int jj = 0; jj < 2; ++jj) {  // issued by the producer
-        int x, y;
-        if (has_c && box_at(jj, x, y)) c_pending |= 1u << jj;
+      Cursor ldc{unit0, 0, 0, 0};  // the next chunk whose C is to be requested
+      set_tile(ldc);
+      for (int jj = 0; jj < 2; ++jj) {  // chunks 0 and 1: requested by the producer
+        if (has_c && live_at(ldc)) c_pending |= 1u << jj;
+        advance(ldc);
       }
+      // Requests C of the chunk at `ldc` (stream index jl) into box jl & 1.
+      auto load_c = [&](int jl) {
+        if (has_c && live_at(ldc)) {
+          const int b = jl & 1;
+          c_pending |= 1u << b;
+          if (lane == 0) {
+            bulk_wait_group_read<0>();  // the store that last used the box has read it
+            const int x = ldc.x0 + ldc.k * 32;
+            mbar_arrive_expect_tx(&cbar[b], tc::kEpiBoxBytes);
+            tma_load_2d(&tmap_c, &cbar[b], boxes + b * tc::kEpiBoxBytes, x, ldc.y, pol_c);
+            if (ldc.k == 0)  // the tile's later chunks into L2 ahead of their loads
+              for (int k = 2; k < n_mine; ++k)
+                if (x + k * 32 < p.N) tma_prefetch_l2_2d(&tmap_c, x + k * 32, ldc.y);
+          }
+        }
+        advance(ldc);
+      };
       int j = 0;
-      for (int t = unit0; t < p.num_tiles && ok; t += units) {
+      Cursor cur{unit0, 0, 0, 0};
+      set_tile(cur);
+      while (cur.t < p.num_tiles && ok) {
         const bool ready =
             !aborted(abort_flag) &&
             mbar_wait_sleepy(&tmem_full[acc], acc_phase, p.timeout_ns, p.status, 256);
@@ -520,16 +649,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t tbase = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t tbase =
+            tmem_base + lane_base + static_cast<uint32_t>(acc * BN + chunk_lo * 32);
+        const bool row_live = cur.y < p.M;
 #pragma unroll 1
-        for (int c = chunk_lo; c < chunk_hi; ++c, ++j) {
+        for (int k = 0; k < n_mine; ++k) {
+          uint32_t r[32];
           const int b = j & 1;
           uint8_t* box = boxes + b * tc::kEpiBoxBytes;
-          int x, y;
-          const bool live = box_at(j, x, y);
+          const int x = cur.x0 + k * 32;
+          const bool live = row_live && x < p.N;
           if (live) {
-            uint32_t r[32];
-            tmem_ld_32cols(tbase + c * 32, r);
+            tmem_ld_32cols(tbase + k * 32, r);
             bool got = true;
             if (has_c) {
               got = mbar_wait(&cbar[b], (c_phase >> b) & 1u, p.timeout_ns, p.status);
@@ -558,12 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmap_d, box, x, y);
+              tma_store_2d(&tmap_d, box, x, cur.y);
               bulk_commit_group();
             }
           }
           prev_stored = live;
           load_c(j + 2);
+          ++j;
         }
         if (!ok) break;
         tc_fence_before_sync();
@@ -575,6 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc = 0;
           acc_phase ^= 1;
         }
+        cur.t += units;
+        set_tile(cur);
       }
       // Copies into and out of the boxes end before the CTA does.
       if (lane == 0) {
@@ -645,18 +779,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int Stages, int CG, int Out>
+template <int BN, int Stages, int CG, int Out, int Kind>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
-  using L = TcSmem<BN, Stages, CG>;
+  using L = TcSmem<BN, Stages, CG, Kind>;
+  constexpr bool kMx = Kind == kKindMx;
   CUtensorMap ta, tb;
   // A problem with fewer than 128 rows loads only its rows (rounded up to a
   // swizzle atom of 8): TMA is slow on boxes that are mostly out of bounds,
   // and the stale shared-memory rows below only feed accumulator rows >= M,
   // which the epilogue never stores.
   const int box_a = (CG == 1 && a.M < kBlockM) ? static_cast<int>((a.M + 7) / 8 * 8) : kBlockM;
-  cudaError_t e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, box_a);
-  if (e != cudaSuccess) return e;
-  e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, L::kRowsB);
+  cudaError_t e;
+  if (kMx) {
+    // packed codes as bytes: K / 2 bytes per row (K even), 128-byte boxes;
+    // the zero fill past K / 2 gives code 0 (value 0) to every K past the end
+    e = tc::make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.M, a.K / 2, a.lda / 2, box_a,
+                        128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    e = tc::make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.N, a.K / 2, a.ldb / 2,
+                        L::kRowsB, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    e = tc::make_f16_kmajor_map(&ta, a.A, a.M, a.K, a.lda, box_a);
+    if (e != cudaSuccess) return e;
+    e = tc::make_f16_kmajor_map(&tb, a.B, a.N, a.K, a.ldb, L::kRowsB);
+  }
   if (e != cudaSuccess) return e;
   // The staged epilogue moves D (and FP16 C) as boxes of 64-byte rows, which
   // needs 16-byte aligned rows (ld % 8 == 0 for FP16, ld % 4 == 0 for INT32)
@@ -686,7 +832,8 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.num_m_blocks = static_cast<int>((a.M + kBlockM * CG - 1) / (kBlockM * CG));
   p.num_n_blocks = static_cast<int>((a.N + BN - 1) / BN);
   p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-  p.num_k_blocks = static_cast<int>((a.K + kBlockK - 1) / kBlockK);
+  const int64_t k_per_block = kMx ? 256 : kBlockK;  // K values per stage
+  p.num_k_blocks = static_cast<int>((a.K + k_per_block - 1) / k_per_block);
   p.group_m = 16 / CG;
   p.epi = make_epi(a);
   p.C = a.C;
@@ -694,15 +841,19 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.D = a.D;
   p.ldd = a.ldd;
   p.bias = static_cast<const __half*>(a.bias);
-  p.alpha_i = static_cast<int32_t>(a.alpha);
-  p.beta_i = static_cast<int32_t>(a.beta);
+  if (kMx) {
+    p.sf = static_cast<const uint8_t*>(a.sf_packed);
+  } else {
+    p.alpha_i = static_cast<int32_t>(a.alpha);
+    p.beta_i = static_cast<int32_t>(a.beta);
+  }
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB));
+  p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB) + L::kSfBytes);
   p.staged = staged ? 1 : 0;
   p.idesc_ab = a.bf16_ab ? idesc_ab_bf16() : 0u;
 
-  auto kern = gemm_f16_tc_kernel<BN, Stages, CG, Out>;
+  auto kern = gemm_tc_kernel<BN, Stages, CG, Out, Kind>;
   int dev = 0;
   cudaGetDevice(&dev);
   // One shared-memory opt-in and one co-residency query per variant and device.
@@ -757,10 +908,10 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   return e;
 }
 
-template <int BN, int Stages, int CG, int Out>
+template <int BN, int Stages, int CG, int Out, int Kind = kKind16>
 int regs_of() {
   static std::atomic<int> slot{-1};
-  return kernel_regs(gemm_f16_tc_kernel<BN, Stages, CG, Out>, slot);
+  return kernel_regs(gemm_tc_kernel<BN, Stages, CG, Out, Kind>, slot);
 }
 
 }  // namespace
@@ -784,6 +935,12 @@ int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32) {
   return 0;
 }
 
+int mx_kernel_regs(int n_tile, int stages) {
+  if (n_tile == 224 && stages == 4) return regs_of<224, 4, 1, kOutF16, kKindMx>();
+  if (n_tile == 128 && stages == 5) return regs_of<128, 5, 1, kOutF16, kKindMx>();
+  return 0;
+}
+
 // Tile shapes compiled into the library; the planner only proposes these.
 // `a` holds FP16 operands (the caller's, or widened copies) or, with
 // a.bf16_ab, BF16 ones (widened MXFP4); a.exact_i32 selects the exact INT32
@@ -791,33 +948,43 @@ int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32) {
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (a.exact_i32) {
     if (plan.n_tile == 192 && plan.cta_group == 2 && plan.stages == 6)
-      return run_tc<192, 6, 2, kOutI32>(a, plan);
+      return run_tc<192, 6, 2, kOutI32, kKind16>(a, plan);
     if (plan.n_tile == 128 && plan.cta_group == 1 && plan.stages == 6)
-      return run_tc<128, 6, 1, kOutI32>(a, plan);
+      return run_tc<128, 6, 1, kOutI32, kKind16>(a, plan);
     return cudaErrorNotSupported;
   }
   if (plan.cta_group == 2) {
-    if (plan.n_tile == 256 && plan.stages == 6) return run_tc<256, 6, 2, kOutF16>(a, plan);
+    if (plan.n_tile == 256 && plan.stages == 6) return run_tc<256, 6, 2, kOutF16, kKind16>(a, plan);
     // 224 columns: 19 column tiles cover N = 4096 (the last one partly), so a
     // 4096^2 output is 16 x 19 = 304 pair tiles, four whole waves of 76 pairs
-    if (plan.n_tile == 224 && plan.stages == 6) return run_tc<224, 6, 2, kOutF16>(a, plan);
+    if (plan.n_tile == 224 && plan.stages == 6) return run_tc<224, 6, 2, kOutF16, kKind16>(a, plan);
     // 192 columns: N = 8960 is 47 column tiles, so M = 2048 gives 376 pair
     // tiles, 4.95 waves of 76 pairs (256 columns: 280 tiles, 3.68 waves)
-    if (plan.n_tile == 192 && plan.stages == 6) return run_tc<192, 6, 2, kOutF16>(a, plan);
-    if (plan.n_tile == 128 && plan.stages == 8) return run_tc<128, 8, 2, kOutF16>(a, plan);
+    if (plan.n_tile == 192 && plan.stages == 6) return run_tc<192, 6, 2, kOutF16, kKind16>(a, plan);
+    if (plan.n_tile == 128 && plan.stages == 8) return run_tc<128, 8, 2, kOutF16, kKind16>(a, plan);
     return cudaErrorNotSupported;
   }
   switch (plan.n_tile) {
     case 256:
-      if (plan.stages == 4) return run_tc<256, 4, 1, kOutF16>(a, plan);
+      if (plan.stages == 4) return run_tc<256, 4, 1, kOutF16, kKind16>(a, plan);
       break;
     case 128:
-      if (plan.stages == 6) return run_tc<128, 6, 1, kOutF16>(a, plan);
+      if (plan.stages == 6) return run_tc<128, 6, 1, kOutF16, kKind16>(a, plan);
       break;
     case 64:
-      if (plan.stages == 8) return run_tc<64, 8, 1, kOutF16>(a, plan);
+      if (plan.stages == 8) return run_tc<64, 8, 1, kOutF16, kKind16>(a, plan);
       break;
   }
+  return cudaErrorNotSupported;
+}
+
+// MXFP4 tiles on the block-scaled MMA: `a` holds packed codes (K even) and,
+// in a.sf_packed, both operands' scales packed by pack_mx_scales for this
+// plan's N_tile.
+cudaError_t launch_tc_mx(const GemmArgs& a, const dg_tile_plan& plan) {
+  if (plan.cta_group != 1) return cudaErrorNotSupported;
+  if (plan.n_tile == 224 && plan.stages == 4) return run_tc<224, 4, 1, kOutF16, kKindMx>(a, plan);
+  if (plan.n_tile == 128 && plan.stages == 5) return run_tc<128, 5, 1, kOutF16, kKindMx>(a, plan);
   return cudaErrorNotSupported;
 }
 

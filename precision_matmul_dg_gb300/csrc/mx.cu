@@ -26,6 +26,8 @@
 // exponent range; BF16 subnormals reach 2^-133) up to e = 251; above that the
 // largest codes overflow to infinities.  The copy is laid out as the FP16
 // widening's copies are: rows of widened_ld(K) = 32 * ceil(K / 32) values.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -321,6 +323,99 @@ cudaError_t launch_widen_mxf4(const MxWidenJob* jobs, int njobs, int64_t K, cuda
   widen_mxf4_kernel<<<grid, kMxThreads, 0, stream>>>(ops[0], ops[1], nblk);
   count_launches(1);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Scale packing for the block-scaled MMA
+// ---------------------------------------------------------------------------
+//
+// The block-scaled MMA reads the E8M0 scales from tensor memory, where a
+// copy instruction places 32 lines of 16 bytes (each line into the same
+// lanes of all four warp quarters).  Row m of a 128-row block takes word
+// m / 32 of line m % 32; the four bytes of a word are four consecutive
+// 32-value blocks along K.  One 256-wide K block (a pipeline stage) needs
+// two such images per 128 rows.  This kernel gathers the row-major scale
+// bytes of both operands into that order, one 16-byte line per thread.
+
+namespace {
+
+constexpr int kPackThreads = 256;
+
+struct PackOperand {
+  const uint8_t* scales;
+  int64_t lds, rows;
+  int group;        // rows per tile row group (128 for A, N_tile for B)
+  int halves;       // 128-row blocks per group
+  int64_t lines;    // 16-byte lines of the operand's packed section
+  uint8_t* out;
+};
+
+__global__ void __launch_bounds__(kPackThreads)
+    pack_mx_scales_kernel(PackOperand a, PackOperand b, int64_t kb_count, int64_t nblk) {
+  grid_dependency_wait();  // the scales may come from the kernel before this one
+  grid_launch_dependents();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       t < a.lines + b.lines; t += stride) {
+    const bool in_a = t < a.lines;
+    const PackOperand& o = in_a ? a : b;
+    const int64_t line = in_a ? t : t - a.lines;
+    // line = (((g * kb_count + kb) * halves + h) * 2 + j) * 32 + r
+    const int r = static_cast<int>(line & 31);
+    const int j = static_cast<int>((line >> 5) & 1);
+    int64_t rest = line >> 6;
+    const int h = static_cast<int>(rest % o.halves);
+    rest /= o.halves;
+    const int64_t kb = rest % kb_count;
+    const int64_t g = rest / kb_count;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int in_group = h * 128 + i * 32 + r;
+      const int64_t row = g * o.group + in_group;
+      uint32_t word = 0;
+      if (in_group < o.group && row < o.rows) {
+        const uint8_t* src = o.scales + row * o.lds;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int64_t blk = kb * 8 + 4 * j + k;
+          if (blk < nblk) word |= static_cast<uint32_t>(__ldg(src + blk)) << (8 * k);
+        }
+      }
+      w[i] = word;
+    }
+    reinterpret_cast<uint4*>(o.out)[line] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+int64_t pack_lines(int64_t rows, int group, int64_t kb_count) {
+  const int halves = (group + 127) / 128;
+  return (rows + group - 1) / group * kb_count * halves * 64;
+}
+
+}  // namespace
+
+int64_t pack_mx_scales_bytes(int64_t M, int64_t N, int64_t K, int n_tile) {
+  const int64_t kb_count = (K + 255) / 256;
+  return 16 * (pack_lines(M, 128, kb_count) + pack_lines(N, n_tile, kb_count));
+}
+
+cudaError_t launch_pack_mx_scales(int64_t M, int64_t N, int64_t K, int n_tile,
+                                  const void* scale_a, int64_t lds_a, const void* scale_b,
+                                  int64_t lds_b, void* out, cudaStream_t stream) {
+  const int64_t kb_count = (K + 255) / 256;
+  const int64_t nblk = (K + kMxBlock - 1) / kMxBlock;
+  PackOperand a{static_cast<const uint8_t*>(scale_a), lds_a, M, 128, 1,
+                pack_lines(M, 128, kb_count), static_cast<uint8_t*>(out)};
+  PackOperand b{static_cast<const uint8_t*>(scale_b), lds_b, N, n_tile, (n_tile + 127) / 128,
+                pack_lines(N, n_tile, kb_count), static_cast<uint8_t*>(out) + 16 * a.lines};
+  const int64_t total = a.lines + b.lines;
+  if (total <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((total + kPackThreads - 1) / kPackThreads, 4096);
+  const cudaError_t e = launch_dependent(pack_mx_scales_kernel, dim3(static_cast<unsigned>(blocks)),
+                                         dim3(kPackThreads), 0, stream, a, b, kb_count, nblk);
+  count_launches(1);
+  return e;
 }
 
 }  // namespace dg

@@ -47,6 +47,12 @@ constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
 // running INT32 sums in registers: N_tile a multiple of 64, at most 192)
 constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {192, 6, 2, 0}};
 constexpr TcVariant kTcVariantsE2M1[] = {{256, 6, 1, 2}, {128, 8, 1, 3}, {64, 8, 1, 4}};
+// MXFP4 x MXFP4 on the block-scaled MMA (the tensor-core kernel with packed
+// E2M1 stages and scale images; single CTAs)
+constexpr TcVariant kTcVariantsMx[] = {{224, 4, 1, 0}, {128, 5, 1, 0}};
+// E2M1 values per MMA FLOP relative to FP16: the block-scaled 4-bit MMA runs
+// at four times the 16-bit rate (the nominal Blackwell ratio)
+constexpr double kMxRateRatio = 4.0;
 constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;
 constexpr int kTcThreads = 384;      // FP16 x FP16 kernel (eight epilogue warps)
@@ -67,6 +73,7 @@ TcFamily tc_family(dg_dtype da, dg_dtype db) {
   if (da == DG_F16 && db == DG_F16) return {kTcVariantsF16, kNumTcVariantsF16, kTcThreads};
   if (da == DG_I8 && db == DG_I8) return {kTcVariantsI8, 1, kConvThreads};
   if (da == DG_F16 && db == DG_E2M1) return {kTcVariantsE2M1, 3, kConvThreads};
+  if (da == DG_MXF4 && db == DG_MXF4) return {kTcVariantsMx, 2, kTcThreads};
   return {nullptr, 0, 0};
 }
 
@@ -76,6 +83,8 @@ TcFamily tc_family(dg_dtype da, dg_dtype db) {
 // packed-E2M1 B) plus `cv_stages` slots of widened FP16 operands.
 int tc_ring_bytes(dg_dtype da, dg_dtype db, const TcVariant& v) {
   const int a16 = kTcBlockM * kTcBlockK * 2;
+  if (da == DG_MXF4 && db == DG_MXF4)  // 128-byte rows of codes, plus the scale images
+    return v.stages * (a16 + v.n_tile * kTcBlockK * 2 + 1024 * (1 + (v.n_tile + 127) / 128));
   if (da == DG_F16 && db == DG_F16)
     return v.stages * (a16 + (v.n_tile / v.cta_group) * kTcBlockK * 2);
   const int in_a = da == DG_I8 ? kTcBlockM * kTcBlockK : a16;
@@ -85,8 +94,12 @@ int tc_ring_bytes(dg_dtype da, dg_dtype db, const TcVariant& v) {
 }
 
 // Tensor-memory columns: two FP32 accumulators, plus INT32 running sums in the
-// converting INT8 kernel (the FP16 kernel's INT32 mode keeps them in registers).
-int tc_tmem_cols(bool conv_i8, int n_tile) { return (conv_i8 ? 3 : 2) * n_tile; }
+// converting INT8 kernel (the FP16 kernel's INT32 mode keeps them in registers),
+// or two buffers of scale words (8 columns for A, 8 per 128 rows of B) for MXFP4.
+int tc_tmem_cols(bool conv_i8, bool mx, int n_tile) {
+  if (mx) return 2 * n_tile + 2 * (8 + 8 * ((n_tile + 127) / 128));
+  return (conv_i8 ? 3 : 2) * n_tile;
+}
 
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
@@ -140,8 +153,15 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
                        std::string* why) {
   const bool narrow = !(da == DG_F16 && db == DG_F16);
   if (widened && !narrow) return;
-  // MXFP4 operands run only widened (to BF16, on the FP16 kernel's tiles)
   if ((da == DG_MXF4) != (db == DG_MXF4)) return;
+  // MXFP4 runs natively on the block-scaled MMA, or widened to BF16 on the
+  // 16-bit tiles; the native kernel reads whole bytes of codes, so an odd K
+  // (half a byte past the end of each row) runs widened
+  const bool mx_native = da == DG_MXF4 && !widened;
+  if (mx_native && K % 2 != 0) {
+    if (why) *why += "block-scaled MXFP4: odd K; ";
+    return;
+  }
   TcFamily fam = widened ? (da == DG_I8 ? TcFamily{kTcVariantsI8Widened, 2, kTcThreads}
                                         : TcFamily{kTcVariantsF16, kNumTcVariantsF16, kTcThreads})
                          : tc_family(da, db);
@@ -166,8 +186,9 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
       widened ? (da == DG_F16 ? 0.0 : (elem_a + 2.0) * M * static_cast<double>(K)) +
                     (elem_b + 2.0) * N * static_cast<double>(K)
               : 0.0;
-  const double t_pre = widened ? pre_bytes / hbm_bytes_per_us(hw) + (da == DG_I8 ? 4.0 : 2.0)
-                               : 0.0;
+  const double t_pre =
+      widened ? pre_bytes / hbm_bytes_per_us(hw) + (da == DG_I8 ? 4.0 : 2.0)
+              : (mx_native ? 2.0 : 0.0);  // native MXFP4: the scale-packing launch
   // shared memory / tensor memory are those of the kernel that runs
   const dg_dtype ka = widened ? DG_F16 : da, kb = widened ? DG_F16 : db;
   for (int vi = 0; vi < fam.n; ++vi) {
@@ -178,18 +199,20 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
       if (why) *why += name + ": M fits one CTA; ";
       continue;
     }
-    // the FP16 x FP16 kernel stages its output (FP16, or INT32 for widened INT8)
-    const bool staged = ka == DG_F16 && kb == DG_F16;
+    // the FP16 x FP16 kernel stages its output (FP16, or INT32 for widened
+    // INT8), and so does the MXFP4 kernel
+    const bool staged = (ka == DG_F16 && kb == DG_F16) || mx_native;
     const int smem = tc_smem_bytes(ka, kb, v, staged);
     if (smem > hw.smem_per_block_optin) {
       if (why) *why += name + ": shared memory; ";
       continue;
     }
-    if (tc_tmem_cols(da == DG_I8 && !widened, v.n_tile) > hw.tmem_cols) {
+    if (tc_tmem_cols(da == DG_I8 && !widened, mx_native, v.n_tile) > hw.tmem_cols) {
       if (why) *why += name + ": tensor memory; ";
       continue;
     }
-    const int measured = (ka == DG_F16 && kb == DG_F16)
+    const int measured = mx_native ? mx_kernel_regs(v.n_tile, v.stages)
+                         : (ka == DG_F16 && kb == DG_F16)
                              ? tc_kernel_regs(v.n_tile, v.stages, v.cta_group,
                                               widened && da == DG_I8)
                              : conv_kernel_regs(ka, kb, v.n_tile, v.stages);
@@ -208,12 +231,15 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
       if (why) *why += name + ": occupancy; ";
       continue;
     }
-    const int64_t k_pad = ceil_div(K, kTcBlockK) * kTcBlockK;
+    const int64_t k_step = mx_native ? 256 : kTcBlockK;  // K per pipeline stage
+    const int64_t k_pad = ceil_div(K, k_step) * k_step;
     // FLOPs of one tile per SM of its unit
     const double tile_flops = 2.0 * kTcBlockM * v.n_tile * static_cast<double>(k_pad);
     // The converting kernel spends shared-memory bandwidth and issue slots
     // widening tiles (calibrated on GB300: INT8 4096^3, W4A16 2048x8960x1536).
-    const double conv_eff = (narrow && !widened) ? (da == DG_I8 ? 0.36 : 0.54) : 1.0;
+    const double conv_eff = mx_native ? kMxRateRatio
+                            : (narrow && !widened) ? (da == DG_I8 ? 0.36 : 0.54)
+                                                   : 1.0;
     const double t_math =
         waves * tile_flops /
         (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile, v.cta_group) * conv_eff);
@@ -224,7 +250,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     p.kernel = widened ? DG_KERNEL_TC_WIDENED : DG_KERNEL_TC;
     p.m_tile = tile_m;
     p.n_tile = v.n_tile;
-    p.k_tile = kTcBlockK;
+    p.k_tile = static_cast<int>(k_step);
     p.split_k = 1;
     p.stages = v.stages;
     p.cta_group = v.cta_group;
@@ -588,10 +614,15 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
       if (why) *why = "tensor-core plan for a dtype pair it does not take";
       return false;
     }
+    const bool mx = dtype_a == DG_MXF4;
     if ((plan.cta_group != 1 && plan.cta_group != 2) ||
-        plan.m_tile != kTcBlockM * plan.cta_group || plan.k_tile != kTcBlockK ||
+        plan.m_tile != kTcBlockM * plan.cta_group || plan.k_tile != (mx ? 256 : kTcBlockK) ||
         plan.split_k != 1 || plan.swap_ab != 0) {
       if (why) *why = "tensor-core plan shape not compiled";
+      return false;
+    }
+    if (mx && K % 2 != 0) {
+      if (why) *why = "block-scaled MXFP4 plan with an odd K";
       return false;
     }
     for (int vi = 0; vi < fam.n; ++vi)

@@ -402,4 +402,68 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
 // the A and the B field); OR-ed into idesc_f16_f32's value.
 __host__ __device__ constexpr uint32_t idesc_ab_bf16() { return (1u << 7) | (1u << 10); }
 
+// ------------------------------------------- block-scaled 4-bit MMA (MXFP4)
+// Instruction descriptor of kind::mxf4 (packed E2M1 A and B, FP32
+// accumulator, one E8M0 scale per 32 values along K): A and B format E2M1
+// (1) in bits 7-9 and 10-12, both K-major, N / 8 in bits 17-22, scale format
+// E8M0 (1) in bit 23, M / 16 in bits 24-28, and the byte of the 32-bit scale
+// word where this MMA's scales start: B's in bits 4-5, A's in bits 29-30
+// (0 or 2 with two scales per MMA of K = 64).
+__host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n, uint32_t sf_id) {
+  return (sf_id << 4)                               // B scale byte
+         | (1u << 7) | (1u << 10)                   // A, B format: E2M1
+         | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
+         | (1u << 23)                               // scales are E8M0
+         | (static_cast<uint32_t>(m >> 4) << 24)    // M / 16
+         | (sf_id << 29);                           // A scale byte
+}
+
+// D[tmem] (+)= (A . diag(scales)) x (B . diag(scales))^T for one K = 64 step
+// of packed E2M1 operands (both K-major, 32 bytes per row per step); the
+// scale words of A and B are read from tensor memory at sfa / sfb.
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], "
+      "p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies 32 rows of 16 bytes from shared memory (descriptor `src`) into
+// tensor memory at column taddr .. taddr + 3 of lanes 0-31, and the same
+// data into lanes 32-63, 64-95 and 96-127 (the four warp quarters).
+// Executed in order with the MMAs the same thread issues afterwards.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t src) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src)
+               : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled K-major matrix of 16-byte rows
+// stored back to back (8-row groups 128 bytes apart): the source layout of
+// tc_cp_32x128b_warpx4.  Start address >> 4 (bits 0-13), stride byte offset
+// 128 >> 4 (bits 32-45), descriptor version 1 (bits 46-47), no swizzle.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// One-dimensional bulk copy of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned) from global to this CTA's shared memory, counted on `bar`
+// as transaction bytes.
+__device__ __forceinline__ void bulk_load_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(cache_policy)
+      : "memory");
+}
+
 }  // namespace dg

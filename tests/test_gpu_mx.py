@@ -97,7 +97,7 @@ def test_quantize_full_size_sampled(dg):
     _assert_quantize_parity(dg, x, 4096, rows)
 
 
-def _run_gemm(dg, case):
+def _run_gemm(dg, case, plan=None):
     dev = "cuda"
     A = torch.from_numpy(case.A).to(dev)
     B = torch.from_numpy(case.B).to(dev)
@@ -107,7 +107,7 @@ def _run_gemm(dg, case):
          else torch.zeros(case.M, case.N, dtype=torch.float16, device=dev))
     bias = torch.from_numpy(case.bias).to(dev) if case.bias is not None else None
     dg.gemm_mxf4(A, sa, B, sb, C, case.K, bias=bias, alpha=case.alpha, beta=case.beta,
-                 epilogue=case.epilogue)
+                 epilogue=case.epilogue, plan=plan)
     dg.check_status()
     return C.cpu().numpy()
 
@@ -250,3 +250,32 @@ def test_gemm_mxf4_padded_operands(dg, shape):
     got = _run_gemm(dg, case)
     assert not np.isnan(got).any()
     _assert_gemm_parity(case, got)
+
+
+@pytest.mark.parametrize("shape", [(256, 520, 640), (300, 460, 1000), (1, 100, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gemm_mxf4_every_plan(dg, shape):
+    # every plan the planner offers for the shape, the block-scaled MMA's
+    # tiles (N_tile 224 and 128) and the BF16 widening's, against the oracle
+    M, N, K = shape
+    case = workloads.mxf4_case(M, N, K, alpha=1.25, beta=-0.5, epilogue="bias_gelu", seed=M + K)
+    plans = dg.plan_tiles(M, N, K, "mxf4", "mxf4", max_out=64)
+    native = {(p["n_tile"], p["stages"]) for p in plans if p["kernel_name"] == "tc"}
+    assert native == {(224, 4), (128, 5)}
+    for plan in plans:
+        got = _run_gemm(dg, case, plan=plan)
+        _assert_gemm_parity(case, got)
+
+
+def test_gemm_mxf4_odd_k_is_widened(dg):
+    # the block-scaled kernel reads whole bytes of codes: an odd K runs through
+    # the widening, and a block-scaled plan is refused
+    case = workloads.mxf4_case(64, 96, 99, beta=0.5, seed=9)
+    plans = dg.plan_tiles(64, 96, 99, "mxf4", "mxf4", max_out=64)
+    assert {p["kernel_name"] for p in plans} == {"tc_widened"}
+    _assert_gemm_parity(case, _run_gemm(dg, case))
+    native = dg.plan_tiles(64, 96, 100, "mxf4", "mxf4", max_out=64)
+    native = next(p for p in native if p["kernel_name"] == "tc")
+    with pytest.raises(dg.DgError) as ei:
+        _run_gemm(dg, case, plan=native)
+    assert ei.value.name == "DG_ERR_INVALID_STATE"

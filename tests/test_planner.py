@@ -283,12 +283,34 @@ def test_skinny_plans(dg, M):
                 if q["kernel_name"] == "skinny"]
 
 
-def test_mxf4_plans_are_widened(dg):
-    # MXFP4 operands run only through the widening pre-pass and the FP16
-    # kernel's tiles; mixed pairs are refused
+def mx_smem(n_tile, stages):
+    # 128-byte rows of packed codes for A (128 rows) and B, the stage's scale
+    # images (1 KB per 128 rows), the FP16 output staging boxes, barriers and
+    # the 1 KB alignment slack
+    return (stages * (128 * 128 + n_tile * 128 + 1024 * (1 + math.ceil(n_tile / 128)))
+            + EPI_STAGING + 512 + 1024)
+
+
+def test_mxf4_plans(dg):
+    # MXFP4 runs on the block-scaled MMA (kernel "tc", 256 values of K per
+    # stage) or through the BF16 widening ("tc_widened"); every native plan
+    # fits the shared memory and tensor memory (two accumulators plus two
+    # buffers of scale words), and an odd K leaves only the widening
     for shape in [(1, 4096, 4096), (16, 8960, 1536), (4096, 4096, 4096), (130, 1000, 1000)]:
         plans = dg.plan_tiles(*shape, "mxf4", "mxf4", hw=GB300, max_out=64)
-        assert plans and {p["kernel_name"] for p in plans} == {"tc_widened"}, shape
+        assert {p["kernel_name"] for p in plans} == {"tc", "tc_widened"}, shape
+        for p in plans:
+            if p["kernel_name"] != "tc":
+                continue
+            assert (p["m_tile"], p["k_tile"], p["cta_group"]) == (128, 256, 1)
+            assert (p["n_tile"], p["stages"]) in ((224, 4), (128, 5))
+            assert p["smem_bytes"] == mx_smem(p["n_tile"], p["stages"])
+            assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
+            sf_cols = 2 * (8 + 8 * math.ceil(p["n_tile"] / 128))
+            assert 2 * p["n_tile"] + sf_cols <= GB300["tmem_cols"]
+    for K in (33, 1001):
+        plans = dg.plan_tiles(256, 512, K, "mxf4", "mxf4", hw=GB300, max_out=64)
+        assert {p["kernel_name"] for p in plans} == {"tc_widened"}, K
     for pair in (("f16", "mxf4"), ("mxf4", "e2m1")):
         with pytest.raises(dg.DgError) as ei:
             dg.plan_tiles(64, 64, 64, *pair, hw=GB300)
