@@ -130,6 +130,73 @@ __device__ __forceinline__ void write_out(const GemvParams& p, const GemvOut& o,
             prog);
 }
 
+// This warp's partial dot products of B row j with the M rows of A over
+// [k0, k1), one FP32 sum per lane and row (not yet reduced across the warp).
+// Batches of `Unroll` 256-element steps: every load of a batch is in flight
+// at once (one memory round trip per batch); steps past the end of the K
+// range are predicated off.
+template <int MROWS, int Unroll>
+__device__ __forceinline__ void gemv_accumulate(const GemvParams& p, const __half* A,
+                                                const __half* B, int j, int lane, int k0, int k1,
+                                                float (&acc)[MROWS]) {
+#pragma unroll
+  for (int m = 0; m < MROWS; ++m) acc[m] = 0.0f;
+  if (j >= p.N || k0 >= k1) return;
+  const __half* brow = B + static_cast<int64_t>(j) * p.ldb;
+  int k = k0 + lane * 8;
+  constexpr int kStep = 256;
+  // full batches: no predicates in the streaming loop
+  for (; k + (Unroll - 1) * kStep + 8 <= k1; k += Unroll * kStep) {
+    uint4 bv[Unroll];
+#pragma unroll
+    for (int u = 0; u < Unroll; ++u) bv[u] = ld_stream(brow + k + u * kStep);
+#pragma unroll
+    for (int u = 0; u < Unroll; ++u) {
+#pragma unroll
+      for (int m = 0; m < MROWS; ++m) {
+        if (m < p.M) {
+          const uint4 av = __ldg(reinterpret_cast<const uint4*>(
+              A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
+          fma8(acc[m], av, bv[u]);
+        }
+      }
+    }
+  }
+  // at most one partial batch, predicated per step
+  if (k + 8 <= k1) {
+    uint4 bv[Unroll];
+#pragma unroll
+    for (int u = 0; u < Unroll; ++u)
+      bv[u] = (k + u * kStep + 8 <= k1) ? ld_stream(brow + k + u * kStep) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < Unroll; ++u) {
+      if (k + u * kStep + 8 <= k1) {
+#pragma unroll
+        for (int m = 0; m < MROWS; ++m) {
+          if (m < p.M) {
+            const uint4 av = __ldg(reinterpret_cast<const uint4*>(
+                A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
+            fma8(acc[m], av, bv[u]);
+          }
+        }
+      }
+    }
+  }
+  // k is now past the last whole 8-element group this lane owns; the ragged
+  // tail (< 8 elements at the end of the K range) is done by the lane whose
+  // next group would have started there.
+  k = k1 - ((k1 - k0) & 7);
+  if ((k - k0) % kStep == lane * 8 && k < k1) {
+    for (int kk = k; kk < k1; ++kk) {
+      const float bf = __half2float(brow[kk]);
+#pragma unroll
+      for (int m = 0; m < MROWS; ++m)
+        if (m < p.M)
+          acc[m] = fmaf(__half2float(A[static_cast<int64_t>(m) * p.lda + kk]), bf, acc[m]);
+    }
+  }
+}
+
 template <int MROWS>
 __global__ void __launch_bounds__(kGemvWarps * 32)
     gemv_splitk_kernel(const GemvParams p, const __grid_constant__ EpiProgram prog,
@@ -147,68 +214,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
   const int k1 = min(p.K, k0 + p.k_chunk);
 
   float acc[MROWS];
-#pragma unroll
-  for (int m = 0; m < MROWS; ++m) acc[m] = 0.0f;
-
-  if (j < p.N && k0 < k1) {
-    const __half* brow = B + static_cast<int64_t>(j) * p.ldb;
-    int k = k0 + lane * 8;
-    // Batches of kGemvUnroll 256-element steps: every load of a batch is in
-    // flight at once (one memory round trip per batch); steps past the end
-    // of the K range are predicated off.
-    constexpr int kStep = 256;
-    // full batches: no predicates in the streaming loop
-    for (; k + (kGemvUnroll - 1) * kStep + 8 <= k1; k += kGemvUnroll * kStep) {
-      uint4 bv[kGemvUnroll];
-#pragma unroll
-      for (int u = 0; u < kGemvUnroll; ++u) bv[u] = ld_stream(brow + k + u * kStep);
-#pragma unroll
-      for (int u = 0; u < kGemvUnroll; ++u) {
-#pragma unroll
-        for (int m = 0; m < MROWS; ++m) {
-          if (m < p.M) {
-            const uint4 av = __ldg(reinterpret_cast<const uint4*>(
-                A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
-            fma8(acc[m], av, bv[u]);
-          }
-        }
-      }
-    }
-    // at most one partial batch, predicated per step
-    if (k + 8 <= k1) {
-      uint4 bv[kGemvUnroll];
-#pragma unroll
-      for (int u = 0; u < kGemvUnroll; ++u)
-        bv[u] = (k + u * kStep + 8 <= k1) ? ld_stream(brow + k + u * kStep)
-                                          : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < kGemvUnroll; ++u) {
-        if (k + u * kStep + 8 <= k1) {
-#pragma unroll
-          for (int m = 0; m < MROWS; ++m) {
-            if (m < p.M) {
-              const uint4 av = __ldg(reinterpret_cast<const uint4*>(
-                  A + static_cast<int64_t>(m) * p.lda + k + u * kStep));
-              fma8(acc[m], av, bv[u]);
-            }
-          }
-        }
-      }
-    }
-    // k is now past the last whole 8-element group this lane owns; the
-    // ragged tail (< 8 elements at the end of the K range) is done by the
-    // lane whose next group would have started there.
-    k = k1 - ((k1 - k0) & 7);
-    if ((k - k0) % kStep == lane * 8 && k < k1) {
-      for (int kk = k; kk < k1; ++kk) {
-        const float bf = __half2float(brow[kk]);
-#pragma unroll
-        for (int m = 0; m < MROWS; ++m)
-          if (m < p.M)
-            acc[m] = fmaf(__half2float(A[static_cast<int64_t>(m) * p.lda + kk]), bf, acc[m]);
-      }
-    }
-  }
+  gemv_accumulate<MROWS, kGemvUnroll>(p, A, B, j, lane, k0, k1, acc);
 
 #pragma unroll
   for (int m = 0; m < MROWS; ++m) acc[m] = warp_sum(acc[m]);
@@ -255,6 +261,66 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
     write_out(p, out, prog, m, jj, s);
   }
   if (threadIdx.x == 0) counters[blockIdx.x] = 0u;  // ready for the next launch
+}
+
+// Split-K inside a thread-block cluster (2 <= split <= 8): the CTAs of a row
+// group's splits form one cluster along grid.y.  Each CTA streams its K
+// range (eight 256-element steps in flight per lane, so that a split of up
+// to 2048 K costs one memory round trip), leaves its warps' sums in its own
+// shared memory, and after a cluster barrier the CTA of rank 0 reads every
+// split's sums from the others' shared memory (distributed shared memory) in
+// split order, applies the epilogue and stores D.  No partial sums go to
+// global memory and no arrival counter is needed, which saves the L2 round
+// trips of the last-CTA reduction; the order of the additions is fixed, so
+// results are bit-stable from run to run.
+constexpr int kGemvClusterUnroll = 8;
+constexpr int kGemvClusterMax = 8;  // portable cluster size
+
+template <int MROWS>
+__global__ void __launch_bounds__(kGemvWarps * 32)
+    gemv_cluster_kernel(const GemvParams p, const __grid_constant__ EpiProgram prog,
+                        const GemvBatch bt) {
+  __shared__ float part[MROWS][kGemvWarps];
+  grid_dependency_wait();  // launched as a dependent of the previous kernel
+  const int64_t z = blockIdx.z;
+  const __half* A = p.A + z * bt.sa;
+  const __half* B = p.B + z * bt.sb;
+  const GemvOut out{p.C + z * bt.sc, p.D + z * bt.sd, p.bias ? p.bias + z * bt.sbias : nullptr};
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x * kGemvWarps + warp;
+  const int split = blockIdx.y;  // = the CTA's rank in its cluster
+  const int k0 = split * p.k_chunk;
+  const int k1 = min(p.K, k0 + p.k_chunk);
+
+  float acc[MROWS];
+  gemv_accumulate<MROWS, kGemvClusterUnroll>(p, A, B, j, lane, k0, k1, acc);
+#pragma unroll
+  for (int m = 0; m < MROWS; ++m) acc[m] = warp_sum(acc[m]);
+  grid_launch_dependents();
+  if (lane == 0) {
+#pragma unroll
+    for (int m = 0; m < MROWS; ++m) part[m][warp] = acc[m];
+  }
+  cluster_sync();  // every split's sums are in its shared memory
+  if (split == 0) {
+    for (int t = threadIdx.x; t < kGemvWarps * p.M; t += blockDim.x) {
+      const int m = t / kGemvWarps, w = t % kGemvWarps;
+      const int jj = blockIdx.x * kGemvWarps + w;
+      const uint32_t local = smem_addr(&part[m][w]);
+      // every split's value in flight at once, then added in split order
+      float v[kGemvClusterMax];
+#pragma unroll
+      for (int r = 0; r < kGemvClusterMax; ++r)
+        v[r] = r < p.split_k ? ld_shared_cluster_f32(mapa_shared(local, r)) : 0.0f;
+      float sum = 0.0f;
+#pragma unroll
+      for (int r = 0; r < kGemvClusterMax; ++r)
+        if (r < p.split_k) sum += v[r];
+      if (jj < p.N) write_out(p, out, prog, m, jj, sum);
+    }
+  }
+  cluster_sync();  // the other CTAs stay resident until rank 0 has read them
 }
 
 // K == 0: D = epilogue(beta * C), no product term.  Element i of the M x N
@@ -460,16 +526,27 @@ __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 
 }  // namespace
 
+// Splits of 2 .. 8 reduce inside a cluster and need no workspace.
+bool gemv_split_in_cluster(int split) { return split >= 2 && split <= kGemvClusterMax; }
+
 int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t batch) {
+  if (plan.kernel == DG_KERNEL_GEMV && gemv_split_in_cluster(plan.split_k)) return 0;
   return plan.split_k > 1 ? static_cast<int64_t>(plan.split_k) * M * N * batch : 0;
 }
 
 int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N, int64_t batch) {
+  if (plan.kernel == DG_KERNEL_GEMV && gemv_split_in_cluster(plan.split_k)) return 0;
   return plan.split_k > 1 ? (N + kGemvWarps - 1) / kGemvWarps * batch : 0;
 }
 
-int gemv_kernel_regs(int64_t M) {
-  static std::atomic<int> slot[4] = {{-1}, {-1}, {-1}, {-1}};
+int gemv_kernel_regs(int64_t M, int split) {
+  static std::atomic<int> slot[8] = {{-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}};
+  if (gemv_split_in_cluster(split)) {
+    if (M <= 1) return kernel_regs(gemv_cluster_kernel<1>, slot[4]);
+    if (M <= 2) return kernel_regs(gemv_cluster_kernel<2>, slot[5]);
+    if (M <= 4) return kernel_regs(gemv_cluster_kernel<4>, slot[6]);
+    return kernel_regs(gemv_cluster_kernel<kGemvMaxM>, slot[7]);
+  }
   if (M <= 1) return kernel_regs(gemv_splitk_kernel<1>, slot[0]);
   if (M <= 2) return kernel_regs(gemv_splitk_kernel<2>, slot[1]);
   if (M <= 4) return kernel_regs(gemv_splitk_kernel<4>, slot[2]);
@@ -504,10 +581,15 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
   const dim3 grid(static_cast<unsigned>((a.N + kGemvWarps - 1) / kGemvWarps),
                   static_cast<unsigned>(plan.split_k));
   const dim3 block(kGemvWarps * 32);
-  auto kern = a.M <= 1   ? gemv_splitk_kernel<1>
-              : a.M <= 2 ? gemv_splitk_kernel<2>
-              : a.M <= 4 ? gemv_splitk_kernel<4>
-                         : gemv_splitk_kernel<kGemvMaxM>;
+  const bool cluster = gemv_split_in_cluster(plan.split_k);
+  auto kern = cluster ? (a.M <= 1   ? gemv_cluster_kernel<1>
+                         : a.M <= 2 ? gemv_cluster_kernel<2>
+                         : a.M <= 4 ? gemv_cluster_kernel<4>
+                                    : gemv_cluster_kernel<kGemvMaxM>)
+                      : (a.M <= 1   ? gemv_splitk_kernel<1>
+                         : a.M <= 2 ? gemv_splitk_kernel<2>
+                         : a.M <= 4 ? gemv_splitk_kernel<4>
+                                    : gemv_splitk_kernel<kGemvMaxM>);
   // grid.z takes at most 65535 problems per launch
   constexpr int64_t kMaxZ = 65535;
   const int64_t groups = (a.N + kGemvWarps - 1) / kGemvWarps;
@@ -523,7 +605,26 @@ cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const Split
     if (q.partial) q.partial += z0 * plan.split_k * a.M * a.N;
     if (q.counters) q.counters += z0 * groups;
     const dim3 g(grid.x, grid.y, static_cast<unsigned>(nz));
-    const cudaError_t e = launch_dependent(kern, g, block, 0, a.stream, q, make_program(a), bt);
+    cudaError_t e;
+    if (cluster) {
+      // the splits of a row group as one cluster along y
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = g;
+      cfg.blockDim = block;
+      cfg.stream = a.stream;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = static_cast<unsigned>(plan.split_k);
+      attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      e = cudaLaunchKernelEx(&cfg, kern, q, make_program(a), bt);
+    } else {
+      e = launch_dependent(kern, g, block, 0, a.stream, q, make_program(a), bt);
+    }
     count_launches(1);
     if (e != cudaSuccess) return e;
   }

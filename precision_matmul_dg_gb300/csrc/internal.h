@@ -132,7 +132,7 @@ struct GemmArgs {
 int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32);
 int mx_kernel_regs(int n_tile, int stages);  // the MXFP4 block-scaled kernel (gemm_tc.cu)
 int conv_kernel_regs(dg_dtype da, dg_dtype db, int n_tile, int stages);
-int gemv_kernel_regs(int64_t M);
+int gemv_kernel_regs(int64_t M, int split);
 int gemv_mma_kernel_regs(int64_t M);
 int skinny_kernel_regs();
 
@@ -219,6 +219,9 @@ cudaError_t launch_pack_mx_scales(int64_t M, int64_t N, int64_t K, int n_tile,
                                   int64_t lds_b, void* out, cudaStream_t stream);
 cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns);
 
+// Whether the split-K GEMV reduces `split` splits inside a thread-block
+// cluster (no workspace) rather than through global partial sums.
+bool gemv_split_in_cluster(int split);
 // Workspace sizes a GEMV plan needs for `batch` problems.
 int64_t gemv_partial_elems(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t batch);
 int64_t gemv_counter_elems(const dg_tile_plan& plan, int64_t N, int64_t batch);

@@ -17,9 +17,8 @@
 //             an all-zero block takes s = -127; a block with an infinity or
 //             a NaN takes e = 255 and codes 0;
 //   codes  -- v * 2^-s, exact in FP32, rounded to E2M1 by the conversion
-//             instruction (nearest, ties to even, saturating at 6) on the
-//             magnitude, with the sign bit of v put back, so that -0 and
-//             negative values that round to 0 keep their sign.
+//             instruction (nearest, ties to even, saturating at 6), which
+//             keeps the sign of -0 and of negative values that round to 0.
 //
 // Widening: e2m1(code) has at most two significant bits and e spans 2^-127 ..
 // 2^127, so e2m1(code) * X is exact in FP32 and again in BF16 (FP32's
@@ -46,13 +45,21 @@ constexpr int kMxBlock = 32;  // values per scale
 // Quantization
 // ---------------------------------------------------------------------------
 
-// Two non-negative FP32 values -> one byte of two E2M1 codes (lo in the low
-// nibble), nearest with ties to even, saturated to the largest finite code.
-__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+// Eight FP32 values -> four bytes of E2M1 codes (value 2i in the low nibble
+// of byte i), nearest with ties to even, saturated to the largest finite
+// code.  The conversion keeps the sign of negative values that round to zero
+// (code 8, -0), as the format's rounding asks (checked on GB300 for -0,
+// -1e-30, -0.1 and -0.2499).
+__device__ __forceinline__ uint32_t e2m1x8_from_f32(const float (&v)[8]) {
   uint32_t out;
-  asm("{\n\t.reg .b8 q;\n\tcvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\tcvt.u32.u8 %0, q;\n\t}"
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
       : "=r"(out)
-      : "f"(hi), "f"(lo));
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
   return out;
 }
 
@@ -88,18 +95,16 @@ __device__ __forceinline__ uint32_t quantize_block(const uint32_t (&w)[4], unsig
   }
   scale_byte = static_cast<uint32_t>(s + 127);
   // 2^-s as FP32 bits (s in [-26, 13] for a non-zero block; 2^127 for the
-  // all-zero block, whose products are zero anyway)
+  // all-zero block, whose products are zero anyway); v * 2^-s is exact
   const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-  uint32_t packed = 0;
+  float v[8];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float lo = fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[q])))) * inv;
-    const float hi = fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[q] >> 16)))) * inv;
-    uint32_t byte = e2m1x2_from_f32(lo, hi);
-    byte |= ((w[q] >> 12) & 0x8u) | ((w[q] >> 24) & 0x80u);  // the two sign bits
-    packed |= byte << (8 * q);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+    v[2 * q] = f.x * inv;
+    v[2 * q + 1] = f.y * inv;
   }
-  return packed;
+  return e2m1x8_from_f32(v);
 }
 
 // Threads are laid out by rows: a row is shared by lpr = 2^log2_lpr lanes
@@ -339,58 +344,86 @@ cudaError_t launch_widen_mxf4(const MxWidenJob* jobs, int njobs, int64_t K, cuda
 
 namespace {
 
-constexpr int kPackThreads = 256;
+// One CTA per (operand, tile row group g, 128-row block h of it, 4 K blocks):
+// its 128 threads read 32 scale bytes of one row each (one sector, 16-byte
+// loads when the row pitch allows), and then write the four K blocks' images
+// (4 x 1024 bytes) as 16-byte lines from shared memory.
+constexpr int kPackThreads = 128;
+constexpr int kPackKb = 4;  // K blocks (of 256 values, 8 scales) per CTA
 
 struct PackOperand {
   const uint8_t* scales;
   int64_t lds, rows;
-  int group;        // rows per tile row group (128 for A, N_tile for B)
-  int halves;       // 128-row blocks per group
-  int64_t lines;    // 16-byte lines of the operand's packed section
+  int group;      // rows per tile row group (128 for A, N_tile for B)
+  int halves;     // 128-row blocks per group
+  int64_t ctas;   // CTAs for this operand
   uint8_t* out;
 };
 
 __global__ void __launch_bounds__(kPackThreads)
     pack_mx_scales_kernel(PackOperand a, PackOperand b, int64_t kb_count, int64_t nblk) {
+  __shared__ __align__(16) uint8_t rows_sf[kPackThreads][kPackKb * 8];
   grid_dependency_wait();  // the scales may come from the kernel before this one
   grid_launch_dependents();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-       t < a.lines + b.lines; t += stride) {
-    const bool in_a = t < a.lines;
-    const PackOperand& o = in_a ? a : b;
-    const int64_t line = in_a ? t : t - a.lines;
-    // line = (((g * kb_count + kb) * halves + h) * 2 + j) * 32 + r
-    const int r = static_cast<int>(line & 31);
-    const int j = static_cast<int>((line >> 5) & 1);
-    int64_t rest = line >> 6;
-    const int h = static_cast<int>(rest % o.halves);
-    rest /= o.halves;
-    const int64_t kb = rest % kb_count;
-    const int64_t g = rest / kb_count;
+  const bool in_a = blockIdx.x < a.ctas;
+  const PackOperand& o = in_a ? a : b;
+  int64_t c = in_a ? blockIdx.x : blockIdx.x - a.ctas;
+  const int64_t quads = (kb_count + kPackKb - 1) / kPackKb;
+  const int64_t q = c % quads;
+  c /= quads;
+  const int h = static_cast<int>(c % o.halves);
+  const int64_t g = c / o.halves;
+  const int64_t kb0 = q * kPackKb;
+  // 1. row t of the block: scale bytes of K blocks kb0 .. kb0 + 3
+  {
+    const int t = threadIdx.x;
+    const int in_group = h * 128 + t;
+    const int64_t row = g * o.group + in_group;
+    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (in_group < o.group && row < o.rows) {
+      const uint8_t* src = o.scales + row * o.lds + kb0 * 8;
+      const int64_t left = nblk - kb0 * 8;
+      const int n = left < 32 ? static_cast<int>(left) : 32;  // scale bytes of these K blocks
+      if (n == 32 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(src));
+        const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+      } else {
+        for (int i = 0; i < n; ++i) w[i >> 2] |= static_cast<uint32_t>(__ldg(src + i)) << (8 * (i & 3));
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(rows_sf[t]);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  __syncthreads();
+  // 2. line L of the 4 K blocks' images: K block kb0 + L / 64, image j =
+  //    (L / 32) % 2, line r = L % 32; word i is row 32 i + r's scale word j
+  //    of that K block
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+    const int L = part * kPackThreads + threadIdx.x;
+    const int kq = L >> 6, j = (L >> 5) & 1, r = L & 31;
+    const int64_t kb = kb0 + kq;
+    if (kb >= kb_count) continue;
     uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int in_group = h * 128 + i * 32 + r;
-      const int64_t row = g * o.group + in_group;
-      uint32_t word = 0;
-      if (in_group < o.group && row < o.rows) {
-        const uint8_t* src = o.scales + row * o.lds;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int64_t blk = kb * 8 + 4 * j + k;
-          if (blk < nblk) word |= static_cast<uint32_t>(__ldg(src + blk)) << (8 * k);
-        }
-      }
-      w[i] = word;
-    }
-    reinterpret_cast<uint4*>(o.out)[line] = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < 4; ++i)
+      w[i] = reinterpret_cast<const uint32_t*>(rows_sf[32 * i + r])[kq * 2 + j];
+    uint8_t* dst = o.out + ((g * kb_count + kb) * o.halves + h) * 1024 + j * 512 + r * 16;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
 int64_t pack_lines(int64_t rows, int group, int64_t kb_count) {
   const int halves = (group + 127) / 128;
   return (rows + group - 1) / group * kb_count * halves * 64;
+}
+
+int64_t pack_ctas(int64_t rows, int group, int64_t kb_count) {
+  const int halves = (group + 127) / 128;
+  return (rows + group - 1) / group * halves * ((kb_count + kPackKb - 1) / kPackKb);
 }
 
 }  // namespace
@@ -406,12 +439,13 @@ cudaError_t launch_pack_mx_scales(int64_t M, int64_t N, int64_t K, int n_tile,
   const int64_t kb_count = (K + 255) / 256;
   const int64_t nblk = (K + kMxBlock - 1) / kMxBlock;
   PackOperand a{static_cast<const uint8_t*>(scale_a), lds_a, M, 128, 1,
-                pack_lines(M, 128, kb_count), static_cast<uint8_t*>(out)};
+                pack_ctas(M, 128, kb_count), static_cast<uint8_t*>(out)};
   PackOperand b{static_cast<const uint8_t*>(scale_b), lds_b, N, n_tile, (n_tile + 127) / 128,
-                pack_lines(N, n_tile, kb_count), static_cast<uint8_t*>(out) + 16 * a.lines};
-  const int64_t total = a.lines + b.lines;
-  if (total <= 0) return cudaSuccess;
-  const int64_t blocks = std::min<int64_t>((total + kPackThreads - 1) / kPackThreads, 4096);
+                pack_ctas(N, n_tile, kb_count),
+                static_cast<uint8_t*>(out) + 16 * pack_lines(M, 128, kb_count)};
+  const int64_t blocks = a.ctas + b.ctas;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   const cudaError_t e = launch_dependent(pack_mx_scales_kernel, dim3(static_cast<unsigned>(blocks)),
                                          dim3(kPackThreads), 0, stream, a, b, kb_count, nblk);
   count_launches(1);

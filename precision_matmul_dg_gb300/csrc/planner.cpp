@@ -134,7 +134,10 @@ double hbm_bytes_per_us(const dg_hw_desc& hw) {
 // Fraction of the tensor rate a tile shape sustains per busy SM, calibrated on
 // GB300 at 4096^3 (measured time x wave efficiency): wider tiles and CTA pairs
 // move fewer operand bytes through L2 and shared memory per FLOP.
-double tc_tile_efficiency(int n_tile, int cta_group) {
+double tc_tile_efficiency(int n_tile, int cta_group, bool mx = false) {
+  // block-scaled MXFP4 tiles (single CTAs), calibrated at 8192^3: 128 x 224
+  // ran 1.17x as fast as 128 x 128 per FLOP (199 against 233 us)
+  if (mx) return n_tile >= 224 ? 0.86 : 0.73;
   if (cta_group == 2) return n_tile >= 224 ? 0.86 : (n_tile >= 192 ? 0.80 : 0.63);
   switch (n_tile) {
     case 256: return 0.72;
@@ -242,7 +245,8 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
                                                    : 1.0;
     const double t_math =
         waves * tile_flops /
-        (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile, v.cta_group) * conv_eff);
+        (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile, v.cta_group, mx_native) *
+         conv_eff);
     const double bytes = elem_a * M * K + elem_b * N * K + 2.0 * M * N * elem_d;
     const double t_mem = bytes / hbm_bytes_per_us(hw);
     const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
@@ -277,14 +281,16 @@ void add_gemv_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype 
     if (why) *why += "GEMV: M > 8; ";
     return;
   }
-  const int measured = gemv_kernel_regs(M);
-  const int regs = measured > 0 ? measured : kGemvRegsPerThread;
-  if (regs * kGemvThreads > hw.regs_per_sm) {
-    if (why) *why += "GEMV: registers; ";
-    return;
-  }
   const int64_t resident = static_cast<int64_t>(hw.sm_count) * kGemvResidentWarpsPerSm;
   for (int split : kGemvSplits) {
+    // splits of 2 .. 8 run the cluster-reduction variant, the others the
+    // global-memory one: each its own register figure
+    const int measured = gemv_kernel_regs(M, split);
+    const int regs = measured > 0 ? measured : kGemvRegsPerThread;
+    if (regs * kGemvThreads > hw.regs_per_sm) {
+      if (why) *why += "GEMV split " + std::to_string(split) + ": registers; ";
+      continue;
+    }
     int64_t chunk = 0;
     const double t = gemv_estimate_us(M, N, K, split, hw, &chunk);
     if (t < 0) continue;  // the last split would be empty
@@ -510,15 +516,22 @@ double gemv_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_
   const int64_t units = N * split * batch;
   const double active = static_cast<double>(std::min(units, resident));
   const double bw = std::min(hbm_bytes_per_us(hw), active * 2.0e3);
-  const double bytes = batch * (2.0 * (N * K + M * K) + (split > 1 ? 8.0 * split * M * N : 0.0) +
-                                4.0 * M * N);
-  // A warp streams its K range in batches of 4 x 256 elements, one memory
-  // round trip (~0.8 us) each; small problems are bound by that latency.
-  const double batches = static_cast<double>(ceil_div(chunk, 1024));
+  // Splits of 2 .. 8 reduce in a thread-block cluster through distributed
+  // shared memory (no partial sums in global memory, one cluster barrier);
+  // more splits write FP32 partials that the last CTA of a row group reads
+  // back.
+  const bool cluster = split >= 2 && split <= 8;
+  const double partial_bytes = (split > 1 && !cluster) ? 8.0 * split * M * N : 0.0;
+  const double bytes = batch * (2.0 * (N * K + M * K) + partial_bytes + 4.0 * M * N);
+  // A warp streams its K range in batches of 256-element steps (4 at a time,
+  // 8 in the cluster variant), one memory round trip (~0.8 us) each; small
+  // problems are bound by that latency.
+  const double batches = static_cast<double>(ceil_div(chunk, cluster ? 2048 : 1024));
   // Each further row of A costs the FMA loop about 0.65 of the one-row time
   // (measured on GB300 at M = 2..8: 1.7x, 3.0x, 5.8x at M = 2, 4, 8).
   const double rows = 1.0 + 0.65 * static_cast<double>(M - 1);
-  return std::max(bytes / bw, 0.8 * batches) * rows + (split > 1 ? 1.0 : 0.0) + 2.0;
+  const double reduce = split == 1 ? 0.0 : (cluster ? 0.3 : 1.0);
+  return std::max(bytes / bw, 0.8 * batches) * rows + reduce + 2.0;
 }
 
 double gemv_mma_estimate_us(int64_t M, int64_t N, int64_t K, int split, const dg_hw_desc& hw,

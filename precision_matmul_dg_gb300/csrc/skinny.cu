@@ -24,7 +24,12 @@
 // and 2 tig + 8, 2 tig + 9.  The A fragment takes the same four K positions
 // of rows grp and grp + 8 from shared memory, so every MMA step covers 16
 // distinct K values of the window and the K order inside the dot product is
-// merely permuted.  The two K halves are summed in shared memory; the fused
+// merely permuted.  The activation chunk is staged in shared memory in that
+// fragment order (window, step, lane: the lane's four 32-bit A registers
+// side by side), so a step's A fragment is one conflict-free 16-byte load
+// (row-major staging cost two 8-byte loads at a 4-way bank conflict, and the
+// eight column-group warps each read all of A).  The two K halves are summed
+// in shared memory; the fused
 // epilogue (alpha, beta * C, bias, erf-GELU, FP16 rounding) runs on the MMA
 // fragments.  Columns >= N and rows >= M are computed on clamped or zero
 // inputs and never stored; codes at k >= K meet zeroed activations.
@@ -47,9 +52,9 @@ constexpr int kSkWindow = 128;   // codes per window: 16 bytes per lane
 constexpr int kSkBatch = 8;      // windows per warp per chunk (all loads in flight)
 constexpr int kSkPairs = kSkBatch / 2;  // window pairs per warp per chunk
 constexpr int kSkChunk = 2 * kSkBatch * kSkWindow;  // K codes per activation chunk
-constexpr int kSkRowPad = 8;     // halves of padding per activation row
-constexpr int kSkStride = kSkChunk + kSkRowPad;
-constexpr int kSkSmemA = 16 * kSkStride * 2;
+// activations of a chunk in fragment order: [window][step][lane] x 16 bytes
+constexpr int kSkSmemA = (kSkChunk / kSkWindow) * 8 * 32 * 16;
+static_assert(kSkSmemA == 16 * kSkChunk * 2, "16 rows of a chunk");
 constexpr int kSkAPer = 16 * (kSkChunk / 8) / kSkThreads;  // 16-byte pieces per thread
 static_assert(kSkAPer * kSkThreads == 16 * (kSkChunk / 8), "whole pieces per thread");
 constexpr int kSkSmemRed = kSkGroups * 32 * 4 * 4;
@@ -99,7 +104,7 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[
 __global__ void __launch_bounds__(kSkThreads)
     skinny_w4a16_kernel(const SkParams p, const __grid_constant__ EpiProgram prog) {
   extern __shared__ __align__(16) uint8_t sk_smem[];
-  __half* As = reinterpret_cast<__half*>(sk_smem);             // [16][kSkStride]
+  uint32_t* As = reinterpret_cast<uint32_t*>(sk_smem);  // [window][step][lane][4]
   float* red = reinterpret_cast<float*>(sk_smem + kSkSmemA);   // [8 groups][32 lanes][4]
   grid_dependency_wait();  // launched as a dependent of the previous kernel
 
@@ -113,7 +118,9 @@ __global__ void __launch_bounds__(kSkThreads)
   const uint8_t* brow1 =
       p.B + static_cast<int64_t>(min(n0 + 4 + (lane >> 3), p.N - 1)) * p.ldb_bytes;
   const int row_groups = (p.K + 31) / 32;  // 16-byte groups holding codes < K
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // Two independent accumulator chains (even and odd MMA steps): one chain
+  // of dependent MMAs per warp would be bound by the MMA latency.
+  float acc2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 
   for (int kc0 = 0; kc0 < p.K; kc0 += kSkChunk) {
     const int nwin = (min(kSkChunk, p.K - kc0) + kSkWindow - 1) / kSkWindow;
@@ -154,7 +161,18 @@ __global__ void __launch_bounds__(kSkThreads)
           for (int e = 0; e < 8; ++e)
             if (k + e >= p.K) h[e] = __ushort_as_half(0);
         }
-        *reinterpret_cast<uint4*>(As + r * kSkStride + u * 8) = v[i];
+        // the 8 values at chunk offset 8u of row r: window u / 16, lane
+        // group tig = (u / 4) % 4 of row r % 8, steps 2 (u % 4) and the next;
+        // each step's first pair goes to fragment register r / 8, its second
+        // pair to register 2 + r / 8
+        const int w = u >> 4, tig = (u >> 2) & 3, s0 = 2 * (u & 3);
+        const int ln = (r & 7) * 4 + tig, hr = r >> 3;
+        uint32_t* f0 = As + ((w * 8 + s0) * 32 + ln) * 4;
+        uint32_t* f1 = f0 + 32 * 4;  // step s0 + 1
+        f0[hr] = v[i].x;
+        f0[2 + hr] = v[i].y;
+        f1[hr] = v[i].z;
+        f1[2 + hr] = v[i].w;
       }
     }
     __syncthreads();
@@ -174,22 +192,24 @@ __global__ void __launch_bounds__(kSkThreads)
       uint32_t wv[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) wv[j] = grp < 4 ? s0[j] : s1[j];
-      const __half* a_lo = As + grp * kSkStride + w * kSkWindow + 32 * tig;
-      const __half* a_hi = a_lo + 8 * kSkStride;
+      const uint4* af = reinterpret_cast<const uint4*>(As) + w * 8 * 32 + lane;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const uint32_t word = wv[s >> 1];
         const int sh = 16 * (s & 1);
         const uint32_t b0 = e2m1x2_to_f16x2((word >> sh) & 0xFFu);        // codes 4s, 4s+1
         const uint32_t b1 = e2m1x2_to_f16x2((word >> (sh + 8)) & 0xFFu);  // codes 4s+2, 4s+3
-        const uint2 lo = *reinterpret_cast<const uint2*>(a_lo + 4 * s);
-        const uint2 hi = *reinterpret_cast<const uint2*>(a_hi + 4 * s);
-        const uint32_t a[4] = {lo.x, hi.x, lo.y, hi.y};
-        mma_m16n8k16(acc, a, b0, b1);
+        // rows grp and grp + 8 at the step's K positions 32 tig + 4s .. + 3
+        const uint4 f = af[s * 32];
+        const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+        mma_m16n8k16(acc2[s & 1], a, b0, b1);
       }
     }
   }
 
+  float acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = acc2[0][j] + acc2[1][j];
   // the two K halves of each column group
   if (kh == 1) {
 #pragma unroll

@@ -58,8 +58,11 @@ def _assert_quantize_parity(dg, x, K, rows=None):
     assert (s[:, nblk:] == CANARY).all(), "scales written past the row"
 
 
+# ragged K (33, 1, 1000), and long rows (8200, 12296, 4104: more than one
+# trip of a row's lanes, the last one short)
 @pytest.mark.parametrize("shape", [(1, 32), (3, 40), (2, 33), (5, 1), (64, 1000), (257, 4096),
-                                   (1000, 96), (7, 8)], ids=lambda s: "%dx%d" % s)
+                                   (1000, 96), (7, 8), (9, 8200), (3, 12296), (5, 4104)],
+                         ids=lambda s: "%dx%d" % s)
 def test_quantize_parity(dg, shape):
     rows, K = shape
     x = workloads.mx_activations(rows, K, seed=rows * 7 + K)

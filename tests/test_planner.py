@@ -274,7 +274,7 @@ def test_skinny_plans(dg, M):
     p = sk[0]
     assert (p["m_tile"], p["n_tile"], p["k_tile"], p["split_k"]) == (16, 64, 2048, 2)
     assert p["threads"] == 512 and p["grid"] == math.ceil(N / 64)
-    assert p["smem_bytes"] == 16 * (2048 + 8) * 2 + 8 * 32 * 4 * 4
+    assert p["smem_bytes"] == 16 * 2048 * 2 + 8 * 32 * 4 * 4
     assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
     # it streams the weights once: ranked first for the HBM-bound shape
     assert plans[0]["kernel_name"] == "skinny"
