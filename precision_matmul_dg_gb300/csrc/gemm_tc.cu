@@ -84,9 +84,11 @@ struct TcParams {
     struct {
       int32_t alpha_i, beta_i;  // integer scalars of the INT32 output
     };
-    // MXFP4 operands: the block scales of A, then of B, packed per tile and
-    // K block in the layout the scale copies into tensor memory read
-    const uint8_t* sf;
+    // MXFP4 operands: the first 16-byte line of B's section in the packed
+    // scales (A's section starts at line 0; see tmap_sf)
+    struct {
+      int32_t sf_b_line0, sf_unused;
+    };
   };
   int* status;
   uint64_t timeout_ns;
@@ -118,8 +120,10 @@ template <int BN, int Stages, int CG, int Kind = kKind16>
 struct TcSmem {
   static constexpr int kRowsB = BN / CG;  // B rows this CTA loads
   static constexpr int kTileBytesB = kRowsB * kBlockK * 2;
-  // MXFP4: scale images of a stage, A's 128 rows then B's rows in 128-row blocks
-  static constexpr int kSfBlocksB = (kRowsB + 127) / 128;
+  // MXFP4: scale images of a stage, this CTA's 128 rows of A, then the whole
+  // B tile's rows in 128-row blocks (a CTA pair's MMA reads every column's
+  // scales in each CTA's tensor memory)
+  static constexpr int kSfBlocksB = (BN + 127) / 128;
   static constexpr int kSfBytes = Kind == kKindMx ? kMxSfRowBlock * (1 + kSfBlocksB) : 0;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + Stages * kTileBytesA;
@@ -138,6 +142,16 @@ struct TcSmem {
 };
 
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
+
+// First 16-byte line, in the packed MXFP4 scales, of 128-row group g of A at
+// K block kb (1024 bytes = 64 lines per group and K block), and of N tile
+// n_blk of B (blocks128 x 64 lines per tile and K block, after A's section).
+__device__ __forceinline__ int32_t sf_line_a(const TcParams& p, int g, int kb) {
+  return (g * p.num_k_blocks + kb) * 64;
+}
+__device__ __forceinline__ int32_t sf_line_b(const TcParams& p, int n_blk, int kb, int blocks128) {
+  return p.sf_b_line0 + (n_blk * p.num_k_blocks + kb) * 64 * blocks128;
+}
 
 // Staged epilogue: epilogue warp wi (0..7) owns TMEM lane quarter wi & 3 and
 // half wi >> 2 of the tile's 32-column chunks.  Its chunks form one stream over
@@ -185,11 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c,
-                       const __grid_constant__ CUtensorMap tmap_d, const TcParams p,
+                       const __grid_constant__ CUtensorMap tmap_d,
+                       const __grid_constant__ CUtensorMap tmap_sf, const TcParams p,
                        const __grid_constant__ EpiProgram prog) {
   using L = TcSmem<BN, Stages, CG, Kind>;
   constexpr bool kMx = Kind == kKindMx;
-  static_assert(!kMx || (CG == 1 && Out == kOutF16), "MXFP4: single CTAs, FP16 output");
+  static_assert(!kMx || Out == kOutF16, "MXFP4: FP16 output");
   // two FP32 accumulators (the INT32 mode keeps its running sums in registers);
   // MXFP4 adds two buffers of scale words after them: A's 128 rows (4
   // columns per scale word, one per 32-row group) and B's rows (one column
@@ -308,22 +323,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kMx) {
               // this stage's scale images: A's row block, then B's tile
               uint8_t* dst_sf = smem_sf + stage * L::kSfBytes;
-              const uint8_t* sfa =
-                  p.sf + (static_cast<int64_t>(m_blk) * p.num_k_blocks + kb) * kMxSfRowBlock;
-              const uint8_t* sfb =
-                  p.sf + static_cast<int64_t>(p.num_m_blocks) * p.num_k_blocks * kMxSfRowBlock +
-                  (static_cast<int64_t>(n_blk) * p.num_k_blocks + kb) * kMxSfRowBlock *
-                      L::kSfBlocksB;
-              bulk_load_g2s(dst_sf, sfa, kMxSfRowBlock, &full_bar[stage], pol);
-              bulk_load_g2s(dst_sf + kMxSfRowBlock, sfb, kMxSfRowBlock * L::kSfBlocksB,
-                            &full_bar[stage], pol);
+              tma_load_2d(&tmap_sf, &full_bar[stage], dst_sf, 0, sf_line_a(p, m_blk, kb), pol);
+#pragma unroll
+              for (int h = 0; h < L::kSfBlocksB; ++h)
+                tma_load_2d(&tmap_sf, &full_bar[stage], dst_sf + kMxSfRowBlock * (1 + h), 0,
+                            sf_line_b(p, n_blk, kb, L::kSfBlocksB) + 64 * h, pol);
             }
           } else {
             // both CTAs' copies complete on the even CTA's full barrier
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], p.stage_tx);
             const uint32_t bar0 = mapa_shared(smem_addr(&full_bar[stage]), 0);
-            tma_load_2d_pair(&tmap_a, bar0, dst_a, kb * kBlockK, a_row, pol);
-            tma_load_2d_pair(&tmap_b, bar0, dst_b, kb * kBlockK, b_row, pol);
+            tma_load_2d_pair(&tmap_a, bar0, dst_a, kb * (kMx ? 128 : kBlockK), a_row, pol);
+            tma_load_2d_pair(&tmap_b, bar0, dst_b, kb * (kMx ? 128 : kBlockK), b_row, pol);
+            if (kMx) {
+              // this CTA's 128 rows of A scales, and the whole B tile's
+              uint8_t* dst_sf = smem_sf + stage * L::kSfBytes;
+              tma_load_2d_pair(&tmap_sf, bar0, dst_sf, 0,
+                               sf_line_a(p, m_blk * CG + static_cast<int>(rank), kb), pol);
+#pragma unroll
+              for (int h = 0; h < L::kSfBlocksB; ++h)
+                tma_load_2d_pair(&tmap_sf, bar0, dst_sf + kMxSfRowBlock * (1 + h), 0,
+                                 sf_line_b(p, n_blk, kb, L::kSfBlocksB) + 64 * h, pol);
+            }
           }
           ++issued;
           if (first_c && issued == Stages) initial_c();
@@ -390,21 +411,36 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t src = smem_addr(smem_sf + stage * L::kSfBytes);
 #pragma unroll
               for (int w = 0; w < 2; ++w) {
-                tc_cp_32x128b_warpx4(sfa_t + 4 * w, smem_desc_rows16(src + w * kMxSfImage));
+                // a pair's copy fills both CTAs' tensor memory, each from its
+                // own shared memory at the same offset
+                const uint32_t sa = sfa_t + 4 * w;
+                const uint64_t da = smem_desc_rows16(src + w * kMxSfImage);
+                if (CG == 2)
+                  tc_cp_32x128b_warpx4_pair(sa, da);
+                else
+                  tc_cp_32x128b_warpx4(sa, da);
 #pragma unroll
-                for (int h = 0; h < L::kSfBlocksB; ++h)
-                  tc_cp_32x128b_warpx4(
-                      sfb_t + w * 4 * L::kSfBlocksB + 4 * h,
-                      smem_desc_rows16(src + kMxSfRowBlock * (1 + h) + w * kMxSfImage));
+                for (int h = 0; h < L::kSfBlocksB; ++h) {
+                  const uint32_t sb = sfb_t + w * 4 * L::kSfBlocksB + 4 * h;
+                  const uint64_t db = smem_desc_rows16(src + kMxSfRowBlock * (1 + h) + w * kMxSfImage);
+                  if (CG == 2)
+                    tc_cp_32x128b_warpx4_pair(sb, db);
+                  else
+                    tc_cp_32x128b_warpx4(sb, db);
+                }
               }
               // MMA k (K = 64, scale blocks 2k and 2k + 1) reads word k / 2
               // at byte 2 (k % 2)
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-                tc_mma_mxf4(d_tmem, da0 + 2 * k, db0 + 2 * k,
-                            idesc_mxf4(kBlockM, BN, 2u * (k & 1)),
-                            sfa_t + 4 * (k >> 1), sfb_t + (k >> 1) * 4 * L::kSfBlocksB, accum);
+                const uint32_t id = idesc_mxf4(kTileM, BN, 2u * (k & 1));
+                const uint32_t sa = sfa_t + 4 * (k >> 1);
+                const uint32_t sb = sfb_t + (k >> 1) * 4 * L::kSfBlocksB;
+                if (CG == 2)
+                  tc_mma_mxf4_pair(d_tmem, da0 + 2 * k, db0 + 2 * k, id, sa, sb, accum);
+                else
+                  tc_mma_mxf4(d_tmem, da0 + 2 * k, db0 + 2 * k, id, sa, sb, accum);
               }
               sf_buf ^= 1;
             } else {
@@ -814,7 +850,15 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   const bool staged = !(a.epi & kEpiOutI8) && a.ldd % vec == 0 &&
                       (reinterpret_cast<uintptr_t>(a.D) & 15) == 0 &&
                       (!c_tma || (a.ldc % vec == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0));
-  CUtensorMap tc_map = ta, td_map = ta;  // copies of a map that the kernel does not use
+  CUtensorMap tc_map = ta, td_map = ta, tsf_map = ta;  // copies of a map the kernel does not use
+  if (kMx) {
+    // the packed scales as rows of 16 bytes: A's section, then B's; boxes of
+    // 64 lines (1 KB: 128 rows x 8 scales)
+    const int64_t lines = pack_mx_scales_bytes(a.M, a.N, a.K, BN) / 16;
+    e = tc::make_map_2d(&tsf_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sf_packed, lines, 16, 16, 64,
+                        16, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+  }
   if (staged) {
     e = Out == kOutF16 ? tc::make_f16_epi_map(&td_map, a.D, a.M, a.N, a.ldd)
                        : tc::make_i32_epi_map(&td_map, a.D, a.M, a.N, a.ldd);
@@ -842,14 +886,18 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.ldd = a.ldd;
   p.bias = static_cast<const __half*>(a.bias);
   if (kMx) {
-    p.sf = static_cast<const uint8_t*>(a.sf_packed);
+    // A's section: ceil(M / 128) groups x K blocks x 64 lines
+    p.sf_b_line0 = static_cast<int32_t>((a.M + 127) / 128 * p.num_k_blocks * 64);
+    p.sf_unused = 0;
   } else {
     p.alpha_i = static_cast<int32_t>(a.alpha);
     p.beta_i = static_cast<int32_t>(a.beta);
   }
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB) + L::kSfBytes);
+  // bytes one stage brings in: both CTAs' operand tiles (and, for MXFP4,
+  // both CTAs' scale images), counted on the even CTA's barrier for a pair
+  p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB + L::kSfBytes));
   p.staged = staged ? 1 : 0;
   p.idesc_ab = a.bf16_ab ? idesc_ab_bf16() : 0u;
 
@@ -903,7 +951,7 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs += 1;
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc_map, td_map, p, make_program(a));
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc_map, td_map, tsf_map, p, make_program(a));
   count_launches(1);
   return e;
 }
@@ -935,7 +983,12 @@ int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32) {
   return 0;
 }
 
-int mx_kernel_regs(int n_tile, int stages) {
+int mx_kernel_regs(int n_tile, int stages, int cta_group) {
+  if (cta_group == 2) {
+    if (n_tile == 224 && stages == 5) return regs_of<224, 5, 2, kOutF16, kKindMx>();
+    if (n_tile == 192 && stages == 6) return regs_of<192, 6, 2, kOutF16, kKindMx>();
+    return 0;
+  }
   if (n_tile == 224 && stages == 4) return regs_of<224, 4, 1, kOutF16, kKindMx>();
   if (n_tile == 128 && stages == 5) return regs_of<128, 5, 1, kOutF16, kKindMx>();
   return 0;
@@ -982,7 +1035,11 @@ cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
 // in a.sf_packed, both operands' scales packed by pack_mx_scales for this
 // plan's N_tile.
 cudaError_t launch_tc_mx(const GemmArgs& a, const dg_tile_plan& plan) {
-  if (plan.cta_group != 1) return cudaErrorNotSupported;
+  if (plan.cta_group == 2) {
+    if (plan.n_tile == 224 && plan.stages == 5) return run_tc<224, 5, 2, kOutF16, kKindMx>(a, plan);
+    if (plan.n_tile == 192 && plan.stages == 6) return run_tc<192, 6, 2, kOutF16, kKindMx>(a, plan);
+    return cudaErrorNotSupported;
+  }
   if (plan.n_tile == 224 && plan.stages == 4) return run_tc<224, 4, 1, kOutF16, kKindMx>(a, plan);
   if (plan.n_tile == 128 && plan.stages == 5) return run_tc<128, 5, 1, kOutF16, kKindMx>(a, plan);
   return cudaErrorNotSupported;

@@ -130,7 +130,7 @@ struct GemmArgs {
 // split-K GEMV and warp-MMA GEMV for M rows (gemv.cu), skinny W4A16 kernel
 // (skinny.cu).  0 too for a variant that is not compiled.
 int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32);
-int mx_kernel_regs(int n_tile, int stages);  // the MXFP4 block-scaled kernel (gemm_tc.cu)
+int mx_kernel_regs(int n_tile, int stages, int cta_group);  // MXFP4 block-scaled (gemm_tc.cu)
 int conv_kernel_regs(dg_dtype da, dg_dtype db, int n_tile, int stages);
 int gemv_kernel_regs(int64_t M, int split);
 int gemv_mma_kernel_regs(int64_t M);

@@ -49,7 +49,8 @@ constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {192, 6, 2, 0}};
 constexpr TcVariant kTcVariantsE2M1[] = {{256, 6, 1, 2}, {128, 8, 1, 3}, {64, 8, 1, 4}};
 // MXFP4 x MXFP4 on the block-scaled MMA (the tensor-core kernel with packed
 // E2M1 stages and scale images; single CTAs)
-constexpr TcVariant kTcVariantsMx[] = {{224, 4, 1, 0}, {128, 5, 1, 0}};
+constexpr TcVariant kTcVariantsMx[] = {{224, 4, 1, 0}, {128, 5, 1, 0}, {224, 5, 2, 0},
+                                       {192, 6, 2, 0}};
 // E2M1 values per MMA FLOP relative to FP16: the block-scaled 4-bit MMA runs
 // at four times the 16-bit rate (the nominal Blackwell ratio)
 constexpr double kMxRateRatio = 4.0;
@@ -73,7 +74,7 @@ TcFamily tc_family(dg_dtype da, dg_dtype db) {
   if (da == DG_F16 && db == DG_F16) return {kTcVariantsF16, kNumTcVariantsF16, kTcThreads};
   if (da == DG_I8 && db == DG_I8) return {kTcVariantsI8, 1, kConvThreads};
   if (da == DG_F16 && db == DG_E2M1) return {kTcVariantsE2M1, 3, kConvThreads};
-  if (da == DG_MXF4 && db == DG_MXF4) return {kTcVariantsMx, 2, kTcThreads};
+  if (da == DG_MXF4 && db == DG_MXF4) return {kTcVariantsMx, 4, kTcThreads};
   return {nullptr, 0, 0};
 }
 
@@ -83,8 +84,10 @@ TcFamily tc_family(dg_dtype da, dg_dtype db) {
 // packed-E2M1 B) plus `cv_stages` slots of widened FP16 operands.
 int tc_ring_bytes(dg_dtype da, dg_dtype db, const TcVariant& v) {
   const int a16 = kTcBlockM * kTcBlockK * 2;
-  if (da == DG_MXF4 && db == DG_MXF4)  // 128-byte rows of codes, plus the scale images
-    return v.stages * (a16 + v.n_tile * kTcBlockK * 2 + 1024 * (1 + (v.n_tile + 127) / 128));
+  if (da == DG_MXF4 && db == DG_MXF4)  // 128-byte rows of codes (a CTA of a pair holds half
+                                       // of B's), the scale images (the whole B tile's)
+    return v.stages * (a16 + (v.n_tile / v.cta_group) * kTcBlockK * 2 +
+                       1024 * (1 + (v.n_tile + 127) / 128));
   if (da == DG_F16 && db == DG_F16)
     return v.stages * (a16 + (v.n_tile / v.cta_group) * kTcBlockK * 2);
   const int in_a = da == DG_I8 ? kTcBlockM * kTcBlockK : a16;
@@ -135,8 +138,10 @@ double hbm_bytes_per_us(const dg_hw_desc& hw) {
 // GB300 at 4096^3 (measured time x wave efficiency): wider tiles and CTA pairs
 // move fewer operand bytes through L2 and shared memory per FLOP.
 double tc_tile_efficiency(int n_tile, int cta_group, bool mx = false) {
-  // block-scaled MXFP4 tiles (single CTAs), calibrated at 8192^3: 128 x 224
-  // ran 1.17x as fast as 128 x 128 per FLOP (199 against 233 us)
+  // block-scaled MXFP4 tiles, calibrated at 8192^3: single CTAs 128 x 224
+  // ran 1.17x as fast as 128 x 128 per FLOP (199 against 233 us), CTA pairs
+  // 256 x 224 and 256 x 192 took 184 and 191 us against 210 for 128 x 224
+  if (mx && cta_group == 2) return n_tile >= 224 ? 0.98 : 0.945;
   if (mx) return n_tile >= 224 ? 0.86 : 0.73;
   if (cta_group == 2) return n_tile >= 224 ? 0.86 : (n_tile >= 192 ? 0.80 : 0.63);
   switch (n_tile) {
@@ -214,7 +219,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
       if (why) *why += name + ": tensor memory; ";
       continue;
     }
-    const int measured = mx_native ? mx_kernel_regs(v.n_tile, v.stages)
+    const int measured = mx_native ? mx_kernel_regs(v.n_tile, v.stages, v.cta_group)
                          : (ka == DG_F16 && kb == DG_F16)
                              ? tc_kernel_regs(v.n_tile, v.stages, v.cta_group,
                                               widened && da == DG_I8)

@@ -450,6 +450,26 @@ __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sr
                : "memory");
 }
 
+// Pair forms (issued by the even CTA of a CTA pair): the block-scaled MMA
+// over both CTAs' operands (256 rows of A, each CTA's accumulator rows in its
+// own tensor memory), and the scale copy into both CTAs' tensor memory.
+__device__ __forceinline__ void tc_mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa_tmem,
+                                                 uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], "
+      "p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t src) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src)
+               : "memory");
+}
+
 // Shared-memory descriptor of an unswizzled K-major matrix of 16-byte rows
 // stored back to back (8-row groups 128 bytes apart): the source layout of
 // tc_cp_32x128b_warpx4.  Start address >> 4 (bits 0-13), stride byte offset

@@ -24,12 +24,13 @@
 // and 2 tig + 8, 2 tig + 9.  The A fragment takes the same four K positions
 // of rows grp and grp + 8 from shared memory, so every MMA step covers 16
 // distinct K values of the window and the K order inside the dot product is
-// merely permuted.  The activation chunk is staged in shared memory in that
-// fragment order (window, step, lane: the lane's four 32-bit A registers
-// side by side), so a step's A fragment is one conflict-free 16-byte load
-// (row-major staging cost two 8-byte loads at a 4-way bank conflict, and the
-// eight column-group warps each read all of A).  The two K halves are summed
-// in shared memory; the fused
+// merely permuted.  The activation chunk is staged in shared memory twice:
+// row-major as loaded (16-byte stores), then rearranged once into fragment
+// order (window, step, lane: the lane's four 32-bit A registers side by
+// side), so that in the MMA loop a step's A fragment is one conflict-free
+// 16-byte load.  Read row-major, every step cost two 8-byte loads at a
+// 4-way bank conflict, and the eight column-group warps each read all of A.
+// The two K halves are summed in shared memory; the fused
 // epilogue (alpha, beta * C, bias, erf-GELU, FP16 rounding) runs on the MMA
 // fragments.  Columns >= N and rows >= M are computed on clamped or zero
 // inputs and never stored; codes at k >= K meet zeroed activations.
@@ -55,10 +56,13 @@ constexpr int kSkChunk = 2 * kSkBatch * kSkWindow;  // K codes per activation ch
 // activations of a chunk in fragment order: [window][step][lane] x 16 bytes
 constexpr int kSkSmemA = (kSkChunk / kSkWindow) * 8 * 32 * 16;
 static_assert(kSkSmemA == 16 * kSkChunk * 2, "16 rows of a chunk");
+// and row-major as loaded, rows padded by 16 bytes
+constexpr int kSkRowStride = kSkChunk + 8;  // halves
+constexpr int kSkSmemRows = 16 * kSkRowStride * 2;
 constexpr int kSkAPer = 16 * (kSkChunk / 8) / kSkThreads;  // 16-byte pieces per thread
 static_assert(kSkAPer * kSkThreads == 16 * (kSkChunk / 8), "whole pieces per thread");
 constexpr int kSkSmemRed = kSkGroups * 32 * 4 * 4;
-constexpr int kSkSmem = kSkSmemA + kSkSmemRed;
+constexpr int kSkSmem = kSkSmemA + kSkSmemRows + kSkSmemRed;
 
 struct SkParams {
   int M, N, K;
@@ -105,7 +109,8 @@ __global__ void __launch_bounds__(kSkThreads)
     skinny_w4a16_kernel(const SkParams p, const __grid_constant__ EpiProgram prog) {
   extern __shared__ __align__(16) uint8_t sk_smem[];
   uint32_t* As = reinterpret_cast<uint32_t*>(sk_smem);  // [window][step][lane][4]
-  float* red = reinterpret_cast<float*>(sk_smem + kSkSmemA);   // [8 groups][32 lanes][4]
+  __half* Ar = reinterpret_cast<__half*>(sk_smem + kSkSmemA);  // [16][kSkRowStride]
+  float* red = reinterpret_cast<float*>(sk_smem + kSkSmemA + kSkSmemRows);  // [8][32][4]
   grid_dependency_wait();  // launched as a dependent of the previous kernel
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,19 +166,21 @@ __global__ void __launch_bounds__(kSkThreads)
           for (int e = 0; e < 8; ++e)
             if (k + e >= p.K) h[e] = __ushort_as_half(0);
         }
-        // the 8 values at chunk offset 8u of row r: window u / 16, lane
-        // group tig = (u / 4) % 4 of row r % 8, steps 2 (u % 4) and the next;
-        // each step's first pair goes to fragment register r / 8, its second
-        // pair to register 2 + r / 8
-        const int w = u >> 4, tig = (u >> 2) & 3, s0 = 2 * (u & 3);
-        const int ln = (r & 7) * 4 + tig, hr = r >> 3;
-        uint32_t* f0 = As + ((w * 8 + s0) * 32 + ln) * 4;
-        uint32_t* f1 = f0 + 32 * 4;  // step s0 + 1
-        f0[hr] = v[i].x;
-        f0[2 + hr] = v[i].y;
-        f1[hr] = v[i].z;
-        f1[2 + hr] = v[i].w;
+        *reinterpret_cast<uint4*>(Ar + r * kSkRowStride + u * 8) = v[i];
       }
+    }
+    __syncthreads();
+    // fragment slot q = (window w, step s, lane (grp, tig)): rows grp and
+    // grp + 8 at window offset 32 tig + 4s .. + 3, as the registers
+    // {row grp (+0, +1), row grp + 8 (+0, +1), row grp (+2, +3), row grp + 8 (+2, +3)}
+#pragma unroll
+    for (int i = 0; i < (kSkSmemA / 16) / kSkThreads; ++i) {
+      const int q = threadIdx.x + i * kSkThreads;
+      const int ln = q & 31, st = (q >> 5) & 7, w = q >> 8;
+      const int k = w * kSkWindow + 32 * (ln & 3) + 4 * st;
+      const uint2 lo = *reinterpret_cast<const uint2*>(Ar + (ln >> 2) * kSkRowStride + k);
+      const uint2 hi = *reinterpret_cast<const uint2*>(Ar + ((ln >> 2) + 8) * kSkRowStride + k);
+      reinterpret_cast<uint4*>(As)[q] = make_uint4(lo.x, hi.x, lo.y, hi.y);
     }
     __syncthreads();
     // lane (grp, tig) takes, for window h of a pair, piece 4h + tig of row

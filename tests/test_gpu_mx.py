@@ -255,16 +255,20 @@ def test_gemm_mxf4_padded_operands(dg, shape):
     _assert_gemm_parity(case, got)
 
 
-@pytest.mark.parametrize("shape", [(256, 520, 640), (300, 460, 1000), (1, 100, 64)],
+@pytest.mark.parametrize("shape", [(256, 520, 640), (300, 460, 1000), (1, 100, 64),
+                                   (520, 700, 512)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_gemm_mxf4_every_plan(dg, shape):
     # every plan the planner offers for the shape, the block-scaled MMA's
-    # tiles (N_tile 224 and 128) and the BF16 widening's, against the oracle
+    # tiles (single CTAs: N_tile 224 and 128; CTA pairs: 256 x 224 and
+    # 256 x 192) and the BF16 widening's, against the oracle
     M, N, K = shape
     case = workloads.mxf4_case(M, N, K, alpha=1.25, beta=-0.5, epilogue="bias_gelu", seed=M + K)
     plans = dg.plan_tiles(M, N, K, "mxf4", "mxf4", max_out=64)
-    native = {(p["n_tile"], p["stages"]) for p in plans if p["kernel_name"] == "tc"}
-    assert native == {(224, 4), (128, 5)}
+    native = {(p["n_tile"], p["stages"], p["cta_group"]) for p in plans
+              if p["kernel_name"] == "tc"}
+    want = {(224, 4, 1), (128, 5, 1)} | ({(224, 5, 2), (192, 6, 2)} if M > 128 else set())
+    assert native == want
     for plan in plans:
         got = _run_gemm(dg, case, plan=plan)
         _assert_gemm_parity(case, got)

@@ -274,7 +274,7 @@ def test_skinny_plans(dg, M):
     p = sk[0]
     assert (p["m_tile"], p["n_tile"], p["k_tile"], p["split_k"]) == (16, 64, 2048, 2)
     assert p["threads"] == 512 and p["grid"] == math.ceil(N / 64)
-    assert p["smem_bytes"] == 16 * 2048 * 2 + 8 * 32 * 4 * 4
+    assert p["smem_bytes"] == 16 * 2048 * 2 + 16 * (2048 + 8) * 2 + 8 * 32 * 4 * 4
     assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
     # it streams the weights once: ranked first for the HBM-bound shape
     assert plans[0]["kernel_name"] == "skinny"
@@ -283,11 +283,12 @@ def test_skinny_plans(dg, M):
                 if q["kernel_name"] == "skinny"]
 
 
-def mx_smem(n_tile, stages):
-    # 128-byte rows of packed codes for A (128 rows) and B, the stage's scale
-    # images (1 KB per 128 rows), the FP16 output staging boxes, barriers and
-    # the 1 KB alignment slack
-    return (stages * (128 * 128 + n_tile * 128 + 1024 * (1 + math.ceil(n_tile / 128)))
+def mx_smem(n_tile, stages, cg):
+    # 128-byte rows of packed codes for A (128 rows) and B (a CTA of a pair
+    # holds half of the tile's rows), the stage's scale images (1 KB per 128
+    # rows: this CTA's A rows and the whole B tile), the FP16 output staging
+    # boxes, barriers and the 1 KB alignment slack
+    return (stages * (128 * 128 + (n_tile // cg) * 128 + 1024 * (1 + math.ceil(n_tile / 128)))
             + EPI_STAGING + 512 + 1024)
 
 
@@ -302,9 +303,12 @@ def test_mxf4_plans(dg):
         for p in plans:
             if p["kernel_name"] != "tc":
                 continue
-            assert (p["m_tile"], p["k_tile"], p["cta_group"]) == (128, 256, 1)
-            assert (p["n_tile"], p["stages"]) in ((224, 4), (128, 5))
-            assert p["smem_bytes"] == mx_smem(p["n_tile"], p["stages"])
+            cg = p["cta_group"]
+            assert (p["m_tile"], p["k_tile"]) == (128 * cg, 256)
+            assert (p["n_tile"], p["stages"], cg) in ((224, 4, 1), (128, 5, 1), (224, 5, 2),
+                                                      (192, 6, 2))
+            assert cg == 1 or shape[0] > 128   # a pair needs more than one CTA's rows
+            assert p["smem_bytes"] == mx_smem(p["n_tile"], p["stages"], cg)
             assert p["smem_bytes"] <= GB300["smem_per_block_optin"]
             sf_cols = 2 * (8 + 8 * math.ceil(p["n_tile"] / 128))
             assert 2 * p["n_tile"] + sf_cols <= GB300["tmem_cols"]
