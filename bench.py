@@ -186,6 +186,7 @@ KERNEL_SOURCES = {
     "gemm_conv_tc_kernel": ("gemm_conv.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh",
                             "internal.h"),
     "gemv_splitk_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
+    "gemv_cluster_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
     "gemv_mma_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
     "skinny_w4a16_kernel": ("skinny.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
 }
@@ -200,9 +201,10 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current sources of that kernel and on this workload; else None."""
+def recorded_capture(kernel, workload):
+    """The committed ncu launch-list entry of a kernel on a workload (DRAM
+    bytes per launch, the kernel's share of the step's launch time), if it
+    was taken on the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -211,7 +213,12 @@ def recorded_traffic(kernel, workload):
     e = d.get(kernel, {}).get(workload)
     if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
-    return e.get("dram_bytes_per_launch")
+    return e
+
+
+def recorded_traffic(kernel, workload):
+    e = recorded_capture(kernel, workload)
+    return e.get("dram_bytes_per_launch") if e else None
 
 
 def workload_info(name):
@@ -262,7 +269,8 @@ def kernel_name(plan, case):
     (FP16; widened INT8 / E2M1 / MXFP4 operands; MXFP4 on the block-scaled
     MMA) or the converting kernel."""
     if plan["kernel_name"] == "gemv":
-        return "gemv_splitk_kernel"
+        # 2 .. 8 splits reduce inside a thread-block cluster
+        return "gemv_cluster_kernel" if 2 <= plan["split_k"] <= 8 else "gemv_splitk_kernel"
     if plan["kernel_name"] == "skinny":
         return "skinny_w4a16_kernel"
     if plan["kernel_name"] == "gemv_mma":
@@ -440,7 +448,12 @@ def roofline(w, kern_avg_ms, peaks, peak_src):
             roof["peak_source"] += ("; INT8 runs on the FP16 tensor path (sm_103a has no "
                                     "integer tcgen05 MMA), so its denominator is the FP16 peak")
         if base.dtype_a == "mxf4":
-            roof["peak_source"] += "; the MXFP4 step is measured against the 16-bit peak"
+            # block-scaled 4-bit operands: the FP4 dense peak, the measured
+            # bf16 burst times the nominal FP4 / bf16 ratio (13.5 / 2.25)
+            peak = round(peaks["bf16_tflops"] * 6.0, 1)
+            roof.update(peak=peak, frac=round(achieved / peak, 4),
+                        peak_source="%s bf16 dense burst x 6 (nominal FP4 / bf16 dense ratio)"
+                                    % peak_src)
     else:
         gbs = algorithmic_bytes(base) / (kern_avg_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -450,6 +463,14 @@ def roofline(w, kern_avg_ms, peaks, peak_src):
     roof["kernel"] = kname
     roof["kernel_avg_us"] = round(kern_avg_ms * 1e3, 2)
     roof["traffic"] = recorded_traffic(kname, w.name)
+    steps = STEP_KERNELS.get(w.name)
+    if steps:
+        # A step of several launches: `achieved` divides by the whole step's
+        # time; the committed launch list gives the dominant kernel's share
+        cap = recorded_capture(kname, w.name)
+        roof["step_kernels"] = steps
+        roof["timed"] = "the whole step (every launch of it)"
+        roof["share_of_step_ncu"] = cap.get("share_of_step") if cap else None
     roof["algorithmic_bytes"] = algorithmic_bytes(base)
     roof["algorithmic_flops"] = flops
     return roof
@@ -674,6 +695,10 @@ def run_dg(args, world, rank, local):
 # the two thin M = 1 shapes, W4A16 at M = 16 and 2048, block-scaled FP4).
 DEFAULT_CONFIGS = ("f16_256", "f16_2048", "f16_8192", "i8_4096", "thin_1x4096x131072",
                    "thin_1x256x12800", "w4a16_m16", "w4a16_m2048", "mxf4_4096")
+# Steps of more than one launch (the dominant kernel last).
+STEP_KERNELS = {"i8_4096": ["widen_dense_kernel", "gemm_tc_kernel"],
+                "w4a16_m2048": ["widen_dense_kernel", "gemm_tc_kernel"],
+                "mxf4_4096": ["quantize_mxf4_kernel", "pack_mx_scales_kernel", "gemm_tc_kernel"]}
 # Workloads of a few microseconds a step, also timed as a CUDA-graph replay.
 GRAPH_TOO = ("f16_256", "thin_1x256x12800", "w4a16_m16")
 
