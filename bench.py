@@ -698,7 +698,7 @@ DEFAULT_CONFIGS = ("f16_256", "f16_2048", "f16_8192", "i8_4096", "thin_1x4096x13
 # Steps of more than one launch (the dominant kernel last).
 STEP_KERNELS = {"i8_4096": ["widen_dense_kernel", "gemm_tc_kernel"],
                 "w4a16_m2048": ["widen_dense_kernel", "gemm_tc_kernel"],
-                "mxf4_4096": ["quantize_mxf4_kernel", "pack_mx_scales_kernel", "gemm_tc_kernel"]}
+                "mxf4_4096": ["quantize_mxf4_kernel", "gemm_tc_kernel"]}
 # Workloads of a few microseconds a step, also timed as a CUDA-graph replay.
 GRAPH_TOO = ("f16_256", "thin_1x256x12800", "w4a16_m16")
 

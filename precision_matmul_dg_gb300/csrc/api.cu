@@ -492,17 +492,36 @@ dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev) {
     e = launch_skinny(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC && da == DG_MXF4) {
     // MXFP4 on the block-scaled MMA: the codes go to the tensor cores as
-    // they are; the scales are first packed into the order the kernel
-    // copies into tensor memory.
-    const int64_t bytes = pack_mx_scales_bytes(M, N, K, plan.n_tile);
-    __half* packed = nullptr;
-    s = get_wide_workspace(dev, stream, (bytes + 1) / 2, &packed);
-    if (s != DG_OK) return s;
-    e = launch_pack_mx_scales(M, N, K, plan.n_tile, a.scale_a, a.lds_a, a.scale_b, a.lds_b,
-                              packed, stream);
-    if (e != cudaSuccess) return fail_cuda(e, "scale packing launch");
+    // they are, and the kernel loads the scale bytes with TMA, 16 bytes of a
+    // row at a time, so each operand's scale rows must start on 16-byte
+    // boundaries.  Other scale layouts are first copied into the workspace
+    // with a 16-byte row pitch.
     GemmArgs w = a;
-    w.sf_packed = packed;
+    const int64_t nblk = (K + 31) / 32, pitch = (nblk + 15) / 16 * 16;
+    const bool fit_a = (reinterpret_cast<uintptr_t>(a.scale_a) & 15) == 0 && a.lds_a % 16 == 0;
+    const bool fit_b = (reinterpret_cast<uintptr_t>(a.scale_b) & 15) == 0 && a.lds_b % 16 == 0;
+    if (!fit_a || !fit_b) {
+      const int64_t bytes = (fit_a ? 0 : M * pitch) + (fit_b ? 0 : N * pitch);
+      __half* ws = nullptr;
+      s = get_wide_workspace(dev, stream, (bytes + 1) / 2, &ws);
+      if (s != DG_OK) return s;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(ws);
+      if (!fit_a) {
+        e = cudaMemcpy2DAsync(dst, pitch, a.scale_a, a.lds_a, nblk, M, cudaMemcpyDeviceToDevice,
+                              stream);
+        if (e != cudaSuccess) return fail_cuda(e, "scale copy");
+        w.scale_a = dst;
+        w.lds_a = pitch;
+        dst += M * pitch;
+      }
+      if (!fit_b) {
+        e = cudaMemcpy2DAsync(dst, pitch, a.scale_b, a.lds_b, nblk, N, cudaMemcpyDeviceToDevice,
+                              stream);
+        if (e != cudaSuccess) return fail_cuda(e, "scale copy");
+        w.scale_b = dst;
+        w.lds_b = pitch;
+      }
+    }
     e = launch_tc_mx(w, plan);
   } else if (plan.kernel == DG_KERNEL_TC) {
     e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);

@@ -32,14 +32,14 @@
 //   from L2 once per pair instead of once per CTA, halving L2->SM traffic per
 //   FLOP, and each SM's shared memory feeds half of the B operand.
 //
-// MXFP4 (single CTAs): a stage holds 128 bytes of packed codes per row (256
-// values of K, as 16-bit stages hold 64), loaded by TMA as bytes into the
-// same swizzled slots, plus the stage's E8M0 scales, which a pre-pass packed
-// into 16-byte lines and one bulk copy per operand brings in.  The MMA
-// thread copies the scales into tensor memory (tcgen05.cp, in issue order
-// with its MMAs) and issues four block-scaled MMAs of K = 64 per stage: the
-// 4-bit codes reach the tensor cores as they are stored, with no 16-bit
-// copy (discosf.com/news/5532976, section 4.3: packed 4-bit weights instead
+// MXFP4: a stage holds 128 bytes of packed codes per row (256 values of K,
+// as 16-bit stages hold 64), loaded by TMA as bytes into the same swizzled
+// slots, plus the stage's E8M0 scales: TMA brings 16 row-major scale bytes
+// per row of A and B (the stage's 8 and the next stage's), warp 3 rearranges
+// the stage's into the interleaved images the MMA thread copies into tensor
+// memory (tcgen05.cp, in issue order with its MMAs), and the MMA thread
+// issues four block-scaled MMAs of K = 64 per stage: the 4-bit codes reach
+// the tensor cores as they are stored, with no 16-bit copy (discosf.com/news/5532976, section 4.3: packed 4-bit weights instead
 // of an FP16 emulation; section 2.2, layer 2: each precision in the tensor
 // core's own format).
 //
@@ -80,16 +80,7 @@ struct TcParams {
   void* D;
   int64_t ldd;
   const __half* bias;
-  union {
-    struct {
-      int32_t alpha_i, beta_i;  // integer scalars of the INT32 output
-    };
-    // MXFP4 operands: the first 16-byte line of B's section in the packed
-    // scales (A's section starts at line 0; see tmap_sf)
-    struct {
-      int32_t sf_b_line0, sf_unused;
-    };
-  };
+  int32_t alpha_i, beta_i;  // integer scalars of the INT32 output
   int* status;
   uint64_t timeout_ns;
   uint32_t stage_tx;  // bytes TMA delivers per stage (both CTAs of a pair)
@@ -120,38 +111,73 @@ template <int BN, int Stages, int CG, int Kind = kKind16>
 struct TcSmem {
   static constexpr int kRowsB = BN / CG;  // B rows this CTA loads
   static constexpr int kTileBytesB = kRowsB * kBlockK * 2;
-  // MXFP4: scale images of a stage, this CTA's 128 rows of A, then the whole
-  // B tile's rows in 128-row blocks (a CTA pair's MMA reads every column's
-  // scales in each CTA's tensor memory)
+  // MXFP4, per stage: the scale images, this CTA's 128 rows of A, then the
+  // whole B tile's rows in 128-row blocks (a CTA pair's MMA reads every
+  // column's scales in each CTA's tensor memory); and the row-major scale
+  // bytes they are built from, 16 per row (this CTA's 128 rows of A, then
+  // the B tile's BN rows)
   static constexpr int kSfBlocksB = (BN + 127) / 128;
   static constexpr int kSfBytes = Kind == kKindMx ? kMxSfRowBlock * (1 + kSfBlocksB) : 0;
+  static constexpr int kSfRowsBytes = Kind == kKindMx ? 16 * (kBlockM + BN) : 0;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + Stages * kTileBytesA;
   static constexpr int kOffSf = kOffB + Stages * kTileBytesB;
-  static constexpr int kOffEpi = kOffSf + Stages * kSfBytes;
+  static constexpr int kOffSfRows = kOffSf + Stages * kSfBytes;
+  static constexpr int kOffEpi = kOffSfRows + Stages * kSfRowsBytes;
   static constexpr int kEpiBytes = kEpiWarps * 2 * tc::kEpiBoxBytes;
   static constexpr int kOffBar = kOffEpi + kEpiBytes;
-  // full[Stages], empty[Stages], tmem_full[2], tmem_empty[2], drain, then
-  // one C-load barrier per staging box
-  static constexpr int kNumBars = 2 * Stages + 5 + 2 * kEpiWarps;
+  // full[Stages], empty[Stages], tmem_full[2], tmem_empty[2], drain, one
+  // C-load barrier per staging box, then (MXFP4) sf_full[Stages] (the
+  // stage's scale bytes landed) and img_ready[Stages] (its images built)
+  static constexpr int kNumBars = 2 * Stages + 5 + 2 * kEpiWarps + (Kind == kKindMx ? 2 * Stages : 0);
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
   static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1 KB
   static_assert(kTileBytesB % 1024 == 0, "B tiles keep 1 KB alignment");
+  static_assert(kOffSfRows % 128 == 0 && kSfRowsBytes % 128 == 0, "TMA destinations aligned");
 };
 
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
 
-// First 16-byte line, in the packed MXFP4 scales, of 128-row group g of A at
-// K block kb (1024 bytes = 64 lines per group and K block), and of N tile
-// n_blk of B (blocks128 x 64 lines per tile and K block, after A's section).
-__device__ __forceinline__ int32_t sf_line_a(const TcParams& p, int g, int kb) {
-  return (g * p.num_k_blocks + kb) * 64;
-}
-__device__ __forceinline__ int32_t sf_line_b(const TcParams& p, int n_blk, int kb, int blocks128) {
-  return p.sf_b_line0 + (n_blk * p.num_k_blocks + kb) * 64 * blocks128;
-}
+// MXFP4 scale images.  A pair of K blocks (2 kp, 2 kp + 1) has its scale
+// bytes loaded once, 16 per row (this CTA's 128 rows of A, then the B
+// tile's BN rows): bytes 0..7 are K block 2 kp's 8 scales, 8..15 the next
+// one's.  Lane r of the building warp reads rows r, 32 + r, 64 + r and
+// 96 + r of each 128-row block (whole 16-byte rows: a warp's reads are free
+// of bank conflicts); B rows past BN read 0.
+template <int BN>
+struct MxScaleRows {
+  static constexpr int kBlocks = 1 + (BN + 127) / 128;  // A, then B's 128-row blocks
+  uint4 v[kBlocks][4];
+  __device__ __forceinline__ void load(const uint8_t* rows, int r) {
+#pragma unroll
+    for (int blk = 0; blk < kBlocks; ++blk)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int row = (blk == 0 ? 0 : kBlockM + 128 * (blk - 1)) + 32 * w + r;
+        v[blk][w] = (blk == 0 || row - kBlockM < BN)
+                        ? *reinterpret_cast<const uint4*>(rows + 16 * row)
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+  }
+  // Line r of both images of every block for the pair's first (second) K
+  // block: image j line r = the 4 scales 4 j .. 4 j + 3 of the four rows.
+  __device__ __forceinline__ void store(uint8_t* img, int r, bool second) const {
+#pragma unroll
+    for (int blk = 0; blk < kBlocks; ++blk) {
+      uint8_t* dst = img + blk * kMxSfRowBlock + r * 16;
+      const uint4* q = v[blk];
+      if (second) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(q[0].z, q[1].z, q[2].z, q[3].z);
+        *reinterpret_cast<uint4*>(dst + kMxSfImage) = make_uint4(q[0].w, q[1].w, q[2].w, q[3].w);
+      } else {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(q[0].x, q[1].x, q[2].x, q[3].x);
+        *reinterpret_cast<uint4*>(dst + kMxSfImage) = make_uint4(q[0].y, q[1].y, q[2].y, q[3].y);
+      }
+    }
+  }
+};
 
 // Staged epilogue: epilogue warp wi (0..7) owns TMEM lane quarter wi & 3 and
 // half wi >> 2 of the tile's 32-column chunks.  Its chunks form one stream over
@@ -200,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c,
                        const __grid_constant__ CUtensorMap tmap_d,
-                       const __grid_constant__ CUtensorMap tmap_sf, const TcParams p,
+                       const __grid_constant__ CUtensorMap tmap_sfa,
+                       const __grid_constant__ CUtensorMap tmap_sfb, const TcParams p,
                        const __grid_constant__ EpiProgram prog) {
   using L = TcSmem<BN, Stages, CG, Kind>;
   constexpr bool kMx = Kind == kKindMx;
@@ -227,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem_a = smem + L::kOffA;
   uint8_t* smem_b = smem + L::kOffB;
   uint8_t* smem_sf = smem + L::kOffSf;
+  uint8_t* smem_sf_rows = smem + L::kOffSfRows;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + Stages;
@@ -234,6 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_empty = bars + 2 * Stages + 2;
   uint64_t* drain_bar = bars + 2 * Stages + 4;
   uint64_t* epi_bar = bars + 2 * Stages + 5;  // [kEpiWarps][2]
+  uint64_t* sf_full = epi_bar + 2 * kEpiWarps;  // MXFP4 only
+  uint64_t* img_ready = sf_full + Stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
 
@@ -255,12 +285,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(&epi_bar[b], 1);
+    if (kMx) {
+      for (int s = 0; s < Stages; ++s) {
+        mbar_init(&sf_full[s], 1);
+        mbar_init(&img_ready[s], CG);  // the building warp of each CTA of the pair
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
+    if (kMx) {
+      tma_prefetch_desc(&tmap_sfa);
+      tma_prefetch_desc(&tmap_sfb);
+    }
     if (p.staged) {
       tma_prefetch_desc(&tmap_d);
       if (Out == kOutF16 && p.epi.beta != 0.0f) tma_prefetch_desc(&tmap_c);
@@ -302,6 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
+      // MXFP4: ring slots whose latest fill loaded scale bytes, and per slot
+      // the parity of the scale loads so far (a slot that holds an odd K
+      // block loads none, so these phases do not follow the ring's)
+      uint32_t sf_slots = 0, sf_loads = 0;
       for (int t = unit0; t < p.num_tiles && ok; t += units) {
         int m_blk, n_blk;
         tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
@@ -313,6 +357,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (kMx && (kb & 1) == 0) {
+            // The scale bytes of K blocks kb and kb + 1, on this CTA's own
+            // barrier, ahead of the operand tiles so that the images are
+            // built while those land: 16 per row (x = 8 kb, on a 16-byte
+            // boundary as TMA needs), this CTA's rows of A and the whole B
+            // tile's rows.
+            uint8_t* dst_rows = smem_sf_rows + stage * L::kSfRowsBytes;
+            mbar_arrive_expect_tx(&sf_full[stage], L::kSfRowsBytes);
+            tma_load_2d(&tmap_sfa, &sf_full[stage], dst_rows, 8 * kb, a_row, pol);
+            tma_load_2d(&tmap_sfb, &sf_full[stage], dst_rows + 16 * kBlockM, 8 * kb, n_blk * BN,
+                        pol);
+            sf_slots |= 1u << stage;
+            sf_loads ^= 1u << stage;
+          } else if (kMx) {
+            sf_slots &= ~(1u << stage);
+          }
           uint8_t* dst_a = smem_a + stage * kTileBytesA;
           uint8_t* dst_b = smem_b + stage * L::kTileBytesB;
           if (CG == 1) {
@@ -320,31 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // x counts elements of the map: FP16 values, or bytes of two codes
             tma_load_2d(&tmap_a, &full_bar[stage], dst_a, kb * (kMx ? 128 : kBlockK), a_row, pol);
             tma_load_2d(&tmap_b, &full_bar[stage], dst_b, kb * (kMx ? 128 : kBlockK), b_row, pol);
-            if (kMx) {
-              // this stage's scale images: A's row block, then B's tile
-              uint8_t* dst_sf = smem_sf + stage * L::kSfBytes;
-              tma_load_2d(&tmap_sf, &full_bar[stage], dst_sf, 0, sf_line_a(p, m_blk, kb), pol);
-#pragma unroll
-              for (int h = 0; h < L::kSfBlocksB; ++h)
-                tma_load_2d(&tmap_sf, &full_bar[stage], dst_sf + kMxSfRowBlock * (1 + h), 0,
-                            sf_line_b(p, n_blk, kb, L::kSfBlocksB) + 64 * h, pol);
-            }
           } else {
             // both CTAs' copies complete on the even CTA's full barrier
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], p.stage_tx);
             const uint32_t bar0 = mapa_shared(smem_addr(&full_bar[stage]), 0);
             tma_load_2d_pair(&tmap_a, bar0, dst_a, kb * (kMx ? 128 : kBlockK), a_row, pol);
             tma_load_2d_pair(&tmap_b, bar0, dst_b, kb * (kMx ? 128 : kBlockK), b_row, pol);
-            if (kMx) {
-              // this CTA's 128 rows of A scales, and the whole B tile's
-              uint8_t* dst_sf = smem_sf + stage * L::kSfBytes;
-              tma_load_2d_pair(&tmap_sf, bar0, dst_sf, 0,
-                               sf_line_a(p, m_blk * CG + static_cast<int>(rank), kb), pol);
-#pragma unroll
-              for (int h = 0; h < L::kSfBlocksB; ++h)
-                tma_load_2d_pair(&tmap_sf, bar0, dst_sf + kMxSfRowBlock * (1 + h), 0,
-                                 sf_line_b(p, n_blk, kb, L::kSfBlocksB) + 64 * h, pol);
-            }
           }
           ++issued;
           if (first_c && issued == Stages) initial_c();
@@ -361,12 +402,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       grid_launch_dependents();
       if (!ok) {
         *abort_flag = 1;
-        if (CG == 1 || leader) {
-          // Let the copies this thread started land before the CTA goes away.
-          const int64_t first = issued > Stages ? issued - Stages : 0;
-          for (int64_t i = first; i < issued; ++i)
-            mbar_wait(&full_bar[i % Stages], static_cast<uint32_t>((i / Stages) & 1),
-                      p.timeout_ns, p.status);
+        // Let the copies this thread started land before the CTA goes away.
+        const int64_t first = issued > Stages ? issued - Stages : 0;
+        for (int64_t i = first; i < issued; ++i) {
+          const uint32_t par = static_cast<uint32_t>((i / Stages) & 1);
+          if (CG == 1 || leader) mbar_wait(&full_bar[i % Stages], par, p.timeout_ns, p.status);
+          // a slot's latest scale load completes the phase of parity loads - 1
+          if (kMx && ((sf_slots >> (i % Stages)) & 1u))
+            mbar_wait(&sf_full[i % Stages], ((sf_loads >> (i % Stages)) & 1u) ^ 1u, p.timeout_ns,
+                      p.status);
         }
       }
     }
@@ -391,7 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb1 = min(p.num_k_blocks, kb0 + chunk_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait_abortable(&full_bar[stage], phase, p.timeout_ns, p.status,
-                                     abort_flag)) {
+                                     abort_flag) ||
+                (kMx && !mbar_wait_abortable(&img_ready[stage], phase, p.timeout_ns, p.status,
+                                             abort_flag))) {
               ok = false;
               break;
             }
@@ -482,6 +528,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           tc_commit(drain_bar);
         mbar_wait(drain_bar, 0, p.timeout_ns, p.status);
+      }
+    }
+  } else if (kMx && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------ scale images
+    // The images of K-block pair kp (stages of K blocks 2 kp and 2 kp + 1 of
+    // a tile) are built by warp 2 (once it has allocated the tensor memory)
+    // for even pair numbers and warp 3 for odd ones, each walking the ring
+    // as the MMA thread does.  When the pair's scale bytes have landed (in
+    // the first stage's slot) the warp reads them into registers, writes the
+    // first stage's images and reports them on the even CTA's barrier; once
+    // the second stage's slot has been freed by the MMA commit of its
+    // previous use, it writes that stage's images too, ahead of its operand
+    // tiles.  The slot's scale bytes are all in registers before the first
+    // report, since the slot may be refilled as soon as that stage is
+    // consumed.  Each report follows a proxy fence (generic writes, then
+    // the tensor core's reads), which waits about as long as the MMAs of a
+    // stage take: two warps share the pairs so that neither falls behind.
+    const uint32_t mine = static_cast<uint32_t>(warp - 2);
+    uint32_t pair = 0;  // K-block pairs seen so far
+    uint32_t sf_loads = 0;  // per slot: parity of the scale loads seen so far
+    const uint32_t img0 = CG == 2 ? mapa_shared(smem_addr(&img_ready[0]), 0) : 0u;
+    auto report = [&](int st) {
+      fence_proxy_async_smem();  // the images, before the tensor core reads them
+      __syncwarp();
+      if (lane == 0) {
+        if (CG == 2 && !leader)
+          mbar_arrive_remote(img0 + static_cast<uint32_t>(st * 8));
+        else
+          mbar_arrive(&img_ready[st]);
+      }
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = unit0; t < p.num_tiles && ok; t += units) {
+      for (int kb = 0; kb < p.num_k_blocks; kb += 2, ++pair) {
+        // the pair's stages: `stage` (phase `phase`), then the next slot
+        const int st2 = stage + 1 == Stages ? 0 : stage + 1;
+        const uint32_t ph2 = stage + 1 == Stages ? phase ^ 1u : phase;
+        const bool two = kb + 1 < p.num_k_blocks;
+        if ((pair & 1u) == mine) {
+          bool ready = mbar_wait_abortable(&sf_full[stage], (sf_loads >> stage) & 1u,
+                                           p.timeout_ns, p.status, abort_flag);
+          if (!__all_sync(0xffffffffu, ready)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          MxScaleRows<BN> sr;
+          sr.load(smem_sf_rows + stage * L::kSfRowsBytes, lane);
+          sr.store(smem_sf + stage * L::kSfBytes, lane, false);
+          report(stage);
+          if (two) {
+            // the slot's previous use is over when the MMA commit of that
+            // use has arrived (as the producer waits before refilling it)
+            ready = mbar_wait_abortable(&empty_bar[st2], ph2 ^ 1u, p.timeout_ns, p.status,
+                                        abort_flag);
+            if (!__all_sync(0xffffffffu, ready)) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            sr.store(smem_sf + st2 * L::kSfBytes, lane, true);
+            report(st2);
+          }
+        }
+        sf_loads ^= 1u << stage;  // each pair loads once, into its first slot
+        stage = two ? (st2 + 1 == Stages ? 0 : st2 + 1) : st2;
+        phase = two ? (st2 + 1 == Stages ? ph2 ^ 1u : ph2) : ph2;
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -850,13 +964,17 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   const bool staged = !(a.epi & kEpiOutI8) && a.ldd % vec == 0 &&
                       (reinterpret_cast<uintptr_t>(a.D) & 15) == 0 &&
                       (!c_tma || (a.ldc % vec == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0));
-  CUtensorMap tc_map = ta, td_map = ta, tsf_map = ta;  // copies of a map the kernel does not use
+  CUtensorMap tc_map = ta, td_map = ta;  // copies of a map the kernel does not use
+  CUtensorMap tsfa_map = ta, tsfb_map = ta;
   if (kMx) {
-    // the packed scales as rows of 16 bytes: A's section, then B's; boxes of
-    // 64 lines (1 KB: 128 rows x 8 scales)
-    const int64_t lines = pack_mx_scales_bytes(a.M, a.N, a.K, BN) / 16;
-    e = tc::make_map_2d(&tsf_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.sf_packed, lines, 16, 16, 64,
-                        16, CU_TENSOR_MAP_SWIZZLE_NONE);
+    // the row-major scale bytes: boxes of 16 bytes (two stages' scales) by
+    // 128 rows of A or BN rows of B (rows start on 16-byte boundaries)
+    const int64_t nblk = (a.K + 31) / 32;
+    e = tc::make_map_2d(&tsfa_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scale_a, a.M, nblk, a.lds_a,
+                        kBlockM, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    e = tc::make_map_2d(&tsfb_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scale_b, a.N, nblk, a.lds_b,
+                        BN, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
   }
   if (staged) {
@@ -885,19 +1003,13 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.D = a.D;
   p.ldd = a.ldd;
   p.bias = static_cast<const __half*>(a.bias);
-  if (kMx) {
-    // A's section: ceil(M / 128) groups x K blocks x 64 lines
-    p.sf_b_line0 = static_cast<int32_t>((a.M + 127) / 128 * p.num_k_blocks * 64);
-    p.sf_unused = 0;
-  } else {
-    p.alpha_i = static_cast<int32_t>(a.alpha);
-    p.beta_i = static_cast<int32_t>(a.beta);
-  }
+  p.alpha_i = static_cast<int32_t>(a.alpha);
+  p.beta_i = static_cast<int32_t>(a.beta);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  // bytes one stage brings in: both CTAs' operand tiles (and, for MXFP4,
-  // both CTAs' scale images), counted on the even CTA's barrier for a pair
-  p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB + L::kSfBytes));
+  // bytes one stage brings in: both CTAs' operand tiles, counted on the
+  // even CTA's barrier for a pair (MXFP4 scale bytes: on each CTA's own)
+  p.stage_tx = static_cast<uint32_t>(CG * (box_a * kBlockK * 2 + L::kTileBytesB));
   p.staged = staged ? 1 : 0;
   p.idesc_ab = a.bf16_ab ? idesc_ab_bf16() : 0u;
 
@@ -951,7 +1063,8 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs += 1;
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc_map, td_map, tsf_map, p, make_program(a));
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc_map, td_map, tsfa_map, tsfb_map, p,
+                         make_program(a));
   count_launches(1);
   return e;
 }
@@ -986,10 +1099,10 @@ int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32) {
 int mx_kernel_regs(int n_tile, int stages, int cta_group) {
   if (cta_group == 2) {
     if (n_tile == 224 && stages == 5) return regs_of<224, 5, 2, kOutF16, kKindMx>();
-    if (n_tile == 192 && stages == 6) return regs_of<192, 6, 2, kOutF16, kKindMx>();
+    if (n_tile == 192 && stages == 5) return regs_of<192, 5, 2, kOutF16, kKindMx>();
     return 0;
   }
-  if (n_tile == 224 && stages == 4) return regs_of<224, 4, 1, kOutF16, kKindMx>();
+  if (n_tile == 224 && stages == 3) return regs_of<224, 3, 1, kOutF16, kKindMx>();
   if (n_tile == 128 && stages == 5) return regs_of<128, 5, 1, kOutF16, kKindMx>();
   return 0;
 }
@@ -1031,16 +1144,15 @@ cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   return cudaErrorNotSupported;
 }
 
-// MXFP4 tiles on the block-scaled MMA: `a` holds packed codes (K even) and,
-// in a.sf_packed, both operands' scales packed by pack_mx_scales for this
-// plan's N_tile.
+// MXFP4 tiles on the block-scaled MMA: `a` holds packed codes (K even) and
+// row-major scale bytes whose rows start on 16-byte boundaries.
 cudaError_t launch_tc_mx(const GemmArgs& a, const dg_tile_plan& plan) {
   if (plan.cta_group == 2) {
     if (plan.n_tile == 224 && plan.stages == 5) return run_tc<224, 5, 2, kOutF16, kKindMx>(a, plan);
-    if (plan.n_tile == 192 && plan.stages == 6) return run_tc<192, 6, 2, kOutF16, kKindMx>(a, plan);
+    if (plan.n_tile == 192 && plan.stages == 5) return run_tc<192, 5, 2, kOutF16, kKindMx>(a, plan);
     return cudaErrorNotSupported;
   }
-  if (plan.n_tile == 224 && plan.stages == 4) return run_tc<224, 4, 1, kOutF16, kKindMx>(a, plan);
+  if (plan.n_tile == 224 && plan.stages == 3) return run_tc<224, 3, 1, kOutF16, kKindMx>(a, plan);
   if (plan.n_tile == 128 && plan.stages == 5) return run_tc<128, 5, 1, kOutF16, kKindMx>(a, plan);
   return cudaErrorNotSupported;
 }

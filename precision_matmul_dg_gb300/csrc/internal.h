@@ -119,9 +119,6 @@ struct GemmArgs {
   int64_t lds_a = 0;
   const void* scale_b = nullptr;
   int64_t lds_b = 0;
-  // MXFP4 on the block-scaled MMA: both operands' scales packed by
-  // launch_pack_mx_scales (device memory)
-  const void* sf_packed = nullptr;
 };
 
 // Measured registers per thread of the kernel a plan would launch (0 when
@@ -156,7 +153,8 @@ struct SplitKWorkspace {
 // Launchers (gemm_tc.cu, gemv.cu).  Each returns cudaSuccess or the launch error.
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);    // F16 x F16
 // MXFP4 x MXFP4 on the block-scaled MMA (gemm_tc.cu): a.A, a.B packed codes
-// with K even, a.sf_packed the packed scales (pack_mx_scales_bytes bytes).
+// with K even; a.scale_a, a.scale_b 16-byte aligned with lds_a, lds_b
+// multiples of 16.
 cudaError_t launch_tc_mx(const GemmArgs& a, const dg_tile_plan& plan);
 cudaError_t launch_conv(const GemmArgs& a, const dg_tile_plan& plan);  // I8 x I8, F16 x E2M1
 cudaError_t launch_gemv(const GemmArgs& a, const dg_tile_plan& plan, const SplitKWorkspace& ws);
@@ -207,16 +205,6 @@ struct MxWidenJob {
 };
 cudaError_t launch_widen_mxf4(const MxWidenJob* jobs, int njobs, int64_t K, cudaStream_t stream,
                               int sm_count);
-// The block scales of both operands of a native MXFP4 GEMM packed for its
-// tiles (mx.cu): for each tile row group (128 rows of A; n_tile rows of B)
-// and each 256-wide K block, 1024 bytes per 128 rows holding the K block's 8
-// scales per row as two images of 32 lines x 16 bytes (line r, word i, byte
-// k: row 32 i + r, scale 4 j + k of the K block, image j).  Rows past the
-// operand and scales past K read 0.  Writes pack_mx_scales_bytes(...) bytes.
-int64_t pack_mx_scales_bytes(int64_t M, int64_t N, int64_t K, int n_tile);
-cudaError_t launch_pack_mx_scales(int64_t M, int64_t N, int64_t K, int n_tile,
-                                  const void* scale_a, int64_t lds_a, const void* scale_b,
-                                  int64_t lds_b, void* out, cudaStream_t stream);
 cudaError_t launch_wait_selftest(cudaStream_t stream, int* status, uint64_t timeout_ns);
 
 // Whether the split-K GEMV reduces `split` splits inside a thread-block

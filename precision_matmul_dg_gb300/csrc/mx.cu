@@ -330,126 +330,4 @@ cudaError_t launch_widen_mxf4(const MxWidenJob* jobs, int njobs, int64_t K, cuda
   return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------------------
-// Scale packing for the block-scaled MMA
-// ---------------------------------------------------------------------------
-//
-// The block-scaled MMA reads the E8M0 scales from tensor memory, where a
-// copy instruction places 32 lines of 16 bytes (each line into the same
-// lanes of all four warp quarters).  Row m of a 128-row block takes word
-// m / 32 of line m % 32; the four bytes of a word are four consecutive
-// 32-value blocks along K.  One 256-wide K block (a pipeline stage) needs
-// two such images per 128 rows.  This kernel gathers the row-major scale
-// bytes of both operands into that order, one 16-byte line per thread.
-
-namespace {
-
-// One CTA per (operand, tile row group g, 128-row block h of it, 4 K blocks):
-// its 128 threads read 32 scale bytes of one row each (one sector, 16-byte
-// loads when the row pitch allows), and then write the four K blocks' images
-// (4 x 1024 bytes) as 16-byte lines from shared memory.
-constexpr int kPackThreads = 128;
-constexpr int kPackKb = 4;  // K blocks (of 256 values, 8 scales) per CTA
-
-struct PackOperand {
-  const uint8_t* scales;
-  int64_t lds, rows;
-  int group;      // rows per tile row group (128 for A, N_tile for B)
-  int halves;     // 128-row blocks per group
-  int64_t ctas;   // CTAs for this operand
-  uint8_t* out;
-};
-
-__global__ void __launch_bounds__(kPackThreads)
-    pack_mx_scales_kernel(PackOperand a, PackOperand b, int64_t kb_count, int64_t nblk) {
-  __shared__ __align__(16) uint8_t rows_sf[kPackThreads][kPackKb * 8];
-  grid_dependency_wait();  // the scales may come from the kernel before this one
-  grid_launch_dependents();
-  const bool in_a = blockIdx.x < a.ctas;
-  const PackOperand& o = in_a ? a : b;
-  int64_t c = in_a ? blockIdx.x : blockIdx.x - a.ctas;
-  const int64_t quads = (kb_count + kPackKb - 1) / kPackKb;
-  const int64_t q = c % quads;
-  c /= quads;
-  const int h = static_cast<int>(c % o.halves);
-  const int64_t g = c / o.halves;
-  const int64_t kb0 = q * kPackKb;
-  // 1. row t of the block: scale bytes of K blocks kb0 .. kb0 + 3
-  {
-    const int t = threadIdx.x;
-    const int in_group = h * 128 + t;
-    const int64_t row = g * o.group + in_group;
-    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (in_group < o.group && row < o.rows) {
-      const uint8_t* src = o.scales + row * o.lds + kb0 * 8;
-      const int64_t left = nblk - kb0 * 8;
-      const int n = left < 32 ? static_cast<int>(left) : 32;  // scale bytes of these K blocks
-      if (n == 32 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-        const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(src));
-        const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-      } else {
-        for (int i = 0; i < n; ++i) w[i >> 2] |= static_cast<uint32_t>(__ldg(src + i)) << (8 * (i & 3));
-      }
-    }
-    uint4* dst = reinterpret_cast<uint4*>(rows_sf[t]);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  }
-  __syncthreads();
-  // 2. line L of the 4 K blocks' images: K block kb0 + L / 64, image j =
-  //    (L / 32) % 2, line r = L % 32; word i is row 32 i + r's scale word j
-  //    of that K block
-#pragma unroll
-  for (int part = 0; part < 2; ++part) {
-    const int L = part * kPackThreads + threadIdx.x;
-    const int kq = L >> 6, j = (L >> 5) & 1, r = L & 31;
-    const int64_t kb = kb0 + kq;
-    if (kb >= kb_count) continue;
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      w[i] = reinterpret_cast<const uint32_t*>(rows_sf[32 * i + r])[kq * 2 + j];
-    uint8_t* dst = o.out + ((g * kb_count + kb) * o.halves + h) * 1024 + j * 512 + r * 16;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-int64_t pack_lines(int64_t rows, int group, int64_t kb_count) {
-  const int halves = (group + 127) / 128;
-  return (rows + group - 1) / group * kb_count * halves * 64;
-}
-
-int64_t pack_ctas(int64_t rows, int group, int64_t kb_count) {
-  const int halves = (group + 127) / 128;
-  return (rows + group - 1) / group * halves * ((kb_count + kPackKb - 1) / kPackKb);
-}
-
-}  // namespace
-
-int64_t pack_mx_scales_bytes(int64_t M, int64_t N, int64_t K, int n_tile) {
-  const int64_t kb_count = (K + 255) / 256;
-  return 16 * (pack_lines(M, 128, kb_count) + pack_lines(N, n_tile, kb_count));
-}
-
-cudaError_t launch_pack_mx_scales(int64_t M, int64_t N, int64_t K, int n_tile,
-                                  const void* scale_a, int64_t lds_a, const void* scale_b,
-                                  int64_t lds_b, void* out, cudaStream_t stream) {
-  const int64_t kb_count = (K + 255) / 256;
-  const int64_t nblk = (K + kMxBlock - 1) / kMxBlock;
-  PackOperand a{static_cast<const uint8_t*>(scale_a), lds_a, M, 128, 1,
-                pack_ctas(M, 128, kb_count), static_cast<uint8_t*>(out)};
-  PackOperand b{static_cast<const uint8_t*>(scale_b), lds_b, N, n_tile, (n_tile + 127) / 128,
-                pack_ctas(N, n_tile, kb_count),
-                static_cast<uint8_t*>(out) + 16 * pack_lines(M, 128, kb_count)};
-  const int64_t blocks = a.ctas + b.ctas;
-  if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  const cudaError_t e = launch_dependent(pack_mx_scales_kernel, dim3(static_cast<unsigned>(blocks)),
-                                         dim3(kPackThreads), 0, stream, a, b, kb_count, nblk);
-  count_launches(1);
-  return e;
-}
-
 }  // namespace dg

@@ -49,8 +49,8 @@ constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {192, 6, 2, 0}};
 constexpr TcVariant kTcVariantsE2M1[] = {{256, 6, 1, 2}, {128, 8, 1, 3}, {64, 8, 1, 4}};
 // MXFP4 x MXFP4 on the block-scaled MMA (the tensor-core kernel with packed
 // E2M1 stages and scale images; single CTAs)
-constexpr TcVariant kTcVariantsMx[] = {{224, 4, 1, 0}, {128, 5, 1, 0}, {224, 5, 2, 0},
-                                       {192, 6, 2, 0}};
+constexpr TcVariant kTcVariantsMx[] = {{224, 3, 1, 0}, {128, 5, 1, 0}, {224, 5, 2, 0},
+                                       {192, 5, 2, 0}};
 // E2M1 values per MMA FLOP relative to FP16: the block-scaled 4-bit MMA runs
 // at four times the 16-bit rate (the nominal Blackwell ratio)
 constexpr double kMxRateRatio = 4.0;
@@ -86,8 +86,10 @@ int tc_ring_bytes(dg_dtype da, dg_dtype db, const TcVariant& v) {
   const int a16 = kTcBlockM * kTcBlockK * 2;
   if (da == DG_MXF4 && db == DG_MXF4)  // 128-byte rows of codes (a CTA of a pair holds half
                                        // of B's), the scale images (the whole B tile's)
+                                       // and the row-major scale bytes they are built
+                                       // from (16 per row of A and of the B tile)
     return v.stages * (a16 + (v.n_tile / v.cta_group) * kTcBlockK * 2 +
-                       1024 * (1 + (v.n_tile + 127) / 128));
+                       1024 * (1 + (v.n_tile + 127) / 128) + 16 * (kTcBlockM + v.n_tile));
   if (da == DG_F16 && db == DG_F16)
     return v.stages * (a16 + (v.n_tile / v.cta_group) * kTcBlockK * 2);
   const int in_a = da == DG_I8 ? kTcBlockM * kTcBlockK : a16;
@@ -194,9 +196,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
       widened ? (da == DG_F16 ? 0.0 : (elem_a + 2.0) * M * static_cast<double>(K)) +
                     (elem_b + 2.0) * N * static_cast<double>(K)
               : 0.0;
-  const double t_pre =
-      widened ? pre_bytes / hbm_bytes_per_us(hw) + (da == DG_I8 ? 4.0 : 2.0)
-              : (mx_native ? 2.0 : 0.0);  // native MXFP4: the scale-packing launch
+  const double t_pre = widened ? pre_bytes / hbm_bytes_per_us(hw) + (da == DG_I8 ? 4.0 : 2.0) : 0.0;
   // shared memory / tensor memory are those of the kernel that runs
   const dg_dtype ka = widened ? DG_F16 : da, kb = widened ? DG_F16 : db;
   for (int vi = 0; vi < fam.n; ++vi) {

@@ -318,6 +318,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Arrive on a barrier of another CTA of the cluster with the default (CTA
+// scope) release: this thread's earlier shared-memory writes are performed
+// in its own CTA before the arrival leaves, without the cluster-scope fence,
+// which costs about a thousand cycles.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is counted on a
 // barrier that may live in the peer CTA of the pair (`bar_cluster_addr`).
 __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar_cluster_addr,
