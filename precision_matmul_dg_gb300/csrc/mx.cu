@@ -128,6 +128,13 @@ __global__ void __launch_bounds__(kMxThreads, kQuantCtasPerSm)
                          int64_t rows, int log2_tpr, bool vec_in, bool vec_out,
                          uint8_t* __restrict__ codes, int64_t ldq_bytes,
                          uint8_t* __restrict__ scales, int64_t lds) {
+  // Launched as a programmatic dependent: the grid is scheduled while the
+  // kernel before it drains, and reads nothing before that kernel is done.
+  // The GEMM that follows may be scheduled at once: it waits for this grid
+  // to finish before reading the codes (and every CTA of this grid is
+  // resident from the start: one wave).
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int tpr = 1 << log2_tpr;
   const int in_row = threadIdx.x & (tpr - 1);
   const int rows_per_cta = kMxThreads >> log2_tpr;
@@ -295,11 +302,12 @@ cudaError_t launch_quantize_mxf4(int64_t rows, int64_t K, const void* X, int64_t
   const int grid = static_cast<int>(ctas < cap ? ctas : cap);
   const bool vec_in = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && ldx % 8 == 0;
   const bool vec_out = (reinterpret_cast<uintptr_t>(codes) & 15) == 0 && (ldq / 2) % 16 == 0;
-  quantize_mxf4_kernel<<<grid, kMxThreads, 0, stream>>>(
+  const cudaError_t e = launch_dependent(
+      quantize_mxf4_kernel, dim3(static_cast<unsigned>(grid)), dim3(kMxThreads), 0, stream,
       static_cast<const __half*>(X), ldx, K, nblk, rows, log2_tpr, vec_in, vec_out,
       static_cast<uint8_t*>(codes), ldq / 2, static_cast<uint8_t*>(scales), lds);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_widen_mxf4(const MxWidenJob* jobs, int njobs, int64_t K, cudaStream_t stream,
