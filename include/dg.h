@@ -333,11 +333,12 @@ dg_status dg_quantize_mxf4(int64_t rows, int64_t K, const void *X, int64_t ldx, 
  * FP16), bias, the epilogue, alpha and beta are as in dg_gemm.
  * Runs the plan dg_plan_tiles gives for the pair DG_MXF4 x DG_MXF4:
  *  - DG_KERNEL_TC (K even): the codes go to the tensor cores as stored, on
- *    block-scaled kind::mxf4 MMAs with FP32 accumulation; one small launch
- *    first packs both operands' scales into the order the kernel copies into
- *    tensor memory (a per-(device, stream) workspace of about
- *    (M + N) * K / 256 bytes).  Codes past K (and, for the scales, blocks
- *    past ceil(K / 32)) are never read.
+ *    block-scaled kind::mxf4 MMAs with FP32 accumulation; the kernel reads
+ *    the scale bytes where they are when each operand's scale rows start on
+ *    16-byte boundaries (pointer and lds multiples of 16), and otherwise
+ *    first copies them to a 16-byte pitch in a per-(device, stream)
+ *    workspace (M or N times ceil(K / 32) rounded up to 16 bytes).  Codes
+ *    past K (and, for the scales, blocks past ceil(K / 32)) are never read.
  *  - DG_KERNEL_TC_WIDENED (any K; the only plan for odd K): both operands
  *    are widened with their scales into a BF16 copy in that workspace (exact:
  *    each value has at most two significant bits and BF16 keeps FP32's
