@@ -79,12 +79,18 @@ struct SkParams {
 };
 static_assert(sizeof(SkParams) <= 128, "parameter struct within 128 bytes (see Epi)");
 
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t o;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
-      : "=r"(o)
-      : "r"(byte));
-  return o;
+// The four bytes of `w` (eight E2M1 codes) -> four FP16 pairs, byte i into
+// f[i] (low nibble in the low half), exact: the word is split into its bytes
+// once and each byte goes through the hardware pair conversion.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&f)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
+      : "r"(w));
 }
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
@@ -201,15 +207,19 @@ __global__ void __launch_bounds__(kSkThreads)
       for (int j = 0; j < 4; ++j) wv[j] = grp < 4 ? s0[j] : s1[j];
       const uint4* af = reinterpret_cast<const uint4*>(As) + w * 8 * 32 + lane;
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t word = wv[s >> 1];
-        const int sh = 16 * (s & 1);
-        const uint32_t b0 = e2m1x2_to_f16x2((word >> sh) & 0xFFu);        // codes 4s, 4s+1
-        const uint32_t b1 = e2m1x2_to_f16x2((word >> (sh + 8)) & 0xFFu);  // codes 4s+2, 4s+3
-        // rows grp and grp + 8 at the step's K positions 32 tig + 4s .. + 3
-        const uint4 f = af[s * 32];
-        const uint32_t a[4] = {f.x, f.y, f.z, f.w};
-        mma_m16n8k16(acc2[s & 1], a, b0, b1);
+      for (int j = 0; j < 4; ++j) {
+        // word j: codes 8j .. 8j + 7 of the lane's 32, bytes 2s and 2s + 1
+        // for steps s = 2j and 2j + 1
+        uint32_t bf[4];
+        e2m1x8_to_f16x2x4(wv[j], bf);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int s = 2 * j + h;
+          // rows grp and grp + 8 at the step's K positions 32 tig + 4s .. + 3
+          const uint4 f = af[s * 32];
+          const uint32_t a[4] = {f.x, f.y, f.z, f.w};
+          mma_m16n8k16(acc2[h], a, bf[2 * h], bf[2 * h + 1]);  // codes 4s .. 4s + 3
+        }
       }
     }
   }

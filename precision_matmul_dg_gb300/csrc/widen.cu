@@ -32,11 +32,19 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t two_bytes) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t o;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
-      : "=r"(o)
-      : "r"(byte));
+// The four bytes of `w` (eight E2M1 codes) -> four FP16 pairs (byte i into
+// the i-th word, low nibble in the low half), exact: the word is split into
+// its bytes once and each byte goes through the hardware pair conversion.
+__device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w) {
+  uint4 o;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
+      : "r"(w));
   return o;
 }
 
@@ -77,8 +85,7 @@ struct WidenChunk {
   }
   static __device__ __forceinline__ uint4 convert(const In& w) {
     if constexpr (kE2M1) {
-      return make_uint4(e2m1x2_to_f16x2(w & 0xFFu), e2m1x2_to_f16x2((w >> 8) & 0xFFu),
-                        e2m1x2_to_f16x2((w >> 16) & 0xFFu), e2m1x2_to_f16x2(w >> 24));
+      return e2m1x8_to_f16x8(w);
     } else {
       return make_uint4(i8x2_to_f16x2(w.x & 0xFFFFu), i8x2_to_f16x2(w.x >> 16),
                         i8x2_to_f16x2(w.y & 0xFFFFu), i8x2_to_f16x2(w.y >> 16));
