@@ -129,6 +129,25 @@ __global__ void __launch_bounds__(kSkThreads)
   const uint8_t* brow1 =
       p.B + static_cast<int64_t>(min(n0 + 4 + (lane >> 3), p.N - 1)) * p.ldb_bytes;
   const int row_groups = (p.K + 31) / 32;  // 16-byte groups holding codes < K
+  // The epilogue's inputs of this lane (warps of the first K half: bias of
+  // columns n0 + 2 tig + {0, 1}, C at rows grp and grp + 8), loaded now so
+  // that they arrive while the weights stream.
+  float pre_b[2] = {0.0f, 0.0f}, pre_c[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+  if (kh == 0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int nn = n0 + 2 * tig + e;
+      if (nn >= p.N) continue;
+      if (p.epi.flags & kEpiBias) pre_b[e] = __half2float(p.bias[nn]);
+      if (p.epi.beta != 0.0f) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int m = grp + 8 * h;
+          if (m < p.M) pre_c[h][e] = __half2float(p.C[static_cast<int64_t>(m) * p.ldc + nn]);
+        }
+      }
+    }
+  }
   // Two independent accumulator chains (even and odd MMA steps): one chain
   // of dependent MMAs per warp would be bound by the MMA latency.
   float acc2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
@@ -246,10 +265,7 @@ __global__ void __launch_bounds__(kSkThreads)
     for (int e = 0; e < 2; ++e) {
       const int nn = n0 + 2 * tig + e;
       if (nn >= p.N) continue;
-      const float c =
-          p.epi.beta != 0.0f ? __half2float(p.C[static_cast<int64_t>(m) * p.ldc + nn]) : 0.0f;
-      const float b = (p.epi.flags & kEpiBias) ? __half2float(p.bias[nn]) : 0.0f;
-      const float t = epi_apply(acc[2 * h + e], c, b, p.epi, prog);
+      const float t = epi_apply(acc[2 * h + e], pre_c[h][e], pre_b[e], p.epi, prog);
       epi_store(p.D, static_cast<int64_t>(m) * p.ldd + nn, t, p.epi, prog);
     }
   }
