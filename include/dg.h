@@ -121,8 +121,23 @@ typedef enum {
                                operands are widened to BF16 with their block scales */
   DG_KERNEL_SKINNY = 3, /* FP16 x E2M1 with M <= 16 (HBM-bound): packed weights streamed into
                            registers, widened there and fed to warp-level m16n8k16 MMAs */
-  DG_KERNEL_GEMV_MMA = 4 /* FP16 x FP16 with 2 <= M <= 16 (HBM-bound): the split-K GEMV's
+  DG_KERNEL_GEMV_MMA = 4, /* FP16 x FP16 with 2 <= M <= 16 (HBM-bound): the split-K GEMV's
                             streaming of B rows, multiplied on warp-level m16n8k16 MMAs */
+  DG_KERNEL_TC_STREAMK = 5 /* FP16 x FP16 tensor-core pipeline with stream-K work division
+                              (kwkr.cn/news/562171, section 2.2 first layer: the K step of
+                              each piece of work chosen so that ragged tile counts fill every
+                              SM): the tiles that fill whole waves run whole, the K blocks of
+                              the rest are cut into one even range per CTA (pair); a tile
+                              split between ranges is finished by the range holding its first
+                              K block, which adds the others' FP32 partials in a fixed order
+                              (results are bit-stable run to run).  Partials and flags live
+                              in a library workspace per device and stream.  D and C (when
+                              beta != 0) need 16-byte aligned bases and rows (ldd, ldc
+                              multiples of 8) and no int8 output; other layouts, and shapes
+                              whose tiles fill whole waves, run the data-parallel kernel of
+                              the same tile.  The plan's grid is the CTAs the work is divided
+                              over (those left without work are not launched) and split_k the
+                              most ranges one tile meets */
 } dg_kernel;
 
 /* Hardware description the planner solves against

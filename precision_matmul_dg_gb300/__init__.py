@@ -28,7 +28,8 @@ MAX_EPILOGUE_OPS = 8
 STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
           3: "DG_ERR_NO_VALID_CANDIDATE", 4: "DG_ERR_CUDA", 5: "DG_ERR_TIMEOUT",
           6: "DG_ERR_INVALID_STATE"}
-KERNELS = {0: "tc", 1: "gemv", 2: "tc_widened", 3: "skinny", 4: "gemv_mma", -1: "none"}
+KERNELS = {0: "tc", 1: "gemv", 2: "tc_widened", 3: "skinny", 4: "gemv_mma", 5: "tc_streamk",
+           -1: "none"}
 
 # Every symbol include/dg.h declares.
 EXPORTS = ["dg_query_hw", "dg_plan_tiles", "dg_gemm", "dg_gemm_planned", "dg_gemm_host",

@@ -58,6 +58,10 @@ struct Workspace {
   int64_t wide_elems = 0;
   void* table = nullptr;   // problem descriptors of a grouped launch
   int64_t table_bytes = 0;
+  float* sk_partial = nullptr;  // stream-K partial tiles
+  int64_t sk_partial_elems = 0;
+  unsigned* sk_sync = nullptr;  // stream-K epoch, finished-CTA count and flags
+  int64_t sk_sync_elems = 0;
 };
 
 std::mutex g_mu;
@@ -525,6 +529,8 @@ dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev) {
     e = launch_tc_mx(w, plan);
   } else if (plan.kernel == DG_KERNEL_TC) {
     e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);
+  } else if (plan.kernel == DG_KERNEL_TC_STREAMK) {
+    e = launch_tc_streamk(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC_WIDENED && da == DG_MXF4) {
     // Widen both MXFP4 operands with their block scales into BF16 copies
     // (exact), then the tensor-core kernel on BF16 operands.
@@ -695,6 +701,34 @@ dg_status run_gemm_mxf4(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
 }
 
 }  // namespace
+
+dg_status get_sk_workspace(int dev, cudaStream_t stream, int64_t partial_elems,
+                           int64_t sync_elems, float** partial, unsigned** sync) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+  if (w.sk_partial_elems < partial_elems) {
+    if (w.sk_partial) cudaFree(w.sk_partial);  // synchronises the device: no kernel still uses it
+    w.sk_partial = nullptr;
+    w.sk_partial_elems = 0;
+    cudaError_t e = cudaMalloc(&w.sk_partial, partial_elems * sizeof(float));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(stream-K partials)");
+    w.sk_partial_elems = partial_elems;
+  }
+  if (w.sk_sync_elems < sync_elems) {
+    if (w.sk_sync) cudaFree(w.sk_sync);
+    w.sk_sync = nullptr;
+    w.sk_sync_elems = 0;
+    cudaError_t e = cudaMalloc(&w.sk_sync, sync_elems * sizeof(unsigned));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMalloc(stream-K flags)");
+    // epoch 0, no CTA finished, no flag raised
+    e = cudaMemset(w.sk_sync, 0, sync_elems * sizeof(unsigned));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemset(stream-K flags)");
+    w.sk_sync_elems = sync_elems;
+  }
+  *partial = w.sk_partial;
+  *sync = w.sk_sync;
+  return DG_OK;
+}
 
 void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 
@@ -1103,6 +1137,8 @@ dg_status dg_shutdown(void) {
     if (kv.second.counters) cudaFree(kv.second.counters);
     if (kv.second.wide) cudaFree(kv.second.wide);
     if (kv.second.table) cudaFree(kv.second.table);
+    if (kv.second.sk_partial) cudaFree(kv.second.sk_partial);
+    if (kv.second.sk_sync) cudaFree(kv.second.sk_sync);
   }
   g_workspaces.clear();
   for (auto& kv : g_host_ws) {

@@ -58,6 +58,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "tc_common.cuh"
 
 namespace dg {
@@ -88,6 +90,106 @@ struct TcParams {
   uint32_t idesc_ab;  // instruction-descriptor bits of the operand type (0: FP16; BF16 bits)
 };
 static_assert(sizeof(TcParams) <= 128, "parameter struct within 128 bytes (see Epi)");
+
+// Stream-K division of the work (kwkr.cn/news/562171, section 2.2 first
+// layer: a K step chosen per piece of work, so that ragged tile counts
+// still fill every SM).  Tiles [0, dp_tiles) are whole work units, walked as
+// in the data-parallel kernel (unit u takes u, u + units, ...).  The K
+// blocks of tiles [dp_tiles, num_tiles), taken tile after tile, form one
+// sequence of sk_iters iterations that is cut into sk_units contiguous
+// ranges of equal length (+-1), unit u < sk_units taking range u after its
+// whole tiles.  A tile that several ranges meet is finished by the unit
+// holding its first K block (piece 0), which meets it last in its range;
+// every later piece q stores its FP32 partial accumulator in slot q - 1 of
+// the tile and raises one flag per epilogue warp, and piece 0 adds the
+// partials to its own in piece order (a fixed order: the result does not
+// depend on timing).  Flags hold the launch's epoch + 1, read from sync[0]
+// at the start; the last CTA to finish advances the epoch (sync[1] counts
+// finished CTAs), so flags left by an earlier or an aborted launch never
+// match.
+struct SkParams {
+  int dp_tiles;      // tiles walked whole (num_tiles without stream-K)
+  int sk_units;      // units holding a range (0: none)
+  int64_t sk_iters;  // (num_tiles - dp_tiles) * num_k_blocks
+  int max_pieces;    // most ranges a tile meets; partial slots per tile: max_pieces - 1
+  float* partial;    // [tile - dp_tiles][piece - 1][kBlockM * CG][BN]
+  unsigned* sync;    // [0] epoch, [1] CTAs finished, then flags
+                     // [tile - dp_tiles][piece - 1][CG][kEpiWarps]
+};
+
+// One unit's piece of work: K blocks [kb0, kb1) of tile t.  pieces == 1: the
+// whole tile; else piece 0 finishes the tile and pieces > 0 store partials.
+struct Work {
+  int t, kb0, kb1, piece, pieces;
+};
+
+// A unit's position in its list of works: the next whole tile, then the
+// stream-K iterations [it, it_end) still to take.
+struct WorkWalk {
+  int t;
+  int64_t it, it_end;
+};
+
+__device__ __forceinline__ int64_t sk_range_begin(const SkParams& s, int u) {
+  return static_cast<int64_t>(u) * s.sk_iters / s.sk_units;
+}
+
+// The unit whose range holds stream-K iteration i: the largest u with
+// sk_range_begin(u) <= i.
+__device__ __forceinline__ int sk_unit_of(const SkParams& s, int64_t i) {
+  return static_cast<int>(((i + 1) * s.sk_units - 1) / s.sk_iters);
+}
+
+template <bool SK>
+__device__ __forceinline__ WorkWalk walk_start(const SkParams& s, int unit0) {
+  WorkWalk w{unit0, 0, 0};
+  if (SK && unit0 < s.sk_units) {
+    w.it = sk_range_begin(s, unit0);
+    w.it_end = sk_range_begin(s, unit0 + 1);
+  }
+  return w;
+}
+
+// The unit's next work, false past its last.
+template <bool SK>
+__device__ __forceinline__ bool walk_next(WorkWalk& w, const TcParams& p, const SkParams& s,
+                                          int unit0, int units, Work& out) {
+  const int dp_end = SK ? s.dp_tiles : p.num_tiles;
+  if (w.t < dp_end) {
+    out = Work{w.t, 0, p.num_k_blocks, 0, 1};
+    w.t += units;
+    return true;
+  }
+  if (!SK || w.it >= w.it_end) return false;
+  const int kbn = p.num_k_blocks;
+  const int64_t ts = w.it / kbn;
+  const int kb0 = static_cast<int>(w.it - ts * kbn);
+  const int64_t left = w.it_end - w.it;
+  const int kb1 = left < kbn - kb0 ? kb0 + static_cast<int>(left) : kbn;
+  const int first = sk_unit_of(s, ts * kbn);
+  const int last = sk_unit_of(s, ts * kbn + kbn - 1);
+  out = Work{s.dp_tiles + static_cast<int>(ts), kb0, kb1, unit0 - first, last - first + 1};
+  w.it += kb1 - kb0;
+  return true;
+}
+
+// A work whose accumulator goes to a partial slot instead of D.
+__device__ __forceinline__ bool sk_writer(const Work& w) { return w.pieces > 1 && w.piece > 0; }
+
+// The tile of the unit's idx-th work that writes D (-1: none).
+template <bool SK>
+__device__ __forceinline__ int nth_output_tile(const TcParams& p, const SkParams& s, int unit0,
+                                               int units, int idx) {
+  if (!SK) {
+    const int t = unit0 + idx * units;
+    return t < p.num_tiles ? t : -1;
+  }
+  WorkWalk w = walk_start<SK>(s, unit0);
+  Work wk;
+  while (walk_next<SK>(w, p, s, unit0, units, wk))
+    if (!sk_writer(wk) && idx-- == 0) return wk.t;
+  return -1;
+}
 
 // Output modes: FP16 with the fused epilogue, or exact INT32 for INT8 inputs
 // widened to FP16 (K accumulated in exact FP32 chunks, INT32 running sum).
@@ -181,46 +283,41 @@ struct MxScaleRows {
 
 // Staged epilogue: epilogue warp wi (0..7) owns TMEM lane quarter wi & 3 and
 // half wi >> 2 of the tile's 32-column chunks.  Its chunks form one stream over
-// the CTA's tiles; chunk j of the stream is the (j % n)-th chunk of the CTA's
-// (j / n)-th tile.  Returns the chunk's D coordinates, false past the end of
-// the stream or when the box lies wholly outside D.
+// the tiles the CTA writes to D.  Returns the D coordinates of chunk k of the
+// warp's share of tile t, false when the box lies wholly outside D.
 template <int BN, int CG>
-__device__ __forceinline__ bool epi_box(const TcParams& p, int unit0, int units, uint32_t rank,
-                                        int wi, int j, int& x, int& y) {
+__device__ __forceinline__ bool epi_box(const TcParams& p, int t, uint32_t rank, int wi, int k,
+                                        int& x, int& y) {
   constexpr int kChunks = BN / 32;
-  const int half = wi >> 2;
-  const int lo = half == 0 ? 0 : (kChunks + 1) / 2;
-  const int n = half == 0 ? (kChunks + 1) / 2 : kChunks - (kChunks + 1) / 2;
-  const int t = unit0 + (j / n) * units;
-  if (t >= p.num_tiles) return false;
+  const int lo = (wi >> 2) == 0 ? 0 : (kChunks + 1) / 2;
   int mb, nb;
   tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
-  x = nb * BN + (lo + j % n) * 32;
+  x = nb * BN + (lo + k) * 32;
   y = mb * kBlockM * CG + static_cast<int>(rank) * kBlockM + (wi & 3) * 32;
   return x < p.N && y < p.M;
 }
 
-// Loads C of stream chunk j of warp wi into its box j & 1 (arriving on that
-// box's barrier).  For the first chunk of a tile it also asks L2 for the
-// tile's chunks from the third on, which are loaded only during the
-// epilogue.  Box j & 1 must no longer feed a store.
+// Loads C of chunk k of warp wi's share of tile t (stream chunk j) into its
+// box j & 1 (arriving on that box's barrier).  For the first chunk of a tile
+// it also asks L2 for the share's chunks from the third on, which are loaded
+// only during the epilogue.  Box j & 1 must no longer feed a store.
 template <int BN, int CG>
-__device__ __forceinline__ void epi_load_c(const CUtensorMap* map, const TcParams& p, int unit0,
-                                           int units, uint32_t rank, int wi, int j,
-                                           uint8_t* boxes, uint64_t* cbar, uint64_t policy) {
+__device__ __forceinline__ void epi_load_c(const CUtensorMap* map, const TcParams& p, int t,
+                                           uint32_t rank, int wi, int k, int j, uint8_t* boxes,
+                                           uint64_t* cbar, uint64_t policy) {
   constexpr int kChunks = BN / 32;
   const int n = (wi >> 2) == 0 ? (kChunks + 1) / 2 : kChunks - (kChunks + 1) / 2;
   int x, y;
-  if (!epi_box<BN, CG>(p, unit0, units, rank, wi, j, x, y)) return;
+  if (t < 0 || !epi_box<BN, CG>(p, t, rank, wi, k, x, y)) return;
   const int b = j & 1;
   mbar_arrive_expect_tx(&cbar[b], tc::kEpiBoxBytes);
   tma_load_2d(map, &cbar[b], boxes + b * tc::kEpiBoxBytes, x, y, policy);
-  if (j % n == 0)
-    for (int k = 2; k < n; ++k)
-      if (epi_box<BN, CG>(p, unit0, units, rank, wi, j + k, x, y)) tma_prefetch_l2_2d(map, x, y);
+  if (k == 0)
+    for (int kk = 2; kk < n; ++kk)
+      if (epi_box<BN, CG>(p, t, rank, wi, kk, x, y)) tma_prefetch_l2_2d(map, x, y);
 }
 
-template <int BN, int Stages, int CG, int Out, int Kind>
+template <int BN, int Stages, int CG, int Out, int Kind, bool SK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_b,
@@ -228,10 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_d,
                        const __grid_constant__ CUtensorMap tmap_sfa,
                        const __grid_constant__ CUtensorMap tmap_sfb, const TcParams p,
-                       const __grid_constant__ EpiProgram prog) {
+                       const __grid_constant__ EpiProgram prog, const SkParams sk) {
   using L = TcSmem<BN, Stages, CG, Kind>;
   constexpr bool kMx = Kind == kKindMx;
   static_assert(!kMx || Out == kOutF16, "MXFP4: FP16 output");
+  // Stream-K: 16-bit operands, FP16 output through the staged epilogue, and
+  // at least two 32-column chunks per epilogue warp (so that the producer's
+  // first two C boxes belong to one tile)
+  static_assert(!SK || (Kind == kKind16 && Out == kOutF16 && BN >= 128), "stream-K variant");
   // two FP32 accumulators (the INT32 mode keeps its running sums in registers);
   // MXFP4 adds two buffers of scale words after them: A's 128 rows (4
   // columns per scale word, one per 32-row group) and B's rows (one column
@@ -333,11 +434,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool first_c = Out == kOutF16 && p.staged && p.epi.beta != 0.0f;
       auto initial_c = [&]() {
         const uint64_t pol_c = policy_evict_first();
-        for (int wi = 0; wi < kEpiWarps; ++wi)
+        constexpr int kChunks = BN / 32;
+        const int t0 = nth_output_tile<SK>(p, sk, unit0, units, 0);
+        const int t1 = nth_output_tile<SK>(p, sk, unit0, units, 1);
+        for (int wi = 0; wi < kEpiWarps; ++wi) {
+          const int n = (wi >> 2) == 0 ? (kChunks + 1) / 2 : kChunks - (kChunks + 1) / 2;
           for (int j = 0; j < 2; ++j)
-            epi_load_c<BN, CG>(&tmap_c, p, unit0, units, rank, wi, j,
+            epi_load_c<BN, CG>(&tmap_c, p, j < n ? t0 : t1, rank, wi, j % n, j,
                                smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes, epi_bar + wi * 2,
                                pol_c);
+        }
       };
       int stage = 0;
       uint32_t phase = 0;
@@ -346,12 +452,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the parity of the scale loads so far (a slot that holds an odd K
       // block loads none, so these phases do not follow the ring's)
       uint32_t sf_slots = 0, sf_loads = 0;
-      for (int t = unit0; t < p.num_tiles && ok; t += units) {
+      WorkWalk walk = walk_start<SK>(sk, unit0);
+      Work wk;
+      while (ok && walk_next<SK>(walk, p, sk, unit0, units, wk)) {
         int m_blk, n_blk;
-        tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
+        tc::tile_coords(wk.t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
         const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBlockM;
         const int b_row = n_blk * BN + static_cast<int>(rank) * L::kRowsB;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           if (!mbar_wait_abortable(&empty_bar[stage], phase ^ 1, p.timeout_ns, p.status,
                                    abort_flag)) {
             ok = false;
@@ -422,7 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       int sf_buf = 0;  // MXFP4: scale buffer of the next stage
-      for (int t = unit0; t < p.num_tiles && ok; t += units) {
+      WorkWalk walk = walk_start<SK>(sk, unit0);
+      Work wk;
+      while (ok && walk_next<SK>(walk, p, sk, unit0, units, wk)) {
         for (int ch = 0; ch < num_chunks && ok; ++ch) {
           if (!mbar_wait_abortable(&tmem_empty[acc], acc_phase ^ 1, p.timeout_ns, p.status,
                                    abort_flag)) {
@@ -431,8 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-          const int kb0 = ch * chunk_kb;
-          const int kb1 = min(p.num_k_blocks, kb0 + chunk_kb);
+          const int kb0 = wk.kb0 + ch * chunk_kb;
+          const int kb1 = min(wk.kb1, kb0 + chunk_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait_abortable(&full_bar[stage], phase, p.timeout_ns, p.status,
                                      abort_flag) ||
@@ -719,17 +829,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) bulk_wait_group<0>();  // stores end before the CTA does
       __syncwarp();
     } else if (p.staged) {
-      // Staged epilogue.  The warp's chunks form one stream over its tiles:
-      // chunk j of the stream is chunk j % n of the warp's (j / n)-th tile
-      // (n = the warp's chunks per tile) and goes through box j & 1 of its two
-      // boxes.  C of chunks 0 and 1 is loaded by the producer; lane 0 loads C
-      // of chunk j + 2 as soon as chunk j's store has read its box, so it
-      // arrives while the warp finishes chunk j + 1 or, across tiles, during
-      // the next main loop.  Tile coordinates are worked out once per tile (a
-      // second cursor runs two chunks ahead for the C loads).  Reading chunk
-      // j + 1's accumulator columns while chunk j is converted was measured
-      // and not kept: it took the registers to the 168 limit and the FP16
-      // 2048^3 and W4A16 M = 2048 GEMMs 5-7% slower.
+      // Staged epilogue.  The warp's chunks of the works that write D form one
+      // stream: chunk j of the stream is chunk k of the warp's share of one
+      // tile and goes through box j & 1 of its two boxes.  C of chunks 0 and
+      // 1 is loaded by the producer; lane 0 loads C of chunk j + 2 as soon as
+      // chunk j's store has read its box, so it arrives while the warp
+      // finishes chunk j + 1 or, across tiles, during the next main loop.
+      // Tile coordinates are worked out once per work (a second cursor runs
+      // two chunks ahead over the works that write D, for the C loads).
+      // Reading chunk j + 1's accumulator columns while chunk j is converted
+      // was measured and not kept: it took the registers to the 168 limit
+      // and the FP16 2048^3 and W4A16 M = 2048 GEMMs 5-7% slower.
+      //
+      // Stream-K: a work that stores a partial (sk_writer) copies the warp's
+      // accumulator region to its slot, then raises its flag; the work that
+      // finishes a split tile waits for the flags of the tile's later pieces
+      // and adds their partials, in piece order, before the epilogue.
       const int wi = warp - kEpiWarp0;
       uint8_t* boxes = smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes;
       uint64_t* cbar = epi_bar + wi * 2;
@@ -737,34 +852,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_c = policy_evict_first();
       const int n_mine = chunk_hi - chunk_lo;
       const int row_off = static_cast<int>(rank) * kBlockM + ew * 32;
-      // A stream position: tile t, chunk k of the warp's share of it, the
-      // share's first D column x0 and the warp's first D row y.
-      struct Cursor {
-        int t, k, x0, y;
+      // stream-K: the value of this launch's flags
+      const unsigned flag_val = SK ? *reinterpret_cast<volatile unsigned*>(sk.sync) + 1u : 0u;
+      // The warp's region of partial slot (tile, piece): its 32 rows x its
+      // half of the columns, stored as float4 (k * 8 + q) * 32 + lane for
+      // columns 4q .. 4q + 3 of chunk k of the lane's row, so that each
+      // store and load of the warp covers 512 contiguous bytes.
+      auto sk_region = [&](const Work& w, int piece) {
+        const int64_t slot =
+            static_cast<int64_t>(w.t - sk.dp_tiles) * (sk.max_pieces - 1) + (piece - 1);
+        const int region = ((static_cast<int>(rank) * 4 + ew) * 2 + half);
+        return reinterpret_cast<float4*>(sk.partial + slot * kTileM * BN) +
+               static_cast<int64_t>(region) * (BN / 2) * 8;
       };
-      auto set_tile = [&](Cursor& q) {
-        if (q.t < p.num_tiles) {
+      auto sk_flag = [&](const Work& w, int piece) {
+        const int64_t slot =
+            static_cast<int64_t>(w.t - sk.dp_tiles) * (sk.max_pieces - 1) + (piece - 1);
+        return sk.sync + 2 + (slot * CG + rank) * kEpiWarps + wi;
+      };
+      // A position in the warp's works: the work, chunk k of the warp's share
+      // of its tile, the share's first D column x0 and the warp's first D row y.
+      struct Cursor {
+        WorkWalk w;
+        Work wk;
+        bool valid;
+        int k, x0, y;
+      };
+      // moves q to the unit's next work (outputs_only: the next that writes D)
+      auto seek = [&](Cursor& q, bool outputs_only) {
+        bool v = walk_next<SK>(q.w, p, sk, unit0, units, q.wk);
+        while (SK && v && outputs_only && sk_writer(q.wk))
+          v = walk_next<SK>(q.w, p, sk, unit0, units, q.wk);
+        q.valid = v;
+        q.k = 0;
+        if (v) {
           int mb, nb;
-          tc::tile_coords(q.t, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
+          tc::tile_coords(q.wk.t, p.num_m_blocks, p.num_n_blocks, p.group_m, mb, nb);
           q.x0 = nb * BN + chunk_lo * 32;
           q.y = mb * kTileM + row_off;
         }
       };
       auto advance = [&](Cursor& q) {
-        if (++q.k == n_mine) {
-          q.k = 0;
-          q.t += units;
-          set_tile(q);
-        }
+        if (++q.k == n_mine) seek(q, true);
       };
       auto live_at = [&](const Cursor& q) {
-        return q.t < p.num_tiles && q.x0 + q.k * 32 < p.N && q.y < p.M;
+        return q.valid && q.x0 + q.k * 32 < p.N && q.y < p.M;
       };
       uint32_t c_phase = 0;    // bit b: parity of box b's next C arrival
       uint32_t c_pending = 0;  // bit b: a C load into box b not yet waited for
       bool prev_stored = false;
-      Cursor ldc{unit0, 0, 0, 0};  // the next chunk whose C is to be requested
-      set_tile(ldc);
+      Cursor ldc;  // the next chunk whose C is to be requested
+      ldc.w = walk_start<SK>(sk, unit0);
+      seek(ldc, true);
       for (int jj = 0; jj < 2; ++jj) {  // chunks 0 and 1: requested by the producer
         if (has_c && live_at(ldc)) c_pending |= 1u << jj;
         advance(ldc);
@@ -787,9 +926,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         advance(ldc);
       };
       int j = 0;
-      Cursor cur{unit0, 0, 0, 0};
-      set_tile(cur);
-      while (cur.t < p.num_tiles && ok) {
+      Cursor cur;
+      cur.w = walk_start<SK>(sk, unit0);
+      seek(cur, false);
+      while (cur.valid && ok) {
         const bool ready =
             !aborted(abort_flag) &&
             mbar_wait_sleepy(&tmem_full[acc], acc_phase, p.timeout_ns, p.status, 256);
@@ -802,50 +942,98 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tbase =
             tmem_base + lane_base + static_cast<uint32_t>(acc * BN + chunk_lo * 32);
         const bool row_live = cur.y < p.M;
+        if (SK && sk_writer(cur.wk)) {
+          // the whole region (rows and columns past D included), in stores
+          // that stay in L2; then every lane's stores before the flag
+          float4* dst = sk_region(cur.wk, cur.wk.piece) + lane;
 #pragma unroll 1
-        for (int k = 0; k < n_mine; ++k) {
-          uint32_t r[32];
-          const int b = j & 1;
-          uint8_t* box = boxes + b * tc::kEpiBoxBytes;
-          const int x = cur.x0 + k * 32;
-          const bool live = row_live && x < p.N;
-          if (live) {
+          for (int k = 0; k < n_mine; ++k) {
+            uint32_t r[32];
             tmem_ld_32cols(tbase + k * 32, r);
-            bool got = true;
-            if (has_c) {
-              got = mbar_wait(&cbar[b], (c_phase >> b) & 1u, p.timeout_ns, p.status);
-              if (got) {
-                c_phase ^= 1u << b;
-                c_pending &= ~(1u << b);
-              }
-            } else {
-              // box b was last read by the store of chunk j - 2
-              if (lane == 0) {
-                if (prev_stored)
-                  bulk_wait_group_read<1>();
-                else
-                  bulk_wait_group_read<0>();
-              }
-              __syncwarp();
-            }
-            got = __all_sync(0xffffffffu, got);
             tc_wait_ld();
-            if (!got) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              __stcg(dst + (k * 8 + q) * 32,
+                     make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) st_release_gpu(sk_flag(cur.wk, cur.wk.piece), flag_val);
+        } else {
+          if (SK && cur.wk.pieces > 1) {
+            // every lane acquires the flags itself before reading partials
+            bool got = true;
+            for (int q = 1; q < cur.wk.pieces && got; ++q)
+              got = wait_flag_eq(sk_flag(cur.wk, q), flag_val, p.timeout_ns, p.status);
+            if (!__all_sync(0xffffffffu, got)) {
               *abort_flag = 1;
               ok = false;
               break;
             }
-            tc::epilogue_f16_box(r, box, lane, x, p.N, p.epi, prog, p.bias, has_c);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmap_d, box, x, cur.y);
-              bulk_commit_group();
-            }
+            // the first chunk's partials into L1 (after the acquire: current)
+            for (int q = 1; q < cur.wk.pieces; ++q) prefetch_l1(sk_region(cur.wk, q) + lane * 8);
           }
-          prev_stored = live;
-          load_c(j + 2);
-          ++j;
+#pragma unroll 1
+          for (int k = 0; k < n_mine; ++k) {
+            uint32_t r[32];
+            const int b = j & 1;
+            uint8_t* box = boxes + b * tc::kEpiBoxBytes;
+            const int x = cur.x0 + k * 32;
+            const bool live = row_live && x < p.N;
+            if (live) {
+              tmem_ld_32cols(tbase + k * 32, r);
+              bool got = true;
+              if (has_c) {
+                got = mbar_wait(&cbar[b], (c_phase >> b) & 1u, p.timeout_ns, p.status);
+                if (got) {
+                  c_phase ^= 1u << b;
+                  c_pending &= ~(1u << b);
+                }
+              } else {
+                // box b was last read by the store of chunk j - 2
+                if (lane == 0) {
+                  if (prev_stored)
+                    bulk_wait_group_read<1>();
+                  else
+                    bulk_wait_group_read<0>();
+                }
+                __syncwarp();
+              }
+              got = __all_sync(0xffffffffu, got);
+              tc_wait_ld();
+              if (!got) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+              }
+              if (SK && cur.wk.pieces > 1) {
+                for (int q = 1; q < cur.wk.pieces; ++q) {
+                  const float4* src = sk_region(cur.wk, q) + k * 8 * 32 + lane;
+                  // the next chunk's 4 KB: one 128-byte line per lane
+                  if (k + 1 < n_mine) prefetch_l1(src - lane + 8 * 32 + lane * 8);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    const float4 v = __ldca(src + i * 32);
+                    r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + v.x);
+                    r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + v.y);
+                    r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + v.z);
+                    r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + v.w);
+                  }
+                }
+              }
+              tc::epilogue_f16_box(r, box, lane, x, p.N, p.epi, prog, p.bias, has_c);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmap_d, box, x, cur.y);
+                bulk_commit_group();
+              }
+            }
+            prev_stored = live;
+            load_c(j + 2);
+            ++j;
+          }
         }
         if (!ok) break;
         tc_fence_before_sync();
@@ -857,8 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc = 0;
           acc_phase ^= 1;
         }
-        cur.t += units;
-        set_tile(cur);
+        seek(cur, false);
       }
       // Copies into and out of the boxes end before the CTA does.
       if (lane == 0) {
@@ -869,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-    for (int t = unit0; t < p.num_tiles && ok && Out == kOutF16 && !p.staged; t += units) {
+    for (int t = unit0; t < p.num_tiles && ok && Out == kOutF16 && !SK && !p.staged; t += units) {
       int m_blk, n_blk;
       tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
       const int row = m_blk * kTileM + static_cast<int>(rank) * kBlockM + ew * 32 + lane;
@@ -927,9 +1114,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       tmem_dealloc<kTmemCols>(tmem_base);
   }
+  if (SK && threadIdx.x == 0) {
+    // The last CTA to finish (aborted or not) advances the epoch: the next
+    // launch's flags take the next value.
+    __threadfence();
+    if (atomicAdd(sk.sync + 1, 1u) == gridDim.x - 1) {
+      sk.sync[1] = 0;
+      __threadfence();
+      atomicAdd(sk.sync, 1u);
+    }
+  }
 }
 
-template <int BN, int Stages, int CG, int Out, int Kind>
+template <int BN, int Stages, int CG, int Out, int Kind, bool SK = false>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   using L = TcSmem<BN, Stages, CG, Kind>;
   constexpr bool kMx = Kind == kKindMx;
@@ -1013,7 +1210,7 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   p.staged = staged ? 1 : 0;
   p.idesc_ab = a.bf16_ab ? idesc_ab_bf16() : 0u;
 
-  auto kern = gemm_tc_kernel<BN, Stages, CG, Out, Kind>;
+  auto kern = gemm_tc_kernel<BN, Stages, CG, Out, Kind, SK>;
   int dev = 0;
   cudaGetDevice(&dev);
   // One shared-memory opt-in and one co-residency query per variant and device.
@@ -1054,8 +1251,30 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   // grid: CTAs (pairs x 2 when CG == 2), never more units than tiles
   int units = plan.grid > 0 ? plan.grid / CG : a.sm_count / CG;
   if (CG == 2 && units > max_pairs[dev & 63]) units = max_pairs[dev & 63];
-  if (units > p.num_tiles) units = p.num_tiles;
+  if (units > p.num_tiles && !SK) units = p.num_tiles;
   if (units < 1) units = 1;
+  SkParams sk{p.num_tiles, 0, 0, 1, nullptr, nullptr};
+  if (SK) {
+    // Stream-K needs the staged epilogue; a problem without ragged work (or
+    // another layout) runs the data-parallel kernel of the same tile.
+    const SkSplit sp = stream_k_split(p.num_tiles, p.num_k_blocks, units);
+    if (!staged || sp.sk_tiles == 0) return run_tc<BN, Stages, CG, Out, Kind, false>(a, plan);
+    const int64_t slots = sp.sk_tiles * (sp.max_pieces - 1);
+    float* partial = nullptr;
+    unsigned* sync = nullptr;
+    if (get_sk_workspace(dev, a.stream, std::max<int64_t>(1, slots * kBlockM * CG * BN),
+                         2 + slots * CG * kEpiWarps, &partial, &sync) != DG_OK)
+      return cudaErrorMemoryAllocation;
+    sk.dp_tiles = static_cast<int>(sp.dp_tiles);
+    sk.sk_units = sp.sk_units;
+    sk.sk_iters = sp.sk_iters;
+    sk.max_pieces = sp.max_pieces;
+    sk.partial = partial;
+    sk.sync = sync;
+    // every unit with a whole tile or a range
+    const int64_t busy = std::max<int64_t>(std::min<int64_t>(sp.dp_tiles, units), sp.sk_units);
+    units = static_cast<int>(std::max<int64_t>(1, busy));
+  }
   cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
   // Programmatic dependent launch: this grid's CTAs may start (and set up
   // barriers and tensor memory) while the previous kernel in the stream
@@ -1064,15 +1283,15 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs += 1;
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc_map, td_map, tsfa_map, tsfb_map, p,
-                         make_program(a));
+                         make_program(a), sk);
   count_launches(1);
   return e;
 }
 
-template <int BN, int Stages, int CG, int Out, int Kind = kKind16>
+template <int BN, int Stages, int CG, int Out, int Kind = kKind16, bool SK = false>
 int regs_of() {
   static std::atomic<int> slot{-1};
-  return kernel_regs(gemm_tc_kernel<BN, Stages, CG, Out, Kind>, slot);
+  return kernel_regs(gemm_tc_kernel<BN, Stages, CG, Out, Kind, SK>, slot);
 }
 
 }  // namespace
@@ -1093,6 +1312,12 @@ int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32) {
   if (n_tile == 256 && stages == 4) return regs_of<256, 4, 1, kOutF16>();
   if (n_tile == 128 && stages == 6) return regs_of<128, 6, 1, kOutF16>();
   if (n_tile == 64 && stages == 8) return regs_of<64, 8, 1, kOutF16>();
+  return 0;
+}
+
+int tc_streamk_kernel_regs(int n_tile, int stages, int cta_group) {
+  if (n_tile == 256 && stages == 6 && cta_group == 2) return regs_of<256, 6, 2, kOutF16, kKind16, true>();
+  if (n_tile == 128 && stages == 6 && cta_group == 1) return regs_of<128, 6, 1, kOutF16, kKind16, true>();
   return 0;
 }
 
@@ -1141,6 +1366,17 @@ cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
       if (plan.stages == 8) return run_tc<64, 8, 1, kOutF16, kKind16>(a, plan);
       break;
   }
+  return cudaErrorNotSupported;
+}
+
+// Stream-K tiles (FP16 x FP16): whole tiles first, then the rest of the
+// tiles' K blocks in even ranges over the units.
+cudaError_t launch_tc_streamk(const GemmArgs& a, const dg_tile_plan& plan) {
+  if (a.exact_i32 || a.bf16_ab) return cudaErrorNotSupported;
+  if (plan.n_tile == 256 && plan.stages == 6 && plan.cta_group == 2)
+    return run_tc<256, 6, 2, kOutF16, kKind16, true>(a, plan);
+  if (plan.n_tile == 128 && plan.stages == 6 && plan.cta_group == 1)
+    return run_tc<128, 6, 1, kOutF16, kKind16, true>(a, plan);
   return cudaErrorNotSupported;
 }
 

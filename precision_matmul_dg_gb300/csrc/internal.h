@@ -127,6 +127,7 @@ struct GemmArgs {
 // split-K GEMV and warp-MMA GEMV for M rows (gemv.cu), skinny W4A16 kernel
 // (skinny.cu).  0 too for a variant that is not compiled.
 int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32);
+int tc_streamk_kernel_regs(int n_tile, int stages, int cta_group);  // stream-K (gemm_tc.cu)
 int mx_kernel_regs(int n_tile, int stages, int cta_group);  // MXFP4 block-scaled (gemm_tc.cu)
 int conv_kernel_regs(dg_dtype da, dg_dtype db, int n_tile, int stages);
 int gemv_kernel_regs(int64_t M, int split);
@@ -150,8 +151,29 @@ struct SplitKWorkspace {
   int64_t counter_elems;
 };
 
+// Stream-K division of `tiles` output tiles of `kblocks` K blocks each over
+// `units` scheduling units (CTAs, or CTA pairs), as the stream-K kernel
+// walks it: tiles [0, dp_tiles) whole, then the sk_iters K blocks of the
+// other sk_tiles tiles cut into sk_units contiguous ranges of equal length
+// (+-1); a tile meets at most max_pieces ranges.  sk_tiles == 0: the tiles
+// fill whole waves (or a tile has one K block) and there is nothing to
+// balance.  Host only (planner.cpp).
+struct SkSplit {
+  int64_t dp_tiles, sk_tiles, sk_iters;
+  int sk_units, max_pieces;
+};
+SkSplit stream_k_split(int64_t tiles, int64_t kblocks, int64_t units);
+
+// Scratch of the stream-K kernel on (device, stream) (api.cu): at least
+// `partial_elems` FP32 partial sums, and `sync_elems` words (the launch
+// epoch, a count of finished CTAs, then the flags) zeroed when allocated.
+dg_status get_sk_workspace(int dev, cudaStream_t stream, int64_t partial_elems,
+                           int64_t sync_elems, float** partial, unsigned** sync);
+
 // Launchers (gemm_tc.cu, gemv.cu).  Each returns cudaSuccess or the launch error.
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);    // F16 x F16
+// F16 x F16 with stream-K work division (DG_KERNEL_TC_STREAMK plans).
+cudaError_t launch_tc_streamk(const GemmArgs& a, const dg_tile_plan& plan);
 // MXFP4 x MXFP4 on the block-scaled MMA (gemm_tc.cu): a.A, a.B packed codes
 // with K even; a.scale_a, a.scale_b 16-byte aligned with lds_a, lds_b
 // multiples of 16.

@@ -42,6 +42,21 @@ constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1, 0}, {128, 6, 1, 0}, {64, 8, 
                                         {256, 6, 2, 0}, {224, 6, 2, 0}, {192, 6, 2, 0},
                                         {128, 8, 2, 0}};
 constexpr int kNumTcVariantsF16 = 7;
+// FP16 x FP16 tiles also compiled with stream-K work division
+bool tc_streamk_variant(const TcVariant& v) {
+  return (v.n_tile == 256 && v.stages == 6 && v.cta_group == 2) ||
+         (v.n_tile == 128 && v.stages == 6 && v.cta_group == 1);
+}
+// Stream-K ranges are at least this many K blocks long
+constexpr int64_t kSkMinIters = 4;
+// Cost of a split tile per extra piece and accumulator element of the tile
+// (microseconds): the writers' partial stores competing with their next
+// main loop, and the finisher's exposed read and add before its epilogue.
+// Calibrated on GB300 against the data-parallel kernel of every FP16 tile:
+// 256 x 256 pair tiles lost 8-10 us a launch at 2048^3, 2560^2 x 4096,
+// 3072^2 x 4096 and 4096^3 and won 30 us at 8192^3; 128 x 128 tiles won
+// 8 us at 128 and 256 x 4096 x 16384.
+constexpr double kSkFixUsPerElem = 1.15e-4;
 constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
 // FP16 kernel in its exact-INT32 mode (two FP32 chunk accumulators in TMEM,
 // running INT32 sums in registers: N_tile a multiple of 64, at most 192)
@@ -235,14 +250,58 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     const int64_t tiles = ceil_div(M, tile_m) * ceil_div(N, v.n_tile);
     const int64_t waves = ceil_div(tiles, units);
     const double occ = static_cast<double>(tiles) / static_cast<double>(waves * units);
-    if (occ < target) {
-      if (why) *why += name + ": occupancy; ";
-      continue;
-    }
     const int64_t k_step = mx_native ? 256 : kTcBlockK;  // K per pipeline stage
     const int64_t k_pad = ceil_div(K, k_step) * k_step;
     // FLOPs of one tile per SM of its unit
     const double tile_flops = 2.0 * kTcBlockM * v.n_tile * static_cast<double>(k_pad);
+    const double t_tile =
+        tile_flops / (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile, v.cta_group));
+    const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
+    if (!widened && !narrow && tc_streamk_variant(v)) {
+      // The same tile with stream-K division: whole waves of tiles, then the
+      // rest of the K blocks in one even range per unit; a split tile costs
+      // its finisher the read of the other ranges' partials.
+      const int64_t kbn = k_pad / k_step;
+      const SkSplit sp = stream_k_split(tiles, kbn, units);
+      const int sk_regs = tc_streamk_kernel_regs(v.n_tile, v.stages, v.cta_group);
+      const int regs_sk = sk_regs > 0 ? sk_regs : kTcRegsPerThread;
+      if (sp.sk_tiles > 0 && regs_sk <= hw.regs_per_thread_max &&
+          regs_sk * fam.threads <= hw.regs_per_sm) {
+        const int64_t range = ceil_div(sp.sk_iters, sp.sk_units);
+        const double unit_iters = static_cast<double>(sp.dp_tiles / units * kbn + range);
+        const double occ_sk = static_cast<double>(tiles * kbn) / (units * unit_iters);
+        if (occ_sk >= target) {
+          const double t_math = unit_iters / kbn * t_tile;
+          const double t_fix =
+              sp.max_pieces > 1
+                  ? 0.5 + (sp.max_pieces - 1) * static_cast<double>(tile_m) * v.n_tile *
+                              kSkFixUsPerElem
+                  : 0.0;
+          const double bytes = 2.0 * (M * K + N * K) + 4.0 * M * N;
+          dg_tile_plan q{};
+          q.kernel = DG_KERNEL_TC_STREAMK;
+          q.m_tile = tile_m;
+          q.n_tile = v.n_tile;
+          q.k_tile = static_cast<int>(k_step);
+          q.split_k = sp.max_pieces;
+          q.stages = v.stages;
+          q.cta_group = v.cta_group;
+          q.swap_ab = 0;
+          q.smem_bytes = tc_smem_bytes(ka, kb, v, true);
+          q.threads = fam.threads;
+          q.regs_per_thread = regs_sk;
+          q.grid = static_cast<int>(units * v.cta_group);  // the units the work is divided over
+          q.occupancy = occ_sk;
+          q.est_us = std::max(t_math, bytes / hbm_bytes_per_us(hw)) + t_epi + 2.0 + t_fix;
+          q.est_tflops = 2.0 * M * N * K / (q.est_us * 1e6);
+          out->push_back(q);
+        }
+      }
+    }
+    if (occ < target) {
+      if (why) *why += name + ": occupancy; ";
+      continue;
+    }
     // The converting kernel spends shared-memory bandwidth and issue slots
     // widening tiles (calibrated on GB300: INT8 4096^3, W4A16 2048x8960x1536).
     const double conv_eff = mx_native ? kMxRateRatio
@@ -254,7 +313,6 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
          conv_eff);
     const double bytes = elem_a * M * K + elem_b * N * K + 2.0 * M * N * elem_d;
     const double t_mem = bytes / hbm_bytes_per_us(hw);
-    const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
     dg_tile_plan p{};
     p.kernel = widened ? DG_KERNEL_TC_WIDENED : DG_KERNEL_TC;
     p.m_tile = tile_m;
@@ -598,6 +656,28 @@ int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64
   return best;
 }
 
+SkSplit stream_k_split(int64_t tiles, int64_t kblocks, int64_t units) {
+  SkSplit s{tiles, 0, 0, 0, 1};
+  if (tiles < 1 || kblocks < 2 || units < 2 || tiles % units == 0) return s;
+  // the last, ragged wave and (when there is one) the whole wave before it:
+  // every range is then at least one tile long unless the problem has fewer
+  // tiles than units
+  s.sk_tiles = tiles % units + (tiles >= units ? units : 0);
+  s.dp_tiles = tiles - s.sk_tiles;
+  s.sk_iters = s.sk_tiles * kblocks;
+  // ranges of at least half a tile (a tile then meets at most three of them)
+  // and at least kSkMinIters K blocks
+  int64_t u = std::min<int64_t>(units, 2 * s.sk_tiles);
+  u = std::min<int64_t>(u, std::max<int64_t>(1, s.sk_iters / kSkMinIters));
+  s.sk_units = static_cast<int>(u);
+  auto unit_of = [&](int64_t i) { return ((i + 1) * u - 1) / s.sk_iters; };
+  for (int64_t ts = 0; ts < s.sk_tiles; ++ts) {
+    const int64_t pieces = unit_of(ts * kblocks + kblocks - 1) - unit_of(ts * kblocks) + 1;
+    s.max_pieces = std::max<int>(s.max_pieces, static_cast<int>(pieces));
+  }
+  return s;
+}
+
 dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype dtype_b,
                      dg_epilogue epilogue, const dg_hw_desc& hw, double target_occupancy,
                      dg_tile_plan* out, int max_out, int* n_out, std::string* why) {
@@ -649,6 +729,23 @@ bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
         return true;
     if (why) *why = "tensor-core N_tile/stages pair not compiled";
     return false;
+  }
+  if (plan.kernel == DG_KERNEL_TC_STREAMK) {
+    if (!(dtype_a == DG_F16 && dtype_b == DG_F16)) {
+      if (why) *why = "stream-K plans are for F16 x F16";
+      return false;
+    }
+    if ((plan.cta_group != 1 && plan.cta_group != 2) ||
+        plan.m_tile != kTcBlockM * plan.cta_group || plan.k_tile != kTcBlockK ||
+        plan.split_k < 1 || plan.swap_ab != 0) {
+      if (why) *why = "stream-K plan shape not compiled";
+      return false;
+    }
+    if (!tc_streamk_variant(TcVariant{plan.n_tile, plan.stages, plan.cta_group, 0})) {
+      if (why) *why = "stream-K N_tile/stages pair not compiled";
+      return false;
+    }
+    return true;
   }
   if (plan.kernel == DG_KERNEL_TC_WIDENED) {
     const bool i8 = dtype_a == DG_I8 && dtype_b == DG_I8;

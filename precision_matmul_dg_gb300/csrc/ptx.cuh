@@ -407,6 +407,39 @@ __device__ __forceinline__ void sleep_ns(uint32_t ns) {
   asm volatile("nanosleep.u32 %0;" ::"r"(ns));
 }
 
+// A 32-bit flag in global memory shared by CTAs of one grid: a release
+// store (the writer's earlier writes become visible to whoever acquires the
+// value) and an acquire load.
+__device__ __forceinline__ void st_release_gpu(unsigned* flag, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* flag) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  return v;
+}
+
+// Asks for the 128-byte line holding `p` in this SM's L1.
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+// Waits until *flag == want, for at most timeout_ns; on timeout records
+// kStatusTimeout in *status and returns false.
+__device__ __forceinline__ bool wait_flag_eq(const unsigned* flag, unsigned want,
+                                             uint64_t timeout_ns, int* status) {
+  if (ld_acquire_gpu(flag) == want) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    sleep_ns(100);
+    if (ld_acquire_gpu(flag) == want) return true;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      if (status) atomicExch(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes, 8-row groups 1024 bytes apart.
 // Fields: start address >> 4 (bits 0-13), leading-dimension byte offset >> 4

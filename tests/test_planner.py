@@ -61,6 +61,54 @@ def tc_feasible(M, N, hw, target):
     return out
 
 
+# FP16 tensor-core variants also compiled with stream-K work division
+SK_VARIANTS = [(256, 6, 2), (128, 6, 1)]
+
+
+def stream_k_model(tiles, kb, units):
+    """The stream-K division as the kernel documents it, by brute force:
+    whole tiles for all but the last ragged wave and the wave before it, the
+    K blocks of those tiles dealt out in even contiguous ranges (ranges of at
+    least half a tile and at least 4 K blocks), and the pieces of each tile
+    counted by scanning its K blocks.  Returns (dp_tiles, sk_units,
+    max_pieces, longest range) or None when the tiles fill whole waves."""
+    if kb < 2 or units < 2 or tiles % units == 0:
+        return None
+    sk_tiles = tiles % units + (units if tiles >= units else 0)
+    iters = sk_tiles * kb
+    n = min(units, 2 * sk_tiles, max(1, iters // 4))
+    bounds = [u * iters // n for u in range(n + 1)]
+    owner = []
+    for u in range(n):
+        owner += [u] * (bounds[u + 1] - bounds[u])
+    assert len(owner) == iters and all(bounds[u + 1] > bounds[u] for u in range(n))
+    pieces = max(len(set(owner[t * kb:(t + 1) * kb])) for t in range(sk_tiles))
+    longest = max(bounds[u + 1] - bounds[u] for u in range(n))
+    return tiles - sk_tiles, n, pieces, longest
+
+
+def sk_feasible(M, N, K, hw, target):
+    out = {}
+    kb = math.ceil(K / 64)
+    for n_tile, stages, cg in SK_VARIANTS:
+        if cg == 2 and M <= 128:
+            continue
+        if tc_smem(n_tile, stages, cg) > hw["smem_per_block_optin"] or 2 * n_tile > hw["tmem_cols"]:
+            continue
+        if 384 * 168 > hw["regs_per_sm"]:
+            continue
+        units = hw["sm_count"] // cg
+        tiles = math.ceil(M / (128 * cg)) * math.ceil(N / n_tile)
+        m = stream_k_model(tiles, kb, units)
+        if m is None:
+            continue
+        dp, n, pieces, longest = m
+        occ = tiles * kb / (units * (dp // units * kb + longest))
+        if occ >= target:
+            out[("tc_streamk", n_tile, stages, cg)] = (pieces, cg * units)
+    return out
+
+
 def gemv_feasible(M, N, K, hw, target):
     out = set()
     if M > 8:
@@ -108,8 +156,9 @@ SHAPES = [(256, 256, 256), (4096, 4096, 4096), (2048, 2048, 2048), (8192, 8192, 
 @pytest.mark.parametrize("target", [0.0, 0.5, 0.7, 0.9])
 def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
     M, N, K = shape
+    sk = sk_feasible(M, N, K, GB300, target)
     want = (tc_feasible(M, N, GB300, target) | gemv_feasible(M, N, K, GB300, target) |
-            gemv_mma_feasible(M, N, K, GB300, target))
+            gemv_mma_feasible(M, N, K, GB300, target) | set(sk))
     if not want:
         with pytest.raises(dg.DgError) as ei:
             dg.plan_tiles(M, N, K, hw=GB300, target_occupancy=target)
@@ -132,6 +181,17 @@ def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
             assert p["grid"] == cg * min(tiles, GB300["sm_count"] // cg)
             assert p["m_tile"] == 128 * cg and p["k_tile"] == 64 and p["split_k"] == 1
             got.add(("tc", p["n_tile"], p["stages"], cg))
+        elif p["kernel_name"] == "tc_streamk":
+            cg = p["cta_group"]
+            key = ("tc_streamk", p["n_tile"], p["stages"], cg)
+            assert key in sk
+            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], cg)
+            assert 0 < p["regs_per_thread"] <= 168
+            assert p["m_tile"] == 128 * cg and p["k_tile"] == 64
+            # split_k: the most ranges one tile is cut into; grid: the CTAs
+            # the work is divided over
+            assert (p["split_k"], p["grid"]) == sk[key]
+            got.add(key)
         else:
             assert p["kernel_name"] in ("gemv", "gemv_mma")
             assert p["k_tile"] % 256 == 0
@@ -142,6 +202,36 @@ def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
     # ranked by estimated time
     ests = [p["est_us"] for p in plans]
     assert ests == sorted(ests)
+
+
+def test_stream_k_division():
+    # 2048^3 in 256 x 256 pair tiles: 64 tiles of 32 K blocks on 76 pairs,
+    # all of them split (ranges of 26-27 K blocks, a tile meets up to 3)
+    assert stream_k_model(64, 32, 76) == (0, 76, 3, 27)
+    # 4096^3: 256 tiles, 3 whole waves and 28 left: 2 waves stay whole
+    dp, n, pieces, longest = stream_k_model(256, 64, 76)
+    assert (dp, n, pieces) == (152, 76, 2) and longest == 88
+    # one tile of 8 K blocks: two ranges of 4
+    assert stream_k_model(1, 8, 76) == (0, 2, 2, 4)
+    # whole waves, or a single K block: nothing to balance
+    assert stream_k_model(152, 64, 76) is None and stream_k_model(10, 1, 76) is None
+
+
+def test_stream_k_plans_where_waves_are_ragged(dg):
+    # 2560^2 x 4096: 100 pair tiles of 256 x 256 on 76 pairs (1.3 waves)
+    plans = dg.plan_tiles(2560, 2560, 4096, hw=GB300, target_occupancy=0.0)
+    sk = [p for p in plans if p["kernel_name"] == "tc_streamk"]
+    assert {(p["n_tile"], p["cta_group"]) for p in sk} == {(256, 2), (128, 1)}
+    # 4096^3 in 128 x 128 tiles: 1024 tiles on 152 CTAs, 6.7 waves
+    assert any(p["n_tile"] == 128 for p in dg.plan_tiles(4096, 4096, 4096, hw=GB300,
+                                                          target_occupancy=0.0)
+               if p["kernel_name"] == "tc_streamk")
+    # 256 x 256 pair tiles that fill whole waves (76 x 2 = 152 tiles): none of that tile
+    plans = dg.plan_tiles(256 * 76, 512, 4096, hw=GB300, target_occupancy=0.0)
+    assert not [p for p in plans if p["kernel_name"] == "tc_streamk" and p["n_tile"] == 256]
+    # other dtype pairs have none
+    assert not [p for p in dg.plan_tiles(2560, 2560, 4096, "i8", "i8", hw=GB300)
+                if p["kernel_name"] == "tc_streamk"]
 
 
 def test_resources_prune(dg):
