@@ -52,10 +52,10 @@ constexpr int64_t kSkMinIters = 4;
 // Cost of a split tile per extra piece and accumulator element of the tile
 // (microseconds): the writers' partial stores competing with their next
 // main loop, and the finisher's exposed read and add before its epilogue.
-// Calibrated on GB300 against the data-parallel kernel of every FP16 tile:
-// 256 x 256 pair tiles lost 8-10 us a launch at 2048^3, 2560^2 x 4096,
-// 3072^2 x 4096 and 4096^3 and won 30 us at 8192^3; 128 x 128 tiles won
-// 8 us at 128 and 256 x 4096 x 16384.
+// Calibrated on GB300 against the data-parallel kernel of every FP16 tile
+// (CUDA-graph replay): 256 x 256 pair tiles lost 8-10 us a launch at 2048^3,
+// 2560^2 x 4096, 3072^2 x 4096 and 4096^3 and won 30 us at 8192^3; 128 x 128
+// tiles won 8 us at 128 and 256 x 4096 x 16384.
 constexpr double kSkFixUsPerElem = 1.15e-4;
 constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
 // FP16 kernel in its exact-INT32 mode (two FP32 chunk accumulators in TMEM,
@@ -257,10 +257,17 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     const double t_tile =
         tile_flops / (sm_rate_flops_per_us(hw) * tc_tile_efficiency(v.n_tile, v.cta_group));
     const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
-    if (!widened && !narrow && tc_streamk_variant(v)) {
-      // The same tile with stream-K division: whole waves of tiles, then the
-      // rest of the K blocks in one even range per unit; a split tile costs
-      // its finisher the read of the other ranges' partials.
+    if (!widened && !narrow && tc_streamk_variant(v) && tiles < units) {
+      // The same tile with stream-K division: the K blocks in one even range
+      // per unit; a split tile costs its finisher the read of the other
+      // ranges' partials.  Proposed only when the tiles do not fill one wave:
+      // with more tiles than units the ranges start at scattered K offsets,
+      // units that share an operand panel no longer read it in step, and the
+      // panels are read again from DRAM (FP16 8192^3: 1.69 GB a launch
+      // against 1.09 GB for the data-parallel plan, measured on GB300),
+      // which the power cap turns into lost clock: 1501 against 1492 TFLOP/s
+      // under a sustained load.  Forced plans may still divide whole waves
+      // plus ranges.
       const int64_t kbn = k_pad / k_step;
       const SkSplit sp = stream_k_split(tiles, kbn, units);
       const int sk_regs = tc_streamk_kernel_regs(v.n_tile, v.stages, v.cta_group);

@@ -27,7 +27,8 @@ def dg():
 
 # ------------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("name", ["f16_256", "f16_2048", "f16_4096", "f16_8192",
-                                  "thin_1x256x12800", "thin_1x4096x131072"])
+                                  "f16_256x4096x16384", "thin_1x256x12800",
+                                  "thin_1x4096x131072"])
 def test_workload_full_size(dg, name):
     case = workloads.WORKLOADS[name]()
     got, _ = run_case(dg, case)

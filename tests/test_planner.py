@@ -99,6 +99,8 @@ def sk_feasible(M, N, K, hw, target):
             continue
         units = hw["sm_count"] // cg
         tiles = math.ceil(M / (128 * cg)) * math.ceil(N / n_tile)
+        if tiles >= units:            # proposed only below one wave of tiles
+            continue
         m = stream_k_model(tiles, kb, units)
         if m is None:
             continue
@@ -217,20 +219,19 @@ def test_stream_k_division():
     assert stream_k_model(152, 64, 76) is None and stream_k_model(10, 1, 76) is None
 
 
-def test_stream_k_plans_where_waves_are_ragged(dg):
-    # 2560^2 x 4096: 100 pair tiles of 256 x 256 on 76 pairs (1.3 waves)
-    plans = dg.plan_tiles(2560, 2560, 4096, hw=GB300, target_occupancy=0.0)
+def test_stream_k_plans_below_one_wave(dg):
+    # 256 x 4096 x 16384: 16 pair tiles of 256 x 256 on 76 pairs, 64 tiles of
+    # 128 x 128 on 152 CTAs: both divided by K, and ranked first
+    plans = dg.plan_tiles(256, 4096, 16384, hw=GB300, target_occupancy=0.0)
     sk = [p for p in plans if p["kernel_name"] == "tc_streamk"]
     assert {(p["n_tile"], p["cta_group"]) for p in sk} == {(256, 2), (128, 1)}
-    # 4096^3 in 128 x 128 tiles: 1024 tiles on 152 CTAs, 6.7 waves
-    assert any(p["n_tile"] == 128 for p in dg.plan_tiles(4096, 4096, 4096, hw=GB300,
-                                                          target_occupancy=0.0)
-               if p["kernel_name"] == "tc_streamk")
-    # 256 x 256 pair tiles that fill whole waves (76 x 2 = 152 tiles): none of that tile
-    plans = dg.plan_tiles(256 * 76, 512, 4096, hw=GB300, target_occupancy=0.0)
-    assert not [p for p in plans if p["kernel_name"] == "tc_streamk" and p["n_tile"] == 256]
+    assert plans[0]["kernel_name"] == "tc_streamk"
+    # more tiles than units (2560^2 x 4096: 100 pair tiles, 400 single tiles):
+    # whole waves, no stream-K plan
+    plans = dg.plan_tiles(2560, 2560, 4096, hw=GB300, target_occupancy=0.0)
+    assert not [p for p in plans if p["kernel_name"] == "tc_streamk"]
     # other dtype pairs have none
-    assert not [p for p in dg.plan_tiles(2560, 2560, 4096, "i8", "i8", hw=GB300)
+    assert not [p for p in dg.plan_tiles(256, 4096, 16384, "i8", "i8", hw=GB300)
                 if p["kernel_name"] == "tc_streamk"]
 
 

@@ -213,6 +213,14 @@ def f16_square(n, seed=0):
                        name="f16_%d" % n)
 
 
+def f16_long_k(M, N, K, seed=0):
+    """FP16 GEMM with fewer output tiles than the GPU has SMs and a long K (a
+    projection of a few hundred rows), A,B ~ N(0,1)/sqrt(K), C ~ N(0,1),
+    D = 1.0*A.B + 0.5*C."""
+    return random_case(M, N, K, "f16", "f16", alpha=1.0, beta=0.5, seed=seed,
+                       name="f16_%dx%dx%d" % (M, N, K))
+
+
 def i8_square(n=4096, seed=0):
     """INT8 n^3, A,B uniform integers in [-128, 127], alpha=1, beta=0, int32 out."""
     return random_case(n, n, n, "i8", "i8", seed=seed, name="i8_%d" % n)
@@ -259,6 +267,7 @@ WORKLOADS = {
     "f16_2048": lambda: f16_square(2048),
     "f16_4096": lambda: f16_square(4096),
     "f16_8192": lambda: f16_square(8192),
+    "f16_256x4096x16384": lambda: f16_long_k(256, 4096, 16384),
     "i8_4096": lambda: i8_square(4096),
     "thin_1x4096x131072": lambda: thin(4096, 131072),
     "thin_1x256x12800": lambda: thin(256, 12800),
