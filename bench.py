@@ -229,7 +229,7 @@ def workload_info(name):
         "f16_8192": ("FP16 GEMM M=N=K=8192, D=1.0*A.B+0.5*C", "tensor"),
         "f16_256": ("FP16 GEMM M=N=K=256, A,B~U[-1,1)", "tensor"),
         "f16_256x4096x16384": ("FP16 GEMM M=256,N=4096,K=16384 (fewer tiles than SMs, long K), "
-                               "D=1.0*A.B+0.5*C", "tensor"),
+                               "D=1.0*A.B+0.5*C", "hbm"),
         "thin_1x4096x131072": ("FP16 GEMV M=1,N=4096,K=131072 split-K", "hbm"),
         "thin_1x256x12800": ("FP16 GEMV M=1,N=256,K=12800 split-K", "hbm"),
         "i8_4096": ("INT8 GEMM M=N=K=4096, A,B uniform int8, exact INT32 out", "tensor"),

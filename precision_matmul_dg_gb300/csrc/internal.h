@@ -155,9 +155,11 @@ struct SplitKWorkspace {
 // `units` scheduling units (CTAs, or CTA pairs), as the stream-K kernel
 // walks it: tiles [0, dp_tiles) whole, then the sk_iters K blocks of the
 // other sk_tiles tiles cut into sk_units contiguous ranges of equal length
-// (+-1); a tile meets at most max_pieces ranges.  sk_tiles == 0: the tiles
-// fill whole waves (or a tile has one K block) and there is nothing to
-// balance.  Host only (planner.cpp).
+// (+-1); a tile meets at most max_pieces ranges.  With fewer tiles than
+// units every tile is cut into the same number of equal ranges.
+// sk_tiles == 0: the tiles fill whole waves, a tile has one K block, or
+// fewer tiles than units leave no two units per tile: nothing to balance.
+// Host only (planner.cpp).
 struct SkSplit {
   int64_t dp_tiles, sk_tiles, sk_iters;
   int sk_units, max_pieces;

@@ -47,8 +47,10 @@ bool tc_streamk_variant(const TcVariant& v) {
   return (v.n_tile == 256 && v.stages == 6 && v.cta_group == 2) ||
          (v.n_tile == 128 && v.stages == 6 && v.cta_group == 1);
 }
-// Stream-K ranges are at least this many K blocks long
+// Stream-K ranges are at least this many K blocks long, and a tile with
+// fewer tiles than units is cut into at most kSkMaxPieces ranges
 constexpr int64_t kSkMinIters = 4;
+constexpr int64_t kSkMaxPieces = 4;
 // Cost of a split tile per extra piece and accumulator element of the tile
 // (microseconds): the writers' partial stores competing with their next
 // main loop, and the finisher's exposed read and add before its epilogue.
@@ -57,6 +59,11 @@ constexpr int64_t kSkMinIters = 4;
 // 2560^2 x 4096, 3072^2 x 4096 and 4096^3 and won 30 us at 8192^3; 128 x 128
 // tiles won 8 us at 128 and 256 x 4096 x 16384.
 constexpr double kSkFixUsPerElem = 1.15e-4;
+// and a fixed cost of a launch with split tiles (flag hand-off, the
+// finisher's wait): with equal pieces per tile, 128 x 128 tiles measured 1.5
+// to 7.6 us above the model on eight shapes where the data-parallel plan
+// measured -2.4 to 6.2 us above it (K = 3000 to 32768, 6 to 64 tiles)
+constexpr double kSkFixedUs = 3.0;
 constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
 // FP16 kernel in its exact-INT32 mode (two FP32 chunk accumulators in TMEM,
 // running INT32 sums in registers: N_tile a multiple of 64, at most 192)
@@ -281,8 +288,8 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
           const double t_math = unit_iters / kbn * t_tile;
           const double t_fix =
               sp.max_pieces > 1
-                  ? 0.5 + (sp.max_pieces - 1) * static_cast<double>(tile_m) * v.n_tile *
-                              kSkFixUsPerElem
+                  ? kSkFixedUs + (sp.max_pieces - 1) * static_cast<double>(tile_m) * v.n_tile *
+                                     kSkFixUsPerElem
                   : 0.0;
           const double bytes = 2.0 * (M * K + N * K) + 4.0 * M * N;
           dg_tile_plan q{};
@@ -666,16 +673,32 @@ int gemv_best_split(int64_t M, int64_t N, int64_t K, const dg_hw_desc& hw, int64
 SkSplit stream_k_split(int64_t tiles, int64_t kblocks, int64_t units) {
   SkSplit s{tiles, 0, 0, 0, 1};
   if (tiles < 1 || kblocks < 2 || units < 2 || tiles % units == 0) return s;
-  // the last, ragged wave and (when there is one) the whole wave before it:
-  // every range is then at least one tile long unless the problem has fewer
-  // tiles than units
-  s.sk_tiles = tiles % units + (tiles >= units ? units : 0);
-  s.dp_tiles = tiles - s.sk_tiles;
+  int64_t u;
+  if (tiles < units) {
+    // Fewer tiles than units: every tile cut into p equal K ranges (p units
+    // per tile, at most kSkMaxPieces, ranges of at least kSkMinIters K
+    // blocks).  Ranges then never straddle two tiles, and the units holding
+    // the same piece of tiles that share an operand panel read the same K
+    // slices of it at the same time, so each byte crosses DRAM once (with
+    // ranges at scattered offsets the panels were read again: 256 x 4096 x
+    // 16384 in 128 x 128 tiles took 53 us with 152 ranges, 41 us with two
+    // pieces per tile).
+    const int64_t p = std::min<int64_t>(std::min<int64_t>(units / tiles, kSkMaxPieces),
+                                        kblocks / kSkMinIters);
+    if (p < 2) return s;
+    s.sk_tiles = tiles;
+    s.dp_tiles = 0;
+    u = tiles * p;
+  } else {
+    // the last, ragged wave and the whole wave before it, so that every
+    // range is at least one tile long; ranges of at least half a tile and
+    // at least kSkMinIters K blocks
+    s.sk_tiles = tiles % units + units;
+    s.dp_tiles = tiles - s.sk_tiles;
+    u = std::min<int64_t>(units, 2 * s.sk_tiles);
+    u = std::min<int64_t>(u, std::max<int64_t>(1, s.sk_tiles * kblocks / kSkMinIters));
+  }
   s.sk_iters = s.sk_tiles * kblocks;
-  // ranges of at least half a tile (a tile then meets at most three of them)
-  // and at least kSkMinIters K blocks
-  int64_t u = std::min<int64_t>(units, 2 * s.sk_tiles);
-  u = std::min<int64_t>(u, std::max<int64_t>(1, s.sk_iters / kSkMinIters));
   s.sk_units = static_cast<int>(u);
   auto unit_of = [&](int64_t i) { return ((i + 1) * u - 1) / s.sk_iters; };
   for (int64_t ts = 0; ts < s.sk_tiles; ++ts) {

@@ -66,17 +66,25 @@ SK_VARIANTS = [(256, 6, 2), (128, 6, 1)]
 
 
 def stream_k_model(tiles, kb, units):
-    """The stream-K division as the kernel documents it, by brute force:
+    """The stream-K division as the kernel documents it, by brute force.
+    Fewer tiles than units: every tile cut into p = units // tiles equal
+    ranges (at most 4, each at least 4 K blocks; none when p < 2).  Else
     whole tiles for all but the last ragged wave and the wave before it, the
-    K blocks of those tiles dealt out in even contiguous ranges (ranges of at
-    least half a tile and at least 4 K blocks), and the pieces of each tile
-    counted by scanning its K blocks.  Returns (dp_tiles, sk_units,
-    max_pieces, longest range) or None when the tiles fill whole waves."""
+    K blocks of those tiles dealt out in even contiguous ranges (at least half
+    a tile and 4 K blocks each).  The pieces of each tile are counted by
+    scanning its K blocks.  Returns (dp_tiles, sk_units, max_pieces, longest
+    range) or None when there is nothing to balance."""
     if kb < 2 or units < 2 or tiles % units == 0:
         return None
-    sk_tiles = tiles % units + (units if tiles >= units else 0)
+    if tiles < units:
+        p = min(units // tiles, 4, kb // 4)
+        if p < 2:
+            return None
+        sk_tiles, n = tiles, tiles * p
+    else:
+        sk_tiles = tiles % units + units
+        n = min(units, 2 * sk_tiles, max(1, sk_tiles * kb // 4))
     iters = sk_tiles * kb
-    n = min(units, 2 * sk_tiles, max(1, iters // 4))
     bounds = [u * iters // n for u in range(n + 1)]
     owner = []
     for u in range(n):
@@ -207,14 +215,20 @@ def test_plans_satisfy_constraints_and_match_enumeration(dg, shape, target):
 
 
 def test_stream_k_division():
-    # 2048^3 in 256 x 256 pair tiles: 64 tiles of 32 K blocks on 76 pairs,
-    # all of them split (ranges of 26-27 K blocks, a tile meets up to 3)
-    assert stream_k_model(64, 32, 76) == (0, 76, 3, 27)
+    # 2048^3 in 256 x 256 pair tiles: 64 tiles on 76 pairs, no two pairs per
+    # tile: nothing to balance
+    assert stream_k_model(64, 32, 76) is None
+    # 16 tiles of 256 K blocks on 76 pairs: four equal pieces per tile
+    assert stream_k_model(16, 256, 76) == (0, 64, 4, 64)
     # 4096^3: 256 tiles, 3 whole waves and 28 left: 2 waves stay whole
     dp, n, pieces, longest = stream_k_model(256, 64, 76)
     assert (dp, n, pieces) == (152, 76, 2) and longest == 88
     # one tile of 8 K blocks: two ranges of 4
     assert stream_k_model(1, 8, 76) == (0, 2, 2, 4)
+    # 64 tiles of 256 K blocks on 152 CTAs: two halves per tile
+    assert stream_k_model(64, 256, 152) == (0, 128, 2, 128)
+    # one tile of 9 K blocks: two ranges (of at least 4)
+    assert stream_k_model(1, 9, 76) == (0, 2, 2, 5)
     # whole waves, or a single K block: nothing to balance
     assert stream_k_model(152, 64, 76) is None and stream_k_model(10, 1, 76) is None
 
