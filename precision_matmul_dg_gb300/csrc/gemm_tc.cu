@@ -1261,6 +1261,9 @@ cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   int units = plan.grid > 0 ? plan.grid / CG : a.sm_count / CG;
   if (CG == 2 && units > max_pairs[dev & 63]) units = max_pairs[dev & 63];
   if (units > p.num_tiles && !SK) units = p.num_tiles;
+  // Stream-K CTAs wait for one another: every one must be resident at once
+  // (one CTA per SM: the shared memory of a CTA exceeds half an SM's)
+  if (SK && CG == 1 && units > a.sm_count) units = a.sm_count;
   if (units < 1) units = 1;
   SkParams sk{p.num_tiles, 0, 0, 1, nullptr, nullptr};
   if (SK) {
