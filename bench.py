@@ -189,6 +189,7 @@ KERNEL_SOURCES = {
     "gemv_cluster_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
     "gemv_mma_kernel": ("gemv.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
     "skinny_w4a16_kernel": ("skinny.cu", "ptx.cuh", "epilogue.cuh", "internal.h"),
+    "gemm_w4t_kernel": ("gemm_w4t.cu", "tc_common.cuh", "ptx.cuh", "epilogue.cuh", "internal.h"),
 }
 
 
@@ -234,6 +235,8 @@ def workload_info(name):
         "thin_1x256x12800": ("FP16 GEMV M=1,N=256,K=12800 split-K", "hbm"),
         "i8_4096": ("INT8 GEMM M=N=K=4096, A,B uniform int8, exact INT32 out", "tensor"),
         "w4a16_m16": ("W4A16 M=16,N=8960,K=1536, E2M1 weights x FP16, bias+erf-GELU", "hbm"),
+        "w4a16_m256": ("W4A16 M=256,N=8960,K=1536, E2M1 weights x FP16, bias+erf-GELU",
+                       "tensor"),
         "w4a16_m2048": ("W4A16 M=2048,N=8960,K=1536, E2M1 weights x FP16, bias+erf-GELU",
                         "tensor"),
         "qkv_1x128x4096_b96": ("96 FP16 GEMMs M=1,N=128,K=4096 in one strided-batched call "
@@ -269,7 +272,8 @@ def algorithmic_bytes(case):
 def kernel_name(plan, case):
     """The step's dominant kernel: the split-K GEMV, the tensor-core kernel
     (FP16; widened INT8 / E2M1 / MXFP4 operands; MXFP4 on the block-scaled
-    MMA) or the converting kernel."""
+    MMA), the W4A16 kernel that widens the weights in tensor memory, or the
+    converting kernel."""
     if plan["kernel_name"] == "gemv":
         # 2 .. 8 splits reduce inside a thread-block cluster
         return "gemv_cluster_kernel" if 2 <= plan["split_k"] <= 8 else "gemv_splitk_kernel"
@@ -277,6 +281,8 @@ def kernel_name(plan, case):
         return "skinny_w4a16_kernel"
     if plan["kernel_name"] == "gemv_mma":
         return "gemv_mma_kernel"
+    if plan["kernel_name"] == "tc" and plan.get("swap_ab"):
+        return "gemm_w4t_kernel"  # W4A16 with the weights widened in tensor memory
     if plan["kernel_name"] == "tc_widened" or case.dtype_a == "mxf4" or \
             (case.dtype_a == "f16" and case.dtype_b == "f16"):
         return "gemm_tc_kernel"
@@ -480,7 +486,7 @@ def roofline(w, kern_avg_ms, peaks, peak_src):
 
 def plan_summary(plan):
     return {k: plan[k] for k in ("kernel_name", "m_tile", "n_tile", "k_tile", "split_k", "stages",
-                                 "grid")}
+                                 "grid", "swap_ab")}
 
 
 def measure_e2e(w, args, world, stream):

@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdg.so")
 
 SOURCES = ["api.cu", "planner.cpp", "gemv.cu", "gemm_tc.cu", "gemm_conv.cu", "widen.cu",
-           "skinny.cu", "mx.cu"]
+           "skinny.cu", "mx.cu", "gemm_w4t.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-I", INCLUDE, "-I", CSRC]

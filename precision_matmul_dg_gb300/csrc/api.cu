@@ -527,6 +527,23 @@ dg_status dispatch(const GemmArgs& a, const dg_tile_plan& plan, int dev) {
       }
     }
     e = launch_tc_mx(w, plan);
+  } else if (plan.kernel == DG_KERNEL_TC && plan.swap_ab) {
+    // FP16 x E2M1 with the weights widened in tensor memory.  Layouts its
+    // TMA copies cannot take run the widening path on a compiled FP16 tile.
+    if (!w4t_layout_ok(a)) {
+      dg_tile_plan wp = plan;
+      wp.kernel = DG_KERNEL_TC_WIDENED;
+      wp.swap_ab = 0;
+      wp.k_tile = 64;
+      wp.split_k = 1;
+      wp.grid = 0;
+      wp.cta_group = M > 128 ? 2 : 1;
+      wp.m_tile = 128 * wp.cta_group;
+      wp.n_tile = M > 128 ? 192 : 128;
+      wp.stages = 6;
+      return dispatch(a, wp, dev);
+    }
+    e = launch_w4t(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC) {
     e = (da == DG_F16 && db == DG_F16) ? launch_tc(a, plan) : launch_conv(a, plan);
   } else if (plan.kernel == DG_KERNEL_TC_STREAMK) {

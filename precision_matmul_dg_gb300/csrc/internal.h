@@ -176,6 +176,13 @@ dg_status get_sk_workspace(int dev, cudaStream_t stream, int64_t partial_elems,
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan);    // F16 x F16
 // F16 x F16 with stream-K work division (DG_KERNEL_TC_STREAMK plans).
 cudaError_t launch_tc_streamk(const GemmArgs& a, const dg_tile_plan& plan);
+// F16 x E2M1 with the weights widened in tensor memory (gemm_w4t.cu):
+// DG_KERNEL_TC plans with swap_ab == 1 (tiles of 128 weight rows x n_tile
+// activation rows).  w4t_layout_ok: the operand and output layouts its TMA
+// copies need (otherwise the call runs the widening path).
+cudaError_t launch_w4t(const GemmArgs& a, const dg_tile_plan& plan);
+bool w4t_layout_ok(const GemmArgs& a);
+int w4t_kernel_regs(int n_tile, int stages);
 // MXFP4 x MXFP4 on the block-scaled MMA (gemm_tc.cu): a.A, a.B packed codes
 // with K even; a.scale_a, a.scale_b 16-byte aligned with lds_a, lds_b
 // multiples of 16.

@@ -42,6 +42,20 @@ constexpr TcVariant kTcVariantsF16[] = {{256, 4, 1, 0}, {128, 6, 1, 0}, {64, 8, 
                                         {256, 6, 2, 0}, {224, 6, 2, 0}, {192, 6, 2, 0},
                                         {128, 8, 2, 0}};
 constexpr int kNumTcVariantsF16 = 7;
+// FP16 x E2M1 with the weights widened in tensor memory (gemm_w4t.cu): D^T
+// tiles of 128 weight rows x n_tile activation rows, single CTAs, 448
+// threads; shared memory: per stage an activation tile (n_tile rows of 128
+// bytes) and 4 KB of codes, and 32 KB of epilogue boxes
+constexpr TcVariant kW4tVariants[] = {{160, 7, 1, 0}};
+constexpr int kW4tThreads = 448;
+// Its cost per tile: a fixed part and the stages at this fraction of the
+// tensor rate (the converters widen every weight again for each activation
+// tile and share the SMs' issue slots with the epilogue).  Calibrated on
+// GB300 (CUDA-graph replay, no epilogue): 2048 x 8960 x 1536, 41.1 us in 6
+// waves of 24 K blocks; 4096^3, 94.4 us in 6 waves of 64 K blocks.
+constexpr double kW4tEfficiency = 0.70;
+constexpr double kW4tTileUs = 0.9;
+
 // FP16 x FP16 tiles also compiled with stream-K work division
 bool tc_streamk_variant(const TcVariant& v) {
   return (v.n_tile == 256 && v.stages == 6 && v.cta_group == 2) ||
@@ -342,6 +356,69 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     p.grid = static_cast<int>(std::min<int64_t>(tiles, units) * v.cta_group);
     p.occupancy = occ;
     p.est_us = std::max(t_math, t_mem) + t_epi + 2.0 + t_pre;
+    p.est_tflops = 2.0 * M * N * K / (p.est_us * 1e6);
+    out->push_back(p);
+  }
+}
+
+int w4t_smem_bytes(const TcVariant& v) {
+  return v.stages * (v.n_tile * kTcBlockK * 2 + kTcBlockM * kTcBlockK / 2) +
+         8 * 2 * 32 * 32 * 2 + 1024 + 512;
+}
+
+// FP16 x E2M1 with the weights widened in tensor memory: D^T tiles of 128
+// weight rows x n_tile activation rows, one CTA per SM.
+void add_w4t_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db,
+                        const dg_hw_desc& hw, double target, std::vector<dg_tile_plan>* out,
+                        std::string* why) {
+  if (!(da == DG_F16 && db == DG_E2M1) || hw.cc_major < 10 || hw.tmem_cols <= 0) return;
+  for (const TcVariant& v : kW4tVariants) {
+    const std::string name = "tensor-memory widening N_tile " + std::to_string(v.n_tile);
+    const int smem = w4t_smem_bytes(v);
+    if (smem > hw.smem_per_block_optin) {
+      if (why) *why += name + ": shared memory; ";
+      continue;
+    }
+    if (2 * v.n_tile + 2 * 32 > hw.tmem_cols) {  // two accumulators and two A slots
+      if (why) *why += name + ": tensor memory; ";
+      continue;
+    }
+    const int measured = w4t_kernel_regs(v.n_tile, v.stages);
+    const int regs = measured > 0 ? measured : 144;
+    if (regs > hw.regs_per_thread_max || regs * kW4tThreads > hw.regs_per_sm) {
+      if (why) *why += name + ": registers; ";
+      continue;
+    }
+    const int64_t units = std::max(1, hw.sm_count);
+    const int64_t tiles = ceil_div(N, kTcBlockM) * ceil_div(M, v.n_tile);
+    const int64_t waves = ceil_div(tiles, units);
+    const double occ = static_cast<double>(tiles) / static_cast<double>(waves * units);
+    if (occ < target) {
+      if (why) *why += name + ": occupancy; ";
+      continue;
+    }
+    const int64_t kbn = ceil_div(K, kTcBlockK);
+    const double t_stage = 2.0 * kTcBlockM * v.n_tile * kTcBlockK /
+                           (sm_rate_flops_per_us(hw) * kW4tEfficiency);
+    const double t_math = waves * (kW4tTileUs + kbn * t_stage);
+    const double bytes = 2.0 * M * K + 0.5 * N * K + 2.0 * M * N;
+    const double t_mem = bytes / hbm_bytes_per_us(hw);
+    const double t_epi = (128.0 * v.n_tile * 4.0) / (hbm_bytes_per_us(hw) / hw.sm_count);
+    dg_tile_plan p{};
+    p.kernel = DG_KERNEL_TC;
+    p.m_tile = kTcBlockM;
+    p.n_tile = v.n_tile;
+    p.k_tile = kTcBlockK;
+    p.split_k = 1;
+    p.stages = v.stages;
+    p.cta_group = 1;
+    p.swap_ab = 1;
+    p.smem_bytes = smem;
+    p.threads = kW4tThreads;
+    p.regs_per_thread = regs;
+    p.grid = static_cast<int>(std::min<int64_t>(tiles, units));
+    p.occupancy = occ;
+    p.est_us = std::max(t_math, t_mem) + t_epi + 2.0;
     p.est_tflops = 2.0 * M * N * K / (p.est_us * 1e6);
     out->push_back(p);
   }
@@ -717,6 +794,7 @@ dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype
   if (hw.tmem_cols > 0) {
     add_tc_candidates(M, N, K, dtype_a, dtype_b, false, hw, target_occupancy, &cands, why);
     add_tc_candidates(M, N, K, dtype_a, dtype_b, true, hw, target_occupancy, &cands, why);
+    add_w4t_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
     add_gemv_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
     add_gemv_mma_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
     add_skinny_candidates(M, N, K, dtype_a, dtype_b, hw, target_occupancy, &cands, why);
@@ -736,6 +814,21 @@ dg_status plan_tiles(int64_t M, int64_t N, int64_t K, dg_dtype dtype_a, dg_dtype
 bool plan_is_runnable(const dg_tile_plan& plan, int64_t M, int64_t N, int64_t K,
                       dg_dtype dtype_a, dg_dtype dtype_b, std::string* why) {
   (void)N;
+  if (plan.kernel == DG_KERNEL_TC && plan.swap_ab == 1) {
+    if (!(dtype_a == DG_F16 && dtype_b == DG_E2M1)) {
+      if (why) *why = "tensor-memory widening plans (swap_ab) are for F16 x E2M1";
+      return false;
+    }
+    if (plan.cta_group != 1 || plan.m_tile != kTcBlockM || plan.k_tile != kTcBlockK ||
+        plan.split_k != 1) {
+      if (why) *why = "tensor-memory widening plan shape not compiled";
+      return false;
+    }
+    for (const TcVariant& v : kW4tVariants)
+      if (v.n_tile == plan.n_tile && v.stages == plan.stages) return true;
+    if (why) *why = "tensor-memory widening N_tile/stages pair not compiled";
+    return false;
+  }
   if (plan.kernel == DG_KERNEL_TC) {
     const TcFamily fam = tc_family(dtype_a, dtype_b);
     if (!fam.v) {

@@ -377,7 +377,7 @@ def test_int8_widened_extremes(dg):
 
 
 # ------------------------------------------------------- W4A16
-@pytest.mark.parametrize("name", ["w4a16_m16", "w4a16_m2048"])
+@pytest.mark.parametrize("name", ["w4a16_m16", "w4a16_m256", "w4a16_m2048"])
 def test_w4a16_workload_full_size(dg, name):
     case = workloads.WORKLOADS[name]()
     got, _ = run_case(dg, case)
@@ -456,7 +456,9 @@ def test_w4a16_every_plan(dg):
     case = workloads.random_case(200, 700, 600, "f16", "e2m1", epilogue="bias_gelu", beta=0.5,
                                  seed=5)
     plans = [p for p in _plans(dg, case) if p["kernel_name"] in ("tc", "tc_widened")]
-    assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc"} == {64, 128, 256}
+    assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc" and not p["swap_ab"]} == \
+        {64, 128, 256}
+    assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc" and p["swap_ab"]} == {160}
     assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc_widened"} >= {128, 224, 256}
     assert {p["cta_group"] for p in plans if p["kernel_name"] == "tc_widened"} == {1, 2}
     for p in plans:

@@ -272,6 +272,7 @@ WORKLOADS = {
     "thin_1x4096x131072": lambda: thin(4096, 131072),
     "thin_1x256x12800": lambda: thin(256, 12800),
     "w4a16_m16": lambda: w4a16(16),
+    "w4a16_m256": lambda: w4a16(256),
     "w4a16_m2048": lambda: w4a16(2048),
     "qkv_1x128x4096_b96": lambda: batched_thin(96, 128, 4096),
     "mxf4_4096": lambda: mxf4_case(4096, 4096, 4096, beta=0.5, name="mxf4_4096", fp16_a=True),
