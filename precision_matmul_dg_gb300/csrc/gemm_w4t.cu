@@ -91,6 +91,7 @@ struct W4tSmem {
   static constexpr int kLaunchBytes = kBytes + 1024;
   static_assert(kXBytes % 1024 == 0, "activation tiles keep the 1 KB swizzle alignment");
   static_assert(kASlots >= 2, "tensor memory for at least two A slots");
+  static_assert(kBytes + 1024 <= 232448, "shared memory of one CTA");
 };
 
 // Eight E2M1 codes (one 32-bit word, code 2i in the low nibble of byte i) as
@@ -485,13 +486,17 @@ bool w4t_layout_ok(const GemmArgs& a) {
 
 int w4t_kernel_regs(int n_tile, int stages) {
   if (n_tile == 160 && stages == 7) return w4t_regs<160, 7>();
+  if (n_tile == 224 && stages == 6) return w4t_regs<224, 6>();
   return 0;
 }
 
 // FP16 activations x packed E2M1 weights, D^T tiles of 128 weight rows x
 // plan.n_tile activation rows (plan.swap_ab == 1).
 cudaError_t launch_w4t(const GemmArgs& a, const dg_tile_plan& plan) {
+  // 160 rows: six A slots; 224 rows: two, but 448 cycles of MMA a stage,
+  // half again the converters' time
   if (plan.n_tile == 160 && plan.stages == 7) return run_w4t<160, 7>(a, plan);
+  if (plan.n_tile == 224 && plan.stages == 6) return run_w4t<224, 6>(a, plan);
   return cudaErrorNotSupported;
 }
 

@@ -46,7 +46,7 @@ constexpr int kNumTcVariantsF16 = 7;
 // tiles of 128 weight rows x n_tile activation rows, single CTAs, 448
 // threads; shared memory: per stage an activation tile (n_tile rows of 128
 // bytes) and 4 KB of codes, and 32 KB of epilogue boxes
-constexpr TcVariant kW4tVariants[] = {{160, 7, 1, 0}};
+constexpr TcVariant kW4tVariants[] = {{160, 7, 1, 0}, {224, 6, 1, 0}};
 constexpr int kW4tThreads = 448;
 // Its cost per tile: a fixed part and the stages at this fraction of the
 // tensor rate (the converters widen every weight again for each activation

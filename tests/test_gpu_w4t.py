@@ -27,12 +27,16 @@ def dg():
     return dg
 
 
-def _w4t_plan(dg, case):
+def _w4t_plans(dg, case):
     plans = [p for p in dg.plan_tiles(case.M, case.N, case.K, "f16", "e2m1", case.epilogue,
                                       target_occupancy=0.0)
              if p["kernel_name"] == "tc" and p["swap_ab"]]
-    assert len(plans) == 1
-    return plans[0]
+    assert sorted(p["n_tile"] for p in plans) == [160, 224]
+    return plans
+
+
+def _w4t_plan(dg, case, n_tile=160):
+    return [p for p in _w4t_plans(dg, case) if p["n_tile"] == n_tile][0]
 
 
 # ragged M, N and K (odd K: a half byte past the last code of each row), M
@@ -47,17 +51,18 @@ def test_w4t_shapes(dg, shape, epi):
     M, N, K = shape
     case = workloads.random_case(M, N, K, "f16", "e2m1", epilogue=epi, alpha=0.75, beta=-0.5,
                                  seed=hash((M, N, K, epi)) % 991, pad=255)
-    p = _w4t_plan(dg, case)
-    for grid in (p["grid"], 5, 1):  # persistent CTAs walking several tiles
-        got, _ = run_case(dg, case, plan=dict(p, grid=grid))
-        assert_parity(case, got)
+    for p in _w4t_plans(dg, case):
+        for grid in (p["grid"], 5, 1):  # persistent CTAs walking several tiles
+            got, _ = run_case(dg, case, plan=dict(p, grid=grid))
+            assert_parity(case, got)
 
 
 def test_w4t_without_c(dg):
     case = workloads.random_case(900, 1100, 768, "f16", "e2m1", epilogue="bias_gelu", seed=21)
-    got, tail = run_case(dg, case, plan=_w4t_plan(dg, case), canary=64)
-    assert_parity(case, got)
-    assert np.all(tail == np.float16(-7.5))
+    for p in _w4t_plans(dg, case):
+        got, tail = run_case(dg, case, plan=p, canary=64)
+        assert_parity(case, got)
+        assert np.all(tail == np.float16(-7.5))
 
 
 def test_w4t_every_code_one_hot(dg):
@@ -78,17 +83,19 @@ def test_w4t_every_code_one_hot(dg):
         k, code = j % K, j % 16
         packed[j, k // 2] |= np.uint8(code << (4 * (k % 2)))
     case.B = packed
-    got, _ = run_case(dg, case, plan=_w4t_plan(dg, case))
-    for j in range(N):
-        want = case.A[:, j % K].astype(np.float64) * table[j % 16]
-        assert np.array_equal(got[:, j].astype(np.float64), want), j
+    for p in _w4t_plans(dg, case):
+        got, _ = run_case(dg, case, plan=p)
+        for j in range(N):
+            want = case.A[:, j % K].astype(np.float64) * table[j % 16]
+            assert np.array_equal(got[:, j].astype(np.float64), want), j
 
 
-def test_w4t_full_size(dg):
+@pytest.mark.parametrize("n_tile", [160, 224])
+def test_w4t_full_size(dg, n_tile):
     case = workloads.WORKLOADS["w4a16_m2048"]()
-    a, _ = run_case(dg, case, plan=_w4t_plan(dg, case))
+    a, _ = run_case(dg, case, plan=_w4t_plan(dg, case, n_tile))
     assert_parity(case, a)
-    b, _ = run_case(dg, case, plan=_w4t_plan(dg, case))
+    b, _ = run_case(dg, case, plan=_w4t_plan(dg, case, n_tile))
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))  # fixed summation order
 
 

@@ -343,17 +343,18 @@ def test_converting_kernel_plans(dg, pair, shape):
     conv = [p for p in plans if p["kernel_name"] == "tc" and not p["swap_ab"]]
     assert {(p["n_tile"], p["stages"]) for p in conv} == set(CONV_VARIANTS[pair])
     # FP16 x E2M1 also: the weights widened in tensor memory, D^T tiles of 128
-    # weight rows x 160 activation rows (7 stages of a 20 KB activation tile
-    # and 4 KB of codes, 32 KB of epilogue boxes), 448 threads
+    # weight rows x 160 or 224 activation rows (7 or 6 stages of an activation
+    # tile and 4 KB of codes, 32 KB of epilogue boxes), 448 threads
     swapped = [p for p in plans if p["kernel_name"] == "tc" and p["swap_ab"]]
     if pair == ("f16", "e2m1"):
-        assert [(p["m_tile"], p["n_tile"], p["stages"], p["cta_group"]) for p in swapped] == \
-            [(128, 160, 7, 1)]
-        w4t = swapped[0]
-        assert w4t["threads"] == 448
-        assert w4t["smem_bytes"] == 7 * (160 * 128 + 128 * 32) + 8 * 2 * 2048 + 1024 + 512
-        assert w4t["smem_bytes"] <= GB300["smem_per_block_optin"]
-        assert w4t["grid"] == min(152, math.ceil(N / 128) * math.ceil(M / 160))
+        assert sorted((p["m_tile"], p["n_tile"], p["stages"], p["cta_group"]) for p in swapped) == \
+            [(128, 160, 7, 1), (128, 224, 6, 1)]
+        for w4t in swapped:
+            bn, st = w4t["n_tile"], w4t["stages"]
+            assert w4t["threads"] == 448
+            assert w4t["smem_bytes"] == st * (bn * 128 + 128 * 32) + 8 * 2 * 2048 + 1024 + 512
+            assert w4t["smem_bytes"] <= GB300["smem_per_block_optin"]
+            assert w4t["grid"] == min(152, math.ceil(N / 128) * math.ceil(M / bn))
     else:
         assert not swapped
     for p in conv:
