@@ -458,7 +458,7 @@ def test_w4a16_every_plan(dg):
     plans = [p for p in _plans(dg, case) if p["kernel_name"] in ("tc", "tc_widened")]
     assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc" and not p["swap_ab"]} == \
         {64, 128, 256}
-    assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc" and p["swap_ab"]} == {160}
+    assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc" and p["swap_ab"]} == {160, 224}
     assert {p["n_tile"] for p in plans if p["kernel_name"] == "tc_widened"} >= {128, 224, 256}
     assert {p["cta_group"] for p in plans if p["kernel_name"] == "tc_widened"} == {1, 2}
     for p in plans:
