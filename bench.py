@@ -451,6 +451,11 @@ def roofline(w, kern_avg_ms, peaks, peak_src):
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "peak_source": "%s bf16 dense burst (fp16 runs at the bf16 rate)" % peak_src}
+        # The same figure against the measured sustained rate (seconds of
+        # back-to-back GEMMs under the power cap), for context: a timed region
+        # of many launches runs under the same cap.  `frac` keeps the burst.
+        if peaks.get("bf16_tflops_sustained"):
+            roof["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
         if base.dtype_a == "i8":
             roof["unit"] = "TOPS"
             roof["peak_source"] += ("; INT8 runs on the FP16 tensor path (sm_103a has no "
@@ -462,6 +467,9 @@ def roofline(w, kern_avg_ms, peaks, peak_src):
             roof.update(peak=peak, frac=round(achieved / peak, 4),
                         peak_source="%s bf16 dense burst x 6 (nominal FP4 / bf16 dense ratio)"
                                     % peak_src)
+            if peaks.get("bf16_tflops_sustained"):
+                roof["frac_of_sustained"] = round(achieved / (peaks["bf16_tflops_sustained"] * 6.0),
+                                                  4)
     else:
         gbs = algorithmic_bytes(base) / (kern_avg_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
