@@ -35,13 +35,15 @@ PROGRAMS = {
 FAMILIES = [
     (("f16", "f16"), (512, 1040, 520), "tc, single CTA"),
     (("f16", "f16"), (1536, 2000, 512), "tc, CTA pair"),
+    (("f16", "f16"), (128, 4096, 16384), "tc, stream-K (two K halves per tile)"),
     (("f16", "f16"), (3, 300, 5000), "gemv, split-K"),
     (("f16", "f16"), (1, 4000, 3000), "gemv"),
     (("f16", "f16"), (5, 1000, 3000), "warp-MMA gemv"),
     (("f16", "f16"), (16, 700, 20000), "warp-MMA gemv, split-K"),
     (("f16", "e2m1"), (8, 1000, 2048), "skinny"),
     (("f16", "e2m1"), (130, 1000, 512), "tc with in-kernel widening"),
-    (("f16", "e2m1"), (1024, 2048, 1024), "widened then tc pair"),
+    (("f16", "e2m1"), (1024, 2048, 1024), "tc, weights widened in tensor memory"),
+    (("f16", "e2m1"), (2048, 2048, 1024), "widened then tc pair"),
 ]
 
 
