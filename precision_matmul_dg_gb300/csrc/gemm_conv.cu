@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "convert.cuh"
 #include "tc_common.cuh"
 
 namespace dg {
@@ -112,20 +113,6 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
   lo = *reinterpret_cast<uint32_t*>(&ha);
   hi = *reinterpret_cast<uint32_t*>(&hb);
-}
-
-// Eight E2M1 codes (one 32-bit word, code k in bits 4k..4k+3) -> eight FP16.
-__device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w) {
-  uint4 o;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
-      : "r"(w));
-  return o;
 }
 
 // Byte offset of the 16-byte chunk c (0..7) of row r in a 128-byte-swizzled

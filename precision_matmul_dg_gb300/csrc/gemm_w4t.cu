@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "convert.cuh"
 #include "tc_common.cuh"
 
 namespace dg {
@@ -93,19 +94,6 @@ struct W4tSmem {
   static_assert(kASlots >= 2, "tensor memory for at least two A slots");
   static_assert(kBytes + 1024 <= 232448, "shared memory of one CTA");
 };
-
-// Eight E2M1 codes (one 32-bit word, code 2i in the low nibble of byte i) as
-// four FP16 pairs, exact.
-__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t* f) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
-      : "r"(w));
-}
 
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
 

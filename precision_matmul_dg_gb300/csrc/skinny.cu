@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "convert.cuh"
 #include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -78,28 +79,6 @@ struct SkParams {
   Epi epi;
 };
 static_assert(sizeof(SkParams) <= 128, "parameter struct within 128 bytes (see Epi)");
-
-// The four bytes of `w` (eight E2M1 codes) -> four FP16 pairs, byte i into
-// f[i] (low nibble in the low half), exact: the word is split into its bytes
-// once and each byte goes through the hardware pair conversion.
-__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&f)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
-      : "r"(w));
-}
-
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
 
 // d += a (16 x 16, row-major fragment) . b (16 x 8, column-major fragment)
 __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,

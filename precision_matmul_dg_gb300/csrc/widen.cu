@@ -17,50 +17,12 @@
 
 #include <type_traits>
 
+#include "convert.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace dg {
 namespace {
-
-__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t two_bytes) {
-  // byte b -> fp16 bits 0x6400 | (b ^ 0x80) = 1024 + (v + 128); minus 1152
-  const uint32_t x = (two_bytes ^ 0x8080u);
-  uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-  __half2 h = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// The four bytes of `w` (eight E2M1 codes) -> four FP16 pairs (byte i into
-// the i-th word, low nibble in the low half), exact: the word is split into
-// its bytes once and each byte goes through the hardware pair conversion.
-__device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w) {
-  uint4 o;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
-      : "r"(w));
-  return o;
-}
-
-// Streaming loads that do not allocate in L1 (each byte is read once).
-__device__ __forceinline__ uint2 ld_stream8(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
-               : "=r"(v.x), "=r"(v.y)
-               : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
 
 // The copy is written in chunks of 16 bytes (8 FP16 values), each made from
 // 8 int8 bytes or 4 bytes of packed E2M1 codes.  Consecutive threads take
