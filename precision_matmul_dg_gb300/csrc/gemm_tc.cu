@@ -208,8 +208,9 @@ constexpr int kMxSfImage = 512;           // one image: 128 rows x 4 scales
 constexpr int kMxSfRowBlock = 2 * kMxSfImage;  // 128 rows x the 8 scales of a stage
 
 // Shared memory: the operand ring, then two staging boxes per epilogue warp,
-// then the barriers.
-template <int BN, int Stages, int CG, int Kind = kKind16>
+// then (INT32 mode with an odd number of 32-column chunks) the running sums
+// of the last chunk, then the barriers.
+template <int BN, int Stages, int CG, int Kind = kKind16, int ExtraBytes = 0>
 struct TcSmem {
   static constexpr int kRowsB = BN / CG;  // B rows this CTA loads
   static constexpr int kTileBytesB = kRowsB * kBlockK * 2;
@@ -227,7 +228,8 @@ struct TcSmem {
   static constexpr int kOffSfRows = kOffSf + Stages * kSfBytes;
   static constexpr int kOffEpi = kOffSfRows + Stages * kSfRowsBytes;
   static constexpr int kEpiBytes = kEpiWarps * 2 * tc::kEpiBoxBytes;
-  static constexpr int kOffBar = kOffEpi + kEpiBytes;
+  static constexpr int kOffExtra = kOffEpi + kEpiBytes;
+  static constexpr int kOffBar = kOffExtra + ExtraBytes;
   // full[Stages], empty[Stages], tmem_full[2], tmem_empty[2], drain, one
   // C-load barrier per staging box, then (MXFP4) sf_full[Stages] (the
   // stage's scale bytes landed) and img_ready[Stages] (its images built)
@@ -236,6 +238,7 @@ struct TcSmem {
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
   static constexpr int kLaunchBytes = kBytes + 1024;  // room to align the base to 1 KB
+  static_assert(kLaunchBytes <= 232448, "shared memory of one CTA");
   static_assert(kTileBytesB % 1024 == 0, "B tiles keep 1 KB alignment");
   static_assert(kOffSfRows % 128 == 0 && kSfRowsBytes % 128 == 0, "TMA destinations aligned");
 };
@@ -317,6 +320,13 @@ __device__ __forceinline__ void epi_load_c(const CUtensorMap* map, const TcParam
       if (epi_box<BN, CG>(p, t, rank, wi, kk, x, y)) tma_prefetch_l2_2d(map, x, y);
 }
 
+// INT32 mode: running sums of a tile's last 32 columns when BN / 32 is odd
+// (the registers of a warp hold whole pairs of chunks; see the epilogue).
+template <int BN, int Out>
+struct I32Extra {
+  static constexpr int kBytes = (Out == kOutI32 && BN % 64 == 32) ? kBlockM * 32 * 4 : 0;
+};
+
 template <int BN, int Stages, int CG, int Out, int Kind, bool SK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -326,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_sfa,
                        const __grid_constant__ CUtensorMap tmap_sfb, const TcParams p,
                        const __grid_constant__ EpiProgram prog, const SkParams sk) {
-  using L = TcSmem<BN, Stages, CG, Kind>;
+  using L = TcSmem<BN, Stages, CG, Kind, I32Extra<BN, Out>::kBytes>;
   constexpr bool kMx = Kind == kKindMx;
   static_assert(!kMx || Out == kOutF16, "MXFP4: FP16 output");
   // Stream-K: 16-bit operands, FP16 output through the staged epilogue, and
@@ -734,15 +744,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (Out == kOutI32) {
       // Exact INT32 (INT8 operands widened to FP16).  Each K chunk of at most
       // 1024 accumulates exact integers in FP32 (|chunk sum| <= 1024 * 2^14 =
-      // 2^24); the warp converts them and adds them to running INT32 sums in
-      // registers (wrapping mod 2^32), and after the tile's last chunk writes
-      // D = alpha * sum + beta * C (mod 2^32) as 32 x 16 INT32 boxes through
-      // the staging buffers (or straight from registers without staging).
-      static_assert(Out != kOutI32 || BN % 64 == 0, "INT32 mode: equal chunks per warp");
-      constexpr int kCpw = BN / 64;  // 32-column chunks per warp
+      // 2^24); the warp converts them and adds them to running INT32 sums
+      // (wrapping mod 2^32), and after the tile's last chunk writes D = alpha
+      // * sum + beta * C (mod 2^32) as 32 x 16 INT32 boxes through the
+      // staging buffers (or straight from registers without staging).  The
+      // two warps of a lane quarter take kCpw 32-column chunks each, their
+      // sums in registers (32 per chunk); when BN / 32 is odd the last chunk
+      // is split between them, 16 columns each, its sums in shared memory
+      // (column-major, so that the lanes' rows fall in different banks):
+      // 224 columns keep 96 sum registers a thread, as 192 do.
+      static_assert(Out != kOutI32 || BN % 32 == 0, "INT32 mode: whole 32-column chunks");
+      constexpr int kCpw = BN / 64;  // 32-column chunks per warp in registers
+      constexpr bool kSplitLast = BN % 64 == 32;
       const int c_lo = half * kCpw;
       const int wi = warp - kEpiWarp0;
       uint8_t* boxes = smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes;
+      // this lane's 16 sums of the split chunk: column half * 16 + i at i * kBlockM
+      uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L::kOffExtra) +
+                     half * 16 * kBlockM + ew * 32 + lane;
       const uint32_t al = static_cast<uint32_t>(p.alpha_i), be = static_cast<uint32_t>(p.beta_i);
       uint32_t sum[kCpw][32];
       int nstores = 0;  // stores issued; store i goes through box i & 1
@@ -772,6 +791,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               sum[cl][i] = ch == 0 ? v : sum[cl][i] + v;
             }
           }
+          if constexpr (kSplitLast) {
+            uint32_t r[16];
+            tmem_ld_16cols(tbase + 2 * kCpw * 32 + half * 16, r);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t v = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+              xs[i * kBlockM] = ch == 0 ? v : xs[i * kBlockM] + v;
+            }
+          }
           tc_fence_before_sync();
           if (CG == 2)
             mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc * 8));
@@ -785,54 +814,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const int row = y + lane;
         const int32_t* crow = static_cast<const int32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
+        // D's 16 columns from x: o = alpha * sums (+ beta * C), stored
+        auto emit = [&](int x, uint32_t (&o)[16]) {
+          if (x >= p.N || y >= p.M) return;  // warp-uniform: the box is wholly outside D
+          if (be != 0u && row < p.M) {
+            if (x + 16 <= p.N && (p.ldc & 3) == 0 &&
+                (reinterpret_cast<uintptr_t>(p.C) & 15) == 0) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 c = *reinterpret_cast<const uint4*>(crow + x + q * 4);
+                o[q * 4 + 0] += be * c.x;
+                o[q * 4 + 1] += be * c.y;
+                o[q * 4 + 2] += be * c.z;
+                o[q * 4 + 3] += be * c.w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (x + i < p.N) o[i] += be * static_cast<uint32_t>(crow[x + i]);
+            }
+          }
+          if (p.staged) {
+            uint8_t* box = boxes + (nstores & 1) * tc::kEpiBoxBytes;
+            if (lane == 0) bulk_wait_group_read<1>();  // box's previous store has read it
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(box + tc::epi_box_offset(lane, q)) =
+                  make_uint4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_d, box, x, y);
+              bulk_commit_group();
+            }
+            ++nstores;
+          } else if (row < p.M) {
+            int32_t* drow = static_cast<int32_t*>(p.D) + static_cast<int64_t>(row) * p.ldd;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (x + i < p.N) drow[x + i] = static_cast<int32_t>(o[i]);
+          }
+        };
 #pragma unroll
         for (int cl = 0; cl < kCpw; ++cl) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            const int x = n_blk * BN + (c_lo + cl) * 32 + hh * 16;
-            if (x >= p.N || y >= p.M) continue;  // warp-uniform: the box is wholly outside D
             uint32_t o[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = al * sum[cl][hh * 16 + i];
-            if (be != 0u && row < p.M) {
-              if (x + 16 <= p.N && (p.ldc & 3) == 0 &&
-                  (reinterpret_cast<uintptr_t>(p.C) & 15) == 0) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const uint4 c = *reinterpret_cast<const uint4*>(crow + x + q * 4);
-                  o[q * 4 + 0] += be * c.x;
-                  o[q * 4 + 1] += be * c.y;
-                  o[q * 4 + 2] += be * c.z;
-                  o[q * 4 + 3] += be * c.w;
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  if (x + i < p.N) o[i] += be * static_cast<uint32_t>(crow[x + i]);
-              }
-            }
-            if (p.staged) {
-              uint8_t* box = boxes + (nstores & 1) * tc::kEpiBoxBytes;
-              if (lane == 0) bulk_wait_group_read<1>();  // box's previous store has read it
-              __syncwarp();
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(box + tc::epi_box_offset(lane, q)) =
-                    make_uint4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                tma_store_2d(&tmap_d, box, x, y);
-                bulk_commit_group();
-              }
-              ++nstores;
-            } else if (row < p.M) {
-              int32_t* drow = static_cast<int32_t*>(p.D) + static_cast<int64_t>(row) * p.ldd;
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (x + i < p.N) drow[x + i] = static_cast<int32_t>(o[i]);
-            }
+            emit(n_blk * BN + (c_lo + cl) * 32 + hh * 16, o);
           }
+        }
+        if constexpr (kSplitLast) {
+          uint32_t o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = al * xs[i * kBlockM];
+          emit(n_blk * BN + 2 * kCpw * 32 + half * 16, o);
         }
       }
       if (lane == 0) bulk_wait_group<0>();  // stores end before the CTA does
@@ -1137,7 +1175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int Stages, int CG, int Out, int Kind, bool SK = false>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
-  using L = TcSmem<BN, Stages, CG, Kind>;
+  using L = TcSmem<BN, Stages, CG, Kind, I32Extra<BN, Out>::kBytes>;
   constexpr bool kMx = Kind == kKindMx;
   CUtensorMap ta, tb;
   // A problem with fewer than 128 rows loads only its rows (rounded up to a
@@ -1310,6 +1348,7 @@ int regs_of() {
 
 int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32) {
   if (exact_i32) {
+    if (n_tile == 224 && cta_group == 2 && stages == 5) return regs_of<224, 5, 2, kOutI32>();
     if (n_tile == 192 && cta_group == 2 && stages == 6) return regs_of<192, 6, 2, kOutI32>();
     if (n_tile == 128 && cta_group == 1 && stages == 6) return regs_of<128, 6, 1, kOutI32>();
     return 0;
@@ -1350,6 +1389,11 @@ int mx_kernel_regs(int n_tile, int stages, int cta_group) {
 // output of widened INT8 operands.
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (a.exact_i32) {
+    // 224 columns: 19 x 16 = 304 pair tiles at 4096^2, four whole waves of
+    // 76 pairs (192 columns: 352 tiles, 4.63 waves); five stages leave room
+    // for the split chunk's sums
+    if (plan.n_tile == 224 && plan.cta_group == 2 && plan.stages == 5)
+      return run_tc<224, 5, 2, kOutI32, kKind16>(a, plan);
     if (plan.n_tile == 192 && plan.cta_group == 2 && plan.stages == 6)
       return run_tc<192, 6, 2, kOutI32, kKind16>(a, plan);
     if (plan.n_tile == 128 && plan.cta_group == 1 && plan.stages == 6)

@@ -1,7 +1,9 @@
 """The widening path on CTA pairs, against the oracle.
 
 Plans of 256 x 192 CTA-pair tiles on the widening path (INT8 operands with
-exact INT32 output, E2M1 weights with FP16 output): the narrow operands are
+exact INT32 output, E2M1 weights with FP16 output), and the INT8 plan of
+256 x 224 tiles (whose last 32-column chunk keeps its running INT32 sums in
+shared memory, 16 columns per epilogue warp): the narrow operands are
 widened into FP16 copies and the pair kernel reads them.  These tests run
 that plan on ragged shapes, on K below, at and across 512, on padded source
 rows and on grids from one CTA pair (which walks every tile) to the
@@ -28,10 +30,10 @@ def dg():
     return dg
 
 
-def _pair192(dg, case):
+def _pair192(dg, case, n_tile=192):
     plans = [p for p in dg.plan_tiles(case.M, case.N, case.K, case.dtype_a, case.dtype_b,
                                       case.epilogue, target_occupancy=0.0)
-             if p["kernel_name"] == "tc_widened" and p["n_tile"] == 192 and p["cta_group"] == 2]
+             if p["kernel_name"] == "tc_widened" and p["n_tile"] == n_tile and p["cta_group"] == 2]
     assert len(plans) == 1, plans
     return plans[0]
 
@@ -44,11 +46,12 @@ GRIDS = (None, 2, 6, 22)
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_int8_widened_pair(dg, shape):
+@pytest.mark.parametrize("n_tile", [192, 224])
+def test_int8_widened_pair(dg, shape, n_tile):
     M, N, K = shape
     case = workloads.random_case(M, N, K, "i8", "i8", alpha=3, beta=-2,
                                  seed=hash(shape) % 997, pad=127)
-    p = _pair192(dg, case)
+    p = _pair192(dg, case, n_tile)
     for grid in GRIDS:
         got, _ = run_case(dg, case, plan=p if grid is None else dict(p, grid=grid))
         assert_parity(case, got)
@@ -92,15 +95,34 @@ def test_alternating_shapes_and_types(dg):
             assert_parity(c, got)
 
 
-def test_int8_widened_pair_extremes(dg):
+@pytest.mark.parametrize("n_tile", [192, 224])
+def test_int8_widened_pair_extremes(dg, n_tile):
     # every product -128 * -128 through the widened copies: chunk sums of
-    # exactly 2^24, and the INT32 result exact
+    # exactly 2^24, and the INT32 result exact (D rows 16-byte multiples: the
+    # staged stores; rows of 454 are not, and take the direct stores)
     K = 4096
-    case = workloads.random_case(512, 576, K, "i8", "i8", seed=1)
-    case.A = np.full_like(case.A, -128)
-    case.B = np.full_like(case.B, -128)
-    got, _ = run_case(dg, case, plan=_pair192(dg, case))
-    assert np.all(got == 128 * 128 * K)
+    for N in (576, 454):
+        case = workloads.random_case(512, N, K, "i8", "i8", seed=1)
+        case.A = np.full_like(case.A, -128)
+        case.B = np.full_like(case.B, -128)
+        got, _ = run_case(dg, case, plan=_pair192(dg, case, n_tile))
+        assert np.all(got == 128 * 128 * K)
+
+
+@pytest.mark.parametrize("n_tile", [192, 224])
+def test_int8_column_one_hot(dg, n_tile):
+    # D[:, j] = A[:, j % K] * B[j, j % K]: every column of a tile, including
+    # the split chunk's 32 (columns 192 .. 223 of each 224-wide tile), lands
+    # where it belongs
+    M, N, K = 300, 700, 1100
+    case = workloads.random_case(M, N, K, "i8", "i8", seed=17)
+    B = np.zeros_like(case.B)
+    for j in range(N):
+        B[j, j % K] = (j % 255) - 127
+    case.B = B
+    got, _ = run_case(dg, case, plan=_pair192(dg, case, n_tile))
+    want = case.A[:, np.arange(N) % K].astype(np.int64) * B[np.arange(N), np.arange(N) % K]
+    assert np.array_equal(got.astype(np.int64), want)
 
 
 def test_back_to_back_in_one_stream(dg):
