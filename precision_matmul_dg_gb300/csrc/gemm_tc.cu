@@ -208,9 +208,8 @@ constexpr int kMxSfImage = 512;           // one image: 128 rows x 4 scales
 constexpr int kMxSfRowBlock = 2 * kMxSfImage;  // 128 rows x the 8 scales of a stage
 
 // Shared memory: the operand ring, then two staging boxes per epilogue warp,
-// then (INT32 mode with an odd number of 32-column chunks) the running sums
-// of the last chunk, then the barriers.
-template <int BN, int Stages, int CG, int Kind = kKind16, int ExtraBytes = 0>
+// then the barriers.
+template <int BN, int Stages, int CG, int Kind = kKind16>
 struct TcSmem {
   static constexpr int kRowsB = BN / CG;  // B rows this CTA loads
   static constexpr int kTileBytesB = kRowsB * kBlockK * 2;
@@ -228,8 +227,7 @@ struct TcSmem {
   static constexpr int kOffSfRows = kOffSf + Stages * kSfBytes;
   static constexpr int kOffEpi = kOffSfRows + Stages * kSfRowsBytes;
   static constexpr int kEpiBytes = kEpiWarps * 2 * tc::kEpiBoxBytes;
-  static constexpr int kOffExtra = kOffEpi + kEpiBytes;
-  static constexpr int kOffBar = kOffExtra + ExtraBytes;
+  static constexpr int kOffBar = kOffEpi + kEpiBytes;
   // full[Stages], empty[Stages], tmem_full[2], tmem_empty[2], drain, one
   // C-load barrier per staging box, then (MXFP4) sf_full[Stages] (the
   // stage's scale bytes landed) and img_ready[Stages] (its images built)
@@ -320,13 +318,6 @@ __device__ __forceinline__ void epi_load_c(const CUtensorMap* map, const TcParam
       if (epi_box<BN, CG>(p, t, rank, wi, kk, x, y)) tma_prefetch_l2_2d(map, x, y);
 }
 
-// INT32 mode: running sums of a tile's last 32 columns when BN / 32 is odd
-// (the registers of a warp hold whole pairs of chunks; see the epilogue).
-template <int BN, int Out>
-struct I32Extra {
-  static constexpr int kBytes = (Out == kOutI32 && BN % 64 == 32) ? kBlockM * 32 * 4 : 0;
-};
-
 template <int BN, int Stages, int CG, int Out, int Kind, bool SK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -336,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_sfa,
                        const __grid_constant__ CUtensorMap tmap_sfb, const TcParams p,
                        const __grid_constant__ EpiProgram prog, const SkParams sk) {
-  using L = TcSmem<BN, Stages, CG, Kind, I32Extra<BN, Out>::kBytes>;
+  using L = TcSmem<BN, Stages, CG, Kind>;
   constexpr bool kMx = Kind == kKindMx;
   static_assert(!kMx || Out == kOutF16, "MXFP4: FP16 output");
   // Stream-K: 16-bit operands, FP16 output through the staged epilogue, and
@@ -750,18 +741,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // staging buffers (or straight from registers without staging).  The
       // two warps of a lane quarter take kCpw 32-column chunks each, their
       // sums in registers (32 per chunk); when BN / 32 is odd the last chunk
-      // is split between them, 16 columns each, its sums in shared memory
-      // (column-major, so that the lanes' rows fall in different banks):
-      // 224 columns keep 96 sum registers a thread, as 192 do.
+      // is split between them, 16 columns each, its sums kept during the
+      // tile in the warp's second staging box (sum i of lane l at word 32 i
+      // + l: the lanes fall in different banks) and stored first, before
+      // the tile's other stores reuse the box: 224 columns keep 96 sum
+      // registers a thread, as 192 do, and need no shared memory of their own.
       static_assert(Out != kOutI32 || BN % 32 == 0, "INT32 mode: whole 32-column chunks");
       constexpr int kCpw = BN / 64;  // 32-column chunks per warp in registers
       constexpr bool kSplitLast = BN % 64 == 32;
       const int c_lo = half * kCpw;
       const int wi = warp - kEpiWarp0;
       uint8_t* boxes = smem + L::kOffEpi + wi * 2 * tc::kEpiBoxBytes;
-      // this lane's 16 sums of the split chunk: column half * 16 + i at i * kBlockM
-      uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L::kOffExtra) +
-                     half * 16 * kBlockM + ew * 32 + lane;
+      // this lane's 16 sums of the split chunk, sum i at word 32 i
+      uint32_t* xs = reinterpret_cast<uint32_t*>(boxes + tc::kEpiBoxBytes) + lane;
+      static_assert(16 * 32 * 4 <= tc::kEpiBoxBytes, "split chunk's sums in one box");
       const uint32_t al = static_cast<uint32_t>(p.alpha_i), be = static_cast<uint32_t>(p.beta_i);
       uint32_t sum[kCpw][32];
       int nstores = 0;  // stores issued; store i goes through box i & 1
@@ -769,6 +762,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int m_blk, n_blk;
         tc::tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.group_m, m_blk, n_blk);
         const int y = m_blk * kTileM + static_cast<int>(rank) * kBlockM + ew * 32;
+        if (kSplitLast && p.staged) {
+          // the previous tile's stores have read the box the sums go to
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+        }
         for (int ch = 0; ch < num_chunks; ++ch) {
           const bool ready =
               !aborted(abort_flag) &&
@@ -798,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const uint32_t v = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
-              xs[i * kBlockM] = ch == 0 ? v : xs[i * kBlockM] + v;
+              xs[i * 32] = ch == 0 ? v : xs[i * 32] + v;
             }
           }
           tc_fence_before_sync();
@@ -856,6 +854,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (x + i < p.N) drow[x + i] = static_cast<int32_t>(o[i]);
           }
         };
+        if constexpr (kSplitLast) {
+          // first, so that its sums are read before a store reuses their box
+          uint32_t o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = al * xs[i * 32];
+          __syncwarp();
+          emit(n_blk * BN + 2 * kCpw * 32 + half * 16, o);
+        }
 #pragma unroll
         for (int cl = 0; cl < kCpw; ++cl) {
 #pragma unroll
@@ -865,12 +871,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i) o[i] = al * sum[cl][hh * 16 + i];
             emit(n_blk * BN + (c_lo + cl) * 32 + hh * 16, o);
           }
-        }
-        if constexpr (kSplitLast) {
-          uint32_t o[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = al * xs[i * kBlockM];
-          emit(n_blk * BN + 2 * kCpw * 32 + half * 16, o);
         }
       }
       if (lane == 0) bulk_wait_group<0>();  // stores end before the CTA does
@@ -1175,7 +1175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int Stages, int CG, int Out, int Kind, bool SK = false>
 cudaError_t run_tc(const GemmArgs& a, const dg_tile_plan& plan) {
-  using L = TcSmem<BN, Stages, CG, Kind, I32Extra<BN, Out>::kBytes>;
+  using L = TcSmem<BN, Stages, CG, Kind>;
   constexpr bool kMx = Kind == kKindMx;
   CUtensorMap ta, tb;
   // A problem with fewer than 128 rows loads only its rows (rounded up to a
@@ -1348,7 +1348,7 @@ int regs_of() {
 
 int tc_kernel_regs(int n_tile, int stages, int cta_group, bool exact_i32) {
   if (exact_i32) {
-    if (n_tile == 224 && cta_group == 2 && stages == 5) return regs_of<224, 5, 2, kOutI32>();
+    if (n_tile == 224 && cta_group == 2 && stages == 6) return regs_of<224, 6, 2, kOutI32>();
     if (n_tile == 192 && cta_group == 2 && stages == 6) return regs_of<192, 6, 2, kOutI32>();
     if (n_tile == 128 && cta_group == 1 && stages == 6) return regs_of<128, 6, 1, kOutI32>();
     return 0;
@@ -1390,10 +1390,9 @@ int mx_kernel_regs(int n_tile, int stages, int cta_group) {
 cudaError_t launch_tc(const GemmArgs& a, const dg_tile_plan& plan) {
   if (a.exact_i32) {
     // 224 columns: 19 x 16 = 304 pair tiles at 4096^2, four whole waves of
-    // 76 pairs (192 columns: 352 tiles, 4.63 waves); five stages leave room
-    // for the split chunk's sums
-    if (plan.n_tile == 224 && plan.cta_group == 2 && plan.stages == 5)
-      return run_tc<224, 5, 2, kOutI32, kKind16>(a, plan);
+    // 76 pairs (192 columns: 352 tiles, 4.63 waves)
+    if (plan.n_tile == 224 && plan.cta_group == 2 && plan.stages == 6)
+      return run_tc<224, 6, 2, kOutI32, kKind16>(a, plan);
     if (plan.n_tile == 192 && plan.cta_group == 2 && plan.stages == 6)
       return run_tc<192, 6, 2, kOutI32, kKind16>(a, plan);
     if (plan.n_tile == 128 && plan.cta_group == 1 && plan.stages == 6)

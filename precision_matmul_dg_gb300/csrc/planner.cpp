@@ -81,10 +81,9 @@ constexpr double kSkFixedUs = 3.0;
 constexpr TcVariant kTcVariantsI8[] = {{128, 8, 1, 3}};
 // FP16 kernel in its exact-INT32 mode (two FP32 chunk accumulators in TMEM,
 // running INT32 sums in registers, 32 per 32-column chunk a warp owns: at most
-// 96 per thread, so N_tile 128 or 192, or 224 with the last chunk's sums in
-// shared memory (kI32SplitChunkBytes, and one stage fewer to make room))
-constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {192, 6, 2, 0}, {224, 5, 2, 0}};
-constexpr int kI32SplitChunkBytes = 128 * 32 * 4;
+// 96 per thread, so N_tile 128 or 192, or 224 with the last chunk's sums kept
+// in a staging box during the tile)
+constexpr TcVariant kTcVariantsI8Widened[] = {{128, 6, 1, 0}, {192, 6, 2, 0}, {224, 6, 2, 0}};
 constexpr TcVariant kTcVariantsE2M1[] = {{256, 6, 1, 2}, {128, 8, 1, 3}, {64, 8, 1, 4}};
 // MXFP4 x MXFP4 on the block-scaled MMA (the tensor-core kernel with packed
 // E2M1 stages and scale images; single CTAs)
@@ -250,8 +249,7 @@ void add_tc_candidates(int64_t M, int64_t N, int64_t K, dg_dtype da, dg_dtype db
     // the FP16 x FP16 kernel stages its output (FP16, or INT32 for widened
     // INT8), and so does the MXFP4 kernel
     const bool staged = (ka == DG_F16 && kb == DG_F16) || mx_native;
-    const int smem = tc_smem_bytes(ka, kb, v, staged) +
-                     (widened && da == DG_I8 && v.n_tile % 64 == 32 ? kI32SplitChunkBytes : 0);
+    const int smem = tc_smem_bytes(ka, kb, v, staged);
     if (smem > hw.smem_per_block_optin) {
       if (why) *why += name + ": shared memory; ";
       continue;

@@ -3,7 +3,8 @@
 Plans of 256 x 192 CTA-pair tiles on the widening path (INT8 operands with
 exact INT32 output, E2M1 weights with FP16 output), and the INT8 plan of
 256 x 224 tiles (whose last 32-column chunk keeps its running INT32 sums in
-shared memory, 16 columns per epilogue warp): the narrow operands are
+a staging box during the tile, 16 columns per epilogue warp): the narrow
+operands are
 widened into FP16 copies and the pair kernel reads them.  These tests run
 that plan on ragged shapes, on K below, at and across 512, on padded source
 rows and on grids from one CTA pair (which walks every tile) to the

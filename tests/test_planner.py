@@ -364,11 +364,11 @@ def test_converting_kernel_plans(dg, pair, shape):
         cols = (3 if pair[0] == "i8" else 2) * p["n_tile"]
         assert cols <= GB300["tmem_cols"]
     # widened: the FP16 kernel's variants (INT8: its exact-INT32 mode, 128 x 128,
-    # 256 x 192 and 256 x 224, the last with its split chunk's sums in SMEM)
+    # 256 x 192 and 256 x 224)
     wide = {(p["n_tile"], p["stages"], p["cta_group"]) for p in plans
             if p["kernel_name"] == "tc_widened"}
     if pair[0] == "i8":
-        want = {(128, 6, 1), (192, 6, 2), (224, 5, 2)}
+        want = {(128, 6, 1), (192, 6, 2), (224, 6, 2)}
     else:
         want = set(TC_VARIANTS)
     if M <= 128:
@@ -377,10 +377,8 @@ def test_converting_kernel_plans(dg, pair, shape):
     for p in plans:
         if p["kernel_name"] == "tc_widened":
             assert p["threads"] == 384
-            # INT8 runs the FP16 kernel in its exact INT32 mode (also staged);
-            # 224 columns add the split chunk's INT32 sums (128 rows x 32)
-            split = 128 * 32 * 4 if pair[0] == "i8" and p["n_tile"] % 64 == 32 else 0
-            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], p["cta_group"]) + split
+            # INT8 runs the FP16 kernel in its exact INT32 mode (also staged)
+            assert p["smem_bytes"] == tc_smem(p["n_tile"], p["stages"], p["cta_group"])
 
 
 @pytest.mark.parametrize("M", [1, 7, 16, 17])
