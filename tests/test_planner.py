@@ -460,3 +460,17 @@ def test_noalloc_scratch_covers_every_gemv_split(dg):
                     worst = max(worst, best["split_k"] * M * N * 4 / (2 << 20))
                     assert (N + 7) // 8 * 4 <= 64 << 10
     assert worst <= 0.25
+
+
+@pytest.mark.parametrize("n", [4096, 8192])
+def test_int8_square_takes_the_224_wide_pair(dg, n):
+    # INT8 squares: 256 x 224 pair tiles fill whole waves of 76 pairs at 4096
+    # (304 tiles; 256 x 192: 352 tiles, 4.63 waves), and the planner ranks
+    # them first; 128 x 128 single CTAs and 256 x 192 pairs stay proposed
+    plans = [p for p in dg.plan_tiles(n, n, n, "i8", "i8", hw=GB300)
+             if p["kernel_name"] == "tc_widened"]
+    assert (plans[0]["n_tile"], plans[0]["stages"], plans[0]["cta_group"]) == (224, 6, 2)
+    assert {(p["n_tile"], p["cta_group"]) for p in plans} >= {(128, 1), (192, 2), (224, 2)}
+    first = plans[0]
+    tiles = math.ceil(n / 256) * math.ceil(n / 224)
+    assert first["occupancy"] == pytest.approx(tiles / (math.ceil(tiles / 76) * 76))
